@@ -1,0 +1,173 @@
+// fp4q_api.cu -- the extern "C" entry points of libfp4q.so (declared and
+// documented in include/fp4q.h): argument validation, device status word,
+// dispatch to the kernel launchers.  No entry point allocates memory.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/fp4q.h"
+#include "fp4q_device.cuh"
+#include "fp4q_launch.h"
+
+namespace {
+
+// Latched by kernels (non-finite input, bounded-wait timeout); read and
+// cleared by fp4q_get_device_status.
+__device__ int g_status_word;
+
+int* status_ptr() {
+  // One address per device; looked up on each call (cheap) so that a caller
+  // switching devices gets the right copy.
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+  return static_cast<int*>(p);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+fp4q_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA; }
+
+float scale_max_host(fp4q_scale_fmt f) { return f == FP4Q_SCALE_UE5M3 ? 114688.0f : 448.0f; }
+
+bool valid_fmt(int f) { return f == FP4Q_SCALE_UE5M3 || f == FP4Q_SCALE_UE4M3; }
+
+}  // namespace
+
+extern "C" {
+
+const char* fp4q_status_string(fp4q_status s) {
+  switch (s) {
+    case FP4Q_OK: return "ok";
+    case FP4Q_ERR_ARG: return "invalid argument (null pointer or unknown enum)";
+    case FP4Q_ERR_SHAPE: return "unsupported shape";
+    case FP4Q_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case FP4Q_ERR_CUDA: return "CUDA error";
+    case FP4Q_ERR_NONFINITE: return "non-finite input element";
+    case FP4Q_ERR_TIMEOUT: return "device pipeline wait timed out";
+  }
+  return "unknown status";
+}
+
+fp4q_status fp4q_amax(const void* in_bf16, int64_t n, float* out_amax, void* stream) {
+  if (!out_amax || n < 0 || (n > 0 && !in_bf16)) return FP4Q_ERR_ARG;
+  if ((n > 0 && !aligned16(in_bf16)) || !aligned16(out_amax)) return FP4Q_ERR_ALIGN;
+  int* st = status_ptr();
+  if (!st) return FP4Q_ERR_CUDA;
+  return from_cuda(fp4q::launch_amax(in_bf16, n, out_amax, st, static_cast<cudaStream_t>(stream)));
+}
+
+fp4q_status fp4q_tensor_scale(const float* amax, fp4q_scale_fmt fmt, float headroom, float* out_scale,
+                              void* stream) {
+  if (!amax || !out_scale || !valid_fmt(fmt)) return FP4Q_ERR_ARG;
+  // headroom must be a power of two >= 1 so that 6 * Smax / H is exact
+  int e = 0;
+  if (!(headroom >= 1.0f) || frexpf(headroom, &e) != 0.5f) return FP4Q_ERR_ARG;
+  if (!aligned16(amax) || !aligned16(out_scale)) return FP4Q_ERR_ALIGN;
+  const float denom = (6.0f * scale_max_host(fmt)) / headroom;
+  return from_cuda(fp4q::launch_tensor_scale(amax, denom, out_scale, static_cast<cudaStream_t>(stream)));
+}
+
+fp4q_status fp4q_quantize(const void* in_bf16, int64_t rows, int64_t cols, fp4q_axis axis,
+                          fp4q_scale_fmt fmt, const float* tensor_scale, fp4q_rounding rnd,
+                          uint64_t seed, uint8_t* out_payload_row, uint8_t* out_scales_row,
+                          uint8_t* out_payload_col, uint8_t* out_scales_col, fp4q_stats* out_stats,
+                          float* out_amax, void* stream) {
+  if (axis != FP4Q_AXIS_ROW && axis != FP4Q_AXIS_COL && axis != FP4Q_AXIS_BOTH) return FP4Q_ERR_ARG;
+  if (!valid_fmt(fmt) || (rnd != FP4Q_RNE && rnd != FP4Q_SR) || !tensor_scale) return FP4Q_ERR_ARG;
+  if (rows < 0 || cols < 0 || rows % 16 || cols % 16) return FP4Q_ERR_SHAPE;
+  const bool row = axis != FP4Q_AXIS_COL, col = axis != FP4Q_AXIS_ROW;
+  const bool empty = rows == 0 || cols == 0;
+  if (!empty) {
+    if (!in_bf16) return FP4Q_ERR_ARG;
+    if (row && (!out_payload_row || !out_scales_row)) return FP4Q_ERR_ARG;
+    if (col && (!out_payload_col || !out_scales_col)) return FP4Q_ERR_ARG;
+    if (!aligned16(in_bf16)) return FP4Q_ERR_ALIGN;
+    if (row && (!aligned16(out_payload_row) || !aligned16(out_scales_row))) return FP4Q_ERR_ALIGN;
+    if (col && (!aligned16(out_payload_col) || !aligned16(out_scales_col))) return FP4Q_ERR_ALIGN;
+  }
+  if (!aligned16(tensor_scale) || (out_stats && !aligned16(out_stats)) ||
+      (out_amax && !aligned16(out_amax)))
+    return FP4Q_ERR_ALIGN;
+  int* st = status_ptr();
+  if (!st) return FP4Q_ERR_CUDA;
+  fp4q::QuantArgs a;
+  a.in = in_bf16;
+  a.rows = rows;
+  a.cols = cols;
+  a.axis = (int)axis;
+  a.fmt = (int)fmt;
+  a.tscale = tensor_scale;
+  a.sr = rnd == FP4Q_SR;
+  a.seed = seed;
+  a.pay_row = out_payload_row;
+  a.sc_row = out_scales_row;
+  a.pay_col = out_payload_col;
+  a.sc_col = out_scales_col;
+  a.stats = reinterpret_cast<fp4q::StatsDev*>(out_stats);
+  a.amax_out = out_amax;
+  a.status = st;
+  return from_cuda(fp4q::launch_quantize(a, static_cast<cudaStream_t>(stream)));
+}
+
+fp4q_status fp4q_dequantize(const uint8_t* payload, const uint8_t* scales, int64_t rows, int64_t cols,
+                            fp4q_scale_fmt fmt, const float* tensor_scale, void* out, int out_is_f32,
+                            void* stream) {
+  if (!valid_fmt(fmt) || !tensor_scale) return FP4Q_ERR_ARG;
+  if (rows < 0 || cols < 0 || rows % 16 || cols % 16) return FP4Q_ERR_SHAPE;
+  if (rows > 0 && cols > 0) {
+    if (!payload || !scales || !out) return FP4Q_ERR_ARG;
+    if (!aligned16(payload) || !aligned16(scales) || !aligned16(out)) return FP4Q_ERR_ALIGN;
+  }
+  if (!aligned16(tensor_scale)) return FP4Q_ERR_ALIGN;
+  return from_cuda(fp4q::launch_dequantize(payload, scales, rows, cols, (int)fmt, tensor_scale, out,
+                                           out_is_f32 != 0, static_cast<cudaStream_t>(stream)));
+}
+
+fp4q_status fp4q_gemm(const uint8_t* A, const uint8_t* A_scales, const float* A_tscale, const uint8_t* B,
+                      const uint8_t* B_scales, const float* B_tscale, int64_t M, int64_t N, int64_t K,
+                      fp4q_scale_fmt fmt, void* out, int out_is_f32, void* stream) {
+  if (!valid_fmt(fmt)) return FP4Q_ERR_ARG;
+  if (M < 0 || N < 0 || K < 0 || K % 64 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
+    return FP4Q_ERR_SHAPE;
+  if (M == 0 || N == 0) return FP4Q_OK;
+  if (!out) return FP4Q_ERR_ARG;
+  if (!aligned16(out)) return FP4Q_ERR_ALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (K == 0)
+    return from_cuda(cudaMemsetAsync(out, 0, (size_t)M * N * (out_is_f32 ? 4 : 2), st));
+  if (!A || !A_scales || !A_tscale || !B || !B_scales || !B_tscale) return FP4Q_ERR_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(A_scales) || !aligned16(B_scales) ||
+      !aligned16(A_tscale) || !aligned16(B_tscale))
+    return FP4Q_ERR_ALIGN;
+  int* status = status_ptr();
+  if (!status) return FP4Q_ERR_CUDA;
+  fp4q::GemmArgs a;
+  a.A = A;
+  a.As = A_scales;
+  a.B = B;
+  a.Bs = B_scales;
+  a.TA = A_tscale;
+  a.TB = B_tscale;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.fmt = (int)fmt;
+  a.out = out;
+  a.out_f32 = out_is_f32 != 0;
+  a.status = status;
+  return from_cuda(fp4q::launch_gemm(a, st));
+}
+
+fp4q_status fp4q_get_device_status(int* out) {
+  if (!out) return FP4Q_ERR_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return FP4Q_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(int)) != cudaSuccess) return FP4Q_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int)) != cudaSuccess) return FP4Q_ERR_CUDA;
+  *out = (v & fp4q::kStatusTimeout) ? FP4Q_ERR_TIMEOUT
+         : (v & fp4q::kStatusNonFinite) ? FP4Q_ERR_NONFINITE
+                                        : FP4Q_OK;
+  return FP4Q_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,201 @@
+// fp4q_device.cuh -- device-side format helpers shared by the quantiser,
+// dequantiser and GEMM kernels of libfp4q.so (sm_103a).
+//
+// Formats follow "UE5M3 FP4 Block Scaling for Stable Language Model
+// Pretraining", Abstract: E2M1 elements, unsigned E5M3 block scales on blocks
+// of 16, an FP32 tensor scale.  Every floating-point step is one IEEE binary32
+// operation rounded to nearest even (explicit __f*_rn intrinsics, so that no
+// multiply-add is ever contracted), which makes the encoded bytes a pure
+// function of the input.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fp4q {
+
+enum : int { kUE5M3 = 0, kUE4M3 = 1 };
+
+// Device status bits latched by kernels (read back by fp4q_get_device_status).
+enum : int { kStatusNonFinite = 1, kStatusTimeout = 2 };
+
+struct StatsDev {
+  unsigned long long scale_sat, scale_uflow, elem_clamped, elem_flushed;
+};
+
+// ---------------------------------------------------------------- loads/stores
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void st_stream_u32(void* p, uint32_t v) {
+  asm volatile("st.global.L1::no_allocate.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// BF16 pair (one 32-bit word) -> two binary32 values, exactly.
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// ---------------------------------------------------------------- scale format
+// UE5M3: bias 15, largest 0xFE = 114688, subnormal step 2^-17.
+// UE4M3: bias 7, largest 0x7E = 448, subnormal step 2^-9.
+__device__ __forceinline__ float scale_max(int fmt) { return fmt == kUE5M3 ? 114688.0f : 448.0f; }
+
+// Round a non-negative binary32 s* to the scale format: nearest, ties to the
+// even code, saturating to the largest finite code (flagged in *sat).
+__device__ __forceinline__ uint32_t encode_scale(float s, int fmt, bool* sat) {
+  const bool ue5 = (fmt == kUE5M3);
+  *sat = s > scale_max(fmt);
+  if (!(s > 0.0f)) return 0u;
+  if (*sat) return ue5 ? 0xFEu : 0x7Eu;
+  if (s < (ue5 ? 0x1p-14f : 0x1p-6f)) {
+    // subnormal range: integer multiples of the subnormal step (exact scaling)
+    return (uint32_t)__float2int_rn(__fmul_rn(s, ue5 ? 0x1p17f : 0x1p9f));
+  }
+  // normal range: round the binary32 pattern to 3 mantissa bits (ties to
+  // even; a mantissa carry moves into the exponent), then re-bias.
+  const uint32_t b = __float_as_uint(s);
+  const uint32_t t = (b + 0x7FFFFu + ((b >> 20) & 1u)) >> 20;
+  return t - (ue5 ? (112u << 3) : (120u << 3));
+}
+
+__device__ __forceinline__ float decode_scale(uint32_t code, int fmt) {
+  const bool ue5 = (fmt == kUE5M3);
+  const uint32_t e = code >> 3, m = code & 7u;
+  if (e == 0) return __fmul_rn(__uint2float_rn(m), ue5 ? 0x1p-17f : 0x1p-9f);
+  return __uint_as_float(((e + (ue5 ? 112u : 120u)) << 23) | (m << 20));
+}
+
+// ---------------------------------------------------------------- E2M1
+// Eight binary32 values -> eight E2M1 nibbles (round to nearest even,
+// saturating at +-6, sign kept), element 2j in the low nibble of byte j.
+__device__ __forceinline__ uint32_t cvt_e2m1x8(const float q[8]) {
+  uint32_t out;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(out)
+      : "f"(q[0]), "f"(q[1]), "f"(q[2]), "f"(q[3]), "f"(q[4]), "f"(q[5]), "f"(q[6]), "f"(q[7]));
+  return out;
+}
+
+// Stochastic rounding of a magnitude a >= 0 onto the E2M1 grid, given the
+// random word w: with lo <= a < hi neighbouring grid points and
+// p = (a - lo) / (hi - lo), the result is hi iff (w >> 8) * 2^-24 < p.
+// For a >= 1 the grid points are exactly the binary32 values with one
+// mantissa bit, so lo is a truncation of the pattern and p * 2^24 is four
+// times the 22 dropped mantissa bits; below 1 the grid is uniform (step
+// 1/2).  Results at or above 6 are saturated by the caller's conversion.
+__device__ __forceinline__ float sr_round_mag(float a, uint32_t w) {
+  const uint32_t U = w >> 8;
+  if (a >= 1.0f) {
+    const uint32_t b = __float_as_uint(a);
+    const uint32_t up = ((U >> 2) < (b & 0x3FFFFFu)) ? 1u : 0u;
+    return __uint_as_float((b & ~0x3FFFFFu) + (up << 22));
+  }
+  const float t = __fmul_rn(a, 2.0f);
+  const float fl = floorf(t);
+  const float p = __fsub_rn(t, fl);
+  const float u = __fmul_rn(__uint2float_rn(U), 0x1p-24f);
+  return __fmul_rn(__fadd_rn(fl, (u < p) ? 1.0f : 0.0f), 0.5f);
+}
+
+// ---------------------------------------------------------------- Philox4x32-10
+// Salmon et al., "Parallel random numbers: as easy as 1, 2, 3" (SC 2011):
+// ten rounds of two 32x32->64 multiplies and a key-xor permutation, the key
+// bumped by the Weyl constants between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) { k0 += 0x9E3779B9u; k1 += 0xBB67AE85u; }
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+  }
+  return c;
+}
+
+// The four random words of counter block ctr (= element index / 4) on the
+// given axis (0 row-wise, 1 column-wise).
+__device__ __forceinline__ uint4 sr_words4(uint64_t ctr, uint32_t axis, uint64_t seed) {
+  return philox4x32_10(make_uint4((uint32_t)ctr, (uint32_t)(ctr >> 32), axis, 0u),
+                       (uint32_t)seed, (uint32_t)(seed >> 32));
+}
+
+// ---------------------------------------------------------------- one block
+// Encodes the scale of a block from its amax (as the 16-bit |bf16| pattern)
+// and returns the reciprocal multiplier r = 1 / (s T); r = 0 marks a zero
+// scale (every element then encodes to a signed zero).
+struct BlockScale {
+  uint32_t code;
+  float r;
+  bool sat;
+};
+
+__device__ __forceinline__ BlockScale block_scale(uint32_t amax16, float six_t, float T, int fmt) {
+  BlockScale bs;
+  const float amax_b = __uint_as_float(amax16 << 16);
+  const float s_star = __fdiv_rn(amax_b, six_t);
+  bs.code = encode_scale(s_star, fmt, &bs.sat);
+  const float s = decode_scale(bs.code, fmt);
+  bs.r = (s == 0.0f) ? 0.0f : __frcp_rn(__fmul_rn(s, T));
+  return bs;
+}
+
+// Quantises eight elements (four BF16 words) with multiplier r.  Returns the
+// eight nibbles; with STATS, adds clamped/flushed element counts.
+template <bool SR, bool STATS>
+__device__ __forceinline__ uint32_t quantize8(const uint32_t w[4], float r, const uint32_t* rb,
+                                              uint32_t* clamped, uint32_t* flushed) {
+  float q[8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    q[2 * j] = __fmul_rn(bf16_lo(w[j]), r);
+    q[2 * j + 1] = __fmul_rn(bf16_hi(w[j]), r);
+  }
+  if (r == 0.0f) {
+    // zero scale: signed zeros (x * 0 keeps the sign of x)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      q[2 * j] = __uint_as_float((w[j] << 16) & 0x80000000u);
+      q[2 * j + 1] = __uint_as_float(w[j] & 0x80000000u);
+    }
+  }
+  if (STATS) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) *clamped += (fabsf(q[j]) > 6.0f) ? 1u : 0u;
+  }
+  if (SR) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float m = sr_round_mag(fabsf(q[j]), rb[j]);
+      q[j] = __uint_as_float(__float_as_uint(m) | (__float_as_uint(q[j]) & 0x80000000u));
+    }
+  }
+  const uint32_t nib = cvt_e2m1x8(q);
+  if (STATS) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t xbits = (j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xFFFFu);
+      const bool nonzero = (xbits & 0x7FFFu) != 0u;
+      const bool zero_mag = ((nib >> (4 * j)) & 7u) == 0u;
+      *flushed += (nonzero && zero_mag) ? 1u : 0u;
+    }
+  }
+  return nib;
+}
+
+// max of |bf16| over four words, as a 16-bit pattern (finite values order
+// like their patterns; inf/NaN patterns compare above every finite one).
+__device__ __forceinline__ uint32_t absmax16(const uint32_t w[4]) {
+  uint32_t m = __vmaxu2(w[0] & 0x7FFF7FFFu, w[1] & 0x7FFF7FFFu);
+  m = __vmaxu2(m, __vmaxu2(w[2] & 0x7FFF7FFFu, w[3] & 0x7FFF7FFFu));
+  return max(m & 0xFFFFu, m >> 16);
+}
+
+}  // namespace fp4q

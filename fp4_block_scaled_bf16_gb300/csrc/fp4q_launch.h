@@ -1,0 +1,47 @@
+// fp4q_launch.h -- host-side launch interface between the C ABI (fp4q_api.cu)
+// and the kernel translation units (quantize.cu, gemm.cu).  Internal to
+// libfp4q.so; arguments are validated by the ABI layer before they get here.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fp4q {
+
+struct StatsDev;
+
+struct QuantArgs {
+  const void* in;       // BF16 [rows, cols]
+  int64_t rows, cols;   // multiples of 16
+  int axis;             // 0 row, 1 col, 2 both
+  int fmt;              // 0 UE5M3, 1 UE4M3
+  const float* tscale;  // device T
+  bool sr;
+  uint64_t seed;
+  uint8_t *pay_row, *sc_row, *pay_col, *sc_col;
+  StatsDev* stats;      // nullable; two structs for axis 2
+  float* amax_out;      // nullable
+  int* status;          // device status word
+};
+
+cudaError_t launch_amax(const void* in, int64_t n, float* out, int* status, cudaStream_t st);
+cudaError_t launch_tensor_scale(const float* amax, float denom, float* out, cudaStream_t st);
+cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t st);
+cudaError_t launch_dequantize(const uint8_t* payload, const uint8_t* scales, int64_t rows,
+                              int64_t cols, int fmt, const float* tscale, void* out, bool f32,
+                              cudaStream_t st);
+
+struct GemmArgs {
+  const uint8_t *A, *As, *B, *Bs;   // payloads [M, K/2], [N, K/2]; scales [., K/16]
+  const float *TA, *TB;             // device tensor scales
+  int64_t M, N, K;                  // K multiple of 64
+  int fmt;
+  void* out;                        // [M, N] BF16 or binary32
+  bool out_f32;
+  int* status;
+};
+
+// Returns cudaErrorNotSupported when the driver entry point for tensor maps
+// is missing.
+cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st);
+
+}  // namespace fp4q

@@ -1,0 +1,464 @@
+// gemm.cu -- the emulated UE5M3 block-scaled GEMM of libfp4q.so on the
+// sm_103a tensor cores (tcgen05, TMEM accumulators, TMA, mbarrier pipeline).
+//
+// Method: "UE5M3 FP4 Block Scaling for Stable Language Model Pretraining",
+// Abstract -- the FP4 matrix multiplications of every internal linear run on
+// E2M1 payloads with UE5M3 block-16 scales, emulated in software because the
+// tensor cores' native block-scale formats are E4M3/E8M0.
+//
+//   C[m, n] = (T_A T_B) * sum_k (e_a s_a)[m, k] * (e_b s_b)[n, k]
+//
+// Every product e * s has at most 6 significant bits and lies in
+// [2^-18, 688128], so it is exact in BF16; the contraction therefore runs as a
+// BF16 x BF16 -> FP32 tcgen05 MMA (kind::f16) over operands expanded in shared
+// memory, and differs from an exact sum only by FP32 accumulation rounding.
+//
+// CTA organisation (one CTA per SM, 128 x 256 output tile, K step 64):
+//   warp 8      TMA producer: FP4 payload tiles (A 128 x 32 B, B 256 x 32 B)
+//               into a 4-stage raw ring.
+//   warps 0..7  expand raw stages into a 3-stage BF16 ring laid out in the
+//               128-byte-swizzled K-major form the MMA descriptors read; each
+//               thread expands one 16-element block (one scale) at a time
+//               through an 8-entry per-block value table and byte permutes;
+//               after the main loop they run the epilogue (TMEM -> registers
+//               -> alpha -> BF16/FP32 -> global).
+//   warp 9      allocates TMEM; one lane issues 4 MMAs (M128 N256 K16) per
+//               stage and commits them to the stage's "empty" barrier.
+// Every wait is bounded: a wait that runs out latches FP4Q_ERR_TIMEOUT in the
+// device status word and the CTA drains and exits instead of hanging.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "fp4q_device.cuh"
+#include "fp4q_launch.h"
+
+namespace fp4q {
+namespace gemm {
+
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int S_RAW = 4, S_BF = 3;
+constexpr int RAW_A = BM * BK / 2;             // 4096 B
+constexpr int RAW_B = BN * BK / 2;             // 8192 B
+constexpr int RAW_STAGE = RAW_A + RAW_B;
+constexpr int BF_A = BM * BK * 2;              // 16384 B
+constexpr int BF_B = BN * BK * 2;              // 32768 B
+constexpr int BF_STAGE = BF_A + BF_B;
+constexpr int kDeqThreads = 256;
+constexpr int kThreads = kDeqThreads + 64;
+constexpr uint32_t kTmemCols = 256;
+
+constexpr int OFF_BF = 0;
+constexpr int OFF_RAW = OFF_BF + S_BF * BF_STAGE;
+constexpr int OFF_BAR = OFF_RAW + S_RAW * RAW_STAGE;
+constexpr int NBARS = 2 * S_RAW + 2 * S_BF + 1;
+constexpr int OFF_TMEM = OFF_BAR + 8 * NBARS;
+constexpr int OFF_ABORT = OFF_TMEM + 8;
+constexpr int SMEM_BYTES = OFF_ABORT + 8 + 1024;   // + slack to align the base to 1 KB
+
+constexpr long long kWaitCycles = 4000000000LL;    // about 2 s at 2 GHz
+
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+// Bounded wait on the phase with the given parity.  False when the CTA's
+// abort flag is set or the cycle budget runs out.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitCycles) return false;
+  }
+}
+__device__ __forceinline__ void fail(volatile int* abort_flag, int* status) {
+  *abort_flag = 1;
+  atomicOr(status, kStatusTimeout);
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols) : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+      "%30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 64 BF16 (128 B) grouped by 8 into 1024-byte atoms (stride-dimension offset
+// 1024 B); the leading-dimension offset is unused in this mode.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor for kind::f16: FP32 accumulator, BF16 A and B, both
+// K-major, M = 128, N = 256.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                            ((uint32_t)(BM >> 4) << 24);
+
+// ---------------------------------------------------------------- expansion
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+__device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// The eight magnitudes E2M1(v) * s (v = 0..7) as BF16, split into a table of
+// low bytes (L0: v 0..3, L1: v 4..7) and of high bytes (H0, H1), so that one
+// byte permute per table looks up four elements.
+struct Lut {
+  uint32_t L0, L1, H0, H1;
+};
+__device__ __forceinline__ Lut make_lut(uint32_t code, int fmt) {
+  const float s = decode_scale(code, fmt);
+  uint32_t ss;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(ss) : "f"(s));   // exact: <= 4 significant bits
+  const uint32_t p01 = bmul2(ss, 0x3F000000u);   // (0, 0.5) * s
+  const uint32_t p23 = bmul2(ss, 0x3FC03F80u);   // (1, 1.5) * s
+  const uint32_t p45 = bmul2(ss, 0x40404000u);   // (2, 3) * s
+  const uint32_t p67 = bmul2(ss, 0x40C04080u);   // (4, 6) * s
+  Lut t;
+  t.L0 = prmt(p01, p23, 0x6420u);
+  t.H0 = prmt(p01, p23, 0x7531u);
+  t.L1 = prmt(p45, p67, 0x6420u);
+  t.H1 = prmt(p45, p67, 0x7531u);
+  return t;
+}
+
+// Expands eight nibbles (n0 in the low bits) into four BF16 pairs.  The K
+// order inside each group of eight is permuted to (n0 n4 n1 n5 n2 n6 n3 n7),
+// identically for A and B, which leaves every dot product unchanged and
+// makes each sign bit one shift away from its place.
+__device__ __forceinline__ uint4 expand8(uint32_t w, const Lut& t) {
+  const uint32_t m = w & 0x77777777u;
+  const uint32_t s1 = prmt(m, 0u, 0x4420u);   // nibbles n0 n1 n4 n5
+  const uint32_t s2 = prmt(m, 0u, 0x4431u);   // nibbles n2 n3 n6 n7
+  const uint32_t la = prmt(t.L0, t.L1, s1), ha = prmt(t.H0, t.H1, s1);
+  const uint32_t lb = prmt(t.L0, t.L1, s2), hb = prmt(t.H0, t.H1, s2);
+  uint4 o;
+  o.x = prmt(la, ha, 0x6240u) | ((w << 12) & 0x80008000u);   // (n0, n4)
+  o.y = prmt(la, ha, 0x7351u) | ((w << 8) & 0x80008000u);    // (n1, n5)
+  o.z = prmt(lb, hb, 0x6240u) | ((w << 4) & 0x80008000u);    // (n2, n6)
+  o.w = prmt(lb, hb, 0x7351u) | (w & 0x80008000u);           // (n3, n7)
+  return o;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+
+// ---------------------------------------------------------------- kernel
+template <bool F32OUT>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                const uint8_t* __restrict__ As, const uint8_t* __restrict__ Bs,
+                const float* __restrict__ TA, const float* __restrict__ TB, int M, int N, int K,
+                int fmt, void* __restrict__ out, int* status) {
+  extern __shared__ uint8_t smem_dyn[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(smem);
+  const uint32_t bar_raw_full = sb + OFF_BAR;
+  const uint32_t bar_raw_empty = bar_raw_full + 8 * S_RAW;
+  const uint32_t bar_bf_full = bar_raw_empty + 8 * S_RAW;
+  const uint32_t bar_bf_empty = bar_bf_full + 8 * S_BF;
+  const uint32_t bar_acc = bar_bf_empty + 8 * S_BF;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+  const int nk = K / BK;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S_RAW; ++i) {
+      mbar_init(bar_raw_full + 8 * i, 1);
+      mbar_init(bar_raw_empty + 8 * i, kDeqThreads / 32);
+    }
+    for (int i = 0; i < S_BF; ++i) {
+      mbar_init(bar_bf_full + 8 * i, kDeqThreads / 32);
+      mbar_init(bar_bf_empty + 8 * i, 1);
+    }
+    mbar_init(bar_acc, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 9) tmem_alloc(sb + OFF_TMEM, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + OFF_TMEM);
+
+  if (warp == 8) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % S_RAW;
+        if (!mbar_wait(bar_raw_empty + 8 * s, ((kb / S_RAW) & 1) ^ 1, abort_flag)) {
+          fail(abort_flag, status);
+          break;
+        }
+        const uint32_t dst = sb + OFF_RAW + s * RAW_STAGE;
+        mbar_expect_tx(bar_raw_full + 8 * s, RAW_STAGE);
+        tma_load_2d(dst, &mapA, kb * (BK / 2), m0, bar_raw_full + 8 * s);
+        tma_load_2d(dst + RAW_A, &mapB, kb * (BK / 2), n0, bar_raw_full + 8 * s);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      for (int kb = 0; kb < nk; ++kb) {
+        const int t = kb % S_BF;
+        if (!mbar_wait(bar_bf_full + 8 * t, (kb / S_BF) & 1, abort_flag)) {
+          fail(abort_flag, status);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a_addr = sb + OFF_BF + t * BF_STAGE;
+        const uint64_t adesc = sw128_desc(a_addr), bdesc = sw128_desc(a_addr + BF_A);
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k)
+          mma_bf16(tmem, adesc + 2 * k, bdesc + 2 * k, kIdesc, (kb | k) != 0 ? 1u : 0u);
+        mma_commit(bar_bf_empty + 8 * t);
+      }
+      mma_commit(bar_acc);
+    }
+  } else {
+    // ------------------------------------------------ expansion warps
+    const int tid = threadIdx.x;            // 0..255
+    const int blk = tid & 3;                 // block of 16 inside the 64-wide K step
+    const int rbase = tid >> 2;              // rows rbase + 64 i, i = 0..5 (A: 0..127, B: 128..383)
+    const int64_t lda_s = K / 16;
+    auto load_codes = [&](int kb, uint32_t (&c)[6]) {
+#pragma unroll
+      for (int i = 0; i < 6; ++i) {
+        const int r = rbase + 64 * i;
+        if (i < 2) {
+          const int gr = m0 + r;
+          c[i] = (gr < M) ? __ldg(As + (int64_t)gr * lda_s + kb * 4 + blk) : 0u;
+        } else {
+          const int gr = n0 + (r - BM);
+          c[i] = (gr < N) ? __ldg(Bs + (int64_t)gr * lda_s + kb * 4 + blk) : 0u;
+        }
+      }
+    };
+    uint32_t codes[6], next[6];
+    load_codes(0, codes);
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % S_RAW, t = kb % S_BF;
+      if (kb + 1 < nk) load_codes(kb + 1, next);
+      if (!mbar_wait(bar_raw_full + 8 * s, (kb / S_RAW) & 1, abort_flag) ||
+          !mbar_wait(bar_bf_empty + 8 * t, ((kb / S_BF) & 1) ^ 1, abort_flag)) {
+        fail(abort_flag, status);
+        break;
+      }
+      const uint32_t raw = sb + OFF_RAW + s * RAW_STAGE;
+      const uint32_t bf = sb + OFF_BF + t * BF_STAGE;
+#pragma unroll
+      for (int i = 0; i < 6; ++i) {
+        const int r = rbase + 64 * i;        // 0..383; A rows then B rows
+        const uint2 w = lds64(raw + r * (BK / 2) + blk * 8);
+        const Lut lut = make_lut(codes[i], fmt);
+        const uint4 lo = expand8(w.x, lut);  // K 16*blk + 0..7
+        const uint4 hi = expand8(w.y, lut);  // K 16*blk + 8..15
+        const uint32_t row_addr = bf + r * 128;   // B rows follow A rows: BF_A = 128 * 128
+        const uint32_t sw = r & 7;
+        sts128(row_addr + (((2 * blk) ^ sw) << 4), lo);
+        sts128(row_addr + (((2 * blk + 1) ^ sw) << 4), hi);
+      }
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar_bf_full + 8 * t);
+        mbar_arrive(bar_raw_empty + 8 * s);
+      }
+#pragma unroll
+      for (int i = 0; i < 6; ++i) codes[i] = next[i];
+    }
+
+    // ------------------------------------------------ epilogue
+    if (mbar_wait(bar_acc, 0, abort_flag)) {
+      tc_fence_after();
+      const int q = warp & 3, half = warp >> 2;
+      const float alpha = __fmul_rn(__ldg(TA), __ldg(TB));
+      const int row = m0 + 32 * q + lane;
+      const bool vec = F32OUT ? (N % 4 == 0) : (N % 8 == 0);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        const int col0 = n0 + 128 * half + 32 * c;
+        uint32_t r[32];
+        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(128 * half + 32 * c), r);
+        if (row >= M || col0 >= N) continue;
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(__uint_as_float(r[j]), alpha);
+        if (F32OUT) {
+          float* o = static_cast<float*>(out) + (int64_t)row * N + col0;
+          if (vec && col0 + 32 <= N) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              reinterpret_cast<float4*>(o)[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          } else {
+            for (int j = 0; j < 32 && col0 + j < N; ++j) o[j] = v[j];
+          }
+        } else {
+          uint32_t h[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(h[j]) : "f"(v[2 * j + 1]), "f"(v[2 * j]));
+          uint16_t* o = static_cast<uint16_t*>(out) + (int64_t)row * N + col0;
+          if (vec && col0 + 32 <= N) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              reinterpret_cast<uint4*>(o)[j] = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+          } else {
+            for (int j = 0; j < 32 && col0 + j < N; ++j)
+              o[j] = (uint16_t)((j & 1) ? (h[j >> 1] >> 16) : (h[j >> 1] & 0xFFFFu));
+          }
+        }
+      }
+    } else {
+      fail(abort_flag, status);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace gemm
+
+// ---------------------------------------------------------------- host side
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D uint8 tensor map over a [rows, K/2] payload, box (32 B, box_rows),
+// out-of-range rows read as zero.
+static bool make_payload_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t K,
+                             uint32_t box_rows) {
+  auto fn = get_encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
+  const cuuint32_t box[2] = {(cuuint32_t)(gemm::BK / 2), box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
+  if (a.M == 0 || a.N == 0) return cudaSuccess;
+  CUtensorMap mapA, mapB;
+  if (!make_payload_map(&mapA, a.A, a.M, a.K, gemm::BM) || !make_payload_map(&mapB, a.B, a.N, a.K, gemm::BN))
+    return cudaErrorNotSupported;
+  dim3 grid((unsigned)((a.N + gemm::BN - 1) / gemm::BN), (unsigned)((a.M + gemm::BM - 1) / gemm::BM));
+  cudaError_t e;
+  if (a.out_f32) {
+    e = cudaFuncSetAttribute(gemm::gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, gemm::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    gemm::gemm_kernel<true><<<grid, gemm::kThreads, gemm::SMEM_BYTES, st>>>(
+        mapA, mapB, a.As, a.Bs, a.TA, a.TB, (int)a.M, (int)a.N, (int)a.K, a.fmt, a.out, a.status);
+  } else {
+    e = cudaFuncSetAttribute(gemm::gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, gemm::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    gemm::gemm_kernel<false><<<grid, gemm::kThreads, gemm::SMEM_BYTES, st>>>(
+        mapA, mapB, a.As, a.Bs, a.TA, a.TB, (int)a.M, (int)a.N, (int)a.K, a.fmt, a.out, a.status);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace fp4q

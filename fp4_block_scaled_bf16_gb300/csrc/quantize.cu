@@ -1,0 +1,416 @@
+// quantize.cu -- memory-bound kernels of libfp4q.so: tensor amax, tensor
+// scale, block-16 E2M1/UE5M3 quantisation (row-wise, column-wise, both from
+// one read; RNE or Philox stochastic rounding) and dequantisation.
+//
+// Method: "UE5M3 FP4 Block Scaling for Stable Language Model Pretraining",
+// Abstract -- E2M1 payloads with UE5M3 block-16 scales under a periodically
+// refreshed FP32 tensor scale; stochastic rounding on backward gradients.
+//
+// Design (GB300): every kernel streams BF16 with 128-bit coalesced loads that
+// bypass L1, keeps blocks in registers, and is launched as a grid-stride loop
+// sized to a multiple of the SM count.  The row-wise quantiser treats the
+// tensor as flat (a block never straddles a row), so that one warp covers 256
+// consecutive elements and a lane pair shares one block (one shuffle for the
+// block amax).  The column-wise quantiser reads 128 x 128 tiles coalesced,
+// quantises the row-wise blocks straight from registers when both axes are
+// asked for, transposes through shared memory and quantises 16-row column
+// blocks from there.
+#include "fp4q_device.cuh"
+#include "fp4q_launch.h"
+
+namespace fp4q {
+
+// ---------------------------------------------------------------- reductions
+__device__ __forceinline__ void flush_stats(StatsDev* g, uint32_t sat, uint32_t uflow,
+                                            uint32_t clamped, uint32_t flushed) {
+  __shared__ unsigned long long s[4];
+  if (threadIdx.x < 4) s[threadIdx.x] = 0ull;
+  __syncthreads();
+  sat = __reduce_add_sync(0xFFFFFFFFu, sat);
+  uflow = __reduce_add_sync(0xFFFFFFFFu, uflow);
+  clamped = __reduce_add_sync(0xFFFFFFFFu, clamped);
+  flushed = __reduce_add_sync(0xFFFFFFFFu, flushed);
+  if ((threadIdx.x & 31) == 0) {
+    atomicAdd(&s[0], (unsigned long long)sat);
+    atomicAdd(&s[1], (unsigned long long)uflow);
+    atomicAdd(&s[2], (unsigned long long)clamped);
+    atomicAdd(&s[3], (unsigned long long)flushed);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (s[0]) atomicAdd(&g->scale_sat, s[0]);
+    if (s[1]) atomicAdd(&g->scale_uflow, s[1]);
+    if (s[2]) atomicAdd(&g->elem_clamped, s[2]);
+    if (s[3]) atomicAdd(&g->elem_flushed, s[3]);
+  }
+}
+
+// Publishes a CTA's max |x| (16-bit pattern): device float amax via an
+// unsigned max on the binary32 pattern (valid for non-negative values), and
+// the non-finite flag.
+__device__ __forceinline__ void flush_amax(float* amax_out, int* status, uint32_t m16) {
+  __shared__ uint32_t s_m;
+  if (threadIdx.x == 0) s_m = 0u;
+  __syncthreads();
+  m16 = __reduce_max_sync(0xFFFFFFFFu, m16);
+  if ((threadIdx.x & 31) == 0) atomicMax(&s_m, m16);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t m = s_m;
+    if (m >= 0x7F80u) atomicOr(status, kStatusNonFinite);
+    if (amax_out && m) atomicMax(reinterpret_cast<unsigned int*>(amax_out), m << 16);
+  }
+}
+
+// ---------------------------------------------------------------- amax
+// Streams the tensor with 128-bit loads, four in flight per thread.
+__global__ void __launch_bounds__(256) amax_kernel(const uint4* __restrict__ in, int64_t nchunks,
+                                                   const uint16_t* __restrict__ tail, int ntail,
+                                                   float* amax_out, int* status) {
+  uint32_t m = 0;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; g + 3 * stride < nchunks; g += 4 * stride) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = ld_stream_v4(in + g + u * stride);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      m = max(m, absmax16(w));
+    }
+  }
+  for (; g < nchunks; g += stride) {
+    const uint4 v = ld_stream_v4(in + g);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    m = max(m, absmax16(w));
+  }
+  if (blockIdx.x == 0 && (int)threadIdx.x < ntail) m = max(m, (uint32_t)(tail[threadIdx.x] & 0x7FFFu));
+  flush_amax(amax_out, status, m);
+}
+
+__global__ void tensor_scale_kernel(const float* amax, float denom, float* out) {
+  const float a = *amax;
+  float t = (a == 0.0f) ? 1.0f : __fdiv_rn(a, denom);
+  if (t < 0x1p-100f) t = 0x1p-100f;
+  *out = t;
+}
+
+// ---------------------------------------------------------------- row-wise
+// One chunk = 8 consecutive elements (16 bytes of BF16) per lane; lanes 2k
+// and 2k+1 hold one block of 16.  The warp loop is uniform so that every
+// lane takes part in the shuffle; inactive lanes carry zeros.
+template <bool SR, bool STATS>
+__global__ void __launch_bounds__(256) quantize_row_kernel(
+    const uint4* __restrict__ in, int64_t nchunks, int fmt, const float* __restrict__ tscale,
+    uint64_t seed, uint32_t* __restrict__ payload, uint8_t* __restrict__ scales, StatsDev* stats,
+    float* amax_out, int* status) {
+  const float T = __ldg(tscale);
+  const float six_t = __fmul_rn(6.0f, T);
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  constexpr int U = 2;  // chunks in flight per lane
+  uint32_t tmax = 0, n_sat = 0, n_uflow = 0, n_clamp = 0, n_flush = 0;
+
+  for (int64_t base = warp * 32 * U; base < nchunks; base += nwarps * 32 * U) {
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t g = base + u * 32 + lane;
+      v[u] = (g < nchunks) ? ld_stream_v4(in + g) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t g = base + u * 32 + lane;
+      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      uint32_t m = absmax16(w);
+      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+      tmax = max(tmax, m);
+      const BlockScale bs = block_scale(m, six_t, T, fmt);
+      uint32_t rb[8];
+      if (SR) {
+        const uint4 a = sr_words4((uint64_t)g * 2, 0u, seed);
+        const uint4 b = sr_words4((uint64_t)g * 2 + 1, 0u, seed);
+        rb[0] = a.x; rb[1] = a.y; rb[2] = a.z; rb[3] = a.w;
+        rb[4] = b.x; rb[5] = b.y; rb[6] = b.z; rb[7] = b.w;
+      }
+      uint32_t c = 0, f = 0;
+      const uint32_t nib = quantize8<SR, STATS>(w, bs.r, rb, &c, &f);
+      if (g < nchunks) {
+        st_stream_u32(payload + g, nib);
+        if ((lane & 1) == 0) scales[g >> 1] = (uint8_t)bs.code;
+        if (STATS) {
+          n_clamp += c;
+          n_flush += f;
+          if ((lane & 1) == 0) {
+            n_sat += bs.sat ? 1u : 0u;
+            n_uflow += (m != 0u && bs.code == 0u) ? 1u : 0u;
+          }
+        }
+      }
+    }
+  }
+  if (STATS) flush_stats(stats, n_sat, n_uflow, n_clamp, n_flush);
+  flush_amax(amax_out, status, tmax);
+}
+
+// ---------------------------------------------------------------- tiles
+// One CTA per 128 x 128 tile (ragged edges masked; sizes are multiples of
+// 16).  Phase 1 loads the tile with 128-bit loads (eight per thread: rows
+// t/16 + 16i, column group t%16); phase 2 (row-wise, optional) quantises from
+// registers exactly like the flat kernel; phase 3 stores the tile in shared
+// memory; phase 4 lets thread t quantise columns 4(t%32)..+3 over rows
+// 16(t/32)..+15 -- four column blocks, one Philox block per row.
+constexpr int kTile = 128;
+
+template <bool SR, bool STATS, bool DO_ROW>
+__global__ void __launch_bounds__(256) quantize_tile_kernel(
+    const uint16_t* __restrict__ in, int64_t R, int64_t C, int fmt,
+    const float* __restrict__ tscale, uint64_t seed, uint32_t* __restrict__ pay_row,
+    uint8_t* __restrict__ sc_row, uint8_t* __restrict__ pay_col, uint8_t* __restrict__ sc_col,
+    StatsDev* stats, float* amax_out, int* status) {
+  __shared__ __align__(16) uint16_t tile[kTile][kTile];
+  const float T = __ldg(tscale);
+  const float six_t = __fmul_rn(6.0f, T);
+  const int t = threadIdx.x, lane = t & 31;
+  const int64_t r0 = (int64_t)blockIdx.y * kTile, c0 = (int64_t)blockIdx.x * kTile;
+  const int rows = (int)(R - r0 < kTile ? R - r0 : kTile);
+  const int cols = (int)(C - c0 < kTile ? C - c0 : kTile);
+  uint32_t tmax = 0, n_sat = 0, n_uflow = 0, n_clamp = 0, n_flush = 0;
+
+  // phase 1: coalesced loads
+  const int cg = t & 15;
+  uint4 v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int row = (t >> 4) + 16 * i;
+    const bool ok = row < rows && cg * 8 < cols;
+    v[i] = ok ? ld_stream_v4(in + (r0 + row) * C + c0 + cg * 8) : make_uint4(0, 0, 0, 0);
+  }
+  // phase 2: row-wise blocks from registers
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int row = (t >> 4) + 16 * i;
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+    uint32_t m = absmax16(w);
+    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+    tmax = max(tmax, m);
+    if (DO_ROW) {
+      const bool ok = row < rows && cg * 8 < cols;
+      const int64_t e0 = (r0 + row) * C + c0 + cg * 8;  // logical index of the chunk
+      const BlockScale bs = block_scale(m, six_t, T, fmt);
+      uint32_t rb[8];
+      if (SR) {
+        const uint4 a = sr_words4((uint64_t)e0 >> 2, 0u, seed);
+        const uint4 b = sr_words4(((uint64_t)e0 >> 2) + 1, 0u, seed);
+        rb[0] = a.x; rb[1] = a.y; rb[2] = a.z; rb[3] = a.w;
+        rb[4] = b.x; rb[5] = b.y; rb[6] = b.z; rb[7] = b.w;
+      }
+      uint32_t c = 0, f = 0;
+      const uint32_t nib = quantize8<SR, STATS>(w, bs.r, rb, &c, &f);
+      if (ok) {
+        st_stream_u32(pay_row + (e0 >> 3), nib);
+        if ((lane & 1) == 0) sc_row[e0 >> 4] = (uint8_t)bs.code;
+        if (STATS) {
+          n_clamp += c;
+          n_flush += f;
+          if ((lane & 1) == 0) {
+            n_sat += bs.sat ? 1u : 0u;
+            n_uflow += (m != 0u && bs.code == 0u) ? 1u : 0u;
+          }
+        }
+      }
+    }
+    *reinterpret_cast<uint4*>(&tile[row][cg * 8]) = v[i];
+  }
+  if (DO_ROW && STATS) {
+    // row-wise counters go to stats[0]; column-wise ones to stats[1]
+    flush_stats(stats, n_sat, n_uflow, n_clamp, n_flush);
+    n_sat = n_uflow = n_clamp = n_flush = 0;
+  }
+  __syncthreads();
+
+  // phase 4: column blocks from shared memory
+  const int q4 = lane * 4;         // first of four columns
+  const int rb16 = (t >> 5) * 16;  // first of 16 rows
+  const bool ok = q4 < cols && rb16 < rows;
+  uint32_t cw[4][8];  // [column j][row pair] packed as BF16 pairs (rows 2p, 2p+1)
+  uint32_t cm[4] = {0, 0, 0, 0};
+  uint32_t rnd[16][4];
+#pragma unroll
+  for (int p = 0; p < 8; ++p) {
+    const uint2 a = *reinterpret_cast<const uint2*>(&tile[rb16 + 2 * p][q4]);
+    const uint2 b = *reinterpret_cast<const uint2*>(&tile[rb16 + 2 * p + 1][q4]);
+    // a.x = cols (q4, q4+1) of row 2p, a.y = cols (q4+2, q4+3)
+    cw[0][p] = __byte_perm(a.x, b.x, 0x5410);
+    cw[1][p] = __byte_perm(a.x, b.x, 0x7632);
+    cw[2][p] = __byte_perm(a.y, b.y, 0x5410);
+    cw[3][p] = __byte_perm(a.y, b.y, 0x7632);
+  }
+  if (SR) {
+#pragma unroll
+    for (int rr = 0; rr < 16; ++rr) {
+      const int64_t e = (r0 + rb16 + rr) * C + c0 + q4;  // multiple of 4
+      const uint4 w = sr_words4((uint64_t)e >> 2, 1u, seed);
+      rnd[rr][0] = w.x; rnd[rr][1] = w.y; rnd[rr][2] = w.z; rnd[rr][3] = w.w;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t w4[4] = {cw[j][4 * h], cw[j][4 * h + 1], cw[j][4 * h + 2], cw[j][4 * h + 3]};
+      cm[j] = max(cm[j], absmax16(w4));
+    }
+    const BlockScale bs = block_scale(cm[j], six_t, T, fmt);
+    uint32_t nib[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t w4[4] = {cw[j][4 * h], cw[j][4 * h + 1], cw[j][4 * h + 2], cw[j][4 * h + 3]};
+      uint32_t rb[8];
+      if (SR) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) rb[k] = rnd[8 * h + k][j];
+      }
+      uint32_t c = 0, f = 0;
+      nib[h] = quantize8<SR, STATS>(w4, bs.r, rb, &c, &f);
+      if (STATS && ok) { n_clamp += c; n_flush += f; }
+    }
+    if (STATS && ok) {
+      n_sat += bs.sat ? 1u : 0u;
+      n_uflow += (cm[j] != 0u && bs.code == 0u) ? 1u : 0u;
+    }
+    if (ok) {
+      const int64_t col = c0 + q4 + j;
+      *reinterpret_cast<uint2*>(pay_col + col * (R / 2) + (r0 + rb16) / 2) = make_uint2(nib[0], nib[1]);
+      sc_col[col * (R / 16) + (r0 + rb16) / 16] = (uint8_t)bs.code;
+    }
+  }
+  if (STATS) flush_stats(stats + (DO_ROW ? 1 : 0), n_sat, n_uflow, n_clamp, n_flush);
+  flush_amax(amax_out, status, tmax);
+}
+
+// ---------------------------------------------------------------- dequantise
+// v = (e * s) * T per element, one binary32 rounding each, then BF16 (RNE)
+// or binary32.  One chunk = 8 elements = one payload word.
+template <bool F32>
+__global__ void __launch_bounds__(256) dequantize_kernel(const uint32_t* __restrict__ payload,
+                                                         const uint8_t* __restrict__ scales,
+                                                         int64_t nchunks, int fmt,
+                                                         const float* __restrict__ tscale,
+                                                         void* __restrict__ out) {
+  const float T = __ldg(tscale);
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < nchunks; g += stride) {
+    const uint32_t p = __ldg(payload + g);
+    const float s = decode_scale(__ldg(scales + (g >> 1)), fmt);
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t n = (p >> (4 * j)) & 15u;
+      // E2M1 magnitude: exponent field (n>>1)&3, mantissa n&1
+      const uint32_t e = (n >> 1) & 3u, m = n & 1u;
+      float mag = (e == 0) ? (m ? 0.5f : 0.0f) : __uint_as_float(((e + 126u) << 23) | (m << 22));
+      if (n & 8u) mag = -mag;
+      v[j] = __fmul_rn(__fmul_rn(mag, s), T);
+    }
+    if (F32) {
+      float4* o = reinterpret_cast<float4*>(out) + 2 * g;
+      o[0] = make_float4(v[0], v[1], v[2], v[3]);
+      o[1] = make_float4(v[4], v[5], v[6], v[7]);
+    } else {
+      uint32_t h[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(h[j]) : "f"(v[2 * j + 1]), "f"(v[2 * j]));
+      reinterpret_cast<uint4*>(out)[g] = make_uint4(h[0], h[1], h[2], h[3]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- launchers
+static int grid_for(int64_t work_items, int threads, int per_sm) {
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t need = (work_items + threads - 1) / threads;
+  const int64_t cap = (int64_t)sms * per_sm;
+  const int64_t g = need < cap ? need : cap;
+  return (int)(g < 1 ? 1 : g);
+}
+
+cudaError_t launch_amax(const void* in, int64_t n, float* out, int* status, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(out, 0, sizeof(float), st);
+  if (e != cudaSuccess) return e;
+  const int64_t nchunks = n / 8;
+  const int ntail = (int)(n % 8);
+  const uint16_t* tail = static_cast<const uint16_t*>(in) + nchunks * 8;
+  amax_kernel<<<grid_for(nchunks > 0 ? nchunks : 1, 256, 8), 256, 0, st>>>(
+      static_cast<const uint4*>(in), nchunks, tail, ntail, out, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tensor_scale(const float* amax, float denom, float* out, cudaStream_t st) {
+  tensor_scale_kernel<<<1, 1, 0, st>>>(amax, denom, out);
+  return cudaGetLastError();
+}
+
+template <bool SR, bool STATS>
+static void row_launch(const QuantArgs& a, cudaStream_t st) {
+  const int64_t nchunks = a.rows * a.cols / 8;
+  quantize_row_kernel<SR, STATS><<<grid_for(nchunks / 2, 256, 8), 256, 0, st>>>(
+      static_cast<const uint4*>(a.in), nchunks, a.fmt, a.tscale, a.seed,
+      reinterpret_cast<uint32_t*>(a.pay_row), a.sc_row, a.stats, a.amax_out, a.status);
+}
+
+template <bool SR, bool STATS, bool DO_ROW>
+static void tile_launch(const QuantArgs& a, cudaStream_t st) {
+  dim3 grid((unsigned)((a.cols + kTile - 1) / kTile), (unsigned)((a.rows + kTile - 1) / kTile));
+  quantize_tile_kernel<SR, STATS, DO_ROW><<<grid, 256, 0, st>>>(
+      static_cast<const uint16_t*>(a.in), a.rows, a.cols, a.fmt, a.tscale, a.seed,
+      reinterpret_cast<uint32_t*>(a.pay_row), a.sc_row, a.pay_col, a.sc_col, a.stats, a.amax_out,
+      a.status);
+}
+
+cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t st) {
+  cudaError_t e;
+  if (a.stats) {
+    e = cudaMemsetAsync(a.stats, 0, sizeof(StatsDev) * (a.axis == 2 ? 2 : 1), st);
+    if (e != cudaSuccess) return e;
+  }
+  if (a.amax_out) {
+    e = cudaMemsetAsync(a.amax_out, 0, sizeof(float), st);
+    if (e != cudaSuccess) return e;
+  }
+  if (a.rows == 0 || a.cols == 0) return cudaSuccess;
+  const bool sr = a.sr, stats = a.stats != nullptr;
+  if (a.axis == 0) {
+    if (sr) stats ? row_launch<true, true>(a, st) : row_launch<true, false>(a, st);
+    else stats ? row_launch<false, true>(a, st) : row_launch<false, false>(a, st);
+  } else if (a.axis == 1) {
+    if (sr) stats ? tile_launch<true, true, false>(a, st) : tile_launch<true, false, false>(a, st);
+    else stats ? tile_launch<false, true, false>(a, st) : tile_launch<false, false, false>(a, st);
+  } else {
+    if (sr) stats ? tile_launch<true, true, true>(a, st) : tile_launch<true, false, true>(a, st);
+    else stats ? tile_launch<false, true, true>(a, st) : tile_launch<false, false, true>(a, st);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequantize(const uint8_t* payload, const uint8_t* scales, int64_t rows,
+                              int64_t cols, int fmt, const float* tscale, void* out, bool f32,
+                              cudaStream_t st) {
+  const int64_t nchunks = rows * cols / 8;
+  if (nchunks == 0) return cudaSuccess;
+  const int grid = grid_for(nchunks, 256, 8);
+  if (f32)
+    dequantize_kernel<true><<<grid, 256, 0, st>>>(reinterpret_cast<const uint32_t*>(payload), scales,
+                                                  nchunks, fmt, tscale, out);
+  else
+    dequantize_kernel<false><<<grid, 256, 0, st>>>(reinterpret_cast<const uint32_t*>(payload), scales,
+                                                   nchunks, fmt, tscale, out);
+  return cudaGetLastError();
+}
+
+}  // namespace fp4q

@@ -1,0 +1,204 @@
+"""Python binding of libfp4q.so (include/fp4q.h): argument marshalling only.
+
+Every function named ``fp4q_*`` here calls the C entry point of the same name
+with the device pointers of the torch tensors it is given, on the current
+torch CUDA stream; all arithmetic happens in the library's CUDA kernels.  The
+lower-case helpers (``quantize``, ``gemm`` ...) only allocate the output
+tensors with torch before calling them.
+
+Importing this module loads the library and raises if it is missing: there is
+no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libfp4q.so")
+
+OK, ERR_ARG, ERR_SHAPE, ERR_ALIGN, ERR_CUDA, ERR_NONFINITE, ERR_TIMEOUT = range(7)
+AXIS_ROW, AXIS_COL, AXIS_BOTH = 0, 1, 2
+RNE, SR = 0, 1
+UE5M3, UE4M3 = 0, 1
+
+# every symbol include/fp4q.h declares
+EXPORTS = ("fp4q_amax", "fp4q_tensor_scale", "fp4q_quantize", "fp4q_dequantize", "fp4q_gemm",
+           "fp4q_get_device_status", "fp4q_status_string")
+
+
+class Fp4qError(RuntimeError):
+    def __init__(self, fn, code, lib):
+        msg = lib.fp4q_status_string(code).decode()
+        super().__init__(f"{fn} failed: {msg} (status {code})")
+        self.code = code
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise ImportError(f"libfp4q.so not built at {path}; run "
+                          "`python -m fp4_block_scaled_bf16_gb300.build`")
+    lib = ctypes.CDLL(path)
+    P, i64, i32, u64, f32 = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint64,
+                             ctypes.c_float)
+    lib.fp4q_amax.argtypes = [P, i64, P, P]
+    lib.fp4q_tensor_scale.argtypes = [P, i32, f32, P, P]
+    lib.fp4q_quantize.argtypes = [P, i64, i64, i32, i32, P, i32, u64, P, P, P, P, P, P, P]
+    lib.fp4q_dequantize.argtypes = [P, P, i64, i64, i32, P, P, i32, P]
+    lib.fp4q_gemm.argtypes = [P, P, P, P, P, P, i64, i64, i64, i32, P, i32, P]
+    lib.fp4q_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_int)]
+    lib.fp4q_status_string.argtypes = [i32]
+    lib.fp4q_status_string.restype = ctypes.c_char_p
+    for name in EXPORTS[:-1]:
+        getattr(lib, name).restype = i32
+    return lib
+
+
+_lib = load_library()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _check(fn, code):
+    if code != OK:
+        raise Fp4qError(fn, code, _lib)
+
+
+def _dev(t, name, dtype=None):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+# ------------------------------------------------------------ C entry points
+def fp4q_amax(x: torch.Tensor, out_amax: torch.Tensor) -> None:
+    _dev(x, "x", torch.bfloat16)
+    _dev(out_amax, "out_amax", torch.float32)
+    _check("fp4q_amax", _lib.fp4q_amax(_ptr(x), x.numel(), _ptr(out_amax), _stream()))
+
+
+def fp4q_tensor_scale(amax: torch.Tensor, fmt: int, headroom: float, out_scale: torch.Tensor) -> None:
+    _dev(amax, "amax", torch.float32)
+    _dev(out_scale, "out_scale", torch.float32)
+    _check("fp4q_tensor_scale",
+           _lib.fp4q_tensor_scale(_ptr(amax), fmt, headroom, _ptr(out_scale), _stream()))
+
+
+def fp4q_quantize(x, axis, fmt, tensor_scale, rnd, seed, payload_row, scales_row, payload_col,
+                  scales_col, stats=None, amax=None) -> None:
+    _dev(x, "x", torch.bfloat16)
+    for n, t in (("payload_row", payload_row), ("scales_row", scales_row),
+                 ("payload_col", payload_col), ("scales_col", scales_col)):
+        _dev(t, n, torch.uint8)
+    _dev(tensor_scale, "tensor_scale", torch.float32)
+    _dev(stats, "stats", torch.int64)
+    _dev(amax, "amax", torch.float32)
+    rows, cols = x.shape
+    _check("fp4q_quantize", _lib.fp4q_quantize(
+        _ptr(x), rows, cols, axis, fmt, _ptr(tensor_scale), rnd, ctypes.c_uint64(seed),
+        _ptr(payload_row), _ptr(scales_row), _ptr(payload_col), _ptr(scales_col),
+        _ptr(stats), _ptr(amax), _stream()))
+
+
+def fp4q_dequantize(payload, scales, rows, cols, fmt, tensor_scale, out) -> None:
+    _dev(payload, "payload", torch.uint8)
+    _dev(scales, "scales", torch.uint8)
+    _dev(out, "out")
+    f32 = out.dtype == torch.float32
+    _check("fp4q_dequantize", _lib.fp4q_dequantize(
+        _ptr(payload), _ptr(scales), rows, cols, fmt, _ptr(tensor_scale), _ptr(out), int(f32),
+        _stream()))
+
+
+def fp4q_gemm(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K, fmt, out) -> None:
+    for n, t in (("A", A), ("A_scales", A_scales), ("B", B), ("B_scales", B_scales)):
+        _dev(t, n, torch.uint8)
+    _dev(out, "out")
+    f32 = out.dtype == torch.float32
+    _check("fp4q_gemm", _lib.fp4q_gemm(
+        _ptr(A), _ptr(A_scales), _ptr(A_tscale), _ptr(B), _ptr(B_scales), _ptr(B_tscale),
+        M, N, K, fmt, _ptr(out), int(f32), _stream()))
+
+
+def fp4q_get_device_status() -> int:
+    v = ctypes.c_int(0)
+    _check("fp4q_get_device_status", _lib.fp4q_get_device_status(ctypes.byref(v)))
+    return v.value
+
+
+def fp4q_status_string(code: int) -> str:
+    return _lib.fp4q_status_string(code).decode()
+
+
+# ------------------------------------------------------------ allocating helpers
+def amax(x: torch.Tensor) -> torch.Tensor:
+    out = torch.empty(1, dtype=torch.float32, device=x.device)
+    fp4q_amax(x, out)
+    return out
+
+
+def tensor_scale(amax_t: torch.Tensor, fmt: int = UE5M3, headroom: float = 1.0) -> torch.Tensor:
+    out = torch.empty(1, dtype=torch.float32, device=amax_t.device)
+    fp4q_tensor_scale(amax_t, fmt, headroom, out)
+    return out
+
+
+class Quantized:
+    """Outputs of one quantisation (device tensors)."""
+
+    def __init__(self, **kw):
+        self.__dict__.update(kw)
+
+
+def quantize(x: torch.Tensor, axis: int = AXIS_ROW, T: torch.Tensor | None = None,
+             fmt: int = UE5M3, rnd: int = RNE, seed: int = 0, stats: bool = False,
+             want_amax: bool = False) -> Quantized:
+    """Allocates outputs and calls fp4q_quantize.  T defaults to the current
+    tensor scale (fp4q_amax + fp4q_tensor_scale)."""
+    R, C = x.shape
+    dev = x.device
+    if T is None:
+        T = tensor_scale(amax(x), fmt)
+    pr = sr = pc = sc = None
+    if axis in (AXIS_ROW, AXIS_BOTH):
+        pr = torch.empty((R, C // 2), dtype=torch.uint8, device=dev)
+        sr = torch.empty((R, C // 16), dtype=torch.uint8, device=dev)
+    if axis in (AXIS_COL, AXIS_BOTH):
+        pc = torch.empty((C, R // 2), dtype=torch.uint8, device=dev)
+        sc = torch.empty((C, R // 16), dtype=torch.uint8, device=dev)
+    st = torch.empty((2 if axis == AXIS_BOTH else 1, 4), dtype=torch.int64, device=dev) if stats else None
+    am = torch.empty(1, dtype=torch.float32, device=dev) if want_amax else None
+    fp4q_quantize(x, axis, fmt, T, rnd, seed, pr, sr, pc, sc, st, am)
+    return Quantized(payload_row=pr, scales_row=sr, payload_col=pc, scales_col=sc, stats=st,
+                     amax=am, T=T, fmt=fmt)
+
+
+def dequantize(payload, scales, T, fmt: int = UE5M3, dtype=torch.bfloat16) -> torch.Tensor:
+    R, C = payload.shape[0], payload.shape[1] * 2
+    out = torch.empty((R, C), dtype=dtype, device=payload.device)
+    fp4q_dequantize(payload, scales, R, C, fmt, T, out)
+    return out
+
+
+def gemm(A, A_scales, A_tscale, B, B_scales, B_tscale, fmt: int = UE5M3,
+         dtype=torch.bfloat16, out=None) -> torch.Tensor:
+    """C = (T_A T_B) deq(A) deq(B)^T for K-major quantised A [M, K/2], B [N, K/2]."""
+    M, K = A.shape[0], A.shape[1] * 2
+    N = B.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=dtype, device=A.device)
+    fp4q_gemm(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K, fmt, out)
+    return out

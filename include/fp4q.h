@@ -1,0 +1,147 @@
+/*
+ * fp4q.h -- C ABI of libfp4q.so: UE5M3-scaled FP4 (E2M1) quantisation and the
+ * block-scaled GEMM on a GB300 (sm_103a).
+ *
+ * Method: "UE5M3 FP4 Block Scaling for Stable Language Model Pretraining",
+ * Abstract.  Linear-layer operands are stored as E2M1 payloads with one
+ * unsigned E5M3 (UE5M3) scale per block of 16 elements under an FP32 tensor
+ * scale refreshed periodically; forward operands round to nearest even and
+ * backward gradients round stochastically; all internal linears run their
+ * matrix multiplications (fprop, dgrad, wgrad) on these operands, with UE5M3
+ * emulated in software because tensor cores take only E4M3/E8M0 block scales.
+ *
+ * Conventions shared by every call
+ *  - Every pointer argument except `stream` and those documented as host
+ *    pointers is a DEVICE pointer, owned by the caller; the library never
+ *    allocates or frees memory, and never synchronises the stream (except
+ *    fp4q_get_device_status).  Calls are asynchronous on `stream`
+ *    (a cudaStream_t; NULL = the legacy default stream).
+ *  - Data-dependent scalars (amax, tensor scale) stay on the device, so that a
+ *    whole quantise -> GEMM sequence needs no host round trip.
+ *  - Tensors are row-major and densely packed.  Every pointer must be 16-byte
+ *    aligned.  BF16 is the IEEE bfloat16 bit pattern (uint16).
+ *  - Validation errors (bad enum, shape, null or misaligned pointer) are
+ *    returned synchronously before any launch and nothing is written.
+ *    Launch failures return FP4Q_ERR_CUDA.  Conditions only the GPU can see
+ *    (non-finite input, a pipeline wait that ran out) are latched in a device
+ *    status word read by fp4q_get_device_status.
+ *
+ * Formats (readings of the method where the abstract leaves them open)
+ *  - E2M1 element: sign bit 3, 2-bit exponent (bias 1), 1-bit mantissa;
+ *    magnitudes {0, 0.5, 1, 1.5, 2, 3, 4, 6}.  Packed two per byte, the
+ *    element with the even index in the low nibble.
+ *  - UE5M3 scale: 5-bit exponent (bias 15), 3-bit mantissa, subnormals
+ *    m/8 * 2^-14, 0xFF reserved (never produced), largest 0xFE = 114688.
+ *    UE4M3 (bias 7, largest 0x7E = 448) is available for comparison.
+ *  - Tensor scale T = amax / (6 * Smax / H), T = 1 for an all-zero tensor,
+ *    raised to 2^-100 if smaller.
+ *  - Block of 16: s* = amax_b / (6 T) rounded to the scale format (nearest,
+ *    ties to even, saturating); element q = x * (1 / (s T)); RNE or
+ *    stochastic rounding to E2M1, saturating at 6.  Every product, quotient
+ *    and reciprocal is one IEEE binary32 operation rounded to nearest even.
+ *  - Stochastic rounding draws Philox4x32-10 (key = seed), counter
+ *    (i/4, i/4 >> 32, axis, 0), word i % 4, for the element with row-major
+ *    index i of the input; round up iff (word >> 8) * 2^-24 < fractional
+ *    position between the two neighbouring grid points.
+ */
+#ifndef FP4Q_H
+#define FP4Q_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FP4Q_OK = 0,
+    FP4Q_ERR_ARG = 1,        /* null pointer or unknown enum value */
+    FP4Q_ERR_SHAPE = 2,      /* a size is not a supported multiple */
+    FP4Q_ERR_ALIGN = 3,      /* a pointer is not 16-byte aligned */
+    FP4Q_ERR_CUDA = 4,       /* a CUDA runtime/driver call failed */
+    FP4Q_ERR_NONFINITE = 5,  /* device status: an input element was inf/NaN */
+    FP4Q_ERR_TIMEOUT = 6     /* device status: a bounded pipeline wait gave up */
+} fp4q_status;
+
+typedef enum { FP4Q_AXIS_ROW = 0, FP4Q_AXIS_COL = 1, FP4Q_AXIS_BOTH = 2 } fp4q_axis;
+typedef enum { FP4Q_RNE = 0, FP4Q_SR = 1 } fp4q_rounding;
+typedef enum { FP4Q_SCALE_UE5M3 = 0, FP4Q_SCALE_UE4M3 = 1 } fp4q_scale_fmt;
+
+/* Per-quantisation counters, device resident. */
+typedef struct {
+    unsigned long long scale_sat_blocks;    /* blocks with s* above the largest scale */
+    unsigned long long scale_uflow_blocks;  /* nonzero blocks whose scale encoded to 0 */
+    unsigned long long elem_clamped;        /* elements with |q| > 6 (saturated) */
+    unsigned long long elem_flushed;        /* nonzero elements encoded as (+-)0 */
+} fp4q_stats;
+
+/* amax = max |x| over n BF16 elements (the current-tensor-scaling pass of the
+ * method's TE baseline, and the first refresh of periodic scaling).
+ * in_bf16: device, n elements.  out_amax: device float, overwritten.
+ * n may be 0 (amax = 0).  A non-finite element latches FP4Q_ERR_NONFINITE. */
+fp4q_status fp4q_amax(const void* in_bf16, int64_t n, float* out_amax, void* stream);
+
+/* Tensor scale from an amax (periodic tensor scaling, Abstract):
+ * *out_scale = amax / (6 * Smax(fmt) / headroom) with the zero and floor
+ * rules above.  amax, out_scale: device floats.  headroom: host value, a
+ * power of two >= 1. */
+fp4q_status fp4q_tensor_scale(const float* amax, fp4q_scale_fmt fmt, float headroom,
+                              float* out_scale, void* stream);
+
+/* Block-16 quantisation of a rows x cols BF16 tensor (E2M1 + UE5M3 block
+ * scales, Abstract).  rows and cols: multiples of 16, >= 0.
+ *  axis ROW : blocks along a row.  out_payload_row [rows, cols/2] bytes,
+ *             out_scales_row [rows, cols/16] bytes.
+ *  axis COL : blocks along a column, written as the row-wise quantisation of
+ *             the transpose: out_payload_col [cols, rows/2],
+ *             out_scales_col [cols, rows/16].
+ *  axis BOTH: both outputs from one read of the input.
+ * Unused output pointers may be NULL.  tensor_scale: device float (T).
+ * rnd/seed: FP4Q_SR draws its bits as stated above (row-wise uses axis id 0,
+ * column-wise 1); seed is ignored for FP4Q_RNE.
+ * out_stats (nullable): zeroed, then filled; for BOTH it points to TWO structs
+ * (row-wise, column-wise).  out_amax (nullable): zeroed, then set to max |x|
+ * of this input -- the by-product periodic scaling keeps for its next
+ * refresh. */
+fp4q_status fp4q_quantize(const void* in_bf16, int64_t rows, int64_t cols, fp4q_axis axis,
+                          fp4q_scale_fmt fmt, const float* tensor_scale, fp4q_rounding rnd,
+                          uint64_t seed,
+                          uint8_t* out_payload_row, uint8_t* out_scales_row,
+                          uint8_t* out_payload_col, uint8_t* out_scales_col,
+                          fp4q_stats* out_stats, float* out_amax, void* stream);
+
+/* Dequantisation of a [rows, cols] block-scaled tensor quantised along its
+ * rows: v = (e * s) * T, each product rounded to binary32, written as BF16
+ * (rounded to nearest even) or binary32 (out_is_f32 != 0).
+ * payload [rows, cols/2], scales [rows, cols/16], tensor_scale device float. */
+fp4q_status fp4q_dequantize(const uint8_t* payload, const uint8_t* scales, int64_t rows,
+                            int64_t cols, fp4q_scale_fmt fmt, const float* tensor_scale,
+                            void* out, int out_is_f32, void* stream);
+
+/* Block-scaled GEMM, the method's FP4 matrix multiplication (fprop
+ * Y = X W^T, dgrad dX = dY W, wgrad dW = dY^T X, each written as C = A B^T):
+ *   C[m, n] = (T_A * T_B) * sum_k deq(A)[m, k] * deq(B)[n, k]
+ * A: payload [M, K/2] + scales [M, K/16], B: payload [N, K/2] + scales
+ * [N, K/16], both quantised along K; A_tscale, B_tscale device floats.
+ * The UE5M3 scales are applied in software: each tile is expanded in shared
+ * memory to BF16 (exact: e*s has at most 6 significant bits) and multiplied
+ * on the tcgen05 tensor cores with binary32 accumulation.  out: [M, N] BF16
+ * (out_is_f32 == 0) or binary32.  M, N >= 1 (any), K a multiple of 64. */
+fp4q_status fp4q_gemm(const uint8_t* A, const uint8_t* A_scales, const float* A_tscale,
+                      const uint8_t* B, const uint8_t* B_scales, const float* B_tscale,
+                      int64_t M, int64_t N, int64_t K, fp4q_scale_fmt fmt,
+                      void* out, int out_is_f32, void* stream);
+
+/* Synchronises the current device, returns the latched device status word
+ * in *out (an fp4q_status value, FP4Q_OK if none) and clears it.
+ * out: HOST pointer. */
+fp4q_status fp4q_get_device_status(int* out);
+
+/* Static description of a status code.  Never NULL. */
+const char* fp4q_status_string(fp4q_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP4Q_H */

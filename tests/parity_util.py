@@ -1,0 +1,75 @@
+"""Helpers shared by the GPU parity tests: run the CUDA path through the C ABI
+(binding) and the oracle on the same seeded inputs, compare."""
+import numpy as np
+import torch
+
+import oracle
+from fp4_block_scaled_bf16_gb300 import workloads
+
+# GEMM tolerance: the method's statement of the target is "max relative error
+# <= 1e-3 against the FP64 accumulation of identical dequantised operands",
+# read normwise (max |C - R| / max |R|) because an elementwise ratio is
+# unbounded where R cancels to ~0.  BF16 output adds one BF16 rounding (half
+# an ulp) on top.
+GEMM_TOL = 1e-3
+
+
+def to_dev(bits: np.ndarray) -> torch.Tensor:
+    return workloads.to_torch_bf16(bits).cuda()
+
+
+def np_u8(t: torch.Tensor) -> np.ndarray:
+    return t.cpu().numpy()
+
+
+def gpu_tensor_scale(x: torch.Tensor, fmt=0, headroom=1.0):
+    from fp4_block_scaled_bf16_gb300 import fp4q
+    a = fp4q.amax(x)
+    return a, fp4q.tensor_scale(a, fmt, headroom)
+
+
+def check_quantize(bits: np.ndarray, axis: int, fmt=0, rnd=0, seed=0, T=None, headroom=1.0):
+    """Quantise on the GPU and with the oracle; assert bytes, stats and the
+    fused amax agree exactly.  Returns the oracle outputs."""
+    from fp4_block_scaled_bf16_gb300 import fp4q
+    x = to_dev(bits)
+    if T is None:
+        a_dev, T_dev = gpu_tensor_scale(x, fmt, headroom)
+        a_or, _ = oracle.amax(bits)
+        T_or = oracle.tensor_scale(a_or, fmt, headroom)
+        assert float(a_dev.item()) == a_or
+        assert float(T_dev.item()) == T_or
+    else:
+        T_dev = torch.tensor([T], dtype=torch.float32, device="cuda")
+        T_or = float(np.float32(T))
+    q = fp4q.quantize(x, axis, T_dev, fmt, rnd, seed, stats=True, want_amax=True)
+    torch.cuda.synchronize()
+    out = {}
+    axes = [oracle.ROW, oracle.COL] if axis == fp4q.AXIS_BOTH else [axis]
+    for k, ax in enumerate(axes):
+        p, s, st = oracle.quantize(bits, ax, T_or, fmt, rnd, seed)
+        gp = q.payload_row if ax == oracle.ROW else q.payload_col
+        gs = q.scales_row if ax == oracle.ROW else q.scales_col
+        gp, gs = np_u8(gp), np_u8(gs)
+        if not np.array_equal(gp, p):
+            bad = np.argwhere(gp != p)
+            raise AssertionError(f"payload axis {ax}: {len(bad)} bytes differ, first {bad[:4].tolist()} "
+                                 f"gpu {gp[tuple(bad[0])]:#04x} oracle {p[tuple(bad[0])]:#04x}")
+        if not np.array_equal(gs, s):
+            bad = np.argwhere(gs != s)
+            raise AssertionError(f"scales axis {ax}: {len(bad)} differ, first {bad[:4].tolist()}")
+        gst = q.stats.cpu().numpy()[k].astype(np.uint64)
+        assert np.array_equal(gst, st), (ax, gst, st)
+        out[ax] = (p, s, st)
+    assert float(q.amax.item()) == oracle.amax(bits)[0]
+    return out, T_or, q
+
+
+def gemm_error(C: np.ndarray, R: np.ndarray) -> float:
+    return float(np.abs(C.astype(np.float64) - R).max() / max(np.abs(R).max(), 1e-300))
+
+
+def bf16_ulp(x: np.ndarray) -> np.ndarray:
+    a = np.abs(x).astype(np.float64)
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
+    return 2.0 ** (e - 7)

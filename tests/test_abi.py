@@ -1,0 +1,120 @@
+"""The C ABI boundary without a GPU: libfp4q.so builds for sm_103a, loads,
+exports every entry point that include/fp4q.h declares, and rejects invalid
+arguments on the host before touching the device."""
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp4q.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fp4q_\w+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not shutil.which("nvcc") and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+        pytest.skip("nvcc not available")
+    from fp4_block_scaled_bf16_gb300 import build
+    path = build.build()
+    L = ctypes.CDLL(path)
+    L.fp4q_status_string.restype = ctypes.c_char_p
+    return L
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    assert names == sorted(["fp4q_amax", "fp4q_tensor_scale", "fp4q_quantize", "fp4q_dequantize",
+                            "fp4q_gemm", "fp4q_get_device_status", "fp4q_status_string"] +
+                           [n for n in names if n not in (
+                               "fp4q_amax", "fp4q_tensor_scale", "fp4q_quantize", "fp4q_dequantize",
+                               "fp4q_gemm", "fp4q_get_device_status", "fp4q_status_string")])
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_binding_lists_every_export():
+    names = declared_functions()
+    src = open(os.path.join(ROOT, "fp4_block_scaled_bf16_gb300", "fp4q.py")).read()
+    for n in names:
+        assert f'"{n}"' in src, n
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        s = lib.fp4q_status_string(code)
+        assert s and s != b"unknown status"
+    assert lib.fp4q_status_string(99) == b"unknown status"
+
+
+def _q(lib, **kw):
+    a = dict(inp=16, rows=32, cols=32, axis=0, fmt=0, ts=16, rnd=0, pr=16, sr=16, pc=16, sc=16)
+    a.update(kw)
+    P = ctypes.c_void_p
+    f = lib.fp4q_quantize
+    f.argtypes = [P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int, P, ctypes.c_int,
+                  ctypes.c_uint64, P, P, P, P, P, P, P]
+    return f(P(a["inp"]), a["rows"], a["cols"], a["axis"], a["fmt"], P(a["ts"]), a["rnd"], 0,
+             P(a["pr"]), P(a["sr"]), P(a["pc"]), P(a["sc"]), None, None, None)
+
+
+def test_host_validation_rejects_before_launch(lib):
+    ERR_ARG, ERR_SHAPE, ERR_ALIGN = 1, 2, 3
+    assert _q(lib, rows=17) == ERR_SHAPE
+    assert _q(lib, cols=8) == ERR_SHAPE
+    assert _q(lib, rows=-16) == ERR_SHAPE
+    assert _q(lib, axis=3) == ERR_ARG
+    assert _q(lib, fmt=2) == ERR_ARG
+    assert _q(lib, rnd=2) == ERR_ARG
+    assert _q(lib, ts=0) == ERR_ARG
+    assert _q(lib, inp=0) == ERR_ARG
+    assert _q(lib, pr=0) == ERR_ARG
+    assert _q(lib, axis=1, pc=0) == ERR_ARG
+    assert _q(lib, inp=24) == ERR_ALIGN
+    assert _q(lib, axis=2, sc=40) == ERR_ALIGN
+
+    P = ctypes.c_void_p
+    g = lib.fp4q_gemm
+    g.argtypes = [P, P, P, P, P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, P,
+                  ctypes.c_int, P]
+    ok = P(16)
+    assert g(ok, ok, ok, ok, ok, ok, 128, 128, 96, 0, ok, 0, None) == ERR_SHAPE    # K % 64
+    assert g(ok, ok, ok, ok, ok, ok, 128, 128, 128, 5, ok, 0, None) == ERR_ARG
+    assert g(ok, ok, ok, ok, ok, ok, 128, 128, 128, 0, None, 0, None) == ERR_ARG
+    assert g(None, ok, ok, ok, ok, ok, 128, 128, 128, 0, ok, 0, None) == ERR_ARG
+    assert g(P(8), ok, ok, ok, ok, ok, 128, 128, 128, 0, ok, 0, None) == ERR_ALIGN
+    assert g(ok, ok, ok, ok, ok, ok, 0, 128, 128, 0, ok, 0, None) == 0             # empty: no-op
+
+    t = lib.fp4q_tensor_scale
+    t.argtypes = [P, ctypes.c_int, ctypes.c_float, P, P]
+    assert t(ok, 0, 3.0, ok, None) == ERR_ARG      # headroom not a power of two
+    assert t(ok, 0, 0.5, ok, None) == ERR_ARG
+    assert t(ok, 2, 1.0, ok, None) == ERR_ARG
+    a = lib.fp4q_amax
+    a.argtypes = [P, ctypes.c_int64, P, P]
+    assert a(ok, 16, None, None) == ERR_ARG
+    assert a(P(2), 16, ok, None) == ERR_ALIGN
+    s = lib.fp4q_get_device_status
+    s.argtypes = [P]
+    assert s(None) == ERR_ARG
+
+
+def test_product_path_has_no_fallback():
+    # the binding raises at import time when the library is missing; it never
+    # routes through the oracle or the CPU
+    src = open(os.path.join(ROOT, "fp4_block_scaled_bf16_gb300", "fp4q.py")).read()
+    assert "oracle" not in src.replace("# ", "")
+    for f in os.listdir(os.path.join(ROOT, "fp4_block_scaled_bf16_gb300")):
+        if f.endswith(".py"):
+            body = open(os.path.join(ROOT, "fp4_block_scaled_bf16_gb300", f)).read()
+            assert "import oracle" not in body and "from oracle" not in body, f

@@ -1,0 +1,167 @@
+"""GPU parity of the emulated UE5M3 block-scaled GEMM (tcgen05) against the
+oracle's binary64 contraction of identical dequantised operands.
+
+Tolerance (stated in parity_util): normwise max |C - R| / max |R| <= 1e-3 on
+the FP32-output mode; the BF16 output must lie within one BF16 ulp of R plus
+1e-3 max |R|.  The operands are the GPU's own quantised bytes, which the
+quantiser tests prove equal to the oracle's.
+
+Method: "UE5M3 FP4 Block Scaling for Stable Language Model Pretraining",
+Abstract (FP4 matrix multiplications of fprop, dgrad and wgrad on E2M1 +
+UE5M3 block-16 operands, UE5M3 emulated in software)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp4_block_scaled_bf16_gb300 import workloads
+from parity_util import GEMM_TOL, bf16_ulp, gemm_error, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    from fp4_block_scaled_bf16_gb300 import build
+    build.build()
+    from fp4_block_scaled_bf16_gb300 import fp4q
+    yield fp4q
+    assert fp4q.fp4q_get_device_status() == fp4q.OK
+
+
+def quantised(bits, lib, axis=0, rnd=0, seed=0, fmt=0):
+    x = to_dev(bits)
+    q = lib.quantize(x, axis, None, fmt, rnd, seed)
+    if axis == 1:
+        return q.payload_col, q.scales_col, q.T
+    return q.payload_row, q.scales_row, q.T
+
+
+def run_both(lib, A, B, fmt=0):
+    C32 = lib.gemm(*A, *B, fmt=fmt, dtype=torch.float32)
+    C16 = lib.gemm(*A, *B, fmt=fmt, dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    return C32.cpu().numpy(), C16.float().cpu().numpy()
+
+
+def full_reference(A, B, fmt=0):
+    pa, sa, ta = (t.cpu().numpy() if hasattr(t, "cpu") else t for t in A)
+    pb, sb, tb = (t.cpu().numpy() if hasattr(t, "cpu") else t for t in B)
+    ta, tb = float(ta[0]), float(tb[0])
+    return oracle.gemm(pa, sa, ta, pb, sb, tb, fmt)
+
+
+def assert_close(C32, C16, R):
+    err = gemm_error(C32, R)
+    assert err <= GEMM_TOL, err
+    bound = bf16_ulp(R) + GEMM_TOL * np.abs(R).max()
+    assert (np.abs(C16.astype(np.float64) - R) <= bound).all()
+    return err
+
+
+def rand_bits(shape, seed, spread=0.0):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal(shape).astype(np.float32)
+    if spread:
+        x *= (10.0 ** rng.uniform(-spread, spread, (1, shape[1]))).astype(np.float32)
+    return workloads.f32_to_bf16_bits(x)
+
+
+def test_tiny_config(lib):
+    a, b = workloads.tiny_operands(seed=0)
+    A, B = quantised(a, lib), quantised(b, lib)
+    C32, C16 = run_both(lib, A, B)
+    assert_close(C32, C16, full_reference(A, B))
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (128, 256, 128), (256, 512, 256), (100, 200, 64),
+                                   (16, 16, 64), (300, 700, 320), (129, 257, 192), (640, 384, 1024)])
+def test_shapes_and_ragged_tiles(M, N, K, lib):
+    a = rand_bits((M + (-M) % 16, K), M * 7 + K, spread=2.0)[:M]
+    b = rand_bits((N + (-N) % 16, K), N * 13 + K, spread=2.0)[:N]
+    a = np.ascontiguousarray(np.pad(a, ((0, (-M) % 16), (0, 0))))
+    b = np.ascontiguousarray(np.pad(b, ((0, (-N) % 16), (0, 0))))
+    A, B = quantised(a, lib), quantised(b, lib)
+    A = (A[0][:M].contiguous(), A[1][:M].contiguous(), A[2])
+    B = (B[0][:N].contiguous(), B[1][:N].contiguous(), B[2])
+    C32, C16 = run_both(lib, A, B)
+    assert C32.shape == (M, N)
+    assert_close(C32, C16, full_reference(A, B))
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_wide_dynamic_range_and_formats(lib, fmt):
+    # per-row magnitudes over 1e-8 .. 1e2 (the gradient distribution), SR on A
+    a = workloads.gradients(256, 512, 5)
+    b = rand_bits((384, 512), 6, spread=3.0)
+    A, B = quantised(a, lib, rnd=1, seed=7, fmt=fmt), quantised(b, lib, fmt=fmt)
+    C32, C16 = run_both(lib, A, B, fmt)
+    assert_close(C32, C16, full_reference(A, B, fmt))
+
+
+def test_zero_and_k0(lib):
+    z = np.zeros((128, 128), np.uint16)
+    A = quantised(z, lib)
+    C32, C16 = run_both(lib, A, A)
+    assert (C32 == 0).all() and (C16 == 0).all()
+    out = torch.full((16, 16), 7.0, device="cuda")
+    e = torch.empty((16, 0), dtype=torch.uint8, device="cuda")
+    one = torch.ones(1, device="cuda")
+    lib.fp4q_gemm(e, e, one, e, e, one, 16, 16, 0, 0, out)
+    torch.cuda.synchronize()
+    assert (out == 0).all()
+
+
+def _sampled_check(lib, A, B, Cdev32, rows, cols, fmt=0):
+    """Full row and column stripes of the reference via the oracle's exact
+    e*s operands and a binary64 matmul."""
+    pa, sa = A[0].cpu().numpy(), A[1].cpu().numpy()
+    pb, sb = B[0].cpu().numpy(), B[1].cpu().numpy()
+    alpha = float(A[2].item()) * float(B[2].item())
+    C = Cdev32
+    R_rows = alpha * (oracle.deq_es(pa[rows], sa[rows], fmt) @ oracle.deq_es(pb, sb, fmt).T)
+    R_cols = alpha * (oracle.deq_es(pa, sa, fmt) @ oracle.deq_es(pb[cols], sb[cols], fmt).T)
+    scale = max(np.abs(R_rows).max(), np.abs(R_cols).max())
+    e1 = np.abs(C[rows].cpu().numpy().astype(np.float64) - R_rows).max() / scale
+    e2 = np.abs(C[:, cols].cpu().numpy().astype(np.float64) - R_cols).max() / scale
+    return max(e1, e2)
+
+
+def _stripes(n, rng, tile):
+    s = list(range(0, min(tile, n))) + list(range(max(n - tile, 0), n))
+    s += list(rng.choice(n, 64, replace=False))
+    return np.unique(np.array(s))
+
+
+def test_full_fprop(lib):
+    """Y = X W^T at 8192 x 16384 x 4096 (8B-class fprop), sampled stripes."""
+    X, W = workloads.fprop_operands()
+    A, B = quantised(X, lib), quantised(W, lib)
+    C = lib.gemm(*A, *B, dtype=torch.float32)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(0)
+    err = _sampled_check(lib, A, B, C, _stripes(8192, rng, 128), _stripes(16384, rng, 256))
+    assert err <= GEMM_TOL, err
+
+
+def test_full_dgrad_wgrad(lib):
+    """dX = dY W (8192 x 4096 x 16384) and dW = dY^T X (16384 x 4096 x 8192)
+    with SR gradients (seed 7), sampled stripes."""
+    X, W = workloads.fprop_operands()
+    dY = workloads.backward_gradient()
+    d = to_dev(dY)
+    qd = lib.quantize(d, 2, None, 0, 1, 7)
+    Wc = quantised(W, lib, axis=1)
+    Xc = quantised(X, lib, axis=1)
+    rng = np.random.default_rng(1)
+    dX = lib.gemm(qd.payload_row, qd.scales_row, qd.T, *Wc, dtype=torch.float32)
+    torch.cuda.synchronize()
+    err = _sampled_check(lib, (qd.payload_row, qd.scales_row, qd.T), Wc, dX,
+                         _stripes(8192, rng, 128), _stripes(4096, rng, 256))
+    assert err <= GEMM_TOL, err
+    del dX
+    dW = lib.gemm(qd.payload_col, qd.scales_col, qd.T, *Xc, dtype=torch.float32)
+    torch.cuda.synchronize()
+    err = _sampled_check(lib, (qd.payload_col, qd.scales_col, qd.T), Xc, dW,
+                         _stripes(16384, rng, 128), _stripes(4096, rng, 256))
+    assert err <= GEMM_TOL, err
