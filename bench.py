@@ -1,0 +1,374 @@
+"""Benchmark of the UE5M3 FP4 hot path on one GB300.
+
+One step = one 8B-class internal linear (in 4096 -> out 16384, 8192 tokens)
+through the whole path of "UE5M3 FP4 Block Scaling for Stable Language Model
+Pretraining" (Abstract): amax + tensor scale of X, W, dY; dual-axis block-16
+E2M1/UE5M3 quantisation of X and W (RNE) and of dY (Philox SR, seed 7); the
+three training GEMMs on the block-scaled operands (fprop Y = X W^T, dgrad
+dX = dY W, wgrad dW = dY^T X), each 8192 x 16384 x 4096 multiply-adds.
+
+value = the three GEMMs' 2MNK flops / step time (quantisation included),
+TFLOP/s.  Per-kernel CUDA-event times give the quantiser GB/s and the GEMM
+TFLOP/s against the measured rooflines (MEASURED_PEAKS.json).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+--impl reference times the CPU oracle on a bounded sample of the same step.
+Multi-GPU: replicas only (every rank runs its own independent step).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+M_TOK, HID, FFN = 8192, 4096, 16384
+GEMM_FLOPS = 2.0 * M_TOK * FFN * HID          # each of fprop, dgrad, wgrad
+STEP_FLOPS = 3 * GEMM_FLOPS
+METRIC = "E2M1/UE5M3 quantize GB/s & block-scaled GEMM TFLOP/s, % of roofline"
+WORKLOAD = ("8B-class linear 4096->16384, 8192 tokens: amax+scale, dual-axis quantise X/W (RNE) "
+            "and dY (SR seed 7), fprop+dgrad+wgrad block-scaled GEMMs")
+# algorithmic bytes per element: read BF16 (2) + payload 0.5 + scale 1/16 per axis
+DUAL_BYTES_PER_ELEM = 2 + 2 * (0.5 + 1 / 16)
+AMAX_BYTES_PER_ELEM = 2
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def _peak(d, *keys):
+    for k in keys:
+        v = d.get(k)
+        if isinstance(v, (int, float)):
+            return float(v)
+        if isinstance(v, dict):
+            for kk in ("value", "median", "peak"):
+                if isinstance(v.get(kk), (int, float)):
+                    return float(v[kk])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.index, self.rows, self.proc = index, [], None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([c.strip() for c in line.split(",")])
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(2)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            try:
+                sm.append(float(r[0]))
+                mx = float(r[1])
+                for n, v in zip(names, r[3:7]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                pass
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- GPU path
+class Step:
+    """Device buffers and the launch sequence of one step."""
+
+    def __init__(self, torch, fp4q, X, W, dY):
+        self.t, self.q = torch, fp4q
+        dev = X.device
+        u8 = dict(dtype=torch.uint8, device=dev)
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.X, self.W, self.dY = X, W, dY
+        self.amax = torch.zeros(3, **f32)
+        self.T = torch.zeros(3, **f32)
+        self.Xr, self.Xrs = torch.empty((M_TOK, HID // 2), **u8), torch.empty((M_TOK, HID // 16), **u8)
+        self.Xc, self.Xcs = torch.empty((HID, M_TOK // 2), **u8), torch.empty((HID, M_TOK // 16), **u8)
+        self.Wr, self.Wrs = torch.empty((FFN, HID // 2), **u8), torch.empty((FFN, HID // 16), **u8)
+        self.Wc, self.Wcs = torch.empty((HID, FFN // 2), **u8), torch.empty((HID, FFN // 16), **u8)
+        self.Dr, self.Drs = torch.empty((M_TOK, FFN // 2), **u8), torch.empty((M_TOK, FFN // 16), **u8)
+        self.Dc, self.Dcs = torch.empty((FFN, M_TOK // 2), **u8), torch.empty((FFN, M_TOK // 16), **u8)
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        self.Y = torch.empty((M_TOK, FFN), **bf)
+        self.dX = torch.empty((M_TOK, HID), **bf)
+        self.dW = torch.empty((FFN, HID), **bf)
+        self.launches = 0
+
+    def run(self, ev=None):
+        q = self.q
+        T = [self.T[i:i + 1] for i in range(3)]
+        A = [self.amax[i:i + 1] for i in range(3)]
+        rec = (lambda k: ev[k].record()) if ev else (lambda k: None)
+        rec(0)
+        for i, x in enumerate((self.X, self.W, self.dY)):
+            q.fp4q_amax(x, A[i])
+            q.fp4q_tensor_scale(A[i], q.UE5M3, 1.0, T[i])
+        rec(1)
+        q.fp4q_quantize(self.X, q.AXIS_BOTH, q.UE5M3, T[0], q.RNE, 0, self.Xr, self.Xrs, self.Xc, self.Xcs)
+        rec(2)
+        q.fp4q_quantize(self.W, q.AXIS_BOTH, q.UE5M3, T[1], q.RNE, 0, self.Wr, self.Wrs, self.Wc, self.Wcs)
+        rec(3)
+        q.fp4q_quantize(self.dY, q.AXIS_BOTH, q.UE5M3, T[2], q.SR, 7, self.Dr, self.Drs, self.Dc, self.Dcs)
+        rec(4)
+        q.fp4q_gemm(self.Xr, self.Xrs, T[0], self.Wr, self.Wrs, T[1], M_TOK, FFN, HID, q.UE5M3, self.Y)
+        rec(5)
+        q.fp4q_gemm(self.Dr, self.Drs, T[2], self.Wc, self.Wcs, T[1], M_TOK, HID, FFN, q.UE5M3, self.dX)
+        rec(6)
+        q.fp4q_gemm(self.Dc, self.Dcs, T[2], self.Xc, self.Xcs, T[0], FFN, HID, M_TOK, q.UE5M3, self.dW)
+        rec(7)
+        self.launches += 12
+        return self
+
+
+def run_gpu(args, rank, world):
+    import torch
+    from fp4_block_scaled_bf16_gb300 import build, fp4q, workloads
+
+    build.build()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    if M_TOK == workloads.TOKENS:
+        Xb, Wb = workloads.fprop_operands()
+        dYb = workloads.backward_gradient()
+    else:
+        Xb, Wb = workloads.activations(M_TOK, HID, 1), workloads.weights(FFN, HID, 2)
+        dYb = workloads.gradients(M_TOK, FFN, 3)
+    hX = workloads.to_torch_bf16(Xb).pin_memory()
+    hW = workloads.to_torch_bf16(Wb).pin_memory()
+    hD = workloads.to_torch_bf16(dYb).pin_memory()
+    X, W, dY = hX.to(dev), hW.to(dev), hD.to(dev)
+    step = Step(torch, fp4q, X, W, dY)
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+
+    # ---- device-resident timed region, per-kernel events on the launch stream
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
+    step.launches = 0
+    with ClockSampler(dev.index) as clk:
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for k in range(args.steps):
+            step.run(evs[k])
+        t1.record()
+        torch.cuda.synchronize()
+    launches = step.launches
+    ms = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    seg = lambda a, b: sum(e[a].elapsed_time(e[b]) for e in evs) / args.steps
+    t_scale, t_qx, t_qw, t_qd = seg(0, 1), seg(1, 2), seg(2, 3), seg(3, 4)
+    t_g = [seg(4, 5), seg(5, 6), seg(6, 7)]
+    status = fp4q.fp4q_get_device_status()
+
+    # ---- end to end through the API with host buffers: H2D inputs, D2H results
+    hY = torch.empty(step.Y.shape, dtype=torch.bfloat16).pin_memory()
+    hdX = torch.empty(step.dX.shape, dtype=torch.bfloat16).pin_memory()
+    hdW = torch.empty(step.dW.shape, dtype=torch.bfloat16).pin_memory()
+    e2e_steps = max(1, min(args.steps, 5))
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+    s0.record()
+    for _ in range(e2e_steps):
+        step.X.copy_(hX, non_blocking=True)
+        step.W.copy_(hW, non_blocking=True)
+        step.dY.copy_(hD, non_blocking=True)
+        step.run()
+        hY.copy_(step.Y, non_blocking=True)
+        hdX.copy_(step.dX, non_blocking=True)
+        hdW.copy_(step.dW, non_blocking=True)
+    s1.record()
+    torch.cuda.synchronize()
+    e2e_ms = s0.elapsed_time(s1) / e2e_steps
+    h2d = (hX.numel() + hW.numel() + hD.numel()) * 2
+    d2h = (hY.numel() + hdX.numel() + hdW.numel()) * 2
+    return dict(ms=ms, t_scale=t_scale, t_q=(t_qx, t_qw, t_qd), t_g=t_g, launches=launches,
+                clocks=clk.summary(), status=status, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
+                elems=(X.numel(), W.numel(), dY.numel()))
+
+
+# ---------------------------------------------------------------- oracle path
+def oracle_sample(qrows=512, grows=2, gcols=4096):
+    """Times the CPU oracle on a bounded slice of the step and scales it to
+    the whole step: quantisation per element (row + column, RNE and SR, on
+    qrows rows of X and of dY) and the binary64 GEMM per multiply-add
+    (grows x gcols outputs of fprop).  Returns (seconds for the whole step,
+    seconds actually spent, description)."""
+    import oracle
+    from fp4_block_scaled_bf16_gb300 import workloads
+
+    oracle.build()
+    x = workloads.activations(qrows, HID, 1)
+    d = workloads.gradients(qrows, FFN, 3)
+    w = workloads.weights(gcols, HID, 2)
+    t0 = time.perf_counter()
+    Tx = oracle.tensor_scale(oracle.amax(x)[0])
+    Td = oracle.tensor_scale(oracle.amax(d)[0])
+    oracle.quantize(x, oracle.ROW, Tx)
+    oracle.quantize(x, oracle.COL, Tx)
+    oracle.quantize(d, oracle.ROW, Td, rnd=oracle.SR, seed=7)
+    oracle.quantize(d, oracle.COL, Td, rnd=oracle.SR, seed=7)
+    t_q = time.perf_counter() - t0
+    q_elems = x.size + d.size
+    Tw = oracle.tensor_scale(oracle.amax(w)[0])
+    pa, sa, _ = oracle.quantize(x[:16], oracle.ROW, Tx)
+    pb, sb, _ = oracle.quantize(w, oracle.ROW, Tw)
+    t0 = time.perf_counter()
+    oracle.gemm(pa[:grows], sa[:grows], Tx, pb, sb, Tw)
+    t_g = time.perf_counter() - t0
+    macs = grows * gcols * HID
+    step_elems = M_TOK * HID + FFN * HID + M_TOK * FFN
+    est = t_q / q_elems * step_elems + t_g / macs * (STEP_FLOPS / 2)
+    sample = (f"quantise {q_elems} elements (row+col, RNE and SR) in {t_q:.2f} s and binary64 GEMM "
+              f"{macs} MACs in {t_g:.2f} s, single thread; scaled to the full step "
+              f"({step_elems} elements quantised on two axes, {STEP_FLOPS / 2:.3e} MACs)")
+    return est, t_q + t_g, sample
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="fp4q", choices=["fp4q", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=8192,
+                    help="rows of X and dY; smaller values only for profiling captures")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    global M_TOK, GEMM_FLOPS, STEP_FLOPS
+    if args.tokens != M_TOK:
+        M_TOK = args.tokens
+        GEMM_FLOPS = 2.0 * M_TOK * FFN * HID
+        STEP_FLOPS = 3 * GEMM_FLOPS
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        # each step is a bounded sample of the workload (about 2 s of CPU work)
+        for _ in range(args.warmup):
+            oracle_sample(qrows=64, grows=1, gcols=256)
+        est_total, spent, sample = 0.0, 0.0, None
+        for _ in range(args.steps):
+            est, dt, sample = oracle_sample(qrows=256, grows=1, gcols=4096)
+            est_total += est
+            spent += dt
+        est = est_total / args.steps
+        v = STEP_FLOPS / est / 1e12
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": est * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32/f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "l2": "inputs larger than L2"},
+            "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                             "sample": f"per step: {sample}; {spent:.1f} s of CPU time over {args.steps} steps"},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    r = run_gpu(args, rank, world)
+    if rank != 0:
+        return
+    pk, src = peaks()
+    hbm = _peak(pk, "hbm_gbs", "hbm_GBps", "hbm")
+    bf16 = _peak(pk, "bf16_tflops_sustained", "bf16_tflops")
+    ms = r["ms"] / args.steps
+    value = world * STEP_FLOPS / (ms * 1e-3) / 1e12
+    t_gemm = sum(r["t_g"]) / 3
+    gemm_tflops = GEMM_FLOPS / (t_gemm * 1e-3) / 1e12
+    nX, nW, nD = r["elems"]
+    q_bytes = [n * DUAL_BYTES_PER_ELEM for n in (nX, nW, nD)]
+    q_gbs = [b / (t * 1e-3) / 1e9 for b, t in zip(q_bytes, r["t_q"])]
+    cpu = None
+    if not args.no_cpu_baseline:
+        est, spent, sample = oracle_sample(qrows=1024, grows=6, gcols=4096)
+        cpu = {"value": STEP_FLOPS / est / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+               "sample": f"{sample}; {spent:.1f} s of CPU time"}
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16xbf16->f32 (E2M1/UE5M3 operands)", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": M_TOK, "hidden": HID, "ffn": FFN,
+                   "l2": "inputs larger than L2 (dY 256 MiB, step working set ~1 GiB)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": bf16,
+                     "unit": "TFLOP/s", "frac": gemm_tflops / bf16 if bf16 else None, "traffic": None,
+                     "kernel": "fp4q gemm_kernel (mean of fprop/dgrad/wgrad)",
+                     "peak_source": f"{src} bf16 (sustained)"},
+        "roofline_quantize": {"bound": "hbm", "unit": "GB/s", "peak": hbm,
+                              "achieved": {"X_dual_rne": q_gbs[0], "W_dual_rne": q_gbs[1], "dY_dual_sr": q_gbs[2]},
+                              "frac": {k: g / hbm for k, g in zip(("X_dual_rne", "W_dual_rne", "dY_dual_sr"), q_gbs)} if hbm else None,
+                              "peak_source": f"{src} hbm"},
+        "breakdown_ms": {"amax_scale": r["t_scale"], "quantize_X": r["t_q"][0], "quantize_W": r["t_q"][1],
+                         "quantize_dY": r["t_q"][2], "fprop": r["t_g"][0], "dgrad": r["t_g"][1],
+                         "wgrad": r["t_g"][2]},
+        "e2e": {"value": world * STEP_FLOPS / (r["e2e_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e_ms"]},
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+        "device_status": r["status"],
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()
