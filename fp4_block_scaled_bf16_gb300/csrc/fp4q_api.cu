@@ -23,6 +23,10 @@ int* status_ptr() {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// scalars (amax, tensor scales) need their natural 4-byte alignment, the
+// stats counters 8 bytes
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+bool aligned8(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 7u) == 0; }
 
 fp4q_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA; }
 
@@ -39,7 +43,7 @@ const char* fp4q_status_string(fp4q_status s) {
     case FP4Q_OK: return "ok";
     case FP4Q_ERR_ARG: return "invalid argument (null pointer or unknown enum)";
     case FP4Q_ERR_SHAPE: return "unsupported shape";
-    case FP4Q_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case FP4Q_ERR_ALIGN: return "misaligned pointer";
     case FP4Q_ERR_CUDA: return "CUDA error";
     case FP4Q_ERR_NONFINITE: return "non-finite input element";
     case FP4Q_ERR_TIMEOUT: return "device pipeline wait timed out";
@@ -49,7 +53,7 @@ const char* fp4q_status_string(fp4q_status s) {
 
 fp4q_status fp4q_amax(const void* in_bf16, int64_t n, float* out_amax, void* stream) {
   if (!out_amax || n < 0 || (n > 0 && !in_bf16)) return FP4Q_ERR_ARG;
-  if ((n > 0 && !aligned16(in_bf16)) || !aligned16(out_amax)) return FP4Q_ERR_ALIGN;
+  if ((n > 0 && !aligned16(in_bf16)) || !aligned4(out_amax)) return FP4Q_ERR_ALIGN;
   int* st = status_ptr();
   if (!st) return FP4Q_ERR_CUDA;
   return from_cuda(fp4q::launch_amax(in_bf16, n, out_amax, st, static_cast<cudaStream_t>(stream)));
@@ -61,7 +65,7 @@ fp4q_status fp4q_tensor_scale(const float* amax, fp4q_scale_fmt fmt, float headr
   // headroom must be a power of two >= 1 so that 6 * Smax / H is exact
   int e = 0;
   if (!(headroom >= 1.0f) || frexpf(headroom, &e) != 0.5f) return FP4Q_ERR_ARG;
-  if (!aligned16(amax) || !aligned16(out_scale)) return FP4Q_ERR_ALIGN;
+  if (!aligned4(amax) || !aligned4(out_scale)) return FP4Q_ERR_ALIGN;
   const float denom = (6.0f * scale_max_host(fmt)) / headroom;
   return from_cuda(fp4q::launch_tensor_scale(amax, denom, out_scale, static_cast<cudaStream_t>(stream)));
 }
@@ -84,8 +88,8 @@ fp4q_status fp4q_quantize(const void* in_bf16, int64_t rows, int64_t cols, fp4q_
     if (row && (!aligned16(out_payload_row) || !aligned16(out_scales_row))) return FP4Q_ERR_ALIGN;
     if (col && (!aligned16(out_payload_col) || !aligned16(out_scales_col))) return FP4Q_ERR_ALIGN;
   }
-  if (!aligned16(tensor_scale) || (out_stats && !aligned16(out_stats)) ||
-      (out_amax && !aligned16(out_amax)))
+  if (!aligned4(tensor_scale) || (out_stats && !aligned8(out_stats)) ||
+      (out_amax && !aligned4(out_amax)))
     return FP4Q_ERR_ALIGN;
   int* st = status_ptr();
   if (!st) return FP4Q_ERR_CUDA;
@@ -117,7 +121,7 @@ fp4q_status fp4q_dequantize(const uint8_t* payload, const uint8_t* scales, int64
     if (!payload || !scales || !out) return FP4Q_ERR_ARG;
     if (!aligned16(payload) || !aligned16(scales) || !aligned16(out)) return FP4Q_ERR_ALIGN;
   }
-  if (!aligned16(tensor_scale)) return FP4Q_ERR_ALIGN;
+  if (!aligned4(tensor_scale)) return FP4Q_ERR_ALIGN;
   return from_cuda(fp4q::launch_dequantize(payload, scales, rows, cols, (int)fmt, tensor_scale, out,
                                            out_is_f32 != 0, static_cast<cudaStream_t>(stream)));
 }
@@ -136,7 +140,7 @@ fp4q_status fp4q_gemm(const uint8_t* A, const uint8_t* A_scales, const float* A_
     return from_cuda(cudaMemsetAsync(out, 0, (size_t)M * N * (out_is_f32 ? 4 : 2), st));
   if (!A || !A_scales || !A_tscale || !B || !B_scales || !B_tscale) return FP4Q_ERR_ARG;
   if (!aligned16(A) || !aligned16(B) || !aligned16(A_scales) || !aligned16(B_scales) ||
-      !aligned16(A_tscale) || !aligned16(B_tscale))
+      !aligned4(A_tscale) || !aligned4(B_tscale))
     return FP4Q_ERR_ALIGN;
   int* status = status_ptr();
   if (!status) return FP4Q_ERR_CUDA;

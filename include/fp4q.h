@@ -18,8 +18,9 @@
  *    (a cudaStream_t; NULL = the legacy default stream).
  *  - Data-dependent scalars (amax, tensor scale) stay on the device, so that a
  *    whole quantise -> GEMM sequence needs no host round trip.
- *  - Tensors are row-major and densely packed.  Every pointer must be 16-byte
- *    aligned.  BF16 is the IEEE bfloat16 bit pattern (uint16).
+ *  - Tensors are row-major and densely packed.  Every tensor pointer must be
+ *    16-byte aligned; scalar pointers (amax, tensor scales) 4-byte aligned,
+ *    stats 8-byte aligned.  BF16 is the IEEE bfloat16 bit pattern (uint16).
  *  - Validation errors (bad enum, shape, null or misaligned pointer) are
  *    returned synchronously before any launch and nothing is written.
  *    Launch failures return FP4Q_ERR_CUDA.  Conditions only the GPU can see
@@ -57,7 +58,7 @@ typedef enum {
     FP4Q_OK = 0,
     FP4Q_ERR_ARG = 1,        /* null pointer or unknown enum value */
     FP4Q_ERR_SHAPE = 2,      /* a size is not a supported multiple */
-    FP4Q_ERR_ALIGN = 3,      /* a pointer is not 16-byte aligned */
+    FP4Q_ERR_ALIGN = 3,      /* a pointer is misaligned (see conventions) */
     FP4Q_ERR_CUDA = 4,       /* a CUDA runtime/driver call failed */
     FP4Q_ERR_NONFINITE = 5,  /* device status: an input element was inf/NaN */
     FP4Q_ERR_TIMEOUT = 6     /* device status: a bounded pipeline wait gave up */

@@ -104,6 +104,7 @@ def test_host_validation_rejects_before_launch(lib):
     a.argtypes = [P, ctypes.c_int64, P, P]
     assert a(ok, 16, None, None) == ERR_ARG
     assert a(P(2), 16, ok, None) == ERR_ALIGN
+    assert a(ok, 16, P(18), None) == ERR_ALIGN          # scalars: 4-byte alignment
     s = lib.fp4q_get_device_status
     s.argtypes = [P]
     assert s(None) == ERR_ARG
