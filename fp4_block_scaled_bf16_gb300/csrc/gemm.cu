@@ -13,17 +13,19 @@
 // BF16 x BF16 -> FP32 tcgen05 MMA (kind::f16) over operands expanded in shared
 // memory, and differs from an exact sum only by FP32 accumulation rounding.
 //
-// CTA organisation (one CTA per SM, 128 x 256 output tile, K step 64):
-//   warp 8      TMA producer: FP4 payload tiles (A 128 x 32 B, B 256 x 32 B)
+// CTA organisation (one CTA per SM, 256 x 256 output tile, K step 64; the
+// expansion is the costly part, so the tile is as large as TMEM allows: two
+// 128 x 256 FP32 accumulators fill all 512 columns):
+//   warp 16     TMA producer: FP4 payload tiles (A and B, 256 x 32 B each)
 //               into a 4-stage raw ring.
-//   warps 0..7  expand raw stages into a 3-stage BF16 ring laid out in the
+//   warps 0..15 expand raw stages into a 2-stage BF16 ring laid out in the
 //               128-byte-swizzled K-major form the MMA descriptors read; each
 //               thread expands one 16-element block (one scale) at a time
 //               through an 8-entry per-block value table and byte permutes;
 //               after the main loop they run the epilogue (TMEM -> registers
 //               -> alpha -> BF16/FP32 -> global).
-//   warp 9      allocates TMEM; one lane issues 4 MMAs (M128 N256 K16) per
-//               stage and commits them to the stage's "empty" barrier.
+//   warp 17     allocates TMEM; one lane issues 8 MMAs (2 x M128 N256 K16)
+//               per stage and commits them to the stage's "empty" barrier.
 // Every wait is bounded: a wait that runs out latches FP4Q_ERR_TIMEOUT in the
 // device status word and the CTA drains and exits instead of hanging.
 #include <cuda.h>
@@ -35,17 +37,21 @@
 namespace fp4q {
 namespace gemm {
 
-constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int S_RAW = 4, S_BF = 3;
-constexpr int RAW_A = BM * BK / 2;             // 4096 B
+constexpr int BM = 256, BN = 256, BK = 64;     // CTA tile; two M=128 MMAs per K16 step
+constexpr int UM = 128;                         // rows per MMA instruction
+constexpr int S_RAW = 4, S_BF = 2;
+constexpr int RAW_A = BM * BK / 2;             // 8192 B
 constexpr int RAW_B = BN * BK / 2;             // 8192 B
 constexpr int RAW_STAGE = RAW_A + RAW_B;
-constexpr int BF_A = BM * BK * 2;              // 16384 B
+constexpr int BF_A = BM * BK * 2;              // 32768 B
 constexpr int BF_B = BN * BK * 2;              // 32768 B
 constexpr int BF_STAGE = BF_A + BF_B;
-constexpr int kDeqThreads = 256;
+constexpr int kDeqWarps = 16;
+constexpr int kDeqThreads = 32 * kDeqWarps;
+constexpr int kProducerWarp = kDeqWarps, kMmaWarp = kDeqWarps + 1;
 constexpr int kThreads = kDeqThreads + 64;
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemCols = 512;             // two 128 x 256 FP32 accumulators
+constexpr int kRowsPerThread = (BM + BN) / (kDeqThreads / 4);   // 4
 
 constexpr int OFF_BF = 0;
 constexpr int OFF_RAW = OFF_BF + S_BF * BF_STAGE;
@@ -163,7 +169,7 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 // Instruction descriptor for kind::f16: FP32 accumulator, BF16 A and B, both
 // K-major, M = 128, N = 256.
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                            ((uint32_t)(BM >> 4) << 24);
+                            ((uint32_t)(UM >> 4) << 24);
 
 // ---------------------------------------------------------------- expansion
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -184,7 +190,10 @@ struct Lut {
   uint32_t L0, L1, H0, H1;
 };
 __device__ __forceinline__ Lut make_lut(uint32_t code, int fmt) {
-  const float s = decode_scale(code, fmt);
+  // The code shifted into a binary32 exponent/mantissa field is the scale
+  // times 2^-(127 - bias), subnormal codes included (gradual underflow lines
+  // up), so one exact multiply by a power of two decodes it.
+  const float s = __fmul_rn(__uint_as_float(code << 20), fmt == kUE5M3 ? 0x1p112f : 0x1p120f);
   uint32_t ss;
   asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(ss) : "f"(s));   // exact: <= 4 significant bits
   const uint32_t p01 = bmul2(ss, 0x3F000000u);   // (0, 0.5) * s
@@ -252,23 +261,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < S_RAW; ++i) {
       mbar_init(bar_raw_full + 8 * i, 1);
-      mbar_init(bar_raw_empty + 8 * i, kDeqThreads / 32);
+      mbar_init(bar_raw_empty + 8 * i, kDeqWarps);
     }
     for (int i = 0; i < S_BF; ++i) {
-      mbar_init(bar_bf_full + 8 * i, kDeqThreads / 32);
+      mbar_init(bar_bf_full + 8 * i, kDeqWarps);
       mbar_init(bar_bf_empty + 8 * i, 1);
     }
     mbar_init(bar_acc, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 9) tmem_alloc(sb + OFF_TMEM, kTmemCols);
+  if (warp == kMmaWarp) tmem_alloc(sb + OFF_TMEM, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + OFF_TMEM);
 
-  if (warp == 8) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
       for (int kb = 0; kb < nk; ++kb) {
@@ -283,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(dst + RAW_A, &mapB, kb * (BK / 2), n0, bar_raw_full + 8 * s);
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
       for (int kb = 0; kb < nk; ++kb) {
@@ -294,34 +303,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t a_addr = sb + OFF_BF + t * BF_STAGE;
-        const uint64_t adesc = sw128_desc(a_addr), bdesc = sw128_desc(a_addr + BF_A);
+        const uint64_t a0 = sw128_desc(a_addr), a1 = sw128_desc(a_addr + UM * 128);
+        const uint64_t bd = sw128_desc(a_addr + BF_A);
 #pragma unroll
-        for (int k = 0; k < BK / 16; ++k)
-          mma_bf16(tmem, adesc + 2 * k, bdesc + 2 * k, kIdesc, (kb | k) != 0 ? 1u : 0u);
+        for (int k = 0; k < BK / 16; ++k) {
+          const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
+          mma_bf16(tmem, a0 + 2 * k, bd + 2 * k, kIdesc, acc);          // rows 0..127
+          mma_bf16(tmem + BN, a1 + 2 * k, bd + 2 * k, kIdesc, acc);     // rows 128..255
+        }
         mma_commit(bar_bf_empty + 8 * t);
       }
       mma_commit(bar_acc);
     }
   } else {
     // ------------------------------------------------ expansion warps
-    const int tid = threadIdx.x;            // 0..255
-    const int blk = tid & 3;                 // block of 16 inside the 64-wide K step
-    const int rbase = tid >> 2;              // rows rbase + 64 i, i = 0..5 (A: 0..127, B: 128..383)
-    const int64_t lda_s = K / 16;
-    auto load_codes = [&](int kb, uint32_t (&c)[6]) {
+    // Thread t expands block (t % 4) of the 64-wide K step for rows
+    // t/4 + 128 i, i = 0..3 (A rows 0..255, then B rows 0..255).
+    const int tid = threadIdx.x;
+    const int blk = tid & 3;
+    const int rbase = tid >> 2;
+    const int64_t lds_k = K / 16;
+    const uint8_t* srow[kRowsPerThread];
+    bool rok[kRowsPerThread];
 #pragma unroll
-      for (int i = 0; i < 6; ++i) {
-        const int r = rbase + 64 * i;
-        if (i < 2) {
-          const int gr = m0 + r;
-          c[i] = (gr < M) ? __ldg(As + (int64_t)gr * lda_s + kb * 4 + blk) : 0u;
-        } else {
-          const int gr = n0 + (r - BM);
-          c[i] = (gr < N) ? __ldg(Bs + (int64_t)gr * lda_s + kb * 4 + blk) : 0u;
-        }
-      }
+    for (int i = 0; i < kRowsPerThread; ++i) {
+      const int r = rbase + 128 * i;
+      const int gr = (r < BM) ? m0 + r : n0 + (r - BM);
+      rok[i] = (r < BM) ? (gr < M) : (gr < N);
+      srow[i] = ((r < BM) ? As : Bs) + (int64_t)(rok[i] ? gr : 0) * lds_k + blk;
+    }
+    auto load_codes = [&](int kb, uint32_t (&c)[kRowsPerThread]) {
+#pragma unroll
+      for (int i = 0; i < kRowsPerThread; ++i) c[i] = rok[i] ? __ldg(srow[i] + kb * 4) : 0u;
     };
-    uint32_t codes[6], next[6];
+    uint32_t codes[kRowsPerThread], next[kRowsPerThread];
     load_codes(0, codes);
     for (int kb = 0; kb < nk; ++kb) {
       const int s = kb % S_RAW, t = kb % S_BF;
@@ -331,19 +346,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         fail(abort_flag, status);
         break;
       }
-      const uint32_t raw = sb + OFF_RAW + s * RAW_STAGE;
-      const uint32_t bf = sb + OFF_BF + t * BF_STAGE;
+      const uint32_t raw = sb + OFF_RAW + s * RAW_STAGE + rbase * (BK / 2) + blk * 8;
+      const uint32_t bf = sb + OFF_BF + t * BF_STAGE + rbase * 128;
+      const uint32_t sw = rbase & 7;               // (rbase + 128 i) & 7
+      const uint32_t c_lo = ((2 * blk) ^ sw) << 4, c_hi = ((2 * blk + 1) ^ sw) << 4;
 #pragma unroll
-      for (int i = 0; i < 6; ++i) {
-        const int r = rbase + 64 * i;        // 0..383; A rows then B rows
-        const uint2 w = lds64(raw + r * (BK / 2) + blk * 8);
+      for (int i = 0; i < kRowsPerThread; ++i) {
+        const uint2 w = lds64(raw + i * 128 * (BK / 2));
         const Lut lut = make_lut(codes[i], fmt);
-        const uint4 lo = expand8(w.x, lut);  // K 16*blk + 0..7
-        const uint4 hi = expand8(w.y, lut);  // K 16*blk + 8..15
-        const uint32_t row_addr = bf + r * 128;   // B rows follow A rows: BF_A = 128 * 128
-        const uint32_t sw = r & 7;
-        sts128(row_addr + (((2 * blk) ^ sw) << 4), lo);
-        sts128(row_addr + (((2 * blk + 1) ^ sw) << 4), hi);
+        const uint4 lo = expand8(w.x, lut);        // K 16*blk + 0..7
+        const uint4 hi = expand8(w.y, lut);        // K 16*blk + 8..15
+        const uint32_t row_addr = bf + i * 128 * 128;
+        sts128(row_addr + c_lo, lo);
+        sts128(row_addr + c_hi, hi);
       }
       fence_proxy_async();
       __syncwarp();
@@ -352,21 +367,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(bar_raw_empty + 8 * s);
       }
 #pragma unroll
-      for (int i = 0; i < 6; ++i) codes[i] = next[i];
+      for (int i = 0; i < kRowsPerThread; ++i) codes[i] = next[i];
     }
 
     // ------------------------------------------------ epilogue
+    // warp w drains TMEM lanes 32 (w % 4) .. +31 of accumulator (w / 4) % 2,
+    // columns 128 (w / 8) .. +127.
     if (mbar_wait(bar_acc, 0, abort_flag)) {
       tc_fence_after();
-      const int q = warp & 3, half = warp >> 2;
+      const int q = warp & 3, acc = (warp >> 2) & 1, half = warp >> 3;
       const float alpha = __fmul_rn(__ldg(TA), __ldg(TB));
-      const int row = m0 + 32 * q + lane;
+      const int row = m0 + UM * acc + 32 * q + lane;
       const bool vec = F32OUT ? (N % 4 == 0) : (N % 8 == 0);
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         const int col0 = n0 + 128 * half + 32 * c;
         uint32_t r[32];
-        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(128 * half + 32 * c), r);
+        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(BN * acc + 128 * half + 32 * c), r);
         if (row >= M || col0 >= N) continue;
         float v[32];
 #pragma unroll
@@ -403,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }

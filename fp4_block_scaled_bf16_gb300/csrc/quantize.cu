@@ -161,11 +161,12 @@ __global__ void __launch_bounds__(256) quantize_row_kernel(
 // t/16 + 16i, column group t%16); phase 2 (row-wise, optional) quantises from
 // registers exactly like the flat kernel; phase 3 stores the tile in shared
 // memory; phase 4 lets thread t quantise columns 4(t%32)..+3 over rows
-// 16(t/32)..+15 -- four column blocks, one Philox block per row.
+// 16(t/32)..+15 -- four column blocks, one Philox block per row, drawn row by
+// row so that no more than two blocks of random words are live at a time.
 constexpr int kTile = 128;
 
 template <bool SR, bool STATS, bool DO_ROW>
-__global__ void __launch_bounds__(256) quantize_tile_kernel(
+__global__ void __launch_bounds__(256, 2) quantize_tile_kernel(
     const uint16_t* __restrict__ in, int64_t R, int64_t C, int fmt,
     const float* __restrict__ tscale, uint64_t seed, uint32_t* __restrict__ pay_row,
     uint8_t* __restrict__ sc_row, uint8_t* __restrict__ pay_col, uint8_t* __restrict__ sc_col,
@@ -235,9 +236,7 @@ __global__ void __launch_bounds__(256) quantize_tile_kernel(
   const int q4 = lane * 4;         // first of four columns
   const int rb16 = (t >> 5) * 16;  // first of 16 rows
   const bool ok = q4 < cols && rb16 < rows;
-  uint32_t cw[4][8];  // [column j][row pair] packed as BF16 pairs (rows 2p, 2p+1)
-  uint32_t cm[4] = {0, 0, 0, 0};
-  uint32_t rnd[16][4];
+  uint32_t cw[4][8];  // [column j][row pair p] = BF16 of rows 2p (low), 2p+1 (high)
 #pragma unroll
   for (int p = 0; p < 8; ++p) {
     const uint2 a = *reinterpret_cast<const uint2*>(&tile[rb16 + 2 * p][q4]);
@@ -248,44 +247,45 @@ __global__ void __launch_bounds__(256) quantize_tile_kernel(
     cw[2][p] = __byte_perm(a.y, b.y, 0x5410);
     cw[3][p] = __byte_perm(a.y, b.y, 0x7632);
   }
-  if (SR) {
-#pragma unroll
-    for (int rr = 0; rr < 16; ++rr) {
-      const int64_t e = (r0 + rb16 + rr) * C + c0 + q4;  // multiple of 4
-      const uint4 w = sr_words4((uint64_t)e >> 2, 1u, seed);
-      rnd[rr][0] = w.x; rnd[rr][1] = w.y; rnd[rr][2] = w.z; rnd[rr][3] = w.w;
-    }
-  }
+  float rj[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint32_t w4[4] = {cw[j][4 * h], cw[j][4 * h + 1], cw[j][4 * h + 2], cw[j][4 * h + 3]};
-      cm[j] = max(cm[j], absmax16(w4));
-    }
-    const BlockScale bs = block_scale(cm[j], six_t, T, fmt);
-    uint32_t nib[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint32_t w4[4] = {cw[j][4 * h], cw[j][4 * h + 1], cw[j][4 * h + 2], cw[j][4 * h + 3]};
-      uint32_t rb[8];
-      if (SR) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) rb[k] = rnd[8 * h + k][j];
-      }
-      uint32_t c = 0, f = 0;
-      nib[h] = quantize8<SR, STATS>(w4, bs.r, rb, &c, &f);
-      if (STATS && ok) { n_clamp += c; n_flush += f; }
-    }
+    const uint32_t w4a[4] = {cw[j][0], cw[j][1], cw[j][2], cw[j][3]};
+    const uint32_t w4b[4] = {cw[j][4], cw[j][5], cw[j][6], cw[j][7]};
+    const uint32_t cm = max(absmax16(w4a), absmax16(w4b));
+    const BlockScale bs = block_scale(cm, six_t, T, fmt);
+    rj[j] = bs.r;
     if (STATS && ok) {
       n_sat += bs.sat ? 1u : 0u;
-      n_uflow += (cm[j] != 0u && bs.code == 0u) ? 1u : 0u;
+      n_uflow += (cm != 0u && bs.code == 0u) ? 1u : 0u;
     }
-    if (ok) {
-      const int64_t col = c0 + q4 + j;
-      *reinterpret_cast<uint2*>(pay_col + col * (R / 2) + (r0 + rb16) / 2) = make_uint2(nib[0], nib[1]);
-      sc_col[col * (R / 16) + (r0 + rb16) / 16] = (uint8_t)bs.code;
+    if (ok) sc_col[(c0 + q4 + j) * (R / 16) + (r0 + rb16) / 16] = (uint8_t)bs.code;
+  }
+  // rows in pairs: one Philox block per row gives the words of its four
+  // columns (counter = logical index / 4, word = column offset)
+  uint32_t nib[4][2] = {{0u, 0u}, {0u, 0u}, {0u, 0u}, {0u, 0u}};
+#pragma unroll
+  for (int p = 0; p < 8; ++p) {
+    uint4 wa = make_uint4(0, 0, 0, 0), wb = make_uint4(0, 0, 0, 0);
+    if (SR) {
+      const int64_t e = (r0 + rb16 + 2 * p) * C + c0 + q4;  // multiple of 4
+      wa = sr_words4((uint64_t)e >> 2, 1u, seed);
+      wb = sr_words4((uint64_t)(e + C) >> 2, 1u, seed);
     }
+    const uint32_t ra[4] = {wa.x, wa.y, wa.z, wa.w}, rb_[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t c = 0, f = 0;
+      const uint32_t byte = quantize2<SR, STATS>(cw[j][p], rj[j], ra[j], rb_[j], &c, &f);
+      nib[j][p >> 2] |= byte << (8 * (p & 3));
+      if (STATS && ok) { n_clamp += c; n_flush += f; }
+    }
+  }
+  if (ok) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      *reinterpret_cast<uint2*>(pay_col + (c0 + q4 + j) * (R / 2) + (r0 + rb16) / 2) =
+          make_uint2(nib[j][0], nib[j][1]);
   }
   if (STATS) flush_stats(stats + (DO_ROW ? 1 : 0), n_sat, n_uflow, n_clamp, n_flush);
   flush_amax(amax_out, status, tmax);
