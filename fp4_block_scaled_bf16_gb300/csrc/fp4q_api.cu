@@ -3,6 +3,7 @@
 // dispatch to the kernel launchers.  No entry point allocates memory.
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 #include "../../include/fp4q.h"
 #include "fp4q_device.cuh"
@@ -158,6 +159,16 @@ fp4q_status fp4q_gemm(const uint8_t* A, const uint8_t* A_scales, const float* A_
   a.out = out;
   a.out_f32 = out_is_f32 != 0;
   a.status = status;
+  // Every pipeline wait gives up after about 2 s (4e9 cycles) unless the
+  // test hooks below shorten it; FP4Q_TEST_GEMM_SKIP_LOADS makes the producer
+  // issue no loads so that the consumers' waits run out (failure-path test).
+  a.wait_cycles = 4000000000LL;
+  a.skip_loads = false;
+  if (const char* e = getenv("FP4Q_TEST_GEMM_WAIT_CYCLES")) {
+    const long long v = atoll(e);
+    if (v > 0) a.wait_cycles = v;
+  }
+  if (const char* e = getenv("FP4Q_TEST_GEMM_SKIP_LOADS")) a.skip_loads = atoi(e) != 0;
   return from_cuda(fp4q::launch_gemm(a, st));
 }
 

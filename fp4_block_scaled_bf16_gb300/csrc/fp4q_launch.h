@@ -38,6 +38,8 @@ struct GemmArgs {
   void* out;                        // [M, N] BF16 or binary32
   bool out_f32;
   int* status;
+  long long wait_cycles;            // budget of every pipeline wait (clock64 cycles)
+  bool skip_loads;                  // test hook: the producer issues no loads
 };
 
 // Returns cudaErrorNotSupported when the driver entry point for tensor maps

@@ -61,7 +61,6 @@ constexpr int OFF_TMEM = OFF_BAR + 8 * NBARS;
 constexpr int OFF_ABORT = OFF_TMEM + 8;
 constexpr int SMEM_BYTES = OFF_ABORT + 8 + 1024;   // + slack to align the base to 1 KB
 
-constexpr long long kWaitCycles = 4000000000LL;    // about 2 s at 2 GHz
 
 // ---------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -87,13 +86,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 // Bounded wait on the phase with the given parity.  False when the CTA's
 // abort flag is set or the cycle budget runs out.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                       long long budget) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitCycles) return false;
+    if (clock64() - t0 > budget) return false;
   }
 }
 __device__ __forceinline__ void fail(volatile int* abort_flag, int* status) {
@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                 const uint8_t* __restrict__ As, const uint8_t* __restrict__ Bs,
                 const float* __restrict__ TA, const float* __restrict__ TB, int M, int N, int K,
-                int fmt, void* __restrict__ out, int* status) {
+                int fmt, void* __restrict__ out, int* status, long long budget, int skip_loads) {
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
@@ -282,11 +282,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       for (int kb = 0; kb < nk; ++kb) {
         const int s = kb % S_RAW;
-        if (!mbar_wait(bar_raw_empty + 8 * s, ((kb / S_RAW) & 1) ^ 1, abort_flag)) {
+        if (!mbar_wait(bar_raw_empty + 8 * s, ((kb / S_RAW) & 1) ^ 1, abort_flag, budget)) {
           fail(abort_flag, status);
           break;
         }
         const uint32_t dst = sb + OFF_RAW + s * RAW_STAGE;
+        if (skip_loads) continue;   // test hook: consumers' waits run out
         mbar_expect_tx(bar_raw_full + 8 * s, RAW_STAGE);
         tma_load_2d(dst, &mapA, kb * (BK / 2), m0, bar_raw_full + 8 * s);
         tma_load_2d(dst + RAW_A, &mapB, kb * (BK / 2), n0, bar_raw_full + 8 * s);
@@ -297,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       for (int kb = 0; kb < nk; ++kb) {
         const int t = kb % S_BF;
-        if (!mbar_wait(bar_bf_full + 8 * t, (kb / S_BF) & 1, abort_flag)) {
+        if (!mbar_wait(bar_bf_full + 8 * t, (kb / S_BF) & 1, abort_flag, budget)) {
           fail(abort_flag, status);
           break;
         }
@@ -341,8 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int kb = 0; kb < nk; ++kb) {
       const int s = kb % S_RAW, t = kb % S_BF;
       if (kb + 1 < nk) load_codes(kb + 1, next);
-      if (!mbar_wait(bar_raw_full + 8 * s, (kb / S_RAW) & 1, abort_flag) ||
-          !mbar_wait(bar_bf_empty + 8 * t, ((kb / S_BF) & 1) ^ 1, abort_flag)) {
+      if (!mbar_wait(bar_raw_full + 8 * s, (kb / S_RAW) & 1, abort_flag, budget) ||
+          !mbar_wait(bar_bf_empty + 8 * t, ((kb / S_BF) & 1) ^ 1, abort_flag, budget)) {
         fail(abort_flag, status);
         break;
       }
@@ -373,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ epilogue
     // warp w drains TMEM lanes 32 (w % 4) .. +31 of accumulator (w / 4) % 2,
     // columns 128 (w / 8) .. +127.
-    if (mbar_wait(bar_acc, 0, abort_flag)) {
+    if (mbar_wait(bar_acc, 0, abort_flag, budget)) {
       tc_fence_after();
       const int q = warp & 3, acc = (warp >> 2) & 1, half = warp >> 3;
       const float alpha = __fmul_rn(__ldg(TA), __ldg(TB));
@@ -468,12 +469,14 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
     e = cudaFuncSetAttribute(gemm::gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, gemm::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     gemm::gemm_kernel<true><<<grid, gemm::kThreads, gemm::SMEM_BYTES, st>>>(
-        mapA, mapB, a.As, a.Bs, a.TA, a.TB, (int)a.M, (int)a.N, (int)a.K, a.fmt, a.out, a.status);
+        mapA, mapB, a.As, a.Bs, a.TA, a.TB, (int)a.M, (int)a.N, (int)a.K, a.fmt, a.out, a.status,
+        a.wait_cycles, a.skip_loads ? 1 : 0);
   } else {
     e = cudaFuncSetAttribute(gemm::gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, gemm::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     gemm::gemm_kernel<false><<<grid, gemm::kThreads, gemm::SMEM_BYTES, st>>>(
-        mapA, mapB, a.As, a.Bs, a.TA, a.TB, (int)a.M, (int)a.N, (int)a.K, a.fmt, a.out, a.status);
+        mapA, mapB, a.As, a.Bs, a.TA, a.TB, (int)a.M, (int)a.N, (int)a.K, a.fmt, a.out, a.status,
+        a.wait_cycles, a.skip_loads ? 1 : 0);
   }
   return cudaGetLastError();
 }

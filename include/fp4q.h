@@ -127,7 +127,12 @@ fp4q_status fp4q_dequantize(const uint8_t* payload, const uint8_t* scales, int64
  * The UE5M3 scales are applied in software: each tile is expanded in shared
  * memory to BF16 (exact: e*s has at most 6 significant bits) and multiplied
  * on the tcgen05 tensor cores with binary32 accumulation.  out: [M, N] BF16
- * (out_is_f32 == 0) or binary32.  M, N >= 1 (any), K a multiple of 64. */
+ * (out_is_f32 == 0) or binary32.  M, N >= 0 (any), K a multiple of 64
+ * (K = 0 writes zeros).  Every internal pipeline wait is bounded (about 2 s);
+ * one that runs out latches FP4Q_ERR_TIMEOUT and the kernel exits, leaving
+ * `out` unspecified.  Test hooks (environment, read per call):
+ * FP4Q_TEST_GEMM_WAIT_CYCLES shortens the bound, FP4Q_TEST_GEMM_SKIP_LOADS=1
+ * withholds the operand loads so that the waits run out. */
 fp4q_status fp4q_gemm(const uint8_t* A, const uint8_t* A_scales, const float* A_tscale,
                       const uint8_t* B, const uint8_t* B_scales, const float* B_tscale,
                       int64_t M, int64_t N, int64_t K, fp4q_scale_fmt fmt,
