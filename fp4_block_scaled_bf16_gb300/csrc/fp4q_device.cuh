@@ -86,18 +86,20 @@ __device__ __forceinline__ uint32_t cvt_e2m1x8(const float q[8]) {
 
 // Stochastic rounding of a magnitude a >= 0 onto the E2M1 grid, given the
 // random word w: with lo <= a < hi neighbouring grid points and
-// p = (a - lo) / (hi - lo), the result is hi iff (w >> 8) * 2^-24 < p.
-// For a >= 1 the grid points are exactly the binary32 values with one
-// mantissa bit, so lo is a truncation of the pattern and p * 2^24 is four
-// times the 22 dropped mantissa bits; below 1 the grid is uniform (step
-// 1/2).  Results at or above 6 are saturated by the caller's conversion.
+// p = (a - lo) / (hi - lo), the result is hi iff U = (w >> 8) satisfies
+// U * 2^-24 < p.  For a >= 1 the grid points are exactly the binary32 values
+// with one mantissa bit: p * 2^24 is four times the 22 dropped mantissa bits
+// (rest), and U < 4 rest <=> rest > U / 4 <=> adding the complement of U / 4
+// to the dropped bits carries into the kept bit -- so one add and one mask
+// round the pattern (a carry into the exponent is the step to the next
+// binade).  Below 1 the grid is uniform (step 1/2).  Results at or above 6
+// are saturated by the caller's conversion.
 __device__ __forceinline__ float sr_round_mag(float a, uint32_t w) {
-  const uint32_t U = w >> 8;
   if (a >= 1.0f) {
-    const uint32_t b = __float_as_uint(a);
-    const uint32_t up = ((U >> 2) < (b & 0x3FFFFFu)) ? 1u : 0u;
-    return __uint_as_float((b & ~0x3FFFFFu) + (up << 22));
+    const uint32_t b = __float_as_uint(a) + ((~w >> 10) & 0x3FFFFFu);
+    return __uint_as_float(b & 0xFFC00000u);
   }
+  const uint32_t U = w >> 8;
   const float t = __fmul_rn(a, 2.0f);
   const float fl = floorf(t);
   const float p = __fsub_rn(t, fl);

@@ -85,16 +85,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait on the phase with the given parity.  False when the CTA's
-// abort flag is set or the cycle budget runs out.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                       long long budget) {
-  if (mbar_try_wait(bar, parity)) return true;
+// abort flag is set or the cycle budget runs out.  The first probe is inlined
+// at the call site; only a wait that does not complete at once pays a call.
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                            long long budget) {
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
     if (clock64() - t0 > budget) return false;
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          long long budget) {
+  return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity, abort_flag, budget);
 }
 __device__ __forceinline__ void fail(volatile int* abort_flag, int* status) {
   *abort_flag = 1;
@@ -212,6 +216,14 @@ __device__ __forceinline__ Lut make_lut(uint32_t code, int fmt) {
 // order inside each group of eight is permuted to (n0 n4 n1 n5 n2 n6 n3 n7),
 // identically for A and B, which leaves every dot product unchanged and
 // makes each sign bit one shift away from its place.
+// w * 2^k as an integer multiply-add, which issues on the FMA pipe and so
+// keeps the shift off the integer/logic pipe the byte permutes saturate.
+__device__ __forceinline__ uint32_t shl_fma(uint32_t w, uint32_t pow2) {
+  uint32_t d;
+  asm("mad.lo.u32 %0, %1, %2, 0;" : "=r"(d) : "r"(w), "r"(pow2));
+  return d;
+}
+
 __device__ __forceinline__ uint4 expand8(uint32_t w, const Lut& t) {
   const uint32_t m = w & 0x77777777u;
   const uint32_t s1 = prmt(m, 0u, 0x4420u);   // nibbles n0 n1 n4 n5
@@ -219,10 +231,10 @@ __device__ __forceinline__ uint4 expand8(uint32_t w, const Lut& t) {
   const uint32_t la = prmt(t.L0, t.L1, s1), ha = prmt(t.H0, t.H1, s1);
   const uint32_t lb = prmt(t.L0, t.L1, s2), hb = prmt(t.H0, t.H1, s2);
   uint4 o;
-  o.x = prmt(la, ha, 0x6240u) | ((w << 12) & 0x80008000u);   // (n0, n4)
-  o.y = prmt(la, ha, 0x7351u) | ((w << 8) & 0x80008000u);    // (n1, n5)
-  o.z = prmt(lb, hb, 0x6240u) | ((w << 4) & 0x80008000u);    // (n2, n6)
-  o.w = prmt(lb, hb, 0x7351u) | (w & 0x80008000u);           // (n3, n7)
+  o.x = prmt(la, ha, 0x6240u) | (shl_fma(w, 1u << 12) & 0x80008000u);   // (n0, n4)
+  o.y = prmt(la, ha, 0x7351u) | (shl_fma(w, 1u << 8) & 0x80008000u);    // (n1, n5)
+  o.z = prmt(lb, hb, 0x6240u) | (shl_fma(w, 1u << 4) & 0x80008000u);    // (n2, n6)
+  o.w = prmt(lb, hb, 0x7351u) | (w & 0x80008000u);                      // (n3, n7)
   return o;
 }
 
@@ -335,26 +347,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     auto load_codes = [&](int kb, uint32_t (&c)[kRowsPerThread]) {
 #pragma unroll
-      for (int i = 0; i < kRowsPerThread; ++i) c[i] = rok[i] ? __ldg(srow[i] + kb * 4) : 0u;
+      for (int i = 0; i < kRowsPerThread; ++i) c[i] = (rok[i] && kb < nk) ? __ldg(srow[i] + kb * 4) : 0u;
     };
-    uint32_t codes[kRowsPerThread], next[kRowsPerThread];
-    load_codes(0, codes);
+    // scale codes are prefetched two K steps ahead (their L2 latency is
+    // longer than one step of expansion)
+    uint32_t c0[kRowsPerThread], c1[kRowsPerThread], c2[kRowsPerThread];
+    load_codes(0, c0);
+    load_codes(1, c1);
+    const uint32_t sw = rbase & 7;               // (rbase + 128 i) & 7
+    const uint32_t c_lo = ((2 * blk) ^ sw) << 4, c_hi = ((2 * blk + 1) ^ sw) << 4;
+    int s = 0, t = 0;
+    uint32_t ph_s = 0, ph_t = 1;
     for (int kb = 0; kb < nk; ++kb) {
-      const int s = kb % S_RAW, t = kb % S_BF;
-      if (kb + 1 < nk) load_codes(kb + 1, next);
-      if (!mbar_wait(bar_raw_full + 8 * s, (kb / S_RAW) & 1, abort_flag, budget) ||
-          !mbar_wait(bar_bf_empty + 8 * t, ((kb / S_BF) & 1) ^ 1, abort_flag, budget)) {
+      load_codes(kb + 2, c2);
+      if (!mbar_wait(bar_raw_full + 8 * s, ph_s, abort_flag, budget) ||
+          !mbar_wait(bar_bf_empty + 8 * t, ph_t, abort_flag, budget)) {
         fail(abort_flag, status);
         break;
       }
       const uint32_t raw = sb + OFF_RAW + s * RAW_STAGE + rbase * (BK / 2) + blk * 8;
       const uint32_t bf = sb + OFF_BF + t * BF_STAGE + rbase * 128;
-      const uint32_t sw = rbase & 7;               // (rbase + 128 i) & 7
-      const uint32_t c_lo = ((2 * blk) ^ sw) << 4, c_hi = ((2 * blk + 1) ^ sw) << 4;
 #pragma unroll
       for (int i = 0; i < kRowsPerThread; ++i) {
         const uint2 w = lds64(raw + i * 128 * (BK / 2));
-        const Lut lut = make_lut(codes[i], fmt);
+        const Lut lut = make_lut(c0[i], fmt);
         const uint4 lo = expand8(w.x, lut);        // K 16*blk + 0..7
         const uint4 hi = expand8(w.y, lut);        // K 16*blk + 8..15
         const uint32_t row_addr = bf + i * 128 * 128;
@@ -368,7 +384,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(bar_raw_empty + 8 * s);
       }
 #pragma unroll
-      for (int i = 0; i < kRowsPerThread; ++i) codes[i] = next[i];
+      for (int i = 0; i < kRowsPerThread; ++i) { c0[i] = c1[i]; c1[i] = c2[i]; }
+      if (++s == S_RAW) { s = 0; ph_s ^= 1; }
+      if (++t == S_BF) { t = 0; ph_t ^= 1; }
     }
 
     // ------------------------------------------------ epilogue
