@@ -2,6 +2,8 @@
 // and the kernel translation units (quantize.cu, gemm.cu).  Internal to
 // libfp4q.so; arguments are validated by the ABI layer before they get here.
 #pragma once
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -41,6 +43,10 @@ struct GemmArgs {
   long long wait_cycles;            // budget of every pipeline wait (clock64 cycles)
   bool skip_loads;                  // test hook: the producer issues no loads
 };
+
+// The driver's cuTensorMapEncodeTiled (looked up once through the runtime);
+// null when the driver does not provide it.
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn();
 
 // Returns cudaErrorNotSupported when the driver entry point for tensor maps
 // is missing.

@@ -17,6 +17,7 @@
 // blocks from there.
 #include "fp4q_device.cuh"
 #include "fp4q_launch.h"
+#include "fp4q_pipeline.cuh"
 
 namespace fp4q {
 
@@ -156,138 +157,198 @@ __global__ void __launch_bounds__(256) quantize_row_kernel(
 }
 
 // ---------------------------------------------------------------- tiles
-// One CTA per 128 x 128 tile (ragged edges masked; sizes are multiples of
-// 16).  Phase 1 loads the tile with 128-bit loads (eight per thread: rows
-// t/16 + 16i, column group t%16); phase 2 (row-wise, optional) quantises from
-// registers exactly like the flat kernel; phase 3 stores the tile in shared
-// memory; phase 4 lets thread t quantise columns 4(t%32)..+3 over rows
-// 16(t/32)..+15 -- four column blocks, one Philox block per row, drawn row by
-// row so that no more than two blocks of random words are live at a time.
+// Column-wise and dual-axis quantisation.  A persistent CTA walks 128 x 128
+// tiles (ragged edges read as zero and are masked on output; sizes are
+// multiples of 16).  Warp 8 streams tiles with 2-D TMA into a 3-stage
+// shared-memory ring; warps 0..7 consume them without any CTA-wide barrier:
+//   row blocks (dual axis only): thread t reads rows t/16 + 16 i (i = 0..7),
+//     columns 8 (t % 16) .. +7 with 128-bit shared loads; lanes 2k, 2k+1 hold
+//     one 16-element block (one shuffle for its amax);
+//   column blocks: thread t quantises columns 4 (t % 32) .. +3 over rows
+//     16 (t / 32) .. +15 from 64-bit shared loads -- four column blocks, one
+//     Philox block per row for stochastic rounding, drawn row by row.
+// With stochastic rounding the kernel is bound by instruction latency rather
+// than memory, so two groups of eight consumer warps work on alternate tiles
+// (one CTA per SM); the round-to-nearest kernel runs one group, two CTAs per
+// SM.
 constexpr int kTile = 128;
+constexpr int kQStageBytes = kTile * kTile * 2;
+constexpr long long kQWaitCycles = 4000000000LL;
+template <bool SR>
+struct TileCfg {
+  static constexpr int kGroups = SR ? 2 : 1;
+  static constexpr int kStages = SR ? 4 : 3;
+  static constexpr int kConsumerWarps = 8 * kGroups;
+  static constexpr int kThreads = 32 * (kConsumerWarps + 1);
+  static constexpr int kSmem = kStages * kQStageBytes + 16 * kStages + 128;
+  static constexpr int kCtasPerSm = SR ? 1 : 2;
+};
 
 template <bool SR, bool STATS, bool DO_ROW>
-__global__ void __launch_bounds__(256, 2) quantize_tile_kernel(
-    const uint16_t* __restrict__ in, int64_t R, int64_t C, int fmt,
+__global__ void __launch_bounds__(TileCfg<SR>::kThreads, TileCfg<SR>::kCtasPerSm) quantize_tile_kernel(
+    const __grid_constant__ CUtensorMap map, int64_t R, int64_t C, int fmt,
     const float* __restrict__ tscale, uint64_t seed, uint32_t* __restrict__ pay_row,
     uint8_t* __restrict__ sc_row, uint8_t* __restrict__ pay_col, uint8_t* __restrict__ sc_col,
     StatsDev* stats, float* amax_out, int* status) {
-  __shared__ __align__(16) uint16_t tile[kTile][kTile];
-  const float T = __ldg(tscale);
-  const float six_t = __fmul_rn(6.0f, T);
-  const int t = threadIdx.x, lane = t & 31;
-  const int64_t r0 = (int64_t)blockIdx.y * kTile, c0 = (int64_t)blockIdx.x * kTile;
-  const int rows = (int)(R - r0 < kTile ? R - r0 : kTile);
-  const int cols = (int)(C - c0 < kTile ? C - c0 : kTile);
-  uint32_t tmax = 0, n_sat = 0, n_uflow = 0, n_clamp = 0, n_flush = 0;
-
-  // phase 1: coalesced loads
-  const int cg = t & 15;
-  uint4 v[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int row = (t >> 4) + 16 * i;
-    const bool ok = row < rows && cg * 8 < cols;
-    v[i] = ok ? ld_stream_v4(in + (r0 + row) * C + c0 + cg * 8) : make_uint4(0, 0, 0, 0);
-  }
-  // phase 2: row-wise blocks from registers
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int row = (t >> 4) + 16 * i;
-    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-    uint32_t m = absmax16(w);
-    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-    tmax = max(tmax, m);
-    if (DO_ROW) {
-      const bool ok = row < rows && cg * 8 < cols;
-      const int64_t e0 = (r0 + row) * C + c0 + cg * 8;  // logical index of the chunk
-      const BlockScale bs = block_scale(m, six_t, T, fmt);
-      uint32_t rb[8];
-      if (SR) {
-        const uint4 a = sr_words4((uint64_t)e0 >> 2, 0u, seed);
-        const uint4 b = sr_words4(((uint64_t)e0 >> 2) + 1, 0u, seed);
-        rb[0] = a.x; rb[1] = a.y; rb[2] = a.z; rb[3] = a.w;
-        rb[4] = b.x; rb[5] = b.y; rb[6] = b.z; rb[7] = b.w;
-      }
-      uint32_t c = 0, f = 0;
-      const uint32_t nib = quantize8<SR, STATS>(w, bs.r, rb, &c, &f);
-      if (ok) {
-        st_stream_u32(pay_row + (e0 >> 3), nib);
-        if ((lane & 1) == 0) sc_row[e0 >> 4] = (uint8_t)bs.code;
-        if (STATS) {
-          n_clamp += c;
-          n_flush += f;
-          if ((lane & 1) == 0) {
-            n_sat += bs.sat ? 1u : 0u;
-            n_uflow += (m != 0u && bs.code == 0u) ? 1u : 0u;
-          }
-        }
-      }
+  extern __shared__ uint8_t qsm_dyn[];
+  uint8_t* qsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qsm_dyn) + 127) & ~uintptr_t(127));
+  using Cfg = TileCfg<SR>;
+  constexpr int kQStages = Cfg::kStages;
+  const uint32_t sb = smem_u32(qsm);
+  const uint32_t bar_full = sb + kQStages * kQStageBytes;
+  const uint32_t bar_empty = bar_full + 8 * kQStages;
+  const int64_t tiles_c = (C + kTile - 1) / kTile;
+  const int64_t tiles = tiles_c * ((R + kTile - 1) / kTile);
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  if (t == 0) {
+    for (int i = 0; i < kQStages; ++i) {
+      mbar_init(bar_full + 8 * i, 1);
+      mbar_init(bar_empty + 8 * i, 8);   // the eight warps of one consumer group
     }
-    *reinterpret_cast<uint4*>(&tile[row][cg * 8]) = v[i];
-  }
-  if (DO_ROW && STATS) {
-    // row-wise counters go to stats[0]; column-wise ones to stats[1]
-    flush_stats(stats, n_sat, n_uflow, n_clamp, n_flush);
-    n_sat = n_uflow = n_clamp = n_flush = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
 
-  // phase 4: column blocks from shared memory
-  const int q4 = lane * 4;         // first of four columns
-  const int rb16 = (t >> 5) * 16;  // first of 16 rows
-  const bool ok = q4 < cols && rb16 < rows;
-  uint32_t cw[4][8];  // [column j][row pair p] = BF16 of rows 2p (low), 2p+1 (high)
-#pragma unroll
-  for (int p = 0; p < 8; ++p) {
-    const uint2 a = *reinterpret_cast<const uint2*>(&tile[rb16 + 2 * p][q4]);
-    const uint2 b = *reinterpret_cast<const uint2*>(&tile[rb16 + 2 * p + 1][q4]);
-    // a.x = cols (q4, q4+1) of row 2p, a.y = cols (q4+2, q4+3)
-    cw[0][p] = __byte_perm(a.x, b.x, 0x5410);
-    cw[1][p] = __byte_perm(a.x, b.x, 0x7632);
-    cw[2][p] = __byte_perm(a.y, b.y, 0x5410);
-    cw[3][p] = __byte_perm(a.y, b.y, 0x7632);
-  }
-  float rj[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t w4a[4] = {cw[j][0], cw[j][1], cw[j][2], cw[j][3]};
-    const uint32_t w4b[4] = {cw[j][4], cw[j][5], cw[j][6], cw[j][7]};
-    const uint32_t cm = max(absmax16(w4a), absmax16(w4b));
-    const BlockScale bs = block_scale(cm, six_t, T, fmt);
-    rj[j] = bs.r;
-    if (STATS && ok) {
-      n_sat += bs.sat ? 1u : 0u;
-      n_uflow += (cm != 0u && bs.code == 0u) ? 1u : 0u;
+  uint32_t tmax = 0;
+  uint32_t r_sat = 0, r_uflow = 0, r_clamp = 0, r_flush = 0;   // row-wise counters
+  uint32_t c_sat = 0, c_uflow = 0, c_clamp = 0, c_flush = 0;   // column-wise counters
+  if (warp == Cfg::kConsumerWarps) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+        if (!mbar_wait_bounded(bar_empty + 8 * s, ph ^ 1, kQWaitCycles)) {
+          atomicOr(status, kStatusTimeout);
+          break;
+        }
+        const int r0 = (int)((tile / tiles_c) * kTile), c0 = (int)((tile % tiles_c) * kTile);
+        mbar_expect_tx(bar_full + 8 * s, kQStageBytes);
+        tma_load_2d(sb + s * kQStageBytes, &map, c0, r0, bar_full + 8 * s);
+        if (++s == kQStages) { s = 0; ph ^= 1; }
+      }
     }
-    if (ok) sc_col[(c0 + q4 + j) * (R / 16) + (r0 + rb16) / 16] = (uint8_t)bs.code;
-  }
-  // rows in pairs: one Philox block per row gives the words of its four
-  // columns (counter = logical index / 4, word = column offset)
-  uint32_t nib[4][2] = {{0u, 0u}, {0u, 0u}, {0u, 0u}, {0u, 0u}};
+  } else {
+    // ------------------------------------------------ consumers
+    // group g (warps 8g .. 8g+7) takes the CTA's tiles g, g + G, g + 2G, ...
+    const float T = __ldg(tscale);
+    const float six_t = __fmul_rn(6.0f, T);
+    const int g = warp >> 3;
+    const int tl_id = t & 255;          // thread index inside the group
+    const int cg = tl_id & 15;
+    const int q4 = lane * 4;            // first of four columns (column phase)
+    const int rb16 = (warp & 7) * 16;   // first of 16 rows (column phase)
+    for (int64_t j = g; ; j += Cfg::kGroups) {
+      const int64_t tile = blockIdx.x + j * gridDim.x;
+      if (tile >= tiles) break;
+      const int s = (int)(j % kQStages);
+      const uint32_t ph = (uint32_t)((j / kQStages) & 1);
+      const int64_t r0 = (tile / tiles_c) * kTile, c0 = (tile % tiles_c) * kTile;
+      const int rows = (int)(R - r0 < kTile ? R - r0 : kTile);
+      const int cols = (int)(C - c0 < kTile ? C - c0 : kTile);
+      if (!mbar_wait_bounded(bar_full + 8 * s, ph, kQWaitCycles)) {
+        atomicOr(status, kStatusTimeout);
+        break;
+      }
+      const uint16_t(*tl)[kTile] = reinterpret_cast<const uint16_t(*)[kTile]>(qsm + s * kQStageBytes);
+
+      // row-wise blocks (and the tile's share of the tensor amax)
+#pragma unroll 2
+      for (int i = 0; i < 8; ++i) {
+        const int row = (tl_id >> 4) + 16 * i;
+        const uint4 v = *reinterpret_cast<const uint4*>(&tl[row][cg * 8]);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t m = absmax16(w);
+        tmax = max(tmax, m);
+        if (DO_ROW) {
+          m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+          const bool ok = row < rows && cg * 8 < cols;
+          const int64_t e0 = (r0 + row) * C + c0 + cg * 8;  // logical index of the chunk
+          const BlockScale bs = block_scale(m, six_t, T, fmt);
+          uint32_t rb[8];
+          if (SR) {
+            const uint4 a = sr_words4((uint64_t)e0 >> 2, 0u, seed);
+            const uint4 b = sr_words4(((uint64_t)e0 >> 2) + 1, 0u, seed);
+            rb[0] = a.x; rb[1] = a.y; rb[2] = a.z; rb[3] = a.w;
+            rb[4] = b.x; rb[5] = b.y; rb[6] = b.z; rb[7] = b.w;
+          }
+          uint32_t c = 0, f = 0;
+          const uint32_t nib = quantize8<SR, STATS>(w, bs.r, rb, &c, &f);
+          if (ok) {
+            st_stream_u32(pay_row + (e0 >> 3), nib);
+            if ((lane & 1) == 0) sc_row[e0 >> 4] = (uint8_t)bs.code;
+            if (STATS) {
+              r_clamp += c;
+              r_flush += f;
+              if ((lane & 1) == 0) {
+                r_sat += bs.sat ? 1u : 0u;
+                r_uflow += (m != 0u && bs.code == 0u) ? 1u : 0u;
+              }
+            }
+          }
+        }
+      }
+
+      // column-wise blocks
+      const bool ok = q4 < cols && rb16 < rows;
+      uint32_t cw[4][8];  // [column j][row pair p] = BF16 of rows 2p (low), 2p+1 (high)
 #pragma unroll
-  for (int p = 0; p < 8; ++p) {
-    uint4 wa = make_uint4(0, 0, 0, 0), wb = make_uint4(0, 0, 0, 0);
-    if (SR) {
-      const int64_t e = (r0 + rb16 + 2 * p) * C + c0 + q4;  // multiple of 4
-      wa = sr_words4((uint64_t)e >> 2, 1u, seed);
-      wb = sr_words4((uint64_t)(e + C) >> 2, 1u, seed);
+      for (int p = 0; p < 8; ++p) {
+        const uint2 a = *reinterpret_cast<const uint2*>(&tl[rb16 + 2 * p][q4]);
+        const uint2 b = *reinterpret_cast<const uint2*>(&tl[rb16 + 2 * p + 1][q4]);
+        cw[0][p] = __byte_perm(a.x, b.x, 0x5410);
+        cw[1][p] = __byte_perm(a.x, b.x, 0x7632);
+        cw[2][p] = __byte_perm(a.y, b.y, 0x5410);
+        cw[3][p] = __byte_perm(a.y, b.y, 0x7632);
+      }
+      // the tile is in registers now: release the stage to the producer
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+
+      float rj[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t w4a[4] = {cw[j][0], cw[j][1], cw[j][2], cw[j][3]};
+        const uint32_t w4b[4] = {cw[j][4], cw[j][5], cw[j][6], cw[j][7]};
+        const uint32_t cm = max(absmax16(w4a), absmax16(w4b));
+        const BlockScale bs = block_scale(cm, six_t, T, fmt);
+        rj[j] = bs.r;
+        if (STATS && ok) {
+          c_sat += bs.sat ? 1u : 0u;
+          c_uflow += (cm != 0u && bs.code == 0u) ? 1u : 0u;
+        }
+        if (ok) sc_col[(c0 + q4 + j) * (R / 16) + (r0 + rb16) / 16] = (uint8_t)bs.code;
+      }
+      uint32_t nib[4][2] = {{0u, 0u}, {0u, 0u}, {0u, 0u}, {0u, 0u}};
+#pragma unroll
+      for (int p = 0; p < 8; ++p) {
+        uint4 wa = make_uint4(0, 0, 0, 0), wb = make_uint4(0, 0, 0, 0);
+        if (SR) {
+          const int64_t e = (r0 + rb16 + 2 * p) * C + c0 + q4;  // multiple of 4
+          wa = sr_words4((uint64_t)e >> 2, 1u, seed);
+          wb = sr_words4((uint64_t)(e + C) >> 2, 1u, seed);
+        }
+        const uint32_t ra[4] = {wa.x, wa.y, wa.z, wa.w}, rb_[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t c = 0, f = 0;
+          const uint32_t byte = quantize2<SR, STATS>(cw[j][p], rj[j], ra[j], rb_[j], &c, &f);
+          nib[j][p >> 2] |= byte << (8 * (p & 3));
+          if (STATS && ok) { c_clamp += c; c_flush += f; }
+        }
+      }
+      if (ok) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<uint2*>(pay_col + (c0 + q4 + j) * (R / 2) + (r0 + rb16) / 2) =
+              make_uint2(nib[j][0], nib[j][1]);
+      }
     }
-    const uint32_t ra[4] = {wa.x, wa.y, wa.z, wa.w}, rb_[4] = {wb.x, wb.y, wb.z, wb.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      uint32_t c = 0, f = 0;
-      const uint32_t byte = quantize2<SR, STATS>(cw[j][p], rj[j], ra[j], rb_[j], &c, &f);
-      nib[j][p >> 2] |= byte << (8 * (p & 3));
-      if (STATS && ok) { n_clamp += c; n_flush += f; }
-    }
   }
-  if (ok) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      *reinterpret_cast<uint2*>(pay_col + (c0 + q4 + j) * (R / 2) + (r0 + rb16) / 2) =
-          make_uint2(nib[j][0], nib[j][1]);
+  if (STATS) {
+    if (DO_ROW) flush_stats(stats, r_sat, r_uflow, r_clamp, r_flush);
+    flush_stats(stats + (DO_ROW ? 1 : 0), c_sat, c_uflow, c_clamp, c_flush);
   }
-  if (STATS) flush_stats(stats + (DO_ROW ? 1 : 0), n_sat, n_uflow, n_clamp, n_flush);
   flush_amax(amax_out, status, tmax);
 }
 
@@ -365,12 +426,32 @@ static void row_launch(const QuantArgs& a, cudaStream_t st) {
 }
 
 template <bool SR, bool STATS, bool DO_ROW>
-static void tile_launch(const QuantArgs& a, cudaStream_t st) {
-  dim3 grid((unsigned)((a.cols + kTile - 1) / kTile), (unsigned)((a.rows + kTile - 1) / kTile));
-  quantize_tile_kernel<SR, STATS, DO_ROW><<<grid, 256, 0, st>>>(
-      static_cast<const uint16_t*>(a.in), a.rows, a.cols, a.fmt, a.tscale, a.seed,
-      reinterpret_cast<uint32_t*>(a.pay_row), a.sc_row, a.pay_col, a.sc_col, a.stats, a.amax_out,
-      a.status);
+static cudaError_t tile_launch(const QuantArgs& a, cudaStream_t st) {
+  auto fn = get_encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  CUtensorMap map;
+  const cuuint64_t dims[2] = {(cuuint64_t)a.cols, (cuuint64_t)a.rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)a.cols * 2};
+  const cuuint32_t box[2] = {kTile, kTile};
+  const cuuint32_t estr[2] = {1, 1};
+  if (fn(&map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(a.in), dims, strides, box, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  using Cfg = TileCfg<SR>;
+  auto kern = quantize_tile_kernel<SR, STATS, DO_ROW>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+  if (e != cudaSuccess) return e;
+  const int64_t tiles = ((a.cols + kTile - 1) / kTile) * ((a.rows + kTile - 1) / kTile);
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t cap = (int64_t)sms * Cfg::kCtasPerSm;
+  const unsigned grid = (unsigned)(tiles < cap ? tiles : cap);
+  kern<<<grid, Cfg::kThreads, Cfg::kSmem, st>>>(map, a.rows, a.cols, a.fmt, a.tscale, a.seed,
+                                        reinterpret_cast<uint32_t*>(a.pay_row), a.sc_row, a.pay_col,
+                                        a.sc_col, a.stats, a.amax_out, a.status);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t st) {
@@ -388,14 +469,14 @@ cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t st) {
   if (a.axis == 0) {
     if (sr) stats ? row_launch<true, true>(a, st) : row_launch<true, false>(a, st);
     else stats ? row_launch<false, true>(a, st) : row_launch<false, false>(a, st);
-  } else if (a.axis == 1) {
-    if (sr) stats ? tile_launch<true, true, false>(a, st) : tile_launch<true, false, false>(a, st);
-    else stats ? tile_launch<false, true, false>(a, st) : tile_launch<false, false, false>(a, st);
-  } else {
-    if (sr) stats ? tile_launch<true, true, true>(a, st) : tile_launch<true, false, true>(a, st);
-    else stats ? tile_launch<false, true, true>(a, st) : tile_launch<false, false, true>(a, st);
+    return cudaGetLastError();
   }
-  return cudaGetLastError();
+  if (a.axis == 1) {
+    if (sr) return stats ? tile_launch<true, true, false>(a, st) : tile_launch<true, false, false>(a, st);
+    return stats ? tile_launch<false, true, false>(a, st) : tile_launch<false, false, false>(a, st);
+  }
+  if (sr) return stats ? tile_launch<true, true, true>(a, st) : tile_launch<true, false, true>(a, st);
+  return stats ? tile_launch<false, true, true>(a, st) : tile_launch<false, false, true>(a, st);
 }
 
 cudaError_t launch_dequantize(const uint8_t* payload, const uint8_t* scales, int64_t rows,
