@@ -38,7 +38,33 @@ WORKLOAD = ("8B-class linear 4096->16384, 8192 tokens: amax+scale, dual-axis qua
             "and dY (SR seed 7), fprop+dgrad+wgrad block-scaled GEMMs")
 # algorithmic bytes per element: read BF16 (2) + payload 0.5 + scale 1/16 per axis
 DUAL_BYTES_PER_ELEM = 2 + 2 * (0.5 + 1 / 16)
+ROW_BYTES_PER_ELEM = 2 + 0.5 + 1 / 16
 AMAX_BYTES_PER_ELEM = 2
+
+
+def kernel_sources_sha(files):
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "fp4_block_scaled_bf16_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+GEMM_SOURCES = ["gemm.cu", "fp4q_device.cuh", "fp4q_pipeline.cuh"]
+
+
+def committed_traffic(name, sources):
+    """DRAM bytes per launch from a committed ncu capture, or None when the
+    kernel's sources changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", name)
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("source_sha") != kernel_sources_sha(sources):
+        return None
+    return d.get("dram_bytes_per_launch")
 
 
 def peaks():
@@ -232,9 +258,25 @@ def run_gpu(args, rank, world):
     s1.record()
     torch.cuda.synchronize()
     e2e_ms = s0.elapsed_time(s1) / e2e_steps
+
+    # ---- single-axis quantiser rates (outside the step): W row-wise RNE and
+    # dY row-wise SR, 10 launches each, inputs larger than L2
+    rates = {}
+    for name, x, rnd, pay, sc in (("W_row_rne", step.W, fp4q.RNE, step.Wr, step.Wrs),
+                                  ("dY_row_sr", step.dY, fp4q.SR, step.Dr, step.Drs)):
+        Tn = step.T[1:2] if x is step.W else step.T[2:3]
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        fp4q.fp4q_quantize(x, fp4q.AXIS_ROW, fp4q.UE5M3, Tn, rnd, 7, pay, sc, None, None)
+        a0.record()
+        for _ in range(10):
+            fp4q.fp4q_quantize(x, fp4q.AXIS_ROW, fp4q.UE5M3, Tn, rnd, 7, pay, sc, None, None)
+        a1.record()
+        torch.cuda.synchronize()
+        rates[name] = x.numel() * ROW_BYTES_PER_ELEM / (a0.elapsed_time(a1) / 10 * 1e-3) / 1e9
     h2d = (hX.numel() + hW.numel() + hD.numel()) * 2
     d2h = (hY.numel() + hdX.numel() + hdW.numel()) * 2
-    return dict(ms=ms, t_scale=t_scale, t_q=(t_qx, t_qw, t_qd), t_g=t_g, launches=launches,
+    return dict(ms=ms, t_scale=t_scale, t_q=(t_qx, t_qw, t_qd), t_g=t_g, launches=launches, rates=rates,
                 clocks=clk.summary(), status=status, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
                 elems=(X.numel(), W.numel(), dY.numel()))
 
@@ -350,12 +392,14 @@ def main():
                    "l2": "inputs larger than L2 (dY 256 MiB, step working set ~1 GiB)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": bf16,
-                     "unit": "TFLOP/s", "frac": gemm_tflops / bf16 if bf16 else None, "traffic": None,
+                     "unit": "TFLOP/s", "frac": gemm_tflops / bf16 if bf16 else None,
+                     "traffic": committed_traffic("gemm_kernel_traffic_8B_linear.json", GEMM_SOURCES),
                      "kernel": "fp4q gemm_kernel (mean of fprop/dgrad/wgrad)",
                      "peak_source": f"{src} bf16 (sustained)"},
         "roofline_quantize": {"bound": "hbm", "unit": "GB/s", "peak": hbm,
-                              "achieved": {"X_dual_rne": q_gbs[0], "W_dual_rne": q_gbs[1], "dY_dual_sr": q_gbs[2]},
-                              "frac": {k: g / hbm for k, g in zip(("X_dual_rne", "W_dual_rne", "dY_dual_sr"), q_gbs)} if hbm else None,
+                              "achieved": dict({"X_dual_rne": q_gbs[0], "W_dual_rne": q_gbs[1], "dY_dual_sr": q_gbs[2]}, **r["rates"]),
+                              "frac": dict({k: g / hbm for k, g in zip(("X_dual_rne", "W_dual_rne", "dY_dual_sr"), q_gbs)},
+                                           **{k: g / hbm for k, g in r["rates"].items()}) if hbm else None,
                               "peak_source": f"{src} hbm"},
         "breakdown_ms": {"amax_scale": r["t_scale"], "quantize_X": r["t_q"][0], "quantize_W": r["t_q"][1],
                          "quantize_dY": r["t_q"][2], "fprop": r["t_g"][0], "dgrad": r["t_g"][1],

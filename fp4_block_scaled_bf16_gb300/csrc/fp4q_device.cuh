@@ -130,23 +130,86 @@ __device__ __forceinline__ uint4 sr_words4(uint64_t ctr, uint32_t axis, uint64_t
 }
 
 // ---------------------------------------------------------------- one block
-// Encodes the scale of a block from its amax (as the 16-bit |bf16| pattern)
-// and returns the reciprocal multiplier r = 1 / (s T); r = 0 marks a zero
-// scale (every element then encodes to a signed zero).
+// The block scale depends only on the block's amax -- a non-negative BF16
+// pattern a16 -- and the tensor scale T.  Per block the exact rule is
+//   code = encode(RN(bf16(a16) / RN(6 T))),  r = RN(1 / RN(decode(code) T)),
+// with encode monotone in a16.  A CTA therefore tabulates, once per tensor
+// scale, the smallest a16 reaching each code (found with the exact rule) and
+// r for each code; per block it derives an approximate code from one
+// multiply by 1/(6T) -- never off by more than one, because the binary32
+// error is far below the 1/16 relative spacing of the scale codes -- and
+// corrects it against two table entries.  The result is bit-identical to
+// the exact rule.
 struct BlockScale {
   uint32_t code;
-  float r;
+  float r;        // 1 / (s T); 0 marks a zero scale (elements encode to signed zeros)
   bool sat;
 };
 
-__device__ __forceinline__ BlockScale block_scale(uint32_t amax16, float six_t, float T, int fmt) {
+struct ScaleTab {
+  uint32_t thr[256];   // thr[c]: smallest a16 with code >= c (c = 1..cmax); thr[0] = 0; 0xFFFF past cmax
+  float recip[256];    // RN(1 / RN(s_c T)), 0 where s_c = 0
+  uint32_t thr_sat;    // smallest a16 whose s* exceeds the largest scale
+  uint32_t cmax;
+  float inv6t;         // RN(1 / RN(6 T)), for the approximate code
+  float unbias;        // 2^-(127 - bias): binary32 pattern of s * unbias, shifted by 20, is the code
+};
+
+__device__ __forceinline__ uint32_t exact_code(uint32_t a16, float six_t, int fmt, bool* sat) {
+  return encode_scale(__fdiv_rn(__uint_as_float(a16 << 16), six_t), fmt, sat);
+}
+
+// Block-wide: every thread of the CTA calls it (it ends with __syncthreads).
+__device__ __forceinline__ void build_scale_tab(ScaleTab* tab, float T, int fmt) {
+  const float six_t = __fmul_rn(6.0f, T);
+  const uint32_t cmax = (fmt == kUE5M3) ? 0xFEu : 0x7Eu;
+  for (uint32_t c = threadIdx.x; c < 256; c += blockDim.x) {
+    const float sc = decode_scale(c, fmt);
+    tab->recip[c] = (sc == 0.0f || c > cmax) ? 0.0f : __frcp_rn(__fmul_rn(sc, T));
+    if (c == 0) { tab->thr[0] = 0; continue; }
+    if (c > cmax + 1) { tab->thr[c] = 0xFFFFu; continue; }
+    // smallest a16 in [0, 0x7F80] with exact_code >= c (or saturating, for
+    // c = cmax + 1); 0xFFFF when none
+    uint32_t lo = 0, hi = 0x7F81;
+    while (lo < hi) {
+      const uint32_t mid = (lo + hi) >> 1;
+      bool sat;
+      const uint32_t code = exact_code(mid, six_t, fmt, &sat);
+      const bool ge = (c <= cmax) ? (code >= c) : sat;
+      if (ge) hi = mid; else lo = mid + 1;
+    }
+    const uint32_t v = (lo > 0x7F80u) ? 0xFFFFu : lo;
+    if (c <= cmax) tab->thr[c] = v;
+    else { tab->thr_sat = v; tab->thr[c] = 0xFFFFu; }
+  }
+  if (threadIdx.x == 0) {
+    tab->cmax = cmax;
+    tab->inv6t = __frcp_rn(six_t);
+    tab->unbias = (fmt == kUE5M3) ? 0x1p-112f : 0x1p-120f;
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ BlockScale block_scale(uint32_t a16, const ScaleTab& tab) {
   BlockScale bs;
-  const float amax_b = __uint_as_float(amax16 << 16);
-  const float s_star = __fdiv_rn(amax_b, six_t);
-  bs.code = encode_scale(s_star, fmt, &bs.sat);
-  const float s = decode_scale(bs.code, fmt);
-  bs.r = (s == 0.0f) ? 0.0f : __frcp_rn(__fmul_rn(s, T));
+  const float sa = __fmul_rn(__fmul_rn(__uint_as_float(a16 << 16), tab.inv6t), tab.unbias);
+  uint32_t c = (__float_as_uint(sa) + 0x80000u) >> 20;
+  c = min(c, tab.cmax);
+  c = c - (a16 < tab.thr[c] ? 1u : 0u) + (a16 >= tab.thr[c + 1] ? 1u : 0u);
+  bs.code = c;
+  bs.r = tab.recip[c];
+  bs.sat = a16 >= tab.thr_sat;
   return bs;
+}
+
+// q = x * r for a BF16 pair, as one packed binary32x2 multiply (each lane
+// rounded to nearest even, exactly like two scalar multiplies).
+__device__ __forceinline__ void mul2(uint32_t pair, float r, float& q0, float& q1) {
+  unsigned long long x, rr, y;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "r"(pair << 16), "r"(pair & 0xFFFF0000u));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(rr) : "f"(r));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(y) : "l"(x), "l"(rr));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(q0), "=f"(q1) : "l"(y));
 }
 
 // Quantises eight elements (four BF16 words) with multiplier r.  Returns the
@@ -156,10 +219,7 @@ __device__ __forceinline__ uint32_t quantize8(const uint32_t w[4], float r, cons
                                               uint32_t* clamped, uint32_t* flushed) {
   float q[8];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    q[2 * j] = __fmul_rn(bf16_lo(w[j]), r);
-    q[2 * j + 1] = __fmul_rn(bf16_hi(w[j]), r);
-  }
+  for (int j = 0; j < 4; ++j) mul2(w[j], r, q[2 * j], q[2 * j + 1]);
   if (r == 0.0f) {
     // zero scale: signed zeros (x * 0 keeps the sign of x)
 #pragma unroll
@@ -197,7 +257,8 @@ __device__ __forceinline__ uint32_t quantize8(const uint32_t w[4], float r, cons
 template <bool SR, bool STATS>
 __device__ __forceinline__ uint32_t quantize2(uint32_t pair, float r, uint32_t w0, uint32_t w1,
                                               uint32_t* clamped, uint32_t* flushed) {
-  float q0 = __fmul_rn(bf16_lo(pair), r), q1 = __fmul_rn(bf16_hi(pair), r);
+  float q0, q1;
+  mul2(pair, r, q0, q1);
   if (r == 0.0f) {
     q0 = __uint_as_float((pair << 16) & 0x80000000u);
     q1 = __uint_as_float(pair & 0x80000000u);

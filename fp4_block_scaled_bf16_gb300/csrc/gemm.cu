@@ -20,8 +20,9 @@
 //               into a 4-stage raw ring.
 //   warps 0..15 expand raw stages into a 2-stage BF16 ring laid out in the
 //               128-byte-swizzled K-major form the MMA descriptors read; each
-//               thread expands one 16-element block (one scale) at a time
-//               through an 8-entry per-block value table and byte permutes;
+//               thread expands one 16-element block (one scale) at a time by
+//               placing nibble bits in BF16 patterns and two exact BF16
+//               multiplies (the second by the block scale);
 //               after the main loop they run the epilogue (TMEM -> registers
 //               -> alpha -> BF16/FP32 -> global).
 //   warp 17     allocates TMEM; one lane issues 8 MMAs (2 x M128 N256 K16)
@@ -156,54 +157,48 @@ __device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
   return d;
 }
 
-// The eight magnitudes E2M1(v) * s (v = 0..7) as BF16, split into a table of
-// low bytes (L0: v 0..3, L1: v 4..7) and of high bytes (H0, H1), so that one
-// byte permute per table looks up four elements.
-struct Lut {
-  uint32_t L0, L1, H0, H1;
-};
-__device__ __forceinline__ Lut make_lut(uint32_t code, int fmt) {
-  // The code shifted into a binary32 exponent/mantissa field is the scale
-  // times 2^-(127 - bias), subnormal codes included (gradual underflow lines
-  // up), so one exact multiply by a power of two decodes it.
+// Expansion of E2M1 x UE5M3 to BF16 with the multiplies on the FP16/BF16
+// pipe.  The nibble's three magnitude bits v placed at bits 6..8 of a BF16
+// pattern, with its sign at bit 15, encode exactly +-E2M1(v) * 2^-126: the
+// E2M1 exponent lands in the BF16 exponent field and the E2M1 subnormal
+// (v = 1, 0.5) lands on the BF16 subnormal 2^-127, so gradual underflow lines
+// up.  Two exact multiplies -- by 2^100, then by s * 2^26 -- give +-E2M1(v) * s
+// (at most 6 significant bits, within [2^-18, 688128]); one multiply by
+// s * 2^126 would overflow BF16 for s >= 4.
+
+// (s * 2^26, s * 2^26) as a BF16 pair.  The scale code shifted into a binary32
+// exponent/mantissa field is s * 2^-(127 - bias), subnormal codes included.
+__device__ __forceinline__ uint32_t scale_pair(uint32_t code, int fmt) {
   const float s = __fmul_rn(__uint_as_float(code << 20), fmt == kUE5M3 ? 0x1p112f : 0x1p120f);
+  const float s26 = __fmul_rn(s, 0x1p26f);
   uint32_t ss;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(ss) : "f"(s));   // exact: <= 4 significant bits
-  const uint32_t p01 = bmul2(ss, 0x3F000000u);   // (0, 0.5) * s
-  const uint32_t p23 = bmul2(ss, 0x3FC03F80u);   // (1, 1.5) * s
-  const uint32_t p45 = bmul2(ss, 0x40404000u);   // (2, 3) * s
-  const uint32_t p67 = bmul2(ss, 0x40C04080u);   // (4, 6) * s
-  Lut t;
-  t.L0 = prmt(p01, p23, 0x6420u);
-  t.H0 = prmt(p01, p23, 0x7531u);
-  t.L1 = prmt(p45, p67, 0x6420u);
-  t.H1 = prmt(p45, p67, 0x7531u);
-  return t;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(ss) : "f"(s26));   // exact: <= 4 significant bits
+  return ss;
 }
 
-// Expands eight nibbles (n0 in the low bits) into four BF16 pairs.  The K
-// order inside each group of eight is permuted to (n0 n4 n1 n5 n2 n6 n3 n7),
-// identically for A and B, which leaves every dot product unchanged and
-// makes each sign bit one shift away from its place.
 // w * 2^k as an integer multiply-add, which issues on the FMA pipe and so
-// keeps the shift off the integer/logic pipe the byte permutes saturate.
+// keeps the shift off the integer/logic pipe.
 __device__ __forceinline__ uint32_t shl_fma(uint32_t w, uint32_t pow2) {
   uint32_t d;
   asm("mad.lo.u32 %0, %1, %2, 0;" : "=r"(d) : "r"(w), "r"(pow2));
   return d;
 }
 
-__device__ __forceinline__ uint4 expand8(uint32_t w, const Lut& t) {
-  const uint32_t m = w & 0x77777777u;
-  const uint32_t s1 = prmt(m, 0u, 0x4420u);   // nibbles n0 n1 n4 n5
-  const uint32_t s2 = prmt(m, 0u, 0x4431u);   // nibbles n2 n3 n6 n7
-  const uint32_t la = prmt(t.L0, t.L1, s1), ha = prmt(t.H0, t.H1, s1);
-  const uint32_t lb = prmt(t.L0, t.L1, s2), hb = prmt(t.H0, t.H1, s2);
+// Eight nibbles (n0 in the low bits) -> four BF16 pairs (n_i, n_{i+4}).  The
+// K order inside each group of eight is thereby permuted to
+// (n0 n4 n1 n5 n2 n6 n3 n7), identically for A and B, which leaves every dot
+// product unchanged and puts both elements of a pair at the same shift.
+__device__ __forceinline__ uint4 expand8(uint32_t w, uint32_t ss) {
+  constexpr uint32_t kMag = 0x01C001C0u, kSign = 0x80008000u, k2p100 = 0x71807180u;
   uint4 o;
-  o.x = prmt(la, ha, 0x6240u) | (shl_fma(w, 1u << 12) & 0x80008000u);   // (n0, n4)
-  o.y = prmt(la, ha, 0x7351u) | (shl_fma(w, 1u << 8) & 0x80008000u);    // (n1, n5)
-  o.z = prmt(lb, hb, 0x6240u) | (shl_fma(w, 1u << 4) & 0x80008000u);    // (n2, n6)
-  o.w = prmt(lb, hb, 0x7351u) | (w & 0x80008000u);                      // (n3, n7)
+  o.x = (shl_fma(w, 1u << 6) & kMag) | (shl_fma(w, 1u << 12) & kSign);   // (n0, n4)
+  o.y = (shl_fma(w, 1u << 2) & kMag) | (shl_fma(w, 1u << 8) & kSign);    // (n1, n5)
+  o.z = ((w >> 2) & kMag) | (shl_fma(w, 1u << 4) & kSign);               // (n2, n6)
+  o.w = ((w >> 6) & kMag) | (w & kSign);                                 // (n3, n7)
+  o.x = bmul2(bmul2(o.x, k2p100), ss);
+  o.y = bmul2(bmul2(o.y, k2p100), ss);
+  o.z = bmul2(bmul2(o.z, k2p100), ss);
+  o.w = bmul2(bmul2(o.w, k2p100), ss);
   return o;
 }
 
@@ -339,9 +334,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < kRowsPerThread; ++i) {
         const uint2 w = lds64(raw + i * 128 * (BK / 2));
-        const Lut lut = make_lut(c0[i], fmt);
-        const uint4 lo = expand8(w.x, lut);        // K 16*blk + 0..7
-        const uint4 hi = expand8(w.y, lut);        // K 16*blk + 8..15
+        const uint32_t ss = scale_pair(c0[i], fmt);
+        const uint4 lo = expand8(w.x, ss);         // K 16*blk + 0..7
+        const uint4 hi = expand8(w.y, ss);         // K 16*blk + 8..15
         const uint32_t row_addr = bf + i * 128 * 128;
         sts128(row_addr + c_lo, lo);
         sts128(row_addr + c_hi, hi);

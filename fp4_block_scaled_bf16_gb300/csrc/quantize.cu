@@ -101,17 +101,19 @@ __global__ void tensor_scale_kernel(const float* amax, float denom, float* out) 
 // One chunk = 8 consecutive elements (16 bytes of BF16) per lane; lanes 2k
 // and 2k+1 hold one block of 16.  The warp loop is uniform so that every
 // lane takes part in the shuffle; inactive lanes carry zeros.
+constexpr int kRowThreads = 512;
+
 template <bool SR, bool STATS>
-__global__ void __launch_bounds__(256) quantize_row_kernel(
+__global__ void __launch_bounds__(kRowThreads, 2) quantize_row_kernel(
     const uint4* __restrict__ in, int64_t nchunks, int fmt, const float* __restrict__ tscale,
     uint64_t seed, uint32_t* __restrict__ payload, uint8_t* __restrict__ scales, StatsDev* stats,
     float* amax_out, int* status) {
-  const float T = __ldg(tscale);
-  const float six_t = __fmul_rn(6.0f, T);
+  __shared__ ScaleTab tab;
+  build_scale_tab(&tab, __ldg(tscale), fmt);
   const int lane = threadIdx.x & 31;
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  constexpr int U = 2;  // chunks in flight per lane
+  constexpr int U = SR ? 2 : 4;  // chunks in flight per lane
   uint32_t tmax = 0, n_sat = 0, n_uflow = 0, n_clamp = 0, n_flush = 0;
 
   for (int64_t base = warp * 32 * U; base < nchunks; base += nwarps * 32 * U) {
@@ -128,7 +130,7 @@ __global__ void __launch_bounds__(256) quantize_row_kernel(
       uint32_t m = absmax16(w);
       m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
       tmax = max(tmax, m);
-      const BlockScale bs = block_scale(m, six_t, T, fmt);
+      const BlockScale bs = block_scale(m, tab);
       uint32_t rb[8];
       if (SR) {
         const uint4 a = sr_words4((uint64_t)g * 2, 0u, seed);
@@ -207,7 +209,8 @@ __global__ void __launch_bounds__(TileCfg<SR>::kThreads, TileCfg<SR>::kCtasPerSm
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  __syncthreads();
+  __shared__ ScaleTab tab;
+  build_scale_tab(&tab, __ldg(tscale), fmt);   // ends with __syncthreads
 
   uint32_t tmax = 0;
   uint32_t r_sat = 0, r_uflow = 0, r_clamp = 0, r_flush = 0;   // row-wise counters
@@ -231,8 +234,6 @@ __global__ void __launch_bounds__(TileCfg<SR>::kThreads, TileCfg<SR>::kCtasPerSm
   } else {
     // ------------------------------------------------ consumers
     // group g (warps 8g .. 8g+7) takes the CTA's tiles g, g + G, g + 2G, ...
-    const float T = __ldg(tscale);
-    const float six_t = __fmul_rn(6.0f, T);
     const int g = warp >> 3;
     const int tl_id = t & 255;          // thread index inside the group
     const int cg = tl_id & 15;
@@ -264,7 +265,7 @@ __global__ void __launch_bounds__(TileCfg<SR>::kThreads, TileCfg<SR>::kCtasPerSm
           m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
           const bool ok = row < rows && cg * 8 < cols;
           const int64_t e0 = (r0 + row) * C + c0 + cg * 8;  // logical index of the chunk
-          const BlockScale bs = block_scale(m, six_t, T, fmt);
+          const BlockScale bs = block_scale(m, tab);
           uint32_t rb[8];
           if (SR) {
             const uint4 a = sr_words4((uint64_t)e0 >> 2, 0u, seed);
@@ -301,7 +302,10 @@ __global__ void __launch_bounds__(TileCfg<SR>::kThreads, TileCfg<SR>::kCtasPerSm
         cw[2][p] = __byte_perm(a.y, b.y, 0x5410);
         cw[3][p] = __byte_perm(a.y, b.y, 0x7632);
       }
-      // the tile is in registers now: release the stage to the producer
+      // the tile is in registers now: release the stage to the producer.  The
+      // proxy fence orders these generic-proxy reads before the TMA (async
+      // proxy) write that will refill the stage.
+      fence_proxy_async();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_empty + 8 * s);
 
@@ -311,7 +315,7 @@ __global__ void __launch_bounds__(TileCfg<SR>::kThreads, TileCfg<SR>::kCtasPerSm
         const uint32_t w4a[4] = {cw[j][0], cw[j][1], cw[j][2], cw[j][3]};
         const uint32_t w4b[4] = {cw[j][4], cw[j][5], cw[j][6], cw[j][7]};
         const uint32_t cm = max(absmax16(w4a), absmax16(w4b));
-        const BlockScale bs = block_scale(cm, six_t, T, fmt);
+        const BlockScale bs = block_scale(cm, tab);
         rj[j] = bs.r;
         if (STATS && ok) {
           c_sat += bs.sat ? 1u : 0u;
@@ -420,7 +424,7 @@ cudaError_t launch_tensor_scale(const float* amax, float denom, float* out, cuda
 template <bool SR, bool STATS>
 static void row_launch(const QuantArgs& a, cudaStream_t st) {
   const int64_t nchunks = a.rows * a.cols / 8;
-  quantize_row_kernel<SR, STATS><<<grid_for(nchunks / 2, 256, 8), 256, 0, st>>>(
+  quantize_row_kernel<SR, STATS><<<grid_for(nchunks / 4, kRowThreads, 2), kRowThreads, 0, st>>>(
       static_cast<const uint4*>(a.in), nchunks, a.fmt, a.tscale, a.seed,
       reinterpret_cast<uint32_t*>(a.pay_row), a.sc_row, a.stats, a.amax_out, a.status);
 }
