@@ -324,21 +324,36 @@ __global__ void __launch_bounds__(TileCfg<SR>::kThreads, TileCfg<SR>::kCtasPerSm
         if (ok) sc_col[(c0 + q4 + j) * (R / 16) + (r0 + rb16) / 16] = (uint8_t)bs.code;
       }
       uint32_t nib[4][2] = {{0u, 0u}, {0u, 0u}, {0u, 0u}, {0u, 0u}};
-#pragma unroll
-      for (int p = 0; p < 8; ++p) {
-        uint4 wa = make_uint4(0, 0, 0, 0), wb = make_uint4(0, 0, 0, 0);
-        if (SR) {
-          const int64_t e = (r0 + rb16 + 2 * p) * C + c0 + q4;  // multiple of 4
-          wa = sr_words4((uint64_t)e >> 2, 1u, seed);
-          wb = sr_words4((uint64_t)(e + C) >> 2, 1u, seed);
-        }
-        const uint32_t ra[4] = {wa.x, wa.y, wa.z, wa.w}, rb_[4] = {wb.x, wb.y, wb.z, wb.w};
+      if (!SR) {
+        // round to nearest: each half column (8 rows, four BF16 pairs) is one
+        // eight-element conversion straight into a payload word
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          uint32_t c = 0, f = 0;
-          const uint32_t byte = quantize2<SR, STATS>(cw[j][p], rj[j], ra[j], rb_[j], &c, &f);
-          nib[j][p >> 2] |= byte << (8 * (p & 3));
-          if (STATS && ok) { c_clamp += c; c_flush += f; }
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t w4[4] = {cw[j][4 * h], cw[j][4 * h + 1], cw[j][4 * h + 2], cw[j][4 * h + 3]};
+            uint32_t c = 0, f = 0;
+            nib[j][h] = quantize8<false, STATS>(w4, rj[j], nullptr, &c, &f);
+            if (STATS && ok) { c_clamp += c; c_flush += f; }
+          }
+        }
+      } else {
+        // stochastic rounding: rows in pairs; one Philox block per row gives
+        // the words of its four columns (counter = logical index / 4, word =
+        // column offset)
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+          const int64_t e = (r0 + rb16 + 2 * p) * C + c0 + q4;  // multiple of 4
+          const uint4 wa = sr_words4((uint64_t)e >> 2, 1u, seed);
+          const uint4 wb = sr_words4((uint64_t)(e + C) >> 2, 1u, seed);
+          const uint32_t ra[4] = {wa.x, wa.y, wa.z, wa.w}, rb_[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t c = 0, f = 0;
+            const uint32_t byte = quantize2<true, STATS>(cw[j][p], rj[j], ra[j], rb_[j], &c, &f);
+            nib[j][p >> 2] |= byte << (8 * (p & 3));
+            if (STATS && ok) { c_clamp += c; c_flush += f; }
+          }
         }
       }
       if (ok) {

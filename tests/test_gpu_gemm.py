@@ -165,3 +165,25 @@ def test_full_dgrad_wgrad(lib):
     err = _sampled_check(lib, (qd.payload_col, qd.scales_col, qd.T), Xc, dW,
                          _stripes(16384, rng, 128), _stripes(4096, rng, 256))
     assert err <= GEMM_TOL, err
+
+
+@pytest.mark.parametrize("name", ["qkv", "down"])
+def test_linear_block_shapes(lib, name):
+    """8B-class block linears (qkv 4096->6144, down 16384->4096), 8192 tokens:
+    fprop, dgrad and wgrad through quantise + block-scaled GEMM with SR on
+    dY, sampled stripes against the oracle."""
+    X, W, dY = workloads.linear_block(name)
+    fin, fout = workloads.LINEARS[name]
+    Xr, Wr = quantised(X, lib), quantised(W, lib)
+    Xc, Wc = quantised(X, lib, axis=1), quantised(W, lib, axis=1)
+    qd = lib.quantize(to_dev(dY), 2, None, 0, 1, 7)
+    Dr = (qd.payload_row, qd.scales_row, qd.T)
+    Dc = (qd.payload_col, qd.scales_col, qd.T)
+    rng = np.random.default_rng(len(name))
+    for A, B, M, N in ((Xr, Wr, 8192, fout), (Dr, Wc, 8192, fin), (Dc, Xc, fout, fin)):
+        C = lib.gemm(*A, *B, dtype=torch.float32)
+        torch.cuda.synchronize()
+        assert C.shape == (M, N)
+        err = _sampled_check(lib, A, B, C, _stripes(M, rng, 128), _stripes(N, rng, 256))
+        assert err <= GEMM_TOL, (name, M, N, err)
+        del C
