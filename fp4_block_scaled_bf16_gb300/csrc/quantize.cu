@@ -169,21 +169,21 @@ __global__ void __launch_bounds__(kRowThreads, 2) quantize_row_kernel(
 //   column blocks: thread t quantises columns 4 (t % 32) .. +3 over rows
 //     16 (t / 32) .. +15 from 64-bit shared loads -- four column blocks, one
 //     Philox block per row for stochastic rounding, drawn row by row.
-// With stochastic rounding the kernel is bound by instruction latency rather
-// than memory, so two groups of eight consumer warps work on alternate tiles
-// (one CTA per SM); the round-to-nearest kernel runs one group, two CTAs per
-// SM.
+// Consumers are organised in groups of eight warps, each group taking every
+// G-th tile of the CTA (G = 3 groups for round-to-nearest, 2 for stochastic
+// rounding, whose registers allow fewer warps); one CTA per SM with a ring of
+// 2G stages, so that each group always has a tile landing while it works.
 constexpr int kTile = 128;
 constexpr int kQStageBytes = kTile * kTile * 2;
 constexpr long long kQWaitCycles = 4000000000LL;
 template <bool SR>
 struct TileCfg {
-  static constexpr int kGroups = SR ? 2 : 1;
-  static constexpr int kStages = SR ? 4 : 3;
+  static constexpr int kGroups = SR ? 2 : 3;
+  static constexpr int kStages = 2 * kGroups;
   static constexpr int kConsumerWarps = 8 * kGroups;
   static constexpr int kThreads = 32 * (kConsumerWarps + 1);
   static constexpr int kSmem = kStages * kQStageBytes + 16 * kStages + 128;
-  static constexpr int kCtasPerSm = SR ? 1 : 2;
+  static constexpr int kCtasPerSm = 1;
 };
 
 template <bool SR, bool STATS, bool DO_ROW>
@@ -253,12 +253,16 @@ __global__ void __launch_bounds__(TileCfg<SR>::kThreads, TileCfg<SR>::kCtasPerSm
       }
       const uint16_t(*tl)[kTile] = reinterpret_cast<const uint16_t(*)[kTile]>(qsm + s * kQStageBytes);
 
-      // row-wise blocks (and the tile's share of the tensor amax)
-#pragma unroll 2
+      // row-wise blocks (and the tile's share of the tensor amax); the eight
+      // chunk loads are issued before any of them is used
+      uint4 rv[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        rv[i] = *reinterpret_cast<const uint4*>(&tl[(tl_id >> 4) + 16 * i][cg * 8]);
+#pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int row = (tl_id >> 4) + 16 * i;
-        const uint4 v = *reinterpret_cast<const uint4*>(&tl[row][cg * 8]);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        const uint32_t w[4] = {rv[i].x, rv[i].y, rv[i].z, rv[i].w};
         uint32_t m = absmax16(w);
         tmax = max(tmax, m);
         if (DO_ROW) {
