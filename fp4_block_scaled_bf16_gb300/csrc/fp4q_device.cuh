@@ -130,16 +130,16 @@ __device__ __forceinline__ uint4 sr_words4(uint64_t ctr, uint32_t axis, uint64_t
 }
 
 // ---------------------------------------------------------------- one block
-// The block scale depends only on the block's amax -- a non-negative BF16
-// pattern a16 -- and the tensor scale T.  Per block the exact rule is
-//   code = encode(RN(bf16(a16) / RN(6 T))),  r = RN(1 / RN(decode(code) T)),
-// with encode monotone in a16.  A CTA therefore tabulates, once per tensor
-// scale, the smallest a16 reaching each code (found with the exact rule) and
-// r for each code; per block it derives an approximate code from one
-// multiply by 1/(6T) -- never off by more than one, because the binary32
-// error is far below the 1/16 relative spacing of the scale codes -- and
-// corrects it against two table entries.  The result is bit-identical to
-// the exact rule.
+// The exact rule for a block with amax a (a BF16 value) under tensor scale T:
+//   code = encode(RN(a / RN(6 T))),  r = RN(1 / RN(decode(code) T)).
+// Per block the kernels use a multiply by RN(1 / (6 T)) instead of the
+// division: the product differs from RN(a / (6 T)) by at most two binary32
+// ulps, so it rounds to the same code unless it lies within a few ulps of a
+// code's rounding midpoint (or of the largest scale, for the saturation
+// flag) -- then, rarely, the exact division is taken.  The binary32 image
+// of s * 2^-(127 - bias), shifted right by 20, is the scale code (subnormal
+// codes included), so "a few ulps from a midpoint" is a test on its low 20
+// bits.  The reciprocal r is tabulated per code once per CTA.
 struct BlockScale {
   uint32_t code;
   float r;        // 1 / (s T); 0 marks a zero scale (elements encode to signed zeros)
@@ -147,12 +147,13 @@ struct BlockScale {
 };
 
 struct ScaleTab {
-  uint32_t thr[256];   // thr[c]: smallest a16 with code >= c (c = 1..cmax); thr[0] = 0; 0xFFFF past cmax
   float recip[256];    // RN(1 / RN(s_c T)), 0 where s_c = 0
-  uint32_t thr_sat;    // smallest a16 whose s* exceeds the largest scale
-  uint32_t cmax;
-  float inv6t;         // RN(1 / RN(6 T)), for the approximate code
-  float unbias;        // 2^-(127 - bias): binary32 pattern of s * unbias, shifted by 20, is the code
+  float six_t;         // RN(6 T)
+  float inv6t;         // RN(1 / RN(6 T))
+  float unbias;        // 2^-(127 - bias)
+  float smax;          // largest finite scale
+  uint32_t cmax;       // its code
+  int fmt;
 };
 
 __device__ __forceinline__ uint32_t exact_code(uint32_t a16, float six_t, int fmt, bool* sat) {
@@ -161,44 +162,39 @@ __device__ __forceinline__ uint32_t exact_code(uint32_t a16, float six_t, int fm
 
 // Block-wide: every thread of the CTA calls it (it ends with __syncthreads).
 __device__ __forceinline__ void build_scale_tab(ScaleTab* tab, float T, int fmt) {
-  const float six_t = __fmul_rn(6.0f, T);
   const uint32_t cmax = (fmt == kUE5M3) ? 0xFEu : 0x7Eu;
   for (uint32_t c = threadIdx.x; c < 256; c += blockDim.x) {
     const float sc = decode_scale(c, fmt);
     tab->recip[c] = (sc == 0.0f || c > cmax) ? 0.0f : __frcp_rn(__fmul_rn(sc, T));
-    if (c == 0) { tab->thr[0] = 0; continue; }
-    if (c > cmax + 1) { tab->thr[c] = 0xFFFFu; continue; }
-    // smallest a16 in [0, 0x7F80] with exact_code >= c (or saturating, for
-    // c = cmax + 1); 0xFFFF when none
-    uint32_t lo = 0, hi = 0x7F81;
-    while (lo < hi) {
-      const uint32_t mid = (lo + hi) >> 1;
-      bool sat;
-      const uint32_t code = exact_code(mid, six_t, fmt, &sat);
-      const bool ge = (c <= cmax) ? (code >= c) : sat;
-      if (ge) hi = mid; else lo = mid + 1;
-    }
-    const uint32_t v = (lo > 0x7F80u) ? 0xFFFFu : lo;
-    if (c <= cmax) tab->thr[c] = v;
-    else { tab->thr_sat = v; tab->thr[c] = 0xFFFFu; }
   }
   if (threadIdx.x == 0) {
-    tab->cmax = cmax;
-    tab->inv6t = __frcp_rn(six_t);
+    tab->six_t = __fmul_rn(6.0f, T);
+    tab->inv6t = __frcp_rn(tab->six_t);
     tab->unbias = (fmt == kUE5M3) ? 0x1p-112f : 0x1p-120f;
+    tab->smax = scale_max(fmt);
+    tab->cmax = cmax;
+    tab->fmt = fmt;
   }
   __syncthreads();
 }
 
+__device__ __forceinline__ uint32_t exact_code_slow(uint32_t a16, const ScaleTab& tab, bool* sat) {
+  return exact_code(a16, tab.six_t, tab.fmt, sat);
+}
+
 __device__ __forceinline__ BlockScale block_scale(uint32_t a16, const ScaleTab& tab) {
   BlockScale bs;
-  const float sa = __fmul_rn(__fmul_rn(__uint_as_float(a16 << 16), tab.inv6t), tab.unbias);
-  uint32_t c = (__float_as_uint(sa) + 0x80000u) >> 20;
-  c = min(c, tab.cmax);
-  c = c - (a16 < tab.thr[c] ? 1u : 0u) + (a16 >= tab.thr[c + 1] ? 1u : 0u);
-  bs.code = c;
-  bs.r = tab.recip[c];
-  bs.sat = a16 >= tab.thr_sat;
+  const float sa = __fmul_rn(__uint_as_float(a16 << 16), tab.inv6t);
+  const uint32_t x = __float_as_uint(__fmul_rn(sa, tab.unbias));
+  const bool near_mid = ((x & 0xFFFFFu) - 0x7FFF8u) < 16u;                     // within 8 of the midpoint
+  const bool near_max = (__float_as_uint(sa) - __float_as_uint(tab.smax) + 8u) < 16u;
+  if (near_mid || near_max) {
+    bs.code = exact_code_slow(a16, tab, &bs.sat);
+  } else {
+    bs.code = min((x + 0x80000u) >> 20, tab.cmax);
+    bs.sat = sa > tab.smax;
+  }
+  bs.r = tab.recip[bs.code];
   return bs;
 }
 

@@ -16,9 +16,8 @@
 // CTA organisation (one CTA per SM, 256 x 256 output tile, K step 64; the
 // expansion is the costly part, so the tile is as large as TMEM allows: two
 // 128 x 256 FP32 accumulators fill all 512 columns):
-//   warp 16     producer: FP4 payload tiles (A and B, 256 x 32 B each) by
-//               TMA and the matching scale bytes by cp.async into a 4-stage
-//               raw ring (one barrier per stage tracks both).
+//   warp 16     TMA producer: FP4 payload tiles (A and B, 256 x 32 B each)
+//               into a 4-stage raw ring.
 //   warps 0..15 expand raw stages into a 2-stage BF16 ring laid out in the
 //               128-byte-swizzled K-major form the MMA descriptors read; each
 //               thread expands one 16-element block (one scale) at a time by
@@ -45,9 +44,7 @@ constexpr int UM = 128;                         // rows per MMA instruction
 constexpr int S_RAW = 4, S_BF = 2;
 constexpr int RAW_A = BM * BK / 2;             // 8192 B
 constexpr int RAW_B = BN * BK / 2;             // 8192 B
-constexpr int RAW_SC = (BM + BN) * (BK / 16);  // 2048 B: 4 scale bytes per row
-constexpr int RAW_TMA = RAW_A + RAW_B;
-constexpr int RAW_STAGE = RAW_TMA + RAW_SC;
+constexpr int RAW_STAGE = RAW_A + RAW_B;
 constexpr int BF_A = BM * BK * 2;              // 32768 B
 constexpr int BF_B = BN * BK * 2;              // 32768 B
 constexpr int BF_STAGE = BF_A + BF_B;
@@ -214,11 +211,6 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
                "r"(v.w)
                : "memory");
 }
-__device__ __forceinline__ uint32_t lds_u8(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
-}
 __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   uint2 v;
   asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
@@ -266,41 +258,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + OFF_TMEM);
 
   if (warp == kProducerWarp) {
-    // ------------------------------------------------ producer warp
-    // lane 0 streams the payload tiles with TMA; all 32 lanes copy the
-    // stage's scale bytes (4 per row, rows lane + 32 j) with cp.async, whose
-    // completion the same stage barrier tracks.  Rows past M or N read as 0.
-    const int64_t lds_k = K / 16;
-    for (int kb = 0; kb < nk; ++kb) {
-      const int s = kb % S_RAW;
-      // the warp decides together, so that no lane is left behind at the
-      // __syncwarp below when a wait gives up
-      const bool ok_wait = mbar_wait(bar_raw_empty + 8 * s, ((kb / S_RAW) & 1) ^ 1, abort_flag, budget);
-      if (!__all_sync(0xFFFFFFFFu, ok_wait)) {
-        if (lane == 0) fail(abort_flag, status);
-        break;
-      }
-      const uint32_t dst = sb + OFF_RAW + s * RAW_STAGE;
-      if (skip_loads) continue;   // test hook: consumers' waits run out
-#pragma unroll 4
-      for (int j = 0; j < (BM + BN) / 32; ++j) {
-        const int r = lane + 32 * j;
-        const int gr = (r < BM) ? m0 + r : n0 + (r - BM);
-        const bool ok = (r < BM) ? (gr < M) : (gr < N);
-        const uint8_t* src = ((r < BM) ? As : Bs) + (int64_t)(ok ? gr : 0) * lds_k + kb * 4;
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst + RAW_TMA + 4 * r),
-                     "l"(src), "r"(ok ? 4 : 0)
-                     : "memory");
-      }
-      asm volatile("cp.async.mbarrier.arrive.shared.b64 [%0];" ::"r"(bar_raw_full + 8 * s) : "memory");
-      __syncwarp();
-      if (lane == 0) {
-        mbar_expect_tx(bar_raw_full + 8 * s, RAW_TMA);
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % S_RAW;
+        if (!mbar_wait(bar_raw_empty + 8 * s, ((kb / S_RAW) & 1) ^ 1, abort_flag, budget)) {
+          fail(abort_flag, status);
+          break;
+        }
+        const uint32_t dst = sb + OFF_RAW + s * RAW_STAGE;
+        if (skip_loads) continue;   // test hook: consumers' waits run out
+        mbar_expect_tx(bar_raw_full + 8 * s, RAW_STAGE);
         tma_load_2d(dst, &mapA, kb * (BK / 2), m0, bar_raw_full + 8 * s);
         tma_load_2d(dst + RAW_A, &mapB, kb * (BK / 2), n0, bar_raw_full + 8 * s);
       }
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -331,29 +303,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x;
     const int blk = tid & 3;
     const int rbase = tid >> 2;
+    const int64_t lds_k = K / 16;
+    const uint8_t* srow[kRowsPerThread];
+    bool rok[kRowsPerThread];
+#pragma unroll
+    for (int i = 0; i < kRowsPerThread; ++i) {
+      const int r = rbase + 128 * i;
+      const int gr = (r < BM) ? m0 + r : n0 + (r - BM);
+      rok[i] = (r < BM) ? (gr < M) : (gr < N);
+      srow[i] = ((r < BM) ? As : Bs) + (int64_t)(rok[i] ? gr : 0) * lds_k + blk;
+    }
+    auto load_codes = [&](int kb, uint32_t (&c)[kRowsPerThread]) {
+#pragma unroll
+      for (int i = 0; i < kRowsPerThread; ++i) c[i] = (rok[i] && kb < nk) ? __ldg(srow[i] + kb * 4) : 0u;
+    };
     const uint32_t sw = rbase & 7;               // (rbase + 128 i) & 7
     const uint32_t c_lo = ((2 * blk) ^ sw) << 4, c_hi = ((2 * blk + 1) ^ sw) << 4;
     int s = 0, t = 0;
     uint32_t ph_s = 0, ph_t = 1;
-    for (int kb = 0; kb < nk; ++kb) {
+    // One K step: expand stage kb with the scale codes `cur`, and load the
+    // codes of step kb + 2 into `ahead` (three code arrays rotate, so each
+    // load has two steps of expansion to land and no register copy waits on it).
+    auto step = [&](int kb, const uint32_t (&cur)[kRowsPerThread], uint32_t (&ahead)[kRowsPerThread]) -> bool {
+      load_codes(kb + 2, ahead);
       if (!mbar_wait(bar_raw_full + 8 * s, ph_s, abort_flag, budget) ||
           !mbar_wait(bar_bf_empty + 8 * t, ph_t, abort_flag, budget)) {
         fail(abort_flag, status);
-        break;
+        return false;
       }
-      const uint32_t raw = sb + OFF_RAW + s * RAW_STAGE;
+      const uint32_t raw = sb + OFF_RAW + s * RAW_STAGE + rbase * (BK / 2) + blk * 8;
       const uint32_t bf = sb + OFF_BF + t * BF_STAGE + rbase * 128;
       uint2 w[kRowsPerThread];
-      uint32_t code[kRowsPerThread];
+#pragma unroll
+      for (int i = 0; i < kRowsPerThread; ++i) w[i] = lds64(raw + i * 128 * (BK / 2));
 #pragma unroll
       for (int i = 0; i < kRowsPerThread; ++i) {
-        const int r = rbase + 128 * i;
-        w[i] = lds64(raw + r * (BK / 2) + blk * 8);
-        code[i] = lds_u8(raw + RAW_TMA + 4 * r + blk);
-      }
-#pragma unroll
-      for (int i = 0; i < kRowsPerThread; ++i) {
-        const uint32_t ss = scale_pair(code[i], fmt);
+        const uint32_t ss = scale_pair(cur[i], fmt);
         const uint4 lo = expand8(w[i].x, ss);      // K 16*blk + 0..7
         const uint4 hi = expand8(w[i].y, ss);      // K 16*blk + 8..15
         const uint32_t row_addr = bf + i * 128 * 128;
@@ -368,6 +353,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (++s == S_RAW) { s = 0; ph_s ^= 1; }
       if (++t == S_BF) { t = 0; ph_t ^= 1; }
+      return true;
+    };
+    uint32_t cA[kRowsPerThread], cB[kRowsPerThread], cC[kRowsPerThread];
+    load_codes(0, cA);
+    load_codes(1, cB);
+    for (int kb = 0; kb < nk; kb += 3) {
+      if (!step(kb, cA, cC)) break;
+      if (kb + 1 >= nk || !step(kb + 1, cB, cA)) break;
+      if (kb + 2 >= nk || !step(kb + 2, cC, cB)) break;
     }
 
     // ------------------------------------------------ epilogue
