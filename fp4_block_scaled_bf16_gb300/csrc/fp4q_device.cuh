@@ -248,17 +248,14 @@ __device__ __forceinline__ uint32_t quantize8(const uint32_t w[4], float r, cons
   return nib;
 }
 
-// Two elements (one BF16 word: lo = element 0, hi = element 1) with
-// multiplier r and their random words -> one byte of two nibbles.
+// Two elements (one BF16 word: lo = element 0, hi = element 1), each with its
+// own multiplier and random word -> one byte of two nibbles (element 0 low).
 template <bool SR, bool STATS>
-__device__ __forceinline__ uint32_t quantize2(uint32_t pair, float r, uint32_t w0, uint32_t w1,
-                                              uint32_t* clamped, uint32_t* flushed) {
-  float q0, q1;
-  mul2(pair, r, q0, q1);
-  if (r == 0.0f) {
-    q0 = __uint_as_float((pair << 16) & 0x80000000u);
-    q1 = __uint_as_float(pair & 0x80000000u);
-  }
+__device__ __forceinline__ uint32_t quantize_pair(uint32_t pair, float r0, float r1, uint32_t w0,
+                                                  uint32_t w1, uint32_t* clamped, uint32_t* flushed) {
+  float q0 = __fmul_rn(bf16_lo(pair), r0), q1 = __fmul_rn(bf16_hi(pair), r1);
+  if (r0 == 0.0f) q0 = __uint_as_float((pair << 16) & 0x80000000u);
+  if (r1 == 0.0f) q1 = __uint_as_float(pair & 0x80000000u);
   if (STATS) *clamped += (fabsf(q0) > 6.0f ? 1u : 0u) + (fabsf(q1) > 6.0f ? 1u : 0u);
   if (SR) {
     q0 = __uint_as_float(__float_as_uint(sr_round_mag(fabsf(q0), w0)) | (__float_as_uint(q0) & 0x80000000u));

@@ -21,8 +21,8 @@
 //   warps 0..15 expand raw stages into a 2-stage BF16 ring laid out in the
 //               128-byte-swizzled K-major form the MMA descriptors read; each
 //               thread expands one 16-element block (one scale) at a time by
-//               placing nibble bits in BF16 patterns and one exact BF16
-//               multiply by the block scale;
+//               placing nibble bits in BF16 patterns and two exact BF16
+//               multiplies (the second by the block scale);
 //               after the main loop they run the epilogue (TMEM -> registers
 //               -> alpha -> BF16/FP32 -> global).
 //   warp 17     allocates TMEM; one lane issues 8 MMAs (2 x M128 N256 K16)
@@ -157,26 +157,22 @@ __device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
   return d;
 }
 
-// Expansion of E2M1 x UE5M3 to BF16 with one exact multiply per BF16 pair.
-// The nibble's three magnitude bits v placed at bits 6..8 of a BF16 pattern,
-// with its sign at bit 15, encode exactly +-E2M1(v) * 2^-126: the E2M1
-// exponent lands in the BF16 exponent field and the E2M1 subnormal (v = 1,
-// 0.5) lands on the BF16 subnormal 2^-127, so gradual underflow lines up.  One
-// exact multiply by s * 2^100 gives +-E2M1(v) * s * 2^-26 (at most 6
-// significant bits, within [2^-44, 2^-6.6], all normal).  Both operands carry
-// the 2^-26, so the FP32 accumulator holds C * 2^-52 -- every partial sum
-// stays a normal binary32 number and rounds exactly as C would -- and the
-// epilogue multiplies it back by 2^52 (exact) before the tensor scales.
-constexpr float kAccUnscale = 0x1p52f;
+// Expansion of E2M1 x UE5M3 to BF16 with the multiplies on the FP16/BF16
+// pipe.  The nibble's three magnitude bits v placed at bits 6..8 of a BF16
+// pattern, with its sign at bit 15, encode exactly +-E2M1(v) * 2^-126: the
+// E2M1 exponent lands in the BF16 exponent field and the E2M1 subnormal
+// (v = 1, 0.5) lands on the BF16 subnormal 2^-127, so gradual underflow lines
+// up.  Two exact multiplies -- by 2^100, then by s * 2^26 -- give +-E2M1(v) * s
+// (at most 6 significant bits, within [2^-18, 688128]); one multiply by
+// s * 2^126 would overflow BF16 for s >= 4.
 
-// (s * 2^100, s * 2^100) as a BF16 pair.  The scale code shifted into a
-// binary32 exponent/mantissa field is s * 2^-(127 - bias), subnormal codes
-// included.
+// (s * 2^26, s * 2^26) as a BF16 pair.  The scale code shifted into a binary32
+// exponent/mantissa field is s * 2^-(127 - bias), subnormal codes included.
 __device__ __forceinline__ uint32_t scale_pair(uint32_t code, int fmt) {
   const float s = __fmul_rn(__uint_as_float(code << 20), fmt == kUE5M3 ? 0x1p112f : 0x1p120f);
-  const float s100 = __fmul_rn(s, 0x1p100f);
+  const float s26 = __fmul_rn(s, 0x1p26f);
   uint32_t ss;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(ss) : "f"(s100));   // exact: <= 4 significant bits
+  asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(ss) : "f"(s26));   // exact: <= 4 significant bits
   return ss;
 }
 
@@ -193,16 +189,16 @@ __device__ __forceinline__ uint32_t shl_fma(uint32_t w, uint32_t pow2) {
 // (n0 n4 n1 n5 n2 n6 n3 n7), identically for A and B, which leaves every dot
 // product unchanged and puts both elements of a pair at the same shift.
 __device__ __forceinline__ uint4 expand8(uint32_t w, uint32_t ss) {
-  constexpr uint32_t kMag = 0x01C001C0u, kSign = 0x80008000u;
+  constexpr uint32_t kMag = 0x01C001C0u, kSign = 0x80008000u, k2p100 = 0x71807180u;
   uint4 o;
   o.x = (shl_fma(w, 1u << 6) & kMag) | (shl_fma(w, 1u << 12) & kSign);   // (n0, n4)
   o.y = (shl_fma(w, 1u << 2) & kMag) | (shl_fma(w, 1u << 8) & kSign);    // (n1, n5)
   o.z = ((w >> 2) & kMag) | (shl_fma(w, 1u << 4) & kSign);               // (n2, n6)
   o.w = ((w >> 6) & kMag) | (w & kSign);                                 // (n3, n7)
-  o.x = bmul2(o.x, ss);
-  o.y = bmul2(o.y, ss);
-  o.z = bmul2(o.z, ss);
-  o.w = bmul2(o.w, ss);
+  o.x = bmul2(bmul2(o.x, k2p100), ss);
+  o.y = bmul2(bmul2(o.y, k2p100), ss);
+  o.z = bmul2(bmul2(o.z, k2p100), ss);
+  o.w = bmul2(bmul2(o.w, k2p100), ss);
   return o;
 }
 
@@ -317,30 +313,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < kRowsPerThread; ++i) c[i] = (rok[i] && kb < nk) ? __ldg(srow[i] + kb * 4) : 0u;
     };
+    // scale codes are prefetched two K steps ahead (their L2 latency is
+    // longer than one step of expansion)
+    uint32_t c0[kRowsPerThread], c1[kRowsPerThread], c2[kRowsPerThread];
+    load_codes(0, c0);
+    load_codes(1, c1);
     const uint32_t sw = rbase & 7;               // (rbase + 128 i) & 7
     const uint32_t c_lo = ((2 * blk) ^ sw) << 4, c_hi = ((2 * blk + 1) ^ sw) << 4;
     int s = 0, t = 0;
     uint32_t ph_s = 0, ph_t = 1;
-    // One K step: expand stage kb with the scale codes `cur`, and load the
-    // codes of step kb + 2 into `ahead` (three code arrays rotate, so each
-    // load has two steps of expansion to land and no register copy waits on it).
-    auto step = [&](int kb, const uint32_t (&cur)[kRowsPerThread], uint32_t (&ahead)[kRowsPerThread]) -> bool {
-      load_codes(kb + 2, ahead);
+    for (int kb = 0; kb < nk; ++kb) {
+      load_codes(kb + 2, c2);
       if (!mbar_wait(bar_raw_full + 8 * s, ph_s, abort_flag, budget) ||
           !mbar_wait(bar_bf_empty + 8 * t, ph_t, abort_flag, budget)) {
         fail(abort_flag, status);
-        return false;
+        break;
       }
       const uint32_t raw = sb + OFF_RAW + s * RAW_STAGE + rbase * (BK / 2) + blk * 8;
       const uint32_t bf = sb + OFF_BF + t * BF_STAGE + rbase * 128;
-      uint2 w[kRowsPerThread];
-#pragma unroll
-      for (int i = 0; i < kRowsPerThread; ++i) w[i] = lds64(raw + i * 128 * (BK / 2));
 #pragma unroll
       for (int i = 0; i < kRowsPerThread; ++i) {
-        const uint32_t ss = scale_pair(cur[i], fmt);
-        const uint4 lo = expand8(w[i].x, ss);      // K 16*blk + 0..7
-        const uint4 hi = expand8(w[i].y, ss);      // K 16*blk + 8..15
+        const uint2 w = lds64(raw + i * 128 * (BK / 2));
+        const uint32_t ss = scale_pair(c0[i], fmt);
+        const uint4 lo = expand8(w.x, ss);         // K 16*blk + 0..7
+        const uint4 hi = expand8(w.y, ss);         // K 16*blk + 8..15
         const uint32_t row_addr = bf + i * 128 * 128;
         sts128(row_addr + c_lo, lo);
         sts128(row_addr + c_hi, hi);
@@ -351,17 +347,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(bar_bf_full + 8 * t);
         mbar_arrive(bar_raw_empty + 8 * s);
       }
+#pragma unroll
+      for (int i = 0; i < kRowsPerThread; ++i) { c0[i] = c1[i]; c1[i] = c2[i]; }
       if (++s == S_RAW) { s = 0; ph_s ^= 1; }
       if (++t == S_BF) { t = 0; ph_t ^= 1; }
-      return true;
-    };
-    uint32_t cA[kRowsPerThread], cB[kRowsPerThread], cC[kRowsPerThread];
-    load_codes(0, cA);
-    load_codes(1, cB);
-    for (int kb = 0; kb < nk; kb += 3) {
-      if (!step(kb, cA, cC)) break;
-      if (kb + 1 >= nk || !step(kb + 1, cB, cA)) break;
-      if (kb + 2 >= nk || !step(kb + 2, cC, cB)) break;
     }
 
     // ------------------------------------------------ epilogue
@@ -381,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (row >= M || col0 >= N) continue;
         float v[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(__fmul_rn(__uint_as_float(r[j]), kAccUnscale), alpha);
+        for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(__uint_as_float(r[j]), alpha);
         if (F32OUT) {
           float* o = static_cast<float*>(out) + (int64_t)row * N + col0;
           if (vec && col0 + 32 <= N) {

@@ -7,14 +7,12 @@
 // refreshed FP32 tensor scale; stochastic rounding on backward gradients.
 //
 // Design (GB300): every kernel streams BF16 with 128-bit coalesced loads that
-// bypass L1, keeps blocks in registers, and is launched as a grid-stride loop
-// sized to a multiple of the SM count.  The row-wise quantiser treats the
+// bypass L1 and keeps blocks in registers.  The row-wise quantiser treats the
 // tensor as flat (a block never straddles a row), so that one warp covers 256
 // consecutive elements and a lane pair shares one block (one shuffle for the
-// block amax).  The column-wise quantiser reads 128 x 128 tiles coalesced,
-// quantises the row-wise blocks straight from registers when both axes are
-// asked for, transposes through shared memory and quantises 16-row column
-// blocks from there.
+// block amax).  The column-wise / dual-axis quantiser gives each thread a
+// 16-row x 8-column piece, which holds eight whole column blocks and half of
+// sixteen row blocks, so that neither axis needs shared memory.
 #include "fp4q_device.cuh"
 #include "fp4q_launch.h"
 #include "fp4q_pipeline.cuh"
@@ -159,6 +157,154 @@ __global__ void __launch_bounds__(kRowThreads, 2) quantize_row_kernel(
 }
 
 // ---------------------------------------------------------------- tiles
+// Column-wise and dual-axis quantisation, register-resident.  A CTA covers
+// 128 rows x 256 columns: warp w takes rows 16 w .. +15 and lane l columns
+// 8 l .. +7, loading its 16 x 8 BF16 block with sixteen coalesced 128-bit
+// loads (every load instruction of a warp reads one 512-byte row segment).
+//   row blocks (dual axis): lanes 2k and 2k+1 hold the 16 columns of a
+//     block for each of the 16 rows (one shuffle per row for the amax); each
+//     lane converts its eight elements per row into one payload word;
+//   column blocks: a thread owns 8 complete column blocks (16 rows each);
+//     BF16 pairs of consecutive rows are gathered with byte permutes and
+//     converted eight at a time.  The eight warps of a CTA write the eight
+//     16-row pieces of each column's payload side by side (64 contiguous
+//     bytes per column).
+// Stochastic rounding draws one Philox block per row per four columns for
+// each axis.  Nothing goes through shared memory.
+constexpr int kRcRows = 128, kRcCols = 256, kRcThreads = 256;
+
+template <bool SR, bool STATS, bool DO_ROW>
+__global__ void __launch_bounds__(kRcThreads, 2) quantize_tile_kernel(
+    const uint16_t* __restrict__ in, int64_t R, int64_t C, int fmt,
+    const float* __restrict__ tscale, uint64_t seed, uint32_t* __restrict__ pay_row,
+    uint8_t* __restrict__ sc_row, uint8_t* __restrict__ pay_col, uint8_t* __restrict__ sc_col,
+    StatsDev* stats, float* amax_out, int* status) {
+  __shared__ ScaleTab tab;
+  build_scale_tab(&tab, __ldg(tscale), fmt);
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int64_t r0 = (int64_t)blockIdx.y * kRcRows + warp * 16;
+  const int64_t c0 = (int64_t)blockIdx.x * kRcCols + lane * 8;
+  const bool ok = r0 < R && c0 < C;   // sizes are multiples of 16: whole 16 x 8 pieces
+  uint32_t tmax = 0;
+  uint32_t r_sat = 0, r_uflow = 0, r_clamp = 0, r_flush = 0;
+  uint32_t c_sat = 0, c_uflow = 0, c_clamp = 0, c_flush = 0;
+
+  uint4 v[16];
+#pragma unroll
+  for (int rr = 0; rr < 16; ++rr)
+    v[rr] = ok ? ld_stream_v4(in + (r0 + rr) * C + c0) : make_uint4(0, 0, 0, 0);
+
+  // ---- row blocks
+#pragma unroll
+  for (int rr = 0; rr < 16; ++rr) {
+    const uint32_t w[4] = {v[rr].x, v[rr].y, v[rr].z, v[rr].w};
+    uint32_t m = absmax16(w);
+    tmax = max(tmax, m);
+    if (DO_ROW) {
+      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+      const int64_t e0 = (r0 + rr) * C + c0;  // logical index of the eight elements
+      const BlockScale bs = block_scale(m, tab);
+      uint32_t rb[8];
+      if (SR) {
+        const uint4 a = sr_words4((uint64_t)e0 >> 2, 0u, seed);
+        const uint4 b = sr_words4(((uint64_t)e0 >> 2) + 1, 0u, seed);
+        rb[0] = a.x; rb[1] = a.y; rb[2] = a.z; rb[3] = a.w;
+        rb[4] = b.x; rb[5] = b.y; rb[6] = b.z; rb[7] = b.w;
+      }
+      uint32_t c = 0, f = 0;
+      const uint32_t nib = quantize8<SR, STATS>(w, bs.r, rb, &c, &f);
+      if (ok) {
+        st_stream_u32(pay_row + (e0 >> 3), nib);
+        if ((lane & 1) == 0) sc_row[e0 >> 4] = (uint8_t)bs.code;
+        if (STATS) {
+          r_clamp += c;
+          r_flush += f;
+          if ((lane & 1) == 0) {
+            r_sat += bs.sat ? 1u : 0u;
+            r_uflow += (m != 0u && bs.code == 0u) ? 1u : 0u;
+          }
+        }
+      }
+    }
+  }
+
+  // ---- column blocks: scales of the eight columns first
+  float rj[8];
+#pragma unroll
+  for (int jp = 0; jp < 4; ++jp) {
+    uint32_t cw[2][8];   // [column][row pair p] = BF16 of rows 2p (low), 2p+1 (high)
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+      const uint32_t a = jp == 0 ? v[2 * p].x : jp == 1 ? v[2 * p].y : jp == 2 ? v[2 * p].z : v[2 * p].w;
+      const uint32_t b = jp == 0 ? v[2 * p + 1].x : jp == 1 ? v[2 * p + 1].y : jp == 2 ? v[2 * p + 1].z : v[2 * p + 1].w;
+      cw[0][p] = __byte_perm(a, b, 0x5410);
+      cw[1][p] = __byte_perm(a, b, 0x7632);
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int j = 2 * jp + h;   // column offset within the lane's eight
+      const uint32_t w4a[4] = {cw[h][0], cw[h][1], cw[h][2], cw[h][3]};
+      const uint32_t w4b[4] = {cw[h][4], cw[h][5], cw[h][6], cw[h][7]};
+      const uint32_t cm = max(absmax16(w4a), absmax16(w4b));
+      const BlockScale bs = block_scale(cm, tab);
+      rj[j] = bs.r;
+      if (ok) {
+        sc_col[(c0 + j) * (R / 16) + r0 / 16] = (uint8_t)bs.code;
+        if (STATS) {
+          c_sat += bs.sat ? 1u : 0u;
+          c_uflow += (cm != 0u && bs.code == 0u) ? 1u : 0u;
+        }
+      }
+      if (!SR) {
+        // round to nearest: eight rows of one column per conversion
+        uint32_t c = 0, f = 0;
+        const uint32_t nib0 = quantize8<false, STATS>(w4a, bs.r, nullptr, &c, &f);
+        const uint32_t nib1 = quantize8<false, STATS>(w4b, bs.r, nullptr, &c, &f);
+        if (ok) {
+          *reinterpret_cast<uint2*>(pay_col + (c0 + j) * (R / 2) + r0 / 2) = make_uint2(nib0, nib1);
+          if (STATS) { c_clamp += c; c_flush += f; }
+        }
+      }
+    }
+  }
+  if (SR) {
+    // stochastic rounding, row by row: one Philox block per row and four
+    // columns gives the column-axis words of the row's eight elements
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      uint32_t nibw[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int rr = 8 * hh + k;
+        const uint64_t e = (uint64_t)((r0 + rr) * C + c0) >> 2;
+        const uint4 x0 = sr_words4(e, 1u, seed), x1 = sr_words4(e + 1, 1u, seed);
+        const uint32_t wd[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        const uint32_t vw[4] = {v[rr].x, v[rr].y, v[rr].z, v[rr].w};
+#pragma unroll
+        for (int jp = 0; jp < 4; ++jp) {
+          uint32_t c = 0, f = 0;
+          const uint32_t byte = quantize_pair<true, STATS>(vw[jp], rj[2 * jp], rj[2 * jp + 1],
+                                                          wd[2 * jp], wd[2 * jp + 1], &c, &f);
+          nibw[2 * jp] |= (byte & 15u) << (4 * k);
+          nibw[2 * jp + 1] |= (byte >> 4) << (4 * k);
+          if (STATS && ok) { c_clamp += c; c_flush += f; }
+        }
+      }
+      if (ok) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<uint32_t*>(pay_col + (c0 + j) * (R / 2) + r0 / 2 + 4 * hh) = nibw[j];
+      }
+    }
+  }
+  if (STATS) {
+    if (DO_ROW) flush_stats(stats, r_sat, r_uflow, r_clamp, r_flush);
+    flush_stats(stats + (DO_ROW ? 1 : 0), c_sat, c_uflow, c_clamp, c_flush);
+  }
+  flush_amax(amax_out, status, tmax);
+}
+
+// ---------------------------------------------------------------- tiles, stochastic rounding
 // Column-wise and dual-axis quantisation.  A persistent CTA walks 128 x 128
 // tiles (ragged edges read as zero and are masked on output; sizes are
 // multiples of 16).  Warp 8 streams tiles with 2-D TMA into a 3-stage
@@ -187,7 +333,7 @@ struct TileCfg {
 };
 
 template <bool SR, bool STATS, bool DO_ROW>
-__global__ void __launch_bounds__(TileCfg<SR>::kThreads, TileCfg<SR>::kCtasPerSm) quantize_tile_kernel(
+__global__ void __launch_bounds__(TileCfg<SR>::kThreads, TileCfg<SR>::kCtasPerSm) quantize_tile_sr_kernel(
     const __grid_constant__ CUtensorMap map, int64_t R, int64_t C, int fmt,
     const float* __restrict__ tscale, uint64_t seed, uint32_t* __restrict__ pay_row,
     uint8_t* __restrict__ sc_row, uint8_t* __restrict__ pay_col, uint8_t* __restrict__ sc_col,
@@ -354,7 +500,7 @@ __global__ void __launch_bounds__(TileCfg<SR>::kThreads, TileCfg<SR>::kCtasPerSm
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             uint32_t c = 0, f = 0;
-            const uint32_t byte = quantize2<true, STATS>(cw[j][p], rj[j], ra[j], rb_[j], &c, &f);
+            const uint32_t byte = quantize_pair<true, STATS>(cw[j][p], rj[j], rj[j], ra[j], rb_[j], &c, &f);
             nib[j][p >> 2] |= byte << (8 * (p & 3));
             if (STATS && ok) { c_clamp += c; c_flush += f; }
           }
@@ -450,6 +596,16 @@ static void row_launch(const QuantArgs& a, cudaStream_t st) {
 
 template <bool SR, bool STATS, bool DO_ROW>
 static cudaError_t tile_launch(const QuantArgs& a, cudaStream_t st) {
+  dim3 grid((unsigned)((a.cols + kRcCols - 1) / kRcCols), (unsigned)((a.rows + kRcRows - 1) / kRcRows));
+  quantize_tile_kernel<SR, STATS, DO_ROW><<<grid, kRcThreads, 0, st>>>(
+      static_cast<const uint16_t*>(a.in), a.rows, a.cols, a.fmt, a.tscale, a.seed,
+      reinterpret_cast<uint32_t*>(a.pay_row), a.sc_row, a.pay_col, a.sc_col, a.stats, a.amax_out,
+      a.status);
+  return cudaGetLastError();
+}
+
+template <bool SR, bool STATS, bool DO_ROW>
+static cudaError_t tile_sr_launch(const QuantArgs& a, cudaStream_t st) {
   auto fn = get_encode_fn();
   if (!fn) return cudaErrorNotSupported;
   CUtensorMap map;
@@ -462,7 +618,7 @@ static cudaError_t tile_launch(const QuantArgs& a, cudaStream_t st) {
          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   using Cfg = TileCfg<SR>;
-  auto kern = quantize_tile_kernel<SR, STATS, DO_ROW>;
+  auto kern = quantize_tile_sr_kernel<SR, STATS, DO_ROW>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
   if (e != cudaSuccess) return e;
   const int64_t tiles = ((a.cols + kTile - 1) / kTile) * ((a.rows + kTile - 1) / kTile);
@@ -494,11 +650,14 @@ cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t st) {
     else stats ? row_launch<false, true>(a, st) : row_launch<false, false>(a, st);
     return cudaGetLastError();
   }
+  // stochastic rounding keeps the TMA-fed tile ring (its Philox work needs the
+  // warps that a shared-memory tile lets it spread over); round-to-nearest
+  // runs register-resident
   if (a.axis == 1) {
-    if (sr) return stats ? tile_launch<true, true, false>(a, st) : tile_launch<true, false, false>(a, st);
+    if (sr) return stats ? tile_sr_launch<true, true, false>(a, st) : tile_sr_launch<true, false, false>(a, st);
     return stats ? tile_launch<false, true, false>(a, st) : tile_launch<false, false, false>(a, st);
   }
-  if (sr) return stats ? tile_launch<true, true, true>(a, st) : tile_launch<true, false, true>(a, st);
+  if (sr) return stats ? tile_sr_launch<true, true, true>(a, st) : tile_sr_launch<true, false, true>(a, st);
   return stats ? tile_launch<false, true, true>(a, st) : tile_launch<false, false, true>(a, st);
 }
 
