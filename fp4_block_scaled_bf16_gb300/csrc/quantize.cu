@@ -158,23 +158,24 @@ __global__ void __launch_bounds__(kRowThreads, 2) quantize_row_kernel(
 
 // ---------------------------------------------------------------- tiles
 // Column-wise and dual-axis quantisation, register-resident.  A CTA covers
-// 128 rows x 256 columns: warp w takes rows 16 w .. +15 and lane l columns
-// 8 l .. +7, loading its 16 x 8 BF16 block with sixteen coalesced 128-bit
-// loads (every load instruction of a warp reads one 512-byte row segment).
-//   row blocks (dual axis): lanes 2k and 2k+1 hold the 16 columns of a
-//     block for each of the 16 rows (one shuffle per row for the amax); each
-//     lane converts its eight elements per row into one payload word;
-//   column blocks: a thread owns 8 complete column blocks (16 rows each);
+// 128 rows x 128 columns: warp w takes rows 16 w .. +15 and lane l columns
+// 4 l .. +3, loading its 16 x 4 BF16 piece with sixteen coalesced 64-bit
+// loads (each load instruction of a warp reads one 256-byte row segment).
+//   row blocks (dual axis): four consecutive lanes hold the 16 columns of a
+//     block (two shuffles per row for its amax); each lane converts its four
+//     elements of the row into two payload bytes;
+//   column blocks: a thread owns 4 complete column blocks (16 rows each);
 //     BF16 pairs of consecutive rows are gathered with byte permutes and
 //     converted eight at a time.  The eight warps of a CTA write the eight
 //     16-row pieces of each column's payload side by side (64 contiguous
 //     bytes per column).
-// Stochastic rounding draws one Philox block per row per four columns for
-// each axis.  Nothing goes through shared memory.
-constexpr int kRcRows = 128, kRcCols = 256, kRcThreads = 256;
+// Stochastic rounding draws one Philox block per row and axis: the four
+// words of counter (row C + 4 l) / 4 are exactly the thread's four elements.
+// Nothing goes through shared memory except the block-scale reciprocals.
+constexpr int kRcRows = 128, kRcCols = 128, kRcThreads = 256;
 
 template <bool SR, bool STATS, bool DO_ROW>
-__global__ void __launch_bounds__(kRcThreads, 2) quantize_tile_kernel(
+__global__ void __launch_bounds__(kRcThreads, 3) quantize_tile_kernel(
     const uint16_t* __restrict__ in, int64_t R, int64_t C, int fmt,
     const float* __restrict__ tscale, uint64_t seed, uint32_t* __restrict__ pay_row,
     uint8_t* __restrict__ sc_row, uint8_t* __restrict__ pay_col, uint8_t* __restrict__ sc_col,
@@ -183,43 +184,50 @@ __global__ void __launch_bounds__(kRcThreads, 2) quantize_tile_kernel(
   build_scale_tab(&tab, __ldg(tscale), fmt);
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int64_t r0 = (int64_t)blockIdx.y * kRcRows + warp * 16;
-  const int64_t c0 = (int64_t)blockIdx.x * kRcCols + lane * 8;
-  const bool ok = r0 < R && c0 < C;   // sizes are multiples of 16: whole 16 x 8 pieces
+  const int64_t c0 = (int64_t)blockIdx.x * kRcCols + lane * 4;
+  // sizes are multiples of 16, so a 16-column block is either wholly inside
+  // or wholly outside, and so is each 16 x 4 piece
+  const bool ok = r0 < R && c0 < C;
   uint32_t tmax = 0;
   uint32_t r_sat = 0, r_uflow = 0, r_clamp = 0, r_flush = 0;
   uint32_t c_sat = 0, c_uflow = 0, c_clamp = 0, c_flush = 0;
 
-  uint4 v[16];
+  uint2 v[16];
 #pragma unroll
-  for (int rr = 0; rr < 16; ++rr)
-    v[rr] = ok ? ld_stream_v4(in + (r0 + rr) * C + c0) : make_uint4(0, 0, 0, 0);
+  for (int rr = 0; rr < 16; ++rr) {
+    if (ok) {
+      asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
+                   : "=r"(v[rr].x), "=r"(v[rr].y) : "l"(in + (r0 + rr) * C + c0));
+    } else {
+      v[rr] = make_uint2(0, 0);
+    }
+  }
 
   // ---- row blocks
 #pragma unroll
   for (int rr = 0; rr < 16; ++rr) {
-    const uint32_t w[4] = {v[rr].x, v[rr].y, v[rr].z, v[rr].w};
-    uint32_t m = absmax16(w);
+    const uint32_t w[2] = {v[rr].x, v[rr].y};
+    uint32_t m = __vmaxu2(w[0] & 0x7FFF7FFFu, w[1] & 0x7FFF7FFFu);
+    m = max(m & 0xFFFFu, m >> 16);
     tmax = max(tmax, m);
     if (DO_ROW) {
       m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-      const int64_t e0 = (r0 + rr) * C + c0;  // logical index of the eight elements
+      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+      const int64_t e0 = (r0 + rr) * C + c0;  // logical index of the four elements
       const BlockScale bs = block_scale(m, tab);
-      uint32_t rb[8];
-      if (SR) {
-        const uint4 a = sr_words4((uint64_t)e0 >> 2, 0u, seed);
-        const uint4 b = sr_words4(((uint64_t)e0 >> 2) + 1, 0u, seed);
-        rb[0] = a.x; rb[1] = a.y; rb[2] = a.z; rb[3] = a.w;
-        rb[4] = b.x; rb[5] = b.y; rb[6] = b.z; rb[7] = b.w;
-      }
+      uint4 rw = make_uint4(0, 0, 0, 0);
+      if (SR) rw = sr_words4((uint64_t)e0 >> 2, 0u, seed);
       uint32_t c = 0, f = 0;
-      const uint32_t nib = quantize8<SR, STATS>(w, bs.r, rb, &c, &f);
+      const uint32_t b0 = quantize_pair<SR, STATS>(w[0], bs.r, bs.r, rw.x, rw.y, &c, &f);
+      const uint32_t b1 = quantize_pair<SR, STATS>(w[1], bs.r, bs.r, rw.z, rw.w, &c, &f);
       if (ok) {
-        st_stream_u32(pay_row + (e0 >> 3), nib);
-        if ((lane & 1) == 0) sc_row[e0 >> 4] = (uint8_t)bs.code;
+        *reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(pay_row) + (e0 >> 1)) =
+            (uint16_t)(b0 | (b1 << 8));
+        if ((lane & 3) == 0) sc_row[e0 >> 4] = (uint8_t)bs.code;
         if (STATS) {
           r_clamp += c;
           r_flush += f;
-          if ((lane & 1) == 0) {
+          if ((lane & 3) == 0) {
             r_sat += bs.sat ? 1u : 0u;
             r_uflow += (m != 0u && bs.code == 0u) ? 1u : 0u;
           }
@@ -228,73 +236,62 @@ __global__ void __launch_bounds__(kRcThreads, 2) quantize_tile_kernel(
     }
   }
 
-  // ---- column blocks: scales of the eight columns first
-  float rj[8];
+  // ---- column blocks
+  uint32_t cw[4][8];   // [column j][row pair p] = BF16 of rows 2p (low), 2p+1 (high)
 #pragma unroll
-  for (int jp = 0; jp < 4; ++jp) {
-    uint32_t cw[2][8];   // [column][row pair p] = BF16 of rows 2p (low), 2p+1 (high)
+  for (int p = 0; p < 8; ++p) {
+    cw[0][p] = __byte_perm(v[2 * p].x, v[2 * p + 1].x, 0x5410);
+    cw[1][p] = __byte_perm(v[2 * p].x, v[2 * p + 1].x, 0x7632);
+    cw[2][p] = __byte_perm(v[2 * p].y, v[2 * p + 1].y, 0x5410);
+    cw[3][p] = __byte_perm(v[2 * p].y, v[2 * p + 1].y, 0x7632);
+  }
+  float rj[4];
 #pragma unroll
-    for (int p = 0; p < 8; ++p) {
-      const uint32_t a = jp == 0 ? v[2 * p].x : jp == 1 ? v[2 * p].y : jp == 2 ? v[2 * p].z : v[2 * p].w;
-      const uint32_t b = jp == 0 ? v[2 * p + 1].x : jp == 1 ? v[2 * p + 1].y : jp == 2 ? v[2 * p + 1].z : v[2 * p + 1].w;
-      cw[0][p] = __byte_perm(a, b, 0x5410);
-      cw[1][p] = __byte_perm(a, b, 0x7632);
-    }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int j = 2 * jp + h;   // column offset within the lane's eight
-      const uint32_t w4a[4] = {cw[h][0], cw[h][1], cw[h][2], cw[h][3]};
-      const uint32_t w4b[4] = {cw[h][4], cw[h][5], cw[h][6], cw[h][7]};
-      const uint32_t cm = max(absmax16(w4a), absmax16(w4b));
-      const BlockScale bs = block_scale(cm, tab);
-      rj[j] = bs.r;
-      if (ok) {
-        sc_col[(c0 + j) * (R / 16) + r0 / 16] = (uint8_t)bs.code;
-        if (STATS) {
-          c_sat += bs.sat ? 1u : 0u;
-          c_uflow += (cm != 0u && bs.code == 0u) ? 1u : 0u;
-        }
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t w4a[4] = {cw[j][0], cw[j][1], cw[j][2], cw[j][3]};
+    const uint32_t w4b[4] = {cw[j][4], cw[j][5], cw[j][6], cw[j][7]};
+    const uint32_t cm = max(absmax16(w4a), absmax16(w4b));
+    const BlockScale bs = block_scale(cm, tab);
+    rj[j] = bs.r;
+    if (ok) {
+      sc_col[(c0 + j) * (R / 16) + r0 / 16] = (uint8_t)bs.code;
+      if (STATS) {
+        c_sat += bs.sat ? 1u : 0u;
+        c_uflow += (cm != 0u && bs.code == 0u) ? 1u : 0u;
       }
-      if (!SR) {
-        // round to nearest: eight rows of one column per conversion
-        uint32_t c = 0, f = 0;
-        const uint32_t nib0 = quantize8<false, STATS>(w4a, bs.r, nullptr, &c, &f);
-        const uint32_t nib1 = quantize8<false, STATS>(w4b, bs.r, nullptr, &c, &f);
-        if (ok) {
-          *reinterpret_cast<uint2*>(pay_col + (c0 + j) * (R / 2) + r0 / 2) = make_uint2(nib0, nib1);
-          if (STATS) { c_clamp += c; c_flush += f; }
-        }
+    }
+    if (!SR) {
+      uint32_t c = 0, f = 0;
+      const uint32_t nib0 = quantize8<false, STATS>(w4a, bs.r, nullptr, &c, &f);
+      const uint32_t nib1 = quantize8<false, STATS>(w4b, bs.r, nullptr, &c, &f);
+      if (ok) {
+        *reinterpret_cast<uint2*>(pay_col + (c0 + j) * (R / 2) + r0 / 2) = make_uint2(nib0, nib1);
+        if (STATS) { c_clamp += c; c_flush += f; }
       }
     }
   }
   if (SR) {
-    // stochastic rounding, row by row: one Philox block per row and four
-    // columns gives the column-axis words of the row's eight elements
+    // one Philox block per row gives the column-axis words of its four
+    // elements (counter = logical index / 4, word = column offset)
+    uint32_t nib[4][2] = {{0u, 0u}, {0u, 0u}, {0u, 0u}, {0u, 0u}};
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      uint32_t nibw[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    for (int p = 0; p < 8; ++p) {
+      const uint64_t e = (uint64_t)((r0 + 2 * p) * C + c0) >> 2;
+      const uint4 wa = sr_words4(e, 1u, seed);
+      const uint4 wb = sr_words4(e + ((uint64_t)C >> 2), 1u, seed);
+      const uint32_t ra[4] = {wa.x, wa.y, wa.z, wa.w}, rb_[4] = {wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int rr = 8 * hh + k;
-        const uint64_t e = (uint64_t)((r0 + rr) * C + c0) >> 2;
-        const uint4 x0 = sr_words4(e, 1u, seed), x1 = sr_words4(e + 1, 1u, seed);
-        const uint32_t wd[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-        const uint32_t vw[4] = {v[rr].x, v[rr].y, v[rr].z, v[rr].w};
-#pragma unroll
-        for (int jp = 0; jp < 4; ++jp) {
-          uint32_t c = 0, f = 0;
-          const uint32_t byte = quantize_pair<true, STATS>(vw[jp], rj[2 * jp], rj[2 * jp + 1],
-                                                          wd[2 * jp], wd[2 * jp + 1], &c, &f);
-          nibw[2 * jp] |= (byte & 15u) << (4 * k);
-          nibw[2 * jp + 1] |= (byte >> 4) << (4 * k);
-          if (STATS && ok) { c_clamp += c; c_flush += f; }
-        }
+      for (int j = 0; j < 4; ++j) {
+        uint32_t c = 0, f = 0;
+        const uint32_t byte = quantize_pair<true, STATS>(cw[j][p], rj[j], rj[j], ra[j], rb_[j], &c, &f);
+        nib[j][p >> 2] |= byte << (8 * (p & 3));
+        if (STATS && ok) { c_clamp += c; c_flush += f; }
       }
-      if (ok) {
+    }
+    if (ok) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          *reinterpret_cast<uint32_t*>(pay_col + (c0 + j) * (R / 2) + r0 / 2 + 4 * hh) = nibw[j];
-      }
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint2*>(pay_col + (c0 + j) * (R / 2) + r0 / 2) = make_uint2(nib[j][0], nib[j][1]);
     }
   }
   if (STATS) {
@@ -650,14 +647,11 @@ cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t st) {
     else stats ? row_launch<false, true>(a, st) : row_launch<false, false>(a, st);
     return cudaGetLastError();
   }
-  // stochastic rounding keeps the TMA-fed tile ring (its Philox work needs the
-  // warps that a shared-memory tile lets it spread over); round-to-nearest
-  // runs register-resident
   if (a.axis == 1) {
-    if (sr) return stats ? tile_sr_launch<true, true, false>(a, st) : tile_sr_launch<true, false, false>(a, st);
+    if (sr) return stats ? tile_launch<true, true, false>(a, st) : tile_launch<true, false, false>(a, st);
     return stats ? tile_launch<false, true, false>(a, st) : tile_launch<false, false, false>(a, st);
   }
-  if (sr) return stats ? tile_sr_launch<true, true, true>(a, st) : tile_sr_launch<true, false, true>(a, st);
+  if (sr) return stats ? tile_launch<true, true, true>(a, st) : tile_launch<true, false, true>(a, st);
   return stats ? tile_launch<false, true, true>(a, st) : tile_launch<false, false, true>(a, st);
 }
 
