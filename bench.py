@@ -236,28 +236,53 @@ def run_gpu(args, rank, world):
     t_g = [seg(4, 5), seg(5, 6), seg(6, 7)]
     status = fp4q.fp4q_get_device_status()
 
-    # ---- end to end through the API with host buffers: H2D inputs, D2H results
-    hY = torch.empty(step.Y.shape, dtype=torch.bfloat16).pin_memory()
-    hdX = torch.empty(step.dX.shape, dtype=torch.bfloat16).pin_memory()
-    hdW = torch.empty(step.dW.shape, dtype=torch.bfloat16).pin_memory()
-    e2e_steps = max(1, min(args.steps, 5))
+    # ---- end to end through the API with host buffers: every step copies its
+    # inputs host -> device and its results device -> host.  Copies run on
+    # their own streams and overlap the previous/next step's kernels (two
+    # device buffer sets), which is how a training loop feeds the GPU.
+    hY = [torch.empty(step.Y.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    hdX = [torch.empty(step.dX.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    hdW = [torch.empty(step.dW.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    steps2 = [step, Step(torch, fp4q, torch.empty_like(X), torch.empty_like(W), torch.empty_like(dY))]
+    s_h2d, s_cmp, s_d2h = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    e2e_steps = max(2, min(args.steps, 6))
+    ev_in = [torch.cuda.Event() for _ in range(e2e_steps)]
+    ev_done = [torch.cuda.Event() for _ in range(e2e_steps)]
+    ev_out = [torch.cuda.Event() for _ in range(e2e_steps)]
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     s0 = torch.cuda.Event(enable_timing=True)
     s1 = torch.cuda.Event(enable_timing=True)
-    s0.record()
-    for _ in range(e2e_steps):
-        step.X.copy_(hX, non_blocking=True)
-        step.W.copy_(hW, non_blocking=True)
-        step.dY.copy_(hD, non_blocking=True)
-        step.run()
-        hY.copy_(step.Y, non_blocking=True)
-        hdX.copy_(step.dX, non_blocking=True)
-        hdW.copy_(step.dW, non_blocking=True)
-    s1.record()
+    s0.record(s_h2d)
+    for i in range(e2e_steps):
+        st_i = steps2[i % 2]
+        with torch.cuda.stream(s_h2d):
+            if i >= 2:
+                s_h2d.wait_event(ev_done[i - 2])          # buffer set free again
+            st_i.X.copy_(hX, non_blocking=True)
+            st_i.W.copy_(hW, non_blocking=True)
+            st_i.dY.copy_(hD, non_blocking=True)
+            ev_in[i].record(s_h2d)
+        with torch.cuda.stream(s_cmp):
+            s_cmp.wait_event(ev_in[i])
+            if i >= 2:
+                s_cmp.wait_event(ev_out[i - 2])          # outputs read back
+            st_i.run()
+            ev_done[i].record(s_cmp)
+        with torch.cuda.stream(s_d2h):
+            s_d2h.wait_event(ev_done[i])
+            hY[i % 2].copy_(st_i.Y, non_blocking=True)
+            hdX[i % 2].copy_(st_i.dX, non_blocking=True)
+            hdW[i % 2].copy_(st_i.dW, non_blocking=True)
+            ev_out[i].record(s_d2h)
+    s_h2d.wait_event(ev_out[e2e_steps - 1])
+    s1.record(s_h2d)
     torch.cuda.synchronize()
     e2e_ms = s0.elapsed_time(s1) / e2e_steps
+    h2d = (hX.numel() + hW.numel() + hD.numel()) * 2
+    d2h = (hY[0].numel() + hdX[0].numel() + hdW[0].numel()) * 2
+    del steps2
 
     # ---- single-axis quantiser rates (outside the step): W row-wise RNE and
     # dY row-wise SR, 10 launches each, inputs larger than L2
@@ -274,8 +299,6 @@ def run_gpu(args, rank, world):
         a1.record()
         torch.cuda.synchronize()
         rates[name] = x.numel() * ROW_BYTES_PER_ELEM / (a0.elapsed_time(a1) / 10 * 1e-3) / 1e9
-    h2d = (hX.numel() + hW.numel() + hD.numel()) * 2
-    d2h = (hY.numel() + hdX.numel() + hdW.numel()) * 2
     return dict(ms=ms, t_scale=t_scale, t_q=(t_qx, t_qw, t_qd), t_g=t_g, launches=launches, rates=rates,
                 clocks=clk.summary(), status=status, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
                 elems=(X.numel(), W.numel(), dY.numel()))

@@ -15,7 +15,6 @@
 // sixteen row blocks, so that neither axis needs shared memory.
 #include "fp4q_device.cuh"
 #include "fp4q_launch.h"
-#include "fp4q_pipeline.cuh"
 
 namespace fp4q {
 
@@ -158,6 +157,149 @@ __global__ void __launch_bounds__(kRowThreads, 2) quantize_row_kernel(
 
 // ---------------------------------------------------------------- tiles
 // Column-wise and dual-axis quantisation, register-resident.  A CTA covers
+// 128 rows x 128 columns; warp w takes rows 16 w .. +15.  Lane l holds an
+// 8 x 8 piece: rows 16 w + 8 (l / 16) .. +7, columns 8 (l % 16) .. +7, loaded
+// with eight 128-bit loads (each warp load reads two 256-byte row segments).
+//   row blocks (dual axis): lanes l and l ^ 1 hold the 16 columns of a block
+//     (one shuffle per row for its amax); a lane converts its eight elements
+//     of a row into one payload word;
+//   column blocks: lanes l and l ^ 16 hold the two 8-row halves of a
+//     column's 16-row block (one shuffle per column for its amax); a lane
+//     converts its eight rows of a column into one payload word, after
+//     gathering BF16 pairs of consecutive rows with byte permutes.
+// The eight warps of a CTA write the 16-row pieces of each column's payload
+// side by side (64 contiguous bytes).  Stochastic rounding draws one Philox
+// block per row and per four columns on each axis.  Nothing goes through
+// shared memory except the block-scale reciprocal table.
+constexpr int kRcRows = 128, kRcCols = 128, kRcThreads = 256;
+
+template <bool SR, bool STATS, bool DO_ROW>
+__global__ void __launch_bounds__(kRcThreads, 3) quantize_tile_kernel(
+    const uint16_t* __restrict__ in, int64_t R, int64_t C, int fmt,
+    const float* __restrict__ tscale, uint64_t seed, uint32_t* __restrict__ pay_row,
+    uint8_t* __restrict__ sc_row, uint8_t* __restrict__ pay_col, uint8_t* __restrict__ sc_col,
+    StatsDev* stats, float* amax_out, int* status) {
+  __shared__ ScaleTab tab;
+  build_scale_tab(&tab, __ldg(tscale), fmt);
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int half = lane >> 4, cg = lane & 15;
+  const int64_t rb = (int64_t)blockIdx.y * kRcRows + warp * 16;   // first row of the column block
+  const int64_t r0 = rb + 8 * half;                                 // first of this lane's 8 rows
+  const int64_t c0 = (int64_t)blockIdx.x * kRcCols + cg * 8;
+  // sizes are multiples of 16: a 16 x 16 region is wholly inside or outside
+  const bool ok = rb < R && c0 < C;
+  uint32_t tmax = 0;
+  uint32_t r_sat = 0, r_uflow = 0, r_clamp = 0, r_flush = 0;
+  uint32_t c_sat = 0, c_uflow = 0, c_clamp = 0, c_flush = 0;
+
+  uint4 v[8];
+#pragma unroll
+  for (int rr = 0; rr < 8; ++rr)
+    v[rr] = ok ? ld_stream_v4(in + (r0 + rr) * C + c0) : make_uint4(0, 0, 0, 0);
+
+  // ---- row blocks
+#pragma unroll
+  for (int rr = 0; rr < 8; ++rr) {
+    const uint32_t w[4] = {v[rr].x, v[rr].y, v[rr].z, v[rr].w};
+    uint32_t m = absmax16(w);
+    tmax = max(tmax, m);
+    if (DO_ROW) {
+      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+      const int64_t e0 = (r0 + rr) * C + c0;  // logical index of the eight elements
+      const BlockScale bs = block_scale(m, tab);
+      uint32_t rbits[8];
+      if (SR) {
+        const uint4 a = sr_words4((uint64_t)e0 >> 2, 0u, seed);
+        const uint4 b = sr_words4(((uint64_t)e0 >> 2) + 1, 0u, seed);
+        rbits[0] = a.x; rbits[1] = a.y; rbits[2] = a.z; rbits[3] = a.w;
+        rbits[4] = b.x; rbits[5] = b.y; rbits[6] = b.z; rbits[7] = b.w;
+      }
+      uint32_t c = 0, f = 0;
+      const uint32_t nib = quantize8<SR, STATS>(w, bs.r, rbits, &c, &f);
+      if (ok) {
+        st_stream_u32(pay_row + (e0 >> 3), nib);
+        if ((cg & 1) == 0) sc_row[e0 >> 4] = (uint8_t)bs.code;
+        if (STATS) {
+          r_clamp += c;
+          r_flush += f;
+          if ((cg & 1) == 0) {
+            r_sat += bs.sat ? 1u : 0u;
+            r_uflow += (m != 0u && bs.code == 0u) ? 1u : 0u;
+          }
+        }
+      }
+    }
+  }
+
+  // ---- column blocks: column j of the lane is BF16 word j / 2, half j % 2
+  float rj[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    uint32_t cw[4];   // BF16 of rows 2p (low) and 2p + 1 (high) of column j
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const uint4 a4 = v[2 * p], b4 = v[2 * p + 1];
+      const uint32_t a = (j >> 1) == 0 ? a4.x : (j >> 1) == 1 ? a4.y : (j >> 1) == 2 ? a4.z : a4.w;
+      const uint32_t b = (j >> 1) == 0 ? b4.x : (j >> 1) == 1 ? b4.y : (j >> 1) == 2 ? b4.z : b4.w;
+      cw[p] = __byte_perm(a, b, (j & 1) ? 0x7632 : 0x5410);
+    }
+    uint32_t cm = absmax16(cw);
+    cm = max(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, 16));
+    const BlockScale bs = block_scale(cm, tab);
+    rj[j] = bs.r;
+    if (ok && half == 0) {
+      sc_col[(c0 + j) * (R / 16) + rb / 16] = (uint8_t)bs.code;
+      if (STATS) {
+        c_sat += bs.sat ? 1u : 0u;
+        c_uflow += (cm != 0u && bs.code == 0u) ? 1u : 0u;
+      }
+    }
+    if (!SR) {
+      uint32_t c = 0, f = 0;
+      const uint32_t nib = quantize8<false, STATS>(cw, bs.r, nullptr, &c, &f);
+      if (ok) {
+        *reinterpret_cast<uint32_t*>(pay_col + (c0 + j) * (R / 2) + r0 / 2) = nib;
+        if (STATS) { c_clamp += c; c_flush += f; }
+      }
+    }
+  }
+  if (SR) {
+    // row by row: two Philox blocks give the column-axis words of the row's
+    // eight elements (counter = logical index / 4, word = column offset % 4)
+    uint32_t nib[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int rr = 0; rr < 8; ++rr) {
+      const uint64_t e = (uint64_t)((r0 + rr) * C + c0) >> 2;
+      const uint4 x0 = sr_words4(e, 1u, seed), x1 = sr_words4(e + 1, 1u, seed);
+      const uint32_t wd[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+      const uint32_t vw[4] = {v[rr].x, v[rr].y, v[rr].z, v[rr].w};
+#pragma unroll
+      for (int jp = 0; jp < 4; ++jp) {
+        uint32_t c = 0, f = 0;
+        const uint32_t byte = quantize_pair<true, STATS>(vw[jp], rj[2 * jp], rj[2 * jp + 1],
+                                                         wd[2 * jp], wd[2 * jp + 1], &c, &f);
+        nib[2 * jp] |= (byte & 15u) << (4 * rr);
+        nib[2 * jp + 1] |= (byte >> 4) << (4 * rr);
+        if (STATS && ok) { c_clamp += c; c_flush += f; }
+      }
+    }
+    if (ok) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<uint32_t*>(pay_col + (c0 + j) * (R / 2) + r0 / 2) = nib[j];
+    }
+  }
+  if (STATS) {
+    if (DO_ROW) flush_stats(stats, r_sat, r_uflow, r_clamp, r_flush);
+    flush_stats(stats + (DO_ROW ? 1 : 0), c_sat, c_uflow, c_clamp, c_flush);
+  }
+  flush_amax(amax_out, status, tmax);
+}
+
+// ---------------------------------------------------------------- tiles, 16 x 4 pieces
+// The stochastic-rounding variant of the tile quantiser: its Philox work per
+// row needs the registers that a narrower piece frees.
+// Column-wise and dual-axis quantisation, register-resident.  A CTA covers
 // 128 rows x 128 columns: warp w takes rows 16 w .. +15 and lane l columns
 // 4 l .. +3, loading its 16 x 4 BF16 piece with sixteen coalesced 64-bit
 // loads (each load instruction of a warp reads one 256-byte row segment).
@@ -172,10 +314,9 @@ __global__ void __launch_bounds__(kRowThreads, 2) quantize_row_kernel(
 // Stochastic rounding draws one Philox block per row and axis: the four
 // words of counter (row C + 4 l) / 4 are exactly the thread's four elements.
 // Nothing goes through shared memory except the block-scale reciprocals.
-constexpr int kRcRows = 128, kRcCols = 128, kRcThreads = 256;
 
 template <bool SR, bool STATS, bool DO_ROW>
-__global__ void __launch_bounds__(kRcThreads, 3) quantize_tile_kernel(
+__global__ void __launch_bounds__(kRcThreads, 3) quantize_tile4_kernel(
     const uint16_t* __restrict__ in, int64_t R, int64_t C, int fmt,
     const float* __restrict__ tscale, uint64_t seed, uint32_t* __restrict__ pay_row,
     uint8_t* __restrict__ sc_row, uint8_t* __restrict__ pay_col, uint8_t* __restrict__ sc_col,
@@ -301,223 +442,6 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile_kernel(
   flush_amax(amax_out, status, tmax);
 }
 
-// ---------------------------------------------------------------- tiles, stochastic rounding
-// Column-wise and dual-axis quantisation.  A persistent CTA walks 128 x 128
-// tiles (ragged edges read as zero and are masked on output; sizes are
-// multiples of 16).  Warp 8 streams tiles with 2-D TMA into a 3-stage
-// shared-memory ring; warps 0..7 consume them without any CTA-wide barrier:
-//   row blocks (dual axis only): thread t reads rows t/16 + 16 i (i = 0..7),
-//     columns 8 (t % 16) .. +7 with 128-bit shared loads; lanes 2k, 2k+1 hold
-//     one 16-element block (one shuffle for its amax);
-//   column blocks: thread t quantises columns 4 (t % 32) .. +3 over rows
-//     16 (t / 32) .. +15 from 64-bit shared loads -- four column blocks, one
-//     Philox block per row for stochastic rounding, drawn row by row.
-// Consumers are organised in groups of eight warps, each group taking every
-// G-th tile of the CTA (G = 3 groups for round-to-nearest, 2 for stochastic
-// rounding, whose registers allow fewer warps); one CTA per SM with a ring of
-// 2G stages, so that each group always has a tile landing while it works.
-constexpr int kTile = 128;
-constexpr int kQStageBytes = kTile * kTile * 2;
-constexpr long long kQWaitCycles = 4000000000LL;
-template <bool SR>
-struct TileCfg {
-  static constexpr int kGroups = SR ? 2 : 3;
-  static constexpr int kStages = 2 * kGroups;
-  static constexpr int kConsumerWarps = 8 * kGroups;
-  static constexpr int kThreads = 32 * (kConsumerWarps + 1);
-  static constexpr int kSmem = kStages * kQStageBytes + 16 * kStages + 128;
-  static constexpr int kCtasPerSm = 1;
-};
-
-template <bool SR, bool STATS, bool DO_ROW>
-__global__ void __launch_bounds__(TileCfg<SR>::kThreads, TileCfg<SR>::kCtasPerSm) quantize_tile_sr_kernel(
-    const __grid_constant__ CUtensorMap map, int64_t R, int64_t C, int fmt,
-    const float* __restrict__ tscale, uint64_t seed, uint32_t* __restrict__ pay_row,
-    uint8_t* __restrict__ sc_row, uint8_t* __restrict__ pay_col, uint8_t* __restrict__ sc_col,
-    StatsDev* stats, float* amax_out, int* status) {
-  extern __shared__ uint8_t qsm_dyn[];
-  uint8_t* qsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qsm_dyn) + 127) & ~uintptr_t(127));
-  using Cfg = TileCfg<SR>;
-  constexpr int kQStages = Cfg::kStages;
-  const uint32_t sb = smem_u32(qsm);
-  const uint32_t bar_full = sb + kQStages * kQStageBytes;
-  const uint32_t bar_empty = bar_full + 8 * kQStages;
-  const int64_t tiles_c = (C + kTile - 1) / kTile;
-  const int64_t tiles = tiles_c * ((R + kTile - 1) / kTile);
-  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  if (t == 0) {
-    for (int i = 0; i < kQStages; ++i) {
-      mbar_init(bar_full + 8 * i, 1);
-      mbar_init(bar_empty + 8 * i, 8);   // the eight warps of one consumer group
-    }
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  __shared__ ScaleTab tab;
-  build_scale_tab(&tab, __ldg(tscale), fmt);   // ends with __syncthreads
-
-  uint32_t tmax = 0;
-  uint32_t r_sat = 0, r_uflow = 0, r_clamp = 0, r_flush = 0;   // row-wise counters
-  uint32_t c_sat = 0, c_uflow = 0, c_clamp = 0, c_flush = 0;   // column-wise counters
-  if (warp == Cfg::kConsumerWarps) {
-    // ------------------------------------------------ TMA producer
-    if (lane == 0) {
-      int s = 0;
-      uint32_t ph = 0;
-      for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
-        if (!mbar_wait_bounded(bar_empty + 8 * s, ph ^ 1, kQWaitCycles)) {
-          atomicOr(status, kStatusTimeout);
-          break;
-        }
-        const int r0 = (int)((tile / tiles_c) * kTile), c0 = (int)((tile % tiles_c) * kTile);
-        mbar_expect_tx(bar_full + 8 * s, kQStageBytes);
-        tma_load_2d(sb + s * kQStageBytes, &map, c0, r0, bar_full + 8 * s);
-        if (++s == kQStages) { s = 0; ph ^= 1; }
-      }
-    }
-  } else {
-    // ------------------------------------------------ consumers
-    // group g (warps 8g .. 8g+7) takes the CTA's tiles g, g + G, g + 2G, ...
-    const int g = warp >> 3;
-    const int tl_id = t & 255;          // thread index inside the group
-    const int cg = tl_id & 15;
-    const int q4 = lane * 4;            // first of four columns (column phase)
-    const int rb16 = (warp & 7) * 16;   // first of 16 rows (column phase)
-    for (int64_t j = g; ; j += Cfg::kGroups) {
-      const int64_t tile = blockIdx.x + j * gridDim.x;
-      if (tile >= tiles) break;
-      const int s = (int)(j % kQStages);
-      const uint32_t ph = (uint32_t)((j / kQStages) & 1);
-      const int64_t r0 = (tile / tiles_c) * kTile, c0 = (tile % tiles_c) * kTile;
-      const int rows = (int)(R - r0 < kTile ? R - r0 : kTile);
-      const int cols = (int)(C - c0 < kTile ? C - c0 : kTile);
-      if (!mbar_wait_bounded(bar_full + 8 * s, ph, kQWaitCycles)) {
-        atomicOr(status, kStatusTimeout);
-        break;
-      }
-      const uint16_t(*tl)[kTile] = reinterpret_cast<const uint16_t(*)[kTile]>(qsm + s * kQStageBytes);
-
-      // row-wise blocks (and the tile's share of the tensor amax); the eight
-      // chunk loads are issued before any of them is used
-      uint4 rv[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        rv[i] = *reinterpret_cast<const uint4*>(&tl[(tl_id >> 4) + 16 * i][cg * 8]);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int row = (tl_id >> 4) + 16 * i;
-        const uint32_t w[4] = {rv[i].x, rv[i].y, rv[i].z, rv[i].w};
-        uint32_t m = absmax16(w);
-        tmax = max(tmax, m);
-        if (DO_ROW) {
-          m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-          const bool ok = row < rows && cg * 8 < cols;
-          const int64_t e0 = (r0 + row) * C + c0 + cg * 8;  // logical index of the chunk
-          const BlockScale bs = block_scale(m, tab);
-          uint32_t rb[8];
-          if (SR) {
-            const uint4 a = sr_words4((uint64_t)e0 >> 2, 0u, seed);
-            const uint4 b = sr_words4(((uint64_t)e0 >> 2) + 1, 0u, seed);
-            rb[0] = a.x; rb[1] = a.y; rb[2] = a.z; rb[3] = a.w;
-            rb[4] = b.x; rb[5] = b.y; rb[6] = b.z; rb[7] = b.w;
-          }
-          uint32_t c = 0, f = 0;
-          const uint32_t nib = quantize8<SR, STATS>(w, bs.r, rb, &c, &f);
-          if (ok) {
-            st_stream_u32(pay_row + (e0 >> 3), nib);
-            if ((lane & 1) == 0) sc_row[e0 >> 4] = (uint8_t)bs.code;
-            if (STATS) {
-              r_clamp += c;
-              r_flush += f;
-              if ((lane & 1) == 0) {
-                r_sat += bs.sat ? 1u : 0u;
-                r_uflow += (m != 0u && bs.code == 0u) ? 1u : 0u;
-              }
-            }
-          }
-        }
-      }
-
-      // column-wise blocks
-      const bool ok = q4 < cols && rb16 < rows;
-      uint32_t cw[4][8];  // [column j][row pair p] = BF16 of rows 2p (low), 2p+1 (high)
-#pragma unroll
-      for (int p = 0; p < 8; ++p) {
-        const uint2 a = *reinterpret_cast<const uint2*>(&tl[rb16 + 2 * p][q4]);
-        const uint2 b = *reinterpret_cast<const uint2*>(&tl[rb16 + 2 * p + 1][q4]);
-        cw[0][p] = __byte_perm(a.x, b.x, 0x5410);
-        cw[1][p] = __byte_perm(a.x, b.x, 0x7632);
-        cw[2][p] = __byte_perm(a.y, b.y, 0x5410);
-        cw[3][p] = __byte_perm(a.y, b.y, 0x7632);
-      }
-      // the tile is in registers now: release the stage to the producer.  The
-      // proxy fence orders these generic-proxy reads before the TMA (async
-      // proxy) write that will refill the stage.
-      fence_proxy_async();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_empty + 8 * s);
-
-      float rj[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t w4a[4] = {cw[j][0], cw[j][1], cw[j][2], cw[j][3]};
-        const uint32_t w4b[4] = {cw[j][4], cw[j][5], cw[j][6], cw[j][7]};
-        const uint32_t cm = max(absmax16(w4a), absmax16(w4b));
-        const BlockScale bs = block_scale(cm, tab);
-        rj[j] = bs.r;
-        if (STATS && ok) {
-          c_sat += bs.sat ? 1u : 0u;
-          c_uflow += (cm != 0u && bs.code == 0u) ? 1u : 0u;
-        }
-        if (ok) sc_col[(c0 + q4 + j) * (R / 16) + (r0 + rb16) / 16] = (uint8_t)bs.code;
-      }
-      uint32_t nib[4][2] = {{0u, 0u}, {0u, 0u}, {0u, 0u}, {0u, 0u}};
-      if (!SR) {
-        // round to nearest: each half column (8 rows, four BF16 pairs) is one
-        // eight-element conversion straight into a payload word
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint32_t w4[4] = {cw[j][4 * h], cw[j][4 * h + 1], cw[j][4 * h + 2], cw[j][4 * h + 3]};
-            uint32_t c = 0, f = 0;
-            nib[j][h] = quantize8<false, STATS>(w4, rj[j], nullptr, &c, &f);
-            if (STATS && ok) { c_clamp += c; c_flush += f; }
-          }
-        }
-      } else {
-        // stochastic rounding: rows in pairs; one Philox block per row gives
-        // the words of its four columns (counter = logical index / 4, word =
-        // column offset)
-#pragma unroll
-        for (int p = 0; p < 8; ++p) {
-          const int64_t e = (r0 + rb16 + 2 * p) * C + c0 + q4;  // multiple of 4
-          const uint4 wa = sr_words4((uint64_t)e >> 2, 1u, seed);
-          const uint4 wb = sr_words4((uint64_t)(e + C) >> 2, 1u, seed);
-          const uint32_t ra[4] = {wa.x, wa.y, wa.z, wa.w}, rb_[4] = {wb.x, wb.y, wb.z, wb.w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint32_t c = 0, f = 0;
-            const uint32_t byte = quantize_pair<true, STATS>(cw[j][p], rj[j], rj[j], ra[j], rb_[j], &c, &f);
-            nib[j][p >> 2] |= byte << (8 * (p & 3));
-            if (STATS && ok) { c_clamp += c; c_flush += f; }
-          }
-        }
-      }
-      if (ok) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          *reinterpret_cast<uint2*>(pay_col + (c0 + q4 + j) * (R / 2) + (r0 + rb16) / 2) =
-              make_uint2(nib[j][0], nib[j][1]);
-      }
-    }
-  }
-  if (STATS) {
-    if (DO_ROW) flush_stats(stats, r_sat, r_uflow, r_clamp, r_flush);
-    flush_stats(stats + (DO_ROW ? 1 : 0), c_sat, c_uflow, c_clamp, c_flush);
-  }
-  flush_amax(amax_out, status, tmax);
-}
-
 // ---------------------------------------------------------------- dequantise
 // v = (e * s) * T per element, one binary32 rounding each, then BF16 (RNE)
 // or binary32.  One chunk = 8 elements = one payload word.
@@ -594,39 +518,16 @@ static void row_launch(const QuantArgs& a, cudaStream_t st) {
 template <bool SR, bool STATS, bool DO_ROW>
 static cudaError_t tile_launch(const QuantArgs& a, cudaStream_t st) {
   dim3 grid((unsigned)((a.cols + kRcCols - 1) / kRcCols), (unsigned)((a.rows + kRcRows - 1) / kRcRows));
-  quantize_tile_kernel<SR, STATS, DO_ROW><<<grid, kRcThreads, 0, st>>>(
-      static_cast<const uint16_t*>(a.in), a.rows, a.cols, a.fmt, a.tscale, a.seed,
-      reinterpret_cast<uint32_t*>(a.pay_row), a.sc_row, a.pay_col, a.sc_col, a.stats, a.amax_out,
-      a.status);
-  return cudaGetLastError();
-}
-
-template <bool SR, bool STATS, bool DO_ROW>
-static cudaError_t tile_sr_launch(const QuantArgs& a, cudaStream_t st) {
-  auto fn = get_encode_fn();
-  if (!fn) return cudaErrorNotSupported;
-  CUtensorMap map;
-  const cuuint64_t dims[2] = {(cuuint64_t)a.cols, (cuuint64_t)a.rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)a.cols * 2};
-  const cuuint32_t box[2] = {kTile, kTile};
-  const cuuint32_t estr[2] = {1, 1};
-  if (fn(&map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(a.in), dims, strides, box, estr,
-         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
-  using Cfg = TileCfg<SR>;
-  auto kern = quantize_tile_sr_kernel<SR, STATS, DO_ROW>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
-  if (e != cudaSuccess) return e;
-  const int64_t tiles = ((a.cols + kTile - 1) / kTile) * ((a.rows + kTile - 1) / kTile);
-  int dev = 0, sms = 152;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t cap = (int64_t)sms * Cfg::kCtasPerSm;
-  const unsigned grid = (unsigned)(tiles < cap ? tiles : cap);
-  kern<<<grid, Cfg::kThreads, Cfg::kSmem, st>>>(map, a.rows, a.cols, a.fmt, a.tscale, a.seed,
-                                        reinterpret_cast<uint32_t*>(a.pay_row), a.sc_row, a.pay_col,
-                                        a.sc_col, a.stats, a.amax_out, a.status);
+  const uint16_t* in = static_cast<const uint16_t*>(a.in);
+  uint32_t* pr = reinterpret_cast<uint32_t*>(a.pay_row);
+  if constexpr (SR)
+    quantize_tile4_kernel<SR, STATS, DO_ROW><<<grid, kRcThreads, 0, st>>>(
+        in, a.rows, a.cols, a.fmt, a.tscale, a.seed, pr, a.sc_row, a.pay_col, a.sc_col, a.stats,
+        a.amax_out, a.status);
+  else
+    quantize_tile_kernel<SR, STATS, DO_ROW><<<grid, kRcThreads, 0, st>>>(
+        in, a.rows, a.cols, a.fmt, a.tscale, a.seed, pr, a.sc_row, a.pay_col, a.sc_col, a.stats,
+        a.amax_out, a.status);
   return cudaGetLastError();
 }
 
