@@ -5,7 +5,7 @@
 #include <stdint.h>
 #include <stdlib.h>
 
-#include "../../include/fp4q.h"
+#include "fp4q.h"
 #include "fp4q_device.cuh"
 #include "fp4q_launch.h"
 
