@@ -142,7 +142,8 @@ __device__ __forceinline__ uint4 sr_words4(uint64_t ctr, uint32_t axis, uint64_t
 // bits.  The reciprocal r is tabulated per code once per CTA.
 struct BlockScale {
   uint32_t code;
-  float r;        // 1 / (s T); 0 marks a zero scale (elements encode to signed zeros)
+  float r;        // 1 / (s T); 0 for a zero scale: x * 0 is the signed zero of a
+                  // finite x, and a block holding inf or NaN never gets code 0
   bool sat;
 };
 
@@ -178,16 +179,22 @@ __device__ __forceinline__ void build_scale_tab(ScaleTab* tab, float T, int fmt)
   __syncthreads();
 }
 
-__device__ __forceinline__ uint32_t exact_code_slow(uint32_t a16, const ScaleTab& tab, bool* sat) {
+// Kept out of line: the call is taken by a few blocks in a million, and
+// inlining it makes every block pay for the division's instructions.
+static __device__ __noinline__ uint32_t exact_code_slow(uint32_t a16, const ScaleTab& tab, bool* sat) {
   return exact_code(a16, tab.six_t, tab.fmt, sat);
 }
 
+// With STATS the saturation flag is exact as well; without it, a block
+// whose s* lies near the largest scale needs no exact division, because both
+// sides of the largest scale round to the same (clamped) code.
+template <bool STATS>
 __device__ __forceinline__ BlockScale block_scale(uint32_t a16, const ScaleTab& tab) {
   BlockScale bs;
   const float sa = __fmul_rn(__uint_as_float(a16 << 16), tab.inv6t);
   const uint32_t x = __float_as_uint(__fmul_rn(sa, tab.unbias));
   const bool near_mid = ((x & 0xFFFFFu) - 0x7FFF8u) < 16u;                     // within 8 of the midpoint
-  const bool near_max = (__float_as_uint(sa) - __float_as_uint(tab.smax) + 8u) < 16u;
+  const bool near_max = STATS && (__float_as_uint(sa) - __float_as_uint(tab.smax) + 8u) < 16u;
   if (near_mid || near_max) {
     bs.code = exact_code_slow(a16, tab, &bs.sat);
   } else {
@@ -208,6 +215,26 @@ __device__ __forceinline__ void mul2(uint32_t pair, float r, float& q0, float& q
   asm("mov.b64 {%0, %1}, %2;" : "=f"(q0), "=f"(q1) : "l"(y));
 }
 
+// (a, b) * r as one packed binary32x2 multiply.
+__device__ __forceinline__ void mul2f(float a, float b, float r, float& qa, float& qb) {
+  unsigned long long x, rr, y;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a), "f"(b));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(rr) : "f"(r));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(y) : "l"(x), "l"(rr));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(qa), "=f"(qb) : "l"(y));
+}
+
+// Two binary32 values -> one byte of two E2M1 nibbles (lo in the low nibble),
+// in bits 0..7 of the result.
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+  uint32_t out;
+  asm("{\n\t.reg .b8 b;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b, %2, %1;\n\t"
+      "cvt.u32.u8 %0, b;\n\t}"
+      : "=r"(out) : "f"(lo), "f"(hi));
+  return out;
+}
+
 // Quantises eight elements (four BF16 words) with multiplier r.  Returns the
 // eight nibbles; with STATS, adds clamped/flushed element counts.
 template <bool SR, bool STATS>
@@ -216,14 +243,6 @@ __device__ __forceinline__ uint32_t quantize8(const uint32_t w[4], float r, cons
   float q[8];
 #pragma unroll
   for (int j = 0; j < 4; ++j) mul2(w[j], r, q[2 * j], q[2 * j + 1]);
-  if (r == 0.0f) {
-    // zero scale: signed zeros (x * 0 keeps the sign of x)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      q[2 * j] = __uint_as_float((w[j] << 16) & 0x80000000u);
-      q[2 * j + 1] = __uint_as_float(w[j] & 0x80000000u);
-    }
-  }
   if (STATS) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) *clamped += (fabsf(q[j]) > 6.0f) ? 1u : 0u;
@@ -254,8 +273,6 @@ template <bool SR, bool STATS>
 __device__ __forceinline__ uint32_t quantize_pair(uint32_t pair, float r0, float r1, uint32_t w0,
                                                   uint32_t w1, uint32_t* clamped, uint32_t* flushed) {
   float q0 = __fmul_rn(bf16_lo(pair), r0), q1 = __fmul_rn(bf16_hi(pair), r1);
-  if (r0 == 0.0f) q0 = __uint_as_float((pair << 16) & 0x80000000u);
-  if (r1 == 0.0f) q1 = __uint_as_float(pair & 0x80000000u);
   if (STATS) *clamped += (fabsf(q0) > 6.0f ? 1u : 0u) + (fabsf(q1) > 6.0f ? 1u : 0u);
   if (SR) {
     q0 = __uint_as_float(__float_as_uint(sr_round_mag(fabsf(q0), w0)) | (__float_as_uint(q0) & 0x80000000u));

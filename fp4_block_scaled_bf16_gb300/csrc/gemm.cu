@@ -9,20 +9,21 @@
 //   C[m, n] = (T_A T_B) * sum_k (e_a s_a)[m, k] * (e_b s_b)[n, k]
 //
 // Every product e * s has at most 6 significant bits and lies in
-// [2^-18, 688128], so it is exact in BF16; the contraction therefore runs as a
-// BF16 x BF16 -> FP32 tcgen05 MMA (kind::f16) over operands expanded in shared
-// memory, and differs from an exact sum only by FP32 accumulation rounding.
+// [2^-18, 688128], so e * s * 2^-4 is exact in FP16; the contraction
+// therefore runs as an FP16 x FP16 -> FP32 tcgen05 MMA (kind::f16) over
+// operands expanded in shared memory, and differs from an exact sum only by
+// FP32 accumulation rounding.
 //
 // CTA organisation (one CTA per SM, 256 x 256 output tile, K step 64; the
 // expansion is the costly part, so the tile is as large as TMEM allows: two
 // 128 x 256 FP32 accumulators fill all 512 columns):
 //   warp 16     TMA producer: FP4 payload tiles (A and B, 256 x 32 B each)
 //               into a 4-stage raw ring.
-//   warps 0..15 expand raw stages into a 2-stage BF16 ring laid out in the
+//   warps 0..15 expand raw stages into a 2-stage FP16 ring laid out in the
 //               128-byte-swizzled K-major form the MMA descriptors read; each
 //               thread expands one 16-element block (one scale) at a time by
-//               placing nibble bits in BF16 patterns and two exact BF16
-//               multiplies (the second by the block scale);
+//               the E2M1 -> FP16 conversion and one exact FP16 multiply by
+//               the block scale;
 //               after the main loop they run the epilogue (TMEM -> registers
 //               -> alpha -> BF16/FP32 -> global).
 //   warp 17     allocates TMEM; one lane issues 8 MMAs (2 x M128 N256 K16)
@@ -100,7 +101,7 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                : "memory");
 }
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                          uint32_t idesc, uint32_t accum) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
@@ -128,7 +129,7 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
-// 64 BF16 (128 B) grouped by 8 into 1024-byte atoms (stride-dimension offset
+// 64 FP16 (128 B) grouped by 8 into 1024-byte atoms (stride-dimension offset
 // 1024 B); the leading-dimension offset is unused in this mode.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   uint64_t d = 0;
@@ -140,65 +141,52 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor for kind::f16: FP32 accumulator, BF16 A and B, both
-// K-major, M = 128, N = 256.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                            ((uint32_t)(UM >> 4) << 24);
+// Instruction descriptor for kind::f16: FP32 accumulator, FP16 A and B (format
+// code 0), both K-major, M = 128, N = 256.
+constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(UM >> 4) << 24);
 
 // ---------------------------------------------------------------- expansion
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   uint32_t d;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-  return d;
-}
-__device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
 }
 
-// Expansion of E2M1 x UE5M3 to BF16 with the multiplies on the FP16/BF16
-// pipe.  The nibble's three magnitude bits v placed at bits 6..8 of a BF16
-// pattern, with its sign at bit 15, encode exactly +-E2M1(v) * 2^-126: the
-// E2M1 exponent lands in the BF16 exponent field and the E2M1 subnormal
-// (v = 1, 0.5) lands on the BF16 subnormal 2^-127, so gradual underflow lines
-// up.  Two exact multiplies -- by 2^100, then by s * 2^26 -- give +-E2M1(v) * s
-// (at most 6 significant bits, within [2^-18, 688128]); one multiply by
-// s * 2^126 would overflow BF16 for s >= 4.
+// Expansion of E2M1 x UE5M3 to FP16.  Every product e * s * 2^-4 is exact in
+// FP16: e is a multiple of 1/2 with at most 2 significant bits, s * 2^-4 a
+// multiple of 2^-21 with at most 4, so the product is a multiple of 2^-22
+// (on the FP16 subnormal grid of 2^-24) with at most 6 significant bits, and
+// at most 6 * 114688 / 16 = 43008 < 65504.  The nibbles become FP16 pairs by
+// the hardware E2M1 -> FP16 conversion (exact), and one FP16 multiply by
+// (s * 2^-4) applies the block scale; the 2^-8 of the two operands comes back
+// in the epilogue's alpha.
 
-// (s * 2^26, s * 2^26) as a BF16 pair.  The scale code shifted into a binary32
+// (s * 2^-4, s * 2^-4) as an FP16 pair.  The scale code shifted into a binary32
 // exponent/mantissa field is s * 2^-(127 - bias), subnormal codes included.
 __device__ __forceinline__ uint32_t scale_pair(uint32_t code, int fmt) {
   const float s = __fmul_rn(__uint_as_float(code << 20), fmt == kUE5M3 ? 0x1p112f : 0x1p120f);
-  const float s26 = __fmul_rn(s, 0x1p26f);
+  const float s4 = __fmul_rn(s, 0x1p-4f);
   uint32_t ss;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(ss) : "f"(s26));   // exact: <= 4 significant bits
+  asm("cvt.rn.f16x2.f32 %0, %1, %1;" : "=r"(ss) : "f"(s4));   // exact: <= 4 significant bits
   return ss;
 }
 
-// w * 2^k as an integer multiply-add, which issues on the FMA pipe and so
-// keeps the shift off the integer/logic pipe.
-__device__ __forceinline__ uint32_t shl_fma(uint32_t w, uint32_t pow2) {
-  uint32_t d;
-  asm("mad.lo.u32 %0, %1, %2, 0;" : "=r"(d) : "r"(w), "r"(pow2));
-  return d;
-}
-
-// Eight nibbles (n0 in the low bits) -> four BF16 pairs (n_i, n_{i+4}).  The
-// K order inside each group of eight is thereby permuted to
-// (n0 n4 n1 n5 n2 n6 n3 n7), identically for A and B, which leaves every dot
-// product unchanged and puts both elements of a pair at the same shift.
+// Eight nibbles (byte j holds K elements 2j, 2j + 1) -> four FP16 pairs.  The
+// pair order within a byte is whatever the conversion gives; it is the same
+// for A and B, which leaves every dot product unchanged.
 __device__ __forceinline__ uint4 expand8(uint32_t w, uint32_t ss) {
-  constexpr uint32_t kMag = 0x01C001C0u, kSign = 0x80008000u, k2p100 = 0x71807180u;
   uint4 o;
-  o.x = (shl_fma(w, 1u << 6) & kMag) | (shl_fma(w, 1u << 12) & kSign);   // (n0, n4)
-  o.y = (shl_fma(w, 1u << 2) & kMag) | (shl_fma(w, 1u << 8) & kSign);    // (n1, n5)
-  o.z = ((w >> 2) & kMag) | (shl_fma(w, 1u << 4) & kSign);               // (n2, n6)
-  o.w = ((w >> 6) & kMag) | (w & kSign);                                 // (n3, n7)
-  o.x = bmul2(bmul2(o.x, k2p100), ss);
-  o.y = bmul2(bmul2(o.y, k2p100), ss);
-  o.z = bmul2(bmul2(o.z, k2p100), ss);
-  o.w = bmul2(bmul2(o.w, k2p100), ss);
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(o.x), "=r"(o.y), "=r"(o.z), "=r"(o.w) : "r"(w));
+  o.x = hmul2(o.x, ss);
+  o.y = hmul2(o.y, ss);
+  o.z = hmul2(o.z, ss);
+  o.w = hmul2(o.w, ss);
   return o;
 }
 
@@ -285,8 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < BK / 16; ++k) {
           const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
-          mma_bf16(tmem, a0 + 2 * k, bd + 2 * k, kIdesc, acc);          // rows 0..127
-          mma_bf16(tmem + BN, a1 + 2 * k, bd + 2 * k, kIdesc, acc);     // rows 128..255
+          mma_f16(tmem, a0 + 2 * k, bd + 2 * k, kIdesc, acc);          // rows 0..127
+          mma_f16(tmem + BN, a1 + 2 * k, bd + 2 * k, kIdesc, acc);     // rows 128..255
         }
         mma_commit(bar_bf_empty + 8 * t);
       }
@@ -359,7 +347,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (mbar_wait(bar_acc, 0, abort_flag, budget)) {
       tc_fence_after();
       const int q = warp & 3, acc = (warp >> 2) & 1, half = warp >> 3;
-      const float alpha = __fmul_rn(__ldg(TA), __ldg(TB));
+      // T_A T_B, times 2^8 for the 2^-4 on each operand (exact)
+      const float alpha = __fmul_rn(__fmul_rn(__ldg(TA), __ldg(TB)), 256.0f);
       const int row = m0 + UM * acc + 32 * q + lane;
       const bool vec = F32OUT ? (N % 4 == 0) : (N % 8 == 0);
 #pragma unroll 1

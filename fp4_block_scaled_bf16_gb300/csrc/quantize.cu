@@ -10,9 +10,10 @@
 // bypass L1 and keeps blocks in registers.  The row-wise quantiser treats the
 // tensor as flat (a block never straddles a row), so that one warp covers 256
 // consecutive elements and a lane pair shares one block (one shuffle for the
-// block amax).  The column-wise / dual-axis quantiser gives each thread a
-// 16-row x 8-column piece, which holds eight whole column blocks and half of
-// sixteen row blocks, so that neither axis needs shared memory.
+// block amax).  The column-wise / dual-axis quantisers give each thread a
+// piece of a 128 x 128 tile (8 x 8 for round to nearest, 16 x 4 for
+// stochastic rounding); lanes that share a block combine their maxima with
+// shuffles, so that neither axis needs shared memory.
 #include "fp4q_device.cuh"
 #include "fp4q_launch.h"
 
@@ -127,7 +128,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) quantize_row_kernel(
       uint32_t m = absmax16(w);
       m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
       tmax = max(tmax, m);
-      const BlockScale bs = block_scale(m, tab);
+      const BlockScale bs = block_scale<STATS>(m, tab);
       uint32_t rb[8];
       if (SR) {
         const uint4 a = sr_words4((uint64_t)g * 2, 0u, seed);
@@ -156,39 +157,65 @@ __global__ void __launch_bounds__(kRowThreads, 2) quantize_row_kernel(
 }
 
 // ---------------------------------------------------------------- tiles
-// Column-wise and dual-axis quantisation, register-resident.  A CTA covers
-// 128 rows x 128 columns; warp w takes rows 16 w .. +15.  Lane l holds an
-// 8 x 8 piece: rows 16 w + 8 (l / 16) .. +7, columns 8 (l % 16) .. +7, loaded
-// with eight 128-bit loads (each warp load reads two 256-byte row segments).
-//   row blocks (dual axis): lanes l and l ^ 1 hold the 16 columns of a block
-//     (one shuffle per row for its amax); a lane converts its eight elements
-//     of a row into one payload word;
-//   column blocks: lanes l and l ^ 16 hold the two 8-row halves of a
-//     column's 16-row block (one shuffle per column for its amax); a lane
-//     converts its eight rows of a column into one payload word, after
-//     gathering BF16 pairs of consecutive rows with byte permutes.
+// Column-wise and dual-axis round-to-nearest quantisation, register-resident.
+// A CTA covers 128 rows x 128 columns; warp w takes rows 16 w .. +15.  Lane l
+// holds an 8 x 8 piece: rows 16 w + 8 (l / 16) .. +7, columns 8 (l % 16) .. +7,
+// loaded with eight 128-bit loads (each warp load reads two 256-byte row
+// segments).
+//   magnitudes: one pass over the masked BF16 words gives, per word column,
+//     the maxima of its two columns over the lane's eight rows, and per row
+//     pair the two row maxima, each packed two to a word;
+//   column blocks: lanes l and l ^ 16 hold the two 8-row halves of the same
+//     eight columns; one shuffle per word column completes both columns'
+//     block maxima, lane l computes the scale of the even (l < 16) or odd
+//     column of each word column and one more shuffle hands the reciprocal
+//     to its partner;
+//   row blocks (dual axis): lanes l and l ^ 1 hold the two 8-column halves of
+//     the same rows; per row pair one shuffle completes both maxima and each
+//     lane computes one of the two scales, exchanged the same way;
+//   conversion: each 2 x 2 group (two BF16 words of consecutive rows) is
+//     unpacked once and multiplied by the row and the column reciprocals
+//     (packed binary32x2 multiplies); a row payload word is eight nibbles of
+//     one row, a column payload word eight nibbles of one column.
 // The eight warps of a CTA write the 16-row pieces of each column's payload
-// side by side (64 contiguous bytes).  Stochastic rounding draws one Philox
-// block per row and per four columns on each axis.  Nothing goes through
-// shared memory except the block-scale reciprocal table.
+// side by side (64 contiguous bytes).  Nothing goes through shared memory
+// except the block-scale reciprocal table.
 constexpr int kRcRows = 128, kRcCols = 128, kRcThreads = 256;
 
-template <bool SR, bool STATS, bool DO_ROW>
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int q) {
+  return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
+}
+
+// Places bits 0..7 of b into byte k of acc.
+__device__ __forceinline__ uint32_t put_byte(uint32_t acc, uint32_t b, int k) {
+  return __byte_perm(acc, b, k == 0 ? 0x3214 : k == 1 ? 0x3240 : k == 2 ? 0x3410 : 0x4210);
+}
+
+// Flushed-element count of one converted byte: inputs of non-zero magnitude
+// whose nibble has zero magnitude.
+__device__ __forceinline__ uint32_t flushed2(float x0, float x1, uint32_t byte) {
+  return ((__float_as_uint(x0) & 0x7FFFFFFFu) != 0u && (byte & 7u) == 0u ? 1u : 0u) +
+         ((__float_as_uint(x1) & 0x7FFFFFFFu) != 0u && (byte & 0x70u) == 0u ? 1u : 0u);
+}
+
+__device__ __forceinline__ uint32_t clamped2(float q0, float q1) {
+  return (fabsf(q0) > 6.0f ? 1u : 0u) + (fabsf(q1) > 6.0f ? 1u : 0u);
+}
+
+template <bool STATS, bool DO_ROW>
 __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile_kernel(
     const uint16_t* __restrict__ in, int64_t R, int64_t C, int fmt,
-    const float* __restrict__ tscale, uint64_t seed, uint32_t* __restrict__ pay_row,
+    const float* __restrict__ tscale, uint32_t* __restrict__ pay_row,
     uint8_t* __restrict__ sc_row, uint8_t* __restrict__ pay_col, uint8_t* __restrict__ sc_col,
     StatsDev* stats, float* amax_out, int* status) {
   __shared__ ScaleTab tab;
-  build_scale_tab(&tab, __ldg(tscale), fmt);
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const int half = lane >> 4, cg = lane & 15;
+  const int half = lane >> 4, cg = lane & 15, par = cg & 1;
   const int64_t rb = (int64_t)blockIdx.y * kRcRows + warp * 16;   // first row of the column block
   const int64_t r0 = rb + 8 * half;                                 // first of this lane's 8 rows
   const int64_t c0 = (int64_t)blockIdx.x * kRcCols + cg * 8;
   // sizes are multiples of 16: a 16 x 16 region is wholly inside or outside
   const bool ok = rb < R && c0 < C;
-  uint32_t tmax = 0;
   uint32_t r_sat = 0, r_uflow = 0, r_clamp = 0, r_flush = 0;
   uint32_t c_sat = 0, c_uflow = 0, c_clamp = 0, c_flush = 0;
 
@@ -196,98 +223,111 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile_kernel(
 #pragma unroll
   for (int rr = 0; rr < 8; ++rr)
     v[rr] = ok ? ld_stream_v4(in + (r0 + rr) * C + c0) : make_uint4(0, 0, 0, 0);
+  build_scale_tab(&tab, __ldg(tscale), fmt);   // while the piece is in flight
 
-  // ---- row blocks
+  // ---- magnitudes: cmx[q] = maxima of columns 2q (low) and 2q + 1 (high);
+  // rpx[p] = maxima of rows 2p (low) and 2p + 1 (high) over the lane's columns
+  uint32_t cmx[4] = {0u, 0u, 0u, 0u}, rpx[4];
 #pragma unroll
-  for (int rr = 0; rr < 8; ++rr) {
-    const uint32_t w[4] = {v[rr].x, v[rr].y, v[rr].z, v[rr].w};
-    uint32_t m = absmax16(w);
-    tmax = max(tmax, m);
-    if (DO_ROW) {
-      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-      const int64_t e0 = (r0 + rr) * C + c0;  // logical index of the eight elements
-      const BlockScale bs = block_scale(m, tab);
-      uint32_t rbits[8];
-      if (SR) {
-        const uint4 a = sr_words4((uint64_t)e0 >> 2, 0u, seed);
-        const uint4 b = sr_words4(((uint64_t)e0 >> 2) + 1, 0u, seed);
-        rbits[0] = a.x; rbits[1] = a.y; rbits[2] = a.z; rbits[3] = a.w;
-        rbits[4] = b.x; rbits[5] = b.y; rbits[6] = b.z; rbits[7] = b.w;
+  for (int p = 0; p < 4; ++p) {
+    uint32_t rm[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      uint32_t mw[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        mw[q] = word_of(v[2 * p + k], q) & 0x7FFF7FFFu;
+        cmx[q] = __vmaxu2(cmx[q], mw[q]);
       }
-      uint32_t c = 0, f = 0;
-      const uint32_t nib = quantize8<SR, STATS>(w, bs.r, rbits, &c, &f);
-      if (ok) {
-        st_stream_u32(pay_row + (e0 >> 3), nib);
-        if ((cg & 1) == 0) sc_row[e0 >> 4] = (uint8_t)bs.code;
-        if (STATS) {
-          r_clamp += c;
-          r_flush += f;
-          if ((cg & 1) == 0) {
-            r_sat += bs.sat ? 1u : 0u;
-            r_uflow += (m != 0u && bs.code == 0u) ? 1u : 0u;
-          }
-        }
-      }
+      rm[k] = __vmaxu2(__vmaxu2(mw[0], mw[1]), __vmaxu2(mw[2], mw[3]));
     }
+    rpx[p] = __vmaxu2(__byte_perm(rm[0], rm[1], 0x5410), __byte_perm(rm[0], rm[1], 0x7632));
   }
+  uint32_t tmax = __vmaxu2(__vmaxu2(cmx[0], cmx[1]), __vmaxu2(cmx[2], cmx[3]));
+  tmax = max(tmax & 0xFFFFu, tmax >> 16);
 
-  // ---- column blocks: column j of the lane is BF16 word j / 2, half j % 2
-  float rj[8];
+  // ---- column scales: this lane computes column 2q + half of word column q
+  const uint32_t pick = half ? 0x4432u : 0x4410u;   // high or low 16 bits, zero-extended
+  float colr[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    uint32_t cw[4];   // BF16 of rows 2p (low) and 2p + 1 (high) of column j
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-      const uint4 a4 = v[2 * p], b4 = v[2 * p + 1];
-      const uint32_t a = (j >> 1) == 0 ? a4.x : (j >> 1) == 1 ? a4.y : (j >> 1) == 2 ? a4.z : a4.w;
-      const uint32_t b = (j >> 1) == 0 ? b4.x : (j >> 1) == 1 ? b4.y : (j >> 1) == 2 ? b4.z : b4.w;
-      cw[p] = __byte_perm(a, b, (j & 1) ? 0x7632 : 0x5410);
-    }
-    uint32_t cm = absmax16(cw);
-    cm = max(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, 16));
-    const BlockScale bs = block_scale(cm, tab);
-    rj[j] = bs.r;
-    if (ok && half == 0) {
-      sc_col[(c0 + j) * (R / 16) + rb / 16] = (uint8_t)bs.code;
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t full = __vmaxu2(cmx[q], __shfl_xor_sync(0xFFFFFFFFu, cmx[q], 16));
+    const uint32_t cm = __byte_perm(full, 0u, pick);
+    const BlockScale bs = block_scale<STATS>(cm, tab);
+    const float other = __shfl_xor_sync(0xFFFFFFFFu, bs.r, 16);
+    colr[2 * q] = half ? other : bs.r;
+    colr[2 * q + 1] = half ? bs.r : other;
+    if (ok) {
+      sc_col[(c0 + 2 * q + half) * (R / 16) + rb / 16] = (uint8_t)bs.code;
       if (STATS) {
         c_sat += bs.sat ? 1u : 0u;
         c_uflow += (cm != 0u && bs.code == 0u) ? 1u : 0u;
       }
     }
-    if (!SR) {
-      uint32_t c = 0, f = 0;
-      const uint32_t nib = quantize8<false, STATS>(cw, bs.r, nullptr, &c, &f);
+  }
+
+  // ---- conversion, one row pair at a time
+  const uint32_t rpick = par ? 0x4432u : 0x4410u;
+  uint32_t pcol[8];
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    float re = 0.0f, ro = 0.0f;   // row reciprocals of rows 2p and 2p + 1
+    if (DO_ROW) {
+      const uint32_t full = __vmaxu2(rpx[p], __shfl_xor_sync(0xFFFFFFFFu, rpx[p], 1));
+      const uint32_t m = __byte_perm(full, 0u, rpick);          // row 2p + par
+      const BlockScale bs = block_scale<STATS>(m, tab);
+      const float other = __shfl_xor_sync(0xFFFFFFFFu, bs.r, 1);
+      re = par ? other : bs.r;
+      ro = par ? bs.r : other;
       if (ok) {
-        *reinterpret_cast<uint32_t*>(pay_col + (c0 + j) * (R / 2) + r0 / 2) = nib;
-        if (STATS) { c_clamp += c; c_flush += f; }
+        sc_row[((r0 + 2 * p + par) * C + (c0 & ~(int64_t)15)) >> 4] = (uint8_t)bs.code;
+        if (STATS) {
+          r_sat += bs.sat ? 1u : 0u;
+          r_uflow += (m != 0u && bs.code == 0u) ? 1u : 0u;
+        }
+      }
+    }
+    float xe[8], xo[8];   // row products of rows 2p and 2p + 1
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t wa = word_of(v[2 * p], q), wb = word_of(v[2 * p + 1], q);
+      const float a0 = bf16_lo(wa), a1 = bf16_hi(wa), b0 = bf16_lo(wb), b1 = bf16_hi(wb);
+      if (DO_ROW) {
+        mul2f(a0, a1, re, xe[2 * q], xe[2 * q + 1]);
+        mul2f(b0, b1, ro, xo[2 * q], xo[2 * q + 1]);
+      }
+      float y0, y1, z0, z1;
+      mul2f(a0, b0, colr[2 * q], y0, y1);        // column 2q, rows 2p, 2p + 1
+      mul2f(a1, b1, colr[2 * q + 1], z0, z1);    // column 2q + 1
+      const uint32_t by = e2m1x2(y0, y1), bz = e2m1x2(z0, z1);
+      pcol[2 * q] = p == 0 ? by : put_byte(pcol[2 * q], by, p);
+      pcol[2 * q + 1] = p == 0 ? bz : put_byte(pcol[2 * q + 1], bz, p);
+      if (STATS && ok) {
+        c_clamp += clamped2(y0, y1) + clamped2(z0, z1);
+        c_flush += flushed2(a0, b0, by) + flushed2(a1, b1, bz);
+      }
+    }
+    if (DO_ROW) {
+      const uint32_t ne = cvt_e2m1x8(xe), no = cvt_e2m1x8(xo);
+      if (ok) {
+        st_stream_u32(pay_row + (((r0 + 2 * p) * C + c0) >> 3), ne);
+        st_stream_u32(pay_row + (((r0 + 2 * p + 1) * C + c0) >> 3), no);
+        if (STATS) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t wa = word_of(v[2 * p], q), wb = word_of(v[2 * p + 1], q);
+            r_clamp += clamped2(xe[2 * q], xe[2 * q + 1]) + clamped2(xo[2 * q], xo[2 * q + 1]);
+            r_flush += flushed2(bf16_lo(wa), bf16_hi(wa), (ne >> (8 * q)) & 0xFFu) +
+                       flushed2(bf16_lo(wb), bf16_hi(wb), (no >> (8 * q)) & 0xFFu);
+          }
+        }
       }
     }
   }
-  if (SR) {
-    // row by row: two Philox blocks give the column-axis words of the row's
-    // eight elements (counter = logical index / 4, word = column offset % 4)
-    uint32_t nib[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+  if (ok) {
 #pragma unroll
-    for (int rr = 0; rr < 8; ++rr) {
-      const uint64_t e = (uint64_t)((r0 + rr) * C + c0) >> 2;
-      const uint4 x0 = sr_words4(e, 1u, seed), x1 = sr_words4(e + 1, 1u, seed);
-      const uint32_t wd[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-      const uint32_t vw[4] = {v[rr].x, v[rr].y, v[rr].z, v[rr].w};
-#pragma unroll
-      for (int jp = 0; jp < 4; ++jp) {
-        uint32_t c = 0, f = 0;
-        const uint32_t byte = quantize_pair<true, STATS>(vw[jp], rj[2 * jp], rj[2 * jp + 1],
-                                                         wd[2 * jp], wd[2 * jp + 1], &c, &f);
-        nib[2 * jp] |= (byte & 15u) << (4 * rr);
-        nib[2 * jp + 1] |= (byte >> 4) << (4 * rr);
-        if (STATS && ok) { c_clamp += c; c_flush += f; }
-      }
-    }
-    if (ok) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        *reinterpret_cast<uint32_t*>(pay_col + (c0 + j) * (R / 2) + r0 / 2) = nib[j];
-    }
+    for (int j = 0; j < 8; ++j)
+      *reinterpret_cast<uint32_t*>(pay_col + (c0 + j) * (R / 2) + r0 / 2) = pcol[j];
   }
   if (STATS) {
     if (DO_ROW) flush_stats(stats, r_sat, r_uflow, r_clamp, r_flush);
@@ -322,7 +362,6 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile4_kernel(
     uint8_t* __restrict__ sc_row, uint8_t* __restrict__ pay_col, uint8_t* __restrict__ sc_col,
     StatsDev* stats, float* amax_out, int* status) {
   __shared__ ScaleTab tab;
-  build_scale_tab(&tab, __ldg(tscale), fmt);
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int64_t r0 = (int64_t)blockIdx.y * kRcRows + warp * 16;
   const int64_t c0 = (int64_t)blockIdx.x * kRcCols + lane * 4;
@@ -344,6 +383,8 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile4_kernel(
     }
   }
 
+  build_scale_tab(&tab, __ldg(tscale), fmt);   // while the piece is in flight
+
   // ---- row blocks
 #pragma unroll
   for (int rr = 0; rr < 16; ++rr) {
@@ -355,7 +396,7 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile4_kernel(
       m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
       m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
       const int64_t e0 = (r0 + rr) * C + c0;  // logical index of the four elements
-      const BlockScale bs = block_scale(m, tab);
+      const BlockScale bs = block_scale<STATS>(m, tab);
       uint4 rw = make_uint4(0, 0, 0, 0);
       if (SR) rw = sr_words4((uint64_t)e0 >> 2, 0u, seed);
       uint32_t c = 0, f = 0;
@@ -392,7 +433,7 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile4_kernel(
     const uint32_t w4a[4] = {cw[j][0], cw[j][1], cw[j][2], cw[j][3]};
     const uint32_t w4b[4] = {cw[j][4], cw[j][5], cw[j][6], cw[j][7]};
     const uint32_t cm = max(absmax16(w4a), absmax16(w4b));
-    const BlockScale bs = block_scale(cm, tab);
+    const BlockScale bs = block_scale<STATS>(cm, tab);
     rj[j] = bs.r;
     if (ok) {
       sc_col[(c0 + j) * (R / 16) + r0 / 16] = (uint8_t)bs.code;
@@ -525,8 +566,8 @@ static cudaError_t tile_launch(const QuantArgs& a, cudaStream_t st) {
         in, a.rows, a.cols, a.fmt, a.tscale, a.seed, pr, a.sc_row, a.pay_col, a.sc_col, a.stats,
         a.amax_out, a.status);
   else
-    quantize_tile_kernel<SR, STATS, DO_ROW><<<grid, kRcThreads, 0, st>>>(
-        in, a.rows, a.cols, a.fmt, a.tscale, a.seed, pr, a.sc_row, a.pay_col, a.sc_col, a.stats,
+    quantize_tile_kernel<STATS, DO_ROW><<<grid, kRcThreads, 0, st>>>(
+        in, a.rows, a.cols, a.fmt, a.tscale, pr, a.sc_row, a.pay_col, a.sc_col, a.stats,
         a.amax_out, a.status);
   return cudaGetLastError();
 }
