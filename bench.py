@@ -410,7 +410,7 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16xbf16->f32 (E2M1/UE5M3 operands)", "data": "synthetic",
+        "vs_baseline": None, "dtype": "f16xf16->f32 (E2M1/UE5M3 operands, exact FP16 expansion)", "data": "synthetic",
         "config": {"workload": WORKLOAD, "M": M_TOK, "hidden": HID, "ffn": FFN,
                    "l2": "inputs larger than L2 (dY 256 MiB, step working set ~1 GiB)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},

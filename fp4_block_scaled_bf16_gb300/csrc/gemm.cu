@@ -32,6 +32,7 @@
 // device status word and the CTA drains and exits instead of hanging.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <string.h>
 
 #include "fp4q_device.cuh"
 #include "fp4q_launch.h"
@@ -56,13 +57,22 @@ constexpr int kThreads = kDeqThreads + 64;
 constexpr uint32_t kTmemCols = 512;             // two 128 x 256 FP32 accumulators
 constexpr int kRowsPerThread = (BM + BN) / (kDeqThreads / 4);   // 4
 
+// Scale codes (when K is a multiple of 256): TMA boxes of 16 codes per row
+// (four K steps) for the 256 A rows and the 256 B rows, in a 2-slot ring.
+constexpr int CODE_KB = 4;                      // K steps per code stage
+constexpr int CODE_STAGE = (BM + BN) * 16;      // 8192 B
+constexpr int S_CODE = 2;
+
 constexpr int OFF_BF = 0;
 constexpr int OFF_RAW = OFF_BF + S_BF * BF_STAGE;
-constexpr int OFF_BAR = OFF_RAW + S_RAW * RAW_STAGE;
-constexpr int NBARS = 2 * S_RAW + 2 * S_BF + 1;
-constexpr int OFF_TMEM = OFF_BAR + 8 * NBARS;
-constexpr int OFF_ABORT = OFF_TMEM + 8;
-constexpr int SMEM_BYTES = OFF_ABORT + 8 + 1024;   // + slack to align the base to 1 KB
+constexpr int OFF_CODE = OFF_RAW + S_RAW * RAW_STAGE;
+constexpr int NBARS = 2 * S_RAW + 2 * S_BF + 1 + 2 * S_CODE;
+// Without the code ring the kernel leaves its 16 KB to L1, which then holds
+// the scale codes it loads directly.
+__host__ __device__ constexpr int off_bar(bool tma_codes) { return OFF_CODE + (tma_codes ? S_CODE * CODE_STAGE : 0); }
+__host__ __device__ constexpr int smem_bytes(bool tma_codes) {
+  return off_bar(tma_codes) + 8 * NBARS + 16 + 1024;   // barriers, TMEM address, abort flag, 1 KB alignment slack
+}
 
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -195,6 +205,11 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
                "r"(v.w)
                : "memory");
 }
+__device__ __forceinline__ uint32_t lds_u8(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
 __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   uint2 v;
   asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
@@ -202,20 +217,26 @@ __device__ __forceinline__ uint2 lds64(uint32_t addr) {
 }
 
 // ---------------------------------------------------------------- kernel
-template <bool F32OUT>
+template <bool F32OUT, bool TMA_CODES>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                const __grid_constant__ CUtensorMap mapAs, const __grid_constant__ CUtensorMap mapBs,
                 const uint8_t* __restrict__ As, const uint8_t* __restrict__ Bs,
                 const float* __restrict__ TA, const float* __restrict__ TB, int M, int N, int K,
                 int fmt, void* __restrict__ out, int* status, long long budget, int skip_loads) {
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
+  constexpr int OFF_BAR = off_bar(TMA_CODES);
+  constexpr int OFF_TMEM = OFF_BAR + 8 * NBARS;
+  constexpr int OFF_ABORT = OFF_TMEM + 8;
   const uint32_t bar_raw_full = sb + OFF_BAR;
   const uint32_t bar_raw_empty = bar_raw_full + 8 * S_RAW;
   const uint32_t bar_bf_full = bar_raw_empty + 8 * S_RAW;
   const uint32_t bar_bf_empty = bar_bf_full + 8 * S_BF;
   const uint32_t bar_acc = bar_bf_empty + 8 * S_BF;
+  const uint32_t bar_code_full = bar_acc + 8;
+  const uint32_t bar_code_empty = bar_code_full + 8 * S_CODE;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -232,6 +253,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_bf_empty + 8 * i, 1);
     }
     mbar_init(bar_acc, 1);
+    for (int i = 0; i < S_CODE; ++i) {
+      mbar_init(bar_code_full + 8 * i, 1);
+      mbar_init(bar_code_empty + 8 * i, kDeqWarps);
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -245,6 +270,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
       for (int kb = 0; kb < nk; ++kb) {
+        if (TMA_CODES && kb % CODE_KB == 0) {
+          const int g = kb / CODE_KB, cs = g % S_CODE;
+          if (!mbar_wait(bar_code_empty + 8 * cs, ((g / S_CODE) & 1) ^ 1, abort_flag, budget)) {
+            fail(abort_flag, status);
+            break;
+          }
+          if (!skip_loads) {
+            const uint32_t cdst = sb + OFF_CODE + cs * CODE_STAGE;
+            mbar_expect_tx(bar_code_full + 8 * cs, CODE_STAGE);
+            tma_load_2d(cdst, &mapAs, g * 16, m0, bar_code_full + 8 * cs);
+            tma_load_2d(cdst + BM * 16, &mapBs, g * 16, n0, bar_code_full + 8 * cs);
+          }
+        }
         const int s = kb % S_RAW;
         if (!mbar_wait(bar_raw_empty + 8 * s, ((kb / S_RAW) & 1) ^ 1, abort_flag, budget)) {
           fail(abort_flag, status);
@@ -304,14 +342,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     // scale codes are prefetched two K steps ahead (their L2 latency is
     // longer than one step of expansion)
     uint32_t c0[kRowsPerThread], c1[kRowsPerThread], c2[kRowsPerThread];
-    load_codes(0, c0);
-    load_codes(1, c1);
+    if (!TMA_CODES) {
+      load_codes(0, c0);
+      load_codes(1, c1);
+    }
     const uint32_t sw = rbase & 7;               // (rbase + 128 i) & 7
     const uint32_t c_lo = ((2 * blk) ^ sw) << 4, c_hi = ((2 * blk + 1) ^ sw) << 4;
     int s = 0, t = 0;
     uint32_t ph_s = 0, ph_t = 1;
     for (int kb = 0; kb < nk; ++kb) {
-      load_codes(kb + 2, c2);
+      const int g = kb / CODE_KB, cs = g % S_CODE;
+      if (TMA_CODES) {
+        if (kb % CODE_KB == 0 &&
+            !mbar_wait(bar_code_full + 8 * cs, (g / S_CODE) & 1, abort_flag, budget)) {
+          fail(abort_flag, status);
+          break;
+        }
+        const uint32_t code = sb + OFF_CODE + cs * CODE_STAGE + rbase * 16 + (kb % CODE_KB) * 4 + blk;
+#pragma unroll
+        for (int i = 0; i < kRowsPerThread; ++i) c0[i] = lds_u8(code + i * 128 * 16);
+      } else {
+        load_codes(kb + 2, c2);
+      }
       if (!mbar_wait(bar_raw_full + 8 * s, ph_s, abort_flag, budget) ||
           !mbar_wait(bar_bf_empty + 8 * t, ph_t, abort_flag, budget)) {
         fail(abort_flag, status);
@@ -334,9 +386,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         mbar_arrive(bar_bf_full + 8 * t);
         mbar_arrive(bar_raw_empty + 8 * s);
+        if (TMA_CODES && (kb % CODE_KB == CODE_KB - 1 || kb == nk - 1)) mbar_arrive(bar_code_empty + 8 * cs);
       }
+      if (!TMA_CODES) {
 #pragma unroll
-      for (int i = 0; i < kRowsPerThread; ++i) { c0[i] = c1[i]; c1[i] = c2[i]; }
+        for (int i = 0; i < kRowsPerThread; ++i) { c0[i] = c1[i]; c1[i] = c2[i]; }
+      }
       if (++s == S_RAW) { s = 0; ph_s ^= 1; }
       if (++t == S_BF) { t = 0; ph_t ^= 1; }
     }
@@ -429,27 +484,51 @@ static bool make_payload_map(CUtensorMap* map, const uint8_t* base, int64_t rows
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D uint8 tensor map over a [rows, K/16] scale array, box (16 codes,
+// box_rows); needs a row stride that is a multiple of 16 bytes (K % 256 == 0).
+static bool make_code_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t K,
+                          uint32_t box_rows) {
+  auto fn = get_encode_fn();
+  if (!fn || (K / 16) % 16 != 0) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)(K / 16), (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)(K / 16)};
+  const cuuint32_t box[2] = {16u, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool F32OUT, bool TMA_CODES>
+static cudaError_t launch_gemm_t(const GemmArgs& a, const CUtensorMap& mapA, const CUtensorMap& mapB,
+                                 const CUtensorMap& mapAs, const CUtensorMap& mapBs, cudaStream_t st) {
+  constexpr int smem = gemm::smem_bytes(TMA_CODES);
+  cudaError_t e = cudaFuncSetAttribute(gemm::gemm_kernel<F32OUT, TMA_CODES>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)((a.N + gemm::BN - 1) / gemm::BN), (unsigned)((a.M + gemm::BM - 1) / gemm::BM));
+  gemm::gemm_kernel<F32OUT, TMA_CODES><<<grid, gemm::kThreads, smem, st>>>(
+      mapA, mapB, mapAs, mapBs, a.As, a.Bs, a.TA, a.TB, (int)a.M, (int)a.N, (int)a.K, a.fmt, a.out,
+      a.status, a.wait_cycles, a.skip_loads ? 1 : 0);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   if (a.M == 0 || a.N == 0) return cudaSuccess;
-  CUtensorMap mapA, mapB;
+  CUtensorMap mapA, mapB, mapAs, mapBs;
   if (!make_payload_map(&mapA, a.A, a.M, a.K, gemm::BM) || !make_payload_map(&mapB, a.B, a.N, a.K, gemm::BN))
     return cudaErrorNotSupported;
-  dim3 grid((unsigned)((a.N + gemm::BN - 1) / gemm::BN), (unsigned)((a.M + gemm::BM - 1) / gemm::BM));
-  cudaError_t e;
-  if (a.out_f32) {
-    e = cudaFuncSetAttribute(gemm::gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, gemm::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    gemm::gemm_kernel<true><<<grid, gemm::kThreads, gemm::SMEM_BYTES, st>>>(
-        mapA, mapB, a.As, a.Bs, a.TA, a.TB, (int)a.M, (int)a.N, (int)a.K, a.fmt, a.out, a.status,
-        a.wait_cycles, a.skip_loads ? 1 : 0);
-  } else {
-    e = cudaFuncSetAttribute(gemm::gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, gemm::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    gemm::gemm_kernel<false><<<grid, gemm::kThreads, gemm::SMEM_BYTES, st>>>(
-        mapA, mapB, a.As, a.Bs, a.TA, a.TB, (int)a.M, (int)a.N, (int)a.K, a.fmt, a.out, a.status,
-        a.wait_cycles, a.skip_loads ? 1 : 0);
+  const bool tma_codes = make_code_map(&mapAs, a.As, a.M, a.K, gemm::BM) &&
+                         make_code_map(&mapBs, a.Bs, a.N, a.K, gemm::BN);
+  if (!tma_codes) {
+    memset(&mapAs, 0, sizeof(mapAs));   // unused by the direct-load instantiation
+    memset(&mapBs, 0, sizeof(mapBs));
   }
-  return cudaGetLastError();
+  if (a.out_f32)
+    return tma_codes ? launch_gemm_t<true, true>(a, mapA, mapB, mapAs, mapBs, st)
+                     : launch_gemm_t<true, false>(a, mapA, mapB, mapAs, mapBs, st);
+  return tma_codes ? launch_gemm_t<false, true>(a, mapA, mapB, mapAs, mapBs, st)
+                   : launch_gemm_t<false, false>(a, mapA, mapB, mapAs, mapBs, st);
 }
 
 }  // namespace fp4q
