@@ -296,9 +296,10 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile_kernel(
         mul2f(a0, a1, re, xe[2 * q], xe[2 * q + 1]);
         mul2f(b0, b1, ro, xo[2 * q], xo[2 * q + 1]);
       }
-      float y0, y1, z0, z1;
-      mul2f(a0, b0, colr[2 * q], y0, y1);        // column 2q, rows 2p, 2p + 1
-      mul2f(a1, b1, colr[2 * q + 1], z0, z1);    // column 2q + 1
+      // column products as scalar multiplies: their operand pairs are not
+      // the register pairs the row products use
+      const float y0 = __fmul_rn(a0, colr[2 * q]), y1 = __fmul_rn(b0, colr[2 * q]);
+      const float z0 = __fmul_rn(a1, colr[2 * q + 1]), z1 = __fmul_rn(b1, colr[2 * q + 1]);
       const uint32_t by = e2m1x2(y0, y1), bz = e2m1x2(z0, z1);
       pcol[2 * q] = p == 0 ? by : put_byte(pcol[2 * q], by, p);
       pcol[2 * q + 1] = p == 0 ? bz : put_byte(pcol[2 * q + 1], bz, p);
@@ -337,38 +338,51 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile_kernel(
 }
 
 // ---------------------------------------------------------------- tiles, 16 x 4 pieces
-// The stochastic-rounding variant of the tile quantiser: its Philox work per
-// row needs the registers that a narrower piece frees.
-// Column-wise and dual-axis quantisation, register-resident.  A CTA covers
-// 128 rows x 128 columns: warp w takes rows 16 w .. +15 and lane l columns
-// 4 l .. +3, loading its 16 x 4 BF16 piece with sixteen coalesced 64-bit
-// loads (each load instruction of a warp reads one 256-byte row segment).
+// Column-wise and dual-axis stochastic-rounding quantisation,
+// register-resident; the narrower piece leaves the registers that the Philox
+// work needs.  A CTA covers 128 rows x 128 columns: warp w takes rows
+// 16 w .. +15 and lane l columns 4 l .. +3 (sixteen coalesced 64-bit loads,
+// each warp load one 256-byte row segment).
+//   magnitudes: one pass over the masked BF16 words gives the four column
+//     maxima over the lane's sixteen rows (each column block whole in the
+//     lane) and the row maxima over its four columns, packed two rows to a
+//     word;
 //   row blocks (dual axis): four consecutive lanes hold the 16 columns of a
-//     block (two shuffles per row for its amax); each lane converts its four
-//     elements of the row into two payload bytes;
-//   column blocks: a thread owns 4 complete column blocks (16 rows each);
-//     BF16 pairs of consecutive rows are gathered with byte permutes and
-//     converted eight at a time.  The eight warps of a CTA write the eight
-//     16-row pieces of each column's payload side by side (64 contiguous
-//     bytes per column).
+//     block; two butterfly shuffles per packed word complete the maxima of
+//     two rows, lane l computes the scales of the rows r with r % 4 = l % 4,
+//     and one shuffle per row pair hands each lane the reciprocals it lacks;
+//   conversion: one row pair at a time, each BF16 word of the pair is
+//     unpacked once and multiplied by its row and its column reciprocal; the
+//     row and the column products are rounded with the words of their own
+//     Philox streams.
 // Stochastic rounding draws one Philox block per row and axis: the four
-// words of counter (row C + 4 l) / 4 are exactly the thread's four elements.
-// Nothing goes through shared memory except the block-scale reciprocals.
+// words of counter (row C + 4 l) / 4 are exactly the lane's four elements.
+// The eight warps of a CTA write the eight 16-row pieces of each column's
+// payload side by side (64 contiguous bytes per column).  Nothing goes
+// through shared memory except the block-scale reciprocal table.
 
-template <bool SR, bool STATS, bool DO_ROW>
+// Stochastic rounding of the pair (q0, q1) with random words w0, w1 -> one
+// byte of two E2M1 nibbles (q0 low).
+__device__ __forceinline__ uint32_t sr_e2m1x2(float q0, float q1, uint32_t w0, uint32_t w1) {
+  const float m0 = sr_round_mag(fabsf(q0), w0), m1 = sr_round_mag(fabsf(q1), w1);
+  return e2m1x2(__uint_as_float(__float_as_uint(m0) | (__float_as_uint(q0) & 0x80000000u)),
+                __uint_as_float(__float_as_uint(m1) | (__float_as_uint(q1) & 0x80000000u)));
+}
+
+template <bool STATS, bool DO_ROW>
 __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile4_kernel(
     const uint16_t* __restrict__ in, int64_t R, int64_t C, int fmt,
-    const float* __restrict__ tscale, uint64_t seed, uint32_t* __restrict__ pay_row,
+    const float* __restrict__ tscale, uint64_t seed, uint8_t* __restrict__ pay_row,
     uint8_t* __restrict__ sc_row, uint8_t* __restrict__ pay_col, uint8_t* __restrict__ sc_col,
     StatsDev* stats, float* amax_out, int* status) {
   __shared__ ScaleTab tab;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int own = lane & 3;                                         // rows r with r % 4 == own
   const int64_t r0 = (int64_t)blockIdx.y * kRcRows + warp * 16;
   const int64_t c0 = (int64_t)blockIdx.x * kRcCols + lane * 4;
   // sizes are multiples of 16, so a 16-column block is either wholly inside
   // or wholly outside, and so is each 16 x 4 piece
   const bool ok = r0 < R && c0 < C;
-  uint32_t tmax = 0;
   uint32_t r_sat = 0, r_uflow = 0, r_clamp = 0, r_flush = 0;
   uint32_t c_sat = 0, c_uflow = 0, c_clamp = 0, c_flush = 0;
 
@@ -382,59 +396,34 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile4_kernel(
       v[rr] = make_uint2(0, 0);
     }
   }
-
   build_scale_tab(&tab, __ldg(tscale), fmt);   // while the piece is in flight
 
-  // ---- row blocks
+  // ---- magnitudes: cmx0 = columns 0 (low), 1 (high); cmx1 = columns 2, 3;
+  // rpx[i] = rows 2i (low), 2i + 1 (high)
+  uint32_t cmx0 = 0u, cmx1 = 0u, rpx[8];
 #pragma unroll
-  for (int rr = 0; rr < 16; ++rr) {
-    const uint32_t w[2] = {v[rr].x, v[rr].y};
-    uint32_t m = __vmaxu2(w[0] & 0x7FFF7FFFu, w[1] & 0x7FFF7FFFu);
-    m = max(m & 0xFFFFu, m >> 16);
-    tmax = max(tmax, m);
-    if (DO_ROW) {
-      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-      const int64_t e0 = (r0 + rr) * C + c0;  // logical index of the four elements
-      const BlockScale bs = block_scale<STATS>(m, tab);
-      uint4 rw = make_uint4(0, 0, 0, 0);
-      if (SR) rw = sr_words4((uint64_t)e0 >> 2, 0u, seed);
-      uint32_t c = 0, f = 0;
-      const uint32_t b0 = quantize_pair<SR, STATS>(w[0], bs.r, bs.r, rw.x, rw.y, &c, &f);
-      const uint32_t b1 = quantize_pair<SR, STATS>(w[1], bs.r, bs.r, rw.z, rw.w, &c, &f);
-      if (ok) {
-        *reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(pay_row) + (e0 >> 1)) =
-            (uint16_t)(b0 | (b1 << 8));
-        if ((lane & 3) == 0) sc_row[e0 >> 4] = (uint8_t)bs.code;
-        if (STATS) {
-          r_clamp += c;
-          r_flush += f;
-          if ((lane & 3) == 0) {
-            r_sat += bs.sat ? 1u : 0u;
-            r_uflow += (m != 0u && bs.code == 0u) ? 1u : 0u;
-          }
-        }
-      }
+  for (int i = 0; i < 8; ++i) {
+    uint32_t rm[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const uint32_t a = v[2 * i + k].x & 0x7FFF7FFFu, b = v[2 * i + k].y & 0x7FFF7FFFu;
+      cmx0 = __vmaxu2(cmx0, a);
+      cmx1 = __vmaxu2(cmx1, b);
+      rm[k] = __vmaxu2(a, b);
     }
+    rpx[i] = __vmaxu2(__byte_perm(rm[0], rm[1], 0x5410), __byte_perm(rm[0], rm[1], 0x7632));
   }
+  uint32_t tmax = __vmaxu2(cmx0, cmx1);
+  tmax = max(tmax & 0xFFFFu, tmax >> 16);
 
-  // ---- column blocks
-  uint32_t cw[4][8];   // [column j][row pair p] = BF16 of rows 2p (low), 2p+1 (high)
-#pragma unroll
-  for (int p = 0; p < 8; ++p) {
-    cw[0][p] = __byte_perm(v[2 * p].x, v[2 * p + 1].x, 0x5410);
-    cw[1][p] = __byte_perm(v[2 * p].x, v[2 * p + 1].x, 0x7632);
-    cw[2][p] = __byte_perm(v[2 * p].y, v[2 * p + 1].y, 0x5410);
-    cw[3][p] = __byte_perm(v[2 * p].y, v[2 * p + 1].y, 0x7632);
-  }
-  float rj[4];
+  // ---- column scales (whole blocks in the lane)
+  float rc[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const uint32_t w4a[4] = {cw[j][0], cw[j][1], cw[j][2], cw[j][3]};
-    const uint32_t w4b[4] = {cw[j][4], cw[j][5], cw[j][6], cw[j][7]};
-    const uint32_t cm = max(absmax16(w4a), absmax16(w4b));
+    const uint32_t w = j < 2 ? cmx0 : cmx1;
+    const uint32_t cm = (j & 1) ? (w >> 16) : (w & 0xFFFFu);
     const BlockScale bs = block_scale<STATS>(cm, tab);
-    rj[j] = bs.r;
+    rc[j] = bs.r;
     if (ok) {
       sc_col[(c0 + j) * (R / 16) + r0 / 16] = (uint8_t)bs.code;
       if (STATS) {
@@ -442,39 +431,93 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile4_kernel(
         c_uflow += (cm != 0u && bs.code == 0u) ? 1u : 0u;
       }
     }
-    if (!SR) {
-      uint32_t c = 0, f = 0;
-      const uint32_t nib0 = quantize8<false, STATS>(w4a, bs.r, nullptr, &c, &f);
-      const uint32_t nib1 = quantize8<false, STATS>(w4b, bs.r, nullptr, &c, &f);
+  }
+
+  // ---- row scales: this lane computes rows own, own + 4, own + 8, own + 12
+  float rown[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  if (DO_ROW) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      rpx[i] = __vmaxu2(rpx[i], __shfl_xor_sync(0xFFFFFFFFu, rpx[i], 1));
+      rpx[i] = __vmaxu2(rpx[i], __shfl_xor_sync(0xFFFFFFFFu, rpx[i], 2));
+    }
+    const uint32_t pick = (own & 1) ? 0x4432u : 0x4410u;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      // row 4k + own sits in word 2k + own / 2, half own % 2
+      const uint32_t w = (own >> 1) ? rpx[2 * k + 1] : rpx[2 * k];
+      const uint32_t m = __byte_perm(w, 0u, pick);
+      const BlockScale bs = block_scale<STATS>(m, tab);
+      rown[k] = bs.r;
       if (ok) {
-        *reinterpret_cast<uint2*>(pay_col + (c0 + j) * (R / 2) + r0 / 2) = make_uint2(nib0, nib1);
-        if (STATS) { c_clamp += c; c_flush += f; }
+        sc_row[((r0 + 4 * k + own) * C + (c0 & ~(int64_t)15)) >> 4] = (uint8_t)bs.code;
+        if (STATS) {
+          r_sat += bs.sat ? 1u : 0u;
+          r_uflow += (m != 0u && bs.code == 0u) ? 1u : 0u;
+        }
       }
     }
   }
-  if (SR) {
-    // one Philox block per row gives the column-axis words of its four
-    // elements (counter = logical index / 4, word = column offset)
-    uint32_t nib[4][2] = {{0u, 0u}, {0u, 0u}, {0u, 0u}, {0u, 0u}};
+
+  // ---- conversion, one row pair at a time
+  uint2 pcol[4] = {make_uint2(0, 0), make_uint2(0, 0), make_uint2(0, 0), make_uint2(0, 0)};
+  const int grp = lane & ~3;
 #pragma unroll
-    for (int p = 0; p < 8; ++p) {
-      const uint64_t e = (uint64_t)((r0 + 2 * p) * C + c0) >> 2;
-      const uint4 wa = sr_words4(e, 1u, seed);
-      const uint4 wb = sr_words4(e + ((uint64_t)C >> 2), 1u, seed);
-      const uint32_t ra[4] = {wa.x, wa.y, wa.z, wa.w}, rb_[4] = {wb.x, wb.y, wb.z, wb.w};
+  for (int p = 0; p < 8; ++p) {
+    const int64_t ea = ((r0 + 2 * p) * C + c0) >> 2, eb = ((r0 + 2 * p + 1) * C + c0) >> 2;
+    const uint4 ca = sr_words4((uint64_t)ea, 1u, seed), cb = sr_words4((uint64_t)eb, 1u, seed);
+    const uint32_t wca[4] = {ca.x, ca.y, ca.z, ca.w}, wcb[4] = {cb.x, cb.y, cb.z, cb.w};
+    float re = 0.0f, ro = 0.0f;
+    uint32_t wra[4], wrb[4];
+    if (DO_ROW) {
+      // rows 2p and 2p + 1 belong to lanes grp + (2p) % 4 and grp + (2p + 1) % 4
+      re = __shfl_sync(0xFFFFFFFFu, rown[p >> 1], grp + ((2 * p) & 3));
+      ro = __shfl_sync(0xFFFFFFFFu, rown[p >> 1], grp + ((2 * p + 1) & 3));
+      const uint4 ra = sr_words4((uint64_t)ea, 0u, seed), rb = sr_words4((uint64_t)eb, 0u, seed);
+      wra[0] = ra.x; wra[1] = ra.y; wra[2] = ra.z; wra[3] = ra.w;
+      wrb[0] = rb.x; wrb[1] = rb.y; wrb[2] = rb.z; wrb[3] = rb.w;
+    }
+    uint32_t rowa = 0u, rowb = 0u;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t c = 0, f = 0;
-        const uint32_t byte = quantize_pair<true, STATS>(cw[j][p], rj[j], rj[j], ra[j], rb_[j], &c, &f);
-        nib[j][p >> 2] |= byte << (8 * (p & 3));
-        if (STATS && ok) { c_clamp += c; c_flush += f; }
+    for (int q = 0; q < 2; ++q) {
+      const uint32_t wa = q ? v[2 * p].y : v[2 * p].x, wb = q ? v[2 * p + 1].y : v[2 * p + 1].x;
+      const float a0 = bf16_lo(wa), a1 = bf16_hi(wa), b0 = bf16_lo(wb), b1 = bf16_hi(wb);
+      if (DO_ROW) {
+        float x0, x1, y0, y1;
+        mul2f(a0, a1, re, x0, x1);
+        mul2f(b0, b1, ro, y0, y1);
+        const uint32_t ba = sr_e2m1x2(x0, x1, wra[2 * q], wra[2 * q + 1]);
+        const uint32_t bb = sr_e2m1x2(y0, y1, wrb[2 * q], wrb[2 * q + 1]);
+        rowa |= ba << (8 * q);
+        rowb |= bb << (8 * q);
+        if (STATS && ok) {
+          r_clamp += clamped2(x0, x1) + clamped2(y0, y1);
+          r_flush += flushed2(a0, a1, ba) + flushed2(b0, b1, bb);
+        }
+      }
+      // columns 2q (elements a0, b0) and 2q + 1 (a1, b1), rows 2p, 2p + 1
+      const float y0 = __fmul_rn(a0, rc[2 * q]), y1 = __fmul_rn(b0, rc[2 * q]);
+      const float z0 = __fmul_rn(a1, rc[2 * q + 1]), z1 = __fmul_rn(b1, rc[2 * q + 1]);
+      const uint32_t by = sr_e2m1x2(y0, y1, wca[2 * q], wcb[2 * q]);
+      const uint32_t bz = sr_e2m1x2(z0, z1, wca[2 * q + 1], wcb[2 * q + 1]);
+      uint32_t& py = (p < 4) ? pcol[2 * q].x : pcol[2 * q].y;
+      uint32_t& pz = (p < 4) ? pcol[2 * q + 1].x : pcol[2 * q + 1].y;
+      py = put_byte(py, by, p & 3);
+      pz = put_byte(pz, bz, p & 3);
+      if (STATS && ok) {
+        c_clamp += clamped2(y0, y1) + clamped2(z0, z1);
+        c_flush += flushed2(a0, b0, by) + flushed2(a1, b1, bz);
       }
     }
-    if (ok) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        *reinterpret_cast<uint2*>(pay_col + (c0 + j) * (R / 2) + r0 / 2) = make_uint2(nib[j][0], nib[j][1]);
+    if (DO_ROW && ok) {
+      *reinterpret_cast<uint16_t*>(pay_row + (((r0 + 2 * p) * C + c0) >> 1)) = (uint16_t)rowa;
+      *reinterpret_cast<uint16_t*>(pay_row + (((r0 + 2 * p + 1) * C + c0) >> 1)) = (uint16_t)rowb;
     }
+  }
+  if (ok) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      *reinterpret_cast<uint2*>(pay_col + (c0 + j) * (R / 2) + r0 / 2) = pcol[j];
   }
   if (STATS) {
     if (DO_ROW) flush_stats(stats, r_sat, r_uflow, r_clamp, r_flush);
@@ -562,8 +605,8 @@ static cudaError_t tile_launch(const QuantArgs& a, cudaStream_t st) {
   const uint16_t* in = static_cast<const uint16_t*>(a.in);
   uint32_t* pr = reinterpret_cast<uint32_t*>(a.pay_row);
   if constexpr (SR)
-    quantize_tile4_kernel<SR, STATS, DO_ROW><<<grid, kRcThreads, 0, st>>>(
-        in, a.rows, a.cols, a.fmt, a.tscale, a.seed, pr, a.sc_row, a.pay_col, a.sc_col, a.stats,
+    quantize_tile4_kernel<STATS, DO_ROW><<<grid, kRcThreads, 0, st>>>(
+        in, a.rows, a.cols, a.fmt, a.tscale, a.seed, a.pay_row, a.sc_row, a.pay_col, a.sc_col, a.stats,
         a.amax_out, a.status);
   else
     quantize_tile_kernel<STATS, DO_ROW><<<grid, kRcThreads, 0, st>>>(
