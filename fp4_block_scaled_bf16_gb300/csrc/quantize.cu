@@ -202,29 +202,21 @@ __device__ __forceinline__ uint32_t clamped2(float q0, float q1) {
   return (fabsf(q0) > 6.0f ? 1u : 0u) + (fabsf(q1) > 6.0f ? 1u : 0u);
 }
 
-template <bool STATS, bool DO_ROW>
-__global__ void __launch_bounds__(kRcThreads, 3) quantize_tile_kernel(
-    const uint16_t* __restrict__ in, int64_t R, int64_t C, int fmt,
-    const float* __restrict__ tscale, uint32_t* __restrict__ pay_row,
-    uint8_t* __restrict__ sc_row, uint8_t* __restrict__ pay_col, uint8_t* __restrict__ sc_col,
-    StatsDev* stats, float* amax_out, int* status) {
-  __shared__ ScaleTab tab;
-  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const int half = lane >> 4, cg = lane & 15, par = cg & 1;
-  const int64_t rb = (int64_t)blockIdx.y * kRcRows + warp * 16;   // first row of the column block
-  const int64_t r0 = rb + 8 * half;                                 // first of this lane's 8 rows
-  const int64_t c0 = (int64_t)blockIdx.x * kRcCols + cg * 8;
-  // sizes are multiples of 16: a 16 x 16 region is wholly inside or outside
-  const bool ok = rb < R && c0 < C;
+// Per-thread counters of the tile quantisers.
+struct TileCounts {
+  uint32_t tmax = 0;
   uint32_t r_sat = 0, r_uflow = 0, r_clamp = 0, r_flush = 0;
   uint32_t c_sat = 0, c_uflow = 0, c_clamp = 0, c_flush = 0;
+};
 
-  uint4 v[8];
-#pragma unroll
-  for (int rr = 0; rr < 8; ++rr)
-    v[rr] = ok ? ld_stream_v4(in + (r0 + rr) * C + c0) : make_uint4(0, 0, 0, 0);
-  build_scale_tab(&tab, __ldg(tscale), fmt);   // while the piece is in flight
-
+// One lane's 8 x 8 piece of a 128 x 128 tile: rows r0 .. r0 + 7 (r0 = rb or
+// rb + 8, rb the first row of the 16-row column block), columns c0 .. c0 + 7.
+template <bool STATS, bool DO_ROW>
+__device__ __forceinline__ void rne_piece(const uint4 (&v)[8], int64_t R, int64_t C, int64_t rb,
+                                          int64_t r0, int64_t c0, bool ok, int half, int par,
+                                          const ScaleTab& tab, uint32_t* __restrict__ pay_row,
+                                          uint8_t* __restrict__ sc_row, uint8_t* __restrict__ pay_col,
+                                          uint8_t* __restrict__ sc_col, TileCounts& cnt) {
   // ---- magnitudes: cmx[q] = maxima of columns 2q (low) and 2q + 1 (high);
   // rpx[p] = maxima of rows 2p (low) and 2p + 1 (high) over the lane's columns
   uint32_t cmx[4] = {0u, 0u, 0u, 0u}, rpx[4];
@@ -243,8 +235,8 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile_kernel(
     }
     rpx[p] = __vmaxu2(__byte_perm(rm[0], rm[1], 0x5410), __byte_perm(rm[0], rm[1], 0x7632));
   }
-  uint32_t tmax = __vmaxu2(__vmaxu2(cmx[0], cmx[1]), __vmaxu2(cmx[2], cmx[3]));
-  tmax = max(tmax & 0xFFFFu, tmax >> 16);
+  const uint32_t tm = __vmaxu2(__vmaxu2(cmx[0], cmx[1]), __vmaxu2(cmx[2], cmx[3]));
+  cnt.tmax = max(cnt.tmax, max(tm & 0xFFFFu, tm >> 16));
 
   // ---- column scales: this lane computes column 2q + half of word column q
   const uint32_t pick = half ? 0x4432u : 0x4410u;   // high or low 16 bits, zero-extended
@@ -260,8 +252,8 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile_kernel(
     if (ok) {
       sc_col[(c0 + 2 * q + half) * (R / 16) + rb / 16] = (uint8_t)bs.code;
       if (STATS) {
-        c_sat += bs.sat ? 1u : 0u;
-        c_uflow += (cm != 0u && bs.code == 0u) ? 1u : 0u;
+        cnt.c_sat += bs.sat ? 1u : 0u;
+        cnt.c_uflow += (cm != 0u && bs.code == 0u) ? 1u : 0u;
       }
     }
   }
@@ -282,8 +274,8 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile_kernel(
       if (ok) {
         sc_row[((r0 + 2 * p + par) * C + (c0 & ~(int64_t)15)) >> 4] = (uint8_t)bs.code;
         if (STATS) {
-          r_sat += bs.sat ? 1u : 0u;
-          r_uflow += (m != 0u && bs.code == 0u) ? 1u : 0u;
+          cnt.r_sat += bs.sat ? 1u : 0u;
+          cnt.r_uflow += (m != 0u && bs.code == 0u) ? 1u : 0u;
         }
       }
     }
@@ -304,8 +296,8 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile_kernel(
       pcol[2 * q] = p == 0 ? by : put_byte(pcol[2 * q], by, p);
       pcol[2 * q + 1] = p == 0 ? bz : put_byte(pcol[2 * q + 1], bz, p);
       if (STATS && ok) {
-        c_clamp += clamped2(y0, y1) + clamped2(z0, z1);
-        c_flush += flushed2(a0, b0, by) + flushed2(a1, b1, bz);
+        cnt.c_clamp += clamped2(y0, y1) + clamped2(z0, z1);
+        cnt.c_flush += flushed2(a0, b0, by) + flushed2(a1, b1, bz);
       }
     }
     if (DO_ROW) {
@@ -317,8 +309,8 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile_kernel(
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const uint32_t wa = word_of(v[2 * p], q), wb = word_of(v[2 * p + 1], q);
-            r_clamp += clamped2(xe[2 * q], xe[2 * q + 1]) + clamped2(xo[2 * q], xo[2 * q + 1]);
-            r_flush += flushed2(bf16_lo(wa), bf16_hi(wa), (ne >> (8 * q)) & 0xFFu) +
+            cnt.r_clamp += clamped2(xe[2 * q], xe[2 * q + 1]) + clamped2(xo[2 * q], xo[2 * q + 1]);
+            cnt.r_flush += flushed2(bf16_lo(wa), bf16_hi(wa), (ne >> (8 * q)) & 0xFFu) +
                        flushed2(bf16_lo(wb), bf16_hi(wb), (no >> (8 * q)) & 0xFFu);
           }
         }
@@ -330,11 +322,58 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile_kernel(
     for (int j = 0; j < 8; ++j)
       *reinterpret_cast<uint32_t*>(pay_col + (c0 + j) * (R / 2) + r0 / 2) = pcol[j];
   }
-  if (STATS) {
-    if (DO_ROW) flush_stats(stats, r_sat, r_uflow, r_clamp, r_flush);
-    flush_stats(stats + (DO_ROW ? 1 : 0), c_sat, c_uflow, c_clamp, c_flush);
+}
+
+// Persistent: each CTA walks tiles with a stride of the grid, the loads of
+// its next piece in flight while it converts the current one; the scale table
+// is built and the amax and counts are published once per CTA.
+template <bool STATS, bool DO_ROW>
+__global__ void __launch_bounds__(kRcThreads, 2) quantize_tile_kernel(
+    const uint16_t* __restrict__ in, int64_t R, int64_t C, int fmt,
+    const float* __restrict__ tscale, uint32_t* __restrict__ pay_row,
+    uint8_t* __restrict__ sc_row, uint8_t* __restrict__ pay_col, uint8_t* __restrict__ sc_col,
+    StatsDev* stats, float* amax_out, int* status) {
+  __shared__ ScaleTab tab;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int half = lane >> 4, cg = lane & 15, par = cg & 1;
+  const int64_t tiles_x = (C + kRcCols - 1) / kRcCols;
+  const int64_t ntiles = tiles_x * ((R + kRcRows - 1) / kRcRows);
+  TileCounts cnt;
+  // piece coordinates of tile `tile`; sizes are multiples of 16, so a 16 x 16
+  // region is wholly inside or outside
+  auto coords = [&](int64_t tile, int64_t& rb, int64_t& r0, int64_t& c0) {
+    rb = (tile / tiles_x) * kRcRows + warp * 16;
+    r0 = rb + 8 * half;
+    c0 = (tile % tiles_x) * kRcCols + cg * 8;
+    return tile < ntiles && rb < R && c0 < C;
+  };
+  auto load = [&](uint4 (&v)[8], int64_t r0, int64_t c0, bool ok) {
+#pragma unroll
+    for (int rr = 0; rr < 8; ++rr)
+      v[rr] = ok ? ld_stream_v4(in + (r0 + rr) * C + c0) : make_uint4(0, 0, 0, 0);
+  };
+  uint4 va[8], vb[8];
+  int64_t tile = blockIdx.x, rb, r0, c0;
+  bool ok = coords(tile, rb, r0, c0);
+  load(va, r0, c0, ok);
+  build_scale_tab(&tab, __ldg(tscale), fmt);   // while the first piece is in flight
+  const int64_t stride = gridDim.x;
+  // two tiles per trip, so that the two register buffers swap roles without copies
+  for (; tile < ntiles; tile += 2 * stride) {
+    int64_t rb1, r01, c01;
+    const bool ok1 = coords(tile + stride, rb1, r01, c01);
+    load(vb, r01, c01, ok1);
+    rne_piece<STATS, DO_ROW>(va, R, C, rb, r0, c0, ok, half, par, tab, pay_row, sc_row, pay_col, sc_col, cnt);
+    if (tile + stride >= ntiles) break;
+    ok = coords(tile + 2 * stride, rb, r0, c0);
+    load(va, r0, c0, ok);
+    rne_piece<STATS, DO_ROW>(vb, R, C, rb1, r01, c01, ok1, half, par, tab, pay_row, sc_row, pay_col, sc_col, cnt);
   }
-  flush_amax(amax_out, status, tmax);
+  if (STATS) {
+    if (DO_ROW) flush_stats(stats, cnt.r_sat, cnt.r_uflow, cnt.r_clamp, cnt.r_flush);
+    flush_stats(stats + (DO_ROW ? 1 : 0), cnt.c_sat, cnt.c_uflow, cnt.c_clamp, cnt.c_flush);
+  }
+  flush_amax(amax_out, status, cnt.tmax);
 }
 
 // ---------------------------------------------------------------- tiles, 16 x 4 pieces
@@ -602,6 +641,7 @@ static void row_launch(const QuantArgs& a, cudaStream_t st) {
 template <bool SR, bool STATS, bool DO_ROW>
 static cudaError_t tile_launch(const QuantArgs& a, cudaStream_t st) {
   dim3 grid((unsigned)((a.cols + kRcCols - 1) / kRcCols), (unsigned)((a.rows + kRcRows - 1) / kRcRows));
+  const int64_t ntiles = (int64_t)grid.x * grid.y;
   const uint16_t* in = static_cast<const uint16_t*>(a.in);
   uint32_t* pr = reinterpret_cast<uint32_t*>(a.pay_row);
   if constexpr (SR)
@@ -609,7 +649,7 @@ static cudaError_t tile_launch(const QuantArgs& a, cudaStream_t st) {
         in, a.rows, a.cols, a.fmt, a.tscale, a.seed, a.pay_row, a.sc_row, a.pay_col, a.sc_col, a.stats,
         a.amax_out, a.status);
   else
-    quantize_tile_kernel<STATS, DO_ROW><<<grid, kRcThreads, 0, st>>>(
+    quantize_tile_kernel<STATS, DO_ROW><<<grid_for(ntiles * kRcThreads, kRcThreads, 2), kRcThreads, 0, st>>>(
         in, a.rows, a.cols, a.fmt, a.tscale, pr, a.sc_row, a.pay_col, a.sc_col, a.stats,
         a.amax_out, a.status);
   return cudaGetLastError();
