@@ -221,6 +221,7 @@ template <bool F32OUT, bool TMA_CODES>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                 const __grid_constant__ CUtensorMap mapAs, const __grid_constant__ CUtensorMap mapBs,
+                const __grid_constant__ CUtensorMap mapC, int tma_store,
                 const uint8_t* __restrict__ As, const uint8_t* __restrict__ Bs,
                 const float* __restrict__ TA, const float* __restrict__ TB, int M, int N, int K,
                 int fmt, void* __restrict__ out, int* status, long long budget, int skip_loads) {
@@ -398,20 +399,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ------------------------------------------------ epilogue
     // warp w drains TMEM lanes 32 (w % 4) .. +31 of accumulator (w / 4) % 2,
-    // columns 128 (w / 8) .. +127.
-    if (mbar_wait(bar_acc, 0, abort_flag, budget)) {
+    // columns 128 (w / 8) .. +127.  BF16 output with a tensor map: the tile is
+    // staged in the idle expansion ring as four 256 x 64 boxes (128-byte
+    // swizzled) and leaves by TMA stores, whole lines, while the next CTA
+    // starts; otherwise every thread stores its 32 values directly.
+    const bool staged = !F32OUT && tma_store;
+    const bool drained = mbar_wait(bar_acc, 0, abort_flag, budget);
+    if (drained) {
       tc_fence_after();
       const int q = warp & 3, acc = (warp >> 2) & 1, half = warp >> 3;
       // T_A T_B, times 2^8 for the 2^-4 on each operand (exact)
       const float alpha = __fmul_rn(__fmul_rn(__ldg(TA), __ldg(TB)), 256.0f);
-      const int row = m0 + UM * acc + 32 * q + lane;
+      const int rt = UM * acc + 32 * q + lane;            // row within the tile
+      const int row = m0 + rt;
       const bool vec = F32OUT ? (N % 4 == 0) : (N % 8 == 0);
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
-        const int col0 = n0 + 128 * half + 32 * c;
+        const int ct = 128 * half + 32 * c;                // column within the tile
+        const int col0 = n0 + ct;
         uint32_t r[32];
-        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(BN * acc + 128 * half + 32 * c), r);
-        if (row >= M || col0 >= N) continue;
+        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(BN * acc + ct), r);
+        if (!staged && (row >= M || col0 >= N)) continue;
         float v[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(__uint_as_float(r[j]), alpha);
@@ -429,19 +437,39 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j)
             asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(h[j]) : "f"(v[2 * j + 1]), "f"(v[2 * j]));
-          uint16_t* o = static_cast<uint16_t*>(out) + (int64_t)row * N + col0;
-          if (vec && col0 + 32 <= N) {
+          if (staged) {
+            // box ct / 64, row rt, 16-byte chunks (ct % 64) / 8 + i, swizzled by row
+            const uint32_t rowb = sb + OFF_BF + (uint32_t)(ct >> 6) * (BM * 128) + (uint32_t)rt * 128;
+            const int ch0 = (ct & 63) >> 3;
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              reinterpret_cast<uint4*>(o)[j] = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+            for (int i = 0; i < 4; ++i)
+              sts128(rowb + ((uint32_t)((ch0 + i) ^ (rt & 7)) << 4),
+                     make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]));
           } else {
-            for (int j = 0; j < 32 && col0 + j < N; ++j)
-              o[j] = (uint16_t)((j & 1) ? (h[j >> 1] >> 16) : (h[j >> 1] & 0xFFFFu));
+            uint16_t* o = static_cast<uint16_t*>(out) + (int64_t)row * N + col0;
+            if (vec && col0 + 32 <= N) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                reinterpret_cast<uint4*>(o)[j] = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+            } else {
+              for (int j = 0; j < 32 && col0 + j < N; ++j)
+                o[j] = (uint16_t)((j & 1) ? (h[j >> 1] >> 16) : (h[j >> 1] & 0xFFFFu));
+            }
           }
         }
       }
     } else {
       fail(abort_flag, status);
+    }
+    if (staged) {
+      // every expansion warp passes here exactly once, drained or not
+      fence_proxy_async();
+      asm volatile("bar.sync 1, %0;" ::"n"(kDeqThreads) : "memory");
+      if (threadIdx.x == 0 && drained && !*abort_flag) {
+#pragma unroll
+        for (int j = 0; j < BN / 64; ++j) tma_store_2d(&mapC, sb + OFF_BF + j * (BM * 128), n0 + 64 * j, m0);
+        tma_store_commit_and_wait_read();
+      }
     }
   }
 
@@ -499,16 +527,32 @@ static bool make_code_map(CUtensorMap* map, const uint8_t* base, int64_t rows, i
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D BF16 tensor map over the [M, N] output, box (64 columns, 256 rows),
+// 128-byte swizzle; needs a row stride that is a multiple of 16 bytes.
+static bool make_out_map(CUtensorMap* map, void* base, int64_t M, int64_t N) {
+  auto fn = get_encode_fn();
+  if (!fn || N % 8 != 0) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+  const cuuint64_t strides[1] = {(cuuint64_t)(N * 2)};
+  const cuuint32_t box[2] = {64u, (cuuint32_t)gemm::BM};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <bool F32OUT, bool TMA_CODES>
 static cudaError_t launch_gemm_t(const GemmArgs& a, const CUtensorMap& mapA, const CUtensorMap& mapB,
-                                 const CUtensorMap& mapAs, const CUtensorMap& mapBs, cudaStream_t st) {
+                                 const CUtensorMap& mapAs, const CUtensorMap& mapBs,
+                                 const CUtensorMap& mapC, bool tma_store, cudaStream_t st) {
   constexpr int smem = gemm::smem_bytes(TMA_CODES);
   cudaError_t e = cudaFuncSetAttribute(gemm::gemm_kernel<F32OUT, TMA_CODES>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)((a.N + gemm::BN - 1) / gemm::BN), (unsigned)((a.M + gemm::BM - 1) / gemm::BM));
   gemm::gemm_kernel<F32OUT, TMA_CODES><<<grid, gemm::kThreads, smem, st>>>(
-      mapA, mapB, mapAs, mapBs, a.As, a.Bs, a.TA, a.TB, (int)a.M, (int)a.N, (int)a.K, a.fmt, a.out,
+      mapA, mapB, mapAs, mapBs, mapC, tma_store ? 1 : 0, a.As, a.Bs, a.TA, a.TB, (int)a.M, (int)a.N,
+      (int)a.K, a.fmt, a.out,
       a.status, a.wait_cycles, a.skip_loads ? 1 : 0);
   return cudaGetLastError();
 }
@@ -524,11 +568,14 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
     memset(&mapAs, 0, sizeof(mapAs));   // unused by the direct-load instantiation
     memset(&mapBs, 0, sizeof(mapBs));
   }
+  CUtensorMap mapC;
+  const bool tma_store = !a.out_f32 && make_out_map(&mapC, a.out, a.M, a.N);
+  if (!tma_store) memset(&mapC, 0, sizeof(mapC));
   if (a.out_f32)
-    return tma_codes ? launch_gemm_t<true, true>(a, mapA, mapB, mapAs, mapBs, st)
-                     : launch_gemm_t<true, false>(a, mapA, mapB, mapAs, mapBs, st);
-  return tma_codes ? launch_gemm_t<false, true>(a, mapA, mapB, mapAs, mapBs, st)
-                   : launch_gemm_t<false, false>(a, mapA, mapB, mapAs, mapBs, st);
+    return tma_codes ? launch_gemm_t<true, true>(a, mapA, mapB, mapAs, mapBs, mapC, false, st)
+                     : launch_gemm_t<true, false>(a, mapA, mapB, mapAs, mapBs, mapC, false, st);
+  return tma_codes ? launch_gemm_t<false, true>(a, mapA, mapB, mapAs, mapBs, mapC, tma_store, st)
+                   : launch_gemm_t<false, false>(a, mapA, mapB, mapAs, mapBs, mapC, tma_store, st);
 }
 
 }  // namespace fp4q

@@ -202,6 +202,47 @@ __device__ __forceinline__ uint32_t clamped2(float q0, float q1) {
   return (fabsf(q0) > 6.0f ? 1u : 0u) + (fabsf(q1) > 6.0f ? 1u : 0u);
 }
 
+// Column-wise outputs of one 128 x 128 tile, staged in shared memory so that
+// they leave as contiguous runs per column (the 8 x 8 pieces of a warp belong
+// to 32 different columns).  pay: per column 128 bytes of which 64 are used
+// (16 words of eight row nibbles); word g of column c sits at
+// 32 c + (g ^ 2 ((c >> 3) & 15)), which keeps word pairs (2k, 2k + 1) adjacent
+// and makes the writes of a warp conflict-free.  sc: 8 block codes per column.
+struct ColStage {
+  uint32_t pay[128 * 32];
+  uint8_t sc[128 * 8];
+};
+
+__device__ __forceinline__ int stage_word(int c, int g) { return 32 * c + (g ^ (2 * ((c >> 3) & 15))); }
+
+// Every thread of the CTA: the staged column outputs of the tile whose first
+// row and column are tr, tc -> global, 8-byte pieces (16 rows of a column).
+__device__ __forceinline__ void write_col_stage(const ColStage& st, int64_t R, int64_t C, int64_t tr,
+                                                int64_t tc, uint8_t* __restrict__ pay_col,
+                                                uint8_t* __restrict__ sc_col) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int k = threadIdx.x + kRcThreads * i;
+    const int c = k >> 3, piece = k & 7;
+    if (tc + c < C && tr + 16 * piece < R) {
+      const uint2 w = *reinterpret_cast<const uint2*>(&st.pay[stage_word(c, 2 * piece)]);
+      *reinterpret_cast<uint2*>(pay_col + (tc + c) * (R / 2) + tr / 2 + 8 * piece) = w;
+    }
+  }
+  if (threadIdx.x < 128) {
+    const int c = threadIdx.x;
+    if (tc + c < C) {
+      uint8_t* dst = sc_col + (tc + c) * (R / 16) + tr / 16;
+      const int nb = (int)((R - tr) / 16 < 8 ? (R - tr) / 16 : 8);
+      if (nb == 8 && (reinterpret_cast<uintptr_t>(dst) & 7) == 0) {
+        *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(&st.sc[8 * c]);
+      } else {
+        for (int b = 0; b < nb; ++b) dst[b] = st.sc[8 * c + b];
+      }
+    }
+  }
+}
+
 // Per-thread counters of the tile quantisers.
 struct TileCounts {
   uint32_t tmax = 0;
@@ -215,8 +256,8 @@ template <bool STATS, bool DO_ROW>
 __device__ __forceinline__ void rne_piece(const uint4 (&v)[8], int64_t R, int64_t C, int64_t rb,
                                           int64_t r0, int64_t c0, bool ok, int half, int par,
                                           const ScaleTab& tab, uint32_t* __restrict__ pay_row,
-                                          uint8_t* __restrict__ sc_row, uint8_t* __restrict__ pay_col,
-                                          uint8_t* __restrict__ sc_col, TileCounts& cnt) {
+                                          uint8_t* __restrict__ sc_row, ColStage& stage, int warp, int cg,
+                                          TileCounts& cnt) {
   // ---- magnitudes: cmx[q] = maxima of columns 2q (low) and 2q + 1 (high);
   // rpx[p] = maxima of rows 2p (low) and 2p + 1 (high) over the lane's columns
   uint32_t cmx[4] = {0u, 0u, 0u, 0u}, rpx[4];
@@ -249,8 +290,8 @@ __device__ __forceinline__ void rne_piece(const uint4 (&v)[8], int64_t R, int64_
     const float other = __shfl_xor_sync(0xFFFFFFFFu, bs.r, 16);
     colr[2 * q] = half ? other : bs.r;
     colr[2 * q + 1] = half ? bs.r : other;
+    stage.sc[8 * (8 * cg + 2 * q + half) + warp] = (uint8_t)bs.code;
     if (ok) {
-      sc_col[(c0 + 2 * q + half) * (R / 16) + rb / 16] = (uint8_t)bs.code;
       if (STATS) {
         cnt.c_sat += bs.sat ? 1u : 0u;
         cnt.c_uflow += (cm != 0u && bs.code == 0u) ? 1u : 0u;
@@ -317,11 +358,8 @@ __device__ __forceinline__ void rne_piece(const uint4 (&v)[8], int64_t R, int64_
       }
     }
   }
-  if (ok) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      *reinterpret_cast<uint32_t*>(pay_col + (c0 + j) * (R / 2) + r0 / 2) = pcol[j];
-  }
+  for (int j = 0; j < 8; ++j) stage.pay[stage_word(8 * cg + j, 2 * warp + half)] = pcol[j];
 }
 
 // Persistent: each CTA walks tiles with a stride of the grid, the loads of
@@ -334,6 +372,7 @@ __global__ void __launch_bounds__(kRcThreads, 2) quantize_tile_kernel(
     uint8_t* __restrict__ sc_row, uint8_t* __restrict__ pay_col, uint8_t* __restrict__ sc_col,
     StatsDev* stats, float* amax_out, int* status) {
   __shared__ ScaleTab tab;
+  __shared__ ColStage stage[2];   // double-buffered: one barrier per tile
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int half = lane >> 4, cg = lane & 15, par = cg & 1;
   const int64_t tiles_x = (C + kRcCols - 1) / kRcCols;
@@ -359,15 +398,21 @@ __global__ void __launch_bounds__(kRcThreads, 2) quantize_tile_kernel(
   build_scale_tab(&tab, __ldg(tscale), fmt);   // while the first piece is in flight
   const int64_t stride = gridDim.x;
   // two tiles per trip, so that the two register buffers swap roles without copies
+  auto flush_tile = [&](const ColStage& st, int64_t tl) {
+    __syncthreads();
+    write_col_stage(st, R, C, (tl / tiles_x) * kRcRows, (tl % tiles_x) * kRcCols, pay_col, sc_col);
+  };
   for (; tile < ntiles; tile += 2 * stride) {
     int64_t rb1, r01, c01;
     const bool ok1 = coords(tile + stride, rb1, r01, c01);
     load(vb, r01, c01, ok1);
-    rne_piece<STATS, DO_ROW>(va, R, C, rb, r0, c0, ok, half, par, tab, pay_row, sc_row, pay_col, sc_col, cnt);
+    rne_piece<STATS, DO_ROW>(va, R, C, rb, r0, c0, ok, half, par, tab, pay_row, sc_row, stage[0], warp, cg, cnt);
+    flush_tile(stage[0], tile);
     if (tile + stride >= ntiles) break;
     ok = coords(tile + 2 * stride, rb, r0, c0);
     load(va, r0, c0, ok);
-    rne_piece<STATS, DO_ROW>(vb, R, C, rb1, r01, c01, ok1, half, par, tab, pay_row, sc_row, pay_col, sc_col, cnt);
+    rne_piece<STATS, DO_ROW>(vb, R, C, rb1, r01, c01, ok1, half, par, tab, pay_row, sc_row, stage[1], warp, cg, cnt);
+    flush_tile(stage[1], tile + stride);
   }
   if (STATS) {
     if (DO_ROW) flush_stats(stats, cnt.r_sat, cnt.r_uflow, cnt.r_clamp, cnt.r_flush);
