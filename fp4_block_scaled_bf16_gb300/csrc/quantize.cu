@@ -460,6 +460,7 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile4_kernel(
     uint8_t* __restrict__ sc_row, uint8_t* __restrict__ pay_col, uint8_t* __restrict__ sc_col,
     StatsDev* stats, float* amax_out, int* status) {
   __shared__ ScaleTab tab;
+  __shared__ ColStage stage;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int own = lane & 3;                                         // rows r with r % 4 == own
   const int64_t r0 = (int64_t)blockIdx.y * kRcRows + warp * 16;
@@ -508,8 +509,8 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile4_kernel(
     const uint32_t cm = (j & 1) ? (w >> 16) : (w & 0xFFFFu);
     const BlockScale bs = block_scale<STATS>(cm, tab);
     rc[j] = bs.r;
+    stage.sc[8 * (4 * lane + j) + warp] = (uint8_t)bs.code;
     if (ok) {
-      sc_col[(c0 + j) * (R / 16) + r0 / 16] = (uint8_t)bs.code;
       if (STATS) {
         c_sat += bs.sat ? 1u : 0u;
         c_uflow += (cm != 0u && bs.code == 0u) ? 1u : 0u;
@@ -598,11 +599,11 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile4_kernel(
       *reinterpret_cast<uint16_t*>(pay_row + (((r0 + 2 * p + 1) * C + c0) >> 1)) = (uint16_t)rowb;
     }
   }
-  if (ok) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      *reinterpret_cast<uint2*>(pay_col + (c0 + j) * (R / 2) + r0 / 2) = pcol[j];
-  }
+  for (int j = 0; j < 4; ++j)
+    *reinterpret_cast<uint2*>(&stage.pay[stage_word(4 * lane + j, 2 * warp)]) = pcol[j];
+  __syncthreads();
+  write_col_stage(stage, R, C, (int64_t)blockIdx.y * kRcRows, (int64_t)blockIdx.x * kRcCols, pay_col, sc_col);
   if (STATS) {
     if (DO_ROW) flush_stats(stats, r_sat, r_uflow, r_clamp, r_flush);
     flush_stats(stats + (DO_ROW ? 1 : 0), c_sat, c_uflow, c_clamp, c_flush);
