@@ -70,6 +70,7 @@ def _load():
             "orc_amax_bf16": (f32, [P, i64, P]),
             "orc_tensor_scale": (f32, [f32, i32, f32]),
             "orc_quantize": (None, [P, i64, i64, i32, i32, f32, i32, u64, P, P, P]),
+            "orc_quantize_2d": (None, [P, i64, i64, i32, f32, i32, u64, P, P, P, P, P]),
             "orc_dequantize": (None, [P, P, i64, i64, i32, f32, P, P]),
             "orc_gemm": (None, [P, P, f32, P, P, f32, i64, i64, i64, i32, P, P, i64, P]),
             "orc_deq_es_matrix": (None, [P, P, i64, i64, i32, P]),
@@ -195,6 +196,26 @@ def quantize(x, axis: int, T: float, fmt: int = UE5M3, rnd: int = RNE, seed: int
     _load().orc_quantize(_ptr(x), rows, cols, int(axis), int(fmt), float(T), int(rnd),
                          ctypes.c_uint64(seed), _ptr(payload), _ptr(scales), _ptr(stats))
     return payload, scales, stats
+
+
+def quantize_2d(x, T: float, fmt: int = UE5M3, rnd: int = RNE, seed: int = 0):
+    """One scale per 16 x 16 tile, both layouts from one quantisation.
+
+    Returns (payload_row [rows, cols/2], scales_row [rows, cols/16],
+    payload_col [cols, rows/2], scales_col [cols, rows/16], stats uint64[4]).
+    """
+    x = _as_bf16_bits(x)
+    rows, cols = x.shape
+    if rows % 16 or cols % 16:
+        raise ValueError("rows and cols must be multiples of 16")
+    pr = np.zeros((rows, cols // 2), np.uint8)
+    sr = np.zeros((rows, cols // 16), np.uint8)
+    pc = np.zeros((cols, rows // 2), np.uint8)
+    sc = np.zeros((cols, rows // 16), np.uint8)
+    stats = np.zeros(4, np.uint64)
+    _load().orc_quantize_2d(_ptr(x), rows, cols, int(fmt), float(T), int(rnd), ctypes.c_uint64(seed),
+                            _ptr(pr), _ptr(sr), _ptr(pc), _ptr(sc), _ptr(stats))
+    return pr, sr, pc, sc, stats
 
 
 def dequantize(payload, scales, T: float, fmt: int = UE5M3):

@@ -318,6 +318,67 @@ void orc_quantize(const uint16_t *x, int64_t rows, int64_t cols, int axis, int f
     }
 }
 
+/* Two-dimensional (16 x 16) block scaling -- the transposition-invariant
+ * variant named among the related work of "UE5M3 FP4 Block Scaling for Stable
+ * Language Model Pretraining" (Related papers: "Stable FP4 Training via
+ * Transposition-Invariant Block Quantization").  Reading: one UE5M3 scale per
+ * 16 x 16 tile, chosen by the block rule above with the tile's amax, and one
+ * quantisation per element with that scale (SR with the row-wise random
+ * stream, axis id 0); the result is written in both layouts, so that the
+ * column-wise operand is exactly the transpose of the row-wise one.
+ *   pay_row/sc_row: as axis ROW, sc_row[r, b] = code of tile (r/16, b);
+ *   pay_col/sc_col: as axis COL, sc_col[c, b] = code of tile (b, c/16).
+ * stats[4]: scale counts per tile, element counts once per element. */
+void orc_quantize_2d(const uint16_t *x, int64_t rows, int64_t cols, int fmt, float T, int rnd,
+                     uint64_t seed, uint8_t *pay_row, uint8_t *sc_row, uint8_t *pay_col,
+                     uint8_t *sc_col, uint64_t stats[4]) {
+    for (int64_t tr = 0; tr < rows / 16; ++tr) {
+        for (int64_t tc = 0; tc < cols / 16; ++tc) {
+            /* tile amax (exact) and its scale, as for a block of 16 */
+            float amax_t = 0.0f;
+            for (int i = 0; i < 16; ++i)
+                for (int j = 0; j < 16; ++j) {
+                    float a = fabsf(bf16_to_f32(x[(16 * tr + i) * cols + 16 * tc + j]));
+                    if (a > amax_t) amax_t = a;
+                }
+            float six_t = 6.0f * T;
+            float s_star = amax_t / six_t;
+            int sat = 0;
+            uint8_t code = orc_scale_encode(s_star, fmt, &sat);
+            if (sat) stats[ST_SCALE_SAT]++;
+            if (amax_t > 0.0f && code == 0) stats[ST_SCALE_UFLOW]++;
+            float s = (float)orc_scale_decode(code, fmt);
+            float r = (s == 0.0f) ? 0.0f : 1.0f / (s * T);
+            for (int i = 0; i < 16; ++i) {
+                int64_t row = 16 * tr + i;
+                for (int j = 0; j < 16; ++j) {
+                    int64_t col = 16 * tc + j;
+                    int64_t idx = row * cols + col;            /* logical index */
+                    float v = bf16_to_f32(x[idx]);
+                    uint8_t n;
+                    if (s == 0.0f) {
+                        n = signbit(v) ? 8 : 0;
+                        if (v != 0.0f) stats[ST_ELEM_FLUSH]++;
+                    } else {
+                        float q = v * r;
+                        if (fabsf(q) > 6.0f) stats[ST_ELEM_CLAMP]++;
+                        n = (rnd == ORC_SR) ? orc_e2m1_sr(q, orc_sr_word(seed, (uint64_t)idx, 0u))
+                                            : orc_e2m1_rne(q);
+                        if (v != 0.0f && (n & 7) == 0) stats[ST_ELEM_FLUSH]++;
+                    }
+                    /* row layout: byte (row, col/2); column layout: byte (col, row/2) */
+                    uint8_t *br = &pay_row[row * (cols / 2) + col / 2];
+                    *br = (col & 1) ? (uint8_t)((*br & 0x0f) | (n << 4)) : (uint8_t)((*br & 0xf0) | n);
+                    uint8_t *bc = &pay_col[col * (rows / 2) + row / 2];
+                    *bc = (row & 1) ? (uint8_t)((*bc & 0x0f) | (n << 4)) : (uint8_t)((*bc & 0xf0) | n);
+                }
+                sc_row[row * (cols / 16) + tc] = code;
+            }
+            for (int j = 0; j < 16; ++j) sc_col[(16 * tc + j) * (rows / 16) + tr] = code;
+        }
+    }
+}
+
 /* ------------------------------------------------------------------------ */
 /* Dequantisation and the GEMM                                               */
 /* ------------------------------------------------------------------------ */
