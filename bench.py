@@ -344,6 +344,20 @@ def run_gpu(args, rank, world):
         a1.record()
         torch.cuda.synchronize()
         rates[name] = x.numel() * ROW_BYTES_PER_ELEM / (a0.elapsed_time(a1) / 10 * 1e-3) / 1e9
+    # 16 x 16 (transposition-invariant) scaling: both layouts from one
+    # quantisation, same algorithmic bytes as the dual-axis quantisers
+    for name, x, rnd, outs in (("W_2d_rne", step.W, fp4q.RNE, (step.Wr, step.Wrs, step.Wc, step.Wcs)),
+                               ("dY_2d_sr", step.dY, fp4q.SR, (step.Dr, step.Drs, step.Dc, step.Dcs))):
+        Tn = step.T[1:2] if x is step.W else step.T[2:3]
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        fp4q.fp4q_quantize(x, fp4q.AXIS_BOTH_2D, fp4q.UE5M3, Tn, rnd, 7, *outs)
+        a0.record()
+        for _ in range(10):
+            fp4q.fp4q_quantize(x, fp4q.AXIS_BOTH_2D, fp4q.UE5M3, Tn, rnd, 7, *outs)
+        a1.record()
+        torch.cuda.synchronize()
+        rates[name] = x.numel() * DUAL_BYTES_PER_ELEM / (a0.elapsed_time(a1) / 10 * 1e-3) / 1e9
     return dict(ms=ms, ms_serial=ms_serial, t_scale=t_scale, t_q=(t_qx, t_qw, t_qd), t_g=t_g, launches=launches, rates=rates,
                 clocks=clk.summary(), status=status, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
                 elems=(X.numel(), W.numel(), dY.numel()))

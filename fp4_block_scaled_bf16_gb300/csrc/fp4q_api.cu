@@ -76,7 +76,8 @@ fp4q_status fp4q_quantize(const void* in_bf16, int64_t rows, int64_t cols, fp4q_
                           uint64_t seed, uint8_t* out_payload_row, uint8_t* out_scales_row,
                           uint8_t* out_payload_col, uint8_t* out_scales_col, fp4q_stats* out_stats,
                           float* out_amax, void* stream) {
-  if (axis != FP4Q_AXIS_ROW && axis != FP4Q_AXIS_COL && axis != FP4Q_AXIS_BOTH) return FP4Q_ERR_ARG;
+  if (axis != FP4Q_AXIS_ROW && axis != FP4Q_AXIS_COL && axis != FP4Q_AXIS_BOTH && axis != FP4Q_AXIS_BOTH_2D)
+    return FP4Q_ERR_ARG;
   if (!valid_fmt(fmt) || (rnd != FP4Q_RNE && rnd != FP4Q_SR) || !tensor_scale) return FP4Q_ERR_ARG;
   if (rows < 0 || cols < 0 || rows % 16 || cols % 16) return FP4Q_ERR_SHAPE;
   const bool row = axis != FP4Q_AXIS_COL, col = axis != FP4Q_AXIS_ROW;

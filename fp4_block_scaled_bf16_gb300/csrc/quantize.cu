@@ -252,7 +252,9 @@ struct TileCounts {
 
 // One lane's 8 x 8 piece of a 128 x 128 tile: rows r0 .. r0 + 7 (r0 = rb or
 // rb + 8, rb the first row of the 16-row column block), columns c0 .. c0 + 7.
-template <bool STATS, bool DO_ROW>
+// TWO_D: one scale per 16 x 16 tile (lanes l, l ^ 1, l ^ 16, l ^ 17), used by
+// both layouts, which then hold the same nibbles transposed.
+template <bool STATS, bool DO_ROW, bool TWO_D>
 __device__ __forceinline__ void rne_piece(const uint4 (&v)[8], int64_t R, int64_t C, int64_t rb,
                                           int64_t r0, int64_t c0, bool ok, int half, int par,
                                           const ScaleTab& tab, uint32_t* __restrict__ pay_row,
@@ -279,11 +281,28 @@ __device__ __forceinline__ void rne_piece(const uint4 (&v)[8], int64_t R, int64_
   const uint32_t tm = __vmaxu2(__vmaxu2(cmx[0], cmx[1]), __vmaxu2(cmx[2], cmx[3]));
   cnt.tmax = max(cnt.tmax, max(tm & 0xFFFFu, tm >> 16));
 
+  BlockScale ts;   // the 16 x 16 tile's scale (TWO_D)
+  if (TWO_D) {
+    uint32_t m = max(tm & 0xFFFFu, tm >> 16);
+    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
+    ts = block_scale<STATS>(m, tab);
+    if (STATS && ok && par == 0 && half == 0) {
+      cnt.r_sat += ts.sat ? 1u : 0u;
+      cnt.r_uflow += (m != 0u && ts.code == 0u) ? 1u : 0u;
+    }
+  }
+
   // ---- column scales: this lane computes column 2q + half of word column q
   const uint32_t pick = half ? 0x4432u : 0x4410u;   // high or low 16 bits, zero-extended
   float colr[8];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < 4 && TWO_D; ++q) {
+    colr[2 * q] = colr[2 * q + 1] = ts.r;
+    stage.sc[8 * (8 * cg + 2 * q + half) + warp] = (uint8_t)ts.code;
+  }
+#pragma unroll
+  for (int q = 0; q < 4 && !TWO_D; ++q) {
     const uint32_t full = __vmaxu2(cmx[q], __shfl_xor_sync(0xFFFFFFFFu, cmx[q], 16));
     const uint32_t cm = __byte_perm(full, 0u, pick);
     const BlockScale bs = block_scale<STATS>(cm, tab);
@@ -305,7 +324,10 @@ __device__ __forceinline__ void rne_piece(const uint4 (&v)[8], int64_t R, int64_
 #pragma unroll
   for (int p = 0; p < 4; ++p) {
     float re = 0.0f, ro = 0.0f;   // row reciprocals of rows 2p and 2p + 1
-    if (DO_ROW) {
+    if (DO_ROW && TWO_D) {
+      re = ro = ts.r;
+      if (ok) sc_row[((r0 + 2 * p + par) * C + (c0 & ~(int64_t)15)) >> 4] = (uint8_t)ts.code;
+    } else if (DO_ROW) {
       const uint32_t full = __vmaxu2(rpx[p], __shfl_xor_sync(0xFFFFFFFFu, rpx[p], 1));
       const uint32_t m = __byte_perm(full, 0u, rpick);          // row 2p + par
       const BlockScale bs = block_scale<STATS>(m, tab);
@@ -336,7 +358,7 @@ __device__ __forceinline__ void rne_piece(const uint4 (&v)[8], int64_t R, int64_
       const uint32_t by = e2m1x2(y0, y1), bz = e2m1x2(z0, z1);
       pcol[2 * q] = p == 0 ? by : put_byte(pcol[2 * q], by, p);
       pcol[2 * q + 1] = p == 0 ? bz : put_byte(pcol[2 * q + 1], bz, p);
-      if (STATS && ok) {
+      if (STATS && !TWO_D && ok) {
         cnt.c_clamp += clamped2(y0, y1) + clamped2(z0, z1);
         cnt.c_flush += flushed2(a0, b0, by) + flushed2(a1, b1, bz);
       }
@@ -365,7 +387,7 @@ __device__ __forceinline__ void rne_piece(const uint4 (&v)[8], int64_t R, int64_
 // Persistent: each CTA walks tiles with a stride of the grid, the loads of
 // its next piece in flight while it converts the current one; the scale table
 // is built and the amax and counts are published once per CTA.
-template <bool STATS, bool DO_ROW>
+template <bool STATS, bool DO_ROW, bool TWO_D>
 __global__ void __launch_bounds__(kRcThreads, 2) quantize_tile_kernel(
     const uint16_t* __restrict__ in, int64_t R, int64_t C, int fmt,
     const float* __restrict__ tscale, uint32_t* __restrict__ pay_row,
@@ -406,17 +428,17 @@ __global__ void __launch_bounds__(kRcThreads, 2) quantize_tile_kernel(
     int64_t rb1, r01, c01;
     const bool ok1 = coords(tile + stride, rb1, r01, c01);
     load(vb, r01, c01, ok1);
-    rne_piece<STATS, DO_ROW>(va, R, C, rb, r0, c0, ok, half, par, tab, pay_row, sc_row, stage[0], warp, cg, cnt);
+    rne_piece<STATS, DO_ROW, TWO_D>(va, R, C, rb, r0, c0, ok, half, par, tab, pay_row, sc_row, stage[0], warp, cg, cnt);
     flush_tile(stage[0], tile);
     if (tile + stride >= ntiles) break;
     ok = coords(tile + 2 * stride, rb, r0, c0);
     load(va, r0, c0, ok);
-    rne_piece<STATS, DO_ROW>(vb, R, C, rb1, r01, c01, ok1, half, par, tab, pay_row, sc_row, stage[1], warp, cg, cnt);
+    rne_piece<STATS, DO_ROW, TWO_D>(vb, R, C, rb1, r01, c01, ok1, half, par, tab, pay_row, sc_row, stage[1], warp, cg, cnt);
     flush_tile(stage[1], tile + stride);
   }
   if (STATS) {
     if (DO_ROW) flush_stats(stats, cnt.r_sat, cnt.r_uflow, cnt.r_clamp, cnt.r_flush);
-    flush_stats(stats + (DO_ROW ? 1 : 0), cnt.c_sat, cnt.c_uflow, cnt.c_clamp, cnt.c_flush);
+    if (!TWO_D) flush_stats(stats + (DO_ROW ? 1 : 0), cnt.c_sat, cnt.c_uflow, cnt.c_clamp, cnt.c_flush);
   }
   flush_amax(amax_out, status, cnt.tmax);
 }
@@ -453,7 +475,10 @@ __device__ __forceinline__ uint32_t sr_e2m1x2(float q0, float q1, uint32_t w0, u
                 __uint_as_float(__float_as_uint(m1) | (__float_as_uint(q1) & 0x80000000u)));
 }
 
-template <bool STATS, bool DO_ROW>
+// TWO_D: one scale per 16 x 16 tile (the four lanes of a group), and one
+// quantisation per element with the row-wise random stream, written in both
+// layouts.
+template <bool STATS, bool DO_ROW, bool TWO_D>
 __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile4_kernel(
     const uint16_t* __restrict__ in, int64_t R, int64_t C, int fmt,
     const float* __restrict__ tscale, uint64_t seed, uint8_t* __restrict__ pay_row,
@@ -501,10 +526,26 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile4_kernel(
   uint32_t tmax = __vmaxu2(cmx0, cmx1);
   tmax = max(tmax & 0xFFFFu, tmax >> 16);
 
+  BlockScale ts;   // the 16 x 16 tile's scale (TWO_D)
+  if (TWO_D) {
+    uint32_t m = max(tmax, __shfl_xor_sync(0xFFFFFFFFu, tmax, 1));
+    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+    ts = block_scale<STATS>(m, tab);
+    if (STATS && ok && own == 0) {
+      r_sat += ts.sat ? 1u : 0u;
+      r_uflow += (m != 0u && ts.code == 0u) ? 1u : 0u;
+    }
+  }
+
   // ---- column scales (whole blocks in the lane)
   float rc[4];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int j = 0; j < 4 && TWO_D; ++j) {
+    rc[j] = ts.r;
+    stage.sc[8 * (4 * lane + j) + warp] = (uint8_t)ts.code;
+  }
+#pragma unroll
+  for (int j = 0; j < 4 && !TWO_D; ++j) {
     const uint32_t w = j < 2 ? cmx0 : cmx1;
     const uint32_t cm = (j & 1) ? (w >> 16) : (w & 0xFFFFu);
     const BlockScale bs = block_scale<STATS>(cm, tab);
@@ -520,7 +561,11 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile4_kernel(
 
   // ---- row scales: this lane computes rows own, own + 4, own + 8, own + 12
   float rown[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-  if (DO_ROW) {
+  if (DO_ROW && TWO_D) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (ok) sc_row[((r0 + 4 * k + own) * C + (c0 & ~(int64_t)15)) >> 4] = (uint8_t)ts.code;
+  } else if (DO_ROW) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       rpx[i] = __vmaxu2(rpx[i], __shfl_xor_sync(0xFFFFFFFFu, rpx[i], 1));
@@ -550,17 +595,28 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile4_kernel(
 #pragma unroll
   for (int p = 0; p < 8; ++p) {
     const int64_t ea = ((r0 + 2 * p) * C + c0) >> 2, eb = ((r0 + 2 * p + 1) * C + c0) >> 2;
-    const uint4 ca = sr_words4((uint64_t)ea, 1u, seed), cb = sr_words4((uint64_t)eb, 1u, seed);
-    const uint32_t wca[4] = {ca.x, ca.y, ca.z, ca.w}, wcb[4] = {cb.x, cb.y, cb.z, cb.w};
     float re = 0.0f, ro = 0.0f;
-    uint32_t wra[4], wrb[4];
+    uint32_t wra[4], wrb[4], wca[4], wcb[4];
     if (DO_ROW) {
-      // rows 2p and 2p + 1 belong to lanes grp + (2p) % 4 and grp + (2p + 1) % 4
-      re = __shfl_sync(0xFFFFFFFFu, rown[p >> 1], grp + ((2 * p) & 3));
-      ro = __shfl_sync(0xFFFFFFFFu, rown[p >> 1], grp + ((2 * p + 1) & 3));
+      if (TWO_D) {
+        re = ro = ts.r;
+      } else {
+        // rows 2p and 2p + 1 belong to lanes grp + (2p) % 4 and grp + (2p + 1) % 4
+        re = __shfl_sync(0xFFFFFFFFu, rown[p >> 1], grp + ((2 * p) & 3));
+        ro = __shfl_sync(0xFFFFFFFFu, rown[p >> 1], grp + ((2 * p + 1) & 3));
+      }
       const uint4 ra = sr_words4((uint64_t)ea, 0u, seed), rb = sr_words4((uint64_t)eb, 0u, seed);
       wra[0] = ra.x; wra[1] = ra.y; wra[2] = ra.z; wra[3] = ra.w;
       wrb[0] = rb.x; wrb[1] = rb.y; wrb[2] = rb.z; wrb[3] = rb.w;
+    }
+    if (TWO_D) {
+      // one quantisation per element: the column layout repeats the row words
+#pragma unroll
+      for (int k = 0; k < 4; ++k) { wca[k] = wra[k]; wcb[k] = wrb[k]; }
+    } else {
+      const uint4 ca = sr_words4((uint64_t)ea, 1u, seed), cb = sr_words4((uint64_t)eb, 1u, seed);
+      wca[0] = ca.x; wca[1] = ca.y; wca[2] = ca.z; wca[3] = ca.w;
+      wcb[0] = cb.x; wcb[1] = cb.y; wcb[2] = cb.z; wcb[3] = cb.w;
     }
     uint32_t rowa = 0u, rowb = 0u;
 #pragma unroll
@@ -589,7 +645,7 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile4_kernel(
       uint32_t& pz = (p < 4) ? pcol[2 * q + 1].x : pcol[2 * q + 1].y;
       py = put_byte(py, by, p & 3);
       pz = put_byte(pz, bz, p & 3);
-      if (STATS && ok) {
+      if (STATS && !TWO_D && ok) {
         c_clamp += clamped2(y0, y1) + clamped2(z0, z1);
         c_flush += flushed2(a0, b0, by) + flushed2(a1, b1, bz);
       }
@@ -606,7 +662,7 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile4_kernel(
   write_col_stage(stage, R, C, (int64_t)blockIdx.y * kRcRows, (int64_t)blockIdx.x * kRcCols, pay_col, sc_col);
   if (STATS) {
     if (DO_ROW) flush_stats(stats, r_sat, r_uflow, r_clamp, r_flush);
-    flush_stats(stats + (DO_ROW ? 1 : 0), c_sat, c_uflow, c_clamp, c_flush);
+    if (!TWO_D) flush_stats(stats + (DO_ROW ? 1 : 0), c_sat, c_uflow, c_clamp, c_flush);
   }
   flush_amax(amax_out, status, tmax);
 }
@@ -684,18 +740,18 @@ static void row_launch(const QuantArgs& a, cudaStream_t st) {
       reinterpret_cast<uint32_t*>(a.pay_row), a.sc_row, a.stats, a.amax_out, a.status);
 }
 
-template <bool SR, bool STATS, bool DO_ROW>
+template <bool SR, bool STATS, bool DO_ROW, bool TWO_D = false>
 static cudaError_t tile_launch(const QuantArgs& a, cudaStream_t st) {
   dim3 grid((unsigned)((a.cols + kRcCols - 1) / kRcCols), (unsigned)((a.rows + kRcRows - 1) / kRcRows));
   const int64_t ntiles = (int64_t)grid.x * grid.y;
   const uint16_t* in = static_cast<const uint16_t*>(a.in);
   uint32_t* pr = reinterpret_cast<uint32_t*>(a.pay_row);
   if constexpr (SR)
-    quantize_tile4_kernel<STATS, DO_ROW><<<grid, kRcThreads, 0, st>>>(
+    quantize_tile4_kernel<STATS, DO_ROW, TWO_D><<<grid, kRcThreads, 0, st>>>(
         in, a.rows, a.cols, a.fmt, a.tscale, a.seed, a.pay_row, a.sc_row, a.pay_col, a.sc_col, a.stats,
         a.amax_out, a.status);
   else
-    quantize_tile_kernel<STATS, DO_ROW><<<grid_for(ntiles * kRcThreads, kRcThreads, 2), kRcThreads, 0, st>>>(
+    quantize_tile_kernel<STATS, DO_ROW, TWO_D><<<grid_for(ntiles * kRcThreads, kRcThreads, 2), kRcThreads, 0, st>>>(
         in, a.rows, a.cols, a.fmt, a.tscale, pr, a.sc_row, a.pay_col, a.sc_col, a.stats,
         a.amax_out, a.status);
   return cudaGetLastError();
@@ -721,6 +777,10 @@ cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t st) {
   if (a.axis == 1) {
     if (sr) return stats ? tile_launch<true, true, false>(a, st) : tile_launch<true, false, false>(a, st);
     return stats ? tile_launch<false, true, false>(a, st) : tile_launch<false, false, false>(a, st);
+  }
+  if (a.axis == 3) {   // one scale per 16 x 16 tile, both layouts
+    if (sr) return stats ? tile_launch<true, true, true, true>(a, st) : tile_launch<true, false, true, true>(a, st);
+    return stats ? tile_launch<false, true, true, true>(a, st) : tile_launch<false, false, true, true>(a, st);
   }
   if (sr) return stats ? tile_launch<true, true, true>(a, st) : tile_launch<true, false, true>(a, st);
   return stats ? tile_launch<false, true, true>(a, st) : tile_launch<false, false, true>(a, st);

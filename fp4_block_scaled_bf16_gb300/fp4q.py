@@ -20,7 +20,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libfp4q.so")
 
 OK, ERR_ARG, ERR_SHAPE, ERR_ALIGN, ERR_CUDA, ERR_NONFINITE, ERR_TIMEOUT = range(7)
-AXIS_ROW, AXIS_COL, AXIS_BOTH = 0, 1, 2
+AXIS_ROW, AXIS_COL, AXIS_BOTH, AXIS_BOTH_2D = 0, 1, 2, 3
 RNE, SR = 0, 1
 UE5M3, UE4M3 = 0, 1
 
@@ -173,10 +173,10 @@ def quantize(x: torch.Tensor, axis: int = AXIS_ROW, T: torch.Tensor | None = Non
     if T is None:
         T = tensor_scale(amax(x), fmt)
     pr = sr = pc = sc = None
-    if axis in (AXIS_ROW, AXIS_BOTH):
+    if axis in (AXIS_ROW, AXIS_BOTH, AXIS_BOTH_2D):
         pr = torch.empty((R, C // 2), dtype=torch.uint8, device=dev)
         sr = torch.empty((R, C // 16), dtype=torch.uint8, device=dev)
-    if axis in (AXIS_COL, AXIS_BOTH):
+    if axis in (AXIS_COL, AXIS_BOTH, AXIS_BOTH_2D):
         pc = torch.empty((C, R // 2), dtype=torch.uint8, device=dev)
         sc = torch.empty((C, R // 16), dtype=torch.uint8, device=dev)
     st = torch.empty((2 if axis == AXIS_BOTH else 1, 4), dtype=torch.int64, device=dev) if stats else None

@@ -64,7 +64,7 @@ typedef enum {
     FP4Q_ERR_TIMEOUT = 6     /* device status: a bounded pipeline wait gave up */
 } fp4q_status;
 
-typedef enum { FP4Q_AXIS_ROW = 0, FP4Q_AXIS_COL = 1, FP4Q_AXIS_BOTH = 2 } fp4q_axis;
+typedef enum { FP4Q_AXIS_ROW = 0, FP4Q_AXIS_COL = 1, FP4Q_AXIS_BOTH = 2, FP4Q_AXIS_BOTH_2D = 3 } fp4q_axis;
 typedef enum { FP4Q_RNE = 0, FP4Q_SR = 1 } fp4q_rounding;
 typedef enum { FP4Q_SCALE_UE5M3 = 0, FP4Q_SCALE_UE4M3 = 1 } fp4q_scale_fmt;
 
@@ -97,11 +97,20 @@ fp4q_status fp4q_tensor_scale(const float* amax, fp4q_scale_fmt fmt, float headr
  *             the transpose: out_payload_col [cols, rows/2],
  *             out_scales_col [cols, rows/16].
  *  axis BOTH: both outputs from one read of the input.
+ *  axis BOTH_2D: both outputs, one scale per 16 x 16 tile (the
+ *             transposition-invariant block scaling listed among the related
+ *             work of the UE5M3 page): the tile's amax picks its code by the
+ *             block rule, every element is quantised once with it (FP4Q_SR
+ *             with the row-wise stream, axis id 0), and the result is written
+ *             in both layouts -- the column payload is the nibble transpose
+ *             of the row payload; out_scales_row repeats a tile's code on its
+ *             16 rows, out_scales_col on its 16 columns.
  * Unused output pointers may be NULL.  tensor_scale: device float (T).
  * rnd/seed: FP4Q_SR draws its bits as stated above (row-wise uses axis id 0,
  * column-wise 1); seed is ignored for FP4Q_RNE.
  * out_stats (nullable): zeroed, then filled; for BOTH it points to TWO structs
- * (row-wise, column-wise).  out_amax (nullable): zeroed, then set to max |x|
+ * (row-wise, column-wise); for BOTH_2D to one (scale counts per 16 x 16
+ * tile, element counts once per element).  out_amax (nullable): zeroed, then set to max |x|
  * of this input -- the by-product periodic scaling keeps for its next
  * refresh. */
 fp4q_status fp4q_quantize(const void* in_bf16, int64_t rows, int64_t cols, fp4q_axis axis,

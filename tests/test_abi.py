@@ -73,7 +73,9 @@ def test_host_validation_rejects_before_launch(lib):
     assert _q(lib, rows=17) == ERR_SHAPE
     assert _q(lib, cols=8) == ERR_SHAPE
     assert _q(lib, rows=-16) == ERR_SHAPE
-    assert _q(lib, axis=3) == ERR_ARG
+    assert _q(lib, axis=4) == ERR_ARG
+    assert _q(lib, axis=3, pc=0) == ERR_ARG          # 16 x 16 scaling writes both layouts
+    assert _q(lib, axis=3, pr=0) == ERR_ARG
     assert _q(lib, fmt=2) == ERR_ARG
     assert _q(lib, rnd=2) == ERR_ARG
     assert _q(lib, ts=0) == ERR_ARG
