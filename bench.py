@@ -358,7 +358,34 @@ def run_gpu(args, rank, world):
         a1.record()
         torch.cuda.synchronize()
         rates[name] = x.numel() * DUAL_BYTES_PER_ELEM / (a0.elapsed_time(a1) / 10 * 1e-3) / 1e9
-    return dict(ms=ms, ms_serial=ms_serial, t_scale=t_scale, t_q=(t_qx, t_qw, t_qd), t_g=t_g, launches=launches, rates=rates,
+    # ---- fprop with the quantisation of Y for the next layer: separate
+    # (GEMM, then row-wise RNE quantisation of Y) versus fused into the GEMM's
+    # epilogue, with and without writing Y in BF16; 10 launches each
+    def _timed(fn, n=10):
+        fn()
+        b0 = torch.cuda.Event(enable_timing=True)
+        b1 = torch.cuda.Event(enable_timing=True)
+        b0.record()
+        for _ in range(n):
+            fn()
+        b1.record()
+        torch.cuda.synchronize()
+        return b0.elapsed_time(b1) / n
+    T0, T1 = step.T[0:1], step.T[1:2]
+    TY = fp4q.tensor_scale(fp4q.amax(step.Y))
+    pY = torch.empty((M_TOK, FFN // 2), dtype=torch.uint8, device=dev)
+    sY = torch.empty((M_TOK, FFN // 16), dtype=torch.uint8, device=dev)
+    aY = torch.empty(1, dtype=torch.float32, device=dev)
+    g_args = (step.Xr, step.Xrs, T0, step.Wr, step.Wrs, T1, M_TOK, FFN, HID, fp4q.UE5M3)
+    fused = {
+        "gemm_ms": _timed(lambda: fp4q.fp4q_gemm(*g_args, step.Y)),
+        "gemm_then_quantize_ms": _timed(lambda: (fp4q.fp4q_gemm(*g_args, step.Y), fp4q.fp4q_quantize(
+            step.Y, fp4q.AXIS_ROW, fp4q.UE5M3, TY, fp4q.RNE, 0, pY, sY, None, None))),
+        "fused_ms": _timed(lambda: fp4q.fp4q_gemm_quantize(*g_args, TY, step.Y, pY, sY, aY)),
+        "fused_without_bf16_ms": _timed(lambda: fp4q.fp4q_gemm_quantize(*g_args, TY, None, pY, sY, aY)),
+    }
+
+    return dict(ms=ms, ms_serial=ms_serial, fused=fused, t_scale=t_scale, t_q=(t_qx, t_qw, t_qd), t_g=t_g, launches=launches, rates=rates,
                 clocks=clk.summary(), status=status, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
                 elems=(X.numel(), W.numel(), dY.numel()))
 
@@ -491,6 +518,7 @@ def main():
                          "wgrad": r["t_g"][2]},
         "e2e": {"value": world * STEP_FLOPS / (r["e2e_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e_ms"]},
+        "fused_epilogue_fprop": r["fused"],
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
         "device_status": r["status"],

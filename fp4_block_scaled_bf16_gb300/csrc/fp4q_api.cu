@@ -128,18 +128,37 @@ fp4q_status fp4q_dequantize(const uint8_t* payload, const uint8_t* scales, int64
                                            out_is_f32 != 0, static_cast<cudaStream_t>(stream)));
 }
 
-fp4q_status fp4q_gemm(const uint8_t* A, const uint8_t* A_scales, const float* A_tscale, const uint8_t* B,
-                      const uint8_t* B_scales, const float* B_tscale, int64_t M, int64_t N, int64_t K,
-                      fp4q_scale_fmt fmt, void* out, int out_is_f32, void* stream) {
+// Shared by fp4q_gemm and fp4q_gemm_quantize: validation of the operands and
+// the launch arguments; q* are the epilogue-quantisation outputs (or null).
+static fp4q_status gemm_common(const uint8_t* A, const uint8_t* A_scales, const float* A_tscale,
+                               const uint8_t* B, const uint8_t* B_scales, const float* B_tscale,
+                               int64_t M, int64_t N, int64_t K, fp4q_scale_fmt fmt, void* out,
+                               int out_is_f32, const float* c_tscale, uint8_t* qpay, uint8_t* qsc,
+                               float* qamax, void* stream) {
   if (!valid_fmt(fmt)) return FP4Q_ERR_ARG;
   if (M < 0 || N < 0 || K < 0 || K % 64 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
     return FP4Q_ERR_SHAPE;
-  if (M == 0 || N == 0) return FP4Q_OK;
-  if (!out) return FP4Q_ERR_ARG;
-  if (!aligned16(out)) return FP4Q_ERR_ALIGN;
+  if (qpay && N % 32) return FP4Q_ERR_SHAPE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (K == 0)
-    return from_cuda(cudaMemsetAsync(out, 0, (size_t)M * N * (out_is_f32 ? 4 : 2), st));
+  if (qamax && !aligned4(qamax)) return FP4Q_ERR_ALIGN;
+  if (M == 0 || N == 0) {
+    if (qamax) return from_cuda(cudaMemsetAsync(qamax, 0, sizeof(float), st));
+    return FP4Q_OK;
+  }
+  if (!out && !qpay) return FP4Q_ERR_ARG;
+  if (out && !aligned16(out)) return FP4Q_ERR_ALIGN;
+  if (qpay) {
+    if (!qsc || !c_tscale) return FP4Q_ERR_ARG;
+    if (!aligned16(qpay) || !aligned16(qsc) || !aligned4(c_tscale)) return FP4Q_ERR_ALIGN;
+  }
+  if (K == 0) {   // C = 0: zero output, zero payload (+0 nibbles), zero scale codes, amax 0
+    cudaError_t e = cudaSuccess;
+    if (out) e = cudaMemsetAsync(out, 0, (size_t)M * N * (out_is_f32 ? 4 : 2), st);
+    if (e == cudaSuccess && qpay) e = cudaMemsetAsync(qpay, 0, (size_t)M * N / 2, st);
+    if (e == cudaSuccess && qpay) e = cudaMemsetAsync(qsc, 0, (size_t)M * N / 16, st);
+    if (e == cudaSuccess && qamax) e = cudaMemsetAsync(qamax, 0, sizeof(float), st);
+    return from_cuda(e);
+  }
   if (!A || !A_scales || !A_tscale || !B || !B_scales || !B_tscale) return FP4Q_ERR_ARG;
   if (!aligned16(A) || !aligned16(B) || !aligned16(A_scales) || !aligned16(B_scales) ||
       !aligned4(A_tscale) || !aligned4(B_tscale))
@@ -147,6 +166,10 @@ fp4q_status fp4q_gemm(const uint8_t* A, const uint8_t* A_scales, const float* A_
   int* status = status_ptr();
   if (!status) return FP4Q_ERR_CUDA;
   fp4q::GemmArgs a;
+  a.TC = c_tscale;
+  a.qpay = qpay;
+  a.qsc = qsc;
+  a.qamax = qamax;
   a.A = A;
   a.As = A_scales;
   a.B = B;
@@ -171,6 +194,23 @@ fp4q_status fp4q_gemm(const uint8_t* A, const uint8_t* A_scales, const float* A_
   }
   if (const char* e = getenv("FP4Q_TEST_GEMM_SKIP_LOADS")) a.skip_loads = atoi(e) != 0;
   return from_cuda(fp4q::launch_gemm(a, st));
+}
+
+fp4q_status fp4q_gemm(const uint8_t* A, const uint8_t* A_scales, const float* A_tscale, const uint8_t* B,
+                      const uint8_t* B_scales, const float* B_tscale, int64_t M, int64_t N, int64_t K,
+                      fp4q_scale_fmt fmt, void* out, int out_is_f32, void* stream) {
+  return gemm_common(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K, fmt, out, out_is_f32,
+                     nullptr, nullptr, nullptr, nullptr, stream);
+}
+
+fp4q_status fp4q_gemm_quantize(const uint8_t* A, const uint8_t* A_scales, const float* A_tscale,
+                               const uint8_t* B, const uint8_t* B_scales, const float* B_tscale,
+                               int64_t M, int64_t N, int64_t K, fp4q_scale_fmt fmt,
+                               const float* c_tscale, void* out_bf16, uint8_t* out_payload,
+                               uint8_t* out_scales, float* out_amax, void* stream) {
+  if (M > 0 && N > 0 && !out_payload) return FP4Q_ERR_ARG;
+  return gemm_common(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K, fmt, out_bf16, 0,
+                     c_tscale, out_payload, out_scales, out_amax, stream);
 }
 
 fp4q_status fp4q_get_device_status(int* out) {

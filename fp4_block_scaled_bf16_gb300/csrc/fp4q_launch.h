@@ -40,6 +40,10 @@ struct GemmArgs {
   void* out;                        // [M, N] BF16 or binary32
   bool out_f32;
   int* status;
+  // epilogue quantisation of the BF16 result (null qpay: none); out may then be null
+  const float* TC = nullptr;        // device tensor scale of C
+  uint8_t *qpay = nullptr, *qsc = nullptr;   // [M, N/2], [M, N/16], row-wise, RNE
+  float* qamax = nullptr;           // nullable: max |bf16(C)|
   long long wait_cycles;            // budget of every pipeline wait (clock64 cycles)
   bool skip_loads;                  // test hook: the producer issues no loads
 };

@@ -70,8 +70,11 @@ constexpr int NBARS = 2 * S_RAW + 2 * S_BF + 1 + 2 * S_CODE;
 // Without the code ring the kernel leaves its 16 KB to L1, which then holds
 // the scale codes it loads directly.
 __host__ __device__ constexpr int off_bar(bool tma_codes) { return OFF_CODE + (tma_codes ? S_CODE * CODE_STAGE : 0); }
+// after the barriers: TMEM address (8 B), abort flag (8 B), then the scale
+// table of the epilogue quantisation
+constexpr int TAB_BYTES = (int)((sizeof(ScaleTab) + 15) / 16 * 16);
 __host__ __device__ constexpr int smem_bytes(bool tma_codes) {
-  return off_bar(tma_codes) + 8 * NBARS + 16 + 1024;   // barriers, TMEM address, abort flag, 1 KB alignment slack
+  return off_bar(tma_codes) + 8 * NBARS + 16 + TAB_BYTES + 1024;   // + 1 KB alignment slack
 }
 
 
@@ -217,20 +220,28 @@ __device__ __forceinline__ uint2 lds64(uint32_t addr) {
 }
 
 // ---------------------------------------------------------------- kernel
-template <bool F32OUT, bool TMA_CODES>
+// QOUT: the epilogue also quantises the BF16 result row-wise (blocks of 16
+// along N, round to nearest even, tensor scale TC) -- the input format of the
+// next layer -- and records max |bf16(C)|; `out` may then be null.
+template <bool F32OUT, bool TMA_CODES, bool QOUT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                 const __grid_constant__ CUtensorMap mapAs, const __grid_constant__ CUtensorMap mapBs,
                 const __grid_constant__ CUtensorMap mapC, int tma_store,
                 const uint8_t* __restrict__ As, const uint8_t* __restrict__ Bs,
                 const float* __restrict__ TA, const float* __restrict__ TB, int M, int N, int K,
-                int fmt, void* __restrict__ out, int* status, long long budget, int skip_loads) {
+                int fmt, void* __restrict__ out, int* status, long long budget, int skip_loads,
+                const float* __restrict__ TC, uint8_t* __restrict__ qpay, uint8_t* __restrict__ qsc,
+                float* qamax, const __grid_constant__ CUtensorMap mapQP,
+                const __grid_constant__ CUtensorMap mapQS, int qstaged) {
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
   constexpr int OFF_BAR = off_bar(TMA_CODES);
   constexpr int OFF_TMEM = OFF_BAR + 8 * NBARS;
   constexpr int OFF_ABORT = OFF_TMEM + 8;
+  constexpr int OFF_TAB = OFF_ABORT + 8;
+  ScaleTab* tab = reinterpret_cast<ScaleTab*>(smem + OFF_TAB);
   const uint32_t bar_raw_full = sb + OFF_BAR;
   const uint32_t bar_raw_empty = bar_raw_full + 8 * S_RAW;
   const uint32_t bar_bf_full = bar_raw_empty + 8 * S_RAW;
@@ -244,6 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
   const int nk = K / BK;
 
+  if (QOUT) build_scale_tab(tab, __ldg(TC), fmt);   // block-wide, before the roles split
   if (threadIdx.x == 0) {
     for (int i = 0; i < S_RAW; ++i) {
       mbar_init(bar_raw_full + 8 * i, 1);
@@ -404,6 +416,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // swizzled) and leaves by TMA stores, whole lines, while the next CTA
     // starts; otherwise every thread stores its 32 values directly.
     const bool staged = !F32OUT && tma_store;
+    // quantised result staged in the idle raw ring (payload box 256 x 128 B,
+    // 128-byte swizzled; codes box 256 x 16 B) and stored by TMA
+    const bool qst = QOUT && qstaged;
     const bool drained = mbar_wait(bar_acc, 0, abort_flag, budget);
     if (drained) {
       tc_fence_after();
@@ -413,13 +428,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int rt = UM * acc + 32 * q + lane;            // row within the tile
       const int row = m0 + rt;
       const bool vec = F32OUT ? (N % 4 == 0) : (N % 8 == 0);
+      uint32_t qmax = 0;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         const int ct = 128 * half + 32 * c;                // column within the tile
         const int col0 = n0 + ct;
         uint32_t r[32];
         tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(BN * acc + ct), r);
-        if (!staged && (row >= M || col0 >= N)) continue;
+        const bool live = row < M && col0 < N;
+        if (!staged && !live) continue;
         float v[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(__uint_as_float(r[j]), alpha);
@@ -445,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 4; ++i)
               sts128(rowb + ((uint32_t)((ch0 + i) ^ (rt & 7)) << 4),
                      make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]));
-          } else {
+          } else if (out != nullptr) {
             uint16_t* o = static_cast<uint16_t*>(out) + (int64_t)row * N + col0;
             if (vec && col0 + 32 <= N) {
 #pragma unroll
@@ -456,18 +473,55 @@ __global__ void __launch_bounds__(kThreads, 1)
                 o[j] = (uint16_t)((j & 1) ? (h[j >> 1] >> 16) : (h[j >> 1] & 0xFFFFu));
             }
           }
+          if (QOUT && live) {
+            // two blocks of 16 along N (N % 32 == 0: a chunk is wholly inside)
+            uint32_t pw[4], codes = 0, cl = 0, fl = 0;
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+              const uint32_t a = max(absmax16(h + 8 * b), absmax16(h + 8 * b + 4));
+              qmax = max(qmax, a);
+              const BlockScale bs = block_scale<false>(a, *tab);
+              pw[2 * b] = quantize8<false, false>(h + 8 * b, bs.r, nullptr, &cl, &fl);
+              pw[2 * b + 1] = quantize8<false, false>(h + 8 * b + 4, bs.r, nullptr, &cl, &fl);
+              codes |= bs.code << (8 * b);
+            }
+            if (qst) {
+              sts128(sb + OFF_RAW + (uint32_t)rt * 128 + ((uint32_t)((ct >> 5) ^ (rt & 7)) << 4),
+                     make_uint4(pw[0], pw[1], pw[2], pw[3]));
+              asm volatile("st.shared.u16 [%0], %1;" ::"r"(sb + OFF_RAW + BM * 128 + (uint32_t)rt * 16 + (ct >> 4)),
+                           "h"((unsigned short)codes) : "memory");
+            } else {
+              *reinterpret_cast<uint4*>(qpay + (int64_t)row * (N / 2) + col0 / 2) =
+                  make_uint4(pw[0], pw[1], pw[2], pw[3]);
+              *reinterpret_cast<uint16_t*>(qsc + (int64_t)row * (N / 16) + col0 / 16) = (uint16_t)codes;
+            }
+          }
+        }
+      }
+      if (QOUT) {
+        // max |bf16(C)| (a 16-bit pattern; inf/NaN compare above every finite)
+        qmax = __reduce_max_sync(0xFFFFFFFFu, qmax);
+        if (lane == 0) {
+          if (qmax >= 0x7F80u) atomicOr(status, kStatusNonFinite);
+          if (qamax && qmax) atomicMax(reinterpret_cast<unsigned int*>(qamax), qmax << 16);
         }
       }
     } else {
       fail(abort_flag, status);
     }
-    if (staged) {
+    if (staged || qst) {
       // every expansion warp passes here exactly once, drained or not
       fence_proxy_async();
       asm volatile("bar.sync 1, %0;" ::"n"(kDeqThreads) : "memory");
       if (threadIdx.x == 0 && drained && !*abort_flag) {
+        if (staged) {
 #pragma unroll
-        for (int j = 0; j < BN / 64; ++j) tma_store_2d(&mapC, sb + OFF_BF + j * (BM * 128), n0 + 64 * j, m0);
+          for (int j = 0; j < BN / 64; ++j) tma_store_2d(&mapC, sb + OFF_BF + j * (BM * 128), n0 + 64 * j, m0);
+        }
+        if (qst) {
+          tma_store_2d(&mapQP, sb + OFF_RAW, n0 / 2, m0);
+          tma_store_2d(&mapQS, sb + OFF_RAW + BM * 128, n0 / 16, m0);
+        }
         tma_store_commit_and_wait_read();
       }
     }
@@ -541,19 +595,47 @@ static bool make_out_map(CUtensorMap* map, void* base, int64_t M, int64_t N) {
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool F32OUT, bool TMA_CODES>
+// 2-D uint8 tensor maps over the row-wise quantised result: payload [M, N/2]
+// with box (128 B, 256 rows) and 128-byte swizzle; codes [M, N/16] with box
+// (16 B, 256 rows).  Need row strides that are multiples of 16 bytes.
+static bool make_qout_maps(CUtensorMap* mp, CUtensorMap* ms, uint8_t* pay, uint8_t* sc, int64_t M, int64_t N) {
+  auto fn = get_encode_fn();
+  if (!fn || N % 256 != 0) return false;
+  const cuuint32_t estr[2] = {1, 1};
+  const cuuint64_t pd[2] = {(cuuint64_t)(N / 2), (cuuint64_t)M};
+  const cuuint64_t ps[1] = {(cuuint64_t)(N / 2)};
+  const cuuint32_t pb[2] = {128u, (cuuint32_t)gemm::BM};
+  const cuuint64_t sd[2] = {(cuuint64_t)(N / 16), (cuuint64_t)M};
+  const cuuint64_t ss[1] = {(cuuint64_t)(N / 16)};
+  const cuuint32_t sbx[2] = {16u, (cuuint32_t)gemm::BM};
+  return fn(mp, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, pay, pd, ps, pb, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS &&
+         fn(ms, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, sc, sd, ss, sbx, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool F32OUT, bool TMA_CODES, bool QOUT = false>
 static cudaError_t launch_gemm_t(const GemmArgs& a, const CUtensorMap& mapA, const CUtensorMap& mapB,
                                  const CUtensorMap& mapAs, const CUtensorMap& mapBs,
                                  const CUtensorMap& mapC, bool tma_store, cudaStream_t st) {
+  CUtensorMap mapQP, mapQS;
+  const bool qstaged = QOUT && make_qout_maps(&mapQP, &mapQS, a.qpay, a.qsc, a.M, a.N);
+  if (!qstaged) {
+    memset(&mapQP, 0, sizeof(mapQP));
+    memset(&mapQS, 0, sizeof(mapQS));
+  }
   constexpr int smem = gemm::smem_bytes(TMA_CODES);
-  cudaError_t e = cudaFuncSetAttribute(gemm::gemm_kernel<F32OUT, TMA_CODES>,
+  cudaError_t e = cudaFuncSetAttribute(gemm::gemm_kernel<F32OUT, TMA_CODES, QOUT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)((a.N + gemm::BN - 1) / gemm::BN), (unsigned)((a.M + gemm::BM - 1) / gemm::BM));
-  gemm::gemm_kernel<F32OUT, TMA_CODES><<<grid, gemm::kThreads, smem, st>>>(
+  gemm::gemm_kernel<F32OUT, TMA_CODES, QOUT><<<grid, gemm::kThreads, smem, st>>>(
       mapA, mapB, mapAs, mapBs, mapC, tma_store ? 1 : 0, a.As, a.Bs, a.TA, a.TB, (int)a.M, (int)a.N,
       (int)a.K, a.fmt, a.out,
-      a.status, a.wait_cycles, a.skip_loads ? 1 : 0);
+      a.status, a.wait_cycles, a.skip_loads ? 1 : 0, a.TC, a.qpay, a.qsc, a.qamax, mapQP, mapQS,
+      qstaged ? 1 : 0);
   return cudaGetLastError();
 }
 
@@ -569,8 +651,16 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
     memset(&mapBs, 0, sizeof(mapBs));
   }
   CUtensorMap mapC;
-  const bool tma_store = !a.out_f32 && make_out_map(&mapC, a.out, a.M, a.N);
+  const bool tma_store = !a.out_f32 && a.out != nullptr && make_out_map(&mapC, a.out, a.M, a.N);
   if (!tma_store) memset(&mapC, 0, sizeof(mapC));
+  if (a.qpay) {   // epilogue quantisation (BF16 result)
+    if (a.qamax) {
+      cudaError_t e = cudaMemsetAsync(a.qamax, 0, sizeof(float), st);
+      if (e != cudaSuccess) return e;
+    }
+    return tma_codes ? launch_gemm_t<false, true, true>(a, mapA, mapB, mapAs, mapBs, mapC, tma_store, st)
+                     : launch_gemm_t<false, false, true>(a, mapA, mapB, mapAs, mapBs, mapC, tma_store, st);
+  }
   if (a.out_f32)
     return tma_codes ? launch_gemm_t<true, true>(a, mapA, mapB, mapAs, mapBs, mapC, false, st)
                      : launch_gemm_t<true, false>(a, mapA, mapB, mapAs, mapBs, mapC, false, st);

@@ -26,7 +26,7 @@ UE5M3, UE4M3 = 0, 1
 
 # every symbol include/fp4q.h declares
 EXPORTS = ("fp4q_amax", "fp4q_tensor_scale", "fp4q_quantize", "fp4q_dequantize", "fp4q_gemm",
-           "fp4q_get_device_status", "fp4q_status_string")
+           "fp4q_gemm_quantize", "fp4q_get_device_status", "fp4q_status_string")
 
 
 class Fp4qError(RuntimeError):
@@ -48,6 +48,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fp4q_quantize.argtypes = [P, i64, i64, i32, i32, P, i32, u64, P, P, P, P, P, P, P]
     lib.fp4q_dequantize.argtypes = [P, P, i64, i64, i32, P, P, i32, P]
     lib.fp4q_gemm.argtypes = [P, P, P, P, P, P, i64, i64, i64, i32, P, i32, P]
+    lib.fp4q_gemm_quantize.argtypes = [P, P, P, P, P, P, i64, i64, i64, i32, P, P, P, P, P, P]
     lib.fp4q_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_int)]
     lib.fp4q_status_string.argtypes = [i32]
     lib.fp4q_status_string.restype = ctypes.c_char_p
@@ -133,6 +134,20 @@ def fp4q_gemm(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K, fmt, out) -
         M, N, K, fmt, _ptr(out), int(f32), _stream()))
 
 
+def fp4q_gemm_quantize(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K, fmt, c_tscale,
+                       out_bf16, out_payload, out_scales, out_amax=None) -> None:
+    for n, t in (("A", A), ("A_scales", A_scales), ("B", B), ("B_scales", B_scales),
+                 ("out_payload", out_payload), ("out_scales", out_scales)):
+        _dev(t, n, torch.uint8)
+    _dev(out_bf16, "out_bf16", torch.bfloat16)
+    _dev(c_tscale, "c_tscale", torch.float32)
+    _dev(out_amax, "out_amax", torch.float32)
+    _check("fp4q_gemm_quantize", _lib.fp4q_gemm_quantize(
+        _ptr(A), _ptr(A_scales), _ptr(A_tscale), _ptr(B), _ptr(B_scales), _ptr(B_tscale),
+        M, N, K, fmt, _ptr(c_tscale), _ptr(out_bf16), _ptr(out_payload), _ptr(out_scales),
+        _ptr(out_amax), _stream()))
+
+
 def fp4q_get_device_status() -> int:
     v = ctypes.c_int(0)
     _check("fp4q_get_device_status", _lib.fp4q_get_device_status(ctypes.byref(v)))
@@ -184,6 +199,21 @@ def quantize(x: torch.Tensor, axis: int = AXIS_ROW, T: torch.Tensor | None = Non
     fp4q_quantize(x, axis, fmt, T, rnd, seed, pr, sr, pc, sc, st, am)
     return Quantized(payload_row=pr, scales_row=sr, payload_col=pc, scales_col=sc, stats=st,
                      amax=am, T=T, fmt=fmt)
+
+
+def gemm_quantize(A, A_scales, A_tscale, B, B_scales, B_tscale, c_tscale, fmt: int = UE5M3,
+                  want_bf16: bool = True, want_amax: bool = True) -> Quantized:
+    """fp4q_gemm_quantize with allocated outputs: the row-wise quantised C
+    (payload_row, scales_row), optionally bf16(C) (`C`) and max |bf16(C)|."""
+    M, K = A.shape[0], A.shape[1] * 2
+    N = B.shape[0]
+    dev = A.device
+    pr = torch.empty((M, N // 2), dtype=torch.uint8, device=dev)
+    sr = torch.empty((M, N // 16), dtype=torch.uint8, device=dev)
+    C = torch.empty((M, N), dtype=torch.bfloat16, device=dev) if want_bf16 else None
+    am = torch.empty(1, dtype=torch.float32, device=dev) if want_amax else None
+    fp4q_gemm_quantize(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K, fmt, c_tscale, C, pr, sr, am)
+    return Quantized(payload_row=pr, scales_row=sr, C=C, amax=am, T=c_tscale, fmt=fmt)
 
 
 def dequantize(payload, scales, T, fmt: int = UE5M3, dtype=torch.bfloat16) -> torch.Tensor:

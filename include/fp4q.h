@@ -134,8 +134,9 @@ fp4q_status fp4q_dequantize(const uint8_t* payload, const uint8_t* scales, int64
  * A: payload [M, K/2] + scales [M, K/16], B: payload [N, K/2] + scales
  * [N, K/16], both quantised along K; A_tscale, B_tscale device floats.
  * The UE5M3 scales are applied in software: each tile is expanded in shared
- * memory to BF16 (exact: e*s has at most 6 significant bits) and multiplied
- * on the tcgen05 tensor cores with binary32 accumulation.  out: [M, N] BF16
+ * memory to FP16 as e*s*2^-4 (exact: at most 6 significant bits, within the
+ * FP16 range and on its subnormal grid) and multiplied on the tcgen05 tensor
+ * cores with binary32 accumulation; the 2^-8 returns in the epilogue.  out: [M, N] BF16
  * (out_is_f32 == 0) or binary32.  M, N >= 0 (any), K a multiple of 64
  * (K = 0 writes zeros).  Every internal pipeline wait is bounded (about 2 s);
  * one that runs out latches FP4Q_ERR_TIMEOUT and the kernel exits, leaving
@@ -146,6 +147,24 @@ fp4q_status fp4q_gemm(const uint8_t* A, const uint8_t* A_scales, const float* A_
                       const uint8_t* B, const uint8_t* B_scales, const float* B_tscale,
                       int64_t M, int64_t N, int64_t K, fp4q_scale_fmt fmt,
                       void* out, int out_is_f32, void* stream);
+
+/* fp4q_gemm whose epilogue also quantises the BF16 result for the next layer
+ * (quantisation fused into the producing GEMM -- the "format-aware fusion"
+ * direction the UE5M3 page lists among related work): C is rounded to BF16
+ * as fp4q_gemm writes it and quantised row-wise, blocks of 16 along N, round
+ * to nearest even, with the device tensor scale c_tscale (e.g. refreshed
+ * periodically from an earlier out_amax):
+ *   out_payload [M, N/2], out_scales [M, N/16] = fp4q_quantize(bf16(C), ROW,
+ *   fmt, c_tscale, RNE) byte for byte;
+ *   out_bf16 (nullable) = bf16(C) [M, N]; out_amax (nullable) = max |bf16(C)|
+ *   (zeroed, then set; a non-finite element latches FP4Q_ERR_NONFINITE).
+ * Operands, fmt (also the format of the output scales) and K as fp4q_gemm;
+ * N must be a multiple of 32. */
+fp4q_status fp4q_gemm_quantize(const uint8_t* A, const uint8_t* A_scales, const float* A_tscale,
+                               const uint8_t* B, const uint8_t* B_scales, const float* B_tscale,
+                               int64_t M, int64_t N, int64_t K, fp4q_scale_fmt fmt,
+                               const float* c_tscale, void* out_bf16, uint8_t* out_payload,
+                               uint8_t* out_scales, float* out_amax, void* stream);
 
 /* Synchronises the current device, returns the latched device status word
  * in *out (an fp4q_status value, FP4Q_OK if none) and clears it.
