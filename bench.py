@@ -146,6 +146,9 @@ class Step:
     def __init__(self, torch, fp4q, X, W, dY):
         self.t, self.q = torch, fp4q
         dev = X.device
+        M_TOK, HID = X.shape          # tokens, in
+        FFN = W.shape[0]              # out
+        self.dims = (M_TOK, HID, FFN)
         u8 = dict(dtype=torch.uint8, device=dev)
         f32 = dict(dtype=torch.float32, device=dev)
         self.X, self.W, self.dY = X, W, dY
@@ -167,6 +170,7 @@ class Step:
 
     def run(self, ev=None):
         q = self.q
+        M_TOK, HID, FFN = self.dims
         T = [self.T[i:i + 1] for i in range(3)]
         A = [self.amax[i:i + 1] for i in range(3)]
         rec = (lambda k: ev[k].record()) if ev else (lambda k: None)
@@ -198,6 +202,7 @@ class Step:
         caller's stream waits for the side stream at the end, so a step ends
         when both are done and the next one starts from a clean slate."""
         q, torch = self.q, self.t
+        M_TOK, HID, FFN = self.dims
         main = torch.cuda.current_stream()
         T = [self.T[i:i + 1] for i in range(3)]
         A = [self.amax[i:i + 1] for i in range(3)]
@@ -385,7 +390,36 @@ def run_gpu(args, rank, world):
         "fused_without_bf16_ms": _timed(lambda: fp4q.fp4q_gemm_quantize(*g_args, TY, None, pY, sY, aY)),
     }
 
-    return dict(ms=ms, ms_serial=ms_serial, fused=fused, t_scale=t_scale, t_q=(t_qx, t_qw, t_qd), t_g=t_g, launches=launches, rates=rates,
+    # ---- the full 8B-class linear block: the four internal linears (QKV,
+    # out, up, down) each through the same fwd+bwd step, one after another
+    block = None
+    if M_TOK == workloads.TOKENS and not args.no_block:
+        lin = []
+        for name in workloads.LINEARS:
+            xb, wb, db = workloads.linear_block(name)
+            lin.append(Step(torch, fp4q, workloads.to_torch_bf16(xb).to(dev),
+                            workloads.to_torch_bf16(wb).to(dev), workloads.to_torch_bf16(db).to(dev)))
+        for _ in range(2):
+            for st_l in lin:
+                st_l.run_overlapped()
+        torch.cuda.synchronize()
+        nb = max(2, args.steps // 4)
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        c0.record()
+        for _ in range(nb):
+            for st_l in lin:
+                st_l.run_overlapped()
+        c1.record()
+        torch.cuda.synchronize()
+        bms = c0.elapsed_time(c1) / nb
+        bflops = sum(3 * 2.0 * workloads.TOKENS * fi * fo for fi, fo in workloads.LINEARS.values())
+        block = {"ms_per_block_step": bms, "TFLOP/s": bflops / (bms * 1e-3) / 1e12, "steps": nb,
+                 "linears": ", ".join(f"{k} {fi}->{fo}" for k, (fi, fo) in workloads.LINEARS.items()),
+                 "tokens": workloads.TOKENS}
+        del lin
+
+    return dict(ms=ms, ms_serial=ms_serial, fused=fused, block=block, t_scale=t_scale, t_q=(t_qx, t_qw, t_qd), t_g=t_g, launches=launches, rates=rates,
                 clocks=clk.summary(), status=status, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
                 elems=(X.numel(), W.numel(), dY.numel()))
 
@@ -435,6 +469,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="fp4q", choices=["fp4q", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-block", action="store_true",
+                    help="skip the four-linear block measurement (profiling captures)")
     ap.add_argument("--tokens", type=int, default=8192,
                     help="rows of X and dY; smaller values only for profiling captures")
     args = ap.parse_args()
@@ -519,6 +555,7 @@ def main():
         "e2e": {"value": world * STEP_FLOPS / (r["e2e_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e_ms"]},
         "fused_epilogue_fprop": r["fused"],
+        "linear_block_fwd_bwd": r["block"],
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
         "device_status": r["status"],
