@@ -166,7 +166,8 @@ class Step:
         self.dW = torch.empty((FFN, HID), **bf)
         self.launches = 0
         self.side = torch.cuda.Stream(device=X.device)
-        self.ev_start, self.ev_xw, self.ev_side = (torch.cuda.Event() for _ in range(3))
+        self.side2 = torch.cuda.Stream(device=X.device)
+        self.ev_start, self.ev_xw, self.ev_side, self.ev_dq, self.ev_side2 = (torch.cuda.Event() for _ in range(5))
 
     def run(self, ev=None):
         q = self.q
@@ -195,12 +196,14 @@ class Step:
         return self
 
     def run_overlapped(self):
-        """The same twelve launches on two streams.  The caller's stream takes
-        X and W (amax, tensor scale, dual-axis RNE quantisation) and fprop; a
-        side stream takes dY's amax, tensor scale and dual-axis SR quantisation
-        at the same time, then dgrad and wgrad once X and W are quantised.  The
-        caller's stream waits for the side stream at the end, so a step ends
-        when both are done and the next one starts from a clean slate."""
+        """The same twelve launches on three streams.  The caller's stream
+        takes X and W (amax, tensor scale, dual-axis RNE quantisation) and
+        fprop; a side stream takes dY's amax, tensor scale and dual-axis SR
+        quantisation at the same time, then dgrad once W is quantised; a second
+        side stream runs wgrad once dY and X are quantised, so that the three
+        GEMMs' CTAs fill one another's last waves.  The caller's stream waits
+        for both side streams at the end, so a step ends when all are done and
+        the next one starts from a clean slate."""
         q, torch = self.q, self.t
         M_TOK, HID, FFN = self.dims
         main = torch.cuda.current_stream()
@@ -218,12 +221,18 @@ class Step:
             q.fp4q_amax(self.dY, A[2])
             q.fp4q_tensor_scale(A[2], q.UE5M3, 1.0, T[2])
             q.fp4q_quantize(self.dY, q.AXIS_BOTH, q.UE5M3, T[2], q.SR, 7, self.Dr, self.Drs, self.Dc, self.Dcs)
+            self.ev_dq.record(self.side)
             self.side.wait_event(self.ev_xw)
             q.fp4q_gemm(self.Dr, self.Drs, T[2], self.Wc, self.Wcs, T[1], M_TOK, HID, FFN, q.UE5M3, self.dX)
-            q.fp4q_gemm(self.Dc, self.Dcs, T[2], self.Xc, self.Xcs, T[0], FFN, HID, M_TOK, q.UE5M3, self.dW)
             self.ev_side.record(self.side)
+        with torch.cuda.stream(self.side2):
+            self.side2.wait_event(self.ev_dq)
+            self.side2.wait_event(self.ev_xw)
+            q.fp4q_gemm(self.Dc, self.Dcs, T[2], self.Xc, self.Xcs, T[0], FFN, HID, M_TOK, q.UE5M3, self.dW)
+            self.ev_side2.record(self.side2)
         q.fp4q_gemm(self.Xr, self.Xrs, T[0], self.Wr, self.Wrs, T[1], M_TOK, FFN, HID, q.UE5M3, self.Y)
         main.wait_event(self.ev_side)
+        main.wait_event(self.ev_side2)
         self.launches += 12
         return self
 
@@ -535,8 +544,8 @@ def main():
         "vs_baseline": None, "dtype": "f16xf16->f32 (E2M1/UE5M3 operands, exact FP16 expansion)", "data": "synthetic",
         "config": {"workload": WORKLOAD, "M": M_TOK, "hidden": HID, "ffn": FFN,
                    "l2": "inputs larger than L2 (dY 256 MiB, step working set ~1 GiB)",
-                   "schedule": "dY branch (amax, scale, SR quantise, then dgrad and wgrad) on a second "
-                               "stream, concurrent with X/W quantisation and fprop",
+                   "schedule": "three streams: X/W amax, scale, quantise and fprop; dY amax, scale, SR "
+                               "quantise and dgrad; wgrad once dY and X are quantised",
                    "ms_per_step_one_stream": r["ms_serial"] / args.steps,
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": bf16,
