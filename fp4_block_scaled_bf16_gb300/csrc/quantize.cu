@@ -62,19 +62,19 @@ __device__ __forceinline__ void flush_amax(float* amax_out, int* status, uint32_
 }
 
 // ---------------------------------------------------------------- amax
-// Streams the tensor with 128-bit loads, four in flight per thread.
+// Streams the tensor with 128-bit loads, eight in flight per thread.
 __global__ void __launch_bounds__(256) amax_kernel(const uint4* __restrict__ in, int64_t nchunks,
                                                    const uint16_t* __restrict__ tail, int ntail,
                                                    float* amax_out, int* status) {
   uint32_t m = 0;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  for (; g + 3 * stride < nchunks; g += 4 * stride) {
-    uint4 v[4];
+  for (; g + 7 * stride < nchunks; g += 8 * stride) {
+    uint4 v[8];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) v[u] = ld_stream_v4(in + g + u * stride);
+    for (int u = 0; u < 8; ++u) v[u] = ld_stream_v4(in + g + u * stride);
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < 8; ++u) {
       const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
       m = max(m, absmax16(w));
     }
