@@ -67,6 +67,23 @@ def committed_traffic(name, sources):
     return d.get("dram_bytes_per_launch")
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest x over the ranks of the initialised process group (the
+    job time of N replicas is the slowest rank's); x itself with one rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world: int, flops_per_step: float, ms_per_step: float) -> float:
+    """Whole-job throughput: every one of `world` replicas runs the step."""
+    return world * flops_per_step / (ms_per_step * 1e-3) / 1e12
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -287,9 +304,7 @@ def run_gpu(args, rank, world):
     ms = t0.elapsed_time(t1)
     ms_serial = u0.elapsed_time(u1)
     if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+        ms = max_over_ranks(ms, dev)
     seg = lambda a, b: sum(e[a].elapsed_time(e[b]) for e in evs) / args.steps
     t_scale, t_qx, t_qw, t_qd = seg(0, 1), seg(1, 2), seg(2, 3), seg(3, 4)
     t_g = [seg(4, 5), seg(5, 6), seg(6, 7)]
@@ -527,7 +542,7 @@ def main():
     hbm = _peak(pk, "hbm_gbs", "hbm_GBps", "hbm")
     bf16 = _peak(pk, "bf16_tflops_sustained", "bf16_tflops")
     ms = r["ms"] / args.steps
-    value = world * STEP_FLOPS / (ms * 1e-3) / 1e12
+    value = job_tflops(world, STEP_FLOPS, ms)
     t_gemm = sum(r["t_g"]) / 3
     gemm_tflops = GEMM_FLOPS / (t_gemm * 1e-3) / 1e12
     nX, nW, nD = r["elems"]
@@ -561,7 +576,7 @@ def main():
         "breakdown_ms": {"amax_scale": r["t_scale"], "quantize_X": r["t_q"][0], "quantize_W": r["t_q"][1],
                          "quantize_dY": r["t_q"][2], "fprop": r["t_g"][0], "dgrad": r["t_g"][1],
                          "wgrad": r["t_g"][2]},
-        "e2e": {"value": world * STEP_FLOPS / (r["e2e_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": job_tflops(world, STEP_FLOPS, r["e2e_ms"]), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e_ms"]},
         "fused_epilogue_fprop": r["fused"],
         "linear_block_fwd_bwd": r["block"],
