@@ -267,29 +267,6 @@ __device__ __forceinline__ uint32_t quantize8(const uint32_t w[4], float r, cons
   return nib;
 }
 
-// Two elements (one BF16 word: lo = element 0, hi = element 1), each with its
-// own multiplier and random word -> one byte of two nibbles (element 0 low).
-template <bool SR, bool STATS>
-__device__ __forceinline__ uint32_t quantize_pair(uint32_t pair, float r0, float r1, uint32_t w0,
-                                                  uint32_t w1, uint32_t* clamped, uint32_t* flushed) {
-  float q0 = __fmul_rn(bf16_lo(pair), r0), q1 = __fmul_rn(bf16_hi(pair), r1);
-  if (STATS) *clamped += (fabsf(q0) > 6.0f ? 1u : 0u) + (fabsf(q1) > 6.0f ? 1u : 0u);
-  if (SR) {
-    q0 = __uint_as_float(__float_as_uint(sr_round_mag(fabsf(q0), w0)) | (__float_as_uint(q0) & 0x80000000u));
-    q1 = __uint_as_float(__float_as_uint(sr_round_mag(fabsf(q1), w1)) | (__float_as_uint(q1) & 0x80000000u));
-  }
-  uint32_t out;
-  asm("{\n\t.reg .b8 b;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b, %2, %1;\n\t"
-      "cvt.u32.u8 %0, b;\n\t}"
-      : "=r"(out) : "f"(q0), "f"(q1));
-  if (STATS) {
-    *flushed += (((pair & 0x7FFFu) != 0u) && ((out & 7u) == 0u)) ? 1u : 0u;
-    *flushed += (((pair & 0x7FFF0000u) != 0u) && ((out & 0x70u) == 0u)) ? 1u : 0u;
-  }
-  return out;
-}
-
 // max of |bf16| over four words, as a 16-bit pattern (finite values order
 // like their patterns; inf/NaN patterns compare above every finite one).
 __device__ __forceinline__ uint32_t absmax16(const uint32_t w[4]) {
