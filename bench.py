@@ -373,6 +373,18 @@ def run_gpu(args, rank, world):
         a1.record()
         torch.cuda.synchronize()
         rates[name] = x.numel() * ROW_BYTES_PER_ELEM / (a0.elapsed_time(a1) / 10 * 1e-3) / 1e9
+    # dequantisation (support op): W's row-wise payload and scales -> BF16
+    Wd = torch.empty_like(step.W)
+    fp4q.fp4q_dequantize(step.Wr, step.Wrs, FFN, HID, fp4q.UE5M3, step.T[1:2], Wd)
+    a0 = torch.cuda.Event(enable_timing=True)
+    a1 = torch.cuda.Event(enable_timing=True)
+    a0.record()
+    for _ in range(10):
+        fp4q.fp4q_dequantize(step.Wr, step.Wrs, FFN, HID, fp4q.UE5M3, step.T[1:2], Wd)
+    a1.record()
+    torch.cuda.synchronize()
+    rates["W_dequant_bf16"] = step.W.numel() * ROW_BYTES_PER_ELEM / (a0.elapsed_time(a1) / 10 * 1e-3) / 1e9
+    del Wd
     # 16 x 16 (transposition-invariant) scaling: both layouts from one
     # quantisation, same algorithmic bytes as the dual-axis quantisers
     for name, x, rnd, outs in (("W_2d_rne", step.W, fp4q.RNE, (step.Wr, step.Wrs, step.Wc, step.Wcs)),

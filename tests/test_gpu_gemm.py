@@ -167,9 +167,10 @@ def test_full_dgrad_wgrad(lib):
     assert err <= GEMM_TOL, err
 
 
-@pytest.mark.parametrize("name", ["qkv", "down"])
+@pytest.mark.parametrize("name", ["qkv", "out", "down"])
 def test_linear_block_shapes(lib, name):
-    """8B-class block linears (qkv 4096->6144, down 16384->4096), 8192 tokens:
+    """8B-class block linears (qkv 4096->6144, out 4096->4096, down 16384->4096; up is
+    the full-size case above), 8192 tokens:
     fprop, dgrad and wgrad through quantise + block-scaled GEMM with SR on
     dY, sampled stripes against the oracle."""
     X, W, dY = workloads.linear_block(name)
