@@ -669,7 +669,33 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile4_kernel(
 
 // ---------------------------------------------------------------- dequantise
 // v = (e * s) * T per element, one binary32 rounding each, then BF16 (RNE)
-// or binary32.  One chunk = 8 elements = one payload word.
+// or binary32.  One chunk = 8 elements = one payload word.  E2M1 -> FP16
+// pairs by the hardware conversion (every E2M1 value is an FP16 value, so it
+// is exact), then FP16 -> binary32 (exact); e * s is exact in binary32.
+__device__ __forceinline__ void e2m1x8_to_f32(uint32_t w, float v[8]) {
+  uint32_t h[4];
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3]) : "r"(w));
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "mov.b32 {lo, hi}, %2;\n\t"
+        "cvt.f32.f16 %0, lo;\n\t"
+        "cvt.f32.f16 %1, hi;\n\t}"
+        : "=f"(v[2 * j]), "=f"(v[2 * j + 1]) : "r"(h[j]));
+}
+
+// Each warp walks groups of 32 * kDeqUnroll consecutive chunks (lane l takes
+// chunks l, l + 32, ...): every load and store instruction of a warp covers
+// one contiguous span, and kDeqUnroll payload words and scale bytes are in
+// flight per thread before the first conversion.
+constexpr int kDeqUnroll = 4;
+
 template <bool F32>
 __global__ void __launch_bounds__(256) dequantize_kernel(const uint32_t* __restrict__ payload,
                                                          const uint8_t* __restrict__ scales,
@@ -677,30 +703,38 @@ __global__ void __launch_bounds__(256) dequantize_kernel(const uint32_t* __restr
                                                          const float* __restrict__ tscale,
                                                          void* __restrict__ out) {
   const float T = __ldg(tscale);
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < nchunks; g += stride) {
-    const uint32_t p = __ldg(payload + g);
-    const float s = decode_scale(__ldg(scales + (g >> 1)), fmt);
-    float v[8];
+  const int lane = threadIdx.x & 31;
+  const int64_t span = 32 * kDeqUnroll;
+  const int64_t stride = (((int64_t)gridDim.x * blockDim.x) >> 5) * span;
+  for (int64_t base = (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * span + lane;
+       base < nchunks; base += stride) {
+    uint32_t p[kDeqUnroll], c[kDeqUnroll];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint32_t n = (p >> (4 * j)) & 15u;
-      // E2M1 magnitude: exponent field (n>>1)&3, mantissa n&1
-      const uint32_t e = (n >> 1) & 3u, m = n & 1u;
-      float mag = (e == 0) ? (m ? 0.5f : 0.0f) : __uint_as_float(((e + 126u) << 23) | (m << 22));
-      if (n & 8u) mag = -mag;
-      v[j] = __fmul_rn(__fmul_rn(mag, s), T);
+    for (int u = 0; u < kDeqUnroll; ++u) {
+      const int64_t g = base + 32 * u;
+      p[u] = g < nchunks ? __ldg(payload + g) : 0u;
+      c[u] = g < nchunks ? __ldg(scales + (g >> 1)) : 0u;
     }
-    if (F32) {
-      float4* o = reinterpret_cast<float4*>(out) + 2 * g;
-      o[0] = make_float4(v[0], v[1], v[2], v[3]);
-      o[1] = make_float4(v[4], v[5], v[6], v[7]);
-    } else {
-      uint32_t h[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(h[j]) : "f"(v[2 * j + 1]), "f"(v[2 * j]));
-      reinterpret_cast<uint4*>(out)[g] = make_uint4(h[0], h[1], h[2], h[3]);
+    for (int u = 0; u < kDeqUnroll; ++u) {
+      const int64_t g = base + 32 * u;
+      if (g >= nchunks) continue;
+      const float s = decode_scale(c[u], fmt);
+      float v[8];
+      e2m1x8_to_f32(p[u], v);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(__fmul_rn(v[j], s), T);
+      if (F32) {
+        float4* o = reinterpret_cast<float4*>(out) + 2 * g;
+        o[0] = make_float4(v[0], v[1], v[2], v[3]);
+        o[1] = make_float4(v[4], v[5], v[6], v[7]);
+      } else {
+        uint32_t h[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(h[j]) : "f"(v[2 * j + 1]), "f"(v[2 * j]));
+        reinterpret_cast<uint4*>(out)[g] = make_uint4(h[0], h[1], h[2], h[3]);
+      }
     }
   }
 }
@@ -791,7 +825,7 @@ cudaError_t launch_dequantize(const uint8_t* payload, const uint8_t* scales, int
                               cudaStream_t st) {
   const int64_t nchunks = rows * cols / 8;
   if (nchunks == 0) return cudaSuccess;
-  const int grid = grid_for(nchunks, 256, 8);
+  const int grid = grid_for((nchunks + kDeqUnroll - 1) / kDeqUnroll, 256, 8);
   if (f32)
     dequantize_kernel<true><<<grid, 256, 0, st>>>(reinterpret_cast<const uint32_t*>(payload), scales,
                                                   nchunks, fmt, tscale, out);
