@@ -70,6 +70,7 @@ def _load():
             "orc_amax_bf16": (f32, [P, i64, P]),
             "orc_tensor_scale": (f32, [f32, i32, f32]),
             "orc_quantize": (None, [P, i64, i64, i32, i32, f32, i32, u64, P, P, P]),
+            "orc_quantize_band": (None, [P, i64, i64, i64, i32, i32, f32, i32, u64, P, P, P]),
             "orc_quantize_2d": (None, [P, i64, i64, i32, f32, i32, u64, P, P, P, P, P]),
             "orc_dequantize": (None, [P, P, i64, i64, i32, f32, P, P]),
             "orc_gemm": (None, [P, P, f32, P, P, f32, i64, i64, i64, i32, P, P, i64, P]),
@@ -179,22 +180,29 @@ def tensor_scale(amax_value: float, fmt: int = UE5M3, headroom: float = 1.0) -> 
     return float(np.float32(_load().orc_tensor_scale(float(amax_value), int(fmt), float(headroom))))
 
 
-def quantize(x, axis: int, T: float, fmt: int = UE5M3, rnd: int = RNE, seed: int = 0):
+def quantize(x, axis: int, T: float, fmt: int = UE5M3, rnd: int = RNE, seed: int = 0,
+             row_base: int = 0):
     """Quantise a [rows, cols] BF16 tensor along one axis.
 
     Returns (payload uint8 [o, i/2], scales uint8 [o, i/16], stats uint64[4])
     with (o, i) = (rows, cols) for ROW and (cols, rows) for COL.
+
+    row_base > 0 treats x as rows row_base .. row_base + rows - 1 of a larger
+    tensor with the same columns: the result is that tensor's output for
+    those rows (ROW), or for that span of every column (COL); only the
+    stochastic-rounding counters (logical indices) depend on it.
     """
     x = _as_bf16_bits(x)
     rows, cols = x.shape
-    if rows % 16 or cols % 16:
-        raise ValueError("rows and cols must be multiples of 16")
+    if rows % 16 or cols % 16 or row_base % 16 or row_base < 0:
+        raise ValueError("rows, cols and row_base must be non-negative multiples of 16")
     outer, inner = (rows, cols) if axis == ROW else (cols, rows)
     payload = np.zeros((outer, inner // 2), np.uint8)
     scales = np.zeros((outer, inner // 16), np.uint8)
     stats = np.zeros(4, np.uint64)
-    _load().orc_quantize(_ptr(x), rows, cols, int(axis), int(fmt), float(T), int(rnd),
-                         ctypes.c_uint64(seed), _ptr(payload), _ptr(scales), _ptr(stats))
+    _load().orc_quantize_band(_ptr(x), int(row_base), rows, cols, int(axis), int(fmt), float(T),
+                              int(rnd), ctypes.c_uint64(seed), _ptr(payload), _ptr(scales),
+                              _ptr(stats))
     return payload, scales, stats
 
 

@@ -292,9 +292,25 @@ static uint8_t quantize_block16(const float v[16], float T, int fmt, int rnd,
  *            16b..16b+15 ([cols, rows/16]).
  * stats[4] accumulates {scale saturations, scale underflows, clamped
  * elements, flushed elements}.  rows and cols are multiples of 16. */
+void orc_quantize_band(const uint16_t *x, int64_t row_base, int64_t rows, int64_t cols, int axis,
+                       int fmt, float T, int rnd, uint64_t seed,
+                       uint8_t *payload, uint8_t *scales, uint64_t stats[4]);
+
 void orc_quantize(const uint16_t *x, int64_t rows, int64_t cols, int axis, int fmt,
                   float T, int rnd, uint64_t seed,
                   uint8_t *payload, uint8_t *scales, uint64_t stats[4]) {
+    orc_quantize_band(x, 0, rows, cols, axis, fmt, T, rnd, seed, payload, scales, stats);
+}
+
+/* The same for rows row_base .. row_base + rows - 1 of a larger tensor with
+ * `cols` columns, x pointing at the first of them (row_base a multiple of
+ * 16, so that the band holds whole column blocks).  Only the logical index
+ * of an element, and with it the stochastic-rounding counter, depends on
+ * row_base; the outputs are the band's rows (ROW) or the band's span of each
+ * column (COL). */
+void orc_quantize_band(const uint16_t *x, int64_t row_base, int64_t rows, int64_t cols, int axis,
+                       int fmt, float T, int rnd, uint64_t seed,
+                       uint8_t *payload, uint8_t *scales, uint64_t stats[4]) {
     int64_t outer = (axis == ORC_ROW) ? rows : cols;   /* rows of the output */
     int64_t inner = (axis == ORC_ROW) ? cols : rows;   /* the blocked length */
     for (int64_t o = 0; o < outer; ++o) {
@@ -305,8 +321,8 @@ void orc_quantize(const uint16_t *x, int64_t rows, int64_t cols, int axis, int f
             for (int j = 0; j < 16; ++j) {
                 int64_t r = (axis == ORC_ROW) ? o : 16 * b + j;
                 int64_t c = (axis == ORC_ROW) ? 16 * b + j : o;
-                int64_t i = r * cols + c;                     /* logical index */
-                v[j] = bf16_to_f32(x[i]);
+                int64_t i = (row_base + r) * cols + c;        /* logical index */
+                v[j] = bf16_to_f32(x[r * cols + c]);
                 rb[j] = (rnd == ORC_SR) ? orc_sr_word(seed, (uint64_t)i, (uint32_t)axis) : 0u;
             }
             uint8_t code = quantize_block16(v, T, fmt, rnd, rb, nib, stats);

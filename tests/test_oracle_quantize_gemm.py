@@ -209,6 +209,29 @@ def test_sr_row_and_col_axes_draw_independent_bits():
     assert (pr != pc2).any()
 
 
+def test_row_band_equals_slice_of_full_tensor():
+    """A band of rows quantised with its row offset gives exactly the full
+    tensor's outputs for those rows (ROW) and that span of each column (COL),
+    stochastic-rounding counters included (logical index r * cols + c)."""
+    rng = np.random.default_rng(6)
+    x = bf16_round((rng.standard_normal((96, 48)) * 10 ** rng.uniform(-3, 2, (96, 1))).astype(np.float32))
+    T = oracle.tensor_scale(oracle.amax(x)[0])
+    for rnd in (oracle.RNE, oracle.SR):
+        fr = oracle.quantize(x, oracle.ROW, T, rnd=rnd, seed=11)
+        fc = oracle.quantize(x, oracle.COL, T, rnd=rnd, seed=11)
+        for r0, r1 in ((0, 16), (16, 48), (48, 96)):
+            band = np.ascontiguousarray(x[r0:r1])
+            br = oracle.quantize(band, oracle.ROW, T, rnd=rnd, seed=11, row_base=r0)
+            bc = oracle.quantize(band, oracle.COL, T, rnd=rnd, seed=11, row_base=r0)
+            assert np.array_equal(br[0], fr[0][r0:r1]) and np.array_equal(br[1], fr[1][r0:r1])
+            assert np.array_equal(bc[0], fc[0][:, r0 // 2:r1 // 2])
+            assert np.array_equal(bc[1], fc[1][:, r0 // 16:r1 // 16])
+        if rnd == oracle.SR:
+            # without the offset the band draws other random words
+            b = np.ascontiguousarray(x[48:96])
+            assert not np.array_equal(oracle.quantize(b, oracle.ROW, T, rnd=rnd, seed=11)[0], fr[0][48:96])
+
+
 def test_periodic_scaler_refreshes_every_period():
     rng = np.random.default_rng(6)
     sc = oracle.PeriodicScaler(period=4)
