@@ -80,6 +80,10 @@ fp4q_status fp4q_quantize(const void* in_bf16, int64_t rows, int64_t cols, fp4q_
     return FP4Q_ERR_ARG;
   if (!valid_fmt(fmt) || (rnd != FP4Q_RNE && rnd != FP4Q_SR) || !tensor_scale) return FP4Q_ERR_ARG;
   if (rows < 0 || cols < 0 || rows % 16 || cols % 16) return FP4Q_ERR_SHAPE;
+  if (axis != FP4Q_AXIS_ROW) {   // the tile kernels number 128 x 128 tiles in 32 bits
+    const int64_t tr = (rows + 127) / 128, tc = (cols + 127) / 128;
+    if (tc > 0 && tr > INT32_MAX / tc) return FP4Q_ERR_SHAPE;
+  }
   const bool row = axis != FP4Q_AXIS_COL, col = axis != FP4Q_AXIS_ROW;
   const bool empty = rows == 0 || cols == 0;
   if (!empty) {

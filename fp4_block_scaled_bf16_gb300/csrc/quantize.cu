@@ -488,8 +488,12 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile4_kernel(
   __shared__ ColStage stage;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int own = lane & 3;                                         // rows r with r % 4 == own
-  const int64_t r0 = (int64_t)blockIdx.y * kRcRows + warp * 16;
-  const int64_t c0 = (int64_t)blockIdx.x * kRcCols + lane * 4;
+  // one CTA per tile, tiles numbered row-major (a 1-D grid: no 65535 limit
+  // on the number of tile rows)
+  const int64_t tiles_x = (C + kRcCols - 1) / kRcCols;
+  const int64_t ty = (int64_t)blockIdx.x / tiles_x, tx = (int64_t)blockIdx.x % tiles_x;
+  const int64_t r0 = ty * kRcRows + warp * 16;
+  const int64_t c0 = tx * kRcCols + lane * 4;
   // sizes are multiples of 16, so a 16-column block is either wholly inside
   // or wholly outside, and so is each 16 x 4 piece
   const bool ok = r0 < R && c0 < C;
@@ -659,7 +663,7 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile4_kernel(
   for (int j = 0; j < 4; ++j)
     *reinterpret_cast<uint2*>(&stage.pay[stage_word(4 * lane + j, 2 * warp)]) = pcol[j];
   __syncthreads();
-  write_col_stage(stage, R, C, (int64_t)blockIdx.y * kRcRows, (int64_t)blockIdx.x * kRcCols, pay_col, sc_col);
+  write_col_stage(stage, R, C, ty * kRcRows, tx * kRcCols, pay_col, sc_col);
   if (STATS) {
     if (DO_ROW) flush_stats(stats, r_sat, r_uflow, r_clamp, r_flush);
     if (!TWO_D) flush_stats(stats + (DO_ROW ? 1 : 0), c_sat, c_uflow, c_clamp, c_flush);
@@ -776,12 +780,12 @@ static void row_launch(const QuantArgs& a, cudaStream_t st) {
 
 template <bool SR, bool STATS, bool DO_ROW, bool TWO_D = false>
 static cudaError_t tile_launch(const QuantArgs& a, cudaStream_t st) {
-  dim3 grid((unsigned)((a.cols + kRcCols - 1) / kRcCols), (unsigned)((a.rows + kRcRows - 1) / kRcRows));
-  const int64_t ntiles = (int64_t)grid.x * grid.y;
+  const int64_t ntiles = ((a.cols + kRcCols - 1) / kRcCols) * ((a.rows + kRcRows - 1) / kRcRows);
+  if (ntiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
   const uint16_t* in = static_cast<const uint16_t*>(a.in);
   uint32_t* pr = reinterpret_cast<uint32_t*>(a.pay_row);
   if constexpr (SR)
-    quantize_tile4_kernel<STATS, DO_ROW, TWO_D><<<grid, kRcThreads, 0, st>>>(
+    quantize_tile4_kernel<STATS, DO_ROW, TWO_D><<<(unsigned)ntiles, kRcThreads, 0, st>>>(
         in, a.rows, a.cols, a.fmt, a.tscale, a.seed, a.pay_row, a.sc_row, a.pay_col, a.sc_col, a.stats,
         a.amax_out, a.status);
   else

@@ -57,7 +57,7 @@ extern "C" {
 typedef enum {
     FP4Q_OK = 0,
     FP4Q_ERR_ARG = 1,        /* null pointer or unknown enum value */
-    FP4Q_ERR_SHAPE = 2,      /* a size is not a supported multiple */
+    FP4Q_ERR_SHAPE = 2,      /* a size is not a supported multiple or too large */
     FP4Q_ERR_ALIGN = 3,      /* a pointer is misaligned (see conventions) */
     FP4Q_ERR_CUDA = 4,       /* a CUDA runtime/driver call failed */
     FP4Q_ERR_NONFINITE = 5,  /* device status: an input element was inf/NaN */
@@ -90,7 +90,9 @@ fp4q_status fp4q_tensor_scale(const float* amax, fp4q_scale_fmt fmt, float headr
                               float* out_scale, void* stream);
 
 /* Block-16 quantisation of a rows x cols BF16 tensor (E2M1 + UE5M3 block
- * scales, Abstract).  rows and cols: multiples of 16, >= 0.
+ * scales, Abstract).  rows and cols: multiples of 16, >= 0; for every axis
+ * but ROW, ceil(rows/128) * ceil(cols/128) <= 2^31 - 1 (FP4Q_ERR_SHAPE
+ * otherwise).  Element indices are 64-bit throughout.
  *  axis ROW : blocks along a row.  out_payload_row [rows, cols/2] bytes,
  *             out_scales_row [rows, cols/16] bytes.
  *  axis COL : blocks along a column, written as the row-wise quantisation of

@@ -74,6 +74,8 @@ def test_host_validation_rejects_before_launch(lib):
     assert _q(lib, cols=8) == ERR_SHAPE
     assert _q(lib, rows=-16) == ERR_SHAPE
     assert _q(lib, axis=4) == ERR_ARG
+    assert _q(lib, axis=1, rows=2 ** 32, cols=2 ** 32) == ERR_SHAPE   # > 2^31 - 1 tiles
+    assert _q(lib, axis=2, rows=2 ** 26, cols=2 ** 26) == ERR_SHAPE
     assert _q(lib, axis=3, pc=0) == ERR_ARG          # 16 x 16 scaling writes both layouts
     assert _q(lib, axis=3, pr=0) == ERR_ARG
     assert _q(lib, fmt=2) == ERR_ARG
