@@ -188,8 +188,9 @@ def test_periodic_scaling_sequence(lib):
 
 
 def test_tile_pipeline_is_deterministic(lib):
-    """The TMA-fed tile ring must never hand a consumer a stage that is being
-    refilled: repeated full-size dual-axis quantisations are byte-identical."""
+    """The persistent tile quantiser's double-buffered column stage (and the
+    prefetched next piece) must never be overwritten while still being read:
+    repeated full-size dual-axis quantisations are byte-identical."""
     dY = workloads.backward_gradient()
     x = to_dev(dY)
     T = lib.tensor_scale(lib.amax(x))
