@@ -55,7 +55,14 @@ constexpr int kDeqThreads = 32 * kDeqWarps;
 constexpr int kProducerWarp = kDeqWarps, kMmaWarp = kDeqWarps + 1;
 constexpr int kThreads = kDeqThreads + 64;
 constexpr uint32_t kTmemCols = 512;             // two 128 x 256 FP32 accumulators
-constexpr int kRowsPerThread = (BM + BN) / (kDeqThreads / 4);   // 4
+constexpr int kRowStride = kDeqThreads / 4;                      // rows between a thread's rows
+constexpr int kRowsPerThread = (BM + BN) / kRowStride;
+// epilogue: warps 4j .. 4j + 3 cover the 128 TMEM lanes of one accumulator;
+// the BN columns are split between the kDeqWarps / 8 warps of each lane group
+constexpr int kColParts = kDeqWarps / 8;
+constexpr int kColChunks = BN / kColParts / 32;                  // 32-column TMEM loads per warp
+static_assert(kRowStride % 8 == 0 && (BM + BN) % kRowStride == 0 && BM % kRowStride == 0, "row map");
+static_assert(kDeqWarps % 8 == 0 && BN % (32 * kColParts) == 0, "epilogue map");
 
 // Scale codes (when K is a multiple of 256): TMA boxes of 16 codes per row
 // (four K steps) for the 256 A rows and the 256 B rows, in a 2-slot ring.
@@ -67,6 +74,13 @@ constexpr int OFF_BF = 0;
 constexpr int OFF_RAW = OFF_BF + S_BF * BF_STAGE;
 constexpr int OFF_CODE = OFF_RAW + S_RAW * RAW_STAGE;
 constexpr int NBARS = 2 * S_RAW + 2 * S_BF + 1 + 2 * S_CODE;
+// Epilogue staging: the BF16 result (four 256 x 64 boxes) in the idle BF16
+// ring, the quantised result (payload box 256 x 128 B, codes box 256 x 16 B)
+// in the idle raw ring.
+constexpr int QST_PAY = BM * 128, QST_BYTES = QST_PAY + BM * 16;
+constexpr int OFF_QST = OFF_RAW;
+static_assert(S_BF * BF_STAGE >= (BN / 64) * BM * 128, "BF16 staging fits the BF16 ring");
+static_assert(S_RAW * RAW_STAGE >= QST_BYTES && OFF_QST % 1024 == 0, "quantised staging fits the raw ring");
 // Without the code ring the kernel leaves its 16 KB to L1, which then holds
 // the scale codes it loads directly.
 __host__ __device__ constexpr int off_bar(bool tma_codes) { return OFF_CODE + (tma_codes ? S_CODE * CODE_STAGE : 0); }
@@ -334,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------ expansion warps
     // Thread t expands block (t % 4) of the 64-wide K step for rows
-    // t/4 + 128 i, i = 0..3 (A rows 0..255, then B rows 0..255).
+    // t/4 + kRowStride i, i < kRowsPerThread (A rows 0..255, then B rows 0..255).
     const int tid = threadIdx.x;
     const int blk = tid & 3;
     const int rbase = tid >> 2;
@@ -343,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool rok[kRowsPerThread];
 #pragma unroll
     for (int i = 0; i < kRowsPerThread; ++i) {
-      const int r = rbase + 128 * i;
+      const int r = rbase + kRowStride * i;
       const int gr = (r < BM) ? m0 + r : n0 + (r - BM);
       rok[i] = (r < BM) ? (gr < M) : (gr < N);
       srow[i] = ((r < BM) ? As : Bs) + (int64_t)(rok[i] ? gr : 0) * lds_k + blk;
@@ -359,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       load_codes(0, c0);
       load_codes(1, c1);
     }
-    const uint32_t sw = rbase & 7;               // (rbase + 128 i) & 7
+    const uint32_t sw = rbase & 7;               // (rbase + kRowStride i) & 7
     const uint32_t c_lo = ((2 * blk) ^ sw) << 4, c_hi = ((2 * blk + 1) ^ sw) << 4;
     int s = 0, t = 0;
     uint32_t ph_s = 0, ph_t = 1;
@@ -373,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t code = sb + OFF_CODE + cs * CODE_STAGE + rbase * 16 + (kb % CODE_KB) * 4 + blk;
 #pragma unroll
-        for (int i = 0; i < kRowsPerThread; ++i) c0[i] = lds_u8(code + i * 128 * 16);
+        for (int i = 0; i < kRowsPerThread; ++i) c0[i] = lds_u8(code + i * kRowStride * 16);
       } else {
         load_codes(kb + 2, c2);
       }
@@ -386,11 +400,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t bf = sb + OFF_BF + t * BF_STAGE + rbase * 128;
 #pragma unroll
       for (int i = 0; i < kRowsPerThread; ++i) {
-        const uint2 w = lds64(raw + i * 128 * (BK / 2));
+        const uint2 w = lds64(raw + i * kRowStride * (BK / 2));
         const uint32_t ss = scale_pair(c0[i], fmt);
         const uint4 lo = expand8(w.x, ss);         // K 16*blk + 0..7
         const uint4 hi = expand8(w.y, ss);         // K 16*blk + 8..15
-        const uint32_t row_addr = bf + i * 128 * 128;
+        const uint32_t row_addr = bf + i * kRowStride * 128;
         sts128(row_addr + c_lo, lo);
         sts128(row_addr + c_hi, hi);
       }
@@ -411,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ------------------------------------------------ epilogue
     // warp w drains TMEM lanes 32 (w % 4) .. +31 of accumulator (w / 4) % 2,
-    // columns 128 (w / 8) .. +127.  BF16 output with a tensor map: the tile is
+    // columns 32 kColChunks (w / 8) .. +32 kColChunks - 1.  BF16 output with a tensor map: the tile is
     // staged in the idle expansion ring as four 256 x 64 boxes (128-byte
     // swizzled) and leaves by TMA stores, whole lines, while the next CTA
     // starts; otherwise every thread stores its 32 values directly.
@@ -422,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool drained = mbar_wait(bar_acc, 0, abort_flag, budget);
     if (drained) {
       tc_fence_after();
-      const int q = warp & 3, acc = (warp >> 2) & 1, half = warp >> 3;
+      const int q = warp & 3, acc = (warp >> 2) & 1, part = warp >> 3;
       // T_A T_B, times 2^8 for the 2^-4 on each operand (exact)
       const float alpha = __fmul_rn(__fmul_rn(__ldg(TA), __ldg(TB)), 256.0f);
       const int rt = UM * acc + 32 * q + lane;            // row within the tile
@@ -430,8 +444,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool vec = F32OUT ? (N % 4 == 0) : (N % 8 == 0);
       uint32_t qmax = 0;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        const int ct = 128 * half + 32 * c;                // column within the tile
+      for (int c = 0; c < kColChunks; ++c) {
+        const int ct = 32 * (kColChunks * part + c);       // column within the tile
         const int col0 = n0 + ct;
         uint32_t r[32];
         tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(BN * acc + ct), r);
@@ -486,9 +500,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               codes |= bs.code << (8 * b);
             }
             if (qst) {
-              sts128(sb + OFF_RAW + (uint32_t)rt * 128 + ((uint32_t)((ct >> 5) ^ (rt & 7)) << 4),
+              sts128(sb + OFF_QST + (uint32_t)rt * 128 + ((uint32_t)((ct >> 5) ^ (rt & 7)) << 4),
                      make_uint4(pw[0], pw[1], pw[2], pw[3]));
-              asm volatile("st.shared.u16 [%0], %1;" ::"r"(sb + OFF_RAW + BM * 128 + (uint32_t)rt * 16 + (ct >> 4)),
+              asm volatile("st.shared.u16 [%0], %1;" ::"r"(sb + OFF_QST + QST_PAY + (uint32_t)rt * 16 + (ct >> 4)),
                            "h"((unsigned short)codes) : "memory");
             } else {
               *reinterpret_cast<uint4*>(qpay + (int64_t)row * (N / 2) + col0 / 2) =
@@ -519,8 +533,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < BN / 64; ++j) tma_store_2d(&mapC, sb + OFF_BF + j * (BM * 128), n0 + 64 * j, m0);
         }
         if (qst) {
-          tma_store_2d(&mapQP, sb + OFF_RAW, n0 / 2, m0);
-          tma_store_2d(&mapQS, sb + OFF_RAW + BM * 128, n0 / 16, m0);
+          tma_store_2d(&mapQP, sb + OFF_QST, n0 / 2, m0);
+          tma_store_2d(&mapQS, sb + OFF_QST + QST_PAY, n0 / 16, m0);
         }
         tma_store_commit_and_wait_read();
       }

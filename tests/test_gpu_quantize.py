@@ -145,6 +145,22 @@ def test_dequantize_parity(f32, fmt, lib):
         assert np.array_equal(d.cpu().view(torch.int16).numpy().view(np.uint16), ob)
 
 
+def test_dequantize_empty_and_spans(lib):
+    # empty; and sizes around the kernel's 128-word warp spans (ragged tails)
+    T = torch.ones(1, dtype=torch.float32, device="cuda")
+    for shape in [(0, 16), (16, 0)]:
+        p = torch.empty((shape[0], shape[1] // 2), dtype=torch.uint8, device="cuda")
+        s = torch.empty((shape[0], shape[1] // 16), dtype=torch.uint8, device="cuda")
+        assert lib.dequantize(p, s, T).numel() == 0
+    for shape in [(16, 16), (16, 2048), (16, 2064), (48, 1024 + 16), (1040, 1024)]:
+        bits = rand_bits(shape, shape[1], spread=3.0)
+        out, Tq, q = check_quantize(bits, ROW)
+        d = lib.dequantize(q.payload_row, q.scales_row, q.T)
+        torch.cuda.synchronize()
+        _, ob = oracle.dequantize(out[ROW][0], out[ROW][1], Tq)
+        assert np.array_equal(d.cpu().view(torch.int16).numpy().view(np.uint16), ob), shape
+
+
 # ---------------------------------------------------------------- full sizes
 def test_full_fprop_operands_row_rne():
     X, W = workloads.fprop_operands()
@@ -158,6 +174,24 @@ def test_full_backward_operands():
     check_quantize(dY, BOTH, rnd=1, seed=7)      # SR gradient, both blockings
     check_quantize(W, COL)                      # dgrad B operand
     check_quantize(X, COL)                      # wgrad B operand
+
+
+def test_dequantize_full_size(lib):
+    """W's row payload (16384 x 4096) to BF16 and dY's SR column payload
+    (16384 x 8192) to binary32, bit for bit against the oracle."""
+    X, W = workloads.fprop_operands()
+    for bits, axis, rnd, f32 in ((W, ROW, 0, False), (workloads.backward_gradient(), COL, 1, True)):
+        x = to_dev(bits)
+        q = lib.quantize(x, axis, None, 0, rnd, 7)
+        pay, sc = (q.payload_row, q.scales_row) if axis == ROW else (q.payload_col, q.scales_col)
+        d = lib.dequantize(pay, sc, q.T, dtype=torch.float32 if f32 else torch.bfloat16)
+        torch.cuda.synchronize()
+        of, ob = oracle.dequantize(pay.cpu().numpy(), sc.cpu().numpy(), float(q.T.item()))
+        if f32:
+            assert np.array_equal(d.cpu().numpy().view(np.uint32), of.view(np.uint32))
+        else:
+            assert np.array_equal(d.cpu().view(torch.int16).numpy().view(np.uint16), ob)
+        del x, q, d
 
 
 def test_periodic_scaling_sequence(lib):
