@@ -158,7 +158,8 @@ __global__ void __launch_bounds__(kRowThreads, 2) quantize_row_kernel(
 
 // ---------------------------------------------------------------- tiles
 // Column-wise and dual-axis round-to-nearest quantisation, register-resident.
-// A CTA covers 128 rows x 128 columns; warp w takes rows 16 w .. +15.  Lane l
+// A tile is 128 rows x 128 columns (each persistent CTA walks tiles with a
+// stride of the grid); warp w takes rows 16 w .. +15 of it.  Lane l
 // holds an 8 x 8 piece: rows 16 w + 8 (l / 16) .. +7, columns 8 (l % 16) .. +7,
 // loaded with eight 128-bit loads (each warp load reads two 256-byte row
 // segments).
@@ -174,12 +175,13 @@ __global__ void __launch_bounds__(kRowThreads, 2) quantize_row_kernel(
 //     the same rows; per row pair one shuffle completes both maxima and each
 //     lane computes one of the two scales, exchanged the same way;
 //   conversion: each 2 x 2 group (two BF16 words of consecutive rows) is
-//     unpacked once and multiplied by the row and the column reciprocals
-//     (packed binary32x2 multiplies); a row payload word is eight nibbles of
+//     unpacked once and multiplied by the row reciprocal (packed binary32x2
+//     multiplies) and the column reciprocal (scalar); a row payload word is eight nibbles of
 //     one row, a column payload word eight nibbles of one column.
-// The eight warps of a CTA write the 16-row pieces of each column's payload
-// side by side (64 contiguous bytes).  Nothing goes through shared memory
-// except the block-scale reciprocal table.
+// Row outputs go straight to global memory; the column payload and codes of
+// a tile are staged in shared memory (ColStage, double-buffered) and leave
+// as 64 contiguous bytes per column.  The block-scale reciprocals come from
+// a per-CTA table.
 constexpr int kRcRows = 128, kRcCols = 128, kRcThreads = 256;
 
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int q) {
@@ -463,9 +465,10 @@ __global__ void __launch_bounds__(kRcThreads, 2) quantize_tile_kernel(
 //     Philox streams.
 // Stochastic rounding draws one Philox block per row and axis: the four
 // words of counter (row C + 4 l) / 4 are exactly the lane's four elements.
-// The eight warps of a CTA write the eight 16-row pieces of each column's
-// payload side by side (64 contiguous bytes per column).  Nothing goes
-// through shared memory except the block-scale reciprocal table.
+// Row outputs go straight to global memory; the column payload and codes of
+// the tile are staged in shared memory (ColStage) and leave as 64
+// contiguous bytes per column.  The block-scale reciprocals come from a
+// per-CTA table.
 
 // Stochastic rounding of the pair (q0, q1) with random words w0, w1 -> one
 // byte of two E2M1 nibbles (q0 low).
