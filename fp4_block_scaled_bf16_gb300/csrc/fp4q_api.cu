@@ -142,6 +142,7 @@ static fp4q_status gemm_common(const uint8_t* A, const uint8_t* A_scales, const 
   if (!valid_fmt(fmt)) return FP4Q_ERR_ARG;
   if (M < 0 || N < 0 || K < 0 || K % 64 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
     return FP4Q_ERR_SHAPE;
+  if ((M + 255) / 256 > 65535) return FP4Q_ERR_SHAPE;   // 256-row tiles on the grid's y dimension
   if (qpay && N % 32) return FP4Q_ERR_SHAPE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (qamax && !aligned4(qamax)) return FP4Q_ERR_ALIGN;

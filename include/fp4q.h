@@ -139,8 +139,9 @@ fp4q_status fp4q_dequantize(const uint8_t* payload, const uint8_t* scales, int64
  * memory to FP16 as e*s*2^-4 (exact: at most 6 significant bits, within the
  * FP16 range and on its subnormal grid) and multiplied on the tcgen05 tensor
  * cores with binary32 accumulation; the 2^-8 returns in the epilogue.  out: [M, N] BF16
- * (out_is_f32 == 0) or binary32.  M, N >= 0 (any), K a multiple of 64
- * (K = 0 writes zeros).  Every internal pipeline wait is bounded (about 2 s);
+ * (out_is_f32 == 0) or binary32.  M, N >= 0 (any value up to 2^31 - 1;
+ * M at most 65535 * 256), K a multiple of 64 up to 2^31 - 64 (K = 0 writes
+ * zeros); FP4Q_ERR_SHAPE otherwise.  Every internal pipeline wait is bounded (about 2 s);
  * one that runs out latches FP4Q_ERR_TIMEOUT and the kernel exits, leaving
  * `out` unspecified.  Test hooks (environment, read per call):
  * FP4Q_TEST_GEMM_WAIT_CYCLES shortens the bound, FP4Q_TEST_GEMM_SKIP_LOADS=1

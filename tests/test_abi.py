@@ -93,6 +93,8 @@ def test_host_validation_rejects_before_launch(lib):
                   ctypes.c_int, P]
     ok = P(16)
     assert g(ok, ok, ok, ok, ok, ok, 128, 128, 96, 0, ok, 0, None) == ERR_SHAPE    # K % 64
+    assert g(ok, ok, ok, ok, ok, ok, 65535 * 256 + 1, 128, 128, 0, ok, 0, None) == ERR_SHAPE
+    assert g(ok, ok, ok, ok, ok, ok, 128, 2 ** 31, 128, 0, ok, 0, None) == ERR_SHAPE
     assert g(ok, ok, ok, ok, ok, ok, 128, 128, 128, 5, ok, 0, None) == ERR_ARG
     assert g(ok, ok, ok, ok, ok, ok, 128, 128, 128, 0, None, 0, None) == ERR_ARG
     assert g(None, ok, ok, ok, ok, ok, 128, 128, 128, 0, ok, 0, None) == ERR_ARG
