@@ -188,18 +188,24 @@ static __device__ __noinline__ uint32_t exact_code_slow(uint32_t a16, const Scal
 // With STATS the saturation flag is exact as well; without it, a block
 // whose s* lies near the largest scale needs no exact division, because both
 // sides of the largest scale round to the same (clamped) code.
+// The table's scalars, read once into registers by each kernel (the table
+// itself stays in shared memory).
+struct ScaleRegs { float inv6t, unbias, smax; uint32_t cmax; };
+__device__ __forceinline__ ScaleRegs scale_regs(const ScaleTab& tab) {
+  return ScaleRegs{tab.inv6t, tab.unbias, tab.smax, tab.cmax};
+}
 template <bool STATS>
-__device__ __forceinline__ BlockScale block_scale(uint32_t a16, const ScaleTab& tab) {
+__device__ __forceinline__ BlockScale block_scale(uint32_t a16, const ScaleTab& tab, const ScaleRegs& k) {
   BlockScale bs;
-  const float sa = __fmul_rn(__uint_as_float(a16 << 16), tab.inv6t);
-  const uint32_t x = __float_as_uint(__fmul_rn(sa, tab.unbias));
+  const float sa = __fmul_rn(__uint_as_float(a16 << 16), k.inv6t);
+  const uint32_t x = __float_as_uint(__fmul_rn(sa, k.unbias));
   const bool near_mid = ((x & 0xFFFFFu) - 0x7FFF8u) < 16u;                     // within 8 of the midpoint
-  const bool near_max = STATS && (__float_as_uint(sa) - __float_as_uint(tab.smax) + 8u) < 16u;
+  const bool near_max = STATS && (__float_as_uint(sa) - __float_as_uint(k.smax) + 8u) < 16u;
   if (near_mid || near_max) {
     bs.code = exact_code_slow(a16, tab, &bs.sat);
   } else {
-    bs.code = min((x + 0x80000u) >> 20, tab.cmax);
-    bs.sat = sa > tab.smax;
+    bs.code = min((x + 0x80000u) >> 20, k.cmax);
+    bs.sat = sa > k.smax;
   }
   bs.r = tab.recip[bs.code];
   return bs;

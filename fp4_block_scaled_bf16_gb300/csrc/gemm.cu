@@ -443,6 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = m0 + rt;
       const bool vec = F32OUT ? (N % 4 == 0) : (N % 8 == 0);
       uint32_t qmax = 0;
+      ScaleRegs kr{};
+      if (QOUT) kr = scale_regs(*tab);
 #pragma unroll 1
       for (int c = 0; c < kColChunks; ++c) {
         const int ct = 32 * (kColChunks * part + c);       // column within the tile
@@ -494,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int b = 0; b < 2; ++b) {
               const uint32_t a = max(absmax16(h + 8 * b), absmax16(h + 8 * b + 4));
               qmax = max(qmax, a);
-              const BlockScale bs = block_scale<false>(a, *tab);
+              const BlockScale bs = block_scale<false>(a, *tab, kr);
               pw[2 * b] = quantize8<false, false>(h + 8 * b, bs.r, nullptr, &cl, &fl);
               pw[2 * b + 1] = quantize8<false, false>(h + 8 * b + 4, bs.r, nullptr, &cl, &fl);
               codes |= bs.code << (8 * b);

@@ -108,6 +108,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) quantize_row_kernel(
     float* amax_out, int* status) {
   __shared__ ScaleTab tab;
   build_scale_tab(&tab, __ldg(tscale), fmt);
+  const ScaleRegs kr = scale_regs(tab);
   const int lane = threadIdx.x & 31;
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -128,7 +129,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) quantize_row_kernel(
       uint32_t m = absmax16(w);
       m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
       tmax = max(tmax, m);
-      const BlockScale bs = block_scale<STATS>(m, tab);
+      const BlockScale bs = block_scale<STATS>(m, tab, kr);
       uint32_t rb[8];
       if (SR) {
         const uint4 a = sr_words4((uint64_t)g * 2, 0u, seed);
@@ -262,6 +263,7 @@ __device__ __forceinline__ void rne_piece(const uint4 (&v)[8], int64_t R, int64_
                                           const ScaleTab& tab, uint32_t* __restrict__ pay_row,
                                           uint8_t* __restrict__ sc_row, ColStage& stage, int warp, int cg,
                                           TileCounts& cnt) {
+  const ScaleRegs kr = scale_regs(tab);
   // ---- magnitudes: cmx[q] = maxima of columns 2q (low) and 2q + 1 (high);
   // rpx[p] = maxima of rows 2p (low) and 2p + 1 (high) over the lane's columns
   uint32_t cmx[4] = {0u, 0u, 0u, 0u}, rpx[4];
@@ -288,7 +290,7 @@ __device__ __forceinline__ void rne_piece(const uint4 (&v)[8], int64_t R, int64_
     uint32_t m = max(tm & 0xFFFFu, tm >> 16);
     m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
     m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
-    ts = block_scale<STATS>(m, tab);
+    ts = block_scale<STATS>(m, tab, kr);
     if (STATS && ok && par == 0 && half == 0) {
       cnt.r_sat += ts.sat ? 1u : 0u;
       cnt.r_uflow += (m != 0u && ts.code == 0u) ? 1u : 0u;
@@ -307,7 +309,7 @@ __device__ __forceinline__ void rne_piece(const uint4 (&v)[8], int64_t R, int64_
   for (int q = 0; q < 4 && !TWO_D; ++q) {
     const uint32_t full = __vmaxu2(cmx[q], __shfl_xor_sync(0xFFFFFFFFu, cmx[q], 16));
     const uint32_t cm = __byte_perm(full, 0u, pick);
-    const BlockScale bs = block_scale<STATS>(cm, tab);
+    const BlockScale bs = block_scale<STATS>(cm, tab, kr);
     const float other = __shfl_xor_sync(0xFFFFFFFFu, bs.r, 16);
     colr[2 * q] = half ? other : bs.r;
     colr[2 * q + 1] = half ? bs.r : other;
@@ -332,7 +334,7 @@ __device__ __forceinline__ void rne_piece(const uint4 (&v)[8], int64_t R, int64_
     } else if (DO_ROW) {
       const uint32_t full = __vmaxu2(rpx[p], __shfl_xor_sync(0xFFFFFFFFu, rpx[p], 1));
       const uint32_t m = __byte_perm(full, 0u, rpick);          // row 2p + par
-      const BlockScale bs = block_scale<STATS>(m, tab);
+      const BlockScale bs = block_scale<STATS>(m, tab, kr);
       const float other = __shfl_xor_sync(0xFFFFFFFFu, bs.r, 1);
       re = par ? other : bs.r;
       ro = par ? bs.r : other;
@@ -514,6 +516,7 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile4_kernel(
     }
   }
   build_scale_tab(&tab, __ldg(tscale), fmt);   // while the piece is in flight
+  const ScaleRegs kr = scale_regs(tab);
 
   // ---- magnitudes: cmx0 = columns 0 (low), 1 (high); cmx1 = columns 2, 3;
   // rpx[i] = rows 2i (low), 2i + 1 (high)
@@ -537,7 +540,7 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile4_kernel(
   if (TWO_D) {
     uint32_t m = max(tmax, __shfl_xor_sync(0xFFFFFFFFu, tmax, 1));
     m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-    ts = block_scale<STATS>(m, tab);
+    ts = block_scale<STATS>(m, tab, kr);
     if (STATS && ok && own == 0) {
       r_sat += ts.sat ? 1u : 0u;
       r_uflow += (m != 0u && ts.code == 0u) ? 1u : 0u;
@@ -555,7 +558,7 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile4_kernel(
   for (int j = 0; j < 4 && !TWO_D; ++j) {
     const uint32_t w = j < 2 ? cmx0 : cmx1;
     const uint32_t cm = (j & 1) ? (w >> 16) : (w & 0xFFFFu);
-    const BlockScale bs = block_scale<STATS>(cm, tab);
+    const BlockScale bs = block_scale<STATS>(cm, tab, kr);
     rc[j] = bs.r;
     stage.sc[8 * (4 * lane + j) + warp] = (uint8_t)bs.code;
     if (ok) {
@@ -584,7 +587,7 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile4_kernel(
       // row 4k + own sits in word 2k + own / 2, half own % 2
       const uint32_t w = (own >> 1) ? rpx[2 * k + 1] : rpx[2 * k];
       const uint32_t m = __byte_perm(w, 0u, pick);
-      const BlockScale bs = block_scale<STATS>(m, tab);
+      const BlockScale bs = block_scale<STATS>(m, tab, kr);
       rown[k] = bs.r;
       if (ok) {
         sc_row[((r0 + 4 * k + own) * C + (c0 & ~(int64_t)15)) >> 4] = (uint8_t)bs.code;
