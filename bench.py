@@ -358,47 +358,75 @@ def run_gpu(args, rank, world):
     d2h = (hY[0].numel() + hdX[0].numel() + hdW[0].numel()) * 2
     del steps2
 
-    # ---- single-axis quantiser rates (outside the step): W row-wise RNE and
-    # dY row-wise SR, 10 launches each, inputs larger than L2
+    # ---- quantiser rates outside the step.  Each is timed as the replay of a
+    # CUDA graph of its launches, so that the host's per-call cost does not
+    # enter the device time of these short kernels; inputs larger than L2.
+    def _graph_ms(fn, calls, replays=5):
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            fn()                                    # warm-up outside the capture
+        torch.cuda.current_stream().wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        g.replay()
+        b0 = torch.cuda.Event(enable_timing=True)
+        b1 = torch.cuda.Event(enable_timing=True)
+        b0.record()
+        for _ in range(replays):
+            g.replay()
+        b1.record()
+        torch.cuda.synchronize()
+        del g
+        return b0.elapsed_time(b1) / (replays * calls)
+
     rates = {}
+    # single-axis: W row-wise RNE and dY row-wise SR, 10 launches
     for name, x, rnd, pay, sc in (("W_row_rne", step.W, fp4q.RNE, step.Wr, step.Wrs),
                                   ("dY_row_sr", step.dY, fp4q.SR, step.Dr, step.Drs)):
         Tn = step.T[1:2] if x is step.W else step.T[2:3]
-        a0 = torch.cuda.Event(enable_timing=True)
-        a1 = torch.cuda.Event(enable_timing=True)
-        fp4q.fp4q_quantize(x, fp4q.AXIS_ROW, fp4q.UE5M3, Tn, rnd, 7, pay, sc, None, None)
-        a0.record()
-        for _ in range(10):
-            fp4q.fp4q_quantize(x, fp4q.AXIS_ROW, fp4q.UE5M3, Tn, rnd, 7, pay, sc, None, None)
-        a1.record()
-        torch.cuda.synchronize()
-        rates[name] = x.numel() * ROW_BYTES_PER_ELEM / (a0.elapsed_time(a1) / 10 * 1e-3) / 1e9
+
+        def run(x=x, rnd=rnd, pay=pay, sc=sc, Tn=Tn):
+            for _ in range(10):
+                fp4q.fp4q_quantize(x, fp4q.AXIS_ROW, fp4q.UE5M3, Tn, rnd, 7, pay, sc, None, None)
+        rates[name] = x.numel() * ROW_BYTES_PER_ELEM / (_graph_ms(run, 10) * 1e-3) / 1e9
     # dequantisation (support op): W's row-wise payload and scales -> BF16
     Wd = torch.empty_like(step.W)
-    fp4q.fp4q_dequantize(step.Wr, step.Wrs, FFN, HID, fp4q.UE5M3, step.T[1:2], Wd)
-    a0 = torch.cuda.Event(enable_timing=True)
-    a1 = torch.cuda.Event(enable_timing=True)
-    a0.record()
-    for _ in range(10):
-        fp4q.fp4q_dequantize(step.Wr, step.Wrs, FFN, HID, fp4q.UE5M3, step.T[1:2], Wd)
-    a1.record()
-    torch.cuda.synchronize()
-    rates["W_dequant_bf16"] = step.W.numel() * ROW_BYTES_PER_ELEM / (a0.elapsed_time(a1) / 10 * 1e-3) / 1e9
+
+    def run_deq():
+        for _ in range(10):
+            fp4q.fp4q_dequantize(step.Wr, step.Wrs, FFN, HID, fp4q.UE5M3, step.T[1:2], Wd)
+    rates["W_dequant_bf16"] = step.W.numel() * ROW_BYTES_PER_ELEM / (_graph_ms(run_deq, 10) * 1e-3) / 1e9
     del Wd
     # 16 x 16 (transposition-invariant) scaling: both layouts from one
     # quantisation, same algorithmic bytes as the dual-axis quantisers
     for name, x, rnd, outs in (("W_2d_rne", step.W, fp4q.RNE, (step.Wr, step.Wrs, step.Wc, step.Wcs)),
                                ("dY_2d_sr", step.dY, fp4q.SR, (step.Dr, step.Drs, step.Dc, step.Dcs))):
         Tn = step.T[1:2] if x is step.W else step.T[2:3]
-        a0 = torch.cuda.Event(enable_timing=True)
-        a1 = torch.cuda.Event(enable_timing=True)
-        fp4q.fp4q_quantize(x, fp4q.AXIS_BOTH_2D, fp4q.UE5M3, Tn, rnd, 7, *outs)
-        a0.record()
-        for _ in range(10):
-            fp4q.fp4q_quantize(x, fp4q.AXIS_BOTH_2D, fp4q.UE5M3, Tn, rnd, 7, *outs)
-        a1.record()
-        torch.cuda.synchronize()
-        rates[name] = x.numel() * DUAL_BYTES_PER_ELEM / (a0.elapsed_time(a1) / 10 * 1e-3) / 1e9
+
+        def run2d(x=x, rnd=rnd, outs=outs, Tn=Tn):
+            for _ in range(10):
+                fp4q.fp4q_quantize(x, fp4q.AXIS_BOTH_2D, fp4q.UE5M3, Tn, rnd, 7, *outs)
+        rates[name] = x.numel() * DUAL_BYTES_PER_ELEM / (_graph_ms(run2d, 10) * 1e-3) / 1e9
+    # periodic scaling (config 4's per-step quantisation): a 4096 x 4096
+    # tensor quantised row-wise (RNE) with the fused amax that the next
+    # refresh uses, the tensor scale taken from an earlier step (no amax
+    # pass); eight distinct tensors in turn, 256 MB in all, so that inputs do
+    # not stay in L2.  The block and element counts (a report, not needed by
+    # the scaling) are timed separately.
+    per = [torch.randn(4096, 4096, device=dev).bfloat16() for _ in range(8)]
+    Tp = fp4q.tensor_scale(fp4q.amax(per[0]))
+    pp = torch.empty((4096, 2048), dtype=torch.uint8, device=dev)
+    sp = torch.empty((4096, 256), dtype=torch.uint8, device=dev)
+    stp = torch.empty((1, 4), dtype=torch.int64, device=dev)
+    ap = torch.empty(1, dtype=torch.float32, device=dev)
+    for name, st in (("periodic_4096sq_row_rne_amax", None), ("periodic_4096sq_row_rne_amax_counts", stp)):
+        def run_per(st=st):
+            for x in per:
+                fp4q.fp4q_quantize(x, fp4q.AXIS_ROW, fp4q.UE5M3, Tp, fp4q.RNE, 0, pp, sp, None, None, st, ap)
+        rates[name] = 4096 * 4096 * ROW_BYTES_PER_ELEM / (_graph_ms(run_per, len(per)) * 1e-3) / 1e9
+    del per
     # ---- fprop with the quantisation of Y for the next layer: separate
     # (GEMM, then row-wise RNE quantisation of Y) versus fused into the GEMM's
     # epilogue, with and without writing Y in BF16; 10 launches each
