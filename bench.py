@@ -590,7 +590,8 @@ def main():
     q_gbs = [b / (t * 1e-3) / 1e9 for b, t in zip(q_bytes, r["t_q"])]
     cpu = None
     if not args.no_cpu_baseline:
-        est, spent, sample = oracle_sample(qrows=1024, grows=6, gcols=4096)
+        # about 10 s of single-thread CPU work
+        est, spent, sample = oracle_sample(qrows=3072, grows=20, gcols=4096)
         cpu = {"value": STEP_FLOPS / est / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
                "sample": f"{sample}; {spent:.1f} s of CPU time"}
     line = {
