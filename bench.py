@@ -156,6 +156,30 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def bind_to_gpu_node(torch, index):
+    """Restricts this process to the CPUs local to the GPU (its PCI device's
+    local_cpulist), so that the pinned host buffers of the end-to-end
+    measurement are allocated next to it, as `numactl --cpunodebind` would.
+    Returns the CPU list, or None when it cannot be determined."""
+    try:
+        p = torch.cuda.get_device_properties(index)
+        addr = f"{p.pci_domain_id:04x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+        with open(f"/sys/bus/pci/devices/{addr}/local_cpulist") as f:
+            text = f.read().strip()
+        cpus = set()
+        for part in text.split(","):
+            if "-" in part:
+                a, b = part.split("-")
+                cpus.update(range(int(a), int(b) + 1))
+            elif part:
+                cpus.add(int(part))
+        if cpus and cpus != set(os.sched_getaffinity(0)):
+            os.sched_setaffinity(0, cpus & set(range(os.cpu_count() or 1)) or cpus)
+        return text
+    except Exception:
+        return None
+
+
 # ---------------------------------------------------------------- GPU path
 class Step:
     """Device buffers and the launch sequence of one step."""
@@ -261,6 +285,7 @@ def run_gpu(args, rank, world):
     build.build()
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
+    affinity = bind_to_gpu_node(torch, dev.index)
     if M_TOK == workloads.TOKENS:
         Xb, Wb = workloads.fprop_operands()
         dYb = workloads.backward_gradient()
@@ -355,6 +380,16 @@ def run_gpu(args, rank, world):
     torch.cuda.synchronize()
     e2e_ms = s0.elapsed_time(s1) / e2e_steps
     h2d = (hX.numel() + hW.numel() + hD.numel()) * 2
+    # the host link on its own: one 256 MiB copy each way from pinned memory
+    link = {}
+    for name, src, dst in (("h2d_gbs", hD, steps2[0].dY), ("d2h_gbs", steps2[0].dY, hD)):
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        c0.record()
+        dst.copy_(src, non_blocking=True)
+        c1.record()
+        torch.cuda.synchronize()
+        link[name] = src.numel() * 2 / (c0.elapsed_time(c1) * 1e-3) / 1e9
     d2h = (hY[0].numel() + hdX[0].numel() + hdW[0].numel()) * 2
     del steps2
 
@@ -484,7 +519,7 @@ def run_gpu(args, rank, world):
         del lin
 
     return dict(ms=ms, ms_serial=ms_serial, fused=fused, block=block, t_scale=t_scale, t_q=(t_qx, t_qw, t_qd), t_g=t_g, launches=launches, rates=rates,
-                clocks=clk.summary(), status=status, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
+                clocks=clk.summary(), status=status, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, link=link, affinity=affinity,
                 elems=(X.numel(), W.numel(), dY.numel()))
 
 
@@ -618,7 +653,9 @@ def main():
                          "quantize_dY": r["t_q"][2], "fprop": r["t_g"][0], "dgrad": r["t_g"][1],
                          "wgrad": r["t_g"][2]},
         "e2e": {"value": job_tflops(world, STEP_FLOPS, r["e2e_ms"]), "unit": "TFLOP/s",
-                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e_ms"]},
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e_ms"],
+                "host_link_gbs": {k: round(v, 1) for k, v in r["link"].items()},
+                "cpu_affinity": r["affinity"]},
         "fused_epilogue_fprop": r["fused"],
         "linear_block_fwd_bwd": r["block"],
         "gpu_launches": r["launches"],
