@@ -262,13 +262,18 @@ __device__ __forceinline__ uint32_t quantize8(const uint32_t w[4], float r, cons
   }
   const uint32_t nib = cvt_e2m1x8(q);
   if (STATS) {
+    // one flag bit per element, bit 3 of its nibble: magnitude 0 (adding 7
+    // to a 3-bit magnitude sets bit 3 unless it is 0, with no carry out of
+    // the nibble), and a nonzero input (the two BF16 halves of word j are
+    // elements 2j and 2j + 1, nibbles 2j and 2j + 1)
+    const uint32_t zero_mag = ~((nib & 0x77777777u) + 0x77777777u) & 0x88888888u;
+    uint32_t nonzero = 0u;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint32_t xbits = (j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xFFFFu);
-      const bool nonzero = (xbits & 0x7FFFu) != 0u;
-      const bool zero_mag = ((nib >> (4 * j)) & 7u) == 0u;
-      *flushed += (nonzero && zero_mag) ? 1u : 0u;
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t m = __vsetne2(w[j] & 0x7FFF7FFFu, 0u);     // 1 in each nonzero half
+      nonzero |= ((m | (m >> 12)) & 0x11u) << (8 * j + 3);
     }
+    *flushed += __popc(zero_mag & nonzero);
   }
   return nib;
 }
