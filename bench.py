@@ -156,6 +156,19 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def parse_cpulist(text: str) -> set:
+    """CPU numbers of a sysfs list such as "0-3,8,10-11"."""
+    cpus = set()
+    for part in text.strip().split(","):
+        part = part.strip()
+        if "-" in part:
+            a, b = part.split("-")
+            cpus.update(range(int(a), int(b) + 1))
+        elif part:
+            cpus.add(int(part))
+    return cpus
+
+
 def bind_to_gpu_node(torch, index):
     """Restricts this process to the CPUs local to the GPU (its PCI device's
     local_cpulist), so that the pinned host buffers of the end-to-end
@@ -166,13 +179,7 @@ def bind_to_gpu_node(torch, index):
         addr = f"{p.pci_domain_id:04x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
         with open(f"/sys/bus/pci/devices/{addr}/local_cpulist") as f:
             text = f.read().strip()
-        cpus = set()
-        for part in text.split(","):
-            if "-" in part:
-                a, b = part.split("-")
-                cpus.update(range(int(a), int(b) + 1))
-            elif part:
-                cpus.add(int(part))
+        cpus = parse_cpulist(text)
         if cpus and cpus != set(os.sched_getaffinity(0)):
             os.sched_setaffinity(0, cpus & set(range(os.cpu_count() or 1)) or cpus)
         return text
