@@ -84,6 +84,11 @@ def _dev(t, name, dtype=None):
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
 
 
+def _out_dtype(out):
+    if out.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError(f"out must be bfloat16 or float32, got {out.dtype}")
+
+
 # ------------------------------------------------------------ C entry points
 def fp4q_amax(x: torch.Tensor, out_amax: torch.Tensor) -> None:
     _dev(x, "x", torch.bfloat16)
@@ -118,6 +123,8 @@ def fp4q_dequantize(payload, scales, rows, cols, fmt, tensor_scale, out) -> None
     _dev(payload, "payload", torch.uint8)
     _dev(scales, "scales", torch.uint8)
     _dev(out, "out")
+    _dev(tensor_scale, "tensor_scale", torch.float32)
+    _out_dtype(out)
     f32 = out.dtype == torch.float32
     _check("fp4q_dequantize", _lib.fp4q_dequantize(
         _ptr(payload), _ptr(scales), rows, cols, fmt, _ptr(tensor_scale), _ptr(out), int(f32),
@@ -128,6 +135,9 @@ def fp4q_gemm(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K, fmt, out) -
     for n, t in (("A", A), ("A_scales", A_scales), ("B", B), ("B_scales", B_scales)):
         _dev(t, n, torch.uint8)
     _dev(out, "out")
+    _dev(A_tscale, "A_tscale", torch.float32)
+    _dev(B_tscale, "B_tscale", torch.float32)
+    _out_dtype(out)
     f32 = out.dtype == torch.float32
     _check("fp4q_gemm", _lib.fp4q_gemm(
         _ptr(A), _ptr(A_scales), _ptr(A_tscale), _ptr(B), _ptr(B_scales), _ptr(B_tscale),
