@@ -30,9 +30,18 @@ SR = 1
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "fp4q_oracle.c")
 _BUILD = os.path.join(_HERE, "_build")
-_SO = os.path.join(_BUILD, "liboracle.so")
 _CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
            "-fno-fast-math", "-fno-finite-math-only"]
+# FP4Q_ORACLE_SANITIZE=1 builds a separate AddressSanitizer + UBSan copy (the
+# sanitizer runtimes must then be preloaded, e.g.
+#   LD_PRELOAD="$(gcc -print-file-name=libasan.so):$(gcc -print-file-name=libubsan.so)"
+#   ASAN_OPTIONS=detect_leaks=0 FP4Q_ORACLE_SANITIZE=1 python -m pytest tests -m "not gpu" -k oracle)
+if os.environ.get("FP4Q_ORACLE_SANITIZE") == "1":
+    _SO = os.path.join(_BUILD, "liboracle_sanitize.so")
+    _CFLAGS = [f for f in _CFLAGS if f != "-O2"] + ["-O1", "-g", "-fsanitize=address,undefined",
+                                                     "-fno-sanitize-recover=all"]
+else:
+    _SO = os.path.join(_BUILD, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
