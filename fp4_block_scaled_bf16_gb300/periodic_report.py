@@ -14,32 +14,28 @@ from __future__ import annotations
 import argparse
 import json
 
-import torch
-
 from . import fp4q, workloads
+from .periodic import PeriodicScaler
 
 
-def run(mode: str = "walk", steps: int = 64, period: int = 16, n: int = 4096):
+def run(mode: str = "walk", steps: int = 64, period: int = 16, n: int = 4096, device: str = "cuda",
+        lib=None):
+    """Per-step counts of every variant.  `lib` replaces the binding (tests
+    run the schedule through a stand-in on `device`)."""
     amaxes = workloads.drift_amaxes(steps, mode=mode)
     variants = [("UE5M3", fp4q.UE5M3, 1.0), ("UE5M3", fp4q.UE5M3, 16.0), ("UE5M3", fp4q.UE5M3, 256.0),
                 ("UE4M3", fp4q.UE4M3, 1.0)]
     out = {f"{name}_H{int(h)}": [] for name, _, h in variants}
-    state = {k: (torch.zeros(1, device="cuda"), torch.zeros(1, device="cuda")) for k in out}
+    scalers = {f"{name}_H{int(h)}": PeriodicScaler(period, fmt, h, device=device, lib=lib)
+               for name, fmt, h in variants}
     for t in range(steps):
-        x = workloads.to_torch_bf16(workloads.drift_tensor(t, amaxes[t], n)).cuda()
-        for name, fmt, h in variants:
-            key = f"{name}_H{int(h)}"
-            last, T = state[key]
-            if t == 0:
-                fp4q.fp4q_amax(x, last)
-            if t % period == 0:
-                fp4q.fp4q_tensor_scale(last, fmt, h, T)
-            q = fp4q.quantize(x, fp4q.AXIS_ROW, T, fmt, stats=True, want_amax=True)
+        x = workloads.to_torch_bf16(workloads.drift_tensor(t, amaxes[t], n)).to(device)
+        for key, sc in scalers.items():
+            q = sc.quantize(x, fp4q.AXIS_ROW, stats=True)
             st = q.stats[0].tolist()
-            out[key].append({"step": t, "amax": amaxes[t], "T": float(T.item()),
+            out[key].append({"step": t, "amax": amaxes[t], "T": float(q.T.item()),
                              "scale_sat_blocks": st[0], "scale_uflow_blocks": st[1],
                              "elem_clamped": st[2], "elem_flushed": st[3]})
-            state[key] = (q.amax, T)
     return out
 
 

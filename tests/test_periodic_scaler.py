@@ -104,3 +104,20 @@ def test_gpu_scaler_matches_oracle_scaler():
     again.load_state_dict(state)
     assert again.state_dict() == state
     assert fp4q.fp4q_get_device_status() == fp4q.OK
+
+
+@pytest.mark.parametrize("mode", ["walk", "monotone"])
+def test_periodic_report_counts_match_oracle(mode):
+    from fp4_block_scaled_bf16_gb300 import periodic_report
+    steps, period, n = 20, 8, 64
+    res = periodic_report.run(mode, steps=steps, period=period, n=n, device="cpu", lib=oracle_lib())
+    amaxes = workloads.drift_amaxes(steps, mode=mode)
+    for key, fmt, h in (("UE5M3_H1", 0, 1.0), ("UE5M3_H16", 0, 16.0), ("UE5M3_H256", 0, 256.0),
+                        ("UE4M3_H1", 1, 1.0)):
+        ref = oracle.PeriodicScaler(period=period, fmt=fmt, headroom=h)
+        for t in range(steps):
+            _, _, st = ref.quantize(workloads.drift_tensor(t, amaxes[t], n))
+            row = res[key][t]
+            assert row["T"] == ref.T
+            assert [row["scale_sat_blocks"], row["scale_uflow_blocks"], row["elem_clamped"],
+                    row["elem_flushed"]] == [int(v) for v in st], (key, t)
