@@ -25,6 +25,14 @@ COMMON = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE
           "--expt-relaxed-constexpr"]
 # the quantiser's bytes must be a pure function of its input: no contraction
 PER_FILE = {"quantize.cu": ["-fmad=false"], "fp4q_api.cu": [], "gemm.cu": []}
+# FP4Q_NVTX=1: every C entry point becomes an NVTX range (header-only NVTX 3)
+if os.environ.get("FP4Q_NVTX") == "1":
+    PER_FILE["fp4q_api.cu"] = ["-DFP4Q_NVTX"]
+STAMP = os.path.join(BUILD, "flags.txt")
+
+
+def _flags() -> str:
+    return " ".join(ARCH + COMMON + [f"{k}:{' '.join(v)}" for k, v in sorted(PER_FILE.items())])
 
 
 def nvcc() -> str:
@@ -41,7 +49,13 @@ def _mtime(p):
 def _stale() -> bool:
     deps = [os.path.join(CSRC, f) for f in SOURCES + HEADERS] + [os.path.join(INCLUDE, "fp4q.h"),
                                                                 os.path.abspath(__file__)]
-    return _mtime(LIB) < max(_mtime(d) for d in deps)
+    if _mtime(LIB) < max(_mtime(d) for d in deps):
+        return True
+    try:
+        with open(STAMP) as f:
+            return f.read() != _flags()
+    except OSError:
+        return True
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
@@ -70,6 +84,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(STAMP, "w") as f:
+        f.write(_flags())
     return LIB
 
 

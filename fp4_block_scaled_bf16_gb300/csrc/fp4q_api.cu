@@ -9,6 +9,22 @@
 #include "fp4q_device.cuh"
 #include "fp4q_launch.h"
 
+// Built with -DFP4Q_NVTX (FP4Q_NVTX=1 in the environment of the build), every
+// entry point is an NVTX range named after it, for timeline profilers; the
+// default build has none.
+#ifdef FP4Q_NVTX
+#include <nvtx3/nvToolsExt.h>
+namespace {
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
+}  // namespace
+#define FP4Q_RANGE(name) NvtxRange fp4q_nvtx_range_(name)
+#else
+#define FP4Q_RANGE(name) ((void)0)
+#endif
+
 namespace {
 
 // Latched by kernels (non-finite input, bounded-wait timeout); read and
@@ -53,6 +69,7 @@ const char* fp4q_status_string(fp4q_status s) {
 }
 
 fp4q_status fp4q_amax(const void* in_bf16, int64_t n, float* out_amax, void* stream) {
+  FP4Q_RANGE("fp4q_amax");
   if (!out_amax || n < 0 || (n > 0 && !in_bf16)) return FP4Q_ERR_ARG;
   if ((n > 0 && !aligned16(in_bf16)) || !aligned4(out_amax)) return FP4Q_ERR_ALIGN;
   int* st = status_ptr();
@@ -62,6 +79,7 @@ fp4q_status fp4q_amax(const void* in_bf16, int64_t n, float* out_amax, void* str
 
 fp4q_status fp4q_tensor_scale(const float* amax, fp4q_scale_fmt fmt, float headroom, float* out_scale,
                               void* stream) {
+  FP4Q_RANGE("fp4q_tensor_scale");
   if (!amax || !out_scale || !valid_fmt(fmt)) return FP4Q_ERR_ARG;
   // headroom must be a power of two >= 1 so that 6 * Smax / H is exact
   int e = 0;
@@ -76,6 +94,7 @@ fp4q_status fp4q_quantize(const void* in_bf16, int64_t rows, int64_t cols, fp4q_
                           uint64_t seed, uint8_t* out_payload_row, uint8_t* out_scales_row,
                           uint8_t* out_payload_col, uint8_t* out_scales_col, fp4q_stats* out_stats,
                           float* out_amax, void* stream) {
+  FP4Q_RANGE("fp4q_quantize");
   if (axis != FP4Q_AXIS_ROW && axis != FP4Q_AXIS_COL && axis != FP4Q_AXIS_BOTH && axis != FP4Q_AXIS_BOTH_2D)
     return FP4Q_ERR_ARG;
   if (!valid_fmt(fmt) || (rnd != FP4Q_RNE && rnd != FP4Q_SR) || !tensor_scale) return FP4Q_ERR_ARG;
@@ -121,6 +140,7 @@ fp4q_status fp4q_quantize(const void* in_bf16, int64_t rows, int64_t cols, fp4q_
 fp4q_status fp4q_dequantize(const uint8_t* payload, const uint8_t* scales, int64_t rows, int64_t cols,
                             fp4q_scale_fmt fmt, const float* tensor_scale, void* out, int out_is_f32,
                             void* stream) {
+  FP4Q_RANGE("fp4q_dequantize");
   if (!valid_fmt(fmt) || !tensor_scale) return FP4Q_ERR_ARG;
   if (rows < 0 || cols < 0 || rows % 16 || cols % 16) return FP4Q_ERR_SHAPE;
   if (rows > 0 && cols > 0) {
@@ -204,6 +224,7 @@ static fp4q_status gemm_common(const uint8_t* A, const uint8_t* A_scales, const 
 fp4q_status fp4q_gemm(const uint8_t* A, const uint8_t* A_scales, const float* A_tscale, const uint8_t* B,
                       const uint8_t* B_scales, const float* B_tscale, int64_t M, int64_t N, int64_t K,
                       fp4q_scale_fmt fmt, void* out, int out_is_f32, void* stream) {
+  FP4Q_RANGE("fp4q_gemm");
   return gemm_common(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K, fmt, out, out_is_f32,
                      nullptr, nullptr, nullptr, nullptr, stream);
 }
@@ -213,12 +234,14 @@ fp4q_status fp4q_gemm_quantize(const uint8_t* A, const uint8_t* A_scales, const 
                                int64_t M, int64_t N, int64_t K, fp4q_scale_fmt fmt,
                                const float* c_tscale, void* out_bf16, uint8_t* out_payload,
                                uint8_t* out_scales, float* out_amax, void* stream) {
+  FP4Q_RANGE("fp4q_gemm_quantize");
   if (M > 0 && N > 0 && !out_payload) return FP4Q_ERR_ARG;
   return gemm_common(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K, fmt, out_bf16, 0,
                      c_tscale, out_payload, out_scales, out_amax, stream);
 }
 
 fp4q_status fp4q_get_device_status(int* out) {
+  FP4Q_RANGE("fp4q_get_device_status");
   if (!out) return FP4Q_ERR_ARG;
   if (cudaDeviceSynchronize() != cudaSuccess) return FP4Q_ERR_CUDA;
   int v = 0;
