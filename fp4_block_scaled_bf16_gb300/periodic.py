@@ -13,6 +13,10 @@ refresh is one `fp4q_tensor_scale` launch.
 The state ({T, last amax, step}) is saved and restored with `state_dict` /
 `load_state_dict`, so that a resumed run refreshes on the same steps with the
 same scale.
+
+Every launch goes through libfp4q.so (the `fp4q` binding); the `lib`
+argument exists only so that tests can drive the schedule through a stand-in
+with the same interface.
 """
 from __future__ import annotations
 
