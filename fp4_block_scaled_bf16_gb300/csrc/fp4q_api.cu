@@ -27,9 +27,11 @@ struct NvtxRange {
 
 namespace {
 
-// Latched by kernels (non-finite input, bounded-wait timeout); read and
-// cleared by fp4q_get_device_status.
+// Latched by kernels (non-finite input, bounded-wait timeout) with atomicOr;
+// read and cleared by fp4q_get_device_status.
 __device__ int g_status_word;
+
+__global__ void clear_status_kernel(int* word, int bits) { atomicAnd(word, ~bits); }
 
 int* status_ptr() {
   // One address per device; looked up on each call (cheap) so that a caller
@@ -240,14 +242,22 @@ fp4q_status fp4q_gemm_quantize(const uint8_t* A, const uint8_t* A_scales, const 
                      c_tscale, out_payload, out_scales, out_amax, stream);
 }
 
-fp4q_status fp4q_get_device_status(int* out) {
+fp4q_status fp4q_get_device_status(int* out, void* stream) {
   FP4Q_RANGE("fp4q_get_device_status");
   if (!out) return FP4Q_ERR_ARG;
-  if (cudaDeviceSynchronize() != cudaSuccess) return FP4Q_ERR_CUDA;
+  int* st = status_ptr();
+  if (!st) return FP4Q_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
   int v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(int)) != cudaSuccess) return FP4Q_ERR_CUDA;
-  const int zero = 0;
-  if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int)) != cudaSuccess) return FP4Q_ERR_CUDA;
+  // stream-ordered read of the word, then a wait on this stream only
+  if (cudaMemcpyAsync(&v, st, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return FP4Q_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FP4Q_ERR_CUDA;
+  if (v) {
+    // clear only the bits reported here, atomically: a condition latched by
+    // another stream in the meantime stays set for the next read
+    clear_status_kernel<<<1, 1, 0, s>>>(st, v);
+    if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) return FP4Q_ERR_CUDA;
+  }
   *out = (v & fp4q::kStatusTimeout) ? FP4Q_ERR_TIMEOUT
          : (v & fp4q::kStatusNonFinite) ? FP4Q_ERR_NONFINITE
                                         : FP4Q_OK;

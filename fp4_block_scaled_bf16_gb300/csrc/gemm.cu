@@ -29,7 +29,10 @@
 //   warp 17     allocates TMEM; one lane issues 8 MMAs (2 x M128 N256 K16)
 //               per stage and commits them to the stage's "empty" barrier.
 // Every wait is bounded: a wait that runs out latches FP4Q_ERR_TIMEOUT in the
-// device status word and the CTA drains and exits instead of hanging.
+// device status word and the CTA exits instead of hanging, once the producer
+// has waited (bounded) for the loads it issued and the MMA issuer for the
+// MMAs it issued, so that nothing asynchronous still targets the CTA's
+// shared memory or TMEM when it is freed.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <string.h>
@@ -296,6 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kProducerWarp) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
+      int last_kb = -1, last_g = -1;   // the last K step / code stage whose loads were issued
       for (int kb = 0; kb < nk; ++kb) {
         if (TMA_CODES && kb % CODE_KB == 0) {
           const int g = kb / CODE_KB, cs = g % S_CODE;
@@ -308,6 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_expect_tx(bar_code_full + 8 * cs, CODE_STAGE);
             tma_load_2d(cdst, &mapAs, g * 16, m0, bar_code_full + 8 * cs);
             tma_load_2d(cdst + BM * 16, &mapBs, g * 16, n0, bar_code_full + 8 * cs);
+            last_g = g;
           }
         }
         const int s = kb % S_RAW;
@@ -320,7 +325,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_expect_tx(bar_raw_full + 8 * s, RAW_STAGE);
         tma_load_2d(dst, &mapA, kb * (BK / 2), m0, bar_raw_full + 8 * s);
         tma_load_2d(dst + RAW_A, &mapB, kb * (BK / 2), n0, bar_raw_full + 8 * s);
+        last_kb = kb;
       }
+      // Drain, also after an abort: a load already issued still lands in this
+      // CTA's shared memory, so the CTA must not exit before it has.  A stage
+      // is refilled only after its previous contents were consumed, so only
+      // the last load into each stage can still be in flight; wait for each
+      // of those (bounded, whatever the abort flag says).
+      bool drained = true;
+      for (int s = 0; s < S_RAW; ++s) {
+        if (last_kb < s) continue;
+        const int kb = s + (last_kb - s) / S_RAW * S_RAW;
+        drained &= mbar_wait_bounded(bar_raw_full + 8 * s, (kb / S_RAW) & 1, budget);
+      }
+      for (int cs = 0; TMA_CODES && cs < S_CODE; ++cs) {
+        if (last_g < cs) continue;
+        const int g = cs + (last_g - cs) / S_CODE * S_CODE;
+        drained &= mbar_wait_bounded(bar_code_full + 8 * cs, (g / S_CODE) & 1, budget);
+      }
+      if (!drained) atomicOr(status, kStatusTimeout);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------ MMA issuer
@@ -344,6 +367,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar_bf_empty + 8 * t);
       }
       mma_commit(bar_acc);
+      // Drain, also after an abort: bar_acc completes once every MMA issued
+      // above has finished reading shared memory and writing TMEM, which must
+      // happen before TMEM is freed and the CTA exits (bounded, whatever the
+      // abort flag says).
+      if (!mbar_wait_bounded(bar_acc, 0, budget)) atomicOr(status, kStatusTimeout);
     }
   } else {
     // ------------------------------------------------ expansion warps

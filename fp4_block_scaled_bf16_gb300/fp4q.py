@@ -49,7 +49,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fp4q_dequantize.argtypes = [P, P, i64, i64, i32, P, P, i32, P]
     lib.fp4q_gemm.argtypes = [P, P, P, P, P, P, i64, i64, i64, i32, P, i32, P]
     lib.fp4q_gemm_quantize.argtypes = [P, P, P, P, P, P, i64, i64, i64, i32, P, P, P, P, P, P]
-    lib.fp4q_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_int)]
+    lib.fp4q_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), P]
     lib.fp4q_status_string.argtypes = [i32]
     lib.fp4q_status_string.restype = ctypes.c_char_p
     for name in EXPORTS[:-1]:
@@ -73,15 +73,55 @@ def _check(fn, code):
         raise Fp4qError(fn, code, _lib)
 
 
-def _dev(t, name, dtype=None):
+# ------------------------------------------------------------ validation
+# The library trusts the sizes it is given: a buffer smaller than they imply
+# would be read or written out of bounds on the device.  So every entry point
+# checks here, before the call, that each tensor has exactly the shape the
+# sizes imply, the expected dtype, is contiguous, and lives on the current
+# CUDA device (the library launches on the current device's current stream).
+# Shapes are checked before devices, so that these checks run without a GPU.
+def _mat(t, name, shape, dtype):
     if t is None:
-        return
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
-    if not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous")
-    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} is required")
+    shape = tuple(int(d) for d in shape)
+    if tuple(t.shape) != shape:
+        raise ValueError(f"{name} must have shape {shape}, got {tuple(t.shape)}")
+    if t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def _scalar(t, name, n=1, dtype=torch.float32):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if t.numel() < n:
+        raise ValueError(f"{name} must hold at least {n} element(s), got {t.numel()}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def _sizes(**kw):
+    for k, v in kw.items():
+        if int(v) < 0:
+            raise ValueError(f"{k} must be >= 0, got {v}")
+        if int(v) % 16:
+            raise ValueError(f"{k} must be a multiple of 16, got {v}")
+
+
+def _on_device(*named):
+    """Every given tensor is a contiguous CUDA tensor on the current device."""
+    cur = torch.cuda.current_device() if torch.cuda.is_available() else None
+    for name, t in named:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if t.device.index != cur:
+            raise ValueError(f"{name} is on {t.device}, but the current device is cuda:{cur}; "
+                             "call inside torch.cuda.device(...) of the tensors' device")
 
 
 def _out_dtype(out):
@@ -91,28 +131,51 @@ def _out_dtype(out):
 
 # ------------------------------------------------------------ C entry points
 def fp4q_amax(x: torch.Tensor, out_amax: torch.Tensor) -> None:
-    _dev(x, "x", torch.bfloat16)
-    _dev(out_amax, "out_amax", torch.float32)
+    if x.dtype != torch.bfloat16:
+        raise ValueError(f"x must be torch.bfloat16, got {x.dtype}")
+    _scalar(out_amax, "out_amax")
+    _on_device(("x", x), ("out_amax", out_amax))
     _check("fp4q_amax", _lib.fp4q_amax(_ptr(x), x.numel(), _ptr(out_amax), _stream()))
 
 
 def fp4q_tensor_scale(amax: torch.Tensor, fmt: int, headroom: float, out_scale: torch.Tensor) -> None:
-    _dev(amax, "amax", torch.float32)
-    _dev(out_scale, "out_scale", torch.float32)
+    _scalar(amax, "amax")
+    _scalar(out_scale, "out_scale")
+    _on_device(("amax", amax), ("out_scale", out_scale))
     _check("fp4q_tensor_scale",
            _lib.fp4q_tensor_scale(_ptr(amax), fmt, headroom, _ptr(out_scale), _stream()))
 
 
 def fp4q_quantize(x, axis, fmt, tensor_scale, rnd, seed, payload_row, scales_row, payload_col,
                   scales_col, stats=None, amax=None) -> None:
-    _dev(x, "x", torch.bfloat16)
-    for n, t in (("payload_row", payload_row), ("scales_row", scales_row),
-                 ("payload_col", payload_col), ("scales_col", scales_col)):
-        _dev(t, n, torch.uint8)
-    _dev(tensor_scale, "tensor_scale", torch.float32)
-    _dev(stats, "stats", torch.int64)
-    _dev(amax, "amax", torch.float32)
+    if x.dim() != 2:
+        raise ValueError(f"x must be 2-D [rows, cols], got shape {tuple(x.shape)}")
     rows, cols = x.shape
+    _sizes(rows=rows, cols=cols)
+    u8 = torch.uint8
+    _mat(x, "x", (rows, cols), torch.bfloat16)
+    row = axis in (AXIS_ROW, AXIS_BOTH, AXIS_BOTH_2D)
+    col = axis in (AXIS_COL, AXIS_BOTH, AXIS_BOTH_2D)
+    if not (row or col):
+        raise ValueError(f"unknown axis {axis}")
+    if row:
+        _mat(payload_row, "payload_row", (rows, cols // 2), u8)
+        _mat(scales_row, "scales_row", (rows, cols // 16), u8)
+    else:
+        payload_row = scales_row = None
+    if col:
+        _mat(payload_col, "payload_col", (cols, rows // 2), u8)
+        _mat(scales_col, "scales_col", (cols, rows // 16), u8)
+    else:
+        payload_col = scales_col = None
+    _scalar(tensor_scale, "tensor_scale")
+    if stats is not None:
+        _scalar(stats, "stats", 4 * (2 if axis == AXIS_BOTH else 1), torch.int64)
+    if amax is not None:
+        _scalar(amax, "amax")
+    _on_device(("x", x), ("payload_row", payload_row), ("scales_row", scales_row),
+               ("payload_col", payload_col), ("scales_col", scales_col),
+               ("tensor_scale", tensor_scale), ("stats", stats), ("amax", amax))
     _check("fp4q_quantize", _lib.fp4q_quantize(
         _ptr(x), rows, cols, axis, fmt, _ptr(tensor_scale), rnd, ctypes.c_uint64(seed),
         _ptr(payload_row), _ptr(scales_row), _ptr(payload_col), _ptr(scales_col),
@@ -120,24 +183,38 @@ def fp4q_quantize(x, axis, fmt, tensor_scale, rnd, seed, payload_row, scales_row
 
 
 def fp4q_dequantize(payload, scales, rows, cols, fmt, tensor_scale, out) -> None:
-    _dev(payload, "payload", torch.uint8)
-    _dev(scales, "scales", torch.uint8)
-    _dev(out, "out")
-    _dev(tensor_scale, "tensor_scale", torch.float32)
+    _sizes(rows=rows, cols=cols)
+    _mat(payload, "payload", (rows, cols // 2), torch.uint8)
+    _mat(scales, "scales", (rows, cols // 16), torch.uint8)
     _out_dtype(out)
+    _mat(out, "out", (rows, cols), out.dtype)
+    _scalar(tensor_scale, "tensor_scale")
+    _on_device(("payload", payload), ("scales", scales), ("tensor_scale", tensor_scale), ("out", out))
     f32 = out.dtype == torch.float32
     _check("fp4q_dequantize", _lib.fp4q_dequantize(
         _ptr(payload), _ptr(scales), rows, cols, fmt, _ptr(tensor_scale), _ptr(out), int(f32),
         _stream()))
 
 
+def _gemm_operands(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K):
+    if M < 0 or N < 0:
+        raise ValueError(f"M and N must be >= 0, got {M}, {N}")
+    _sizes(K=K)
+    _mat(A, "A", (M, K // 2), torch.uint8)
+    _mat(A_scales, "A_scales", (M, K // 16), torch.uint8)
+    _mat(B, "B", (N, K // 2), torch.uint8)
+    _mat(B_scales, "B_scales", (N, K // 16), torch.uint8)
+    _scalar(A_tscale, "A_tscale")
+    _scalar(B_tscale, "B_tscale")
+    return [("A", A), ("A_scales", A_scales), ("A_tscale", A_tscale), ("B", B),
+            ("B_scales", B_scales), ("B_tscale", B_tscale)]
+
+
 def fp4q_gemm(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K, fmt, out) -> None:
-    for n, t in (("A", A), ("A_scales", A_scales), ("B", B), ("B_scales", B_scales)):
-        _dev(t, n, torch.uint8)
-    _dev(out, "out")
-    _dev(A_tscale, "A_tscale", torch.float32)
-    _dev(B_tscale, "B_tscale", torch.float32)
+    ops = _gemm_operands(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K)
     _out_dtype(out)
+    _mat(out, "out", (M, N), out.dtype)
+    _on_device(*ops, ("out", out))
     f32 = out.dtype == torch.float32
     _check("fp4q_gemm", _lib.fp4q_gemm(
         _ptr(A), _ptr(A_scales), _ptr(A_tscale), _ptr(B), _ptr(B_scales), _ptr(B_tscale),
@@ -146,21 +223,30 @@ def fp4q_gemm(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K, fmt, out) -
 
 def fp4q_gemm_quantize(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K, fmt, c_tscale,
                        out_bf16, out_payload, out_scales, out_amax=None) -> None:
-    for n, t in (("A", A), ("A_scales", A_scales), ("B", B), ("B_scales", B_scales),
-                 ("out_payload", out_payload), ("out_scales", out_scales)):
-        _dev(t, n, torch.uint8)
-    _dev(out_bf16, "out_bf16", torch.bfloat16)
-    _dev(c_tscale, "c_tscale", torch.float32)
-    _dev(out_amax, "out_amax", torch.float32)
+    ops = _gemm_operands(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K)
+    if N % 32:
+        raise ValueError(f"N must be a multiple of 32 for the epilogue quantisation, got {N}")
+    _mat(out_payload, "out_payload", (M, N // 2), torch.uint8)
+    _mat(out_scales, "out_scales", (M, N // 16), torch.uint8)
+    if out_bf16 is not None:
+        _mat(out_bf16, "out_bf16", (M, N), torch.bfloat16)
+    _scalar(c_tscale, "c_tscale")
+    if out_amax is not None:
+        _scalar(out_amax, "out_amax")
+    _on_device(*ops, ("c_tscale", c_tscale), ("out_bf16", out_bf16), ("out_payload", out_payload),
+               ("out_scales", out_scales), ("out_amax", out_amax))
     _check("fp4q_gemm_quantize", _lib.fp4q_gemm_quantize(
         _ptr(A), _ptr(A_scales), _ptr(A_tscale), _ptr(B), _ptr(B_scales), _ptr(B_tscale),
         M, N, K, fmt, _ptr(c_tscale), _ptr(out_bf16), _ptr(out_payload), _ptr(out_scales),
         _ptr(out_amax), _stream()))
 
 
-def fp4q_get_device_status() -> int:
+def fp4q_get_device_status(stream: torch.cuda.Stream | None = None) -> int:
+    """The latched device status, read in the order of `stream` (default: the
+    current stream); waits for that stream only."""
     v = ctypes.c_int(0)
-    _check("fp4q_get_device_status", _lib.fp4q_get_device_status(ctypes.byref(v)))
+    s = ctypes.c_void_p((stream or torch.cuda.current_stream()).cuda_stream)
+    _check("fp4q_get_device_status", _lib.fp4q_get_device_status(ctypes.byref(v), s))
     return v.value
 
 

@@ -14,7 +14,7 @@
  *  - Every pointer argument except `stream` and those documented as host
  *    pointers is a DEVICE pointer, owned by the caller; the library never
  *    allocates or frees memory, and never synchronises the stream (except
- *    fp4q_get_device_status).  Calls are asynchronous on `stream`
+ *    fp4q_get_device_status, which waits for its own stream).  Calls are asynchronous on `stream`
  *    (a cudaStream_t; NULL = the legacy default stream).
  *  - Data-dependent scalars (amax, tensor scale) stay on the device, so that a
  *    whole quantise -> GEMM sequence needs no host round trip.
@@ -169,10 +169,17 @@ fp4q_status fp4q_gemm_quantize(const uint8_t* A, const uint8_t* A_scales, const 
                                const float* c_tscale, void* out_bf16, uint8_t* out_payload,
                                uint8_t* out_scales, float* out_amax, void* stream);
 
-/* Synchronises the current device, returns the latched device status word
- * in *out (an fp4q_status value, FP4Q_OK if none) and clears it.
- * out: HOST pointer. */
-fp4q_status fp4q_get_device_status(int* out);
+/* Reads the device status word of the current device in the order of
+ * `stream` (after every call already issued on it), waits for `stream` alone
+ * (no other stream of the device is synchronised), returns the latched
+ * condition in *out (FP4Q_ERR_TIMEOUT, else FP4Q_ERR_NONFINITE, else
+ * FP4Q_OK) and clears the bits it reported (an atomic AND on the stream,
+ * waited for before returning).  The word is shared by every stream of the
+ * device: a condition latched by work on another stream is seen once that
+ * work has completed, and one latched between the read and the clear stays
+ * set for the next call.  out: HOST pointer.  Returns FP4Q_ERR_ARG for a
+ * null out, FP4Q_ERR_CUDA if a copy, launch or wait fails. */
+fp4q_status fp4q_get_device_status(int* out, void* stream);
 
 /* Static description of a status code.  Never NULL. */
 const char* fp4q_status_string(fp4q_status s);

@@ -18,7 +18,7 @@ int main(void) {
     if (fp4q_gemm(NULL, NULL, NULL, NULL, NULL, NULL, 128, 128, 96, FP4Q_SCALE_UE5M3,
                   NULL, 0, NULL) != FP4Q_ERR_SHAPE) ++fails;
     if (fp4q_amax(NULL, 16, NULL, NULL) != FP4Q_ERR_ARG) ++fails;
-    if (fp4q_get_device_status(NULL) != FP4Q_ERR_ARG) ++fails;
+    if (fp4q_get_device_status(NULL, NULL) != FP4Q_ERR_ARG) ++fails;
     printf(fails ? "FAIL %d\n" : "ok\n", fails);
     return fails != 0;
 }

@@ -13,6 +13,43 @@ from fp4_block_scaled_bf16_gb300 import workloads
 # an ulp) on top.
 GEMM_TOL = 1e-3
 
+# Elementwise bound of the FP32 result, on top of the normwise one:
+#   |C - R| <= 1e-3 |R| + K 2^-24 S,   S = (T_A T_B) sum_k |(e s)_a| |(e s)_b|,
+# K 2^-24 S being the classical bound of binary32 summation of the K exact
+# products in any order.  It scales with each element's own operands, so a
+# large error on a row of tiny magnitude (a dgrad row of a 1e-8 gradient)
+# cannot hide below the largest entries of the matrix.  Over the entries
+# where the second term is below the first (|R| > 1e3 K 2^-24 S: no heavy
+# cancellation) it is a relative error of at most 2e-3; the largest relative
+# error there is reported.
+def gemm_abs_reference(pa, sa, pb, sb, alpha, fmt=0):
+    """S = alpha |deq(A)| |deq(B)|^T from the oracle's exact e*s operands."""
+    return alpha * (np.abs(oracle.deq_es(pa, sa, fmt)) @ np.abs(oracle.deq_es(pb, sb, fmt)).T)
+
+
+def check_gemm_elementwise(C, R, S, K) -> float:
+    C = np.asarray(C, np.float64)
+    err = np.abs(C - R)
+    floor = K * 2.0 ** -24 * S
+    bad = err > GEMM_TOL * np.abs(R) + floor
+    if bad.any():
+        i = tuple(np.argwhere(bad)[0])
+        raise AssertionError(f"{int(bad.sum())} elements beyond 1e-3|R| + K 2^-24 S; first {i}: "
+                             f"C={C[i]!r} R={R[i]!r} S={S[i]!r}")
+    well = np.abs(R) > floor / GEMM_TOL
+    return float((err[well] / np.abs(R[well])).max()) if well.any() else 0.0
+
+
+def check_gemm_bf16(C16, R):
+    """The BF16 result within one BF16 ulp of R plus 1e-3 max |R|, elementwise."""
+    C16 = np.asarray(C16, np.float64)
+    bound = bf16_ulp(R) + GEMM_TOL * np.abs(R).max()
+    bad = np.abs(C16 - R) > bound
+    if bad.any():
+        i = tuple(np.argwhere(bad)[0])
+        raise AssertionError(f"{int(bad.sum())} BF16 elements beyond ulp + 1e-3 max|R|; first {i}: "
+                             f"C={C16[i]!r} R={R[i]!r}")
+
 
 def to_dev(bits: np.ndarray) -> torch.Tensor:
     return workloads.to_torch_bf16(bits).cuda()

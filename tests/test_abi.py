@@ -112,8 +112,8 @@ def test_host_validation_rejects_before_launch(lib):
     assert a(P(2), 16, ok, None) == ERR_ALIGN
     assert a(ok, 16, P(18), None) == ERR_ALIGN          # scalars: 4-byte alignment
     s = lib.fp4q_get_device_status
-    s.argtypes = [P]
-    assert s(None) == ERR_ARG
+    s.argtypes = [P, P]
+    assert s(None, None) == ERR_ARG
 
 
 def test_product_path_has_no_fallback():

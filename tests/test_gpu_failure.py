@@ -59,3 +59,18 @@ def test_nonfinite_input_is_reported(lib):
     x[3, 7] = 1.0
     lib.quantize(x, lib.AXIS_BOTH, T)
     assert lib.fp4q_get_device_status() == lib.OK
+
+
+def test_status_is_read_in_the_order_of_the_given_stream(lib):
+    # a condition latched by work on a side stream is reported by a read on
+    # that stream (which waits for that stream only), and the read clears it
+    x = torch.randn(64, 64, device="cuda").to(torch.bfloat16)
+    x[5, 9] = float("-inf")
+    out = torch.empty(1, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        lib.fp4q_amax(x, out)
+    assert lib.fp4q_get_device_status(side) == lib.ERR_NONFINITE
+    assert lib.fp4q_get_device_status(side) == lib.OK
+    assert lib.fp4q_get_device_status() == lib.OK

@@ -15,7 +15,8 @@ import torch
 
 import oracle
 from fp4_block_scaled_bf16_gb300 import workloads
-from parity_util import GEMM_TOL, bf16_ulp, gemm_error, to_dev
+from parity_util import (GEMM_TOL, check_gemm_bf16, check_gemm_elementwise, gemm_abs_reference,
+                         gemm_error, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -44,18 +45,25 @@ def run_both(lib, A, B, fmt=0):
     return C32.cpu().numpy(), C16.float().cpu().numpy()
 
 
-def full_reference(A, B, fmt=0):
+def _np_ops(A, B):
     pa, sa, ta = (t.cpu().numpy() if hasattr(t, "cpu") else t for t in A)
     pb, sb, tb = (t.cpu().numpy() if hasattr(t, "cpu") else t for t in B)
-    ta, tb = float(ta[0]), float(tb[0])
-    return oracle.gemm(pa, sa, ta, pb, sb, tb, fmt)
+    return pa, sa, float(ta[0]), pb, sb, float(tb[0])
 
 
-def assert_close(C32, C16, R):
+def full_reference(A, B, fmt=0):
+    """R (binary64 contraction) and S (the same over magnitudes)."""
+    pa, sa, ta, pb, sb, tb = _np_ops(A, B)
+    R = oracle.gemm(pa, sa, ta, pb, sb, tb, fmt)
+    return R, gemm_abs_reference(pa, sa, pb, sb, ta * tb, fmt)
+
+
+def assert_close(C32, C16, ref, K):
+    R, S = ref
     err = gemm_error(C32, R)
     assert err <= GEMM_TOL, err
-    bound = bf16_ulp(R) + GEMM_TOL * np.abs(R).max()
-    assert (np.abs(C16.astype(np.float64) - R) <= bound).all()
+    check_gemm_elementwise(C32, R, S, K)
+    check_gemm_bf16(C16, R)
     return err
 
 
@@ -71,7 +79,7 @@ def test_tiny_config(lib):
     a, b = workloads.tiny_operands(seed=0)
     A, B = quantised(a, lib), quantised(b, lib)
     C32, C16 = run_both(lib, A, B)
-    assert_close(C32, C16, full_reference(A, B))
+    assert_close(C32, C16, full_reference(A, B), 256)
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (128, 256, 128), (256, 512, 256), (100, 200, 64),
@@ -86,7 +94,7 @@ def test_shapes_and_ragged_tiles(M, N, K, lib):
     B = (B[0][:N].contiguous(), B[1][:N].contiguous(), B[2])
     C32, C16 = run_both(lib, A, B)
     assert C32.shape == (M, N)
-    assert_close(C32, C16, full_reference(A, B))
+    assert_close(C32, C16, full_reference(A, B), K)
 
 
 @pytest.mark.parametrize("fmt", [0, 1])
@@ -96,7 +104,7 @@ def test_wide_dynamic_range_and_formats(lib, fmt):
     b = rand_bits((384, 512), 6, spread=3.0)
     A, B = quantised(a, lib, rnd=1, seed=7, fmt=fmt), quantised(b, lib, fmt=fmt)
     C32, C16 = run_both(lib, A, B, fmt)
-    assert_close(C32, C16, full_reference(A, B, fmt))
+    assert_close(C32, C16, full_reference(A, B, fmt), 512)
 
 
 def test_zero_and_k0(lib):
@@ -114,16 +122,26 @@ def test_zero_and_k0(lib):
 
 def _sampled_check(lib, A, B, Cdev32, rows, cols, fmt=0):
     """Full row and column stripes of the reference via the oracle's exact
-    e*s operands and a binary64 matmul."""
+    e*s operands and a binary64 matmul: the normwise error over the stripes
+    (returned) and the elementwise bound on every entry of them."""
     pa, sa = A[0].cpu().numpy(), A[1].cpu().numpy()
     pb, sb = B[0].cpu().numpy(), B[1].cpu().numpy()
     alpha = float(A[2].item()) * float(B[2].item())
+    K = pa.shape[1] * 2
     C = Cdev32
-    R_rows = alpha * (oracle.deq_es(pa[rows], sa[rows], fmt) @ oracle.deq_es(pb, sb, fmt).T)
-    R_cols = alpha * (oracle.deq_es(pa, sa, fmt) @ oracle.deq_es(pb[cols], sb[cols], fmt).T)
+    ea_r, eb = oracle.deq_es(pa[rows], sa[rows], fmt), oracle.deq_es(pb, sb, fmt)
+    R_rows, S_rows = alpha * (ea_r @ eb.T), alpha * (np.abs(ea_r) @ np.abs(eb).T)
+    del ea_r, eb
+    ea, eb_c = oracle.deq_es(pa, sa, fmt), oracle.deq_es(pb[cols], sb[cols], fmt)
+    R_cols, S_cols = alpha * (ea @ eb_c.T), alpha * (np.abs(ea) @ np.abs(eb_c).T)
+    del ea, eb_c
+    c_rows = C[torch.from_numpy(rows).to(C.device)].cpu().numpy().astype(np.float64)
+    c_cols = C[:, torch.from_numpy(cols).to(C.device)].cpu().numpy().astype(np.float64)
+    check_gemm_elementwise(c_rows, R_rows, S_rows, K)
+    check_gemm_elementwise(c_cols, R_cols, S_cols, K)
     scale = max(np.abs(R_rows).max(), np.abs(R_cols).max())
-    e1 = np.abs(C[rows].cpu().numpy().astype(np.float64) - R_rows).max() / scale
-    e2 = np.abs(C[:, cols].cpu().numpy().astype(np.float64) - R_cols).max() / scale
+    e1 = np.abs(c_rows - R_rows).max() / scale
+    e2 = np.abs(c_cols - R_cols).max() / scale
     return max(e1, e2)
 
 

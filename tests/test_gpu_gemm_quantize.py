@@ -14,7 +14,7 @@ import torch
 
 import oracle
 from fp4_block_scaled_bf16_gb300 import workloads
-from parity_util import GEMM_TOL, gemm_error, to_dev
+from parity_util import check_gemm_bf16, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -70,7 +70,7 @@ def check(lib, A, B, T=None, fmt=0, sample=None):
         pb, sb = B[0].cpu().numpy(), B[1].cpu().numpy()
         R = oracle.gemm(pa, sa, float(A[2].item()), pb, sb, float(B[2].item()), fmt)
         C = workloads.bf16_bits_to_f32(cb).astype(np.float64)
-        assert gemm_error(C, R) <= GEMM_TOL + 2.0 ** -8
+        check_gemm_bf16(C, R)
     return q
 
 
