@@ -2,10 +2,14 @@
 
 One step = one 8B-class internal linear (in 4096 -> out 16384, 8192 tokens)
 through the whole path of "UE5M3 FP4 Block Scaling for Stable Language Model
-Pretraining" (Abstract): amax + tensor scale of X, W, dY; dual-axis block-16
-E2M1/UE5M3 quantisation of X and W (RNE) and of dY (Philox SR, seed 7); the
-three training GEMMs on the block-scaled operands (fprop Y = X W^T, dgrad
+Pretraining" (Abstract): the tensor scales of X, W, dY under periodic tensor
+scaling (refreshed every 16 steps from the amax each quantisation fuses in;
+an amax pass only on the very first step); dual-axis block-16 E2M1/UE5M3
+quantisation of X and W (RNE) and of dY (Philox SR, seed 7); the three
+training GEMMs on the block-scaled operands (fprop Y = X W^T, dgrad
 dX = dY W, wgrad dW = dY^T X), each 8192 x 16384 x 4096 multiply-adds.
+The same step under current scaling (amax pass + scale before every
+quantisation) is timed beside it.
 
 value = the three GEMMs' 2MNK flops / step time (quantisation included),
 TFLOP/s.  Per-kernel CUDA-event times give the quantiser GB/s and the GEMM
@@ -34,8 +38,9 @@ M_TOK, HID, FFN = 8192, 4096, 16384
 GEMM_FLOPS = 2.0 * M_TOK * FFN * HID          # each of fprop, dgrad, wgrad
 STEP_FLOPS = 3 * GEMM_FLOPS
 METRIC = "E2M1/UE5M3 quantize GB/s & block-scaled GEMM TFLOP/s, % of roofline"
-WORKLOAD = ("8B-class linear 4096->16384, 8192 tokens: amax+scale, dual-axis quantise X/W (RNE) "
-            "and dY (SR seed 7), fprop+dgrad+wgrad block-scaled GEMMs")
+WORKLOAD = ("8B-class linear 4096->16384, 8192 tokens: periodic tensor scales (refresh every 16 steps "
+            "from the fused amax), dual-axis quantise X/W (RNE) and dY (SR seed 7), fprop+dgrad+wgrad "
+            "block-scaled GEMMs")
 # algorithmic bytes per element: read BF16 (2) + payload 0.5 + scale 1/16 per axis
 DUAL_BYTES_PER_ELEM = 2 + 2 * (0.5 + 1 / 16)
 ROW_BYTES_PER_ELEM = 2 + 0.5 + 1 / 16
@@ -188,106 +193,10 @@ def bind_to_gpu_node(torch, index):
 
 
 # ---------------------------------------------------------------- GPU path
-class Step:
-    """Device buffers and the launch sequence of one step."""
-
-    def __init__(self, torch, fp4q, X, W, dY):
-        self.t, self.q = torch, fp4q
-        dev = X.device
-        M_TOK, HID = X.shape          # tokens, in
-        FFN = W.shape[0]              # out
-        self.dims = (M_TOK, HID, FFN)
-        u8 = dict(dtype=torch.uint8, device=dev)
-        f32 = dict(dtype=torch.float32, device=dev)
-        self.X, self.W, self.dY = X, W, dY
-        self.amax = torch.zeros(3, **f32)
-        self.T = torch.zeros(3, **f32)
-        self.Xr, self.Xrs = torch.empty((M_TOK, HID // 2), **u8), torch.empty((M_TOK, HID // 16), **u8)
-        self.Xc, self.Xcs = torch.empty((HID, M_TOK // 2), **u8), torch.empty((HID, M_TOK // 16), **u8)
-        self.Wr, self.Wrs = torch.empty((FFN, HID // 2), **u8), torch.empty((FFN, HID // 16), **u8)
-        self.Wc, self.Wcs = torch.empty((HID, FFN // 2), **u8), torch.empty((HID, FFN // 16), **u8)
-        self.Dr, self.Drs = torch.empty((M_TOK, FFN // 2), **u8), torch.empty((M_TOK, FFN // 16), **u8)
-        self.Dc, self.Dcs = torch.empty((FFN, M_TOK // 2), **u8), torch.empty((FFN, M_TOK // 16), **u8)
-        bf = dict(dtype=torch.bfloat16, device=dev)
-        self.Y = torch.empty((M_TOK, FFN), **bf)
-        self.dX = torch.empty((M_TOK, HID), **bf)
-        self.dW = torch.empty((FFN, HID), **bf)
-        self.launches = 0
-        self.side = torch.cuda.Stream(device=X.device)
-        self.side2 = torch.cuda.Stream(device=X.device)
-        self.ev_start, self.ev_xw, self.ev_side, self.ev_dq, self.ev_side2 = (torch.cuda.Event() for _ in range(5))
-
-    def run(self, ev=None):
-        q = self.q
-        M_TOK, HID, FFN = self.dims
-        T = [self.T[i:i + 1] for i in range(3)]
-        A = [self.amax[i:i + 1] for i in range(3)]
-        rec = (lambda k: ev[k].record()) if ev else (lambda k: None)
-        rec(0)
-        for i, x in enumerate((self.X, self.W, self.dY)):
-            q.fp4q_amax(x, A[i])
-            q.fp4q_tensor_scale(A[i], q.UE5M3, 1.0, T[i])
-        rec(1)
-        q.fp4q_quantize(self.X, q.AXIS_BOTH, q.UE5M3, T[0], q.RNE, 0, self.Xr, self.Xrs, self.Xc, self.Xcs)
-        rec(2)
-        q.fp4q_quantize(self.W, q.AXIS_BOTH, q.UE5M3, T[1], q.RNE, 0, self.Wr, self.Wrs, self.Wc, self.Wcs)
-        rec(3)
-        q.fp4q_quantize(self.dY, q.AXIS_BOTH, q.UE5M3, T[2], q.SR, 7, self.Dr, self.Drs, self.Dc, self.Dcs)
-        rec(4)
-        q.fp4q_gemm(self.Xr, self.Xrs, T[0], self.Wr, self.Wrs, T[1], M_TOK, FFN, HID, q.UE5M3, self.Y)
-        rec(5)
-        q.fp4q_gemm(self.Dr, self.Drs, T[2], self.Wc, self.Wcs, T[1], M_TOK, HID, FFN, q.UE5M3, self.dX)
-        rec(6)
-        q.fp4q_gemm(self.Dc, self.Dcs, T[2], self.Xc, self.Xcs, T[0], FFN, HID, M_TOK, q.UE5M3, self.dW)
-        rec(7)
-        self.launches += 12
-        return self
-
-    def run_overlapped(self):
-        """The same twelve launches on three streams.  The caller's stream
-        takes X and W (amax, tensor scale, dual-axis RNE quantisation) and
-        fprop; a side stream takes dY's amax, tensor scale and dual-axis SR
-        quantisation at the same time, then dgrad once W is quantised; a second
-        side stream runs wgrad once dY and X are quantised, so that the three
-        GEMMs' CTAs fill one another's last waves.  The caller's stream waits
-        for both side streams at the end, so a step ends when all are done and
-        the next one starts from a clean slate."""
-        q, torch = self.q, self.t
-        M_TOK, HID, FFN = self.dims
-        main = torch.cuda.current_stream()
-        T = [self.T[i:i + 1] for i in range(3)]
-        A = [self.amax[i:i + 1] for i in range(3)]
-        self.ev_start.record(main)
-        for i, x in ((0, self.X), (1, self.W)):
-            q.fp4q_amax(x, A[i])
-            q.fp4q_tensor_scale(A[i], q.UE5M3, 1.0, T[i])
-        q.fp4q_quantize(self.X, q.AXIS_BOTH, q.UE5M3, T[0], q.RNE, 0, self.Xr, self.Xrs, self.Xc, self.Xcs)
-        q.fp4q_quantize(self.W, q.AXIS_BOTH, q.UE5M3, T[1], q.RNE, 0, self.Wr, self.Wrs, self.Wc, self.Wcs)
-        self.ev_xw.record(main)
-        with torch.cuda.stream(self.side):
-            self.side.wait_event(self.ev_start)
-            q.fp4q_amax(self.dY, A[2])
-            q.fp4q_tensor_scale(A[2], q.UE5M3, 1.0, T[2])
-            q.fp4q_quantize(self.dY, q.AXIS_BOTH, q.UE5M3, T[2], q.SR, 7, self.Dr, self.Drs, self.Dc, self.Dcs)
-            self.ev_dq.record(self.side)
-            self.side.wait_event(self.ev_xw)
-            q.fp4q_gemm(self.Dr, self.Drs, T[2], self.Wc, self.Wcs, T[1], M_TOK, HID, FFN, q.UE5M3, self.dX)
-            self.ev_side.record(self.side)
-        with torch.cuda.stream(self.side2):
-            self.side2.wait_event(self.ev_dq)
-            self.side2.wait_event(self.ev_xw)
-            q.fp4q_gemm(self.Dc, self.Dcs, T[2], self.Xc, self.Xcs, T[0], FFN, HID, M_TOK, q.UE5M3, self.dW)
-            self.ev_side2.record(self.side2)
-        q.fp4q_gemm(self.Xr, self.Xrs, T[0], self.Wr, self.Wrs, T[1], M_TOK, FFN, HID, q.UE5M3, self.Y)
-        main.wait_event(self.ev_side)
-        main.wait_event(self.ev_side2)
-        self.launches += 12
-        return self
-
-
 def run_gpu(args, rank, world):
     import torch
     from fp4_block_scaled_bf16_gb300 import build, fp4q, workloads
+    from fp4_block_scaled_bf16_gb300.linear_step import LinearStep
 
     build.build()
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
@@ -303,40 +212,45 @@ def run_gpu(args, rank, world):
     hW = workloads.to_torch_bf16(Wb).pin_memory()
     hD = workloads.to_torch_bf16(dYb).pin_memory()
     X, W, dY = hX.to(dev), hW.to(dev), hD.to(dev)
-    step = Step(torch, fp4q, X, W, dY)
+    step = LinearStep(X, W, dY, seed=7)
     for _ in range(args.warmup):
+        step.run_overlapped(periodic=True)
         step.run_overlapped()
         step.run()
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
 
-    # ---- device-resident timed region: K steps as scheduled (two streams);
-    # then the same K steps launched one kernel after another on one stream
+    # ---- device-resident timed regions, K steps each: the method's step
+    # (periodic tensor scaling, three streams) -- the headline; the same step
+    # under current scaling (an amax pass before every quantisation); and the
+    # current-scaling step launched one kernel after another on one stream
     # with events between the kernels, for the per-kernel times
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
-    step.launches = 0
+
+    def timed(fn):
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for k in range(args.steps):
+            fn(k)
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
     with ClockSampler(dev.index) as clk:
-        torch.cuda.synchronize()
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record()
-        for k in range(args.steps):
-            step.run_overlapped()
-        t1.record()
-        torch.cuda.synchronize()
+        step.launches = 0
+        ms = timed(lambda k: step.run_overlapped(periodic=True))
         launches = step.launches
-        u0 = torch.cuda.Event(enable_timing=True)
-        u1 = torch.cuda.Event(enable_timing=True)
-        u0.record()
-        for k in range(args.steps):
-            step.run(evs[k])
-        u1.record()
-        torch.cuda.synchronize()
-    ms = t0.elapsed_time(t1)
-    ms_serial = u0.elapsed_time(u1)
+        refreshes = [sc.step for sc in step.scalers]
+        ms_current = timed(lambda k: step.run_overlapped())
+        ms_serial = timed(lambda k: step.run(evs[k]))
     if world > 1:
         ms = max_over_ranks(ms, dev)
+        ms_current = max_over_ranks(ms_current, dev)
     seg = lambda a, b: sum(e[a].elapsed_time(e[b]) for e in evs) / args.steps
     t_scale, t_qx, t_qw, t_qd = seg(0, 1), seg(1, 2), seg(2, 3), seg(3, 4)
     t_g = [seg(4, 5), seg(5, 6), seg(6, 7)]
@@ -349,7 +263,7 @@ def run_gpu(args, rank, world):
     hY = [torch.empty(step.Y.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     hdX = [torch.empty(step.dX.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     hdW = [torch.empty(step.dW.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    steps2 = [step, Step(torch, fp4q, torch.empty_like(X), torch.empty_like(W), torch.empty_like(dY))]
+    steps2 = [step, LinearStep(torch.empty_like(X), torch.empty_like(W), torch.empty_like(dY), seed=7)]
     s_h2d, s_cmp, s_d2h = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     e2e_steps = max(2, min(args.steps, 6))
     ev_in = [torch.cuda.Event() for _ in range(e2e_steps)]
@@ -374,7 +288,7 @@ def run_gpu(args, rank, world):
             s_cmp.wait_event(ev_in[i])
             if i >= 2:
                 s_cmp.wait_event(ev_out[i - 2])          # outputs read back
-            st_i.run_overlapped()
+            st_i.run_overlapped(periodic=True)
             ev_done[i].record(s_cmp)
         with torch.cuda.stream(s_d2h):
             s_d2h.wait_event(ev_done[i])
@@ -424,23 +338,31 @@ def run_gpu(args, rank, world):
         return b0.elapsed_time(b1) / (replays * calls)
 
     rates = {}
+    # every rate alternates two distinct inputs of the same shape (each at
+    # least as large as L2), so that no launch reads what the previous one
+    # left in L2: W and a row-reversed copy of it, dY and a row-reversed copy
+    W2 = torch.flip(step.W, dims=(0,)).contiguous()
+    dY2 = torch.flip(step.dY, dims=(0,)).contiguous()
+    rot = {id(step.W): (step.W, W2), id(step.dY): (step.dY, dY2)}
     # single-axis: W row-wise RNE and dY row-wise SR, 10 launches
     for name, x, rnd, pay, sc in (("W_row_rne", step.W, fp4q.RNE, step.Wr, step.Wrs),
                                   ("dY_row_sr", step.dY, fp4q.SR, step.Dr, step.Drs)):
         Tn = step.T[1:2] if x is step.W else step.T[2:3]
 
         def run(x=x, rnd=rnd, pay=pay, sc=sc, Tn=Tn):
-            for _ in range(10):
-                fp4q.fp4q_quantize(x, fp4q.AXIS_ROW, fp4q.UE5M3, Tn, rnd, 7, pay, sc, None, None)
+            for j in range(10):
+                fp4q.fp4q_quantize(rot[id(x)][j % 2], fp4q.AXIS_ROW, fp4q.UE5M3, Tn, rnd, 7, pay, sc, None, None)
         rates[name] = x.numel() * ROW_BYTES_PER_ELEM / (_graph_ms(run, 10) * 1e-3) / 1e9
-    # dequantisation (support op): W's row-wise payload and scales -> BF16
+    # dequantisation (support op): W's and W2's row-wise payload and scales -> BF16
     Wd = torch.empty_like(step.W)
+    q2 = fp4q.quantize(W2, fp4q.AXIS_ROW, step.T[1:2])
+    deq_in = ((step.Wr, step.Wrs), (q2.payload_row, q2.scales_row))
 
     def run_deq():
-        for _ in range(10):
-            fp4q.fp4q_dequantize(step.Wr, step.Wrs, FFN, HID, fp4q.UE5M3, step.T[1:2], Wd)
+        for j in range(10):
+            fp4q.fp4q_dequantize(*deq_in[j % 2], FFN, HID, fp4q.UE5M3, step.T[1:2], Wd)
     rates["W_dequant_bf16"] = step.W.numel() * ROW_BYTES_PER_ELEM / (_graph_ms(run_deq, 10) * 1e-3) / 1e9
-    del Wd
+    del Wd, q2, deq_in
     # 16 x 16 (transposition-invariant) scaling: both layouts from one
     # quantisation, same algorithmic bytes as the dual-axis quantisers
     for name, x, rnd, outs in (("W_2d_rne", step.W, fp4q.RNE, (step.Wr, step.Wrs, step.Wc, step.Wcs)),
@@ -448,9 +370,10 @@ def run_gpu(args, rank, world):
         Tn = step.T[1:2] if x is step.W else step.T[2:3]
 
         def run2d(x=x, rnd=rnd, outs=outs, Tn=Tn):
-            for _ in range(10):
-                fp4q.fp4q_quantize(x, fp4q.AXIS_BOTH_2D, fp4q.UE5M3, Tn, rnd, 7, *outs)
+            for j in range(10):
+                fp4q.fp4q_quantize(rot[id(x)][j % 2], fp4q.AXIS_BOTH_2D, fp4q.UE5M3, Tn, rnd, 7, *outs)
         rates[name] = x.numel() * DUAL_BYTES_PER_ELEM / (_graph_ms(run2d, 10) * 1e-3) / 1e9
+    del W2, dY2, rot
     # periodic scaling (config 4's per-step quantisation): a 4096 x 4096
     # tensor quantised row-wise (RNE) with the fused amax that the next
     # refresh uses, the tensor scale taken from an earlier step (no amax
@@ -503,11 +426,11 @@ def run_gpu(args, rank, world):
         lin = []
         for name in workloads.LINEARS:
             xb, wb, db = workloads.linear_block(name)
-            lin.append(Step(torch, fp4q, workloads.to_torch_bf16(xb).to(dev),
-                            workloads.to_torch_bf16(wb).to(dev), workloads.to_torch_bf16(db).to(dev)))
+            lin.append(LinearStep(workloads.to_torch_bf16(xb).to(dev), workloads.to_torch_bf16(wb).to(dev),
+                                  workloads.to_torch_bf16(db).to(dev), seed=7))
         for _ in range(2):
             for st_l in lin:
-                st_l.run_overlapped()
+                st_l.run_overlapped(periodic=True)
         torch.cuda.synchronize()
         nb = max(2, args.steps // 4)
         c0 = torch.cuda.Event(enable_timing=True)
@@ -515,7 +438,7 @@ def run_gpu(args, rank, world):
         c0.record()
         for _ in range(nb):
             for st_l in lin:
-                st_l.run_overlapped()
+                st_l.run_overlapped(periodic=True)
         c1.record()
         torch.cuda.synchronize()
         bms = c0.elapsed_time(c1) / nb
@@ -525,7 +448,7 @@ def run_gpu(args, rank, world):
                  "tokens": workloads.TOKENS}
         del lin
 
-    return dict(ms=ms, ms_serial=ms_serial, fused=fused, block=block, t_scale=t_scale, t_q=(t_qx, t_qw, t_qd), t_g=t_g, launches=launches, rates=rates,
+    return dict(ms=ms, ms_current=ms_current, refreshes=refreshes, ms_serial=ms_serial, fused=fused, block=block, t_scale=t_scale, t_q=(t_qx, t_qw, t_qd), t_g=t_g, launches=launches, rates=rates,
                 clocks=clk.summary(), status=status, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, link=link, affinity=affinity,
                 elems=(X.numel(), W.numel(), dY.numel()))
 
@@ -622,7 +545,11 @@ def main():
         return
     pk, src = peaks()
     hbm = _peak(pk, "hbm_gbs", "hbm_GBps", "hbm")
-    bf16 = _peak(pk, "bf16_tflops_sustained", "bf16_tflops")
+    # the per-kernel GEMM times come from the one-stream region: a burst of
+    # tens of milliseconds is held to the burst peak, a region of seconds to
+    # the sustained one
+    burst = r["ms_serial"] < 1000.0
+    bf16 = _peak(pk, "bf16_tflops", "bf16_tflops_sustained") if burst else _peak(pk, "bf16_tflops_sustained", "bf16_tflops")
     ms = r["ms"] / args.steps
     value = job_tflops(world, STEP_FLOPS, ms)
     t_gemm = sum(r["t_g"]) / 3
@@ -638,19 +565,26 @@ def main():
                "sample": f"{sample}; {spent:.1f} s of CPU time"}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms, "ms_per_step_periodic": ms,
+        "ms_per_step_current_scaling": r["ms_current"] / args.steps,
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16xf16->f32 (E2M1/UE5M3 operands, exact FP16 expansion)", "data": "synthetic",
         "config": {"workload": WORKLOAD, "M": M_TOK, "hidden": HID, "ffn": FFN,
                    "l2": "inputs larger than L2 (dY 256 MiB, step working set ~1 GiB)",
-                   "schedule": "three streams: X/W amax, scale, quantise and fprop; dY amax, scale, SR "
+                   "schedule": "three streams: X/W scale, quantise and fprop; dY scale, SR "
                                "quantise and dgrad; wgrad once dY and X are quantised",
-                   "ms_per_step_one_stream": r["ms_serial"] / args.steps,
+                   "tensor_scaling": "periodic: T refreshed every 16 steps from the amax fused into the "
+                                     "previous quantisation; amax pass on the first step only "
+                                     f"(scaler steps after the timed region: {r['refreshes']})",
+                   "current_scaling_TFLOP/s": job_tflops(world, STEP_FLOPS, r["ms_current"] / args.steps),
+                   "ms_per_step_one_stream_current_scaling": r["ms_serial"] / args.steps,
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": bf16,
                      "unit": "TFLOP/s", "frac": gemm_tflops / bf16 if bf16 else None,
                      "traffic": committed_traffic("gemm_kernel_traffic_8B_linear.json", GEMM_SOURCES),
                      "kernel": "fp4q gemm_kernel (mean of fprop/dgrad/wgrad)",
-                     "peak_source": f"{src} bf16 (sustained)"},
+                     "peak_source": f"{src} bf16 ({'burst' if burst else 'sustained'}: the per-kernel "
+                                    f"region ran {r['ms_serial']:.0f} ms)"},
         "roofline_quantize": {"bound": "hbm", "unit": "GB/s", "peak": hbm,
                               "achieved": dict({"X_dual_rne": q_gbs[0], "W_dual_rne": q_gbs[1], "dY_dual_sr": q_gbs[2]}, **r["rates"]),
                               "frac": dict({k: g / hbm for k, g in zip(("X_dual_rne", "W_dual_rne", "dY_dual_sr"), q_gbs)},

@@ -1,0 +1,101 @@
+"""Times one libfp4q.so kernel on a synthetic input: CUDA events around
+`--reps` launches on the current stream after `--warmup` launches, two
+distinct inputs alternating so that no launch reads what the previous one
+left in L2.  Prints one JSON line: milliseconds per launch and the rate in
+algorithmic bytes (quantisers: 2 B read + 0.5625 B written per element and
+axis; amax 2 B; dequantiser 0.5625 B read + 2 B written) or 2MNK flops.
+
+Small cases of this command are what the committed ncu summaries capture.
+
+  python -m fp4_block_scaled_bf16_gb300.kernel_bench --case dual_sr --rows 2048 --cols 16384
+  cases: amax, row_rne, row_sr, dual_rne, dual_sr, 2d_rne, 2d_sr, dequant, gemm (--m --n --k)
+"""
+from __future__ import annotations
+
+import argparse
+import json
+
+import torch
+
+from . import build, fp4q, workloads
+
+CASES = ("amax", "row_rne", "row_sr", "dual_rne", "dual_sr", "2d_rne", "2d_sr", "dequant", "gemm")
+
+
+def _inputs(case, rows, cols, dev):
+    gen = workloads.gradients if case.endswith("_sr") else workloads.weights
+    return [workloads.to_torch_bf16(gen(rows, cols, 50 + i)).to(dev) for i in range(2)]
+
+
+def run(case, rows=16384, cols=4096, m=8192, n=16384, k=4096, reps=10, warmup=3):
+    build.build()
+    dev = torch.device("cuda")
+    u8 = dict(dtype=torch.uint8, device=dev)
+    if case == "gemm":
+        xs = [fp4q.quantize(workloads.to_torch_bf16(workloads.activations(m, k, 60)).to(dev)),
+              fp4q.quantize(workloads.to_torch_bf16(workloads.weights(n, k, 61)).to(dev))]
+        A = (xs[0].payload_row, xs[0].scales_row, xs[0].T)
+        B = (xs[1].payload_row, xs[1].scales_row, xs[1].T)
+        out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        launch = lambda j: fp4q.fp4q_gemm(*A, *B, m, n, k, fp4q.UE5M3, out)
+        work, unit = 2.0 * m * n * k, "TFLOP/s"
+    else:
+        xs = _inputs(case, rows, cols, dev)
+        T = fp4q.tensor_scale(fp4q.amax(xs[0]))
+        pr, sr = torch.empty((rows, cols // 2), **u8), torch.empty((rows, cols // 16), **u8)
+        pc, sc = torch.empty((cols, rows // 2), **u8), torch.empty((cols, rows // 16), **u8)
+        rnd = fp4q.SR if case.endswith("_sr") else fp4q.RNE
+        unit = "GB/s"
+        if case == "amax":
+            a = torch.empty(1, dtype=torch.float32, device=dev)
+            launch = lambda j: fp4q.fp4q_amax(xs[j % 2], a)
+            work = 2.0 * rows * cols
+        elif case.startswith("row"):
+            launch = lambda j: fp4q.fp4q_quantize(xs[j % 2], fp4q.AXIS_ROW, fp4q.UE5M3, T, rnd, 7, pr, sr,
+                                                  None, None)
+            work = 2.5625 * rows * cols
+        elif case.startswith("dual") or case.startswith("2d"):
+            axis = fp4q.AXIS_BOTH if case.startswith("dual") else fp4q.AXIS_BOTH_2D
+            launch = lambda j: fp4q.fp4q_quantize(xs[j % 2], axis, fp4q.UE5M3, T, rnd, 7, pr, sr, pc, sc)
+            work = 3.125 * rows * cols
+        elif case == "dequant":
+            qs = [fp4q.quantize(x, fp4q.AXIS_ROW, T) for x in xs]
+            o = torch.empty((rows, cols), dtype=torch.bfloat16, device=dev)
+            launch = lambda j: fp4q.fp4q_dequantize(qs[j % 2].payload_row, qs[j % 2].scales_row, rows, cols,
+                                                    fp4q.UE5M3, T, o)
+            work = 2.5625 * rows * cols
+        else:
+            raise ValueError(f"unknown case {case}")
+    for j in range(warmup):
+        launch(j)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for j in range(reps):
+        launch(j)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    rate = work / (ms * 1e-3) / (1e12 if unit == "TFLOP/s" else 1e9)
+    status = fp4q.fp4q_get_device_status()
+    shape = {"m": m, "n": n, "k": k} if case == "gemm" else {"rows": rows, "cols": cols}
+    return {"case": case, **shape, "reps": reps, "ms_per_launch": ms, "rate": rate, "unit": unit,
+            "device_status": status}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--case", choices=CASES, required=True)
+    ap.add_argument("--rows", type=int, default=16384)
+    ap.add_argument("--cols", type=int, default=4096)
+    ap.add_argument("--m", type=int, default=8192)
+    ap.add_argument("--n", type=int, default=16384)
+    ap.add_argument("--k", type=int, default=4096)
+    ap.add_argument("--reps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    a = ap.parse_args()
+    print(json.dumps(run(a.case, a.rows, a.cols, a.m, a.n, a.k, a.reps, a.warmup)))
+
+
+if __name__ == "__main__":
+    main()

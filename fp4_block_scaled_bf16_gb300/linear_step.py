@@ -1,0 +1,157 @@
+"""One internal linear layer's training step on the block-scaled FP4 path of
+"UE5M3 FP4 Block Scaling for Stable Language Model Pretraining" (Abstract):
+every operand of the three training GEMMs is an E2M1 payload with UE5M3
+block-16 scales under an FP32 tensor scale, gradients rounded
+stochastically.
+
+  fprop  Y  = X W^T    X row-wise, W row-wise         (round to nearest even)
+  dgrad  dX = dY W     dY row-wise (SR), W column-wise
+  wgrad  dW = dY^T X   dY column-wise (SR), X column-wise
+
+X [tokens, in], W [out, in] and dY [tokens, out] are each quantised once on
+both axes (one read).  Two tensor-scale policies:
+  current  -- an amax pass and a tensor scale before every quantisation (the
+              TE recipe's current scaling);
+  periodic -- the method's policy: one PeriodicScaler per tensor, T refreshed
+              every `period` steps from the amax the quantiser fused into the
+              previous step's quantisation, so no amax pass runs after the
+              first step.
+
+Every launch goes through libfp4q.so; buffers are allocated once here with
+torch and reused by every step.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import fp4q as _fp4q
+from .periodic import PeriodicScaler
+
+
+class LinearStep:
+    def __init__(self, X: torch.Tensor, W: torch.Tensor, dY: torch.Tensor, seed: int = 7,
+                 period: int = 16, fmt: int = _fp4q.UE5M3, lib=None):
+        q = self.q = lib if lib is not None else _fp4q
+        tokens, hid = X.shape
+        out = W.shape[0]
+        if W.shape[1] != hid or tuple(dY.shape) != (tokens, out):
+            raise ValueError(f"shapes do not form a linear: X {tuple(X.shape)}, W {tuple(W.shape)}, "
+                             f"dY {tuple(dY.shape)}")
+        self.dims = (tokens, hid, out)
+        self.seed, self.fmt = seed, fmt
+        dev = X.device
+        u8 = dict(dtype=torch.uint8, device=dev)
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.X, self.W, self.dY = X, W, dY
+        self.amax = torch.zeros(3, **f32)
+        self.T = torch.zeros(3, **f32)
+        self.Xr, self.Xrs = torch.empty((tokens, hid // 2), **u8), torch.empty((tokens, hid // 16), **u8)
+        self.Xc, self.Xcs = torch.empty((hid, tokens // 2), **u8), torch.empty((hid, tokens // 16), **u8)
+        self.Wr, self.Wrs = torch.empty((out, hid // 2), **u8), torch.empty((out, hid // 16), **u8)
+        self.Wc, self.Wcs = torch.empty((hid, out // 2), **u8), torch.empty((hid, out // 16), **u8)
+        self.Dr, self.Drs = torch.empty((tokens, out // 2), **u8), torch.empty((tokens, out // 16), **u8)
+        self.Dc, self.Dcs = torch.empty((out, tokens // 2), **u8), torch.empty((out, tokens // 16), **u8)
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        self.Y = torch.empty((tokens, out), **bf)
+        self.dX = torch.empty((tokens, hid), **bf)
+        self.dW = torch.empty((out, hid), **bf)
+        self.scalers = [PeriodicScaler(period, fmt, device=dev, lib=q) for _ in range(3)]
+        self.launches = 0
+        self.side = torch.cuda.Stream(device=dev)
+        self.side2 = torch.cuda.Stream(device=dev)
+        self.ev_start, self.ev_xw, self.ev_side, self.ev_dq, self.ev_side2 = (torch.cuda.Event() for _ in range(5))
+
+    # ------------------------------------------------------------ pieces
+    def _scale(self, i: int, x: torch.Tensor, periodic: bool):
+        """(T, fused-amax output or None) for tensor i, launched on the current stream."""
+        q = self.q
+        if periodic:
+            sc = self.scalers[i]
+            before = sc.step % sc.period == 0
+            T = sc.scale_for(x)
+            self.launches += (2 if sc.step == 0 else 1) if before else 0
+            return T, sc.last_amax
+        T, A = self.T[i:i + 1], self.amax[i:i + 1]
+        q.fp4q_amax(x, A)
+        q.fp4q_tensor_scale(A, self.fmt, 1.0, T)
+        self.launches += 2
+        return T, None
+
+    def _quantize(self, i, x, T, amax, rnd, outs):
+        self.q.fp4q_quantize(x, self.q.AXIS_BOTH, self.fmt, T, rnd, self.seed if rnd else 0, *outs,
+                             None, amax)
+        self.launches += 1
+        if amax is not None:
+            self.scalers[i].advance()
+
+    def _gemm(self, A, B, M, N, K, out):
+        self.q.fp4q_gemm(*A, *B, M, N, K, self.fmt, out)
+        self.launches += 1
+
+    def tensor_scales(self, periodic: bool):
+        """The device T of X, W and dY that the last step used."""
+        if periodic:
+            return [sc.T for sc in self.scalers]
+        return [self.T[i:i + 1] for i in range(3)]
+
+    # ------------------------------------------------------------ steps
+    def run(self, ev=None, periodic: bool = False):
+        """The step on the current stream, one kernel after another; with
+        `ev` (eight timing events) an event is recorded before the scales,
+        before each quantisation and GEMM, and at the end."""
+        q = self.q
+        tokens, hid, out = self.dims
+        rec = (lambda k: ev[k].record()) if ev else (lambda k: None)
+        rec(0)
+        sc = [self._scale(i, x, periodic) for i, x in enumerate((self.X, self.W, self.dY))]
+        (TX, aX), (TW, aW), (TD, aD) = sc
+        rec(1)
+        self._quantize(0, self.X, TX, aX, q.RNE, (self.Xr, self.Xrs, self.Xc, self.Xcs))
+        rec(2)
+        self._quantize(1, self.W, TW, aW, q.RNE, (self.Wr, self.Wrs, self.Wc, self.Wcs))
+        rec(3)
+        self._quantize(2, self.dY, TD, aD, q.SR, (self.Dr, self.Drs, self.Dc, self.Dcs))
+        rec(4)
+        self._gemm((self.Xr, self.Xrs, TX), (self.Wr, self.Wrs, TW), tokens, out, hid, self.Y)
+        rec(5)
+        self._gemm((self.Dr, self.Drs, TD), (self.Wc, self.Wcs, TW), tokens, hid, out, self.dX)
+        rec(6)
+        self._gemm((self.Dc, self.Dcs, TD), (self.Xc, self.Xcs, TX), out, hid, tokens, self.dW)
+        rec(7)
+        return self
+
+    def run_overlapped(self, periodic: bool = False):
+        """The same launches on three streams, in the step's dependency
+        order: the caller's stream takes X and W (scales, dual-axis RNE
+        quantisation) and fprop; a side stream takes dY's scale and dual-axis
+        SR quantisation at the same time, then dgrad once W is quantised; a
+        second side stream runs wgrad once dY and X are quantised, so that the
+        three GEMMs fill one another's last waves.  The caller's stream waits
+        for both side streams at the end, so a step ends when all of its work
+        is done and the next one starts from a clean slate."""
+        q, torch_ = self.q, torch
+        tokens, hid, out = self.dims
+        main = torch_.cuda.current_stream()
+        self.ev_start.record(main)
+        TX, aX = self._scale(0, self.X, periodic)
+        TW, aW = self._scale(1, self.W, periodic)
+        self._quantize(0, self.X, TX, aX, q.RNE, (self.Xr, self.Xrs, self.Xc, self.Xcs))
+        self._quantize(1, self.W, TW, aW, q.RNE, (self.Wr, self.Wrs, self.Wc, self.Wcs))
+        self.ev_xw.record(main)
+        with torch_.cuda.stream(self.side):
+            self.side.wait_event(self.ev_start)
+            TD, aD = self._scale(2, self.dY, periodic)
+            self._quantize(2, self.dY, TD, aD, q.SR, (self.Dr, self.Drs, self.Dc, self.Dcs))
+            self.ev_dq.record(self.side)
+            self.side.wait_event(self.ev_xw)
+            self._gemm((self.Dr, self.Drs, TD), (self.Wc, self.Wcs, TW), tokens, hid, out, self.dX)
+            self.ev_side.record(self.side)
+        with torch_.cuda.stream(self.side2):
+            self.side2.wait_event(self.ev_dq)
+            self.side2.wait_event(self.ev_xw)
+            self._gemm((self.Dc, self.Dcs, TD), (self.Xc, self.Xcs, TX), out, hid, tokens, self.dW)
+            self.ev_side2.record(self.side2)
+        self._gemm((self.Xr, self.Xrs, TX), (self.Wr, self.Wrs, TW), tokens, out, hid, self.Y)
+        main.wait_event(self.ev_side)
+        main.wait_event(self.ev_side2)
+        return self

@@ -37,23 +37,38 @@ class PeriodicScaler:
         self.have_amax = False
         self.step = 0
 
-    def quantize(self, x: torch.Tensor, axis: int = _fp4q.AXIS_ROW, rnd: int = _fp4q.RNE, seed: int = 0,
-                 stats: bool = False):
-        """Quantises x with the current tensor scale (refreshed first on
-        every `period`-th call) and records its amax for the next refresh.
-        The returned T is a copy of the scale used, unaffected by later
-        refreshes."""
+    def scale_for(self, x: torch.Tensor) -> torch.Tensor:
+        """The device tensor scale for the next quantisation, refreshed first
+        when that quantisation is on a period boundary: from an explicit amax
+        pass over x on the very first call, otherwise from the amax the
+        previous quantisation left in `last_amax`.  The caller quantises with
+        the returned T, has the quantiser write its fused amax into
+        `last_amax`, then calls `advance()`.  Launches go to the current
+        stream."""
         lib = self.lib
         if self.step % self.period == 0:
             if not self.have_amax:
                 lib.fp4q_amax(x, self.last_amax)
                 self.have_amax = True
             lib.fp4q_tensor_scale(self.last_amax, self.fmt, self.headroom, self.T)
-        T = self.T.clone()
-        q = lib.quantize(x, axis, T, self.fmt, rnd, seed, stats=stats, want_amax=True)
-        self.last_amax.copy_(q.amax)
+        return self.T
+
+    def advance(self) -> None:
+        """Records that a quantisation with the current T has written its amax
+        into `last_amax`."""
         self.have_amax = True
         self.step += 1
+
+    def quantize(self, x: torch.Tensor, axis: int = _fp4q.AXIS_ROW, rnd: int = _fp4q.RNE, seed: int = 0,
+                 stats: bool = False):
+        """Quantises x with the current tensor scale (refreshed first on
+        every `period`-th call) and records its amax for the next refresh.
+        The returned T is a copy of the scale used, unaffected by later
+        refreshes."""
+        T = self.scale_for(x).clone()
+        q = self.lib.quantize(x, axis, T, self.fmt, rnd, seed, stats=stats, want_amax=True)
+        self.last_amax.copy_(q.amax)
+        self.advance()
         return q
 
     def state_dict(self) -> dict:

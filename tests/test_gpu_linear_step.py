@@ -1,0 +1,95 @@
+"""The method's own step on the GPU: one linear layer's fprop, dgrad and
+wgrad on block-scaled operands under periodic tensor scaling (the step that
+bench.py times as its headline), checked step by step against the oracle.
+
+Over 20 steps whose X, W and dY drift in magnitude (x1.3 per step, seeded
+direction), the step's tensor scales must be exactly the oracle
+PeriodicScaler's (refresh every 16 steps from the previous step's amax, an
+amax pass only on step 0), every payload and scale byte of the six
+quantised operands must equal the oracle's, and the three GEMM results must
+meet the stated tolerance on the refresh steps and the last one.
+
+Method: "UE5M3 FP4 Block Scaling for Stable Language Model Pretraining",
+Abstract (periodic tensor scaling made possible by UE5M3's range; stochastic
+rounding on backward gradients; the FP4 matrix multiplications of every
+internal linear)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp4_block_scaled_bf16_gb300 import workloads
+from parity_util import check_gemm_bf16
+
+pytestmark = pytest.mark.gpu
+
+TOK, HID, OUT, STEPS, PERIOD = 256, 256, 512, 20, 16
+
+
+def _inputs(t, amaxes):
+    """X, W, dY of step t: the generators' distributions, scaled by the
+    drift factor of the step (W drifts the other way)."""
+    def scaled(bits, f):
+        return workloads.f32_to_bf16_bits(workloads.bf16_bits_to_f32(bits) * np.float32(f))
+    X = scaled(workloads.activations(TOK, HID, 200 + t), amaxes[t])
+    W = scaled(workloads.weights(OUT, HID, 300 + t), 1.0 / amaxes[t])
+    dY = scaled(workloads.gradients(TOK, OUT, 400 + t), amaxes[t])
+    return X, W, dY
+
+
+def _u8(t):
+    return t.cpu().numpy()
+
+
+def test_periodic_step_matches_oracle_every_step():
+    from fp4_block_scaled_bf16_gb300 import build
+    build.build()
+    from fp4_block_scaled_bf16_gb300 import fp4q
+    from fp4_block_scaled_bf16_gb300.linear_step import LinearStep
+
+    dev = torch.device("cuda")
+    amaxes = workloads.drift_amaxes(STEPS)
+    X = torch.empty((TOK, HID), dtype=torch.bfloat16, device=dev)
+    W = torch.empty((OUT, HID), dtype=torch.bfloat16, device=dev)
+    dY = torch.empty((TOK, OUT), dtype=torch.bfloat16, device=dev)
+    step = LinearStep(X, W, dY, seed=7, period=PERIOD)
+    refs = [oracle.PeriodicScaler(period=PERIOD) for _ in range(3)]
+    Ts = []
+    for t in range(STEPS):
+        xb, wb, db = _inputs(t, amaxes)
+        X.copy_(workloads.to_torch_bf16(xb))
+        W.copy_(workloads.to_torch_bf16(wb))
+        dY.copy_(workloads.to_torch_bf16(db))
+        step.launches = 0
+        step.run_overlapped(periodic=True)
+        torch.cuda.synchronize()
+        # 3 dual-axis quantisations + 3 GEMMs, plus the refreshes (and the
+        # amax passes of step 0)
+        assert step.launches == 6 + (3 if t % PERIOD == 0 else 0) + (3 if t == 0 else 0), t
+        gT = [float(T.item()) for T in step.tensor_scales(periodic=True)]
+        outs = ((step.Xr, step.Xrs, step.Xc, step.Xcs), (step.Wr, step.Wrs, step.Wc, step.Wcs),
+                (step.Dr, step.Drs, step.Dc, step.Dcs))
+        for i, (bits, rnd) in enumerate(((xb, oracle.RNE), (wb, oracle.RNE), (db, oracle.SR))):
+            seed = 7 if rnd else 0
+            pr, sr, _ = refs[i].quantize(bits, oracle.ROW, rnd, seed)
+            assert gT[i] == refs[i].T, (t, i, gT[i], refs[i].T)
+            pc, sc, _ = oracle.quantize(bits, oracle.COL, refs[i].T, oracle.UE5M3, rnd, seed)
+            for name, g, w in zip(("row payload", "row scales", "col payload", "col scales"),
+                                  outs[i], (pr, sr, pc, sc)):
+                assert np.array_equal(_u8(g), w), (t, i, name)
+            # the quantiser's fused amax is the one the next refresh uses
+            assert float(step.scalers[i].last_amax.item()) == oracle.amax(bits)[0], (t, i)
+        Ts.append(gT)
+        if t % PERIOD == 0 or t == STEPS - 1:
+            for C, A, B, Ta, Tb in ((step.Y, (step.Xr, step.Xrs), (step.Wr, step.Wrs), gT[0], gT[1]),
+                                    (step.dX, (step.Dr, step.Drs), (step.Wc, step.Wcs), gT[2], gT[1]),
+                                    (step.dW, (step.Dc, step.Dcs), (step.Xc, step.Xcs), gT[2], gT[0])):
+                R = oracle.gemm(_u8(A[0]), _u8(A[1]), Ta, _u8(B[0]), _u8(B[1]), Tb)
+                Cf = C.float().cpu().numpy().astype(np.float64)
+                check_gemm_bf16(Cf, R)
+    # T held between refreshes, refreshed at steps 0 and 16
+    for t in range(1, STEPS):
+        if t % PERIOD:
+            assert Ts[t] == Ts[t - 1], t
+    assert Ts[PERIOD] != Ts[PERIOD - 1]
+    assert fp4q.fp4q_get_device_status() == fp4q.OK
