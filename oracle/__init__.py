@@ -75,7 +75,7 @@ def _load():
             "orc_e2m1_sr": (ctypes.c_uint8, [f32, u32]),
             "orc_philox4x32_10": (None, [P, P, P]),
             "orc_philox4x64_10": (None, [P, P, P]),
-            "orc_sr_word": (u32, [u64, u64, u32]),
+            "orc_sr_uniform": (u32, [u64, u64, u32]),
             "orc_amax_bf16": (f32, [P, i64, P]),
             "orc_tensor_scale": (f32, [f32, i32, f32]),
             "orc_quantize": (None, [P, i64, i64, i32, i32, f32, i32, u64, P, P, P]),
@@ -87,7 +87,7 @@ def _load():
             "orc_e2m1_rne_array": (None, [P, i64, P]),
             "orc_e2m1_sr_array": (None, [P, P, i64, P]),
             "orc_scale_encode_array": (None, [P, i64, i32, P, P]),
-            "orc_sr_word_array": (None, [u64, P, i64, u32, P]),
+            "orc_sr_uniform_array": (None, [u64, P, i64, u32, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -134,9 +134,10 @@ def e2m1_rne(q) -> np.ndarray:
     return out
 
 
-def e2m1_sr(q, rbits) -> np.ndarray:
+def e2m1_sr(q, u16) -> np.ndarray:
+    """Stochastic rounding of q with 16-bit uniform integers u16 (low 16 bits used)."""
     q = _c(np.atleast_1d(q), np.float32)
-    rb = _c(np.broadcast_to(np.asarray(rbits, np.uint32), q.shape), np.uint32)
+    rb = _c(np.broadcast_to(np.asarray(u16, np.uint32), q.shape), np.uint32)
     out = np.empty(q.shape, np.uint8)
     _load().orc_e2m1_sr_array(_ptr(q), _ptr(rb), q.size, _ptr(out))
     return out
@@ -159,10 +160,11 @@ def philox4x64_10(ctr, key) -> np.ndarray:
     return out
 
 
-def sr_words(seed: int, idx, axis: int) -> np.ndarray:
+def sr_uniforms(seed: int, idx, axis: int) -> np.ndarray:
+    """The 16-bit uniforms elements with logical indices idx draw on an axis."""
     idx = _c(np.atleast_1d(idx), np.uint64)
     out = np.empty(idx.shape, np.uint32)
-    _load().orc_sr_word_array(ctypes.c_uint64(seed), _ptr(idx), idx.size, int(axis), _ptr(out))
+    _load().orc_sr_uniform_array(ctypes.c_uint64(seed), _ptr(idx), idx.size, int(axis), _ptr(out))
     return out
 
 

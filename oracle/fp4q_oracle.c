@@ -125,9 +125,11 @@ uint8_t orc_e2m1_rne(float q) {
 
 /* E2M1 stochastic rounding.  With lo <= |q| < hi adjacent grid points and
  * p = (|q| - lo) / (hi - lo) (exact: the step is a power of two), the result
- * is hi when u < p and lo otherwise, u = (rbits >> 8) * 2^-24 uniform on
- * [0, 1).  Magnitudes at or above 6 saturate to 6. */
-uint8_t orc_e2m1_sr(float q, uint32_t rbits) {
+ * is hi when u < p and lo otherwise, u = U * 2^-16 for the 16-bit uniform
+ * integer U (the low 16 bits of the argument).  Magnitudes at or above 6
+ * saturate to 6.  Reading: the abstract fixes no random-bit width; 16 bits
+ * keep E[result] within 2^-16 of a grid step of q. */
+uint8_t orc_e2m1_sr(float q, uint32_t u16) {
     static const float grid[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
     uint8_t sign = signbit(q) ? 8 : 0;
     float a = fabsf(q);
@@ -135,7 +137,7 @@ uint8_t orc_e2m1_sr(float q, uint32_t rbits) {
     int lo = 0;
     while (lo < 7 && grid[lo + 1] <= a) lo++;
     float p = (a - grid[lo]) / (grid[lo + 1] - grid[lo]);
-    float u = (float)(rbits >> 8) * 0x1p-24f;
+    float u = (float)(u16 & 0xFFFFu) * 0x1p-16f;
     return sign | (uint8_t)(u < p ? lo + 1 : lo);
 }
 
@@ -190,19 +192,22 @@ void orc_philox4x64_10(const uint64_t ctr_in[4], const uint64_t key_in[2], uint6
     out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
 }
 
-/* The random word an element draws.  Reading (the abstract does not say how
- * random bits are assigned): key = (seed low 32, seed high 32); element
- * (r, c) of the rows x cols input has logical index i = r*cols + c; the
- * counter is (i/4 low 32, i/4 high 32, axis, 0) with axis 0 for the row-wise
- * and 1 for the column-wise quantisation; the element uses word i % 4.  The
- * draw therefore depends only on the element and the axis, never on how the
- * work is split or laid out. */
-uint32_t orc_sr_word(uint64_t seed, uint64_t i, uint32_t axis) {
-    uint32_t ctr[4] = {(uint32_t)(i >> 2), (uint32_t)(i >> 34), axis, 0u};
+/* The 16-bit uniform an element draws.  Reading (the abstract does not say
+ * how random bits are assigned): key = (seed low 32, seed high 32); element
+ * (r, c) of the rows x cols input has logical index i = r*cols + c and draws
+ * word i % 4 of the block with counter (i/4 low 32, i/4 high 32, 0, 0); the
+ * row-wise quantisation (axis 0) uses the word's low 16 bits, the
+ * column-wise one (axis 1) its high 16 bits, so that the two layouts of the
+ * same element round with independent bits from one draw.  The draw depends
+ * only on the element and the axis, never on how the work is split or laid
+ * out. */
+uint32_t orc_sr_uniform(uint64_t seed, uint64_t i, uint32_t axis) {
+    uint32_t ctr[4] = {(uint32_t)(i >> 2), (uint32_t)(i >> 34), 0u, 0u};
     uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
     uint32_t out[4];
     orc_philox4x32_10(ctr, key, out);
-    return out[i & 3];
+    uint32_t w = out[i & 3];
+    return axis == 0 ? (w & 0xFFFFu) : (w >> 16);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -246,7 +251,7 @@ enum { ST_SCALE_SAT = 0, ST_SCALE_UFLOW = 1, ST_ELEM_CLAMP = 2, ST_ELEM_FLUSH = 
 
 /* Quantise one block of 16 binary32 values v[0..15] (already widened from
  * BF16) with tensor scale T.  Writes 16 nibbles and returns the scale code.
- * rbits[j] is the random word of element j (used only for SR). */
+ * rbits[j] is the 16-bit uniform of element j (used only for SR). */
 static uint8_t quantize_block16(const float v[16], float T, int fmt, int rnd,
                                 const uint32_t rbits[16], uint8_t nib[16],
                                 uint64_t stats[4]) {
@@ -323,7 +328,7 @@ void orc_quantize_band(const uint16_t *x, int64_t row_base, int64_t rows, int64_
                 int64_t c = (axis == ORC_ROW) ? 16 * b + j : o;
                 int64_t i = (row_base + r) * cols + c;        /* logical index */
                 v[j] = bf16_to_f32(x[r * cols + c]);
-                rb[j] = (rnd == ORC_SR) ? orc_sr_word(seed, (uint64_t)i, (uint32_t)axis) : 0u;
+                rb[j] = (rnd == ORC_SR) ? orc_sr_uniform(seed, (uint64_t)i, (uint32_t)axis) : 0u;
             }
             uint8_t code = quantize_block16(v, T, fmt, rnd, rb, nib, stats);
             scales[o * (inner / 16) + b] = code;
@@ -339,8 +344,9 @@ void orc_quantize_band(const uint16_t *x, int64_t row_base, int64_t rows, int64_
  * Language Model Pretraining" (Related papers: "Stable FP4 Training via
  * Transposition-Invariant Block Quantization").  Reading: one UE5M3 scale per
  * 16 x 16 tile, chosen by the block rule above with the tile's amax, and one
- * quantisation per element with that scale (SR with the row-wise random
- * stream, axis id 0); the result is written in both layouts, so that the
+ * quantisation per element with that scale (SR with the row-wise uniform,
+ * the low 16 bits of the element's word); the result is written in both
+ * layouts, so that the
  * column-wise operand is exactly the transpose of the row-wise one.
  *   pay_row/sc_row: as axis ROW, sc_row[r, b] = code of tile (r/16, b);
  *   pay_col/sc_col: as axis COL, sc_col[c, b] = code of tile (b, c/16).
@@ -378,7 +384,7 @@ void orc_quantize_2d(const uint16_t *x, int64_t rows, int64_t cols, int fmt, flo
                     } else {
                         float q = v * r;
                         if (fabsf(q) > 6.0f) stats[ST_ELEM_CLAMP]++;
-                        n = (rnd == ORC_SR) ? orc_e2m1_sr(q, orc_sr_word(seed, (uint64_t)idx, 0u))
+                        n = (rnd == ORC_SR) ? orc_e2m1_sr(q, orc_sr_uniform(seed, (uint64_t)idx, 0u))
                                             : orc_e2m1_rne(q);
                         if (v != 0.0f && (n & 7) == 0) stats[ST_ELEM_FLUSH]++;
                     }
@@ -459,8 +465,8 @@ void orc_e2m1_rne_array(const float *q, int64_t n, uint8_t *out) {
     for (int64_t i = 0; i < n; ++i) out[i] = orc_e2m1_rne(q[i]);
 }
 
-void orc_e2m1_sr_array(const float *q, const uint32_t *rbits, int64_t n, uint8_t *out) {
-    for (int64_t i = 0; i < n; ++i) out[i] = orc_e2m1_sr(q[i], rbits[i]);
+void orc_e2m1_sr_array(const float *q, const uint32_t *u16, int64_t n, uint8_t *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_e2m1_sr(q[i], u16[i]);
 }
 
 void orc_scale_encode_array(const float *s, int64_t n, int fmt, uint8_t *out, uint8_t *sat) {
@@ -471,6 +477,6 @@ void orc_scale_encode_array(const float *s, int64_t n, int fmt, uint8_t *out, ui
     }
 }
 
-void orc_sr_word_array(uint64_t seed, const uint64_t *idx, int64_t n, uint32_t axis, uint32_t *out) {
-    for (int64_t i = 0; i < n; ++i) out[i] = orc_sr_word(seed, idx[i], axis);
+void orc_sr_uniform_array(uint64_t seed, const uint64_t *idx, int64_t n, uint32_t axis, uint32_t *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_sr_uniform(seed, idx[i], axis);
 }

@@ -7,7 +7,12 @@ against Triton's Philox4x32 run in Triton's CPU interpreter.
 
 Stochastic rounding of backward gradients ("UE5M3 FP4 Block Scaling for Stable
 Language Model Pretraining", Abstract): it must be unbiased, E[round(q)] = q.
+Reading (the abstract fixes no bit width): u = U * 2^-16 for a 16-bit uniform
+U, round up iff u < p, so E[round(q)] is within 2^-16 of a grid step of q;
+element i draws word i % 4 of Philox4x32-10 at counter (i/4, i/4 >> 32, 0, 0),
+the row-wise layout its low 16 bits, the column-wise layout its high 16 bits.
 """
+from fractions import Fraction
 import os
 import subprocess
 import sys
@@ -83,21 +88,26 @@ def test_philox4x32_matches_triton_interpreter(tmp_path):
         assert list(oracle.philox4x32_10(ctr[j], key)) == list(want[j]), j
 
 
-def test_sr_word_counter_map():
-    # element i draws word i % 4 of Philox((i/4, i/4 >> 32, axis, 0), seed)
+def test_sr_uniform_counter_map():
+    # element i: word i % 4 of Philox((i/4, i/4 >> 32, 0, 0), seed); the
+    # row-wise layout takes its low 16 bits, the column-wise its high 16
     seed = 0xDEADBEEF_00000007
     idx = np.array([0, 1, 2, 3, 4, 7, 2**33 + 5, 2**40 + 2], np.uint64)
     key = np.array([seed & 0xFFFFFFFF, seed >> 32], np.uint32)
-    for axis in (0, 1):
-        got = oracle.sr_words(seed, idx, axis)
-        for i, g in zip(idx, got):
-            i = int(i)
-            blk = oracle.philox4x32_10([(i >> 2) & 0xFFFFFFFF, i >> 34, axis, 0], key)
-            assert int(g) == int(blk[i & 3])
-    # the two axes draw different streams
-    a0 = oracle.sr_words(seed, np.arange(4096, dtype=np.uint64), 0)
-    a1 = oracle.sr_words(seed, np.arange(4096, dtype=np.uint64), 1)
-    assert (a0 != a1).mean() > 0.999
+    got0, got1 = oracle.sr_uniforms(seed, idx, 0), oracle.sr_uniforms(seed, idx, 1)
+    for i, g0, g1 in zip(idx, got0, got1):
+        i = int(i)
+        w = int(oracle.philox4x32_10([(i >> 2) & 0xFFFFFFFF, i >> 34, 0, 0], key)[i & 3])
+        assert int(g0) == w & 0xFFFF and int(g1) == w >> 16
+    # the two halves behave as independent uniforms: uncorrelated, each uniform
+    n = 1 << 18
+    a0 = oracle.sr_uniforms(seed, np.arange(n, dtype=np.uint64), 0).astype(np.float64)
+    a1 = oracle.sr_uniforms(seed, np.arange(n, dtype=np.uint64), 1).astype(np.float64)
+    assert a0.max() < 2 ** 16 and a1.max() < 2 ** 16
+    assert abs(np.corrcoef(a0, a1)[0, 1]) < 5 / np.sqrt(n)
+    for a in (a0, a1):
+        h = np.bincount((a.astype(np.int64) >> 12), minlength=16)
+        assert (np.abs(h - n / 16) < 6 * np.sqrt(n / 16)).all()
 
 
 E2M1 = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
@@ -114,8 +124,8 @@ def _decode(n):
 def test_sr_is_unbiased_over_1e6_draws(q):
     n = 1_000_000
     rng = np.random.default_rng(abs(int(q * 1000)) + 17)
-    rbits = rng.integers(0, 2**32, n, dtype=np.uint64).astype(np.uint32)
-    out = _decode(oracle.e2m1_sr(np.full(n, q, np.float32), rbits))
+    u16 = rng.integers(0, 2**16, n, dtype=np.uint64).astype(np.uint32)
+    out = _decode(oracle.e2m1_sr(np.full(n, q, np.float32), u16))
     a = abs(float(np.float32(q)))
     lo = E2M1[E2M1 <= a].max()
     hi = E2M1[E2M1 > a].min()
@@ -129,25 +139,51 @@ def test_sr_unbiased_with_the_philox_stream():
     # same check, drawing the bits through the oracle's own counter map
     n = 1_000_000
     q = np.float32(2.7)
-    rbits = oracle.sr_words(7, np.arange(n, dtype=np.uint64), 0)
-    out = _decode(oracle.e2m1_sr(np.full(n, q, np.float32), rbits))
-    p = (2.7 - 2.0) / 1.0
-    assert abs(out.mean() - float(q)) < 5 * np.sqrt(p * (1 - p) / n)
+    for axis in (0, 1):
+        u16 = oracle.sr_uniforms(7, np.arange(n, dtype=np.uint64), axis)
+        out = _decode(oracle.e2m1_sr(np.full(n, q, np.float32), u16))
+        p = (float(q) - 2.0) / 1.0
+        assert abs(out.mean() - float(q)) < 5 * np.sqrt(p * (1 - p) / n)
+
+
+@pytest.mark.parametrize("q", [0.0001, 0.1, 0.25, 0.3000001, 0.49999997, 0.5000001, 0.7, 0.99999994,
+                               1.00000012, 1.2, 1.4999999, 1.75, 2.0000002, 2.6, 3.9999998, 4.5,
+                               5.0, 5.9999995, -0.3, -4.2])
+def test_sr_rounds_up_for_exactly_the_uniforms_below_p(q):
+    # every one of the 2^16 uniforms: the ones that round up are exactly those
+    # with U * 2^-16 < p, p the exact (rational) position of |q| between its
+    # grid neighbours -- so P(up) = ceil(p 2^16) / 2^16, within 2^-16 of p
+    qf = np.float32(q)
+    a = abs(Fraction(float(qf)))
+    grid = [Fraction(g) for g in (0, 0.5, 1, 1.5, 2, 3, 4, 6)]
+    lo = max(g for g in grid if g <= a)
+    hi = min(g for g in grid if g > a)
+    p = (a - lo) / (hi - lo)
+    U = np.arange(2 ** 16, dtype=np.uint32)
+    out = oracle.e2m1_sr(np.full(U.size, qf, np.float32), U)
+    mag = E2M1[out & 7]
+    up = mag == float(hi)
+    assert ((mag == float(lo)) | up).all()
+    want = np.array([Fraction(int(u), 2 ** 16) < p for u in range(2 ** 16)])
+    assert np.array_equal(up, want)
+    assert (out >> 3 == (1 if q < 0 else 0)).all()
 
 
 def test_sr_edges():
     grid = np.float32([0, 0.5, 1, 1.5, 2, 3, 4, 6])
-    for rb in (0, 1, 2**31, 0xFFFFFFFF):
-        # on-grid values never move, whatever the random word
-        assert list(oracle.e2m1_sr(grid, np.uint32(rb))) == list(range(8))
+    for u in (0, 1, 2**15, 0xFFFF):
+        # on-grid values never move, whatever the uniform
+        assert list(oracle.e2m1_sr(grid, np.uint32(u))) == list(range(8))
         # at or above 6 saturates
-        assert int(oracle.e2m1_sr(np.float32([7.5]), np.uint32(rb))[0]) == 7
-    # u = 0 rounds up whenever p > 0; u = 1 - 2^-24 rounds up only if p > u
+        assert int(oracle.e2m1_sr(np.float32([7.5]), np.uint32(u))[0]) == 7
+    # U = 0 rounds up whenever p > 0; U = 2^16 - 1 only when p > 1 - 2^-16
     assert int(oracle.e2m1_sr(np.float32([0.0001]), np.uint32(0))[0]) == 1
-    assert int(oracle.e2m1_sr(np.float32([0.4999]), np.uint32(0xFFFFFFFF))[0]) == 0
-    # the decision uses only the top 24 bits of the word
-    assert int(oracle.e2m1_sr(np.float32([0.25]), np.uint32(0x7FFFFFFF))[0]) == 1
-    assert int(oracle.e2m1_sr(np.float32([0.25]), np.uint32(0x80000000))[0]) == 0
-    assert int(oracle.e2m1_sr(np.float32([0.25]), np.uint32(0x800000FF))[0]) == 0
+    assert int(oracle.e2m1_sr(np.float32([0.4999]), np.uint32(0xFFFF))[0]) == 0
+    assert int(oracle.e2m1_sr(np.float32([0.49999997]), np.uint32(0xFFFF))[0]) == 1
+    # only the low 16 bits of the argument are the uniform
+    assert int(oracle.e2m1_sr(np.float32([0.25]), np.uint32(0x7FFF))[0]) == 1
+    assert int(oracle.e2m1_sr(np.float32([0.25]), np.uint32(0x8000))[0]) == 0
+    assert int(oracle.e2m1_sr(np.float32([0.25]), np.uint32(0xFFFF7FFF))[0]) == 1
+    assert int(oracle.e2m1_sr(np.float32([0.25]), np.uint32(0x00018000))[0]) == 0
     # negative values round their magnitude and keep the sign
-    assert int(oracle.e2m1_sr(np.float32([-0.0001]), np.uint32(0xFFFFFFFF))[0]) == 8
+    assert int(oracle.e2m1_sr(np.float32([-0.0001]), np.uint32(0xFFFF))[0]) == 8
