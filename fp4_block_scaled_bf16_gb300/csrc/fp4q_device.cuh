@@ -84,27 +84,28 @@ __device__ __forceinline__ uint32_t cvt_e2m1x8(const float q[8]) {
   return out;
 }
 
-// Stochastic rounding of a magnitude a >= 0 onto the E2M1 grid, given the
-// random word w: with lo <= a < hi neighbouring grid points and
-// p = (a - lo) / (hi - lo), the result is hi iff U = (w >> 8) satisfies
-// U * 2^-24 < p.  For a >= 1 the grid points are exactly the binary32 values
-// with one mantissa bit: p * 2^24 is four times the 22 dropped mantissa bits
-// (rest), and U < 4 rest <=> rest > U / 4 <=> adding the complement of U / 4
-// to the dropped bits carries into the kept bit -- so one add and one mask
-// round the pattern (a carry into the exponent is the step to the next
-// binade).  Below 1 the grid is uniform (step 1/2).  Results at or above 6
-// are saturated by the caller's conversion.
-__device__ __forceinline__ float sr_round_mag(float a, uint32_t w) {
-  if (a >= 1.0f) {
-    const uint32_t b = __float_as_uint(a) + ((~w >> 10) & 0x3FFFFFu);
-    return __uint_as_float(b & 0xFFC00000u);
-  }
-  const uint32_t U = w >> 8;
-  const float t = __fmul_rn(a, 2.0f);
-  const float fl = floorf(t);
-  const float p = __fsub_rn(t, fl);
-  const float u = __fmul_rn(__uint2float_rn(U), 0x1p-24f);
-  return __fmul_rn(__fadd_rn(fl, (u < p) ? 1.0f : 0.0f), 0.5f);
+// Stochastic rounding with a 16-bit uniform U (u = U * 2^-16, round up iff
+// u < p, p the position of the magnitude between its grid neighbours).  On
+// [1, 8) the E2M1 grid points are the binary32 values with one mantissa bit:
+// p * 2^16 = D / 64 for the 22 dropped mantissa bits D, and
+//   U < ceil(D / 64)  <=>  D + ((2^16 - 1 - U) << 6 | 63) carries into bit 22,
+// so one integer add of that addend and one mask round the pattern (a carry
+// into the exponent is the step to the next binade; results of 8 saturate in
+// the caller's conversion).  Below 1 the grid is uniform with step 1/2, the
+// same as on [1, 2): adding 1 rounded upward maps a onto [1, 2] keeping the
+// fraction that decides (ceil at 2^-22, which leaves ceil(p * 2^16)
+// unchanged), and subtracting 1 afterwards is exact.
+// The addend of the uniform in the low (HI = false) or high half of the word.
+template <bool HI>
+__device__ __forceinline__ uint32_t sr_addend(uint32_t w) {
+  return HI ? ((((~w) >> 10) & 0x3FFFC0u) | 0x3Fu) : ((((~w) << 6) & 0x3FFFC0u) | 0x3Fu);
+}
+__device__ __forceinline__ float sr_round_mag(float a, uint32_t addend) {
+  float c;   // 1.0 below 1, else 0.0
+  asm("set.lt.f32.f32 %0, %1, 0f3F800000;" : "=f"(c) : "f"(a));
+  const float z = __fadd_ru(a, c);
+  const float zr = __uint_as_float((__float_as_uint(z) + addend) & 0xFFC00000u);
+  return __fsub_rn(zr, c);
 }
 
 // ---------------------------------------------------------------- Philox4x32-10
@@ -122,10 +123,11 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
   return c;
 }
 
-// The four random words of counter block ctr (= element index / 4) on the
-// given axis (0 row-wise, 1 column-wise).
-__device__ __forceinline__ uint4 sr_words4(uint64_t ctr, uint32_t axis, uint64_t seed) {
-  return philox4x32_10(make_uint4((uint32_t)ctr, (uint32_t)(ctr >> 32), axis, 0u),
+// The four random words of counter block ctr (= element index / 4): word j
+// belongs to element 4 ctr + j; the row-wise layout rounds with its low 16
+// bits, the column-wise layout with its high 16 bits.
+__device__ __forceinline__ uint4 sr_words4(uint64_t ctr, uint64_t seed) {
+  return philox4x32_10(make_uint4((uint32_t)ctr, (uint32_t)(ctr >> 32), 0u, 0u),
                        (uint32_t)seed, (uint32_t)(seed >> 32));
 }
 
@@ -253,10 +255,10 @@ __device__ __forceinline__ uint32_t quantize8(const uint32_t w[4], float r, cons
 #pragma unroll
     for (int j = 0; j < 8; ++j) *clamped += (fabsf(q[j]) > 6.0f) ? 1u : 0u;
   }
-  if (SR) {
+  if (SR) {   // row-wise: the uniforms are the low halves of the words
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const float m = sr_round_mag(fabsf(q[j]), rb[j]);
+      const float m = sr_round_mag(fabsf(q[j]), sr_addend<false>(rb[j]));
       q[j] = __uint_as_float(__float_as_uint(m) | (__float_as_uint(q[j]) & 0x80000000u));
     }
   }

@@ -132,8 +132,8 @@ __global__ void __launch_bounds__(kRowThreads, 2) quantize_row_kernel(
       const BlockScale bs = block_scale<STATS>(m, tab, kr);
       uint32_t rb[8];
       if (SR) {
-        const uint4 a = sr_words4((uint64_t)g * 2, 0u, seed);
-        const uint4 b = sr_words4((uint64_t)g * 2 + 1, 0u, seed);
+        const uint4 a = sr_words4((uint64_t)g * 2, seed);
+        const uint4 b = sr_words4((uint64_t)g * 2 + 1, seed);
         rb[0] = a.x; rb[1] = a.y; rb[2] = a.z; rb[3] = a.w;
         rb[4] = b.x; rb[5] = b.y; rb[6] = b.z; rb[7] = b.w;
       }
@@ -472,10 +472,13 @@ __global__ void __launch_bounds__(kRcThreads, 2) quantize_tile_kernel(
 // contiguous bytes per column.  The block-scale reciprocals come from a
 // per-CTA table.
 
-// Stochastic rounding of the pair (q0, q1) with random words w0, w1 -> one
+// Stochastic rounding of the pair (q0, q1) with the uniforms in the low
+// (HI = false, row-wise) or high halves of the random words w0, w1 -> one
 // byte of two E2M1 nibbles (q0 low).
+template <bool HI>
 __device__ __forceinline__ uint32_t sr_e2m1x2(float q0, float q1, uint32_t w0, uint32_t w1) {
-  const float m0 = sr_round_mag(fabsf(q0), w0), m1 = sr_round_mag(fabsf(q1), w1);
+  const float m0 = sr_round_mag(fabsf(q0), sr_addend<HI>(w0));
+  const float m1 = sr_round_mag(fabsf(q1), sr_addend<HI>(w1));
   return e2m1x2(__uint_as_float(__float_as_uint(m0) | (__float_as_uint(q0) & 0x80000000u)),
                 __uint_as_float(__float_as_uint(m1) | (__float_as_uint(q1) & 0x80000000u)));
 }
@@ -615,18 +618,16 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile4_kernel(
         re = __shfl_sync(0xFFFFFFFFu, rown[p >> 1], grp + ((2 * p) & 3));
         ro = __shfl_sync(0xFFFFFFFFu, rown[p >> 1], grp + ((2 * p + 1) & 3));
       }
-      const uint4 ra = sr_words4((uint64_t)ea, 0u, seed), rb = sr_words4((uint64_t)eb, 0u, seed);
+    }
+    // one Philox block per row and four elements serves both layouts: the
+    // row-wise rounding takes the low halves of the words, the column-wise
+    // the high halves (16 x 16 scaling: one quantisation, the low halves)
+    {
+      const uint4 ra = sr_words4((uint64_t)ea, seed), rb = sr_words4((uint64_t)eb, seed);
       wra[0] = ra.x; wra[1] = ra.y; wra[2] = ra.z; wra[3] = ra.w;
       wrb[0] = rb.x; wrb[1] = rb.y; wrb[2] = rb.z; wrb[3] = rb.w;
-    }
-    if (TWO_D) {
-      // one quantisation per element: the column layout repeats the row words
 #pragma unroll
       for (int k = 0; k < 4; ++k) { wca[k] = wra[k]; wcb[k] = wrb[k]; }
-    } else {
-      const uint4 ca = sr_words4((uint64_t)ea, 1u, seed), cb = sr_words4((uint64_t)eb, 1u, seed);
-      wca[0] = ca.x; wca[1] = ca.y; wca[2] = ca.z; wca[3] = ca.w;
-      wcb[0] = cb.x; wcb[1] = cb.y; wcb[2] = cb.z; wcb[3] = cb.w;
     }
     uint32_t rowa = 0u, rowb = 0u;
 #pragma unroll
@@ -637,8 +638,8 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile4_kernel(
         float x0, x1, y0, y1;
         mul2f(a0, a1, re, x0, x1);
         mul2f(b0, b1, ro, y0, y1);
-        const uint32_t ba = sr_e2m1x2(x0, x1, wra[2 * q], wra[2 * q + 1]);
-        const uint32_t bb = sr_e2m1x2(y0, y1, wrb[2 * q], wrb[2 * q + 1]);
+        const uint32_t ba = sr_e2m1x2<false>(x0, x1, wra[2 * q], wra[2 * q + 1]);
+        const uint32_t bb = sr_e2m1x2<false>(y0, y1, wrb[2 * q], wrb[2 * q + 1]);
         rowa |= ba << (8 * q);
         rowb |= bb << (8 * q);
         if (STATS && ok) {
@@ -649,8 +650,8 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile4_kernel(
       // columns 2q (elements a0, b0) and 2q + 1 (a1, b1), rows 2p, 2p + 1
       const float y0 = __fmul_rn(a0, rc[2 * q]), y1 = __fmul_rn(b0, rc[2 * q]);
       const float z0 = __fmul_rn(a1, rc[2 * q + 1]), z1 = __fmul_rn(b1, rc[2 * q + 1]);
-      const uint32_t by = sr_e2m1x2(y0, y1, wca[2 * q], wcb[2 * q]);
-      const uint32_t bz = sr_e2m1x2(z0, z1, wca[2 * q + 1], wcb[2 * q + 1]);
+      const uint32_t by = sr_e2m1x2<!TWO_D>(y0, y1, wca[2 * q], wcb[2 * q]);
+      const uint32_t bz = sr_e2m1x2<!TWO_D>(z0, z1, wca[2 * q + 1], wcb[2 * q + 1]);
       uint32_t& py = (p < 4) ? pcol[2 * q].x : pcol[2 * q].y;
       uint32_t& pz = (p < 4) ? pcol[2 * q + 1].x : pcol[2 * q + 1].y;
       py = put_byte(py, by, p & 3);
