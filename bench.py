@@ -56,7 +56,7 @@ def kernel_sources_sha(files):
     return h.hexdigest()[:16]
 
 
-GEMM_SOURCES = ["gemm.cu", "fp4q_device.cuh", "fp4q_pipeline.cuh"]
+GEMM_SOURCES = ["gemm.cu", "fp4q_device.cuh", "fp4q_pipeline.cuh", "fp4q_tcgen05.cuh"]
 
 
 def committed_traffic(name, sources):

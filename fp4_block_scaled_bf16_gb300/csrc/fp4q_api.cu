@@ -242,6 +242,47 @@ fp4q_status fp4q_gemm_quantize(const uint8_t* A, const uint8_t* A_scales, const 
                      c_tscale, out_payload, out_scales, out_amax, stream);
 }
 
+fp4q_status fp4q_gemm_nvfp4(const uint8_t* A, const uint8_t* A_scales, const float* A_tscale,
+                            const uint8_t* B, const uint8_t* B_scales, const float* B_tscale, int64_t M,
+                            int64_t N, int64_t K, void* out, int out_is_f32, void* stream) {
+  FP4Q_RANGE("fp4q_gemm_nvfp4");
+  if (M < 0 || N < 0 || K < 0 || K % 256 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
+    return FP4Q_ERR_SHAPE;
+  if ((M + 127) / 128 > 65535) return FP4Q_ERR_SHAPE;   // 128-row tiles on the grid's y dimension
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (M == 0 || N == 0) return FP4Q_OK;
+  if (!out) return FP4Q_ERR_ARG;
+  if (!aligned16(out)) return FP4Q_ERR_ALIGN;
+  if (K == 0) return from_cuda(cudaMemsetAsync(out, 0, (size_t)M * N * (out_is_f32 ? 4 : 2), st));
+  if (!A || !A_scales || !A_tscale || !B || !B_scales || !B_tscale) return FP4Q_ERR_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(A_scales) || !aligned16(B_scales) ||
+      !aligned4(A_tscale) || !aligned4(B_tscale))
+    return FP4Q_ERR_ALIGN;
+  int* status = status_ptr();
+  if (!status) return FP4Q_ERR_CUDA;
+  fp4q::GemmArgs a;
+  a.A = A;
+  a.As = A_scales;
+  a.B = B;
+  a.Bs = B_scales;
+  a.TA = A_tscale;
+  a.TB = B_tscale;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.fmt = FP4Q_SCALE_UE4M3;
+  a.out = out;
+  a.out_f32 = out_is_f32 != 0;
+  a.status = status;
+  a.wait_cycles = 4000000000LL;   // about 2 s per wait, as fp4q_gemm
+  a.skip_loads = false;
+  if (const char* e = getenv("FP4Q_TEST_GEMM_WAIT_CYCLES")) {
+    const long long v = atoll(e);
+    if (v > 0) a.wait_cycles = v;
+  }
+  return from_cuda(fp4q::launch_gemm_nvfp4(a, st));
+}
+
 fp4q_status fp4q_get_device_status(int* out, void* stream) {
   FP4Q_RANGE("fp4q_get_device_status");
   if (!out) return FP4Q_ERR_ARG;

@@ -26,7 +26,7 @@ UE5M3, UE4M3 = 0, 1
 
 # every symbol include/fp4q.h declares
 EXPORTS = ("fp4q_amax", "fp4q_tensor_scale", "fp4q_quantize", "fp4q_dequantize", "fp4q_gemm",
-           "fp4q_gemm_quantize", "fp4q_get_device_status", "fp4q_status_string")
+           "fp4q_gemm_quantize", "fp4q_gemm_nvfp4", "fp4q_get_device_status", "fp4q_status_string")
 
 
 class Fp4qError(RuntimeError):
@@ -49,6 +49,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fp4q_dequantize.argtypes = [P, P, i64, i64, i32, P, P, i32, P]
     lib.fp4q_gemm.argtypes = [P, P, P, P, P, P, i64, i64, i64, i32, P, i32, P]
     lib.fp4q_gemm_quantize.argtypes = [P, P, P, P, P, P, i64, i64, i64, i32, P, P, P, P, P, P]
+    lib.fp4q_gemm_nvfp4.argtypes = [P, P, P, P, P, P, i64, i64, i64, P, i32, P]
     lib.fp4q_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), P]
     lib.fp4q_status_string.argtypes = [i32]
     lib.fp4q_status_string.restype = ctypes.c_char_p
@@ -221,6 +222,18 @@ def fp4q_gemm(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K, fmt, out) -
         M, N, K, fmt, _ptr(out), int(f32), _stream()))
 
 
+def fp4q_gemm_nvfp4(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K, out) -> None:
+    """Native NVFP4 GEMM: UE4M3-scaled operands on the block-scaled MMA."""
+    ops = _gemm_operands(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K)
+    _out_dtype(out)
+    _mat(out, "out", (M, N), out.dtype)
+    _on_device(*ops, ("out", out))
+    f32 = out.dtype == torch.float32
+    _check("fp4q_gemm_nvfp4", _lib.fp4q_gemm_nvfp4(
+        _ptr(A), _ptr(A_scales), _ptr(A_tscale), _ptr(B), _ptr(B_scales), _ptr(B_tscale),
+        M, N, K, _ptr(out), int(f32), _stream()))
+
+
 def fp4q_gemm_quantize(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K, fmt, c_tscale,
                        out_bf16, out_payload, out_scales, out_amax=None) -> None:
     ops = _gemm_operands(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K)
@@ -316,6 +329,16 @@ def dequantize(payload, scales, T, fmt: int = UE5M3, dtype=torch.bfloat16) -> to
     R, C = payload.shape[0], payload.shape[1] * 2
     out = torch.empty((R, C), dtype=dtype, device=payload.device)
     fp4q_dequantize(payload, scales, R, C, fmt, T, out)
+    return out
+
+
+def gemm_nvfp4(A, A_scales, A_tscale, B, B_scales, B_tscale, dtype=torch.bfloat16, out=None) -> torch.Tensor:
+    """C = (T_A T_B) deq(A) deq(B)^T on the native block-scaled MMA (UE4M3 scales)."""
+    M, K = A.shape[0], A.shape[1] * 2
+    N = B.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=dtype, device=A.device)
+    fp4q_gemm_nvfp4(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K, out)
     return out
 
 

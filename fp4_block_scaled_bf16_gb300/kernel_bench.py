@@ -8,7 +8,8 @@ axis; amax 2 B; dequantiser 0.5625 B read + 2 B written) or 2MNK flops.
 Small cases of this command are what the committed ncu summaries capture.
 
   python -m fp4_block_scaled_bf16_gb300.kernel_bench --case dual_sr --rows 2048 --cols 16384
-  cases: amax, row_rne, row_sr, dual_rne, dual_sr, 2d_rne, 2d_sr, dequant, gemm (--m --n --k)
+  cases: amax, row_rne, row_sr, dual_rne, dual_sr, 2d_rne, 2d_sr, dequant, gemm and gemm_nvfp4
+  (--m --n --k; gemm_nvfp4 on UE4M3-scaled operands)
 """
 from __future__ import annotations
 
@@ -19,7 +20,7 @@ import torch
 
 from . import build, fp4q, workloads
 
-CASES = ("amax", "row_rne", "row_sr", "dual_rne", "dual_sr", "2d_rne", "2d_sr", "dequant", "gemm")
+CASES = ("amax", "row_rne", "row_sr", "dual_rne", "dual_sr", "2d_rne", "2d_sr", "dequant", "gemm", "gemm_nvfp4")
 
 
 def _inputs(case, rows, cols, dev):
@@ -31,13 +32,17 @@ def run(case, rows=16384, cols=4096, m=8192, n=16384, k=4096, reps=10, warmup=3)
     build.build()
     dev = torch.device("cuda")
     u8 = dict(dtype=torch.uint8, device=dev)
-    if case == "gemm":
-        xs = [fp4q.quantize(workloads.to_torch_bf16(workloads.activations(m, k, 60)).to(dev)),
-              fp4q.quantize(workloads.to_torch_bf16(workloads.weights(n, k, 61)).to(dev))]
+    if case in ("gemm", "gemm_nvfp4"):
+        fmt = fp4q.UE5M3 if case == "gemm" else fp4q.UE4M3
+        xs = [fp4q.quantize(workloads.to_torch_bf16(workloads.activations(m, k, 60)).to(dev), fmt=fmt),
+              fp4q.quantize(workloads.to_torch_bf16(workloads.weights(n, k, 61)).to(dev), fmt=fmt)]
         A = (xs[0].payload_row, xs[0].scales_row, xs[0].T)
         B = (xs[1].payload_row, xs[1].scales_row, xs[1].T)
         out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
-        launch = lambda j: fp4q.fp4q_gemm(*A, *B, m, n, k, fp4q.UE5M3, out)
+        if case == "gemm":
+            launch = lambda j: fp4q.fp4q_gemm(*A, *B, m, n, k, fmt, out)
+        else:
+            launch = lambda j: fp4q.fp4q_gemm_nvfp4(*A, *B, m, n, k, out)
         work, unit = 2.0 * m * n * k, "TFLOP/s"
     else:
         xs = _inputs(case, rows, cols, dev)
@@ -78,7 +83,7 @@ def run(case, rows=16384, cols=4096, m=8192, n=16384, k=4096, reps=10, warmup=3)
     ms = e0.elapsed_time(e1) / reps
     rate = work / (ms * 1e-3) / (1e12 if unit == "TFLOP/s" else 1e9)
     status = fp4q.fp4q_get_device_status()
-    shape = {"m": m, "n": n, "k": k} if case == "gemm" else {"rows": rows, "cols": cols}
+    shape = {"m": m, "n": n, "k": k} if case.startswith("gemm") else {"rows": rows, "cols": cols}
     return {"case": case, **shape, "reps": reps, "ms_per_launch": ms, "rate": rate, "unit": unit,
             "device_status": status}
 

@@ -169,6 +169,22 @@ fp4q_status fp4q_gemm_quantize(const uint8_t* A, const uint8_t* A_scales, const 
                                const float* c_tscale, void* out_bf16, uint8_t* out_payload,
                                uint8_t* out_scales, float* out_amax, void* stream);
 
+/* Native NVFP4 GEMM: the same contraction as fp4q_gemm on operands whose
+ * block scales are UE4M3 (the NVFP4 format of the TE recipe the method is
+ * compared against, and of the abstract's native-NVFP4 execution ablation),
+ * multiplied by the tensor cores' own block-scaled MMA -- no software
+ * expansion:
+ *   C[m, n] = (T_A * T_B) * sum_k (e s)_A[m, k] * (e s)_B[n, k]
+ * A: payload [M, K/2] + UE4M3 scales [M, K/16]; B: [N, K/2] + [N, K/16]
+ * (fp4q_quantize with FP4Q_SCALE_UE4M3 writes exactly this layout);
+ * A_tscale, B_tscale device floats.  Binary32 accumulation; out [M, N] BF16
+ * (out_is_f32 == 0) or binary32.  M, N >= 0 (M at most 65535 * 128), K a
+ * multiple of 256 (K = 0 writes zeros); FP4Q_ERR_SHAPE otherwise.  Waits are
+ * bounded as in fp4q_gemm (FP4Q_TEST_GEMM_WAIT_CYCLES shortens them). */
+fp4q_status fp4q_gemm_nvfp4(const uint8_t* A, const uint8_t* A_scales, const float* A_tscale,
+                            const uint8_t* B, const uint8_t* B_scales, const float* B_tscale,
+                            int64_t M, int64_t N, int64_t K, void* out, int out_is_f32, void* stream);
+
 /* Reads the device status word of the current device in the order of
  * `stream` (after every call already issued on it), waits for `stream` alone
  * (no other stream of the device is synchronised), returns the latched
