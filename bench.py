@@ -448,7 +448,45 @@ def run_gpu(args, rank, world):
                  "tokens": workloads.TOKENS}
         del lin
 
-    return dict(ms=ms, ms_current=ms_current, refreshes=refreshes, ms_serial=ms_serial, fused=fused, block=block, t_scale=t_scale, t_q=(t_qx, t_qw, t_qd), t_g=t_g, launches=launches, rates=rates,
+    # ---- the native NVFP4 path on the same shapes: UE4M3-scaled operands,
+    # the three GEMMs on the tensor cores' block-scaled MMA; the step as
+    # scheduled (periodic scaling, three streams) and per-kernel times (one
+    # stream), then the four-linear block
+    nstep = LinearStep(step.X, step.W, step.dY, seed=7, fmt=fp4q.UE4M3, native=True)
+    for _ in range(args.warmup):
+        nstep.run_overlapped(periodic=True)
+        nstep.run(periodic=True)
+    evn = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
+    ms_native = timed(lambda k: nstep.run_overlapped(periodic=True))
+    timed(lambda k: nstep.run(evn[k], periodic=True))
+    segn = lambda a, b: sum(e[a].elapsed_time(e[b]) for e in evn) / args.steps
+    native = {"ms_per_step": ms_native / args.steps, "gemm_ms": [segn(4, 5), segn(5, 6), segn(6, 7)],
+              "quantize_ms": [segn(1, 2), segn(2, 3), segn(3, 4)]}
+    del nstep
+    if block is not None:
+        lin = []
+        for name in workloads.LINEARS:
+            xb, wb, db = workloads.linear_block(name)
+            lin.append(LinearStep(workloads.to_torch_bf16(xb).to(dev), workloads.to_torch_bf16(wb).to(dev),
+                                  workloads.to_torch_bf16(db).to(dev), seed=7, fmt=fp4q.UE4M3, native=True))
+        for _ in range(2):
+            for st_l in lin:
+                st_l.run_overlapped(periodic=True)
+        torch.cuda.synchronize()
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        c0.record()
+        for _ in range(block["steps"]):
+            for st_l in lin:
+                st_l.run_overlapped(periodic=True)
+        c1.record()
+        torch.cuda.synchronize()
+        bms = c0.elapsed_time(c1) / block["steps"]
+        native["block_ms_per_step"] = bms
+        native["block_TFLOP/s"] = block["TFLOP/s"] * block["ms_per_block_step"] / bms
+        del lin
+
+    return dict(ms=ms, ms_current=ms_current, refreshes=refreshes, ms_serial=ms_serial, native=native, fused=fused, block=block, t_scale=t_scale, t_q=(t_qx, t_qw, t_qd), t_g=t_g, launches=launches, rates=rates,
                 clocks=clk.summary(), status=status, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, link=link, affinity=affinity,
                 elems=(X.numel(), W.numel(), dY.numel()))
 
@@ -489,6 +527,28 @@ def oracle_sample(qrows=512, grows=2, gcols=4096):
               f"{macs} MACs in {t_g:.2f} s, single thread; scaled to the full step "
               f"({step_elems} elements quantised on two axes, {STEP_FLOPS / 2:.3e} MACs)")
     return est, t_q + t_g, sample
+
+
+# dense FP4 against dense BF16 tensor throughput on GB300 (13.5 / 2.25 PFLOP/s nominal)
+FP4_OVER_BF16 = 6.0
+
+
+def native_line(nat, world, bf16_peak, src):
+    """The native NVFP4 path's numbers: the whole step (UE4M3 quantisation and
+    three block-scaled-MMA GEMMs), the GEMMs against the FP4 peak derived
+    from the measured BF16 one by the nominal dense ratio."""
+    g = GEMM_FLOPS / (sum(nat["gemm_ms"]) / 3 * 1e-3) / 1e12
+    peak = bf16_peak * FP4_OVER_BF16 if bf16_peak else None
+    out = {"ms_per_step": nat["ms_per_step"], "TFLOP/s": job_tflops(world, STEP_FLOPS, nat["ms_per_step"]),
+           "gemm_ms": nat["gemm_ms"], "quantize_ms_one_stream": nat["quantize_ms"],
+           "roofline": {"bound": "tensor", "achieved": g, "peak": peak, "unit": "TFLOP/s",
+                        "frac": g / peak if peak else None,
+                        "kernel": "fp4q gemm_nvfp4_kernel (mean of fprop/dgrad/wgrad)",
+                        "peak_source": f"{src} bf16 x {FP4_OVER_BF16:g} (nominal dense fp4 / bf16)"}}
+    if "block_ms_per_step" in nat:
+        out["linear_block_ms_per_step"] = nat["block_ms_per_step"]
+        out["linear_block_TFLOP/s"] = nat["block_TFLOP/s"]
+    return out
 
 
 def main():
@@ -597,6 +657,7 @@ def main():
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e_ms"],
                 "host_link_gbs": {k: round(v, 1) for k, v in r["link"].items()},
                 "cpu_affinity": r["affinity"]},
+        "native_nvfp4": native_line(r["native"], world, bf16, src),
         "fused_epilogue_fprop": r["fused"],
         "linear_block_fwd_bwd": r["block"],
         "gpu_launches": r["launches"],

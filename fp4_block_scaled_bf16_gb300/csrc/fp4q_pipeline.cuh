@@ -53,6 +53,12 @@ __device__ __forceinline__ void tma_store_commit_and_wait_read() {
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Budget of the waits that drain a CTA's own asynchronous work (issued loads,
+// committed MMAs) before it exits: fixed and generous (about 2 s), never the
+// shortened budget of a test hook, since that work always completes unless
+// the hardware has failed.
+constexpr long long kDrainCycles = 4000000000LL;
+
 // Bounded wait: true once the phase with `parity` has completed, false after
 // `budget` clock64 cycles.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, long long budget) {

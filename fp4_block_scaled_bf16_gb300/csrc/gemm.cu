@@ -266,12 +266,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < S_RAW; ++s) {
         if (last_kb < s) continue;
         const int kb = s + (last_kb - s) / S_RAW * S_RAW;
-        drained &= mbar_wait_bounded(bar_raw_full + 8 * s, (kb / S_RAW) & 1, budget);
+        drained &= mbar_wait_bounded(bar_raw_full + 8 * s, (kb / S_RAW) & 1, kDrainCycles);
       }
       for (int cs = 0; TMA_CODES && cs < S_CODE; ++cs) {
         if (last_g < cs) continue;
         const int g = cs + (last_g - cs) / S_CODE * S_CODE;
-        drained &= mbar_wait_bounded(bar_code_full + 8 * cs, (g / S_CODE) & 1, budget);
+        drained &= mbar_wait_bounded(bar_code_full + 8 * cs, (g / S_CODE) & 1, kDrainCycles);
       }
       if (!drained) atomicOr(status, kStatusTimeout);
     }
@@ -301,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // above has finished reading shared memory and writing TMEM, which must
       // happen before TMEM is freed and the CTA exits (bounded, whatever the
       // abort flag says).
-      if (!mbar_wait_bounded(bar_acc, 0, budget)) atomicOr(status, kStatusTimeout);
+      if (!mbar_wait_bounded(bar_acc, 0, kDrainCycles)) atomicOr(status, kStatusTimeout);
     }
   } else {
     // ------------------------------------------------ expansion warps

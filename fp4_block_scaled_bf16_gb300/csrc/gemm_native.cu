@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < S; ++s) {
         if (last_kb < s) continue;
         const int kb = s + (last_kb - s) / S * S;
-        drained &= mbar_wait_bounded(bar_full + 8 * s, (kb / S) & 1, budget);
+        drained &= mbar_wait_bounded(bar_full + 8 * s, (kb / S) & 1, kDrainCycles);
       }
       if (!drained) atomicOr(status, kStatusTimeout);
     }
@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(bar_acc);
       // Drain, also after an abort: every MMA issued above completes before
       // TMEM is freed.
-      if (!mbar_wait_bounded(bar_acc, 0, budget)) atomicOr(status, kStatusTimeout);
+      if (!mbar_wait_bounded(bar_acc, 0, kDrainCycles)) atomicOr(status, kStatusTimeout);
     }
   } else {
     if (warp < kSfWarps) {

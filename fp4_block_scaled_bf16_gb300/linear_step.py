@@ -17,6 +17,11 @@ both axes (one read).  Two tensor-scale policies:
               previous step's quantisation, so no amax pass runs after the
               first step.
 
+With `native=True` the operands carry UE4M3 scales and the three GEMMs run
+on the tensor cores' block-scaled MMA (fp4q_gemm_nvfp4) -- the native NVFP4
+execution the page ablates against; otherwise the GEMMs are the emulated
+block-scaled ones (fp4q_gemm) for the chosen scale format.
+
 Every launch goes through libfp4q.so; buffers are allocated once here with
 torch and reused by every step.
 """
@@ -30,8 +35,11 @@ from .periodic import PeriodicScaler
 
 class LinearStep:
     def __init__(self, X: torch.Tensor, W: torch.Tensor, dY: torch.Tensor, seed: int = 7,
-                 period: int = 16, fmt: int = _fp4q.UE5M3, lib=None):
+                 period: int = 16, fmt: int = _fp4q.UE5M3, native: bool = False, lib=None):
         q = self.q = lib if lib is not None else _fp4q
+        if native and fmt != q.UE4M3:
+            raise ValueError("the native block-scaled MMA takes UE4M3 scales (fmt=UE4M3)")
+        self.native = native
         tokens, hid = X.shape
         out = W.shape[0]
         if W.shape[1] != hid or tuple(dY.shape) != (tokens, out):
@@ -85,7 +93,10 @@ class LinearStep:
             self.scalers[i].advance()
 
     def _gemm(self, A, B, M, N, K, out):
-        self.q.fp4q_gemm(*A, *B, M, N, K, self.fmt, out)
+        if self.native:
+            self.q.fp4q_gemm_nvfp4(*A, *B, M, N, K, out)
+        else:
+            self.q.fp4q_gemm(*A, *B, M, N, K, self.fmt, out)
         self.launches += 1
 
     def tensor_scales(self, periodic: bool):

@@ -93,3 +93,45 @@ def test_periodic_step_matches_oracle_every_step():
             assert Ts[t] == Ts[t - 1], t
     assert Ts[PERIOD] != Ts[PERIOD - 1]
     assert fp4q.fp4q_get_device_status() == fp4q.OK
+
+
+def test_native_nvfp4_step_matches_oracle():
+    """The same step with UE4M3 scales and the three GEMMs on the native
+    block-scaled MMA: tensor scales and every quantised byte equal the
+    oracle's, GEMM results within the BF16 bound, over the first refresh."""
+    from fp4_block_scaled_bf16_gb300 import build
+    build.build()
+    from fp4_block_scaled_bf16_gb300 import fp4q
+    from fp4_block_scaled_bf16_gb300.linear_step import LinearStep
+
+    steps, period = 3, 2
+    amaxes = workloads.drift_amaxes(steps)
+    dev = torch.device("cuda")
+    X = torch.empty((TOK, HID), dtype=torch.bfloat16, device=dev)
+    W = torch.empty((OUT, HID), dtype=torch.bfloat16, device=dev)
+    dY = torch.empty((TOK, OUT), dtype=torch.bfloat16, device=dev)
+    step = LinearStep(X, W, dY, seed=7, period=period, fmt=fp4q.UE4M3, native=True)
+    refs = [oracle.PeriodicScaler(period=period, fmt=oracle.UE4M3) for _ in range(3)]
+    for t in range(steps):
+        xb, wb, db = _inputs(t, amaxes)
+        X.copy_(workloads.to_torch_bf16(xb))
+        W.copy_(workloads.to_torch_bf16(wb))
+        dY.copy_(workloads.to_torch_bf16(db))
+        step.run_overlapped(periodic=True)
+        torch.cuda.synchronize()
+        gT = [float(T.item()) for T in step.tensor_scales(periodic=True)]
+        outs = ((step.Xr, step.Xrs, step.Xc, step.Xcs), (step.Wr, step.Wrs, step.Wc, step.Wcs),
+                (step.Dr, step.Drs, step.Dc, step.Dcs))
+        for i, (bits, rnd) in enumerate(((xb, oracle.RNE), (wb, oracle.RNE), (db, oracle.SR))):
+            seed = 7 if rnd else 0
+            pr, sr, _ = refs[i].quantize(bits, oracle.ROW, rnd, seed)
+            assert gT[i] == refs[i].T, (t, i)
+            pc, sc, _ = oracle.quantize(bits, oracle.COL, refs[i].T, oracle.UE4M3, rnd, seed)
+            for g, w in zip(outs[i], (pr, sr, pc, sc)):
+                assert np.array_equal(_u8(g), w), (t, i)
+        for C, A, B, Ta, Tb in ((step.Y, (step.Xr, step.Xrs), (step.Wr, step.Wrs), gT[0], gT[1]),
+                                (step.dX, (step.Dr, step.Drs), (step.Wc, step.Wcs), gT[2], gT[1]),
+                                (step.dW, (step.Dc, step.Dcs), (step.Xc, step.Xcs), gT[2], gT[0])):
+            R = oracle.gemm(_u8(A[0]), _u8(A[1]), Ta, _u8(B[0]), _u8(B[1]), Tb, oracle.UE4M3)
+            check_gemm_bf16(C.float().cpu().numpy().astype(np.float64), R)
+    assert fp4q.fp4q_get_device_status() == fp4q.OK
