@@ -189,6 +189,17 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int q) {
   return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
 }
 
+// max(|a|, |b|) of two BF16 pairs lane by lane, on the FP16/BF16 pipe (one
+// instruction instead of a sign mask and an integer max on the ALU): the
+// magnitudes are exact, a NaN input propagates (so that the non-finite flag
+// still sees it), and the sign bits of the result are the XOR of the inputs'
+// -- callers mask them off once, after accumulating.
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 // Places bits 0..7 of b into byte k of acc.
 __device__ __forceinline__ uint32_t put_byte(uint32_t acc, uint32_t b, int k) {
   return __byte_perm(acc, b, k == 0 ? 0x3214 : k == 1 ? 0x3240 : k == 2 ? 0x3410 : 0x4210);
@@ -223,13 +234,18 @@ __device__ __forceinline__ int stage_word(int c, int g) { return 32 * c + (g ^ (
 __device__ __forceinline__ void write_col_stage(const ColStage& st, int64_t R, int64_t C, int64_t tr,
                                                 int64_t tc, uint8_t* __restrict__ pay_col,
                                                 uint8_t* __restrict__ sc_col) {
+  // thread t writes piece t & 7 of columns t / 8 + 32 i, i < 4: one base
+  // pointer, advanced by 32 column rows of R / 2 bytes
+  const int c_t = (int)threadIdx.x >> 3, piece = (int)threadIdx.x & 7;
+  uint8_t* dst = pay_col + (tc + c_t) * (R / 2) + tr / 2 + 8 * piece;
+  const int64_t step = 32 * (R / 2);
+  const bool rows_in = tr + 16 * piece < R;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int k = threadIdx.x + kRcThreads * i;
-    const int c = k >> 3, piece = k & 7;
-    if (tc + c < C && tr + 16 * piece < R) {
+  for (int i = 0; i < 4; ++i, dst += step) {
+    const int c = c_t + 32 * i;
+    if (rows_in && tc + c < C) {
       const uint2 w = *reinterpret_cast<const uint2*>(&st.pay[stage_word(c, 2 * piece)]);
-      *reinterpret_cast<uint2*>(pay_col + (tc + c) * (R / 2) + tr / 2 + 8 * piece) = w;
+      *reinterpret_cast<uint2*>(dst) = w;
     }
   }
   if (threadIdx.x < 128) {
@@ -272,16 +288,18 @@ __device__ __forceinline__ void rne_piece(const uint4 (&v)[8], int64_t R, int64_
     uint32_t rm[2];
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-      uint32_t mw[4];
+      uint32_t w[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        mw[q] = word_of(v[2 * p + k], q) & 0x7FFF7FFFu;
-        cmx[q] = __vmaxu2(cmx[q], mw[q]);
+        w[q] = word_of(v[2 * p + k], q);
+        cmx[q] = absmax_bf16x2(cmx[q], w[q]);
       }
-      rm[k] = __vmaxu2(__vmaxu2(mw[0], mw[1]), __vmaxu2(mw[2], mw[3]));
+      rm[k] = absmax_bf16x2(absmax_bf16x2(w[0], w[1]), absmax_bf16x2(w[2], w[3]));
     }
-    rpx[p] = __vmaxu2(__byte_perm(rm[0], rm[1], 0x5410), __byte_perm(rm[0], rm[1], 0x7632));
+    rpx[p] = absmax_bf16x2(__byte_perm(rm[0], rm[1], 0x5410), __byte_perm(rm[0], rm[1], 0x7632)) & 0x7FFF7FFFu;
   }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) cmx[q] &= 0x7FFF7FFFu;
   const uint32_t tm = __vmaxu2(__vmaxu2(cmx[0], cmx[1]), __vmaxu2(cmx[2], cmx[3]));
   cnt.tmax = max(cnt.tmax, max(tm & 0xFFFFu, tm >> 16));
 
@@ -322,15 +340,20 @@ __device__ __forceinline__ void rne_piece(const uint4 (&v)[8], int64_t R, int64_
     }
   }
 
-  // ---- conversion, one row pair at a time
+  // ---- conversion, one row pair at a time.  Row outputs through base
+  // pointers advanced by two rows per pair: payload words of rows r0 + 2p
+  // (+ 1) at prow, scale code of row r0 + 2p + par at srow.
   const uint32_t rpick = par ? 0x4432u : 0x4410u;
   uint32_t pcol[8];
+  uint32_t* prow = pay_row + ((r0 * C + c0) >> 3);
+  uint8_t* srow = sc_row + (((r0 + par) * C + (c0 & ~(int64_t)15)) >> 4);
+  const int64_t pstep = C >> 3, sstep = C >> 3;   // one row of payload words; two rows of codes
 #pragma unroll
   for (int p = 0; p < 4; ++p) {
     float re = 0.0f, ro = 0.0f;   // row reciprocals of rows 2p and 2p + 1
     if (DO_ROW && TWO_D) {
       re = ro = ts.r;
-      if (ok) sc_row[((r0 + 2 * p + par) * C + (c0 & ~(int64_t)15)) >> 4] = (uint8_t)ts.code;
+      if (ok) srow[p * sstep] = (uint8_t)ts.code;
     } else if (DO_ROW) {
       const uint32_t full = __vmaxu2(rpx[p], __shfl_xor_sync(0xFFFFFFFFu, rpx[p], 1));
       const uint32_t m = __byte_perm(full, 0u, rpick);          // row 2p + par
@@ -339,7 +362,7 @@ __device__ __forceinline__ void rne_piece(const uint4 (&v)[8], int64_t R, int64_
       re = par ? other : bs.r;
       ro = par ? bs.r : other;
       if (ok) {
-        sc_row[((r0 + 2 * p + par) * C + (c0 & ~(int64_t)15)) >> 4] = (uint8_t)bs.code;
+        srow[p * sstep] = (uint8_t)bs.code;
         if (STATS) {
           cnt.r_sat += bs.sat ? 1u : 0u;
           cnt.r_uflow += (m != 0u && bs.code == 0u) ? 1u : 0u;
@@ -370,8 +393,8 @@ __device__ __forceinline__ void rne_piece(const uint4 (&v)[8], int64_t R, int64_
     if (DO_ROW) {
       const uint32_t ne = cvt_e2m1x8(xe), no = cvt_e2m1x8(xo);
       if (ok) {
-        st_stream_u32(pay_row + (((r0 + 2 * p) * C + c0) >> 3), ne);
-        st_stream_u32(pay_row + (((r0 + 2 * p + 1) * C + c0) >> 3), no);
+        st_stream_u32(prow + (2 * p) * pstep, ne);
+        st_stream_u32(prow + (2 * p + 1) * pstep, no);
         if (STATS) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -401,44 +424,62 @@ __global__ void __launch_bounds__(kRcThreads, 2) quantize_tile_kernel(
   __shared__ ColStage stage[2];   // double-buffered: one barrier per tile
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int half = lane >> 4, cg = lane & 15, par = cg & 1;
-  const int64_t tiles_x = (C + kRcCols - 1) / kRcCols;
-  const int64_t ntiles = tiles_x * ((R + kRcRows - 1) / kRcRows);
+  // tile counts fit in 32 bits (the ABI rejects more than 2^31 - 1 tiles)
+  const uint32_t tiles_x = (uint32_t)((C + kRcCols - 1) / kRcCols);
+  const uint32_t ntiles = tiles_x * (uint32_t)((R + kRcRows - 1) / kRcRows);
   TileCounts cnt;
-  // piece coordinates of tile `tile`; sizes are multiples of 16, so a 16 x 16
-  // region is wholly inside or outside
-  auto coords = [&](int64_t tile, int64_t& rb, int64_t& r0, int64_t& c0) {
-    rb = (tile / tiles_x) * kRcRows + warp * 16;
+  // Tile coordinates walk with the grid stride: one 32-bit division per CTA
+  // for the first tile and the stride, then a carry per step (a 64-bit
+  // division per tile would cost more than a piece's conversion).
+  const uint32_t stride = gridDim.x;
+  const uint32_t dy = stride / tiles_x, dx = stride - dy * tiles_x;
+  auto advance = [&](uint32_t& ty, uint32_t& tx) {
+    tx += dx;
+    ty += dy;
+    if (tx >= tiles_x) { tx -= tiles_x; ++ty; }
+  };
+  // piece coordinates of tile (ty, tx); sizes are multiples of 16, so a
+  // 16 x 16 region is wholly inside or outside
+  auto coords = [&](uint32_t ty, uint32_t tx, int64_t& rb, int64_t& r0, int64_t& c0) {
+    rb = (int64_t)ty * kRcRows + warp * 16;
     r0 = rb + 8 * half;
-    c0 = (tile % tiles_x) * kRcCols + cg * 8;
-    return tile < ntiles && rb < R && c0 < C;
+    c0 = (int64_t)tx * kRcCols + cg * 8;
+    return rb < R && c0 < C;
   };
   auto load = [&](uint4 (&v)[8], int64_t r0, int64_t c0, bool ok) {
+    const uint16_t* src = in + r0 * C + c0;
 #pragma unroll
     for (int rr = 0; rr < 8; ++rr)
-      v[rr] = ok ? ld_stream_v4(in + (r0 + rr) * C + c0) : make_uint4(0, 0, 0, 0);
+      v[rr] = ok ? ld_stream_v4(src + rr * C) : make_uint4(0, 0, 0, 0);
   };
   uint4 va[8], vb[8];
-  int64_t tile = blockIdx.x, rb, r0, c0;
-  bool ok = coords(tile, rb, r0, c0);
+  uint32_t tile = blockIdx.x;
+  uint32_t ty = tile / tiles_x, tx = tile - ty * tiles_x;   // tile being converted (buffer a)
+  int64_t rb, r0, c0;
+  bool ok = tile < ntiles && coords(ty, tx, rb, r0, c0);
   load(va, r0, c0, ok);
   build_scale_tab(&tab, __ldg(tscale), fmt);   // while the first piece is in flight
-  const int64_t stride = gridDim.x;
   // two tiles per trip, so that the two register buffers swap roles without copies
-  auto flush_tile = [&](const ColStage& st, int64_t tl) {
+  auto flush_tile = [&](const ColStage& st, uint32_t fy, uint32_t fx) {
     __syncthreads();
-    write_col_stage(st, R, C, (tl / tiles_x) * kRcRows, (tl % tiles_x) * kRcCols, pay_col, sc_col);
+    write_col_stage(st, R, C, (int64_t)fy * kRcRows, (int64_t)fx * kRcCols, pay_col, sc_col);
   };
   for (; tile < ntiles; tile += 2 * stride) {
+    uint32_t ty1 = ty, tx1 = tx;
+    advance(ty1, tx1);
     int64_t rb1, r01, c01;
-    const bool ok1 = coords(tile + stride, rb1, r01, c01);
+    const bool ok1 = tile + stride < ntiles && coords(ty1, tx1, rb1, r01, c01);
     load(vb, r01, c01, ok1);
     rne_piece<STATS, DO_ROW, TWO_D>(va, R, C, rb, r0, c0, ok, half, par, tab, pay_row, sc_row, stage[0], warp, cg, cnt);
-    flush_tile(stage[0], tile);
+    flush_tile(stage[0], ty, tx);
     if (tile + stride >= ntiles) break;
-    ok = coords(tile + 2 * stride, rb, r0, c0);
+    ty = ty1;
+    tx = tx1;
+    advance(ty, tx);
+    ok = tile + 2 * stride < ntiles && coords(ty, tx, rb, r0, c0);
     load(va, r0, c0, ok);
     rne_piece<STATS, DO_ROW, TWO_D>(vb, R, C, rb1, r01, c01, ok1, half, par, tab, pay_row, sc_row, stage[1], warp, cg, cnt);
-    flush_tile(stage[1], tile + stride);
+    flush_tile(stage[1], ty1, tx1);
   }
   if (STATS) {
     if (DO_ROW) flush_stats(stats, cnt.r_sat, cnt.r_uflow, cnt.r_clamp, cnt.r_flush);
@@ -498,10 +539,10 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile4_kernel(
   const int own = lane & 3;                                         // rows r with r % 4 == own
   // one CTA per tile, tiles numbered row-major (a 1-D grid: no 65535 limit
   // on the number of tile rows)
-  const int64_t tiles_x = (C + kRcCols - 1) / kRcCols;
-  const int64_t ty = (int64_t)blockIdx.x / tiles_x, tx = (int64_t)blockIdx.x % tiles_x;
-  const int64_t r0 = ty * kRcRows + warp * 16;
-  const int64_t c0 = tx * kRcCols + lane * 4;
+  const uint32_t tiles_x = (uint32_t)((C + kRcCols - 1) / kRcCols);   // tile counts fit in 32 bits
+  const uint32_t ty = blockIdx.x / tiles_x, tx = blockIdx.x - ty * tiles_x;
+  const int64_t r0 = (int64_t)ty * kRcRows + warp * 16;
+  const int64_t c0 = (int64_t)tx * kRcCols + lane * 4;
   // sizes are multiples of 16, so a 16-column block is either wholly inside
   // or wholly outside, and so is each 16 x 4 piece
   const bool ok = r0 < R && c0 < C;
@@ -509,11 +550,12 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile4_kernel(
   uint32_t c_sat = 0, c_uflow = 0, c_clamp = 0, c_flush = 0;
 
   uint2 v[16];
+  const uint16_t* src = in + r0 * C + c0;
 #pragma unroll
   for (int rr = 0; rr < 16; ++rr) {
     if (ok) {
       asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
-                   : "=r"(v[rr].x), "=r"(v[rr].y) : "l"(in + (r0 + rr) * C + c0));
+                   : "=r"(v[rr].x), "=r"(v[rr].y) : "l"(src + rr * C));
     } else {
       v[rr] = make_uint2(0, 0);
     }
@@ -529,13 +571,15 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile4_kernel(
     uint32_t rm[2];
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-      const uint32_t a = v[2 * i + k].x & 0x7FFF7FFFu, b = v[2 * i + k].y & 0x7FFF7FFFu;
-      cmx0 = __vmaxu2(cmx0, a);
-      cmx1 = __vmaxu2(cmx1, b);
-      rm[k] = __vmaxu2(a, b);
+      const uint32_t a = v[2 * i + k].x, b = v[2 * i + k].y;
+      cmx0 = absmax_bf16x2(cmx0, a);
+      cmx1 = absmax_bf16x2(cmx1, b);
+      rm[k] = absmax_bf16x2(a, b);
     }
-    rpx[i] = __vmaxu2(__byte_perm(rm[0], rm[1], 0x5410), __byte_perm(rm[0], rm[1], 0x7632));
+    rpx[i] = absmax_bf16x2(__byte_perm(rm[0], rm[1], 0x5410), __byte_perm(rm[0], rm[1], 0x7632)) & 0x7FFF7FFFu;
   }
+  cmx0 &= 0x7FFF7FFFu;
+  cmx1 &= 0x7FFF7FFFu;
   uint32_t tmax = __vmaxu2(cmx0, cmx1);
   tmax = max(tmax & 0xFFFFu, tmax >> 16);
 
@@ -573,11 +617,14 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile4_kernel(
   }
 
   // ---- row scales: this lane computes rows own, own + 4, own + 8, own + 12
+  // (codes through a base pointer advanced by four rows)
   float rown[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  uint8_t* srow = sc_row + (((r0 + own) * C + (c0 & ~(int64_t)15)) >> 4);
+  const int64_t sstep = C >> 2;
   if (DO_ROW && TWO_D) {
 #pragma unroll
     for (int k = 0; k < 4; ++k)
-      if (ok) sc_row[((r0 + 4 * k + own) * C + (c0 & ~(int64_t)15)) >> 4] = (uint8_t)ts.code;
+      if (ok) srow[k * sstep] = (uint8_t)ts.code;
   } else if (DO_ROW) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -593,7 +640,7 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile4_kernel(
       const BlockScale bs = block_scale<STATS>(m, tab, kr);
       rown[k] = bs.r;
       if (ok) {
-        sc_row[((r0 + 4 * k + own) * C + (c0 & ~(int64_t)15)) >> 4] = (uint8_t)bs.code;
+        srow[k * sstep] = (uint8_t)bs.code;
         if (STATS) {
           r_sat += bs.sat ? 1u : 0u;
           r_uflow += (m != 0u && bs.code == 0u) ? 1u : 0u;
@@ -605,9 +652,14 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile4_kernel(
   // ---- conversion, one row pair at a time
   uint2 pcol[4] = {make_uint2(0, 0), make_uint2(0, 0), make_uint2(0, 0), make_uint2(0, 0)};
   const int grp = lane & ~3;
+  // Philox counter (element index / 4) of row r0 and the row payload pointer,
+  // both advanced row by row
+  const int64_t e0 = (r0 * C + c0) >> 2, estep = C >> 2;
+  uint8_t* prow = pay_row + ((r0 * C + c0) >> 1);
+  const int64_t pstep = C >> 1;
 #pragma unroll
   for (int p = 0; p < 8; ++p) {
-    const int64_t ea = ((r0 + 2 * p) * C + c0) >> 2, eb = ((r0 + 2 * p + 1) * C + c0) >> 2;
+    const int64_t ea = e0 + (2 * p) * estep, eb = ea + estep;
     float re = 0.0f, ro = 0.0f;
     uint32_t wra[4], wrb[4], wca[4], wcb[4];
     if (DO_ROW) {
@@ -662,15 +714,15 @@ __global__ void __launch_bounds__(kRcThreads, 3) quantize_tile4_kernel(
       }
     }
     if (DO_ROW && ok) {
-      *reinterpret_cast<uint16_t*>(pay_row + (((r0 + 2 * p) * C + c0) >> 1)) = (uint16_t)rowa;
-      *reinterpret_cast<uint16_t*>(pay_row + (((r0 + 2 * p + 1) * C + c0) >> 1)) = (uint16_t)rowb;
+      *reinterpret_cast<uint16_t*>(prow + (2 * p) * pstep) = (uint16_t)rowa;
+      *reinterpret_cast<uint16_t*>(prow + (2 * p + 1) * pstep) = (uint16_t)rowb;
     }
   }
 #pragma unroll
   for (int j = 0; j < 4; ++j)
     *reinterpret_cast<uint2*>(&stage.pay[stage_word(4 * lane + j, 2 * warp)]) = pcol[j];
   __syncthreads();
-  write_col_stage(stage, R, C, ty * kRcRows, tx * kRcCols, pay_col, sc_col);
+  write_col_stage(stage, R, C, (int64_t)ty * kRcRows, (int64_t)tx * kRcCols, pay_col, sc_col);
   if (STATS) {
     if (DO_ROW) flush_stats(stats, r_sat, r_uflow, r_clamp, r_flush);
     if (!TWO_D) flush_stats(stats + (DO_ROW ? 1 : 0), c_sat, c_uflow, c_clamp, c_flush);
