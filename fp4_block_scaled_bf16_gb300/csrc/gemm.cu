@@ -1,5 +1,6 @@
 // gemm.cu -- the emulated UE5M3 block-scaled GEMM of libfp4q.so on the
-// sm_103a tensor cores (tcgen05, TMEM accumulators, TMA, mbarrier pipeline).
+// sm_103a tensor cores (tcgen05 on SM pairs, TMEM accumulators, TMA, mbarrier
+// pipeline).
 //
 // Method: "UE5M3 FP4 Block Scaling for Stable Language Model Pretraining",
 // Abstract -- the FP4 matrix multiplications of every internal linear run on
@@ -14,25 +15,33 @@
 // operands expanded in shared memory, and differs from an exact sum only by
 // FP32 accumulation rounding.
 //
-// CTA organisation (one CTA per SM, 256 x 256 output tile, K step 64; the
-// expansion is the costly part, so the tile is as large as TMEM allows: two
-// 128 x 256 FP32 accumulators fill all 512 columns):
-//   warp 16     TMA producer: FP4 payload tiles (A and B, 256 x 32 B each)
-//               into a 4-stage raw ring.
-//   warps 0..15 expand raw stages into a 2-stage FP16 ring laid out in the
+// Organisation.  A cluster of two CTAs (one per SM) computes a 256 x 512
+// output tile with the two-SM MMA (cta_group::2, M256 N256 K16): CTA rank r
+// holds A rows 128 r .. 128 r + 127 of the tile and, for each of the two
+// N256 halves of the tile, B rows 128 r .. 128 r + 127 of that half; its TMEM
+// holds its 128 rows of both 128 x 256 FP32 accumulators (all 512 columns).
+// The expansion is the costly part, and the pair expands 384 rows per SM and
+// K step for 128 x 512 outputs, a quarter fewer than one SM expanding the
+// 512 rows of a 256 x 256 tile on its own.  Per CTA, K step 64:
+//   warp 16     TMA producer: FP4 payload tiles (the CTA's 384 rows x 32 B)
+//               into a 4-stage raw ring, and the scale codes (16 per row,
+//               four K steps) into a 2-slot ring when K % 256 == 0.
+//   warps 0..15 expand raw stages into a 3-stage FP16 ring laid out in the
 //               128-byte-swizzled K-major form the MMA descriptors read; each
 //               thread expands one 16-element block (one scale) at a time by
 //               the E2M1 -> FP16 conversion and one exact FP16 multiply by
-//               the block scale;
-//               after the main loop they run the epilogue (TMEM -> registers
-//               -> alpha -> BF16/FP32 -> global).
-//   warp 17     allocates TMEM; one lane issues 8 MMAs (2 x M128 N256 K16)
-//               per stage and commits them to the stage's "empty" barrier.
+//               the block scale, then signal the rank-0 CTA's "full"
+//               barrier; after the main loop they run the epilogue (TMEM ->
+//               registers -> alpha -> BF16/FP32 -> global).
+//   warp 17     allocates the pair's TMEM; in the rank-0 CTA one lane waits
+//               until both CTAs have expanded a stage, issues its 8 MMAs
+//               (2 x M256 N256 K16 per K16 step) and commits them to both
+//               CTAs' "empty" barriers.
 // Every wait is bounded: a wait that runs out latches FP4Q_ERR_TIMEOUT in the
-// device status word and the CTA exits instead of hanging, once the producer
-// has waited (bounded) for the loads it issued and the MMA issuer for the
-// MMAs it issued, so that nothing asynchronous still targets the CTA's
-// shared memory or TMEM when it is freed.
+// device status word and the CTA winds down instead of hanging; the loads
+// and MMAs already issued are waited for (bounded) and both CTAs meet at a
+// cluster barrier before either frees TMEM or exits, so that nothing still
+// targets a CTA's shared memory or TMEM when it is released.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <string.h>
@@ -45,47 +54,50 @@
 namespace fp4q {
 namespace gemm {
 
-constexpr int BM = 256, BN = 256, BK = 64;     // CTA tile; two M=128 MMAs per K16 step
-constexpr int UM = 128;                         // rows per MMA instruction
-constexpr int S_RAW = 4, S_BF = 2;
-constexpr int RAW_A = BM * BK / 2;             // 8192 B
-constexpr int RAW_B = BN * BK / 2;             // 8192 B
-constexpr int RAW_STAGE = RAW_A + RAW_B;
-constexpr int BF_A = BM * BK * 2;              // 32768 B
-constexpr int BF_B = BN * BK * 2;              // 32768 B
-constexpr int BF_STAGE = BF_A + BF_B;
+constexpr int PM = 256, PN = 512;              // output tile of a CTA pair
+constexpr int AM = 128;                        // A rows per CTA = M of the MMA per CTA
+constexpr int BH = 128;                        // B rows per CTA and N256 half
+constexpr int UN = 256;                        // N of one MMA = TMEM columns of one accumulator
+constexpr int ROWS = AM + 2 * BH;              // rows expanded per CTA and K step
+constexpr int BK = 64;
+constexpr int S_RAW = 4, S_BF = 3;
+constexpr int RAW_STAGE = ROWS * BK / 2;       // 12288 B
+constexpr int BF_PART = AM * BK * 2;           // 16384 B: A, then the two B parts
+constexpr int BF_STAGE = ROWS * BK * 2;        // 49152 B
 constexpr int kDeqWarps = 16;
 constexpr int kDeqThreads = 32 * kDeqWarps;
 constexpr int kProducerWarp = kDeqWarps, kMmaWarp = kDeqWarps + 1;
 constexpr int kThreads = kDeqThreads + 64;
-constexpr uint32_t kTmemCols = 512;             // two 128 x 256 FP32 accumulators
-constexpr int kRowStride = kDeqThreads / 4;                      // rows between a thread's rows
-constexpr int kRowsPerThread = (BM + BN) / kRowStride;
-// epilogue: warps 4j .. 4j + 3 cover the 128 TMEM lanes of one accumulator;
-// the BN columns are split between the kDeqWarps / 8 warps of each lane group
-constexpr int kColParts = kDeqWarps / 8;
-constexpr int kColChunks = BN / kColParts / 32;                  // 32-column TMEM loads per warp
-static_assert(kRowStride % 8 == 0 && (BM + BN) % kRowStride == 0 && BM % kRowStride == 0, "row map");
-static_assert(kDeqWarps % 8 == 0 && BN % (32 * kColParts) == 0, "epilogue map");
+constexpr uint32_t kTmemCols = 512;            // two 128 x 256 FP32 accumulators
+constexpr int kRowStride = kDeqThreads / 4;    // rows between a thread's rows
+constexpr int kRowsPerThread = ROWS / kRowStride;
+// epilogue: warps 4j .. 4j + 3 cover the 128 TMEM lanes (the CTA's rows);
+// lane group j takes TMEM columns 128 j .. 128 j + 127
+constexpr int kColGroups = kDeqWarps / 4;
+constexpr int kColChunks = 2 * UN / kColGroups / 32;   // 32-column TMEM loads per warp
+static_assert(kRowStride == AM && BH == AM && ROWS % kRowStride == 0, "row map: A, B0, B1 rows per thread");
+static_assert(kDeqWarps % 4 == 0 && (2 * UN) % (32 * kColGroups) == 0, "epilogue map");
 
 // Scale codes (when K is a multiple of 256): TMA boxes of 16 codes per row
-// (four K steps) for the 256 A rows and the 256 B rows, in a 2-slot ring.
-constexpr int CODE_KB = 4;                      // K steps per code stage
-constexpr int CODE_STAGE = (BM + BN) * 16;      // 8192 B
+// (four K steps) for the CTA's 384 rows, in a 2-slot ring.
+constexpr int CODE_KB = 4;                     // K steps per code stage
+constexpr int CODE_STAGE = ROWS * 16;          // 6144 B
 constexpr int S_CODE = 2;
 
 constexpr int OFF_BF = 0;
 constexpr int OFF_RAW = OFF_BF + S_BF * BF_STAGE;
 constexpr int OFF_CODE = OFF_RAW + S_RAW * RAW_STAGE;
 constexpr int NBARS = 2 * S_RAW + 2 * S_BF + 1 + 2 * S_CODE;
-// Epilogue staging: the BF16 result (four 256 x 64 boxes) in the idle BF16
-// ring, the quantised result (payload box 256 x 128 B, codes box 256 x 16 B)
-// in the idle raw ring.
-constexpr int QST_PAY = BM * 128, QST_BYTES = QST_PAY + BM * 16;
+static_assert(OFF_RAW % 1024 == 0 && OFF_CODE % 1024 == 0 && BF_PART % 1024 == 0, "alignment");
+// Epilogue staging: the BF16 result (eight 128 x 64 boxes) in the idle FP16
+// ring, the quantised result (two payload boxes 128 x 128 B, codes box
+// 128 x 32 B) in the idle raw ring.
+constexpr int OUT_BOX = AM * 128;              // one 128 x 64 BF16 box, or 128 x 128 B of payload
+constexpr int QST_PAY = 2 * OUT_BOX, QST_BYTES = QST_PAY + AM * 32;
 constexpr int OFF_QST = OFF_RAW;
-static_assert(S_BF * BF_STAGE >= (BN / 64) * BM * 128, "BF16 staging fits the BF16 ring");
+static_assert(S_BF * BF_STAGE >= (2 * UN / 64) * OUT_BOX, "BF16 staging fits the FP16 ring");
 static_assert(S_RAW * RAW_STAGE >= QST_BYTES && OFF_QST % 1024 == 0, "quantised staging fits the raw ring");
-// Without the code ring the kernel leaves its 16 KB to L1, which then holds
+// Without the code ring the kernel leaves its 12 KB to L1, which then holds
 // the scale codes it loads directly.
 __host__ __device__ constexpr int off_bar(bool tma_codes) { return OFF_CODE + (tma_codes ? S_CODE * CODE_STAGE : 0); }
 // after the barriers: TMEM address (8 B), abort flag (8 B), then the scale
@@ -94,21 +106,89 @@ constexpr int TAB_BYTES = (int)((sizeof(ScaleTab) + 15) / 16 * 16);
 __host__ __device__ constexpr int smem_bytes(bool tma_codes) {
   return off_bar(tma_codes) + 8 * NBARS + 16 + TAB_BYTES + 1024;   // + 1 KB alignment slack
 }
+static_assert(smem_bytes(true) <= 227 * 1024, "shared memory per CTA");
 
+// ---------------------------------------------------------------- the CTA pair
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of both CTAs: release what this CTA wrote, acquire the peer's.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Arrive on the barrier at the same shared-memory offset in the rank-0 CTA.
+// The arrival has the default semantics (release at CTA scope), as the
+// vendor's own cluster pipelines use for remote arrivals: what it publishes
+// is this CTA's FP16 stage, written to its own shared memory and fenced to
+// the async proxy by every writing thread before the warp's __syncwarp, and
+// read by the pair's MMA only after rank 0 has seen the arrival.  A
+// cluster-scope release per warp and stage measured 40 % slower on the
+// 8B-class GEMMs (and one relayed cluster-scope arrival per stage, 20 %).
+__device__ __forceinline__ void mbar_arrive_rank0(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .b32 ra;\n\t"
+      "mapa.shared::cluster.u32 ra, %0, 0;\n\t"
+      "mbarrier.arrive.shared::cluster.b64 _, [ra];\n\t}" ::"r"(bar)
+      : "memory");
+}
+// Parity probe that acquires at cluster scope (arrivals from the peer CTA).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+static __device__ __noinline__ bool mbar_wait_cluster_slow(uint32_t bar, uint32_t parity,
+                                                           volatile int* abort_flag, long long budget) {
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > budget) return false;
+  }
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                  long long budget) {
+  return mbar_try_wait_cluster(bar, parity) || mbar_wait_cluster_slow(bar, parity, abort_flag, budget);
+}
+// TMEM of the pair: one warp of each CTA allocates (and later frees) the
+// same columns in both CTAs' TMEM.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols) : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+// Arrive, once every MMA this thread issued before has completed, on the
+// barrier at this offset in both CTAs of the pair.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"((unsigned short)3)
+      : "memory");
+}
 
 // ---------------------------------------------------------------- kind::f16 MMA
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t accum) {
+__device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t accum) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
       : "memory");
 }
 // Instruction descriptor for kind::f16: FP32 accumulator, FP16 A and B (format
-// code 0), both K-major, M = 128, N = 256.
-constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(UM >> 4) << 24);
+// code 0), both K-major, M = 256 (the pair), N = 256.
+constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(UN >> 3) << 17) | ((uint32_t)((2 * AM) >> 4) << 24);
 
 // ---------------------------------------------------------------- expansion
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
@@ -170,6 +250,8 @@ __device__ __forceinline__ uint2 lds64(uint32_t addr) {
 // QOUT: the epilogue also quantises the BF16 result row-wise (blocks of 16
 // along N, round to nearest even, tensor scale TC) -- the input format of the
 // next layer -- and records max |bf16(C)|; `out` may then be null.
+// Launched in clusters of two along x: blockIdx.x / 2 indexes the 512-column
+// tile, blockIdx.y the 256-row tile.
 template <bool F32OUT, bool TMA_CODES, bool QOUT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
@@ -199,7 +281,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+  const uint32_t rank = cluster_rank();
+  const int m0 = blockIdx.y * PM, n0 = (blockIdx.x >> 1) * PN;
+  const int am0 = m0 + AM * (int)rank;                 // this CTA's A rows
+  const int bn0 = n0 + BH * (int)rank;                 // its B rows of the first N256 half
+  const int bn1 = bn0 + UN;                            // ... and of the second
   const int nk = K / BK;
 
   if (QOUT) build_scale_tab(tab, __ldg(TC), fmt);   // block-wide, before the roles split
@@ -209,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_raw_empty + 8 * i, kDeqWarps);
     }
     for (int i = 0; i < S_BF; ++i) {
-      mbar_init(bar_bf_full + 8 * i, kDeqWarps);
+      mbar_init(bar_bf_full + 8 * i, 2 * kDeqWarps);   // every expansion warp of both CTAs (used in rank 0)
       mbar_init(bar_bf_empty + 8 * i, 1);
     }
     mbar_init(bar_acc, 1);
@@ -220,9 +306,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == kMmaWarp) tmem_alloc(sb + OFF_TMEM, kTmemCols);
+  if (warp == kMmaWarp) tmem_alloc_pair(sb + OFF_TMEM, kTmemCols);
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();   // both CTAs' barriers initialised before either arrives on the other's
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + OFF_TMEM);
 
@@ -240,8 +326,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!skip_loads) {
             const uint32_t cdst = sb + OFF_CODE + cs * CODE_STAGE;
             mbar_expect_tx(bar_code_full + 8 * cs, CODE_STAGE);
-            tma_load_2d(cdst, &mapAs, g * 16, m0, bar_code_full + 8 * cs);
-            tma_load_2d(cdst + BM * 16, &mapBs, g * 16, n0, bar_code_full + 8 * cs);
+            tma_load_2d(cdst, &mapAs, g * 16, am0, bar_code_full + 8 * cs);
+            tma_load_2d(cdst + AM * 16, &mapBs, g * 16, bn0, bar_code_full + 8 * cs);
+            tma_load_2d(cdst + (AM + BH) * 16, &mapBs, g * 16, bn1, bar_code_full + 8 * cs);
             last_g = g;
           }
         }
@@ -253,8 +340,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t dst = sb + OFF_RAW + s * RAW_STAGE;
         if (skip_loads) continue;   // test hook: consumers' waits run out
         mbar_expect_tx(bar_raw_full + 8 * s, RAW_STAGE);
-        tma_load_2d(dst, &mapA, kb * (BK / 2), m0, bar_raw_full + 8 * s);
-        tma_load_2d(dst + RAW_A, &mapB, kb * (BK / 2), n0, bar_raw_full + 8 * s);
+        tma_load_2d(dst, &mapA, kb * (BK / 2), am0, bar_raw_full + 8 * s);
+        tma_load_2d(dst + AM * (BK / 2), &mapB, kb * (BK / 2), bn0, bar_raw_full + 8 * s);
+        tma_load_2d(dst + (AM + BH) * (BK / 2), &mapB, kb * (BK / 2), bn1, bar_raw_full + 8 * s);
         last_kb = kb;
       }
       // Drain, also after an abort: a load already issued still lands in this
@@ -276,37 +364,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!drained) atomicOr(status, kStatusTimeout);
     }
   } else if (warp == kMmaWarp) {
-    // ------------------------------------------------ MMA issuer
+    // ------------------------------------------------ MMA issuer (rank 0)
     if (lane == 0) {
-      for (int kb = 0; kb < nk; ++kb) {
-        const int t = kb % S_BF;
-        if (!mbar_wait(bar_bf_full + 8 * t, (kb / S_BF) & 1, abort_flag, budget)) {
-          fail(abort_flag, status);
-          break;
-        }
-        tc_fence_after();
-        const uint32_t a_addr = sb + OFF_BF + t * BF_STAGE;
-        const uint64_t a0 = sw128_desc(a_addr), a1 = sw128_desc(a_addr + UM * 128);
-        const uint64_t bd = sw128_desc(a_addr + BF_A);
+      if (rank == 0) {
+        for (int kb = 0; kb < nk; ++kb) {
+          const int t = kb % S_BF;
+          if (!mbar_wait_cluster(bar_bf_full + 8 * t, (kb / S_BF) & 1, abort_flag, budget)) {
+            fail(abort_flag, status);
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = sb + OFF_BF + t * BF_STAGE;
+          const uint64_t ad = sw128_desc(a_addr);
+          const uint64_t b0 = sw128_desc(a_addr + BF_PART), b1 = sw128_desc(a_addr + 2 * BF_PART);
 #pragma unroll
-        for (int k = 0; k < BK / 16; ++k) {
-          const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
-          mma_f16(tmem, a0 + 2 * k, bd + 2 * k, kIdesc, acc);          // rows 0..127
-          mma_f16(tmem + BN, a1 + 2 * k, bd + 2 * k, kIdesc, acc);     // rows 128..255
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
+            mma_f16_pair(tmem, ad + 2 * k, b0 + 2 * k, kIdesc, acc);        // columns 0..255
+            mma_f16_pair(tmem + UN, ad + 2 * k, b1 + 2 * k, kIdesc, acc);   // columns 256..511
+          }
+          mma_commit_pair(bar_bf_empty + 8 * t);
         }
-        mma_commit(bar_bf_empty + 8 * t);
+        mma_commit_pair(bar_acc);
       }
-      mma_commit(bar_acc);
-      // Drain, also after an abort: bar_acc completes once every MMA issued
-      // above has finished reading shared memory and writing TMEM, which must
-      // happen before TMEM is freed and the CTA exits (bounded, whatever the
-      // abort flag says).
+      // Drain, also after an abort: bar_acc completes (in both CTAs) once
+      // every MMA issued above has finished reading both CTAs' shared memory
+      // and writing their TMEM, which must happen before TMEM is freed and
+      // either CTA exits (bounded, whatever the abort flag says).
       if (!mbar_wait_bounded(bar_acc, 0, kDrainCycles)) atomicOr(status, kStatusTimeout);
     }
   } else {
     // ------------------------------------------------ expansion warps
-    // Thread t expands block (t % 4) of the 64-wide K step for rows
-    // t/4 + kRowStride i, i < kRowsPerThread (A rows 0..255, then B rows 0..255).
+    // Thread t expands block (t % 4) of the 64-wide K step for row t/4 of
+    // the CTA's A rows, of its first B part and of its second B part.
     const int tid = threadIdx.x;
     const int blk = tid & 3;
     const int rbase = tid >> 2;
@@ -315,10 +405,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool rok[kRowsPerThread];
 #pragma unroll
     for (int i = 0; i < kRowsPerThread; ++i) {
-      const int r = rbase + kRowStride * i;
-      const int gr = (r < BM) ? m0 + r : n0 + (r - BM);
-      rok[i] = (r < BM) ? (gr < M) : (gr < N);
-      srow[i] = ((r < BM) ? As : Bs) + (int64_t)(rok[i] ? gr : 0) * lds_k + blk;
+      const int gr = (i == 0 ? am0 : i == 1 ? bn0 : bn1) + rbase;
+      rok[i] = (i == 0) ? (gr < M) : (gr < N);
+      srow[i] = ((i == 0) ? As : Bs) + (int64_t)(rok[i] ? gr : 0) * lds_k + blk;
     }
     auto load_codes = [&](int kb, uint32_t (&c)[kRowsPerThread]) {
 #pragma unroll
@@ -369,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(bar_bf_full + 8 * t);
+        mbar_arrive_rank0(bar_bf_full + 8 * t);
         mbar_arrive(bar_raw_empty + 8 * s);
         if (TMA_CODES && (kb % CODE_KB == CODE_KB - 1 || kb == nk - 1)) mbar_arrive(bar_code_empty + 8 * cs);
       }
@@ -382,33 +471,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ------------------------------------------------ epilogue
-    // warp w drains TMEM lanes 32 (w % 4) .. +31 of accumulator (w / 4) % 2,
-    // columns 32 kColChunks (w / 8) .. +32 kColChunks - 1.  BF16 output with a tensor map: the tile is
-    // staged in the idle expansion ring as four 256 x 64 boxes (128-byte
-    // swizzled) and leaves by TMA stores, whole lines, while the next CTA
-    // starts; otherwise every thread stores its 32 values directly.
+    // warp w drains TMEM lanes 32 (w % 4) .. +31 (the CTA's rows), columns
+    // 128 (w / 4) .. +127 (accumulator 0 holds output columns 0..255, 1 the
+    // rest).  BF16 output with a tensor map: the CTA's 128 x 512 result is
+    // staged in the idle FP16 ring as eight 128 x 64 boxes (128-byte
+    // swizzled) and leaves by TMA stores, whole lines; otherwise every
+    // thread stores its 32 values directly.
     const bool staged = !F32OUT && tma_store;
-    // quantised result staged in the idle raw ring (payload box 256 x 128 B,
-    // 128-byte swizzled; codes box 256 x 16 B) and stored by TMA
+    // quantised result staged in the idle raw ring (two payload boxes
+    // 128 x 128 B, 128-byte swizzled; codes box 128 x 32 B) and stored by TMA
     const bool qst = QOUT && qstaged;
     const bool drained = mbar_wait(bar_acc, 0, abort_flag, budget);
     if (drained) {
       tc_fence_after();
-      const int q = warp & 3, acc = (warp >> 2) & 1, part = warp >> 3;
+      const int q = warp & 3, grp = warp >> 2;
       // T_A T_B, times 2^8 for the 2^-4 on each operand (exact)
       const float alpha = __fmul_rn(__fmul_rn(__ldg(TA), __ldg(TB)), 256.0f);
-      const int rt = UM * acc + 32 * q + lane;            // row within the tile
-      const int row = m0 + rt;
+      const int rt = 32 * q + lane;                       // row within the CTA's 128
+      const int row = am0 + rt;
       const bool vec = F32OUT ? (N % 4 == 0) : (N % 8 == 0);
       uint32_t qmax = 0;
       ScaleRegs kr{};
       if (QOUT) kr = scale_regs(*tab);
 #pragma unroll 1
       for (int c = 0; c < kColChunks; ++c) {
-        const int ct = 32 * (kColChunks * part + c);       // column within the tile
+        const int ct = 32 * (kColChunks * grp + c);        // column within the 512
         const int col0 = n0 + ct;
         uint32_t r[32];
-        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(BN * acc + ct), r);
+        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)ct, r);
         const bool live = row < M && col0 < N;
         if (!staged && !live) continue;
         float v[32];
@@ -430,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(h[j]) : "f"(v[2 * j + 1]), "f"(v[2 * j]));
           if (staged) {
             // box ct / 64, row rt, 16-byte chunks (ct % 64) / 8 + i, swizzled by row
-            const uint32_t rowb = sb + OFF_BF + (uint32_t)(ct >> 6) * (BM * 128) + (uint32_t)rt * 128;
+            const uint32_t rowb = sb + OFF_BF + (uint32_t)(ct >> 6) * OUT_BOX + (uint32_t)rt * 128;
             const int ch0 = (ct & 63) >> 3;
 #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -460,9 +550,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               codes |= bs.code << (8 * b);
             }
             if (qst) {
-              sts128(sb + OFF_QST + (uint32_t)rt * 128 + ((uint32_t)((ct >> 5) ^ (rt & 7)) << 4),
+              // payload box ct / 256, row rt, 16-byte chunk (ct % 256) / 32, swizzled by row
+              sts128(sb + OFF_QST + (uint32_t)(ct >> 8) * OUT_BOX + (uint32_t)rt * 128 +
+                         ((uint32_t)(((ct & 255) >> 5) ^ (rt & 7)) << 4),
                      make_uint4(pw[0], pw[1], pw[2], pw[3]));
-              asm volatile("st.shared.u16 [%0], %1;" ::"r"(sb + OFF_QST + QST_PAY + (uint32_t)rt * 16 + (ct >> 4)),
+              asm volatile("st.shared.u16 [%0], %1;" ::"r"(sb + OFF_QST + QST_PAY + (uint32_t)rt * 32 + (ct >> 4)),
                            "h"((unsigned short)codes) : "memory");
             } else {
               *reinterpret_cast<uint4*>(qpay + (int64_t)row * (N / 2) + col0 / 2) =
@@ -487,25 +579,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every expansion warp passes here exactly once, drained or not
       fence_proxy_async();
       asm volatile("bar.sync 1, %0;" ::"n"(kDeqThreads) : "memory");
-      if (threadIdx.x == 0 && drained && !*abort_flag) {
+      // boxes that start inside the result only (a ragged edge is clipped by
+      // the store itself)
+      if (threadIdx.x == 0 && drained && !*abort_flag && am0 < M) {
         if (staged) {
-#pragma unroll
-          for (int j = 0; j < BN / 64; ++j) tma_store_2d(&mapC, sb + OFF_BF + j * (BM * 128), n0 + 64 * j, m0);
+          for (int j = 0; j < 2 * UN / 64 && n0 + 64 * j < N; ++j)
+            tma_store_2d(&mapC, sb + OFF_BF + j * OUT_BOX, n0 + 64 * j, am0);
         }
         if (qst) {
-          tma_store_2d(&mapQP, sb + OFF_QST, n0 / 2, m0);
-          tma_store_2d(&mapQS, sb + OFF_QST + QST_PAY, n0 / 16, m0);
+          tma_store_2d(&mapQP, sb + OFF_QST, n0 / 2, am0);
+          if (n0 + 256 < N) tma_store_2d(&mapQP, sb + OFF_QST + OUT_BOX, n0 / 2 + 128, am0);
+          tma_store_2d(&mapQS, sb + OFF_QST + QST_PAY, n0 / 16, am0);
         }
         tma_store_commit_and_wait_read();
       }
     }
   }
 
+  // Both CTAs meet here once their loads, MMAs and remote arrivals are done;
+  // only then is the pair's TMEM freed.
+  __syncwarp();
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();
   if (warp == kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc_pair(tmem, kTmemCols);
   }
 }
 
@@ -555,14 +653,14 @@ static bool make_code_map(CUtensorMap* map, const uint8_t* base, int64_t rows, i
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D BF16 tensor map over the [M, N] output, box (64 columns, 256 rows),
+// 2-D BF16 tensor map over the [M, N] output, box (64 columns, 128 rows),
 // 128-byte swizzle; needs a row stride that is a multiple of 16 bytes.
 static bool make_out_map(CUtensorMap* map, void* base, int64_t M, int64_t N) {
   auto fn = get_encode_fn();
   if (!fn || N % 8 != 0) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
   const cuuint64_t strides[1] = {(cuuint64_t)(N * 2)};
-  const cuuint32_t box[2] = {64u, (cuuint32_t)gemm::BM};
+  const cuuint32_t box[2] = {64u, (cuuint32_t)gemm::AM};
   const cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -570,18 +668,18 @@ static bool make_out_map(CUtensorMap* map, void* base, int64_t M, int64_t N) {
 }
 
 // 2-D uint8 tensor maps over the row-wise quantised result: payload [M, N/2]
-// with box (128 B, 256 rows) and 128-byte swizzle; codes [M, N/16] with box
-// (16 B, 256 rows).  Need row strides that are multiples of 16 bytes.
+// with box (128 B, 128 rows) and 128-byte swizzle; codes [M, N/16] with box
+// (32 B, 128 rows).  Need row strides that are multiples of 16 bytes.
 static bool make_qout_maps(CUtensorMap* mp, CUtensorMap* ms, uint8_t* pay, uint8_t* sc, int64_t M, int64_t N) {
   auto fn = get_encode_fn();
   if (!fn || N % 256 != 0) return false;
   const cuuint32_t estr[2] = {1, 1};
   const cuuint64_t pd[2] = {(cuuint64_t)(N / 2), (cuuint64_t)M};
   const cuuint64_t ps[1] = {(cuuint64_t)(N / 2)};
-  const cuuint32_t pb[2] = {128u, (cuuint32_t)gemm::BM};
+  const cuuint32_t pb[2] = {128u, (cuuint32_t)gemm::AM};
   const cuuint64_t sd[2] = {(cuuint64_t)(N / 16), (cuuint64_t)M};
   const cuuint64_t ss[1] = {(cuuint64_t)(N / 16)};
-  const cuuint32_t sbx[2] = {16u, (cuuint32_t)gemm::BM};
+  const cuuint32_t sbx[2] = {32u, (cuuint32_t)gemm::AM};
   return fn(mp, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, pay, pd, ps, pb, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS &&
@@ -601,25 +699,35 @@ static cudaError_t launch_gemm_t(const GemmArgs& a, const CUtensorMap& mapA, con
     memset(&mapQS, 0, sizeof(mapQS));
   }
   constexpr int smem = gemm::smem_bytes(TMA_CODES);
-  cudaError_t e = cudaFuncSetAttribute(gemm::gemm_kernel<F32OUT, TMA_CODES, QOUT>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  auto kern = gemm::gemm_kernel<F32OUT, TMA_CODES, QOUT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)((a.N + gemm::BN - 1) / gemm::BN), (unsigned)((a.M + gemm::BM - 1) / gemm::BM));
-  gemm::gemm_kernel<F32OUT, TMA_CODES, QOUT><<<grid, gemm::kThreads, smem, st>>>(
-      mapA, mapB, mapAs, mapBs, mapC, tma_store ? 1 : 0, a.As, a.Bs, a.TA, a.TB, (int)a.M, (int)a.N,
-      (int)a.K, a.fmt, a.out,
-      a.status, a.wait_cycles, a.skip_loads ? 1 : 0, a.TC, a.qpay, a.qsc, a.qamax, mapQP, mapQS,
-      qstaged ? 1 : 0);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2u * (unsigned)((a.N + gemm::PN - 1) / gemm::PN), (unsigned)((a.M + gemm::PM - 1) / gemm::PM));
+  cfg.blockDim = dim3(gemm::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, mapA, mapB, mapAs, mapBs, mapC, tma_store ? 1 : 0, a.As, a.Bs, a.TA, a.TB,
+                         (int)a.M, (int)a.N, (int)a.K, a.fmt, a.out, a.status, a.wait_cycles,
+                         a.skip_loads ? 1 : 0, a.TC, a.qpay, a.qsc, a.qamax, mapQP, mapQS, qstaged ? 1 : 0);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   if (a.M == 0 || a.N == 0) return cudaSuccess;
   CUtensorMap mapA, mapB, mapAs, mapBs;
-  if (!make_payload_map(&mapA, a.A, a.M, a.K, gemm::BM) || !make_payload_map(&mapB, a.B, a.N, a.K, gemm::BN))
+  if (!make_payload_map(&mapA, a.A, a.M, a.K, gemm::AM) || !make_payload_map(&mapB, a.B, a.N, a.K, gemm::BH))
     return cudaErrorNotSupported;
-  const bool tma_codes = make_code_map(&mapAs, a.As, a.M, a.K, gemm::BM) &&
-                         make_code_map(&mapBs, a.Bs, a.N, a.K, gemm::BN);
+  const bool tma_codes = make_code_map(&mapAs, a.As, a.M, a.K, gemm::AM) &&
+                         make_code_map(&mapBs, a.Bs, a.N, a.K, gemm::BH);
   if (!tma_codes) {
     memset(&mapAs, 0, sizeof(mapAs));   // unused by the direct-load instantiation
     memset(&mapBs, 0, sizeof(mapBs));
