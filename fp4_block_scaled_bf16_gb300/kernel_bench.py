@@ -9,7 +9,12 @@ Small cases of this command are what the committed ncu summaries capture.
 
   python -m fp4_block_scaled_bf16_gb300.kernel_bench --case dual_sr --rows 2048 --cols 16384
   cases: amax, row_rne, row_sr, dual_rne, dual_sr, 2d_rne, 2d_sr, dequant, gemm and gemm_nvfp4
-  (--m --n --k; gemm_nvfp4 on UE4M3-scaled operands)
+  (--m --n --k; gemm_nvfp4 on UE4M3-scaled operands), and step: the whole
+  linear fwd+bwd step of the bench (X [m, k], W [n, k], dY [m, n]) under
+  periodic tensor scaling on three streams, one "launch" per step (its first
+  step launches 12 kernels -- amax and tensor scale of X, W, dY, three
+  quantisations, three GEMMs -- every later one 6, plus a tensor scale per
+  tensor every 16 steps).
 """
 from __future__ import annotations
 
@@ -20,7 +25,8 @@ import torch
 
 from . import build, fp4q, workloads
 
-CASES = ("amax", "row_rne", "row_sr", "dual_rne", "dual_sr", "2d_rne", "2d_sr", "dequant", "gemm", "gemm_nvfp4")
+CASES = ("amax", "row_rne", "row_sr", "dual_rne", "dual_sr", "2d_rne", "2d_sr", "dequant", "gemm", "gemm_nvfp4",
+         "step")
 
 
 def _inputs(case, rows, cols, dev):
@@ -32,7 +38,16 @@ def run(case, rows=16384, cols=4096, m=8192, n=16384, k=4096, reps=10, warmup=3)
     build.build()
     dev = torch.device("cuda")
     u8 = dict(dtype=torch.uint8, device=dev)
-    if case in ("gemm", "gemm_nvfp4"):
+    if case == "step":
+        from .linear_step import LinearStep
+
+        X = workloads.to_torch_bf16(workloads.activations(m, k, 1)).to(dev)
+        W = workloads.to_torch_bf16(workloads.weights(n, k, 2)).to(dev)
+        dY = workloads.to_torch_bf16(workloads.gradients(m, n, 3)).to(dev)
+        st = LinearStep(X, W, dY, seed=7)
+        launch = lambda j: st.run_overlapped(periodic=True)
+        work, unit = 3 * 2.0 * m * n * k, "TFLOP/s"
+    elif case in ("gemm", "gemm_nvfp4"):
         fmt = fp4q.UE5M3 if case == "gemm" else fp4q.UE4M3
         xs = [fp4q.quantize(workloads.to_torch_bf16(workloads.activations(m, k, 60)).to(dev), fmt=fmt),
               fp4q.quantize(workloads.to_torch_bf16(workloads.weights(n, k, 61)).to(dev), fmt=fmt)]
@@ -83,7 +98,7 @@ def run(case, rows=16384, cols=4096, m=8192, n=16384, k=4096, reps=10, warmup=3)
     ms = e0.elapsed_time(e1) / reps
     rate = work / (ms * 1e-3) / (1e12 if unit == "TFLOP/s" else 1e9)
     status = fp4q.fp4q_get_device_status()
-    shape = {"m": m, "n": n, "k": k} if case.startswith("gemm") else {"rows": rows, "cols": cols}
+    shape = {"m": m, "n": n, "k": k} if case.startswith("gemm") or case == "step" else {"rows": rows, "cols": cols}
     return {"case": case, **shape, "reps": reps, "ms_per_launch": ms, "rate": rate, "unit": unit,
             "device_status": status}
 
