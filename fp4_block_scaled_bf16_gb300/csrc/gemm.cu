@@ -108,74 +108,6 @@ __host__ __device__ constexpr int smem_bytes(bool tma_codes) {
 }
 static_assert(smem_bytes(true) <= 227 * 1024, "shared memory per CTA");
 
-// ---------------------------------------------------------------- the CTA pair
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// Every thread of both CTAs: release what this CTA wrote, acquire the peer's.
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// Arrive on the barrier at the same shared-memory offset in the rank-0 CTA.
-// The arrival has the default semantics (release at CTA scope), as the
-// vendor's own cluster pipelines use for remote arrivals: what it publishes
-// is this CTA's FP16 stage, written to its own shared memory and fenced to
-// the async proxy by every writing thread before the warp's __syncwarp, and
-// read by the pair's MMA only after rank 0 has seen the arrival.  A
-// cluster-scope release per warp and stage measured 40 % slower on the
-// 8B-class GEMMs (and one relayed cluster-scope arrival per stage, 20 %).
-__device__ __forceinline__ void mbar_arrive_rank0(uint32_t bar) {
-  asm volatile(
-      "{\n\t.reg .b32 ra;\n\t"
-      "mapa.shared::cluster.u32 ra, %0, 0;\n\t"
-      "mbarrier.arrive.shared::cluster.b64 _, [ra];\n\t}" ::"r"(bar)
-      : "memory");
-}
-// Parity probe that acquires at cluster scope (arrivals from the peer CTA).
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
-  return ok != 0;
-}
-static __device__ __noinline__ bool mbar_wait_cluster_slow(uint32_t bar, uint32_t parity,
-                                                           volatile int* abort_flag, long long budget) {
-  const long long t0 = clock64();
-  while (true) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (clock64() - t0 > budget) return false;
-  }
-}
-__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                                  long long budget) {
-  return mbar_try_wait_cluster(bar, parity) || mbar_wait_cluster_slow(bar, parity, abort_flag, budget);
-}
-// TMEM of the pair: one warp of each CTA allocates (and later frees) the
-// same columns in both CTAs' TMEM.
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
-               "r"(ncols) : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
-}
-// Arrive, once every MMA this thread issued before has completed, on the
-// barrier at this offset in both CTAs of the pair.
-__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-      "h"((unsigned short)3)
-      : "memory");
-}
-
 // ---------------------------------------------------------------- kind::f16 MMA
 __device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                               uint32_t idesc, uint32_t accum) {
