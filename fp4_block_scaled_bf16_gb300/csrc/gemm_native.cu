@@ -23,9 +23,9 @@
 //   warp 12     TMA producer: the CTA's payload tiles of A (128 x 128 B) and
 //               B (128 x 128 B), 128-byte swizzled as the MMA descriptors
 //               read them, and the stage's scale codes (16 per row: the
-//               CTA's 128 A rows, all 256 B rows of the tile) into a 4-stage
+//               CTA's 128 A rows, all 256 B rows of the tile) into a 5-stage
 //               ring.
-//   warps 0..3  copy the stage's scale codes into this CTA's TMEM
+//   warps 0..3  copy the stage's scale codes into one of four TMEM slots
 //               (tcgen05.st), warp q into lane quadrant q, all four the same
 //               data: for each of the stage's four K64 MMAs, the 32-bit word
 //               of row r (its four block scales, the first K block in the
@@ -60,7 +60,8 @@ constexpr int PM = 256, PN = 256;                // output tile of a CTA pair
 constexpr int BM = 128, BH = 128, BN = 256;      // A rows and B rows per CTA; N of the MMA
 constexpr int BK = 256;                          // K elements per stage
 constexpr int ROWB = BK / 2;                     // payload bytes per row per stage (128)
-constexpr int S = 4;                             // ring stages (the TMEM scale ring holds four)
+constexpr int S = 5;                             // shared-memory ring stages
+constexpr int SF = 4;                            // TMEM scale slots (64 columns each)
 constexpr int A_BYTES = BM * ROWB;               // 16384
 constexpr int B_BYTES = BH * ROWB;               // 16384: this CTA's half of B
 constexpr int SA_BYTES = BM * (BK / 16);         // 2048: 16 scale codes per row
@@ -76,8 +77,8 @@ static_assert(kEpiWarp0 % 4 == 0, "epilogue warp w drains TMEM lane quadrant w %
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol0 = 256;                // scale ring: stage s at 256 + 64 s
 constexpr uint32_t kSfStageCols = 64;            // per MMA 16 columns: B (8) then A (4)
-static_assert(kSfCol0 + S * kSfStageCols <= kTmemCols && BN <= (int)kSfCol0, "TMEM map");
-constexpr int NBARS = 3 * S + 3;   // full, sf (rank 0), empty per stage; acc full / empty, done
+static_assert(kSfCol0 + SF * kSfStageCols <= kTmemCols && BN <= (int)kSfCol0 && SF < S, "TMEM map");
+constexpr int NBARS = 2 * S + SF + 3;   // full, empty per stage; sf (rank 0) per slot; acc full / empty, done
 constexpr int OFF_BAR = S * STAGE;
 constexpr int OFF_TMEM = OFF_BAR + 8 * NBARS;
 constexpr int OFF_ABORT = OFF_TMEM + 8;
@@ -172,9 +173,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
   const uint32_t bar_full = sb + OFF_BAR;            // TMA bytes of stage s landed (this CTA)
-  const uint32_t bar_sf = bar_full + 8 * S;          // stage s scales in both CTAs' TMEM (rank 0)
-  const uint32_t bar_empty = bar_sf + 8 * S;         // stage s MMAs completed
-  const uint32_t bar_acc_full = bar_empty + 8 * S;   // a tile's MMAs completed
+  const uint32_t bar_empty = bar_full + 8 * S;       // stage s MMAs completed
+  const uint32_t bar_sf = bar_empty + 8 * S;         // slot t scales in both CTAs' TMEM (rank 0)
+  const uint32_t bar_acc_full = bar_sf + 8 * SF;     // a tile's MMAs completed
   const uint32_t bar_acc_empty = bar_acc_full + 8;   // both CTAs' epilogues read TMEM (rank 0)
   const uint32_t bar_done = bar_acc_empty + 8;       // every MMA issued completed
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
@@ -196,9 +197,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(bar_full + 8 * i, 1);
-      mbar_init(bar_sf + 8 * i, 2 * kSfWarps);        // the scale warps of both CTAs
       mbar_init(bar_empty + 8 * i, 1);
     }
+    for (int i = 0; i < SF; ++i) mbar_init(bar_sf + 8 * i, 2 * kSfWarps);   // the scale warps of both CTAs
     mbar_init(bar_acc_full, 1);
     mbar_init(bar_acc_empty, 2 * kEpiWarps);          // the epilogue warps of both CTAs
     mbar_init(bar_done, 1);
@@ -260,10 +261,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           for (int kb = 0; kb < nk; ++kb, ++g) {
-            const int s = (int)(g % S);
+            const int s = (int)(g % S), t = (int)(g % SF);
             // both CTAs' scale warps have seen the stage's bytes land and put
-            // its scales in TMEM
-            if (!mbar_wait_cluster(bar_sf + 8 * s, (uint32_t)((g / S) & 1), abort_flag, budget)) {
+            // its scales in TMEM slot t
+            if (!mbar_wait_cluster(bar_sf + 8 * t, (uint32_t)((g / SF) & 1), abort_flag, budget)) {
               fail(abort_flag, status);
               ok = false;
               break;
@@ -273,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t ad = sw128_desc(st + OFF_A), bd = sw128_desc(st + OFF_B);
 #pragma unroll
             for (int i = 0; i < MMAS; ++i) {
-              const uint32_t sf = tmem + kSfCol0 + kSfStageCols * s + 16 * i;
+              const uint32_t sf = tmem + kSfCol0 + kSfStageCols * t + 16 * i;
               mma_nvfp4_pair(tmem, ad + 2 * i, bd + 2 * i, sf + 8, sf, (kb | i) != 0 ? 1u : 0u);
             }
             mma_commit_pair(bar_empty + 8 * s);
@@ -289,17 +290,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < kSfWarps) {
     // ------------------------------------------------ scale codes -> TMEM
-    // lane r0 of warp q writes TMEM lane 32 q + r0: for MMA i, column
-    // 16 i + j holds the word of B row r0 + 32 j (j < 8, the tile's 256 B
-    // rows), column 16 i + 8 + j the word of A row r0 + 32 j (j < 4, this
-    // CTA's 128 A rows).  The stage's TMEM scale slot is free: its loads
-    // were issued only after the MMAs of the previous round had read it.
+    // lane r0 of warp q writes TMEM lane 32 q + r0 of slot t: for MMA i,
+    // column 16 i + j holds the word of B row r0 + 32 j (j < 8, the tile's
+    // 256 B rows), column 16 i + 8 + j the word of A row r0 + 32 j (j < 4,
+    // this CTA's 128 A rows).  Slot t is rewritten once the MMAs of the
+    // stage that last used it (SF stages back) have completed.
     int64_t g = 0;
     bool ok = true;
     for (int tile = cid; tile < ntiles && ok; tile += ncl) {
       for (int kb = 0; kb < nk; ++kb, ++g) {
-        const int s = (int)(g % S);
-        if (!mbar_wait(bar_full + 8 * s, (uint32_t)((g / S) & 1), abort_flag, budget)) {
+        const int s = (int)(g % S), t = (int)(g % SF);
+        const int64_t gp = g - SF;   // the stage that last used slot t
+        if (!mbar_wait(bar_full + 8 * s, (uint32_t)((g / S) & 1), abort_flag, budget) ||
+            (gp >= 0 && !mbar_wait(bar_empty + 8 * (int)(gp % S), (uint32_t)((gp / S) & 1), abort_flag, budget))) {
           fail(abort_flag, status);
           ok = false;
           break;
@@ -310,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int jj = 0; jj < 4; ++jj) a[jj] = lds128(st + OFF_SA + (uint32_t)(lane + 32 * jj) * 16);
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) b[jj] = lds128(st + OFF_SB + (uint32_t)(lane + 32 * jj) * 16);
-        const uint32_t col = tmem + ((uint32_t)(32 * warp) << 16) + kSfCol0 + kSfStageCols * s;
+        const uint32_t col = tmem + ((uint32_t)(32 * warp) << 16) + kSfCol0 + kSfStageCols * t;
 #pragma unroll
         for (int i = 0; i < MMAS; ++i) {
           uint32_t v[16];
@@ -325,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_rank0(bar_sf + 8 * s);
+        if (lane == 0) mbar_arrive_rank0(bar_sf + 8 * t);
       }
     }
   } else {
