@@ -23,7 +23,8 @@
 //   warp 12     TMA producer: the CTA's payload tiles of A (128 x 128 B) and
 //               B (128 x 128 B), 128-byte swizzled as the MMA descriptors
 //               read them, and the stage's scale codes (16 per row: the
-//               CTA's 128 A rows, all 256 B rows of the tile) into a 5-stage
+//               CTA's 128 A rows, and all 256 B rows of the tile -- each CTA
+//               loads its 128 and multicasts them to both) into a 5-stage
 //               ring.
 //   warps 0..3  copy the stage's scale codes into one of four TMEM slots
 //               (tcgen05.st), warp q into lane quadrant q, all four the same
@@ -232,7 +233,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(st + OFF_A, &mapA, kb * ROWB, am0, bar_full + 8 * s);
           tma_load_2d(st + OFF_B, &mapB, kb * ROWB, bn0, bar_full + 8 * s);
           tma_load_2d(st + OFF_SA, &mapSA, kb * (BK / 16), am0, bar_full + 8 * s);
-          tma_load_2d(st + OFF_SB, &mapSB, kb * (BK / 16), n0, bar_full + 8 * s);
+          // the tile's 256 B rows of scale codes: this CTA loads its 128 and
+          // delivers them to both CTAs of the pair
+          tma_load_2d_multicast(st + OFF_SB + (uint32_t)(BH * (BK / 16)) * rank, &mapSB, kb * (BK / 16), bn0,
+                                bar_full + 8 * s, (uint16_t)0x3);
           last_g = g;
         }
       }
@@ -481,7 +485,7 @@ cudaError_t launch_gemm_nvfp4(const GemmArgs& a, cudaStream_t st) {
   CUtensorMap mA, mB, mSA, mSB;
   if (!make_swizzled_payload_map(&mA, a.A, a.M, a.K, native::BM) ||
       !make_swizzled_payload_map(&mB, a.B, a.N, a.K, native::BH) ||
-      !make_scale_map(&mSA, a.As, a.M, a.K, native::BM) || !make_scale_map(&mSB, a.Bs, a.N, a.K, native::BN))
+      !make_scale_map(&mSA, a.As, a.M, a.K, native::BM) || !make_scale_map(&mSB, a.Bs, a.N, a.K, native::BH))
     return cudaErrorNotSupported;
   return a.out_f32 ? launch_native_t<true>(a, mA, mB, mSA, mSB, st) : launch_native_t<false>(a, mA, mB, mSA, mSB, st);
 }
