@@ -166,3 +166,24 @@ def test_linear_block_fprop_shape(lib):
     assert np.abs(cc - Rc).max() / scale <= GEMM_TOL
     check_gemm_elementwise(cr, Rr, Sr, 4096)
     check_gemm_elementwise(cc, Rc, Sc, 4096)
+
+
+def test_persistent_tiles_with_ragged_edges(lib):
+    """More 256 x 256 tiles (9 x 11 = 99) than there are resident clusters of
+    two CTAs, so clusters walk several tiles and reuse TMEM and the stage ring
+    across them; ragged last tiles in both M and N.  Every element against
+    the oracle's exact e*s operands contracted in binary64, in FP32 and BF16."""
+    rng = np.random.default_rng(6)
+    M, N, K = 2200, 2600, 512
+    pa, pb = _payload(rng, M, K), _payload(rng, N, K)
+    sa = rng.integers(0x20, 0x60, (M, K // 16), dtype=np.uint8)
+    sb = rng.integers(0x20, 0x60, (N, K // 16), dtype=np.uint8)
+    ta, tb = 0.75, 1.5
+    C32, C16 = _run(lib, pa, sa, ta, pb, sb, tb)
+    ea, eb = oracle.deq_es(pa, sa, UE4M3), oracle.deq_es(pb, sb, UE4M3)
+    alpha = ta * tb
+    R = alpha * (ea @ eb.T)
+    S = alpha * (np.abs(ea) @ np.abs(eb).T)
+    assert gemm_error(C32, R) <= GEMM_TOL
+    check_gemm_elementwise(C32, R, S, K)
+    check_gemm_bf16(C16, R)
