@@ -72,6 +72,38 @@ def committed_traffic(name, sources):
     return d.get("dram_bytes_per_launch")
 
 
+QUANT_SOURCES = ["quantize.cu", "fp4q_device.cuh"]
+SMS, SCHEDULERS_PER_SM = 152, 4   # GB300: warp instructions issued per SM and clock
+
+
+def issue_roofline(q_gbs, sm_mhz):
+    """The dual-axis quantisers against the instruction-issue rate: at n
+    thread instructions per element (committed ncu counts, used only while
+    the quantiser sources hash to the captured version) the SMs' schedulers
+    (one warp instruction per clock each) cap the rate at
+    SMs x schedulers x 32 x clock / n elements per second, 3.125 B each."""
+    p = os.path.join(ROOT, "profiles", "quantize_instructions.json")
+    if not os.path.exists(p) or not sm_mhz:
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("source_sha") != kernel_sources_sha(QUANT_SOURCES):
+        return None
+    per = d["thread_instructions_per_element"]
+    n_rne = next(v for k, v in per.items() if k.startswith("quantize_tile_kernel"))
+    n_sr = next(v for k, v in per.items() if k.startswith("quantize_tile4_kernel"))
+    thread_ips = SMS * SCHEDULERS_PER_SM * 32 * sm_mhz * 1e6
+    peak = {"X_dual_rne": thread_ips / n_rne * DUAL_BYTES_PER_ELEM / 1e9,
+            "W_dual_rne": thread_ips / n_rne * DUAL_BYTES_PER_ELEM / 1e9,
+            "dY_dual_sr": thread_ips / n_sr * DUAL_BYTES_PER_ELEM / 1e9}
+    ach = dict(zip(("X_dual_rne", "W_dual_rne", "dY_dual_sr"), q_gbs))
+    return {"bound": "alu", "unit": "GB/s", "achieved": ach, "peak": peak,
+            "frac": {k: ach[k] / peak[k] for k in ach},
+            "instructions_per_element": {"dual_rne": n_rne, "dual_sr": n_sr},
+            "peak_source": f"{SMS} SMs x {SCHEDULERS_PER_SM} schedulers x 32 lanes x {sm_mhz:.0f} MHz (median SM "
+                           "clock of the timed region) / ncu instructions per element (profiles/quantize_instructions.json)"}
+
+
 def max_over_ranks(x: float, device=None) -> float:
     """The largest x over the ranks of the initialised process group (the
     job time of N replicas is the slowest rank's); x itself with one rank."""
@@ -736,7 +768,8 @@ def main():
                               "achieved": dict({"X_dual_rne": q_gbs[0], "W_dual_rne": q_gbs[1], "dY_dual_sr": q_gbs[2]}, **r["rates"]),
                               "frac": dict({k: g / hbm for k, g in zip(("X_dual_rne", "W_dual_rne", "dY_dual_sr"), q_gbs)},
                                            **{k: g / hbm for k, g in r["rates"].items()}) if hbm else None,
-                              "peak_source": f"{src} hbm"},
+                              "peak_source": f"{src} hbm",
+                              "issue_roofline": issue_roofline(q_gbs, (r["clocks"] or {}).get("sm_mhz"))},
         "breakdown_ms": {"amax_scale": r["t_scale"], "quantize_X": r["t_q"][0], "quantize_W": r["t_q"][1],
                          "quantize_dY": r["t_q"][2], "fprop": r["t_g"][0], "dgrad": r["t_g"][1],
                          "wgrad": r["t_g"][2]},

@@ -67,3 +67,19 @@ def test_parse_cpulist():
     assert bench.parse_cpulist("0-3,8,10-11\n") == {0, 1, 2, 3, 8, 10, 11}
     assert bench.parse_cpulist("5") == {5}
     assert bench.parse_cpulist("") == set()
+
+
+def test_issue_roofline(monkeypatch):
+    import bench
+    r = bench.issue_roofline([3000.0, 4000.0, 1500.0], 2000.0)
+    assert r is not None and r["bound"] == "alu"
+    n = r["instructions_per_element"]["dual_sr"]
+    # 152 SMs x 4 schedulers x 32 lanes x 2.0e9 clocks / n elements per second, 3.125 B each
+    want = 152 * 4 * 32 * 2.0e9 / n * 3.125 / 1e9
+    assert r["peak"]["dY_dual_sr"] == pytest.approx(want)
+    assert r["frac"]["dY_dual_sr"] == pytest.approx(1500.0 / want)
+    # counts taken on other sources are not used; nor without a sampled clock
+    monkeypatch.setattr(bench, "kernel_sources_sha", lambda files: "0" * 16)
+    assert bench.issue_roofline([3000.0, 4000.0, 1500.0], 2000.0) is None
+    monkeypatch.undo()
+    assert bench.issue_roofline([3000.0, 4000.0, 1500.0], None) is None
