@@ -280,6 +280,7 @@ fp4q_status fp4q_gemm_nvfp4(const uint8_t* A, const uint8_t* A_scales, const flo
     const long long v = atoll(e);
     if (v > 0) a.wait_cycles = v;
   }
+  if (const char* e = getenv("FP4Q_TEST_GEMM_SKIP_LOADS")) a.skip_loads = atoi(e) != 0;
   return from_cuda(fp4q::launch_gemm_nvfp4(a, st));
 }
 

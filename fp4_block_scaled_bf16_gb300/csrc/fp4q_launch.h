@@ -58,7 +58,7 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st);
 
 // The native NVFP4 GEMM (gemm_native.cu): UE4M3-scaled E2M1 operands on the
 // tensor cores' block-scaled MMA.  K % 256 == 0; the epilogue-quantisation
-// fields and skip_loads are unused.
+// fields are unused.
 cudaError_t launch_gemm_nvfp4(const GemmArgs& a, cudaStream_t st);
 
 }  // namespace fp4q

@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                       const __grid_constant__ CUtensorMap mapSA, const __grid_constant__ CUtensorMap mapSB,
                       const float* __restrict__ TA, const float* __restrict__ TB, int M, int N, int K,
-                      void* __restrict__ out, int* status, long long budget) {
+                      void* __restrict__ out, int* status, long long budget, int skip_loads) {
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
@@ -228,6 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+          if (skip_loads) continue;   // test hook: consumers' waits run out
           const uint32_t st = sb + s * STAGE;
           mbar_expect_tx(bar_full + 8 * s, STAGE);
           tma_load_2d(st + OFF_A, &mapA, kb * ROWB, am0, bar_full + 8 * s);
@@ -475,7 +476,7 @@ static cudaError_t launch_native_t(const GemmArgs& a, const CUtensorMap& mA, con
   const int ncl = (int)(ntiles < clusters[dev] ? ntiles : clusters[dev]);
   cfg.gridDim = dim3(2u * (unsigned)ncl);
   e = cudaLaunchKernelEx(&cfg, kern, mA, mB, mSA, mSB, a.TA, a.TB, (int)a.M, (int)a.N, (int)a.K, a.out, a.status,
-                         a.wait_cycles);
+                         a.wait_cycles, a.skip_loads ? 1 : 0);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -180,7 +180,8 @@ fp4q_status fp4q_gemm_quantize(const uint8_t* A, const uint8_t* A_scales, const 
  * A_tscale, B_tscale device floats.  Binary32 accumulation; out [M, N] BF16
  * (out_is_f32 == 0) or binary32.  M, N >= 0 (M at most 65535 * 128), K a
  * multiple of 256 (K = 0 writes zeros); FP4Q_ERR_SHAPE otherwise.  Waits are
- * bounded as in fp4q_gemm (FP4Q_TEST_GEMM_WAIT_CYCLES shortens them). */
+ * bounded as in fp4q_gemm, with the same test hooks
+ * (FP4Q_TEST_GEMM_WAIT_CYCLES, FP4Q_TEST_GEMM_SKIP_LOADS). */
 fp4q_status fp4q_gemm_nvfp4(const uint8_t* A, const uint8_t* A_scales, const float* A_tscale,
                             const uint8_t* B, const uint8_t* B_scales, const float* B_tscale,
                             int64_t M, int64_t N, int64_t K, void* out, int out_is_f32, void* stream);

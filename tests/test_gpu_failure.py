@@ -47,6 +47,34 @@ def test_gemm_wait_timeout_is_reported_and_context_survives(lib, monkeypatch):
     assert torch.equal(again, ref)
 
 
+def test_native_gemm_wait_timeout_is_reported_and_context_survives(lib, monkeypatch):
+    """The native NVFP4 GEMM (persistent CTA pairs): with the operand loads
+    withheld every wait of both CTAs runs out, the kernel winds down (no
+    load or MMA in flight, both CTAs through the cluster barrier before
+    TMEM is freed) and reports FP4Q_ERR_TIMEOUT; the next call is exact."""
+    rng = np.random.default_rng(9)
+    M, N, K = 512, 768, 512
+    a = workloads.f32_to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    b = workloads.f32_to_bf16_bits(rng.standard_normal((N, K)).astype(np.float32))
+    qa = lib.quantize(workloads.to_torch_bf16(a).cuda(), fmt=lib.UE4M3)
+    qb = lib.quantize(workloads.to_torch_bf16(b).cuda(), fmt=lib.UE4M3)
+    A, B = (qa.payload_row, qa.scales_row, qa.T), (qb.payload_row, qb.scales_row, qb.T)
+    ref = lib.gemm_nvfp4(*A, *B, dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert lib.fp4q_get_device_status() == lib.OK
+    monkeypatch.setenv("FP4Q_TEST_GEMM_SKIP_LOADS", "1")
+    monkeypatch.setenv("FP4Q_TEST_GEMM_WAIT_CYCLES", "2000000")     # about 1 ms
+    lib.gemm_nvfp4(*A, *B, dtype=torch.float32)
+    assert lib.fp4q_get_device_status() == lib.ERR_TIMEOUT
+    assert lib.fp4q_get_device_status() == lib.OK
+    monkeypatch.delenv("FP4Q_TEST_GEMM_SKIP_LOADS")
+    monkeypatch.delenv("FP4Q_TEST_GEMM_WAIT_CYCLES")
+    again = lib.gemm_nvfp4(*A, *B, dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert lib.fp4q_get_device_status() == lib.OK
+    assert torch.equal(again, ref)
+
+
 def test_nonfinite_input_is_reported(lib):
     x = torch.randn(64, 64, device="cuda").to(torch.bfloat16)
     x[3, 7] = float("inf")
