@@ -97,6 +97,28 @@ def test_shapes_and_ragged_tiles(M, N, K, lib):
     assert_close(C32, C16, full_reference(A, B), K)
 
 
+def test_two_waves_with_ragged_edges(lib):
+    """More 256 x 512 tiles (9 x 10 = 90) than clusters of two CTAs fit on
+    the GPU at once, so a second wave of clusters starts on SMs the first
+    leaves, with ragged last tiles in M and N (the last tile's second N half
+    partly past N) and K a multiple of 256 (scale codes by TMA).  Every element
+    against the oracle's exact e*s operands contracted in binary64."""
+    M, N, K = 2200, 5000, 512
+    a = rand_bits((M + (-M) % 16, K), 11, spread=2.0)[:M]
+    b = rand_bits((N + (-N) % 16, K), 12, spread=2.0)[:N]
+    a = np.ascontiguousarray(np.pad(a, ((0, (-M) % 16), (0, 0))))
+    b = np.ascontiguousarray(np.pad(b, ((0, (-N) % 16), (0, 0))))
+    A, B = quantised(a, lib), quantised(b, lib)
+    A = (A[0][:M].contiguous(), A[1][:M].contiguous(), A[2])
+    B = (B[0][:N].contiguous(), B[1][:N].contiguous(), B[2])
+    C32, C16 = run_both(lib, A, B)
+    pa, sa, ta, pb, sb, tb = _np_ops(A, B)
+    ea, eb = oracle.deq_es(pa, sa), oracle.deq_es(pb, sb)
+    R = ta * tb * (ea @ eb.T)
+    S = ta * tb * (np.abs(ea) @ np.abs(eb).T)
+    assert_close(C32, C16, (R, S), K)
+
+
 @pytest.mark.parametrize("fmt", [0, 1])
 def test_wide_dynamic_range_and_formats(lib, fmt):
     # per-row magnitudes over 1e-8 .. 1e2 (the gradient distribution), SR on A
