@@ -88,6 +88,7 @@ def _load():
             "orc_e2m1_sr_array": (None, [P, P, i64, P]),
             "orc_scale_encode_array": (None, [P, i64, i32, P, P]),
             "orc_sr_uniform_array": (None, [u64, P, i64, u32, P]),
+            "orc_rebias_scales": (None, [P, i64, i64, i32, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -257,6 +258,19 @@ def deq_es(payload, scales, fmt: int = UE5M3) -> np.ndarray:
     out = np.empty((outer, inner), np.float64)
     _load().orc_deq_es_matrix(_ptr(payload), _ptr(scales), outer, inner, int(fmt), _ptr(out))
     return out
+
+
+def rebias_scales(scales, per_row: bool = True):
+    """UE5M3 scale codes [rows, nb] -> (UE4M3 codes [rows, nb], factors
+    [rows] or [1], fits): v = f * v4 exactly for every group (row, or the
+    whole tensor) whose non-zero scales span at most 14 binades."""
+    scales = _c(scales, np.uint8)
+    rows, nb = scales.shape
+    out = np.empty_like(scales)
+    f = np.empty(rows if per_row else 1, np.float32)
+    nofit = np.zeros(1, np.int32)
+    _load().orc_rebias_scales(_ptr(scales), rows, nb, int(bool(per_row)), _ptr(out), _ptr(f), _ptr(nofit))
+    return out, f, not bool(nofit[0])
 
 
 def gemm(A, As, TA, B, Bs, TB, fmt: int = UE5M3, ms=None, ns=None) -> np.ndarray:

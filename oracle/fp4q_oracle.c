@@ -457,6 +457,54 @@ void orc_deq_es_matrix(const uint8_t *payload, const uint8_t *scales, int64_t ou
 }
 
 /* ------------------------------------------------------------------------ */
+/* Re-expressing UE5M3 block scales as UE4M3 scales times a power of two      */
+/* ------------------------------------------------------------------------ */
+
+/* The two scale formats share their 3 mantissa bits, so a group of UE5M3
+ * scales (one row, or the whole tensor) whose non-zero values v all satisfy
+ * e_max - e_min <= 13, e = floor(log2 v), is exactly f * v4 with one factor
+ * f = 2^(e_max - 7) and UE4M3 values v4 = v / f in [2^-6, 240]: the
+ * dequantised operand e * s is unchanged, so the same GEMM can run on the
+ * tensor cores' UE4M3 block scales with f applied to its result.  (This is the
+ * route to native execution that the method's closing argument motivates;
+ * the abstract gives no procedure for it.)  Per group: out_factor = f
+ * (1.0 for a group of zeros); out_codes = the UE4M3 encoding of v / f
+ * (exact: v / f has at most 4 significant bits and lies in UE4M3's normal
+ * range), 0 for v = 0; *nofit is set to 1 when the group's span exceeds 13
+ * (its out_codes and out_factor are then unspecified).  *nofit is never
+ * cleared. */
+void orc_rebias_scales(const uint8_t *codes, int64_t rows, int64_t nb, int per_row,
+                       uint8_t *out_codes, float *out_factor, int *nofit) {
+    const int64_t groups = per_row ? rows : 1;
+    const int64_t glen = per_row ? nb : rows * nb;
+    for (int64_t g = 0; g < groups; ++g) {
+        const uint8_t *c = codes + g * glen;
+        uint8_t *o = out_codes + g * glen;
+        int emax = -1000, emin = 1000;
+        for (int64_t i = 0; i < glen; ++i) {
+            const double v = orc_scale_decode(c[i], ORC_UE5M3);
+            if (v == 0.0) continue;
+            const int e = ilogb(v);
+            if (e > emax) emax = e;
+            if (e < emin) emin = e;
+        }
+        if (emax == -1000) {   /* every scale of the group is zero */
+            out_factor[g] = 1.0f;
+            for (int64_t i = 0; i < glen; ++i) o[i] = 0;
+            continue;
+        }
+        if (emax - emin > 13) *nofit = 1;
+        const double f = ldexp(1.0, emax - 7);
+        out_factor[g] = (float)f;
+        for (int64_t i = 0; i < glen; ++i) {
+            const double v = orc_scale_decode(c[i], ORC_UE5M3);
+            int sat = 0;
+            o[i] = v == 0.0 ? 0 : orc_scale_encode((float)(v / f), ORC_UE4M3, &sat);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Array forms of the scalar steps, so that the tests can sweep many values  */
 /* through exactly the functions above.                                      */
 /* ------------------------------------------------------------------------ */

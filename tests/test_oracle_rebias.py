@@ -1,0 +1,141 @@
+"""Pins of the oracle's re-expression of UE5M3 block scales as UE4M3 scales
+times one power of two per row (or per tensor).
+
+The two formats share their 3 mantissa bits ("UE5M3 FP4 Block Scaling for
+Stable Language Model Pretraining", Abstract: UE5M3 is emulated because the
+tensor cores take E4M3/E8M0 block scales), so a group of UE5M3 scales whose
+non-zero values span at most 14 binades is exactly f * (UE4M3 values): the
+dequantised operand, and hence the GEMM, is unchanged.  Checked here against
+values decoded independently of the oracle's decoder (from the format
+definitions), brute-force binade spans, and the oracle's own dequantised
+operands and GEMM."""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from fp4_block_scaled_bf16_gb300 import workloads
+
+
+def _ue5m3(code):
+    """Exact value of a UE5M3 code from the format definition (bias 15,
+    exponent 0 subnormal, 0xFF not a value)."""
+    e, m = code >> 3, code & 7
+    return Fraction(m, 8) * Fraction(2) ** -14 if e == 0 else (1 + Fraction(m, 8)) * Fraction(2) ** (e - 15)
+
+
+def _ue4m3(code):
+    e, m = code >> 3, code & 7
+    return Fraction(m, 8) * Fraction(2) ** -6 if e == 0 else (1 + Fraction(m, 8)) * Fraction(2) ** (e - 7)
+
+
+V5 = [_ue5m3(c) for c in range(255)]
+V4 = [_ue4m3(c) for c in range(127)]
+
+
+def _binade(v):
+    """floor(log2 v) of a positive rational."""
+    e = 0
+    while v >= 2:
+        v /= 2
+        e += 1
+    while v < 1:
+        v *= 2
+        e -= 1
+    return e
+
+
+def _codes_with_span(rng, rows, nb, span):
+    """UE5M3 codes whose non-zero values span exactly `span` binades per row
+    (some zero codes and subnormal codes included)."""
+    out = np.zeros((rows, nb), np.uint8)
+    for r in range(rows):
+        top = int(rng.integers(span - 16, 17))          # binade of the largest scale
+        binades = rng.integers(top - span, top + 1, nb)
+        binades[0], binades[1] = top, top - span
+        for i, b in enumerate(binades):
+            m = int(rng.integers(0, 7 if b == 16 else 8))      # 0xFF is not a value
+            if b >= -14:
+                out[r, i] = ((b + 15) << 3) | m
+            else:                                        # subnormal: m/8 * 2^-14 with binade b
+                sh = -14 - b                              # 1..3
+                out[r, i] = (1 << (3 - sh)) | (m >> sh) if sh <= 3 else 0
+        zero = rng.random(nb) < 0.1
+        zero[:2] = False
+        out[r, zero] = 0
+    return out
+
+
+@pytest.mark.parametrize("span", [0, 5, 13])
+def test_fitting_rows_are_exact(span):
+    rng = np.random.default_rng(span)
+    codes = _codes_with_span(rng, 64, 48, span)
+    c4, f, fits = oracle.rebias_scales(codes, per_row=True)
+    assert fits
+    for r in range(codes.shape[0]):
+        fr = Fraction(float(f[r]))
+        assert fr.numerator == 1 or fr.denominator == 1    # a power of two
+        for i in range(codes.shape[1]):
+            assert V4[c4[r, i]] * fr == V5[codes[r, i]], (r, i, codes[r, i], c4[r, i])
+            assert c4[r, i] == 0 or 1 <= (c4[r, i] >> 3) <= 14   # UE4M3 normal, never the NaN code
+        # the convention f = 2^(e_max - 7): the row's largest scale lands in
+        # UE4M3's exponent field 14 (values in [128, 256))
+        if (codes[r] != 0).any():
+            assert (c4[r] >> 3).max() == 14
+
+
+def test_fit_flag_is_the_binade_span():
+    rng = np.random.default_rng(7)
+    for span in range(10, 18):
+        codes = _codes_with_span(rng, 8, 32, span)
+        _, _, fits = oracle.rebias_scales(codes, per_row=True)
+        spans = []
+        for r in range(codes.shape[0]):
+            b = [_binade(V5[c]) for c in codes[r] if c != 0]
+            spans.append(max(b) - min(b))
+        assert max(spans) == span
+        assert fits == (span <= 13), span
+
+
+def test_per_tensor_group_and_zero_group():
+    rng = np.random.default_rng(3)
+    codes = _codes_with_span(rng, 16, 32, 6)
+    c4, f, fits = oracle.rebias_scales(codes, per_row=False)
+    allb = [_binade(V5[c]) for c in codes.ravel() if c != 0]
+    assert fits == (max(allb) - min(allb) <= 13) and f.shape == (1,)
+    if fits:
+        fr = Fraction(float(f[0]))
+        assert all(V4[a] * fr == V5[b] for a, b in zip(c4.ravel(), codes.ravel()))
+    z = np.zeros((3, 16), np.uint8)
+    c4, f, fits = oracle.rebias_scales(z, per_row=True)
+    assert fits and (c4 == 0).all() and (f == 1.0).all()
+    # the largest UE5M3 scale (114688 = 1.75 * 2^16) lands on UE4M3 1.75 * 2^7
+    top = np.array([[0xFE, 0xF0]], np.uint8)             # 1.75 * 2^16 and 2^15
+    c4, f, fits = oracle.rebias_scales(top, per_row=True)
+    assert fits and c4[0, 0] == (14 << 3 | 6) and float(f[0]) == 2.0 ** 9
+
+
+def test_quantised_operand_and_gemm_are_unchanged():
+    """deq(payload, UE4M3 codes) * f equals deq(payload, UE5M3 codes), element
+    by element, and so does the binary64 GEMM scaled by the factors."""
+    rng = np.random.default_rng(11)
+    a = workloads.activations(64, 512, 5)
+    b = workloads.weights(96, 512, 6)
+    ta = oracle.tensor_scale(oracle.amax(a)[0])
+    tb = oracle.tensor_scale(oracle.amax(b)[0])
+    pa, sa, _ = oracle.quantize(a, oracle.ROW, ta)
+    pb, sb, _ = oracle.quantize(b, oracle.ROW, tb)
+    sa4, fa, oka = oracle.rebias_scales(sa, per_row=True)
+    sb4, fb, okb = oracle.rebias_scales(sb, per_row=False)
+    assert oka and okb
+    ea5 = oracle.deq_es(pa, sa, oracle.UE5M3)
+    ea4 = oracle.deq_es(pa, sa4, oracle.UE4M3) * fa.astype(np.float64)[:, None]
+    assert np.array_equal(ea4, ea5)
+    eb5 = oracle.deq_es(pb, sb, oracle.UE5M3)
+    eb4 = oracle.deq_es(pb, sb4, oracle.UE4M3) * float(fb[0])
+    assert np.array_equal(eb4, eb5)
+    R5 = oracle.gemm(pa, sa, ta, pb, sb, tb, oracle.UE5M3)
+    R4 = oracle.gemm(pa, sa4, ta, pb, sb4, tb, oracle.UE4M3) * fa.astype(np.float64)[:, None] * float(fb[0])
+    assert np.array_equal(R4, R5)
+    del rng
