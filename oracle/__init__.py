@@ -262,8 +262,9 @@ def deq_es(payload, scales, fmt: int = UE5M3) -> np.ndarray:
 
 def rebias_scales(scales, per_row: bool = True):
     """UE5M3 scale codes [rows, nb] -> (UE4M3 codes [rows, nb], factors
-    [rows] or [1], fits): v = f * v4 exactly for every group (row, or the
-    whole tensor) whose non-zero scales span at most 14 binades."""
+    [rows] or [1], fits): v = f * v4 exactly for every group whose non-zero
+    scales lie in 14 binades -- per row, the row's top 14; per tensor, the
+    fixed binades 3..16 (f = 2^9)."""
     scales = _c(scales, np.uint8)
     rows, nb = scales.shape
     out = np.empty_like(scales)

@@ -461,18 +461,23 @@ void orc_deq_es_matrix(const uint8_t *payload, const uint8_t *scales, int64_t ou
 /* ------------------------------------------------------------------------ */
 
 /* The two scale formats share their 3 mantissa bits, so a group of UE5M3
- * scales (one row, or the whole tensor) whose non-zero values v all satisfy
- * e_max - e_min <= 13, e = floor(log2 v), is exactly f * v4 with one factor
- * f = 2^(e_max - 7) and UE4M3 values v4 = v / f in [2^-6, 240]: the
+ * scales whose non-zero values v all lie in 14 consecutive binades,
+ * e = floor(log2 v) in [e_top - 13, e_top], is exactly f * v4 with one factor
+ * f = 2^(e_top - 7) and UE4M3 values v4 = v / f in [2^-6, 240]: the
  * dequantised operand e * s is unchanged, so the same GEMM can run on the
  * tensor cores' UE4M3 block scales with f applied to its result.  (This is the
  * route to native execution that the method's closing argument motivates;
- * the abstract gives no procedure for it.)  Per group: out_factor = f
- * (1.0 for a group of zeros); out_codes = the UE4M3 encoding of v / f
- * (exact: v / f has at most 4 significant bits and lies in UE4M3's normal
- * range), 0 for v = 0; *nofit is set to 1 when the group's span exceeds 13
- * (its out_codes and out_factor are then unspecified).  *nofit is never
- * cleared. */
+ * the abstract gives no procedure for it.)
+ *   per_row != 0: each row is a group, e_top = the largest binade of the
+ *     row's non-zero scales (a row of zeros: f = 1);
+ *   per_row == 0: the whole tensor is one group with the fixed e_top = 16,
+ *     the binade of the largest finite UE5M3 scale -- where the tensor scale
+ *     puts the tensor's own amax -- so f = 2^9 and the group fits when every
+ *     non-zero scale lies in binades 3..16.
+ * out_factor[g] = f (one per row, or one); out_codes = the UE4M3 encoding of
+ * v / f (exact: at most 4 significant bits, UE4M3's normal range), 0 for
+ * v = 0; *nofit is set to 1 when a group does not fit (its codes and factor
+ * are then unspecified).  *nofit is never cleared. */
 void orc_rebias_scales(const uint8_t *codes, int64_t rows, int64_t nb, int per_row,
                        uint8_t *out_codes, float *out_factor, int *nofit) {
     const int64_t groups = per_row ? rows : 1;
@@ -489,12 +494,13 @@ void orc_rebias_scales(const uint8_t *codes, int64_t rows, int64_t nb, int per_r
             if (e < emin) emin = e;
         }
         if (emax == -1000) {   /* every scale of the group is zero */
-            out_factor[g] = 1.0f;
+            out_factor[g] = per_row ? 1.0f : 512.0f;
             for (int64_t i = 0; i < glen; ++i) o[i] = 0;
             continue;
         }
-        if (emax - emin > 13) *nofit = 1;
-        const double f = ldexp(1.0, emax - 7);
+        const int etop = per_row ? emax : 16;
+        if (emin < etop - 13 || emax > etop) *nofit = 1;
+        const double f = ldexp(1.0, etop - 7);
         out_factor[g] = (float)f;
         for (int64_t i = 0; i < glen; ++i) {
             const double v = orc_scale_decode(c[i], ORC_UE5M3);

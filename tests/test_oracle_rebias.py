@@ -98,22 +98,33 @@ def test_fit_flag_is_the_binade_span():
         assert fits == (span <= 13), span
 
 
-def test_per_tensor_group_and_zero_group():
+def test_per_tensor_window_and_zero_group():
+    """Per tensor: the fixed window of binades 3..16, f = 2^9, decided code by
+    code."""
     rng = np.random.default_rng(3)
-    codes = _codes_with_span(rng, 16, 32, 6)
-    c4, f, fits = oracle.rebias_scales(codes, per_row=False)
-    allb = [_binade(V5[c]) for c in codes.ravel() if c != 0]
-    assert fits == (max(allb) - min(allb) <= 13) and f.shape == (1,)
-    if fits:
-        fr = Fraction(float(f[0]))
-        assert all(V4[a] * fr == V5[b] for a, b in zip(c4.ravel(), codes.ravel()))
+    for top, span in ((16, 6), (16, 13), (12, 9), (16, 14), (10, 9), (2, 0)):
+        codes = _codes_with_span(np.random.default_rng(top * 100 + span), 16, 32, span)
+        # move every row's window so that its top binade is `top`
+        c = codes.astype(np.int32)
+        e = c >> 3
+        shift = top - max(_binade(V5[x]) for x in codes.ravel() if x != 0)
+        normal = (c != 0) & (e > 0)
+        codes = np.where(normal & (e + shift >= 1) & (e + shift <= 31), ((e + shift) << 3) | (c & 7), c)
+        codes = np.where(codes == 0xFF, 0xFE, codes).astype(np.uint8)
+        c4, f, fits = oracle.rebias_scales(codes, per_row=False)
+        allb = [_binade(V5[x]) for x in codes.ravel() if x != 0]
+        assert f.shape == (1,) and float(f[0]) == 512.0
+        assert fits == (min(allb) >= 3 and max(allb) <= 16), (top, span)
+        if fits:
+            assert all(V4[a] * 512 == V5[b] for a, b in zip(c4.ravel(), codes.ravel()))
     z = np.zeros((3, 16), np.uint8)
     c4, f, fits = oracle.rebias_scales(z, per_row=True)
     assert fits and (c4 == 0).all() and (f == 1.0).all()
     # the largest UE5M3 scale (114688 = 1.75 * 2^16) lands on UE4M3 1.75 * 2^7
     top = np.array([[0xFE, 0xF0]], np.uint8)             # 1.75 * 2^16 and 2^15
-    c4, f, fits = oracle.rebias_scales(top, per_row=True)
-    assert fits and c4[0, 0] == (14 << 3 | 6) and float(f[0]) == 2.0 ** 9
+    for per_row in (True, False):
+        c4, f, fits = oracle.rebias_scales(top, per_row=per_row)
+        assert fits and c4[0, 0] == (14 << 3 | 6) and float(f[0]) == 2.0 ** 9
 
 
 def test_quantised_operand_and_gemm_are_unchanged():
