@@ -18,13 +18,14 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libfp4q.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["fp4q_api.cu", "quantize.cu", "gemm.cu", "gemm_native.cu"]
+SOURCES = ["fp4q_api.cu", "quantize.cu", "gemm.cu", "gemm_native.cu", "rebias.cu"]
 HEADERS = ["fp4q_device.cuh", "fp4q_launch.h", "fp4q_pipeline.cuh", "fp4q_tcgen05.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
           "--expt-relaxed-constexpr"]
 # the quantiser's bytes must be a pure function of its input: no contraction
-PER_FILE = {"quantize.cu": ["-fmad=false"], "fp4q_api.cu": [], "gemm.cu": [], "gemm_native.cu": []}
+PER_FILE = {"quantize.cu": ["-fmad=false"], "fp4q_api.cu": [], "gemm.cu": [], "gemm_native.cu": [],
+            "rebias.cu": []}
 # FP4Q_NVTX=1: every C entry point becomes an NVTX range (header-only NVTX 3)
 if os.environ.get("FP4Q_NVTX") == "1":
     PER_FILE["fp4q_api.cu"] = ["-DFP4Q_NVTX"]

@@ -160,8 +160,9 @@ static fp4q_status gemm_common(const uint8_t* A, const uint8_t* A_scales, const 
                                const uint8_t* B, const uint8_t* B_scales, const float* B_tscale,
                                int64_t M, int64_t N, int64_t K, fp4q_scale_fmt fmt, void* out,
                                int out_is_f32, const float* c_tscale, uint8_t* qpay, uint8_t* qsc,
-                               float* qamax, void* stream) {
+                               float* qamax, void* stream, const int* run_if = nullptr) {
   if (!valid_fmt(fmt)) return FP4Q_ERR_ARG;
+  if (run_if && !aligned4(run_if)) return FP4Q_ERR_ALIGN;
   if (M < 0 || N < 0 || K < 0 || K % 64 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
     return FP4Q_ERR_SHAPE;
   if ((M + 255) / 256 > 65535) return FP4Q_ERR_SHAPE;   // 256-row tiles on the grid's y dimension
@@ -193,6 +194,7 @@ static fp4q_status gemm_common(const uint8_t* A, const uint8_t* A_scales, const 
   int* status = status_ptr();
   if (!status) return FP4Q_ERR_CUDA;
   fp4q::GemmArgs a;
+  a.run_if = run_if;
   a.TC = c_tscale;
   a.qpay = qpay;
   a.qsc = qsc;
@@ -242,10 +244,23 @@ fp4q_status fp4q_gemm_quantize(const uint8_t* A, const uint8_t* A_scales, const 
                      c_tscale, out_payload, out_scales, out_amax, stream);
 }
 
-fp4q_status fp4q_gemm_nvfp4(const uint8_t* A, const uint8_t* A_scales, const float* A_tscale,
-                            const uint8_t* B, const uint8_t* B_scales, const float* B_tscale, int64_t M,
-                            int64_t N, int64_t K, void* out, int out_is_f32, void* stream) {
-  FP4Q_RANGE("fp4q_gemm_nvfp4");
+fp4q_status fp4q_gemm_if(const uint8_t* A, const uint8_t* A_scales, const float* A_tscale, const uint8_t* B,
+                         const uint8_t* B_scales, const float* B_tscale, int64_t M, int64_t N, int64_t K,
+                         fp4q_scale_fmt fmt, const int* run_if_set, void* out, int out_is_f32, void* stream) {
+  FP4Q_RANGE("fp4q_gemm_if");
+  if (!run_if_set) return FP4Q_ERR_ARG;
+  return gemm_common(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K, fmt, out, out_is_f32,
+                     nullptr, nullptr, nullptr, nullptr, stream, run_if_set);
+}
+
+}  // extern "C"
+
+namespace {
+
+fp4q_status gemm_native_common(const uint8_t* A, const uint8_t* A_scales, const float* A_factor,
+                               const float* A_tscale, const uint8_t* B, const uint8_t* B_scales,
+                               const float* B_factor, const float* B_tscale, int64_t M, int64_t N,
+                               int64_t K, const int* skip_if, void* out, int out_is_f32, void* stream) {
   if (M < 0 || N < 0 || K < 0 || K % 256 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
     return FP4Q_ERR_SHAPE;
   if ((M + 127) / 128 > 65535) return FP4Q_ERR_SHAPE;   // 128-row tiles on the grid's y dimension
@@ -256,7 +271,8 @@ fp4q_status fp4q_gemm_nvfp4(const uint8_t* A, const uint8_t* A_scales, const flo
   if (K == 0) return from_cuda(cudaMemsetAsync(out, 0, (size_t)M * N * (out_is_f32 ? 4 : 2), st));
   if (!A || !A_scales || !A_tscale || !B || !B_scales || !B_tscale) return FP4Q_ERR_ARG;
   if (!aligned16(A) || !aligned16(B) || !aligned16(A_scales) || !aligned16(B_scales) ||
-      !aligned4(A_tscale) || !aligned4(B_tscale))
+      !aligned4(A_tscale) || !aligned4(B_tscale) || !aligned4(A_factor) || !aligned4(B_factor) ||
+      !aligned4(skip_if))
     return FP4Q_ERR_ALIGN;
   int* status = status_ptr();
   if (!status) return FP4Q_ERR_CUDA;
@@ -267,6 +283,9 @@ fp4q_status fp4q_gemm_nvfp4(const uint8_t* A, const uint8_t* A_scales, const flo
   a.Bs = B_scales;
   a.TA = A_tscale;
   a.TB = B_tscale;
+  a.fa = A_factor;
+  a.fb = B_factor;
+  a.skip_if = skip_if;
   a.M = M;
   a.N = N;
   a.K = K;
@@ -282,6 +301,45 @@ fp4q_status fp4q_gemm_nvfp4(const uint8_t* A, const uint8_t* A_scales, const flo
   }
   if (const char* e = getenv("FP4Q_TEST_GEMM_SKIP_LOADS")) a.skip_loads = atoi(e) != 0;
   return from_cuda(fp4q::launch_gemm_nvfp4(a, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+fp4q_status fp4q_gemm_nvfp4(const uint8_t* A, const uint8_t* A_scales, const float* A_tscale,
+                            const uint8_t* B, const uint8_t* B_scales, const float* B_tscale, int64_t M,
+                            int64_t N, int64_t K, void* out, int out_is_f32, void* stream) {
+  FP4Q_RANGE("fp4q_gemm_nvfp4");
+  return gemm_native_common(A, A_scales, nullptr, A_tscale, B, B_scales, nullptr, B_tscale, M, N, K, nullptr,
+                            out, out_is_f32, stream);
+}
+
+fp4q_status fp4q_gemm_nvfp4_rebiased(const uint8_t* A, const uint8_t* A_scales4, const float* A_factor,
+                                     const float* A_tscale, const uint8_t* B, const uint8_t* B_scales4,
+                                     const float* B_factor, const float* B_tscale, int64_t M, int64_t N,
+                                     int64_t K, const int* skip_if_set, void* out, int out_is_f32,
+                                     void* stream) {
+  FP4Q_RANGE("fp4q_gemm_nvfp4_rebiased");
+  if (M > 0 && N > 0 && K > 0 && (!A_factor || !B_factor)) return FP4Q_ERR_ARG;
+  return gemm_native_common(A, A_scales4, A_factor, A_tscale, B, B_scales4, B_factor, B_tscale, M, N, K,
+                            skip_if_set, out, out_is_f32, stream);
+}
+
+fp4q_status fp4q_rebias_scales(const uint8_t* scales, int64_t rows, int64_t nblocks, int per_row,
+                               uint8_t* out_scales, float* out_factor, int* inout_nofit, void* stream) {
+  FP4Q_RANGE("fp4q_rebias_scales");
+  if (rows < 0 || nblocks < 0 || nblocks % 16 || nblocks > INT32_MAX) return FP4Q_ERR_SHAPE;
+  if (!out_factor || !inout_nofit) return FP4Q_ERR_ARG;
+  if (rows > 0 && nblocks > 0 && (!scales || !out_scales)) return FP4Q_ERR_ARG;
+  if (!aligned16(scales) || !aligned16(out_scales) || !aligned4(out_factor) || !aligned4(inout_nofit))
+    return FP4Q_ERR_ALIGN;
+  if (scales && out_scales && rows > 0 && nblocks > 0) {
+    const uint8_t *a0 = scales, *a1 = scales + rows * nblocks, *b0 = out_scales, *b1 = out_scales + rows * nblocks;
+    if (a0 < b1 && b0 < a1) return FP4Q_ERR_ARG;   // the input is read after outputs are written
+  }
+  return from_cuda(fp4q::launch_rebias(scales, rows, nblocks, per_row != 0, out_scales, out_factor,
+                                       inout_nofit, static_cast<cudaStream_t>(stream)));
 }
 
 fp4q_status fp4q_get_device_status(int* out, void* stream) {

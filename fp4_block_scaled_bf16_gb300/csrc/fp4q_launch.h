@@ -1,6 +1,7 @@
 // fp4q_launch.h -- host-side launch interface between the C ABI (fp4q_api.cu)
-// and the kernel translation units (quantize.cu, gemm.cu).  Internal to
-// libfp4q.so; arguments are validated by the ABI layer before they get here.
+// and the kernel translation units (quantize.cu, gemm.cu, gemm_native.cu,
+// rebias.cu).  Internal to libfp4q.so; arguments are validated by the ABI
+// layer before they get here.
 #pragma once
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -46,6 +47,12 @@ struct GemmArgs {
   float* qamax = nullptr;           // nullable: max |bf16(C)|
   long long wait_cycles;            // budget of every pipeline wait (clock64 cycles)
   bool skip_loads;                  // test hook: the producer issues no loads
+  // native GEMM, rebiased operands: per-A-row and per-B-tensor power-of-two
+  // factors (nullable), and a device flag that makes the launch a no-op
+  const float *fa = nullptr, *fb = nullptr;
+  const int* skip_if = nullptr;
+  // emulated GEMM: a device flag without which the launch is a no-op (nullable)
+  const int* run_if = nullptr;
 };
 
 // The driver's cuTensorMapEncodeTiled (looked up once through the runtime);
@@ -60,5 +67,11 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st);
 // tensor cores' block-scaled MMA.  K % 256 == 0; the epilogue-quantisation
 // fields are unused.
 cudaError_t launch_gemm_nvfp4(const GemmArgs& a, cudaStream_t st);
+
+// UE5M3 scale codes [rows, nb] -> UE4M3 codes and power-of-two factors
+// (rebias.cu): per row (factor[rows]) or for the whole tensor (factor[1]);
+// ORs 1 into *nofit when a group does not fit.  nb % 16 == 0.
+cudaError_t launch_rebias(const uint8_t* scales, int64_t rows, int64_t nb, bool per_row, uint8_t* out,
+                          float* factor, int* nofit, cudaStream_t st);
 
 }  // namespace fp4q

@@ -160,6 +160,31 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
                                                   long long budget) {
   return mbar_try_wait_cluster(bar, parity) || mbar_wait_cluster_slow(bar, parity, abort_flag, budget);
 }
+// A device flag read once for the pair, before anything else the pair does:
+// once both CTAs are known to run (a first cluster barrier, which is what
+// makes the peer's shared memory addressable), thread 0 of rank 0 loads *flag
+// and writes the value into the word at shared address `slot` in both CTAs;
+// after a second barrier each thread reads its own CTA's copy.  Both CTAs
+// therefore take the same branch even if the flag changes while the kernel
+// runs, and either may return at once without touching the other's memory
+// again.  Every thread of both CTAs calls it.
+__device__ __forceinline__ int pair_read_flag(const int* flag, uint32_t slot) {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
+  if (cluster_rank() == 0 && threadIdx.x == 0) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    asm volatile(
+        "{\n\t.reg .b32 ra;\n\t"
+        "st.shared.b32 [%0], %1;\n\t"
+        "mapa.shared::cluster.u32 ra, %0, 1;\n\t"
+        "st.shared::cluster.b32 [ra], %1;\n\t}" ::"r"(slot), "r"(v)
+        : "memory");
+  }
+  cluster_sync();
+  int v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(slot) : "memory");
+  return v;
+}
 // TMEM of the pair: one warp of each CTA allocates (and later frees) the
 // same columns in both CTAs' TMEM.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {

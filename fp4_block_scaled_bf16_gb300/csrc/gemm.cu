@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int fmt, void* __restrict__ out, int* status, long long budget, int skip_loads,
                 const float* __restrict__ TC, uint8_t* __restrict__ qpay, uint8_t* __restrict__ qsc,
                 float* qamax, const __grid_constant__ CUtensorMap mapQP,
-                const __grid_constant__ CUtensorMap mapQS, int qstaged) {
+                const __grid_constant__ CUtensorMap mapQS, int qstaged, const int* run_if) {
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
@@ -202,6 +202,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int OFF_TMEM = OFF_BAR + 8 * NBARS;
   constexpr int OFF_ABORT = OFF_TMEM + 8;
   constexpr int OFF_TAB = OFF_ABORT + 8;
+  // conditional launch (fp4q_gemm_if): both CTAs return before any setup
+  // unless the device flag is set
+  if (run_if && !pair_read_flag(run_if, sb + OFF_ABORT + 4)) return;
   ScaleTab* tab = reinterpret_cast<ScaleTab*>(smem + OFF_TAB);
   const uint32_t bar_raw_full = sb + OFF_BAR;
   const uint32_t bar_raw_empty = bar_raw_full + 8 * S_RAW;
@@ -648,7 +651,7 @@ static cudaError_t launch_gemm_t(const GemmArgs& a, const CUtensorMap& mapA, con
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, kern, mapA, mapB, mapAs, mapBs, mapC, tma_store ? 1 : 0, a.As, a.Bs, a.TA, a.TB,
                          (int)a.M, (int)a.N, (int)a.K, a.fmt, a.out, a.status, a.wait_cycles,
-                         a.skip_loads ? 1 : 0, a.TC, a.qpay, a.qsc, a.qamax, mapQP, mapQS, qstaged ? 1 : 0);
+                         a.skip_loads ? 1 : 0, a.TC, a.qpay, a.qsc, a.qamax, mapQP, mapQS, qstaged ? 1 : 0, a.run_if);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -42,6 +42,11 @@
 //               MMA waits until both CTAs' epilogues have read the last one.
 //   warps 4..11 epilogue: TMEM -> registers (64 columns per lane at a time)
 //               -> alpha -> BF16 or FP32 -> global.
+// Rebiased mode (fp4q_gemm_nvfp4_rebiased): UE5M3 block scales re-expressed
+// as UE4M3 codes times a power of two, per A row (fa) and for all of B (fb);
+// the epilogue multiplies each row by T_A T_B fb fa[row], exact products of
+// powers of two.  A device flag (skip_if) read once per pair makes the whole
+// launch a no-op, so that the caller need not read it on the host.
 // Every wait is bounded; a wait that runs out latches FP4Q_ERR_TIMEOUT and
 // the CTA winds down once the loads and MMAs it issued have completed; both
 // CTAs meet at a cluster barrier before the pair's TMEM is freed.
@@ -169,10 +174,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                       const __grid_constant__ CUtensorMap mapSA, const __grid_constant__ CUtensorMap mapSB,
                       const float* __restrict__ TA, const float* __restrict__ TB, int M, int N, int K,
-                      void* __restrict__ out, int* status, long long budget, int skip_loads) {
+                      void* __restrict__ out, int* status, long long budget, int skip_loads,
+                      const float* __restrict__ fa, const float* __restrict__ fb, const int* skip_if) {
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
+  if (skip_if && pair_read_flag(skip_if, sb + OFF_ABORT + 4)) return;   // both CTAs, before any setup
   const uint32_t bar_full = sb + OFF_BAR;            // TMA bytes of stage s landed (this CTA)
   const uint32_t bar_empty = bar_full + 8 * S;       // stage s MMAs completed
   const uint32_t bar_sf = bar_empty + 8 * S;         // slot t scales in both CTAs' TMEM (rank 0)
@@ -342,7 +349,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 128 h .. 128 h + 127 (h = (w - 4) / 4), 64 at a time; TMEM is released
     // to the next tile's MMAs as soon as the last 64 are in registers.
     const int q = warp & 3, h = (warp - kEpiWarp0) >> 2;
-    const float alpha = __fmul_rn(__ldg(TA), __ldg(TB));
+    float alpha0 = __fmul_rn(__ldg(TA), __ldg(TB));
+    if (fb) alpha0 = __fmul_rn(alpha0, __ldg(fb));   // a power of two: exact
     int j = 0;
     for (int tile = cid; tile < ntiles; tile += ncl, ++j) {
       if (!mbar_wait(bar_acc_full, (uint32_t)(j & 1), abort_flag, budget)) {
@@ -355,6 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = am0 + 32 * q + lane;
       const int cbase = n0 + 128 * h;
       const bool live = row < M && cbase < N;
+      const float alpha = (fa && row < M) ? __fmul_rn(alpha0, __ldg(fa + row)) : alpha0;
       const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(128 * h);
       if (F32OUT) {
         // 64 columns at a time; TMEM released (the next tile's MMAs may
@@ -476,7 +485,7 @@ static cudaError_t launch_native_t(const GemmArgs& a, const CUtensorMap& mA, con
   const int ncl = (int)(ntiles < clusters[dev] ? ntiles : clusters[dev]);
   cfg.gridDim = dim3(2u * (unsigned)ncl);
   e = cudaLaunchKernelEx(&cfg, kern, mA, mB, mSA, mSB, a.TA, a.TB, (int)a.M, (int)a.N, (int)a.K, a.out, a.status,
-                         a.wait_cycles, a.skip_loads ? 1 : 0);
+                         a.wait_cycles, a.skip_loads ? 1 : 0, a.fa, a.fb, a.skip_if);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -1,0 +1,163 @@
+// rebias.cu -- UE5M3 block-scale codes re-expressed as UE4M3 codes times a
+// power of two, so that a UE5M3-scaled GEMM can run exactly on the tensor
+// cores' UE4M3 block-scaled MMA (gemm_native.cu) with the power of two applied
+// to its result.
+//
+// Method: "UE5M3 FP4 Block Scaling for Stable Language Model Pretraining",
+// Abstract -- UE5M3 is emulated because the tensor cores take only E4M3/E8M0
+// block scales.  The two scale formats share their 3 mantissa bits: a group of
+// UE5M3 scales whose non-zero values lie in 14 consecutive binades
+// [e_top - 13, e_top] equals f * (UE4M3 values) with f = 2^(e_top - 7), the
+// largest landing in UE4M3's exponent field 14.  Groups:
+//   per row   -- e_top is the row's largest binade (one warp per row: a
+//                warp-wide max and min over the row's codes, then the codes);
+//   per tensor -- e_top = 16, the binade of the largest finite UE5M3 scale,
+//                where the tensor scale puts the tensor's amax: f = 2^9 and
+//                every code is checked on its own.
+// A group that does not fit sets *nofit (never cleared here); its codes and
+// factor are then unspecified.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fp4q_device.cuh"
+#include "fp4q_launch.h"
+
+namespace fp4q {
+namespace rebias {
+
+constexpr int kNone = -1000;   // binade of "no non-zero scale"
+
+// Binade e = floor(log2 v) of a non-zero UE5M3 code and its 3 mantissa bits
+// once normalised (a subnormal m/8 * 2^-14 has at most 3 significant bits).
+__device__ __forceinline__ int binade(uint32_t c, uint32_t& mn) {
+  const uint32_t E = c >> 3, m = c & 7u;
+  if (E != 0) {
+    mn = m;
+    return (int)E - 15;
+  }
+  const int lz = 31 - __clz((int)m);   // floor(log2 m), m in 1..7
+  mn = (m << (3 - lz)) & 7u;
+  return lz - 17;
+}
+
+// The UE4M3 code of v / 2^(etop - 7) for a non-zero UE5M3 code; 0 stays 0.
+// Outside the group's window the exponent field is clamped (the group does
+// not fit and its codes are unspecified).
+__device__ __forceinline__ uint32_t recode(uint32_t c, int etop) {
+  if (c == 0) return 0;
+  uint32_t mn;
+  const int e = binade(c, mn);
+  const int f = min(max(e - etop + 14, 0), 15);
+  return ((uint32_t)f << 3) | mn;
+}
+
+__device__ __forceinline__ float pow2(int k) { return __int_as_float((k + 127) << 23); }
+
+__device__ __forceinline__ uint32_t word_at(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// One warp per row (grid-stride over rows); nb % 16 == 0, rows 16-byte aligned.
+__global__ void __launch_bounds__(256) rebias_rows_kernel(const uint8_t* __restrict__ in, int64_t rows, int nb,
+                                                          uint8_t* __restrict__ out, float* __restrict__ factor,
+                                                          int* nofit) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int chunks = nb >> 4;
+  for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += nwarps) {
+    const uint4* src = reinterpret_cast<const uint4*>(in + r * nb);
+    int emax = kNone, emin = -kNone;
+    for (int j = lane; j < chunks; j += 32) {
+      const uint4 v = __ldg(src + j);
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const uint32_t word = word_at(v, w);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const uint32_t c = (word >> (8 * b)) & 0xFFu;
+          if (c != 0) {
+            uint32_t mn;
+            const int e = binade(c, mn);
+            emax = max(emax, e);
+            emin = min(emin, e);
+          }
+        }
+      }
+    }
+    emax = __reduce_max_sync(0xFFFFFFFFu, emax);
+    emin = __reduce_min_sync(0xFFFFFFFFu, emin);
+    const bool any = emax != kNone;
+    if (lane == 0) {
+      factor[r] = any ? pow2(emax - 7) : 1.0f;
+      if (any && emin < emax - 13) atomicOr(nofit, 1);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(out + r * nb);
+    for (int j = lane; j < chunks; j += 32) {
+      const uint4 v = __ldg(src + j);
+      uint32_t o[4];
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const uint32_t word = word_at(v, w);
+        o[w] = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) o[w] |= recode((word >> (8 * b)) & 0xFFu, emax) << (8 * b);
+      }
+      dst[j] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
+// The whole tensor with the fixed window (binades 3..16, factor 2^9),
+// grid-stride over 16-code chunks.
+__global__ void __launch_bounds__(256) rebias_tensor_kernel(const uint4* __restrict__ in, int64_t chunks,
+                                                            uint4* __restrict__ out, float* __restrict__ factor,
+                                                            int* nofit) {
+  constexpr int kTop = 16;
+  if (blockIdx.x == 0 && threadIdx.x == 0) factor[0] = pow2(kTop - 7);
+  bool bad = false;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < chunks; j += stride) {
+    const uint4 v = __ldg(in + j);
+    uint32_t o[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const uint32_t word = word_at(v, w);
+      o[w] = 0;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const uint32_t c = (word >> (8 * b)) & 0xFFu;
+        if (c != 0) {
+          uint32_t mn;
+          bad |= binade(c, mn) < kTop - 13;   // above the top is impossible: 0xFE is binade 16
+        }
+        o[w] |= recode(c, kTop) << (8 * b);
+      }
+    }
+    out[j] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (__any_sync(0xFFFFFFFFu, bad) && (threadIdx.x & 31) == 0) atomicOr(nofit, 1);
+}
+
+}  // namespace rebias
+
+cudaError_t launch_rebias(const uint8_t* scales, int64_t rows, int64_t nb, bool per_row, uint8_t* out,
+                          float* factor, int* nofit, cudaStream_t st) {
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (per_row) {
+    if (rows == 0) return cudaSuccess;
+    const int64_t want = (rows + 7) / 8;   // eight rows (warps) per 256-thread block
+    const int grid = (int)(want < (int64_t)sms * 8 ? want : (int64_t)sms * 8);
+    rebias::rebias_rows_kernel<<<grid, 256, 0, st>>>(scales, rows, (int)nb, out, factor, nofit);
+  } else {
+    const int64_t chunks = rows * nb / 16;
+    const int64_t want = (chunks + 255) / 256;
+    int grid = (int)(want < (int64_t)sms * 8 ? want : (int64_t)sms * 8);
+    if (grid < 1) grid = 1;   // the factor is written even for an empty tensor
+    rebias::rebias_tensor_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const uint4*>(scales), chunks,
+                                                       reinterpret_cast<uint4*>(out), factor, nofit);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace fp4q

@@ -26,7 +26,8 @@ UE5M3, UE4M3 = 0, 1
 
 # every symbol include/fp4q.h declares
 EXPORTS = ("fp4q_amax", "fp4q_tensor_scale", "fp4q_quantize", "fp4q_dequantize", "fp4q_gemm",
-           "fp4q_gemm_quantize", "fp4q_gemm_nvfp4", "fp4q_get_device_status", "fp4q_status_string")
+           "fp4q_gemm_quantize", "fp4q_gemm_nvfp4", "fp4q_rebias_scales", "fp4q_gemm_nvfp4_rebiased",
+           "fp4q_gemm_if", "fp4q_get_device_status", "fp4q_status_string")
 
 
 class Fp4qError(RuntimeError):
@@ -50,6 +51,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fp4q_gemm.argtypes = [P, P, P, P, P, P, i64, i64, i64, i32, P, i32, P]
     lib.fp4q_gemm_quantize.argtypes = [P, P, P, P, P, P, i64, i64, i64, i32, P, P, P, P, P, P]
     lib.fp4q_gemm_nvfp4.argtypes = [P, P, P, P, P, P, i64, i64, i64, P, i32, P]
+    lib.fp4q_rebias_scales.argtypes = [P, i64, i64, i32, P, P, P, P]
+    lib.fp4q_gemm_nvfp4_rebiased.argtypes = [P, P, P, P, P, P, P, P, i64, i64, i64, P, P, i32, P]
+    lib.fp4q_gemm_if.argtypes = [P, P, P, P, P, P, i64, i64, i64, i32, P, P, i32, P]
     lib.fp4q_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), P]
     lib.fp4q_status_string.argtypes = [i32]
     lib.fp4q_status_string.restype = ctypes.c_char_p
@@ -234,6 +238,54 @@ def fp4q_gemm_nvfp4(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K, out) 
         M, N, K, _ptr(out), int(f32), _stream()))
 
 
+def fp4q_rebias_scales(scales, rows, nblocks, per_row, out_scales, out_factor, inout_nofit) -> None:
+    """UE5M3 codes -> UE4M3 codes times a power of two per row (per_row) or for
+    the tensor; ORs 1 into inout_nofit when a group does not fit."""
+    if rows < 0 or nblocks < 0 or nblocks % 16:
+        raise ValueError(f"rows >= 0 and nblocks a multiple of 16 required, got {rows}, {nblocks}")
+    _mat(scales, "scales", (rows, nblocks), torch.uint8)
+    _mat(out_scales, "out_scales", (rows, nblocks), torch.uint8)
+    _scalar(out_factor, "out_factor", rows if per_row else 1)
+    _scalar(inout_nofit, "inout_nofit", 1, torch.int32)
+    _on_device(("scales", scales), ("out_scales", out_scales), ("out_factor", out_factor),
+               ("inout_nofit", inout_nofit))
+    _check("fp4q_rebias_scales", _lib.fp4q_rebias_scales(
+        _ptr(scales), rows, nblocks, int(bool(per_row)), _ptr(out_scales), _ptr(out_factor),
+        _ptr(inout_nofit), _stream()))
+
+
+def fp4q_gemm_nvfp4_rebiased(A, A_scales4, A_factor, A_tscale, B, B_scales4, B_factor, B_tscale,
+                             M, N, K, skip_if_set, out) -> None:
+    """Native block-scaled GEMM on rebiased operands (per-row A factor,
+    per-tensor B factor); a no-op when the device int skip_if_set is set."""
+    ops = _gemm_operands(A, A_scales4, A_tscale, B, B_scales4, B_tscale, M, N, K)
+    _scalar(A_factor, "A_factor", M)
+    _scalar(B_factor, "B_factor")
+    if skip_if_set is not None:
+        _scalar(skip_if_set, "skip_if_set", 1, torch.int32)
+    _out_dtype(out)
+    _mat(out, "out", (M, N), out.dtype)
+    _on_device(*ops, ("A_factor", A_factor), ("B_factor", B_factor), ("skip_if_set", skip_if_set),
+               ("out", out))
+    f32 = out.dtype == torch.float32
+    _check("fp4q_gemm_nvfp4_rebiased", _lib.fp4q_gemm_nvfp4_rebiased(
+        _ptr(A), _ptr(A_scales4), _ptr(A_factor), _ptr(A_tscale), _ptr(B), _ptr(B_scales4),
+        _ptr(B_factor), _ptr(B_tscale), M, N, K, _ptr(skip_if_set), _ptr(out), int(f32), _stream()))
+
+
+def fp4q_gemm_if(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K, fmt, run_if_set, out) -> None:
+    """fp4q_gemm, run only when the device int run_if_set is non-zero."""
+    ops = _gemm_operands(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K)
+    _scalar(run_if_set, "run_if_set", 1, torch.int32)
+    _out_dtype(out)
+    _mat(out, "out", (M, N), out.dtype)
+    _on_device(*ops, ("run_if_set", run_if_set), ("out", out))
+    f32 = out.dtype == torch.float32
+    _check("fp4q_gemm_if", _lib.fp4q_gemm_if(
+        _ptr(A), _ptr(A_scales), _ptr(A_tscale), _ptr(B), _ptr(B_scales), _ptr(B_tscale),
+        M, N, K, fmt, _ptr(run_if_set), _ptr(out), int(f32), _stream()))
+
+
 def fp4q_gemm_quantize(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K, fmt, c_tscale,
                        out_bf16, out_payload, out_scales, out_amax=None) -> None:
     ops = _gemm_operands(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K)
@@ -350,4 +402,36 @@ def gemm(A, A_scales, A_tscale, B, B_scales, B_tscale, fmt: int = UE5M3,
     if out is None:
         out = torch.empty((M, N), dtype=dtype, device=A.device)
     fp4q_gemm(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K, fmt, out)
+    return out
+
+
+def rebias_scales(scales, per_row: bool = True, nofit: torch.Tensor | None = None):
+    """fp4q_rebias_scales with allocated outputs: (UE4M3 codes, factors,
+    nofit).  A given `nofit` (int32 [1]) is OR-ed into, not cleared."""
+    R, nb = scales.shape
+    codes = torch.empty_like(scales)
+    factor = torch.empty(R if per_row else 1, dtype=torch.float32, device=scales.device)
+    if nofit is None:
+        nofit = torch.zeros(1, dtype=torch.int32, device=scales.device)
+    fp4q_rebias_scales(scales, R, nb, per_row, codes, factor, nofit)
+    return codes, factor, nofit
+
+
+def gemm_ue5m3_rebiased(A, A_scales, A_tscale, B, B_scales, B_tscale, dtype=torch.bfloat16, out=None,
+                        nofit: torch.Tensor | None = None) -> torch.Tensor:
+    """The UE5M3 contraction of `gemm` on the native block-scaled MMA: A's
+    scales rebiased per row, B's for the tensor, then the native GEMM, and the
+    emulated GEMM in its place (decided on the device) when a group does not
+    fit.  `nofit` (int32 [1], zeroed here) receives the decision."""
+    M, K = A.shape[0], A.shape[1] * 2
+    N = B.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=dtype, device=A.device)
+    if nofit is None:
+        nofit = torch.empty(1, dtype=torch.int32, device=A.device)
+    nofit.zero_()
+    a4, fa, _ = rebias_scales(A_scales, True, nofit)
+    b4, fb, _ = rebias_scales(B_scales, False, nofit)
+    fp4q_gemm_nvfp4_rebiased(A, a4, fa, A_tscale, B, b4, fb, B_tscale, M, N, K, nofit, out)
+    fp4q_gemm_if(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K, UE5M3, nofit, out)
     return out

@@ -186,6 +186,60 @@ fp4q_status fp4q_gemm_nvfp4(const uint8_t* A, const uint8_t* A_scales, const flo
                             const uint8_t* B, const uint8_t* B_scales, const float* B_tscale,
                             int64_t M, int64_t N, int64_t K, void* out, int out_is_f32, void* stream);
 
+/* Exponent rebias of UE5M3 block-scale codes, so that a UE5M3-scaled GEMM can
+ * run exactly on the tensor cores' UE4M3 block-scaled MMA ("UE5M3 FP4 Block
+ * Scaling for Stable Language Model Pretraining", Abstract: the hardware
+ * takes E4M3/E8M0 block scales, which is why UE5M3 is emulated).  UE5M3 and
+ * UE4M3 share their 3 mantissa bits, so a group of scales whose non-zero
+ * values lie in 14 consecutive binades [e_top - 13, e_top] is exactly
+ * factor * (UE4M3 values) with factor = 2^(e_top - 7); the group's largest
+ * binade lands in UE4M3 exponent field 14.  Groups:
+ *   per_row != 0: each row; e_top is the row's largest binade; a row with no
+ *                 non-zero scale gets factor 1 and zero codes;
+ *   per_row == 0: the whole tensor, with the fixed window e_top = 16 (the
+ *                 binade of UE5M3's largest finite scale, where the tensor
+ *                 scale puts the tensor's amax): factor 2^9, binades 3..16.
+ * scales: UE5M3 codes [rows, nblocks] (device); out_scales: UE4M3 codes of
+ * the same shape (device; must not overlap `scales`); out_factor: binary32
+ * [rows] (per_row) or [1] (device).  Zero codes stay zero.  A group that does
+ * not fit sets *inout_nofit to 1 (a device int, OR-ed, never cleared here: the
+ * caller zeroes it, then may rebias several operands into the same flag); the
+ * codes and factor of such a group are unspecified.  nblocks a multiple of 16
+ * (K = 16 nblocks a multiple of 256, as fp4q_gemm_nvfp4 needs); scales and
+ * out_scales 16-byte aligned, out_factor and inout_nofit 4-byte aligned.
+ * Asynchronous on `stream`; nothing is read back to the host. */
+fp4q_status fp4q_rebias_scales(const uint8_t* scales, int64_t rows, int64_t nblocks, int per_row,
+                               uint8_t* out_scales, float* out_factor, int* inout_nofit, void* stream);
+
+/* fp4q_gemm_nvfp4 on rebiased operands: A's UE4M3 codes with one power-of-two
+ * factor per row (A_factor [M]), B's with one for the tensor (B_factor [1]),
+ * as fp4q_rebias_scales writes them:
+ *   C[m, n] = (T_A * T_B * fb * fa[m]) * sum_k (e s4)_A[m, k] * (e s4)_B[n, k]
+ * the factors applied to the binary32 accumulator after T_A * T_B (exact
+ * products of powers of two while the result stays in binary32's normal
+ * range).  With codes and factors from fp4q_rebias_scales that fitted, this
+ * is the UE5M3 contraction of fp4q_gemm on the original scales, up to the
+ * accumulation order.  skip_if_set (nullable device int): when it is non-zero
+ * as the kernel starts, the launch writes nothing (K = 0 still writes zeros);
+ * it is read once on the device, never on the host.  Shapes, alignment, waits
+ * and test hooks as fp4q_gemm_nvfp4; A_factor, B_factor 4-byte aligned. */
+fp4q_status fp4q_gemm_nvfp4_rebiased(const uint8_t* A, const uint8_t* A_scales4, const float* A_factor,
+                                     const float* A_tscale, const uint8_t* B, const uint8_t* B_scales4,
+                                     const float* B_factor, const float* B_tscale, int64_t M, int64_t N,
+                                     int64_t K, const int* skip_if_set, void* out, int out_is_f32,
+                                     void* stream);
+
+/* fp4q_gemm that runs only when the device int *run_if_set is non-zero as the
+ * kernel starts (read once on the device, never on the host); otherwise the
+ * launch writes nothing (K = 0 still writes zeros).  With the flag of
+ * fp4q_rebias_scales it is the exact fallback of fp4q_gemm_nvfp4_rebiased
+ * into the same `out`: issued after it on one stream, exactly one of the two
+ * writes C.  Arguments otherwise as fp4q_gemm; run_if_set 4-byte aligned. */
+fp4q_status fp4q_gemm_if(const uint8_t* A, const uint8_t* A_scales, const float* A_tscale,
+                         const uint8_t* B, const uint8_t* B_scales, const float* B_tscale, int64_t M,
+                         int64_t N, int64_t K, fp4q_scale_fmt fmt, const int* run_if_set, void* out,
+                         int out_is_f32, void* stream);
+
 /* Reads the device status word of the current device in the order of
  * `stream` (after every call already issued on it), waits for `stream` alone
  * (no other stream of the device is synchronised), returns the latched

@@ -115,6 +115,38 @@ def test_host_validation_rejects_before_launch(lib):
     s.argtypes = [P, P]
     assert s(None, None) == ERR_ARG
 
+    i64 = ctypes.c_int64
+    r = lib.fp4q_rebias_scales
+    r.argtypes = [P, i64, i64, ctypes.c_int, P, P, P, P]
+    buf = ctypes.create_string_buffer(64 * 16 + 16)
+    base = (ctypes.addressof(buf) + 15) & ~15
+    src, dst = P(base), P(base + 16 * 32)   # 16 rows of 16 codes, apart
+    assert r(src, 16, 24, 1, dst, ok, ok, None) == ERR_SHAPE      # nblocks % 16
+    assert r(src, -1, 16, 1, dst, ok, ok, None) == ERR_SHAPE
+    assert r(src, 16, 16, 1, dst, None, ok, None) == ERR_ARG      # factor
+    assert r(src, 16, 16, 1, dst, ok, None, None) == ERR_ARG      # flag
+    assert r(None, 16, 16, 1, dst, ok, ok, None) == ERR_ARG
+    assert r(src, 16, 16, 1, P(base + 8), ok, ok, None) == ERR_ALIGN
+    assert r(src, 16, 16, 1, ok, ok, P(18), None) == ERR_ALIGN
+    assert r(src, 16, 16, 1, P(base + 16 * 8), ok, ok, None) == ERR_ARG   # overlapping in/out
+    assert r(src, 0, 16, 1, dst, ok, ok, None) == 0                     # no rows: no-op
+
+    n = lib.fp4q_gemm_nvfp4_rebiased
+    n.argtypes = [P, P, P, P, P, P, P, P, i64, i64, i64, P, P, ctypes.c_int, P]
+    assert n(ok, ok, ok, ok, ok, ok, ok, ok, 128, 128, 128, None, ok, 0, None) == ERR_SHAPE   # K % 256
+    assert n(ok, ok, None, ok, ok, ok, ok, ok, 128, 128, 256, None, ok, 0, None) == ERR_ARG  # A factor
+    assert n(ok, ok, ok, ok, ok, ok, None, ok, 128, 128, 256, None, ok, 0, None) == ERR_ARG  # B factor
+    assert n(ok, ok, P(18), ok, ok, ok, ok, ok, 128, 128, 256, None, ok, 0, None) == ERR_ALIGN
+    assert n(ok, ok, ok, ok, ok, ok, ok, ok, 128, 128, 256, P(18), ok, 0, None) == ERR_ALIGN
+    assert n(ok, ok, ok, ok, ok, ok, ok, ok, 0, 128, 256, None, ok, 0, None) == 0   # empty: no-op
+
+    c = lib.fp4q_gemm_if
+    c.argtypes = [P, P, P, P, P, P, i64, i64, i64, ctypes.c_int, P, P, ctypes.c_int, P]
+    assert c(ok, ok, ok, ok, ok, ok, 128, 128, 128, 0, None, ok, 0, None) == ERR_ARG     # flag required
+    assert c(ok, ok, ok, ok, ok, ok, 128, 128, 128, 0, P(18), ok, 0, None) == ERR_ALIGN
+    assert c(ok, ok, ok, ok, ok, ok, 128, 128, 96, 0, ok, ok, 0, None) == ERR_SHAPE
+    assert c(ok, ok, ok, ok, ok, ok, 0, 128, 128, 0, ok, ok, 0, None) == 0
+
 
 def test_product_path_has_no_fallback():
     # the binding raises at import time when the library is missing; it never

@@ -110,6 +110,36 @@ def test_gemm_quantize_shapes(fp4q):
     raises(g, *ops48, M, 48, K, 0, T, None, u8(M, 24), u8(M, 3), None, match="multiple of 32")
 
 
+def test_rebias_shapes(fp4q):
+    r = fp4q.fp4q_rebias_scales
+    f1 = torch.ones(1)
+    flag = torch.zeros(1, dtype=torch.int32)
+    raises(r, u8(8, 32), 8, 32, True, u8(8, 32), torch.ones(8), flag, match="CUDA")
+    raises(r, u8(8, 32), 8, 32, False, u8(8, 32), f1, flag, match="CUDA")
+    raises(r, u8(8, 32), 8, 32, True, u8(8, 32), f1, flag, match="out_factor")   # one per row
+    raises(r, u8(8, 24), 8, 24, True, u8(8, 24), torch.ones(8), flag, match="multiple of 16")
+    raises(r, u8(8, 32), 8, 32, True, u8(8, 16), torch.ones(8), flag, match="out_scales")
+    raises(r, u8(8, 32), 8, 32, True, u8(8, 32), torch.ones(8), torch.zeros(1), match="inout_nofit")
+
+
+def test_rebiased_gemm_shapes(fp4q):
+    M, N, K = 32, 64, 256
+    A, As, TA, B, Bs, TB = _gemm_ops(M, N, K)
+    flag = torch.zeros(1, dtype=torch.int32)
+    g = fp4q.fp4q_gemm_nvfp4_rebiased
+    raises(g, A, As, torch.ones(M), TA, B, Bs, torch.ones(1), TB, M, N, K, flag, bf(M, N), match="CUDA")
+    raises(g, A, As, torch.ones(M), TA, B, Bs, torch.ones(1), TB, M, N, K, None, bf(M, N), match="CUDA")
+    raises(g, A, As, torch.ones(M - 1), TA, B, Bs, torch.ones(1), TB, M, N, K, flag, bf(M, N),
+           match="A_factor")
+    raises(g, A, As, torch.ones(M), TA, B, Bs, None, TB, M, N, K, flag, bf(M, N), match="B_factor")
+    raises(g, A, As, torch.ones(M), TA, B, Bs, torch.ones(1), TB, M, N, K, torch.zeros(1), bf(M, N),
+           match="skip_if_set")
+    c = fp4q.fp4q_gemm_if
+    raises(c, A, As, TA, B, Bs, TB, M, N, K, 0, flag, bf(M, N), match="CUDA")
+    raises(c, A, As, TA, B, Bs, TB, M, N, K, 0, None, bf(M, N), match="run_if_set")
+    raises(c, A, As, TA, B, Bs, TB, M, N, K, 0, flag, bf(M, N + 16), match="out")
+
+
 def test_scalar_entry_points(fp4q):
     raises(fp4q.fp4q_amax, bf(16), torch.ones(0), match="out_amax")
     raises(fp4q.fp4q_amax, torch.zeros(16), torch.ones(1), match="bfloat16")

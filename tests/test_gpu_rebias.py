@@ -1,0 +1,194 @@
+"""GPU parity of the UE5M3 -> UE4M3 exponent rebias and of the UE5M3 GEMM
+run on the native block-scaled MMA through it.
+
+fp4q_rebias_scales is byte work: codes and factors must equal the oracle's
+bit for bit for every group that fits, and the "does not fit" flag must equal
+the oracle's decision.  The rebiased GEMM (fp4q_gemm_nvfp4_rebiased) must meet
+the GEMM bound against the oracle's binary64 UE5M3 contraction of the
+ORIGINAL operands, and the device-side fallback (fp4q_gemm_if) must make the
+whole sequence equal plain fp4q_gemm when a group does not fit.
+
+Method: "UE5M3 FP4 Block Scaling for Stable Language Model Pretraining",
+Abstract -- UE5M3 is emulated because the tensor cores take only E4M3/E8M0
+block scales; the two formats share their mantissa bits, so a group of UE5M3
+scales within 14 binades is a power of two times UE4M3 scales."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp4_block_scaled_bf16_gb300 import workloads
+from parity_util import (GEMM_TOL, check_gemm_bf16, check_gemm_elementwise, gemm_abs_reference,
+                         gemm_error, np_u8, to_dev)
+from scale_codes import codes_with_span
+
+pytestmark = pytest.mark.gpu
+UE5M3 = oracle.UE5M3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    from fp4_block_scaled_bf16_gb300 import build
+    build.build()
+    from fp4_block_scaled_bf16_gb300 import fp4q
+    yield fp4q
+    assert fp4q.fp4q_get_device_status() == fp4q.OK
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _rebias(lib, codes, per_row):
+    c4, f, flag = lib.rebias_scales(_dev(codes), per_row)
+    torch.cuda.synchronize()
+    return np_u8(c4), f.cpu().numpy(), int(flag.item())
+
+
+def _fitting_groups(codes, per_row):
+    """Per row: which rows the oracle says fit (each row alone)."""
+    if not per_row:
+        return None
+    return np.array([oracle.rebias_scales(codes[r:r + 1], True)[2] for r in range(codes.shape[0])])
+
+
+@pytest.mark.parametrize("rows,nb", [(1, 16), (37, 32), (300, 16), (9, 528), (130, 256)])
+@pytest.mark.parametrize("span", [0, 7, 13, 14, 19])
+def test_per_row_codes_factors_and_flag(lib, rows, nb, span):
+    """Rows of one span each (span 14 and 19 do not fit), plus zero rows; nb
+    up to 528 codes makes a lane handle more than one 16-code chunk."""
+    rng = np.random.default_rng(rows * 1000 + nb + span)
+    codes = codes_with_span(rng, rows, nb, span)
+    codes[rng.random(rows) < 0.1] = 0                      # all-zero rows: factor 1, zero codes
+    c4, f, flag = _rebias(lib, codes, True)
+    r4, rf, fits = oracle.rebias_scales(codes, per_row=True)
+    assert flag == int(not fits)
+    ok = _fitting_groups(codes, True)
+    assert ok.any() or span > 13
+    np.testing.assert_array_equal(c4[ok], r4[ok])
+    np.testing.assert_array_equal(f[ok], rf[ok])
+
+
+def test_per_row_mixed_fit(lib):
+    """One row that does not fit among fitting ones sets the flag; the other
+    rows are still exact."""
+    rng = np.random.default_rng(5)
+    codes = codes_with_span(rng, 64, 64, 10)
+    codes[17] = codes_with_span(rng, 1, 64, 15)[0]
+    c4, f, flag = _rebias(lib, codes, True)
+    r4, rf, fits = oracle.rebias_scales(codes, per_row=True)
+    assert flag == 1 and not fits
+    ok = np.ones(64, bool)
+    ok[17] = False
+    np.testing.assert_array_equal(c4[ok], r4[ok])
+    np.testing.assert_array_equal(f[ok], rf[ok])
+
+
+@pytest.mark.parametrize("rows,nb", [(16, 16), (1000, 32), (77, 256)])
+def test_per_tensor_window(lib, rows, nb):
+    """Per tensor: codes in binades 3..16 (and zeros) fit with factor 2^9,
+    bit-exact; one code below binade 3 anywhere sets the flag."""
+    rng = np.random.default_rng(rows + nb)
+    e = rng.integers(18, 32, (rows, nb))                     # exponent fields of binades 3..16
+    m = rng.integers(0, 8, (rows, nb))
+    codes = ((e << 3) | m).astype(np.uint8)
+    codes[codes == 0xFF] = 0xFE
+    codes[rng.random((rows, nb)) < 0.05] = 0
+    c4, f, flag = _rebias(lib, codes, False)
+    r4, rf, fits = oracle.rebias_scales(codes, per_row=False)
+    assert fits and flag == 0
+    np.testing.assert_array_equal(c4, r4)
+    np.testing.assert_array_equal(f, rf)
+    codes[rows // 2, nb - 1] = (17 << 3) | 3                # binade 2
+    _, _, flag = _rebias(lib, codes, False)
+    assert flag == 1 and not oracle.rebias_scales(codes, per_row=False)[2]
+
+
+def test_flag_is_or_ed_not_cleared(lib):
+    codes = codes_with_span(np.random.default_rng(1), 8, 16, 3)
+    flag = torch.ones(1, dtype=torch.int32, device="cuda")
+    lib.rebias_scales(_dev(codes), True, flag)
+    assert int(flag.item()) == 1
+
+
+def _quantised(lib, a_bits, b_bits):
+    qa = lib.quantize(to_dev(a_bits))
+    qb = lib.quantize(to_dev(b_bits))
+    return (qa.payload_row, qa.scales_row, qa.T), (qb.payload_row, qb.scales_row, qb.T)
+
+
+def _oracle_check(C32, C16, A, B):
+    pa, sa, pb, sb = (np_u8(t) for t in (A[0], A[1], B[0], B[1]))
+    ta, tb = float(A[2].item()), float(B[2].item())
+    R = oracle.gemm(pa, sa, ta, pb, sb, tb, UE5M3)
+    S = gemm_abs_reference(pa, sa, pb, sb, ta * tb, UE5M3)
+    C32 = C32.cpu().numpy().astype(np.float64)
+    assert gemm_error(C32, R) <= GEMM_TOL
+    check_gemm_elementwise(C32, R, S, pa.shape[1] * 2)
+    check_gemm_bf16(C16.float().cpu().numpy().astype(np.float64), R)
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 256), (208, 304, 512), (16, 48, 256), (384, 784, 768),
+                                   (608, 528, 1280)])
+def test_rebiased_gemm_matches_the_ue5m3_oracle(lib, M, N, K):
+    """Quantised activations (per-channel magnitudes) and weights: every A
+    row and the whole of B fit, so the native MMA computes the UE5M3 GEMM."""
+    a = workloads.activations(M, K, M + K)
+    b = workloads.weights(N, K, N + K)
+    A, B = _quantised(lib, a, b)
+    flag = torch.empty(1, dtype=torch.int32, device="cuda")
+    C32 = lib.gemm_ue5m3_rebiased(*A, *B, dtype=torch.float32, nofit=flag)
+    C16 = lib.gemm_ue5m3_rebiased(*A, *B, dtype=torch.bfloat16, nofit=flag)
+    torch.cuda.synchronize()
+    assert int(flag.item()) == 0
+    _oracle_check(C32, C16, A, B)
+
+
+def test_fallback_when_a_row_does_not_fit(lib):
+    """A row of A whose block scales span more than 14 binades: the flag is
+    set, the native launch writes nothing and the emulated GEMM writes C --
+    the result is fp4q_gemm's, bit for bit, and meets the oracle bound."""
+    M, N, K = 256, 512, 512
+    a = workloads.activations(M, K, 3)
+    af = workloads.bf16_bits_to_f32(a)
+    af[5, :16] *= 2.0 ** -20                                   # one tiny block in row 5
+    a = workloads.f32_to_bf16_bits(af)
+    b = workloads.weights(N, K, 4)
+    A, B = _quantised(lib, a, b)
+    assert not oracle.rebias_scales(np_u8(A[1]), per_row=True)[2]
+    flag = torch.empty(1, dtype=torch.int32, device="cuda")
+    C = lib.gemm_ue5m3_rebiased(*A, *B, dtype=torch.float32, nofit=flag)
+    E = lib.gemm(*A, *B, dtype=torch.float32)
+    C16 = lib.gemm_ue5m3_rebiased(*A, *B, dtype=torch.bfloat16, nofit=flag)
+    torch.cuda.synchronize()
+    assert int(flag.item()) == 1
+    assert torch.equal(C, E)
+    _oracle_check(C, C16, A, B)
+
+
+def test_skip_and_run_flags_leave_out_untouched(lib):
+    M, N, K = 256, 256, 256
+    A, B = _quantised(lib, workloads.activations(M, K, 8), workloads.weights(N, K, 9))
+    a4, fa, _ = lib.rebias_scales(A[1], True)
+    b4, fb, _ = lib.rebias_scales(B[1], False)
+    sentinel = torch.full((M, N), 12345.0, device="cuda")
+    one = torch.ones(1, dtype=torch.int32, device="cuda")
+    zero = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = sentinel.clone()
+    lib.fp4q_gemm_nvfp4_rebiased(A[0], a4, fa, A[2], B[0], b4, fb, B[2], M, N, K, one, out)
+    lib.fp4q_gemm_if(*A, *B, M, N, K, lib.UE5M3, zero, out)
+    torch.cuda.synchronize()
+    assert torch.equal(out, sentinel)
+    # the same calls with the flags the other way round write C
+    lib.fp4q_gemm_nvfp4_rebiased(A[0], a4, fa, A[2], B[0], b4, fb, B[2], M, N, K, zero, out)
+    n = out.clone()
+    out.copy_(sentinel)
+    lib.fp4q_gemm_if(*A, *B, M, N, K, lib.UE5M3, one, out)
+    torch.cuda.synchronize()
+    assert not torch.equal(n, sentinel) and not torch.equal(out, sentinel)
+    assert gemm_error(n.cpu().numpy().astype(np.float64), out.cpu().numpy().astype(np.float64)) <= GEMM_TOL
+    # no flag at all: the native launch always runs
+    out.copy_(sentinel)
+    lib.fp4q_gemm_nvfp4_rebiased(A[0], a4, fa, A[2], B[0], b4, fb, B[2], M, N, K, None, out)
+    torch.cuda.synchronize()
+    assert torch.equal(out, n)

@@ -16,6 +16,7 @@ import pytest
 
 import oracle
 from fp4_block_scaled_bf16_gb300 import workloads
+from scale_codes import codes_with_span as _codes_with_span
 
 
 def _ue5m3(code):
@@ -44,27 +45,6 @@ def _binade(v):
         v *= 2
         e -= 1
     return e
-
-
-def _codes_with_span(rng, rows, nb, span):
-    """UE5M3 codes whose non-zero values span exactly `span` binades per row
-    (some zero codes and subnormal codes included)."""
-    out = np.zeros((rows, nb), np.uint8)
-    for r in range(rows):
-        top = int(rng.integers(span - 16, 17))          # binade of the largest scale
-        binades = rng.integers(top - span, top + 1, nb)
-        binades[0], binades[1] = top, top - span
-        for i, b in enumerate(binades):
-            m = int(rng.integers(0, 7 if b == 16 else 8))      # 0xFF is not a value
-            if b >= -14:
-                out[r, i] = ((b + 15) << 3) | m
-            else:                                        # subnormal: m/8 * 2^-14 with binade b
-                sh = -14 - b                              # 1..3
-                out[r, i] = (1 << (3 - sh)) | (m >> sh) if sh <= 3 else 0
-        zero = rng.random(nb) < 0.1
-        zero[:2] = False
-        out[r, zero] = 0
-    return out
 
 
 @pytest.mark.parametrize("span", [0, 5, 13])
