@@ -8,8 +8,12 @@ an amax pass only on the very first step); dual-axis block-16 E2M1/UE5M3
 quantisation of X and W (RNE) and of dY (Philox SR, seed 7); the three
 training GEMMs on the block-scaled operands (fprop Y = X W^T, dgrad
 dX = dY W, wgrad dW = dY^T X), each 8192 x 16384 x 4096 multiply-adds.
-The same step under current scaling (amax pass + scale before every
-quantisation) is timed beside it.
+fprop and dgrad run on the tensor cores' block-scaled MMA with their UE5M3
+scale codes rebiased to UE4M3 codes times powers of two (exact; the emulated
+GEMM takes over on the device when a group does not fit), wgrad on the
+emulated GEMM.  The same step with all three GEMMs emulated, and under
+current scaling (amax pass + scale before every quantisation), are timed
+beside it.
 
 value = the three GEMMs' 2MNK flops / step time (quantisation included),
 TFLOP/s.  Per-kernel CUDA-event times give the quantiser GB/s and the GEMM
@@ -225,6 +229,34 @@ def bind_to_gpu_node(torch, index):
 
 
 # ---------------------------------------------------------------- GPU path
+def rebias_parts(torch, fp4q, st, steps):
+    """Per-launch times of the pieces of the step's rebiased fprop, one
+    stream, CUDA events between them: the per-row rebias of X's codes, the
+    per-tensor rebias of W's, the native GEMM, and the emulated GEMM's launch
+    when the flag tells it not to run (the operands and buffers of the
+    step's last one-stream run; the flag is zeroed once before the region)."""
+    tokens, hid, out = st.dims
+    a4, fa, b4, fb, flag = st.rb[0]
+    TX, TW = st.tensor_scales(periodic=False)[:2]   # the last run() quantised under current scaling
+    flag.zero_()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    for k in range(steps):
+        ev[k][0].record()
+        fp4q.fp4q_rebias_scales(st.Xrs, tokens, hid // 16, True, a4, fa, flag)
+        ev[k][1].record()
+        fp4q.fp4q_rebias_scales(st.Wrs, out, hid // 16, False, b4, fb, flag)
+        ev[k][2].record()
+        fp4q.fp4q_gemm_nvfp4_rebiased(st.Xr, a4, fa, TX, st.Wr, b4, fb, TW, tokens, out, hid, flag, st.Y)
+        ev[k][3].record()
+        fp4q.fp4q_gemm_if(st.Xr, st.Xrs, TX, st.Wr, st.Wrs, TW, tokens, out, hid, fp4q.UE5M3, flag, st.Y)
+        ev[k][4].record()
+    torch.cuda.synchronize()
+    seg = lambda a, b: sum(e[a].elapsed_time(e[b]) for e in ev) / steps
+    return {"rebias_rows_X_ms": seg(0, 1), "rebias_tensor_W_ms": seg(1, 2), "native_gemm_ms": seg(2, 3),
+            "skipped_emulated_launch_ms": seg(3, 4), "flag": int(flag.item())}
+
+
 def run_gpu(args, rank, world):
     import torch
     from fp4_block_scaled_bf16_gb300 import build, fp4q, workloads
@@ -244,21 +276,29 @@ def run_gpu(args, rank, world):
     hW = workloads.to_torch_bf16(Wb).pin_memory()
     hD = workloads.to_torch_bf16(dYb).pin_memory()
     X, W, dY = hX.to(dev), hW.to(dev), hD.to(dev)
+    # the step as the library runs it: fprop and dgrad on the block-scaled
+    # MMA through rebiased UE5M3 scale codes (emulated fallback decided on
+    # the device), wgrad emulated; and the same step with all three GEMMs
+    # emulated
+    rstep = LinearStep(X, W, dY, seed=7, rebias=True)
     step = LinearStep(X, W, dY, seed=7)
     for _ in range(args.warmup):
-        step.run_overlapped(periodic=True)
-        step.run_overlapped()
-        step.run()
+        for st_w in (rstep, step):
+            st_w.run_overlapped(periodic=True)
+            st_w.run_overlapped()
+            st_w.run()
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
 
     # ---- device-resident timed regions, K steps each: the method's step
     # (periodic tensor scaling, three streams) -- the headline; the same step
-    # under current scaling (an amax pass before every quantisation); and the
-    # current-scaling step launched one kernel after another on one stream
-    # with events between the kernels, for the per-kernel times
+    # with all three GEMMs emulated; the headline step under current scaling
+    # (an amax pass before every quantisation); and both current-scaling
+    # steps launched one kernel after another on one stream with events
+    # between the pieces, for the per-kernel times
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
+    evr = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
 
     def timed(fn):
         torch.cuda.synchronize()
@@ -274,18 +314,25 @@ def run_gpu(args, rank, world):
         return e0.elapsed_time(e1)
 
     with ClockSampler(dev.index) as clk:
-        step.launches = 0
-        ms = timed(lambda k: step.run_overlapped(periodic=True))
-        launches = step.launches
-        refreshes = [sc.step for sc in step.scalers]
-        ms_current = timed(lambda k: step.run_overlapped())
+        rstep.launches = 0
+        ms = timed(lambda k: rstep.run_overlapped(periodic=True))
+        launches = rstep.launches
+        fallbacks = rstep.fallbacks()
+        refreshes = [sc.step for sc in rstep.scalers]
+        ms_emulated = timed(lambda k: step.run_overlapped(periodic=True))
+        ms_current = timed(lambda k: rstep.run_overlapped())
         ms_serial = timed(lambda k: step.run(evs[k]))
+        ms_serial_r = timed(lambda k: rstep.run(evr[k]))
+        parts = rebias_parts(torch, fp4q, rstep, args.steps)
     if world > 1:
         ms = max_over_ranks(ms, dev)
+        ms_emulated = max_over_ranks(ms_emulated, dev)
         ms_current = max_over_ranks(ms_current, dev)
     seg = lambda a, b: sum(e[a].elapsed_time(e[b]) for e in evs) / args.steps
+    segr = lambda a, b: sum(e[a].elapsed_time(e[b]) for e in evr) / args.steps
     t_scale, t_qx, t_qw, t_qd = seg(0, 1), seg(1, 2), seg(2, 3), seg(3, 4)
     t_g = [seg(4, 5), seg(5, 6), seg(6, 7)]
+    t_gr = [segr(4, 5), segr(5, 6), segr(6, 7)]
     status = fp4q.fp4q_get_device_status()
 
     # ---- end to end through the API with host buffers: every step copies its
@@ -295,7 +342,8 @@ def run_gpu(args, rank, world):
     hY = [torch.empty(step.Y.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     hdX = [torch.empty(step.dX.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     hdW = [torch.empty(step.dW.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    steps2 = [step, LinearStep(torch.empty_like(X), torch.empty_like(W), torch.empty_like(dY), seed=7)]
+    steps2 = [rstep, LinearStep(torch.empty_like(X), torch.empty_like(W), torch.empty_like(dY), seed=7,
+                                rebias=True)]
     s_h2d, s_cmp, s_d2h = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     e2e_warm = 3
     e2e_steps = max(2, min(args.steps, 8))
@@ -469,7 +517,7 @@ def run_gpu(args, rank, world):
         for name in workloads.LINEARS:
             xb, wb, db = workloads.linear_block(name)
             lin.append(LinearStep(workloads.to_torch_bf16(xb).to(dev), workloads.to_torch_bf16(wb).to(dev),
-                                  workloads.to_torch_bf16(db).to(dev), seed=7))
+                                  workloads.to_torch_bf16(db).to(dev), seed=7, rebias=True))
         for _ in range(2):
             for st_l in lin:
                 st_l.run_overlapped(periodic=True)
@@ -486,6 +534,7 @@ def run_gpu(args, rank, world):
         bms = c0.elapsed_time(c1) / nb
         bflops = sum(3 * 2.0 * workloads.TOKENS * fi * fo for fi, fo in workloads.LINEARS.values())
         block = {"ms_per_block_step": bms, "TFLOP/s": bflops / (bms * 1e-3) / 1e12, "steps": nb,
+                 "fallbacks_fprop_dgrad": [st_l.fallbacks() for st_l in lin],
                  "linears": ", ".join(f"{k} {fi}->{fo}" for k, (fi, fo) in workloads.LINEARS.items()),
                  "tokens": workloads.TOKENS}
         del lin
@@ -528,7 +577,9 @@ def run_gpu(args, rank, world):
         native["block_TFLOP/s"] = block["TFLOP/s"] * block["ms_per_block_step"] / bms
         del lin
 
-    return dict(ms=ms, ms_current=ms_current, refreshes=refreshes, ms_serial=ms_serial, native=native, fused=fused, block=block, t_scale=t_scale, t_q=(t_qx, t_qw, t_qd), t_g=t_g, launches=launches, rates=rates,
+    return dict(ms=ms, ms_emulated=ms_emulated, ms_current=ms_current, refreshes=refreshes, ms_serial=ms_serial,
+                ms_serial_r=ms_serial_r, t_gr=t_gr, parts=parts, fallbacks=fallbacks,
+                native=native, fused=fused, block=block, t_scale=t_scale, t_q=(t_qx, t_qw, t_qd), t_g=t_g, launches=launches, rates=rates,
                 clocks=clk.summary(), status=status, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, link=link, affinity=affinity,
                 elems=(X.numel(), W.numel(), dY.numel()))
 
@@ -728,6 +779,12 @@ def main():
     value = job_tflops(world, STEP_FLOPS, ms)
     t_gemm = sum(r["t_g"]) / 3
     gemm_tflops = GEMM_FLOPS / (t_gemm * 1e-3) / 1e12
+    # the dominant kernel of the headline step: the emulated GEMM, which runs
+    # its wgrad (the one-stream pass of the headline step's GEMM paths)
+    wgrad_tflops = GEMM_FLOPS / (r["t_gr"][2] * 1e-3) / 1e12
+    pr = r["parts"]
+    native_tflops = GEMM_FLOPS / (pr["native_gemm_ms"] * 1e-3) / 1e12
+    fp4_peak = bf16 * FP4_OVER_BF16 if bf16 else None
     nX, nW, nD = r["elems"]
     q_bytes = [n * DUAL_BYTES_PER_ELEM for n in (nX, nW, nD)]
     q_gbs = [b / (t * 1e-3) / 1e9 for b, t in zip(q_bytes, r["t_q"])]
@@ -746,8 +803,12 @@ def main():
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "ms_per_step_periodic": ms,
         "ms_per_step_current_scaling": r["ms_current"] / args.steps,
+        "ms_per_step_all_gemms_emulated": r["ms_emulated"] / args.steps,
         "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f16xf16->f32 (E2M1/UE5M3 operands, exact FP16 expansion)", "data": "synthetic",
+        "vs_baseline": None,
+        "dtype": "E2M1/UE5M3 operands; fprop, dgrad: e2m1 x e2m1 block-scaled MMA -> f32 (UE5M3 scales as UE4M3 "
+                 "codes x 2^k, exact); wgrad: f16xf16->f32 (exact FP16 expansion)",
+        "data": "synthetic",
         "config": {"workload": WORKLOAD, "M": M_TOK, "hidden": HID, "ffn": FFN,
                    "l2": "inputs larger than L2 (dY 256 MiB, step working set ~1 GiB)",
                    "schedule": "three streams: X/W scale, quantise and fprop; dY scale, SR "
@@ -755,15 +816,28 @@ def main():
                    "tensor_scaling": "periodic: T refreshed every 16 steps from the amax fused into the "
                                      "previous quantisation; amax pass on the first step only "
                                      f"(scaler steps after the timed region: {r['refreshes']})",
+                   "gemm_paths": "fprop, dgrad: scale codes rebiased (A per row, B per tensor) + native "
+                                 "block-scaled MMA, emulated GEMM launched after it and run on the device only "
+                                 "if a group spans > 14 binades; wgrad: emulated (FP16 expansion)",
+                   "fallbacks_fprop_dgrad": r["fallbacks"],
                    "current_scaling_TFLOP/s": job_tflops(world, STEP_FLOPS, r["ms_current"] / args.steps),
-                   "ms_per_step_one_stream_current_scaling": r["ms_serial"] / args.steps,
+                   "all_gemms_emulated_TFLOP/s": job_tflops(world, STEP_FLOPS, r["ms_emulated"] / args.steps),
+                   "ms_per_step_one_stream_current_scaling": r["ms_serial_r"] / args.steps,
+                   "ms_per_step_one_stream_current_scaling_all_emulated": r["ms_serial"] / args.steps,
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": bf16,
-                     "unit": "TFLOP/s", "frac": gemm_tflops / bf16 if bf16 else None,
+        "roofline": {"bound": "tensor", "achieved": wgrad_tflops, "peak": bf16,
+                     "unit": "TFLOP/s", "frac": wgrad_tflops / bf16 if bf16 else None,
                      "traffic": committed_traffic("gemm_kernel_traffic_8B_linear.json", GEMM_SOURCES),
-                     "kernel": "fp4q gemm_kernel (mean of fprop/dgrad/wgrad)",
+                     "kernel": "fp4q gemm_kernel (emulated UE5M3 GEMM; its wgrad launch, 16384 x 4096 x 8192)",
                      "peak_source": f"{src} bf16 ({'burst' if burst else 'sustained'}: the per-kernel "
-                                    f"region ran {r['ms_serial']:.0f} ms)"},
+                                    f"region ran {r['ms_serial_r']:.0f} ms)",
+                     "all_three_emulated": {"achieved": gemm_tflops, "frac": gemm_tflops / bf16 if bf16 else None,
+                                            "note": "mean over fprop/dgrad/wgrad of the all-emulated one-stream step"}},
+        "roofline_native_rebiased": {"bound": "tensor", "achieved": native_tflops, "peak": fp4_peak,
+                                     "unit": "TFLOP/s", "frac": native_tflops / fp4_peak if fp4_peak else None,
+                                     "kernel": "fp4q gemm_nvfp4_kernel on rebiased UE5M3 operands (fprop)",
+                                     "peak_source": f"{src} bf16 x {FP4_OVER_BF16:g} (nominal dense fp4 / bf16)",
+                                     "parts_ms": pr},
         "roofline_quantize": {"bound": "hbm", "unit": "GB/s", "peak": hbm,
                               "achieved": dict({"X_dual_rne": q_gbs[0], "W_dual_rne": q_gbs[1], "dY_dual_sr": q_gbs[2]}, **r["rates"]),
                               "frac": dict({k: g / hbm for k, g in zip(("X_dual_rne", "W_dual_rne", "dY_dual_sr"), q_gbs)},
@@ -771,8 +845,9 @@ def main():
                               "peak_source": f"{src} hbm",
                               "issue_roofline": issue_roofline(q_gbs, (r["clocks"] or {}).get("sm_mhz"))},
         "breakdown_ms": {"amax_scale": r["t_scale"], "quantize_X": r["t_q"][0], "quantize_W": r["t_q"][1],
-                         "quantize_dY": r["t_q"][2], "fprop": r["t_g"][0], "dgrad": r["t_g"][1],
-                         "wgrad": r["t_g"][2]},
+                         "quantize_dY": r["t_q"][2], "fprop": r["t_gr"][0], "dgrad": r["t_gr"][1],
+                         "wgrad": r["t_gr"][2], "fprop_emulated": r["t_g"][0], "dgrad_emulated": r["t_g"][1],
+                         "wgrad_emulated": r["t_g"][2]},
         "e2e": {"value": job_tflops(world, STEP_FLOPS, r["e2e_ms"]), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e_ms"],
                 "host_link_gbs": {k: round(v, 1) for k, v in r["link"].items()},

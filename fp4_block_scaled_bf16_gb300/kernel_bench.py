@@ -9,12 +9,15 @@ Small cases of this command are what the committed ncu summaries capture.
 
   python -m fp4_block_scaled_bf16_gb300.kernel_bench --case dual_sr --rows 2048 --cols 16384
   cases: amax, row_rne, row_sr, dual_rne, dual_sr, 2d_rne, 2d_sr, dequant, gemm and gemm_nvfp4
-  (--m --n --k; gemm_nvfp4 on UE4M3-scaled operands), and step: the whole
-  linear fwd+bwd step of the bench (X [m, k], W [n, k], dY [m, n]) under
-  periodic tensor scaling on three streams, one "launch" per step (its first
-  step launches 12 kernels -- amax and tensor scale of X, W, dY, three
-  quantisations, three GEMMs -- every later one 6, plus a tensor scale per
-  tensor every 16 steps).
+  (--m --n --k; gemm_nvfp4 on UE4M3-scaled operands), gemm_rebias (the UE5M3
+  GEMM through rebiased codes: two rebias launches, the native GEMM, the
+  conditional emulated one), and step: the whole linear fwd+bwd step of the
+  bench (X [m, k], W [n, k], dY [m, n]) under periodic tensor scaling on
+  three streams, one "launch" per step (its first step launches 12 kernels --
+  amax and tensor scale of X, W, dY, three quantisations, three GEMMs -- every
+  later one 6, plus a tensor scale per tensor every 16 steps); step_rebias:
+  the same step with fprop and dgrad through rebiased codes (6 more launches
+  per step: two rebias kernels and a conditional emulated GEMM each).
 """
 from __future__ import annotations
 
@@ -26,7 +29,7 @@ import torch
 from . import build, fp4q, workloads
 
 CASES = ("amax", "row_rne", "row_sr", "dual_rne", "dual_sr", "2d_rne", "2d_sr", "dequant", "gemm", "gemm_nvfp4",
-         "step")
+         "gemm_rebias", "step", "step_rebias")
 
 
 def _inputs(case, rows, cols, dev):
@@ -38,17 +41,17 @@ def run(case, rows=16384, cols=4096, m=8192, n=16384, k=4096, reps=10, warmup=3)
     build.build()
     dev = torch.device("cuda")
     u8 = dict(dtype=torch.uint8, device=dev)
-    if case == "step":
+    if case in ("step", "step_rebias"):
         from .linear_step import LinearStep
 
         X = workloads.to_torch_bf16(workloads.activations(m, k, 1)).to(dev)
         W = workloads.to_torch_bf16(workloads.weights(n, k, 2)).to(dev)
         dY = workloads.to_torch_bf16(workloads.gradients(m, n, 3)).to(dev)
-        st = LinearStep(X, W, dY, seed=7)
+        st = LinearStep(X, W, dY, seed=7, rebias=case == "step_rebias")
         launch = lambda j: st.run_overlapped(periodic=True)
         work, unit = 3 * 2.0 * m * n * k, "TFLOP/s"
-    elif case in ("gemm", "gemm_nvfp4"):
-        fmt = fp4q.UE5M3 if case == "gemm" else fp4q.UE4M3
+    elif case in ("gemm", "gemm_nvfp4", "gemm_rebias"):
+        fmt = fp4q.UE4M3 if case == "gemm_nvfp4" else fp4q.UE5M3
         xs = [fp4q.quantize(workloads.to_torch_bf16(workloads.activations(m, k, 60)).to(dev), fmt=fmt),
               fp4q.quantize(workloads.to_torch_bf16(workloads.weights(n, k, 61)).to(dev), fmt=fmt)]
         A = (xs[0].payload_row, xs[0].scales_row, xs[0].T)
@@ -56,6 +59,17 @@ def run(case, rows=16384, cols=4096, m=8192, n=16384, k=4096, reps=10, warmup=3)
         out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
         if case == "gemm":
             launch = lambda j: fp4q.fp4q_gemm(*A, *B, m, n, k, fmt, out)
+        elif case == "gemm_rebias":
+            a4, b4 = torch.empty_like(A[1]), torch.empty_like(B[1])
+            fa = torch.empty(m, dtype=torch.float32, device=dev)
+            fb = torch.empty(1, dtype=torch.float32, device=dev)
+            flag = torch.zeros(1, dtype=torch.int32, device=dev)
+
+            def launch(j):
+                fp4q.fp4q_rebias_scales(A[1], m, k // 16, True, a4, fa, flag)
+                fp4q.fp4q_rebias_scales(B[1], n, k // 16, False, b4, fb, flag)
+                fp4q.fp4q_gemm_nvfp4_rebiased(A[0], a4, fa, A[2], B[0], b4, fb, B[2], m, n, k, flag, out)
+                fp4q.fp4q_gemm_if(*A, *B, m, n, k, fmt, flag, out)
         else:
             launch = lambda j: fp4q.fp4q_gemm_nvfp4(*A, *B, m, n, k, out)
         work, unit = 2.0 * m * n * k, "TFLOP/s"
@@ -98,7 +112,7 @@ def run(case, rows=16384, cols=4096, m=8192, n=16384, k=4096, reps=10, warmup=3)
     ms = e0.elapsed_time(e1) / reps
     rate = work / (ms * 1e-3) / (1e12 if unit == "TFLOP/s" else 1e9)
     status = fp4q.fp4q_get_device_status()
-    shape = {"m": m, "n": n, "k": k} if case.startswith("gemm") or case == "step" else {"rows": rows, "cols": cols}
+    shape = {"m": m, "n": n, "k": k} if case.startswith(("gemm", "step")) else {"rows": rows, "cols": cols}
     return {"case": case, **shape, "reps": reps, "ms_per_launch": ms, "rate": rate, "unit": unit,
             "device_status": status}
 

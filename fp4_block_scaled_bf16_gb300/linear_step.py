@@ -22,6 +22,16 @@ on the tensor cores' block-scaled MMA (fp4q_gemm_nvfp4) -- the native NVFP4
 execution the page ablates against; otherwise the GEMMs are the emulated
 block-scaled ones (fp4q_gemm) for the chosen scale format.
 
+With `rebias=True` (UE5M3 only) fprop and dgrad compute the same UE5M3 GEMMs
+on the block-scaled MMA: the A operand's scale codes are rebiased per row and
+B's per tensor to UE4M3 codes times powers of two (fp4q_rebias_scales), the
+native kernel applies the factors (fp4q_gemm_nvfp4_rebiased), and the
+emulated kernel (fp4q_gemm_if) is launched after it and runs only if some
+group spanned more than the 14 binades UE4M3 holds -- decided on the device,
+no host read.  wgrad stays emulated: its A operand is dY column-wise, each row
+running over the batch's tokens, whose gradient magnitudes differ by many
+more binades than that.
+
 Every launch goes through libfp4q.so; buffers are allocated once here with
 torch and reused by every step.
 """
@@ -35,10 +45,13 @@ from .periodic import PeriodicScaler
 
 class LinearStep:
     def __init__(self, X: torch.Tensor, W: torch.Tensor, dY: torch.Tensor, seed: int = 7,
-                 period: int = 16, fmt: int = _fp4q.UE5M3, native: bool = False, lib=None):
+                 period: int = 16, fmt: int = _fp4q.UE5M3, native: bool = False, rebias: bool = False,
+                 lib=None):
         q = self.q = lib if lib is not None else _fp4q
         if native and fmt != q.UE4M3:
             raise ValueError("the native block-scaled MMA takes UE4M3 scales (fmt=UE4M3)")
+        if rebias and (native or fmt != q.UE5M3):
+            raise ValueError("rebias re-expresses UE5M3 scales (fmt=UE5M3, native=False)")
         self.native = native
         tokens, hid = X.shape
         out = W.shape[0]
@@ -63,6 +76,16 @@ class LinearStep:
         self.Y = torch.empty((tokens, out), **bf)
         self.dX = torch.empty((tokens, hid), **bf)
         self.dW = torch.empty((out, hid), **bf)
+        # fprop (A = X rows, B = W rows) and dgrad (A = dY rows, B = W columns)
+        # on the native MMA: rebiased codes, factors and a fallback flag each;
+        # a GEMM whose K is not a multiple of 256 stays emulated
+        self.rb = [None, None]
+        self.nofit = torch.zeros(2, dtype=torch.int32, device=dev)
+        if rebias:
+            for g, (m, n, k) in enumerate(((tokens, out, hid), (tokens, hid, out))):
+                if k % 256 == 0:
+                    self.rb[g] = (torch.empty((m, k // 16), **u8), torch.empty(m, **f32),
+                                  torch.empty((n, k // 16), **u8), torch.empty(1, **f32), self.nofit[g:g + 1])
         self.scalers = [PeriodicScaler(period, fmt, device=dev, lib=q) for _ in range(3)]
         self.launches = 0
         self.side = torch.cuda.Stream(device=dev)
@@ -92,12 +115,26 @@ class LinearStep:
         if amax is not None:
             self.scalers[i].advance()
 
-    def _gemm(self, A, B, M, N, K, out):
+    def _gemm(self, A, B, M, N, K, out, rb=None):
+        q = self.q
         if self.native:
-            self.q.fp4q_gemm_nvfp4(*A, *B, M, N, K, out)
+            q.fp4q_gemm_nvfp4(*A, *B, M, N, K, out)
+        elif rb is not None:
+            a4, fa, b4, fb, flag = rb
+            flag.zero_()
+            q.fp4q_rebias_scales(A[1], M, K // 16, True, a4, fa, flag)
+            q.fp4q_rebias_scales(B[1], N, K // 16, False, b4, fb, flag)
+            q.fp4q_gemm_nvfp4_rebiased(A[0], a4, fa, A[2], B[0], b4, fb, B[2], M, N, K, flag, out)
+            q.fp4q_gemm_if(*A, *B, M, N, K, self.fmt, flag, out)
+            self.launches += 3
         else:
-            self.q.fp4q_gemm(*A, *B, M, N, K, self.fmt, out)
+            q.fp4q_gemm(*A, *B, M, N, K, self.fmt, out)
         self.launches += 1
+
+    def fallbacks(self):
+        """Whether fprop and dgrad each fell back to the emulated GEMM on the
+        last step (reads the device flags; synchronises)."""
+        return [bool(v) for v in self.nofit.tolist()]
 
     def tensor_scales(self, periodic: bool):
         """The device T of X, W and dY that the last step used."""
@@ -123,9 +160,9 @@ class LinearStep:
         rec(3)
         self._quantize(2, self.dY, TD, aD, q.SR, (self.Dr, self.Drs, self.Dc, self.Dcs))
         rec(4)
-        self._gemm((self.Xr, self.Xrs, TX), (self.Wr, self.Wrs, TW), tokens, out, hid, self.Y)
+        self._gemm((self.Xr, self.Xrs, TX), (self.Wr, self.Wrs, TW), tokens, out, hid, self.Y, self.rb[0])
         rec(5)
-        self._gemm((self.Dr, self.Drs, TD), (self.Wc, self.Wcs, TW), tokens, hid, out, self.dX)
+        self._gemm((self.Dr, self.Drs, TD), (self.Wc, self.Wcs, TW), tokens, hid, out, self.dX, self.rb[1])
         rec(6)
         self._gemm((self.Dc, self.Dcs, TD), (self.Xc, self.Xcs, TX), out, hid, tokens, self.dW)
         rec(7)
@@ -155,14 +192,14 @@ class LinearStep:
             self._quantize(2, self.dY, TD, aD, q.SR, (self.Dr, self.Drs, self.Dc, self.Dcs))
             self.ev_dq.record(self.side)
             self.side.wait_event(self.ev_xw)
-            self._gemm((self.Dr, self.Drs, TD), (self.Wc, self.Wcs, TW), tokens, hid, out, self.dX)
+            self._gemm((self.Dr, self.Drs, TD), (self.Wc, self.Wcs, TW), tokens, hid, out, self.dX, self.rb[1])
             self.ev_side.record(self.side)
         with torch_.cuda.stream(self.side2):
             self.side2.wait_event(self.ev_dq)
             self.side2.wait_event(self.ev_xw)
             self._gemm((self.Dc, self.Dcs, TD), (self.Xc, self.Xcs, TX), out, hid, tokens, self.dW)
             self.ev_side2.record(self.side2)
-        self._gemm((self.Xr, self.Xrs, TX), (self.Wr, self.Wrs, TW), tokens, out, hid, self.Y)
+        self._gemm((self.Xr, self.Xrs, TX), (self.Wr, self.Wrs, TW), tokens, out, hid, self.Y, self.rb[0])
         main.wait_event(self.ev_side)
         main.wait_event(self.ev_side2)
         return self

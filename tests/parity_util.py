@@ -110,3 +110,34 @@ def bf16_ulp(x: np.ndarray) -> np.ndarray:
     a = np.abs(x).astype(np.float64)
     e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
     return 2.0 ** (e - 7)
+
+
+def sampled_check(A, B, Cdev32, rows, cols, fmt=0):
+    """Full row and column stripes of the reference via the oracle's exact
+    e*s operands and a binary64 matmul: the normwise error over the stripes
+    (returned) and the elementwise bound on every entry of them."""
+    pa, sa = A[0].cpu().numpy(), A[1].cpu().numpy()
+    pb, sb = B[0].cpu().numpy(), B[1].cpu().numpy()
+    alpha = float(A[2].item()) * float(B[2].item())
+    K = pa.shape[1] * 2
+    C = Cdev32
+    ea_r, eb = oracle.deq_es(pa[rows], sa[rows], fmt), oracle.deq_es(pb, sb, fmt)
+    R_rows, S_rows = alpha * (ea_r @ eb.T), alpha * (np.abs(ea_r) @ np.abs(eb).T)
+    del ea_r, eb
+    ea, eb_c = oracle.deq_es(pa, sa, fmt), oracle.deq_es(pb[cols], sb[cols], fmt)
+    R_cols, S_cols = alpha * (ea @ eb_c.T), alpha * (np.abs(ea) @ np.abs(eb_c).T)
+    del ea, eb_c
+    c_rows = C[torch.from_numpy(rows).to(C.device)].cpu().numpy().astype(np.float64)
+    c_cols = C[:, torch.from_numpy(cols).to(C.device)].cpu().numpy().astype(np.float64)
+    check_gemm_elementwise(c_rows, R_rows, S_rows, K)
+    check_gemm_elementwise(c_cols, R_cols, S_cols, K)
+    scale = max(np.abs(R_rows).max(), np.abs(R_cols).max())
+    e1 = np.abs(c_rows - R_rows).max() / scale
+    e2 = np.abs(c_cols - R_cols).max() / scale
+    return max(e1, e2)
+
+
+def stripes(n, rng, tile):
+    s = list(range(0, min(tile, n))) + list(range(max(n - tile, 0), n))
+    s += list(rng.choice(n, 64, replace=False))
+    return np.unique(np.array(s))

@@ -16,7 +16,7 @@ import torch
 import oracle
 from fp4_block_scaled_bf16_gb300 import workloads
 from parity_util import (GEMM_TOL, check_gemm_bf16, check_gemm_elementwise, gemm_abs_reference,
-                         gemm_error, to_dev)
+                         gemm_error, sampled_check, stripes, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -142,37 +142,6 @@ def test_zero_and_k0(lib):
     assert (out == 0).all()
 
 
-def _sampled_check(lib, A, B, Cdev32, rows, cols, fmt=0):
-    """Full row and column stripes of the reference via the oracle's exact
-    e*s operands and a binary64 matmul: the normwise error over the stripes
-    (returned) and the elementwise bound on every entry of them."""
-    pa, sa = A[0].cpu().numpy(), A[1].cpu().numpy()
-    pb, sb = B[0].cpu().numpy(), B[1].cpu().numpy()
-    alpha = float(A[2].item()) * float(B[2].item())
-    K = pa.shape[1] * 2
-    C = Cdev32
-    ea_r, eb = oracle.deq_es(pa[rows], sa[rows], fmt), oracle.deq_es(pb, sb, fmt)
-    R_rows, S_rows = alpha * (ea_r @ eb.T), alpha * (np.abs(ea_r) @ np.abs(eb).T)
-    del ea_r, eb
-    ea, eb_c = oracle.deq_es(pa, sa, fmt), oracle.deq_es(pb[cols], sb[cols], fmt)
-    R_cols, S_cols = alpha * (ea @ eb_c.T), alpha * (np.abs(ea) @ np.abs(eb_c).T)
-    del ea, eb_c
-    c_rows = C[torch.from_numpy(rows).to(C.device)].cpu().numpy().astype(np.float64)
-    c_cols = C[:, torch.from_numpy(cols).to(C.device)].cpu().numpy().astype(np.float64)
-    check_gemm_elementwise(c_rows, R_rows, S_rows, K)
-    check_gemm_elementwise(c_cols, R_cols, S_cols, K)
-    scale = max(np.abs(R_rows).max(), np.abs(R_cols).max())
-    e1 = np.abs(c_rows - R_rows).max() / scale
-    e2 = np.abs(c_cols - R_cols).max() / scale
-    return max(e1, e2)
-
-
-def _stripes(n, rng, tile):
-    s = list(range(0, min(tile, n))) + list(range(max(n - tile, 0), n))
-    s += list(rng.choice(n, 64, replace=False))
-    return np.unique(np.array(s))
-
-
 def test_full_fprop(lib):
     """Y = X W^T at 8192 x 16384 x 4096 (8B-class fprop), sampled stripes."""
     X, W = workloads.fprop_operands()
@@ -180,7 +149,7 @@ def test_full_fprop(lib):
     C = lib.gemm(*A, *B, dtype=torch.float32)
     torch.cuda.synchronize()
     rng = np.random.default_rng(0)
-    err = _sampled_check(lib, A, B, C, _stripes(8192, rng, 128), _stripes(16384, rng, 256))
+    err = sampled_check(A, B, C, stripes(8192, rng, 128), stripes(16384, rng, 256))
     assert err <= GEMM_TOL, err
 
 
@@ -196,14 +165,14 @@ def test_full_dgrad_wgrad(lib):
     rng = np.random.default_rng(1)
     dX = lib.gemm(qd.payload_row, qd.scales_row, qd.T, *Wc, dtype=torch.float32)
     torch.cuda.synchronize()
-    err = _sampled_check(lib, (qd.payload_row, qd.scales_row, qd.T), Wc, dX,
-                         _stripes(8192, rng, 128), _stripes(4096, rng, 256))
+    err = sampled_check((qd.payload_row, qd.scales_row, qd.T), Wc, dX,
+                         stripes(8192, rng, 128), stripes(4096, rng, 256))
     assert err <= GEMM_TOL, err
     del dX
     dW = lib.gemm(qd.payload_col, qd.scales_col, qd.T, *Xc, dtype=torch.float32)
     torch.cuda.synchronize()
-    err = _sampled_check(lib, (qd.payload_col, qd.scales_col, qd.T), Xc, dW,
-                         _stripes(16384, rng, 128), _stripes(4096, rng, 256))
+    err = sampled_check((qd.payload_col, qd.scales_col, qd.T), Xc, dW,
+                         stripes(16384, rng, 128), stripes(4096, rng, 256))
     assert err <= GEMM_TOL, err
 
 
@@ -225,6 +194,6 @@ def test_linear_block_shapes(lib, name):
         C = lib.gemm(*A, *B, dtype=torch.float32)
         torch.cuda.synchronize()
         assert C.shape == (M, N)
-        err = _sampled_check(lib, A, B, C, _stripes(M, rng, 128), _stripes(N, rng, 256))
+        err = sampled_check(A, B, C, stripes(M, rng, 128), stripes(N, rng, 256))
         assert err <= GEMM_TOL, (name, M, N, err)
         del C

@@ -135,3 +135,48 @@ def test_native_nvfp4_step_matches_oracle():
             R = oracle.gemm(_u8(A[0]), _u8(A[1]), Ta, _u8(B[0]), _u8(B[1]), Tb, oracle.UE4M3)
             check_gemm_bf16(C.float().cpu().numpy().astype(np.float64), R)
     assert fp4q.fp4q_get_device_status() == fp4q.OK
+
+
+def test_rebiased_step_matches_oracle():
+    """The UE5M3 step with fprop and dgrad on the native MMA through rebiased
+    scale codes: quantised bytes as in the emulated step, the fallback flags
+    equal to the oracle's fit decisions on the same codes, and all three GEMM
+    results within the BF16 bound of the oracle's UE5M3 contraction, on the
+    refresh steps of a drifting sequence."""
+    from fp4_block_scaled_bf16_gb300 import build
+    build.build()
+    from fp4_block_scaled_bf16_gb300 import fp4q
+    from fp4_block_scaled_bf16_gb300.linear_step import LinearStep
+
+    steps, period = 3, 2
+    amaxes = workloads.drift_amaxes(steps)
+    dev = torch.device("cuda")
+    X = torch.empty((TOK, HID), dtype=torch.bfloat16, device=dev)
+    W = torch.empty((OUT, HID), dtype=torch.bfloat16, device=dev)
+    dY = torch.empty((TOK, OUT), dtype=torch.bfloat16, device=dev)
+    step = LinearStep(X, W, dY, seed=7, period=period, rebias=True)
+    assert all(rb is not None for rb in step.rb)
+    for t in range(steps):
+        xb, wb, db = _inputs(t, amaxes)
+        X.copy_(workloads.to_torch_bf16(xb))
+        W.copy_(workloads.to_torch_bf16(wb))
+        dY.copy_(workloads.to_torch_bf16(db))
+        step.launches = 0
+        step.run_overlapped(periodic=True)
+        torch.cuda.synchronize()
+        # each of fprop and dgrad: two rebias launches, the native GEMM and
+        # the conditional emulated one
+        assert step.launches == 12 + (3 if t % period == 0 else 0) + (3 if t == 0 else 0), t
+        gT = [float(T.item()) for T in step.tensor_scales(periodic=True)]
+        fell = step.fallbacks()
+        for g, (A, B) in enumerate((((step.Xr, step.Xrs), (step.Wr, step.Wrs)),
+                                    ((step.Dr, step.Drs), (step.Wc, step.Wcs)))):
+            fits = oracle.rebias_scales(_u8(A[1]), True)[2] and oracle.rebias_scales(_u8(B[1]), False)[2]
+            assert fell[g] == (not fits), (t, g)
+        for C, A, B, Ta, Tb in ((step.Y, (step.Xr, step.Xrs), (step.Wr, step.Wrs), gT[0], gT[1]),
+                                (step.dX, (step.Dr, step.Drs), (step.Wc, step.Wcs), gT[2], gT[1]),
+                                (step.dW, (step.Dc, step.Dcs), (step.Xc, step.Xcs), gT[2], gT[0])):
+            R = oracle.gemm(_u8(A[0]), _u8(A[1]), Ta, _u8(B[0]), _u8(B[1]), Tb)
+            check_gemm_bf16(C.float().cpu().numpy().astype(np.float64), R)
+    assert fp4q.fp4q_get_device_status() == fp4q.OK
+

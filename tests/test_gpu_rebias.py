@@ -19,7 +19,7 @@ import torch
 import oracle
 from fp4_block_scaled_bf16_gb300 import workloads
 from parity_util import (GEMM_TOL, check_gemm_bf16, check_gemm_elementwise, gemm_abs_reference,
-                         gemm_error, np_u8, to_dev)
+                         gemm_error, np_u8, sampled_check, stripes, to_dev)
 from scale_codes import codes_with_span
 
 pytestmark = pytest.mark.gpu
@@ -192,3 +192,28 @@ def test_skip_and_run_flags_leave_out_untouched(lib):
     lib.fp4q_gemm_nvfp4_rebiased(A[0], a4, fa, A[2], B[0], b4, fb, B[2], M, N, K, None, out)
     torch.cuda.synchronize()
     assert torch.equal(out, n)
+
+
+def test_full_size_fprop_and_dgrad_take_the_native_path(lib):
+    """The 8B-class linear's fprop (8192 x 16384 x 4096) and dgrad (8192 x
+    4096 x 16384, dY with SR, seed 7) as the step runs them: every group fits
+    (the flag agrees with the oracle's decision on the same codes), and
+    sampled row and column stripes meet the bound against the oracle's UE5M3
+    contraction of the original operands."""
+    X, W = workloads.fprop_operands()
+    dY = workloads.backward_gradient()
+    qx = lib.quantize(to_dev(X))
+    qw = lib.quantize(to_dev(W), 2)
+    qd = lib.quantize(to_dev(dY), 2, None, 0, 1, 7)
+    rng = np.random.default_rng(2)
+    flag = torch.empty(1, dtype=torch.int32, device="cuda")
+    for A, B, M, N in (((qx.payload_row, qx.scales_row, qx.T), (qw.payload_row, qw.scales_row, qw.T), 8192, 16384),
+                       ((qd.payload_row, qd.scales_row, qd.T), (qw.payload_col, qw.scales_col, qw.T), 8192, 4096)):
+        C = lib.gemm_ue5m3_rebiased(*A, *B, dtype=torch.float32, nofit=flag)
+        torch.cuda.synchronize()
+        fits = oracle.rebias_scales(np_u8(A[1]), True)[2] and oracle.rebias_scales(np_u8(B[1]), False)[2]
+        assert fits and int(flag.item()) == 0, (M, N)
+        err = sampled_check(A, B, C, stripes(M, rng, 128), stripes(N, rng, 256))
+        assert err <= GEMM_TOL, (M, N, err)
+        del C
+
