@@ -63,8 +63,9 @@ def kernel_sources_sha(files):
 GEMM_SOURCES = ["gemm.cu", "fp4q_device.cuh", "fp4q_pipeline.cuh", "fp4q_tcgen05.cuh"]
 
 
-def committed_traffic(name, sources):
-    """DRAM bytes per launch from a committed ncu capture, or None when the
+def committed_traffic(name, sources, launch=None):
+    """DRAM bytes per launch from a committed ncu capture (of the launch
+    whose "gemm" entry starts with `launch`, else the mean), or None when the
     kernel's sources changed since the counters were taken."""
     p = os.path.join(ROOT, "profiles", name)
     if not os.path.exists(p):
@@ -72,6 +73,11 @@ def committed_traffic(name, sources):
     with open(p) as f:
         d = json.load(f)
     if d.get("source_sha") != kernel_sources_sha(sources):
+        return None
+    if launch is not None:
+        for l in d.get("launches", []):
+            if l.get("gemm", "").startswith(launch):
+                return l["dram_read_bytes"] + l["dram_write_bytes"]
         return None
     return d.get("dram_bytes_per_launch")
 
@@ -162,6 +168,11 @@ class ClockSampler:
                  "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            # nvidia-smi's start-up (NVML initialisation) takes CPU and driver
+            # time; the timed regions begin only once it is sampling
+            t0 = time.time()
+            while not self.rows and self.proc.poll() is None and time.time() - t0 < 5.0:
+                time.sleep(0.01)
         except Exception:
             self.proc = None
         return self
@@ -827,11 +838,13 @@ def main():
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor", "achieved": wgrad_tflops, "peak": bf16,
                      "unit": "TFLOP/s", "frac": wgrad_tflops / bf16 if bf16 else None,
-                     "traffic": committed_traffic("gemm_kernel_traffic_8B_linear.json", GEMM_SOURCES),
+                     "traffic": committed_traffic("gemm_kernel_traffic_8B_linear.json", GEMM_SOURCES, "wgrad"),
                      "kernel": "fp4q gemm_kernel (emulated UE5M3 GEMM; its wgrad launch, 16384 x 4096 x 8192)",
                      "peak_source": f"{src} bf16 ({'burst' if burst else 'sustained'}: the per-kernel "
                                     f"region ran {r['ms_serial_r']:.0f} ms)",
                      "all_three_emulated": {"achieved": gemm_tflops, "frac": gemm_tflops / bf16 if bf16 else None,
+                                            "traffic": committed_traffic("gemm_kernel_traffic_8B_linear.json",
+                                                                         GEMM_SOURCES),
                                             "note": "mean over fprop/dgrad/wgrad of the all-emulated one-stream step"}},
         "roofline_native_rebiased": {"bound": "tensor", "achieved": native_tflops, "peak": fp4_peak,
                                      "unit": "TFLOP/s", "frac": native_tflops / fp4_peak if fp4_peak else None,

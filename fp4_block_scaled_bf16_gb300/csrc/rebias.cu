@@ -57,6 +57,24 @@ __device__ __forceinline__ uint32_t word_at(const uint4& v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
+// Four codes per 32-bit word.  Codes order like their values (zero lowest),
+// so a group's largest and smallest non-zero binades are those of its
+// largest and smallest non-zero codes: a bytewise max, and a bytewise min
+// with the zero bytes raised to 0xFF (not a value).  When every non-zero code
+// of a fitting group is normal, the re-encode is the same for each of them --
+// exponent field E -> E - (E_top - 14), mantissa kept -- one bytewise add per
+// word, with the zero bytes masked back to zero.
+__device__ __forceinline__ uint32_t max_byte(uint32_t v) {
+  return max(max(v & 0xFFu, (v >> 8) & 0xFFu), max((v >> 16) & 0xFFu, v >> 24));
+}
+__device__ __forceinline__ uint32_t min_byte(uint32_t v) {
+  return min(min(v & 0xFFu, (v >> 8) & 0xFFu), min((v >> 16) & 0xFFu, v >> 24));
+}
+__device__ __forceinline__ uint4 add_nonzero4(const uint4& v, uint32_t k) {
+  return make_uint4(__vadd4(v.x, k) & __vcmpne4(v.x, 0u), __vadd4(v.y, k) & __vcmpne4(v.y, 0u),
+                    __vadd4(v.z, k) & __vcmpne4(v.z, 0u), __vadd4(v.w, k) & __vcmpne4(v.w, 0u));
+}
+
 // One warp per row (grid-stride over rows); nb % 16 == 0, rows 16-byte aligned.
 __global__ void __launch_bounds__(256) rebias_rows_kernel(const uint8_t* __restrict__ in, int64_t rows, int nb,
                                                           uint8_t* __restrict__ out, float* __restrict__ factor,
@@ -66,76 +84,66 @@ __global__ void __launch_bounds__(256) rebias_rows_kernel(const uint8_t* __restr
   const int chunks = nb >> 4;
   for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += nwarps) {
     const uint4* src = reinterpret_cast<const uint4*>(in + r * nb);
-    int emax = kNone, emin = -kNone;
+    uint32_t vmax = 0u, vmin = 0xFFFFFFFFu;
     for (int j = lane; j < chunks; j += 32) {
       const uint4 v = __ldg(src + j);
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
         const uint32_t word = word_at(v, w);
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          const uint32_t c = (word >> (8 * b)) & 0xFFu;
-          if (c != 0) {
-            uint32_t mn;
-            const int e = binade(c, mn);
-            emax = max(emax, e);
-            emin = min(emin, e);
-          }
-        }
+        vmax = __vmaxu4(vmax, word);
+        vmin = __vminu4(vmin, word | ~__vcmpne4(word, 0u));
       }
     }
-    emax = __reduce_max_sync(0xFFFFFFFFu, emax);
-    emin = __reduce_min_sync(0xFFFFFFFFu, emin);
-    const bool any = emax != kNone;
+    const uint32_t cmax = __reduce_max_sync(0xFFFFFFFFu, max_byte(vmax));
+    const uint32_t cmin = __reduce_min_sync(0xFFFFFFFFu, min_byte(vmin));
+    uint32_t mn;
+    const bool any = cmax != 0u;
+    const int emax = any ? binade(cmax, mn) : kNone;
     if (lane == 0) {
       factor[r] = any ? pow2(emax - 7) : 1.0f;
-      if (any && emin < emax - 13) atomicOr(nofit, 1);
+      if (any && binade(cmin, mn) < emax - 13) atomicOr(nofit, 1);
     }
     uint4* dst = reinterpret_cast<uint4*>(out + r * nb);
-    for (int j = lane; j < chunks; j += 32) {
-      const uint4 v = __ldg(src + j);
-      uint32_t o[4];
+    if (cmin >= 8u) {   // every non-zero code normal (an all-zero row: cmin = 0xFF)
+      const uint32_t k = ((14u - (cmax >> 3)) << 3 & 0xFFu) * 0x01010101u;
+      for (int j = lane; j < chunks; j += 32) dst[j] = add_nonzero4(__ldg(src + j), k);
+    } else {            // subnormal codes: normalised code by code
+      for (int j = lane; j < chunks; j += 32) {
+        const uint4 v = __ldg(src + j);
+        uint32_t o[4];
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const uint32_t word = word_at(v, w);
-        o[w] = 0;
+        for (int w = 0; w < 4; ++w) {
+          const uint32_t word = word_at(v, w);
+          o[w] = 0;
 #pragma unroll
-        for (int b = 0; b < 4; ++b) o[w] |= recode((word >> (8 * b)) & 0xFFu, emax) << (8 * b);
+          for (int b = 0; b < 4; ++b) o[w] |= recode((word >> (8 * b)) & 0xFFu, emax) << (8 * b);
+        }
+        dst[j] = make_uint4(o[0], o[1], o[2], o[3]);
       }
-      dst[j] = make_uint4(o[0], o[1], o[2], o[3]);
     }
   }
 }
 
-// The whole tensor with the fixed window (binades 3..16, factor 2^9),
-// grid-stride over 16-code chunks.
+// The whole tensor with the fixed window (binades 3..16, factor 2^9): a
+// non-zero code fits iff its exponent field is at least 18, and then its
+// field drops by 17 (the code by 0x88); grid-stride over 16-code chunks.
 __global__ void __launch_bounds__(256) rebias_tensor_kernel(const uint4* __restrict__ in, int64_t chunks,
                                                             uint4* __restrict__ out, float* __restrict__ factor,
                                                             int* nofit) {
   constexpr int kTop = 16;
   if (blockIdx.x == 0 && threadIdx.x == 0) factor[0] = pow2(kTop - 7);
-  bool bad = false;
+  uint32_t bad = 0u;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < chunks; j += stride) {
     const uint4 v = __ldg(in + j);
-    uint32_t o[4];
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
       const uint32_t word = word_at(v, w);
-      o[w] = 0;
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const uint32_t c = (word >> (8 * b)) & 0xFFu;
-        if (c != 0) {
-          uint32_t mn;
-          bad |= binade(c, mn) < kTop - 13;   // above the top is impossible: 0xFE is binade 16
-        }
-        o[w] |= recode(c, kTop) << (8 * b);
-      }
+      bad |= __vcmpltu4(word, 0x90909090u) & __vcmpne4(word, 0u);   // binade below 3
     }
-    out[j] = make_uint4(o[0], o[1], o[2], o[3]);
+    out[j] = add_nonzero4(v, 0x78787878u);   // - 0x88 per byte
   }
-  if (__any_sync(0xFFFFFFFFu, bad) && (threadIdx.x & 31) == 0) atomicOr(nofit, 1);
+  if (__any_sync(0xFFFFFFFFu, bad != 0u) && (threadIdx.x & 31) == 0) atomicOr(nofit, 1);
 }
 
 }  // namespace rebias
