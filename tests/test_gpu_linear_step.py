@@ -180,3 +180,43 @@ def test_rebiased_step_matches_oracle():
             check_gemm_bf16(C.float().cpu().numpy().astype(np.float64), R)
     assert fp4q.fp4q_get_device_status() == fp4q.OK
 
+
+def test_rebiased_step_falls_back_to_the_emulated_step_exactly():
+    """A W whose block scales span more than the per-tensor window (one
+    16 x 16 tile 2^-24 of the rest, so a row block and a column block):
+    both rebiased GEMMs' flags are set, the native
+    launches write nothing and the emulated ones run -- Y, dX and dW equal
+    the all-emulated step's bit for bit; with W back in range both flags
+    clear and the results stay within the BF16 bound of the emulated step."""
+    from fp4_block_scaled_bf16_gb300 import build
+    build.build()
+    from fp4_block_scaled_bf16_gb300 import fp4q
+    from fp4_block_scaled_bf16_gb300.linear_step import LinearStep
+
+    dev = torch.device("cuda")
+    xb = workloads.activations(TOK, HID, 7)
+    wf = workloads.bf16_bits_to_f32(workloads.weights(OUT, HID, 8))
+    db = workloads.gradients(TOK, OUT, 9)
+    for tiny, want in ((True, [True, True]), (False, [False, False])):
+        w = wf.copy()
+        if tiny:
+            w[0:16, 16:32] *= np.float32(2.0 ** -24)
+        wb = workloads.f32_to_bf16_bits(w)
+        X = workloads.to_torch_bf16(xb).to(dev)
+        W = workloads.to_torch_bf16(wb).to(dev)
+        dY = workloads.to_torch_bf16(db).to(dev)
+        fast = LinearStep(X, W, dY, seed=7, rebias=True)
+        ref = LinearStep(X, W, dY, seed=7)
+        fast.run_overlapped(periodic=True)
+        ref.run_overlapped(periodic=True)
+        torch.cuda.synchronize()
+        assert fast.fallbacks() == want
+        for a, b in ((fast.Y, ref.Y), (fast.dX, ref.dX), (fast.dW, ref.dW)):
+            if tiny:
+                assert torch.equal(a, b)
+            else:
+                R = b.float().cpu().numpy().astype(np.float64)
+                check_gemm_bf16(a.float().cpu().numpy().astype(np.float64), R)
+        assert torch.equal(fast.dW, ref.dW)   # wgrad is emulated in both
+    assert fp4q.fp4q_get_device_status() == fp4q.OK
+

@@ -217,3 +217,53 @@ def test_full_size_fprop_and_dgrad_take_the_native_path(lib):
         assert err <= GEMM_TOL, (M, N, err)
         del C
 
+
+def test_empty_shapes_and_k0(lib):
+    """No rows: the per-tensor factor is still written (2^9) and the flag
+    untouched; K = 0: both GEMM entry points write zeros whatever the flag;
+    M = 0: nothing is launched."""
+    e = torch.empty((0, 16), dtype=torch.uint8, device="cuda")
+    f = torch.full((1,), -1.0, device="cuda")
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lib.fp4q_rebias_scales(e, 0, 16, False, torch.empty_like(e), f, flag)
+    torch.cuda.synchronize()
+    assert float(f.item()) == 512.0 and int(flag.item()) == 0
+    one = torch.ones(1, device="cuda")
+    z = torch.empty((16, 0), dtype=torch.uint8, device="cuda")
+    set_ = torch.ones(1, dtype=torch.int32, device="cuda")
+    for out in (torch.full((16, 32), 7.0, device="cuda"), torch.full((16, 32), 7.0, device="cuda").bfloat16()):
+        lib.fp4q_gemm_nvfp4_rebiased(z, z, torch.ones(16, device="cuda"), one, torch.empty((32, 0), dtype=torch.uint8,
+                                     device="cuda"), torch.empty((32, 0), dtype=torch.uint8, device="cuda"), one, one,
+                                     16, 32, 0, set_, out)
+        torch.cuda.synchronize()
+        assert (out == 0).all()
+        out.fill_(7.0)
+        lib.fp4q_gemm_if(z, z, one, torch.empty((32, 0), dtype=torch.uint8, device="cuda"),
+                         torch.empty((32, 0), dtype=torch.uint8, device="cuda"), one, 16, 32, 0, lib.UE5M3,
+                         torch.zeros(1, dtype=torch.int32, device="cuda"), out)
+        torch.cuda.synchronize()
+        assert (out == 0).all()
+    out = torch.empty((0, 32), device="cuda")
+    lib.fp4q_gemm_if(torch.empty((0, 128), dtype=torch.uint8, device="cuda"),
+                     torch.empty((0, 16), dtype=torch.uint8, device="cuda"), one,
+                     torch.empty((32, 128), dtype=torch.uint8, device="cuda"),
+                     torch.empty((32, 16), dtype=torch.uint8, device="cuda"), one, 0, 32, 256, lib.UE5M3, set_, out)
+    torch.cuda.synchronize()
+
+
+def test_per_tensor_b_that_does_not_fit_falls_back(lib):
+    """B's fixed window fails (one B block far below the tensor's amax):
+    the sequence equals fp4q_gemm bit for bit, BF16 and FP32."""
+    M, N, K = 256, 256, 512
+    a = workloads.activations(M, K, 21)
+    bf = workloads.bf16_bits_to_f32(workloads.weights(N, K, 22))
+    bf[7, 32:48] *= np.float32(2.0 ** -24)
+    A, B = _quantised(lib, a, workloads.f32_to_bf16_bits(bf))
+    assert not oracle.rebias_scales(np_u8(B[1]), per_row=False)[2]
+    flag = torch.empty(1, dtype=torch.int32, device="cuda")
+    for dt in (torch.float32, torch.bfloat16):
+        C = lib.gemm_ue5m3_rebiased(*A, *B, dtype=dt, nofit=flag)
+        E = lib.gemm(*A, *B, dtype=dt)
+        torch.cuda.synchronize()
+        assert int(flag.item()) == 1 and torch.equal(C, E)
+
