@@ -474,7 +474,21 @@ def run_gpu(args, rank, world):
             for j in range(10):
                 fp4q.fp4q_quantize(rot[id(x)][j % 2], fp4q.AXIS_BOTH_2D, fp4q.UE5M3, Tn, rnd, 7, *outs)
         rates[name] = x.numel() * DUAL_BYTES_PER_ELEM / (_graph_ms(run2d, 10) * 1e-3) / 1e9
-    del W2, dY2, rot
+    # the step's dual-axis quantisers on their own (graph replays, as above):
+    # X (64 MiB) rotates through four distinct copies, W and dY through two,
+    # so every rotation spans at least twice the L2
+    Xs = [step.X] + [torch.roll(step.X, shifts=1024 * i, dims=0).contiguous() for i in (1, 2, 3)]
+    dual = {}
+    for name, xs, rnd, outs, Ti in (("X_dual_rne", Xs, fp4q.RNE, (step.Xr, step.Xrs, step.Xc, step.Xcs), 0),
+                                    ("W_dual_rne", rot[id(step.W)], fp4q.RNE, (step.Wr, step.Wrs, step.Wc, step.Wcs), 1),
+                                    ("dY_dual_sr", rot[id(step.dY)], fp4q.SR, (step.Dr, step.Drs, step.Dc, step.Dcs), 2)):
+        Tn = step.T[Ti:Ti + 1]
+
+        def run_dual(xs=xs, rnd=rnd, outs=outs, Tn=Tn):
+            for j in range(8):
+                fp4q.fp4q_quantize(xs[j % len(xs)], fp4q.AXIS_BOTH, fp4q.UE5M3, Tn, rnd, 7, *outs)
+        dual[name] = xs[0].numel() * DUAL_BYTES_PER_ELEM / (_graph_ms(run_dual, 8) * 1e-3) / 1e9
+    del W2, dY2, rot, Xs
     # periodic scaling (config 4's per-step quantisation): a 4096 x 4096
     # tensor quantised row-wise (RNE) with the fused amax that the next
     # refresh uses, the tensor scale taken from an earlier step (no amax
@@ -589,7 +603,7 @@ def run_gpu(args, rank, world):
         del lin
 
     return dict(ms=ms, ms_emulated=ms_emulated, ms_current=ms_current, refreshes=refreshes, ms_serial=ms_serial,
-                ms_serial_r=ms_serial_r, t_gr=t_gr, parts=parts, fallbacks=fallbacks,
+                ms_serial_r=ms_serial_r, t_gr=t_gr, parts=parts, fallbacks=fallbacks, dual=dual,
                 native=native, fused=fused, block=block, t_scale=t_scale, t_q=(t_qx, t_qw, t_qd), t_g=t_g, launches=launches, rates=rates,
                 clocks=clk.summary(), status=status, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, link=link, affinity=affinity,
                 elems=(X.numel(), W.numel(), dY.numel()))
@@ -798,7 +812,11 @@ def main():
     fp4_peak = bf16 * FP4_OVER_BF16 if bf16 else None
     nX, nW, nD = r["elems"]
     q_bytes = [n * DUAL_BYTES_PER_ELEM for n in (nX, nW, nD)]
-    q_gbs = [b / (t * 1e-3) / 1e9 for b, t in zip(q_bytes, r["t_q"])]
+    # the dual-axis quantisers: their own rate (graph replays), and the rate
+    # of their launch inside the one-stream pass of the step (CUDA events
+    # around each call, so the host's gaps between calls count too)
+    q_gbs_step = [b / (t * 1e-3) / 1e9 for b, t in zip(q_bytes, r["t_q"])]
+    q_gbs = [r["dual"][k] for k in ("X_dual_rne", "W_dual_rne", "dY_dual_sr")]
     cpu = None
     if not args.no_cpu_baseline:
         # about 30 s of CPU work spread over the host cores
@@ -856,6 +874,8 @@ def main():
                               "frac": dict({k: g / hbm for k, g in zip(("X_dual_rne", "W_dual_rne", "dY_dual_sr"), q_gbs)},
                                            **{k: g / hbm for k, g in r["rates"].items()}) if hbm else None,
                               "peak_source": f"{src} hbm",
+                              "dual_axis_in_step_gbs": dict(zip(("X_dual_rne", "W_dual_rne", "dY_dual_sr"),
+                                                                q_gbs_step)),
                               "issue_roofline": issue_roofline(q_gbs, (r["clocks"] or {}).get("sm_mhz"))},
         "breakdown_ms": {"amax_scale": r["t_scale"], "quantize_X": r["t_q"][0], "quantize_W": r["t_q"][1],
                          "quantize_dY": r["t_q"][2], "fprop": r["t_gr"][0], "dgrad": r["t_gr"][1],
