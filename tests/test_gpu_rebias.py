@@ -267,3 +267,36 @@ def test_per_tensor_b_that_does_not_fit_falls_back(lib):
         torch.cuda.synchronize()
         assert int(flag.item()) == 1 and torch.equal(C, E)
 
+
+def test_full_size_rebias_bytes(lib):
+    """The step's four rebias inputs at the 8B-class sizes, byte for byte
+    against the oracle: X's and dY's row-wise codes per row (8192 x 256 and
+    8192 x 1024), W's row-wise and column-wise codes per tensor (16384 x 256
+    and 4096 x 1024)."""
+    X, W = workloads.fprop_operands()
+    dY = workloads.backward_gradient()
+    qx = lib.quantize(to_dev(X))
+    qw = lib.quantize(to_dev(W), 2)
+    qd = lib.quantize(to_dev(dY), 2, None, 0, 1, 7)
+    for codes, per_row in ((qx.scales_row, True), (qd.scales_row, True), (qw.scales_row, False),
+                           (qw.scales_col, False)):
+        c4, f, flag = lib.rebias_scales(codes, per_row)
+        torch.cuda.synchronize()
+        r4, rf, fits = oracle.rebias_scales(np_u8(codes), per_row=per_row)
+        assert fits and int(flag.item()) == 0, (tuple(codes.shape), per_row)
+        np.testing.assert_array_equal(np_u8(c4), r4)
+        np.testing.assert_array_equal(f.cpu().numpy(), rf)
+
+
+def test_rows_beyond_one_pass_of_the_grid(lib):
+    """More rows than the per-row kernel's grid holds warps (each warp then
+    takes several rows), mixed spans and zero rows."""
+    rng = np.random.default_rng(77)
+    codes = codes_with_span(rng, 30000, 16, 9)
+    codes[rng.random(30000) < 0.02] = 0
+    c4, f, flag = _rebias(lib, codes, True)
+    r4, rf, fits = oracle.rebias_scales(codes, per_row=True)
+    assert fits and flag == 0
+    np.testing.assert_array_equal(c4, r4)
+    np.testing.assert_array_equal(f, rf)
+
