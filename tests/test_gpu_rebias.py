@@ -300,3 +300,28 @@ def test_rows_beyond_one_pass_of_the_grid(lib):
     np.testing.assert_array_equal(c4, r4)
     np.testing.assert_array_equal(f, rf)
 
+
+@pytest.mark.parametrize("name", ["qkv", "out", "down"])
+def test_block_linears_through_the_native_path(lib, name):
+    """The 8B-class block's other linears (qkv 4096->6144, out 4096->4096,
+    down 16384->4096; up is the full-size case above), 8192 tokens: fprop
+    and dgrad through rebiased codes, as the block step runs them -- the
+    flag agrees with the oracle's fit decision and sampled row and column
+    stripes meet the bound against the oracle's UE5M3 contraction."""
+    X, W, dY = workloads.linear_block(name)
+    fin, fout = workloads.LINEARS[name]
+    qx = lib.quantize(to_dev(X))
+    qw = lib.quantize(to_dev(W), 2)
+    qd = lib.quantize(to_dev(dY), 2, None, 0, 1, 7)
+    rng = np.random.default_rng(len(name) + 100)
+    flag = torch.empty(1, dtype=torch.int32, device="cuda")
+    for A, B, M, N in (((qx.payload_row, qx.scales_row, qx.T), (qw.payload_row, qw.scales_row, qw.T), 8192, fout),
+                       ((qd.payload_row, qd.scales_row, qd.T), (qw.payload_col, qw.scales_col, qw.T), 8192, fin)):
+        C = lib.gemm_ue5m3_rebiased(*A, *B, dtype=torch.float32, nofit=flag)
+        torch.cuda.synchronize()
+        fits = oracle.rebias_scales(np_u8(A[1]), True)[2] and oracle.rebias_scales(np_u8(B[1]), False)[2]
+        assert int(flag.item()) == int(not fits), (name, M, N)
+        err = sampled_check(A, B, C, stripes(M, rng, 128), stripes(N, rng, 256))
+        assert err <= GEMM_TOL, (name, M, N, err)
+        del C
+
