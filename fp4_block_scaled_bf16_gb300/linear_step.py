@@ -88,9 +88,19 @@ class LinearStep:
                                   torch.empty((n, k // 16), **u8), torch.empty(1, **f32), self.nofit[g:g + 1])
         self.scalers = [PeriodicScaler(period, fmt, device=dev, lib=q) for _ in range(3)]
         self.launches = 0
-        self.side = torch.cuda.Stream(device=dev)
-        self.side2 = torch.cuda.Stream(device=dev)
-        self.ev_start, self.ev_xw, self.ev_side, self.ev_dq, self.ev_side2 = (torch.cuda.Event() for _ in range(5))
+        # run_overlapped's work runs on streams of the highest priority, the
+        # emulated fallbacks of fprop and dgrad (which return at once unless
+        # a group did not fit) on one of the lowest: their CTAs then take SMs
+        # the step's kernels leave idle instead of queueing between them
+        least, greatest = torch.cuda.Stream.priority_range()
+        self.main = torch.cuda.Stream(device=dev, priority=greatest)
+        self.side = torch.cuda.Stream(device=dev, priority=greatest)
+        self.side2 = torch.cuda.Stream(device=dev, priority=greatest)
+        self.fallback = torch.cuda.Stream(device=dev, priority=least)
+        self.ev_start, self.ev_xw, self.ev_side, self.ev_dq, self.ev_side2, self.ev_main = (
+            torch.cuda.Event() for _ in range(6))
+        self.ev_rb = [torch.cuda.Event(), torch.cuda.Event()]
+        self.ev_fb = [torch.cuda.Event(), torch.cuda.Event()]
 
     # ------------------------------------------------------------ pieces
     def _scale(self, i: int, x: torch.Tensor, periodic: bool):
@@ -115,7 +125,11 @@ class LinearStep:
         if amax is not None:
             self.scalers[i].advance()
 
-    def _gemm(self, A, B, M, N, K, out, rb=None):
+    def _gemm(self, A, B, M, N, K, out, rb=None, g=None):
+        """One GEMM on the current stream.  Through rebiased codes (rb), the
+        emulated fallback goes on the low-priority stream when g (0 fprop,
+        1 dgrad) is given -- after the rebias launches, joined back before
+        anything later on the current stream -- else in line."""
         q = self.q
         if self.native:
             q.fp4q_gemm_nvfp4(*A, *B, M, N, K, out)
@@ -124,8 +138,18 @@ class LinearStep:
             flag.zero_()
             q.fp4q_rebias_scales(A[1], M, K // 16, True, a4, fa, flag)
             q.fp4q_rebias_scales(B[1], N, K // 16, False, b4, fb, flag)
-            q.fp4q_gemm_nvfp4_rebiased(A[0], a4, fa, A[2], B[0], b4, fb, B[2], M, N, K, flag, out)
-            q.fp4q_gemm_if(*A, *B, M, N, K, self.fmt, flag, out)
+            if g is None:
+                q.fp4q_gemm_nvfp4_rebiased(A[0], a4, fa, A[2], B[0], b4, fb, B[2], M, N, K, flag, out)
+                q.fp4q_gemm_if(*A, *B, M, N, K, self.fmt, flag, out)
+            else:
+                cur = torch.cuda.current_stream()
+                self.ev_rb[g].record(cur)
+                q.fp4q_gemm_nvfp4_rebiased(A[0], a4, fa, A[2], B[0], b4, fb, B[2], M, N, K, flag, out)
+                self.fallback.wait_event(self.ev_rb[g])
+                with torch.cuda.stream(self.fallback):
+                    q.fp4q_gemm_if(*A, *B, M, N, K, self.fmt, flag, out)
+                    self.ev_fb[g].record(self.fallback)
+                cur.wait_event(self.ev_fb[g])   # exactly one of the two wrote `out`
             self.launches += 3
         else:
             q.fp4q_gemm(*A, *B, M, N, K, self.fmt, out)
@@ -169,37 +193,45 @@ class LinearStep:
         return self
 
     def run_overlapped(self, periodic: bool = False):
-        """The same launches on three streams, in the step's dependency
-        order: the caller's stream takes X and W (scales, dual-axis RNE
+        """The same launches on three streams of the highest priority, in
+        the step's dependency order: one takes X and W (scales, dual-axis RNE
         quantisation) and fprop; a side stream takes dY's scale and dual-axis
         SR quantisation at the same time, then dgrad once W is quantised; a
         second side stream runs wgrad once dY and X are quantised, so that the
-        three GEMMs fill one another's last waves.  The caller's stream waits
-        for both side streams at the end, so a step ends when all of its work
-        is done and the next one starts from a clean slate."""
+        three GEMMs fill one another's last waves (fprop's and dgrad's
+        emulated fallbacks on the low-priority stream).  All start after the
+        caller's stream reaches the step, and the caller's stream waits for
+        all of them at the end, so a step ends when all of its work is done
+        and the next one starts from a clean slate."""
         q, torch_ = self.q, torch
         tokens, hid, out = self.dims
-        main = torch_.cuda.current_stream()
-        self.ev_start.record(main)
-        TX, aX = self._scale(0, self.X, periodic)
-        TW, aW = self._scale(1, self.W, periodic)
-        self._quantize(0, self.X, TX, aX, q.RNE, (self.Xr, self.Xrs, self.Xc, self.Xcs))
-        self._quantize(1, self.W, TW, aW, q.RNE, (self.Wr, self.Wrs, self.Wc, self.Wcs))
-        self.ev_xw.record(main)
+        caller = torch_.cuda.current_stream()
+        main = self.main
+        self.ev_start.record(caller)
+        main.wait_event(self.ev_start)
+        with torch_.cuda.stream(main):
+            TX, aX = self._scale(0, self.X, periodic)
+            TW, aW = self._scale(1, self.W, periodic)
+            self._quantize(0, self.X, TX, aX, q.RNE, (self.Xr, self.Xrs, self.Xc, self.Xcs))
+            self._quantize(1, self.W, TW, aW, q.RNE, (self.Wr, self.Wrs, self.Wc, self.Wcs))
+            self.ev_xw.record(main)
         with torch_.cuda.stream(self.side):
             self.side.wait_event(self.ev_start)
             TD, aD = self._scale(2, self.dY, periodic)
             self._quantize(2, self.dY, TD, aD, q.SR, (self.Dr, self.Drs, self.Dc, self.Dcs))
             self.ev_dq.record(self.side)
             self.side.wait_event(self.ev_xw)
-            self._gemm((self.Dr, self.Drs, TD), (self.Wc, self.Wcs, TW), tokens, hid, out, self.dX, self.rb[1])
+            self._gemm((self.Dr, self.Drs, TD), (self.Wc, self.Wcs, TW), tokens, hid, out, self.dX, self.rb[1], 1)
             self.ev_side.record(self.side)
         with torch_.cuda.stream(self.side2):
             self.side2.wait_event(self.ev_dq)
             self.side2.wait_event(self.ev_xw)
             self._gemm((self.Dc, self.Dcs, TD), (self.Xc, self.Xcs, TX), out, hid, tokens, self.dW)
             self.ev_side2.record(self.side2)
-        self._gemm((self.Xr, self.Xrs, TX), (self.Wr, self.Wrs, TW), tokens, out, hid, self.Y, self.rb[0])
-        main.wait_event(self.ev_side)
-        main.wait_event(self.ev_side2)
+        with torch_.cuda.stream(main):
+            self._gemm((self.Xr, self.Xrs, TX), (self.Wr, self.Wrs, TW), tokens, out, hid, self.Y, self.rb[0], 0)
+            self.ev_main.record(main)
+        caller.wait_event(self.ev_main)
+        caller.wait_event(self.ev_side)
+        caller.wait_event(self.ev_side2)
         return self
