@@ -220,3 +220,65 @@ def test_rebiased_step_falls_back_to_the_emulated_step_exactly():
         assert torch.equal(fast.dW, ref.dW)   # wgrad is emulated in both
     assert fp4q.fp4q_get_device_status() == fp4q.OK
 
+
+def test_full_size_step_fallback_is_the_emulated_step():
+    """The 8B-class step (8192 tokens, 4096 -> 16384) with one 16 x 16 tile of
+    W 2^-24 of the rest: both rebiased GEMMs fall back on the device and the
+    step's Y, dX, dW equal the all-emulated step's bit for bit (every cluster
+    of both launches took the same decision)."""
+    from fp4_block_scaled_bf16_gb300 import build
+    build.build()
+    from fp4_block_scaled_bf16_gb300 import fp4q
+    from fp4_block_scaled_bf16_gb300.linear_step import LinearStep
+
+    dev = torch.device("cuda")
+    X, Wb = workloads.fprop_operands()
+    w = workloads.bf16_bits_to_f32(Wb)
+    w[4096:4112, 1024:1040] *= np.float32(2.0 ** -24)
+    Xd = workloads.to_torch_bf16(X).to(dev)
+    Wd = workloads.to_torch_bf16(workloads.f32_to_bf16_bits(w)).to(dev)
+    Dd = workloads.to_torch_bf16(workloads.backward_gradient()).to(dev)
+    fast = LinearStep(Xd, Wd, Dd, seed=7, rebias=True)
+    ref = LinearStep(Xd, Wd, Dd, seed=7)
+    for _ in range(2):
+        fast.run_overlapped(periodic=True)
+        ref.run_overlapped(periodic=True)
+    torch.cuda.synchronize()
+    assert fast.fallbacks() == [True, True]
+    for a, b in ((fast.Y, ref.Y), (fast.dX, ref.dX), (fast.dW, ref.dW)):
+        assert torch.equal(a, b)
+    assert fp4q.fp4q_get_device_status() == fp4q.OK
+
+
+def test_two_steps_on_two_caller_streams():
+    """Two rebiased steps (separate inputs, buffers and internal streams)
+    issued from two caller streams at once give the results each gives
+    alone."""
+    from fp4_block_scaled_bf16_gb300 import build
+    build.build()
+    from fp4_block_scaled_bf16_gb300 import fp4q
+    from fp4_block_scaled_bf16_gb300.linear_step import LinearStep
+
+    dev = torch.device("cuda")
+    steps = []
+    for k in range(2):
+        X = workloads.to_torch_bf16(workloads.activations(TOK, HID, 50 + k)).to(dev)
+        W = workloads.to_torch_bf16(workloads.weights(OUT, HID, 60 + k)).to(dev)
+        dY = workloads.to_torch_bf16(workloads.gradients(TOK, OUT, 70 + k)).to(dev)
+        steps.append(LinearStep(X, W, dY, seed=7, rebias=True))
+    alone = []
+    for st in steps:
+        st.run_overlapped()
+        torch.cuda.synchronize()
+        alone.append([t.clone() for t in (st.Y, st.dX, st.dW)])
+    callers = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for _ in range(3):
+        for st, cs in zip(steps, callers):
+            with torch.cuda.stream(cs):
+                st.run_overlapped()
+    torch.cuda.synchronize()
+    for st, ref in zip(steps, alone):
+        for a, b in zip((st.Y, st.dX, st.dW), ref):
+            assert torch.equal(a, b)
+    assert fp4q.fp4q_get_device_status() == fp4q.OK
+
