@@ -88,14 +88,17 @@ class LinearStep:
                                   torch.empty((n, k // 16), **u8), torch.empty(1, **f32), self.nofit[g:g + 1])
         self.scalers = [PeriodicScaler(period, fmt, device=dev, lib=q) for _ in range(3)]
         self.launches = 0
-        # run_overlapped's work runs on streams of the highest priority, the
-        # emulated fallbacks of fprop and dgrad (which return at once unless
-        # a group did not fit) on one of the lowest: their CTAs then take SMs
-        # the step's kernels leave idle instead of queueing between them
+        # run_overlapped's streams, by priority: X, W and fprop highest, dY
+        # and dgrad one step lower, wgrad (the long emulated GEMM, whose CTAs
+        # fill what the others leave) and the emulated fallbacks of fprop and
+        # dgrad (which return at once unless a group did not fit) lowest --
+        # the fallbacks' CTAs then take SMs the step's kernels leave idle
+        # instead of queueing between them
         least, greatest = torch.cuda.Stream.priority_range()
+        second = min(greatest + 1, least)
         self.main = torch.cuda.Stream(device=dev, priority=greatest)
-        self.side = torch.cuda.Stream(device=dev, priority=greatest)
-        self.side2 = torch.cuda.Stream(device=dev, priority=greatest)
+        self.side = torch.cuda.Stream(device=dev, priority=second)
+        self.side2 = torch.cuda.Stream(device=dev, priority=least)
         self.fallback = torch.cuda.Stream(device=dev, priority=least)
         self.ev_start, self.ev_xw, self.ev_side, self.ev_dq, self.ev_side2, self.ev_main = (
             torch.cuda.Event() for _ in range(6))
@@ -193,13 +196,13 @@ class LinearStep:
         return self
 
     def run_overlapped(self, periodic: bool = False):
-        """The same launches on three streams of the highest priority, in
-        the step's dependency order: one takes X and W (scales, dual-axis RNE
-        quantisation) and fprop; a side stream takes dY's scale and dual-axis
-        SR quantisation at the same time, then dgrad once W is quantised; a
-        second side stream runs wgrad once dY and X are quantised, so that the
-        three GEMMs fill one another's last waves (fprop's and dgrad's
-        emulated fallbacks on the low-priority stream).  All start after the
+        """The same launches on three streams, in the step's dependency
+        order: one takes X and W (scales, dual-axis RNE quantisation) and
+        fprop; a side stream takes dY's scale and dual-axis SR quantisation
+        at the same time, then dgrad once W is quantised; a second side
+        stream runs wgrad once dY and X are quantised, so that the three GEMMs
+        fill one another's last waves (priorities and fprop's and dgrad's
+        emulated fallbacks: see the constructor).  All start after the
         caller's stream reaches the step, and the caller's stream waits for
         all of them at the end, so a step ends when all of its work is done
         and the next one starts from a clean slate."""
