@@ -141,3 +141,14 @@ def stripes(n, rng, tile):
     s = list(range(0, min(tile, n))) + list(range(max(n - tile, 0), n))
     s += list(rng.choice(n, 64, replace=False))
     return np.unique(np.array(s))
+
+
+def extreme_rows(bits: np.ndarray, k: int = 4) -> np.ndarray:
+    """The k rows of a BF16 matrix with the largest and the k with the
+    smallest non-zero row amax (a dgrad's rows of extreme gradient
+    magnitude, where a scale or factor error would hide below the rest)."""
+    a = np.abs(workloads.bf16_bits_to_f32(bits)).max(axis=1)
+    order = np.argsort(a)
+    nz = order[a[order] > 0]
+    return np.unique(np.r_[nz[:k], nz[-k:]])
+

@@ -16,7 +16,7 @@ import torch
 import oracle
 from fp4_block_scaled_bf16_gb300 import workloads
 from parity_util import (GEMM_TOL, check_gemm_bf16, check_gemm_elementwise, gemm_abs_reference,
-                         gemm_error, sampled_check, stripes, to_dev)
+                         extreme_rows, gemm_error, sampled_check, stripes, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -165,8 +165,8 @@ def test_full_dgrad_wgrad(lib):
     rng = np.random.default_rng(1)
     dX = lib.gemm(qd.payload_row, qd.scales_row, qd.T, *Wc, dtype=torch.float32)
     torch.cuda.synchronize()
-    err = sampled_check((qd.payload_row, qd.scales_row, qd.T), Wc, dX,
-                         stripes(8192, rng, 128), stripes(4096, rng, 256))
+    rows = np.unique(np.r_[stripes(8192, rng, 128), extreme_rows(dY)])   # and the extreme-magnitude tokens
+    err = sampled_check((qd.payload_row, qd.scales_row, qd.T), Wc, dX, rows, stripes(4096, rng, 256))
     assert err <= GEMM_TOL, err
     del dX
     dW = lib.gemm(qd.payload_col, qd.scales_col, qd.T, *Xc, dtype=torch.float32)

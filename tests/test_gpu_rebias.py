@@ -19,7 +19,7 @@ import torch
 import oracle
 from fp4_block_scaled_bf16_gb300 import workloads
 from parity_util import (GEMM_TOL, check_gemm_bf16, check_gemm_elementwise, gemm_abs_reference,
-                         gemm_error, np_u8, sampled_check, stripes, to_dev)
+                         extreme_rows, gemm_error, np_u8, sampled_check, stripes, to_dev)
 from scale_codes import codes_with_span
 
 pytestmark = pytest.mark.gpu
@@ -207,13 +207,17 @@ def test_full_size_fprop_and_dgrad_take_the_native_path(lib):
     qd = lib.quantize(to_dev(dY), 2, None, 0, 1, 7)
     rng = np.random.default_rng(2)
     flag = torch.empty(1, dtype=torch.int32, device="cuda")
-    for A, B, M, N in (((qx.payload_row, qx.scales_row, qx.T), (qw.payload_row, qw.scales_row, qw.T), 8192, 16384),
-                       ((qd.payload_row, qd.scales_row, qd.T), (qw.payload_col, qw.scales_col, qw.T), 8192, 4096)):
+    for A, B, M, N, extra in (((qx.payload_row, qx.scales_row, qx.T), (qw.payload_row, qw.scales_row, qw.T), 8192,
+                               16384, extreme_rows(X)),
+                              ((qd.payload_row, qd.scales_row, qd.T), (qw.payload_col, qw.scales_col, qw.T), 8192,
+                               4096, extreme_rows(dY))):
         C = lib.gemm_ue5m3_rebiased(*A, *B, dtype=torch.float32, nofit=flag)
         torch.cuda.synchronize()
         fits = oracle.rebias_scales(np_u8(A[1]), True)[2] and oracle.rebias_scales(np_u8(B[1]), False)[2]
         assert fits and int(flag.item()) == 0, (M, N)
-        err = sampled_check(A, B, C, stripes(M, rng, 128), stripes(N, rng, 256))
+        # rows of extreme magnitude carry the extreme per-row factors
+        rows = np.unique(np.r_[stripes(M, rng, 128), extra])
+        err = sampled_check(A, B, C, rows, stripes(N, rng, 256))
         assert err <= GEMM_TOL, (M, N, err)
         del C
 
