@@ -348,45 +348,46 @@ def run_gpu(args, rank, world):
 
     # ---- end to end through the API with host buffers: every step copies its
     # inputs host -> device and its results device -> host.  Copies run on
-    # their own streams and overlap the previous/next step's kernels (two
-    # device buffer sets), which is how a training loop feeds the GPU.
-    hY = [torch.empty(step.Y.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    hdX = [torch.empty(step.dX.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    hdW = [torch.empty(step.dW.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    steps2 = [rstep, LinearStep(torch.empty_like(X), torch.empty_like(W), torch.empty_like(dY), seed=7,
-                                rebias=True)]
+    # their own streams and overlap the neighbouring steps' kernels (NSETS
+    # device buffer sets in turn), which is how a training loop feeds the GPU.
+    NSETS = args.e2e_sets
+    hY = [torch.empty(step.Y.shape, dtype=torch.bfloat16).pin_memory() for _ in range(NSETS)]
+    hdX = [torch.empty(step.dX.shape, dtype=torch.bfloat16).pin_memory() for _ in range(NSETS)]
+    hdW = [torch.empty(step.dW.shape, dtype=torch.bfloat16).pin_memory() for _ in range(NSETS)]
+    steps2 = [rstep] + [LinearStep(torch.empty_like(X), torch.empty_like(W), torch.empty_like(dY), seed=7,
+                                   rebias=True) for _ in range(NSETS - 1)]
     s_h2d, s_cmp, s_d2h = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-    e2e_warm = 3
-    e2e_steps = max(2, min(args.steps, 8))
+    e2e_warm = NSETS + 1
+    e2e_steps = max(2, args.steps)
     n_e2e = e2e_warm + e2e_steps
     ev_in = [torch.cuda.Event() for _ in range(n_e2e)]
     ev_done = [torch.cuda.Event() for _ in range(n_e2e)]
     ev_out = [torch.cuda.Event() for _ in range(n_e2e)]
 
     def e2e_step(i):
-        st_i = steps2[i % 2]
+        st_i = steps2[i % NSETS]
         with torch.cuda.stream(s_h2d):
-            if i >= 2:
-                s_h2d.wait_event(ev_done[i - 2])          # buffer set free again
+            if i >= NSETS:
+                s_h2d.wait_event(ev_done[i - NSETS])      # buffer set free again
             st_i.X.copy_(hX, non_blocking=True)
             st_i.W.copy_(hW, non_blocking=True)
             st_i.dY.copy_(hD, non_blocking=True)
             ev_in[i].record(s_h2d)
         with torch.cuda.stream(s_cmp):
             s_cmp.wait_event(ev_in[i])
-            if i >= 2:
-                s_cmp.wait_event(ev_out[i - 2])          # outputs read back
+            if i >= NSETS:
+                s_cmp.wait_event(ev_out[i - NSETS])      # outputs read back
             st_i.run_overlapped(periodic=True)
             ev_done[i].record(s_cmp)
         with torch.cuda.stream(s_d2h):
             s_d2h.wait_event(ev_done[i])
-            hY[i % 2].copy_(st_i.Y, non_blocking=True)
-            hdX[i % 2].copy_(st_i.dX, non_blocking=True)
-            hdW[i % 2].copy_(st_i.dW, non_blocking=True)
+            hY[i % NSETS].copy_(st_i.Y, non_blocking=True)
+            hdX[i % NSETS].copy_(st_i.dX, non_blocking=True)
+            hdW[i % NSETS].copy_(st_i.dW, non_blocking=True)
             ev_out[i].record(s_d2h)
 
-    # warm-up: both buffer sets and both copy directions once through the
-    # pipeline, untimed (the second set's first step also runs its amax pass)
+    # warm-up: every buffer set and both copy directions once through the
+    # pipeline, untimed (each set's first step also runs its amax pass)
     for i in range(e2e_warm):
         e2e_step(i)
     torch.cuda.synchronize()
@@ -605,7 +606,8 @@ def run_gpu(args, rank, world):
     return dict(ms=ms, ms_emulated=ms_emulated, ms_current=ms_current, refreshes=refreshes, ms_serial=ms_serial,
                 ms_serial_r=ms_serial_r, t_gr=t_gr, parts=parts, fallbacks=fallbacks, dual=dual,
                 native=native, fused=fused, block=block, t_scale=t_scale, t_q=(t_qx, t_qw, t_qd), t_g=t_g, launches=launches, rates=rates,
-                clocks=clk.summary(), status=status, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, link=link, affinity=affinity,
+                clocks=clk.summary(), status=status, e2e_ms=e2e_ms, e2e_steps=e2e_steps, e2e_sets=NSETS,
+                h2d=h2d, d2h=d2h, link=link, affinity=affinity,
                 elems=(X.numel(), W.numel(), dY.numel()))
 
 
@@ -742,6 +744,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-block", action="store_true",
                     help="skip the four-linear block measurement (profiling captures)")
+    ap.add_argument("--e2e-sets", type=int, default=2,
+                    help="device buffer sets the end-to-end pipeline rotates through")
     ap.add_argument("--tokens", type=int, default=8192,
                     help="rows of X and dY; smaller values only for profiling captures")
     args = ap.parse_args()
@@ -888,6 +892,7 @@ def main():
                          "wgrad_emulated": r["t_g"][2]},
         "e2e": {"value": job_tflops(world, STEP_FLOPS, r["e2e_ms"]), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e_ms"],
+                "steps": r["e2e_steps"], "device_buffer_sets": r["e2e_sets"],
                 "host_link_gbs": {k: round(v, 1) for k, v in r["link"].items()},
                 "cpu_affinity": r["affinity"]},
         "native_nvfp4": native_line(r["native"], world, bf16, src),
