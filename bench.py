@@ -534,6 +534,31 @@ def run_gpu(args, rank, world):
         "fused_ms": _timed(lambda: fp4q.fp4q_gemm_quantize(*g_args, TY, step.Y, pY, sY, aY)),
         "fused_without_bf16_ms": _timed(lambda: fp4q.fp4q_gemm_quantize(*g_args, TY, None, pY, sY, aY)),
     }
+    # the same on the step's fast path: rebias of X's and W's codes, the
+    # native GEMM (quantising in its epilogue) and the conditional fallback
+    a4, fa, b4, fb, flag = step_rb = rstep.rb[0]
+    nat = (step.Xr, a4, fa, T0, step.Wr, b4, fb, T1, M_TOK, FFN, HID, flag)
+
+    def fast(quantize, bf16=True):
+        flag.zero_()
+        fp4q.fp4q_rebias_scales(step.Xrs, M_TOK, HID // 16, True, a4, fa, flag)
+        fp4q.fp4q_rebias_scales(step.Wrs, FFN, HID // 16, False, b4, fb, flag)
+        if quantize:
+            aY.zero_()
+            fp4q.fp4q_gemm_nvfp4_rebiased_quantize(*nat, fp4q.UE5M3, TY, step.Y if bf16 else None, pY, sY, aY)
+            fp4q.fp4q_gemm_quantize_if(*g_args, flag, TY, step.Y if bf16 else None, pY, sY, aY)
+        else:
+            fp4q.fp4q_gemm_nvfp4_rebiased(*nat, step.Y)
+            fp4q.fp4q_gemm_if(*g_args, flag, step.Y)
+
+    fused.update({
+        "rebiased_gemm_ms": _timed(lambda: fast(False)),
+        "rebiased_gemm_then_quantize_ms": _timed(lambda: (fast(False), fp4q.fp4q_quantize(
+            step.Y, fp4q.AXIS_ROW, fp4q.UE5M3, TY, fp4q.RNE, 0, pY, sY, None, None))),
+        "rebiased_fused_ms": _timed(lambda: fast(True)),
+        "rebiased_fused_without_bf16_ms": _timed(lambda: fast(True, False)),
+    })
+    del step_rb
 
     # ---- the full 8B-class linear block: the four internal linears (QKV,
     # out, up, down) each through the same fwd+bwd step, one after another

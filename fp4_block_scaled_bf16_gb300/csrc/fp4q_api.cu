@@ -160,7 +160,8 @@ static fp4q_status gemm_common(const uint8_t* A, const uint8_t* A_scales, const 
                                const uint8_t* B, const uint8_t* B_scales, const float* B_tscale,
                                int64_t M, int64_t N, int64_t K, fp4q_scale_fmt fmt, void* out,
                                int out_is_f32, const float* c_tscale, uint8_t* qpay, uint8_t* qsc,
-                               float* qamax, void* stream, const int* run_if = nullptr) {
+                               float* qamax, void* stream, const int* run_if = nullptr,
+                               bool zero_qamax = true) {
   if (!valid_fmt(fmt)) return FP4Q_ERR_ARG;
   if (run_if && !aligned4(run_if)) return FP4Q_ERR_ALIGN;
   if (M < 0 || N < 0 || K < 0 || K % 64 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
@@ -170,7 +171,7 @@ static fp4q_status gemm_common(const uint8_t* A, const uint8_t* A_scales, const 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (qamax && !aligned4(qamax)) return FP4Q_ERR_ALIGN;
   if (M == 0 || N == 0) {
-    if (qamax) return from_cuda(cudaMemsetAsync(qamax, 0, sizeof(float), st));
+    if (qamax && zero_qamax) return from_cuda(cudaMemsetAsync(qamax, 0, sizeof(float), st));
     return FP4Q_OK;
   }
   if (!out && !qpay) return FP4Q_ERR_ARG;
@@ -184,7 +185,7 @@ static fp4q_status gemm_common(const uint8_t* A, const uint8_t* A_scales, const 
     if (out) e = cudaMemsetAsync(out, 0, (size_t)M * N * (out_is_f32 ? 4 : 2), st);
     if (e == cudaSuccess && qpay) e = cudaMemsetAsync(qpay, 0, (size_t)M * N / 2, st);
     if (e == cudaSuccess && qpay) e = cudaMemsetAsync(qsc, 0, (size_t)M * N / 16, st);
-    if (e == cudaSuccess && qamax) e = cudaMemsetAsync(qamax, 0, sizeof(float), st);
+    if (e == cudaSuccess && qamax && zero_qamax) e = cudaMemsetAsync(qamax, 0, sizeof(float), st);
     return from_cuda(e);
   }
   if (!A || !A_scales || !A_tscale || !B || !B_scales || !B_tscale) return FP4Q_ERR_ARG;
@@ -195,6 +196,7 @@ static fp4q_status gemm_common(const uint8_t* A, const uint8_t* A_scales, const 
   if (!status) return FP4Q_ERR_CUDA;
   fp4q::GemmArgs a;
   a.run_if = run_if;
+  a.zero_qamax = zero_qamax;
   a.TC = c_tscale;
   a.qpay = qpay;
   a.qsc = qsc;
@@ -253,6 +255,18 @@ fp4q_status fp4q_gemm_if(const uint8_t* A, const uint8_t* A_scales, const float*
                      nullptr, nullptr, nullptr, nullptr, stream, run_if_set);
 }
 
+fp4q_status fp4q_gemm_quantize_if(const uint8_t* A, const uint8_t* A_scales, const float* A_tscale,
+                                  const uint8_t* B, const uint8_t* B_scales, const float* B_tscale, int64_t M,
+                                  int64_t N, int64_t K, fp4q_scale_fmt fmt, const int* run_if_set,
+                                  const float* c_tscale, void* out_bf16, uint8_t* out_payload,
+                                  uint8_t* out_scales, float* out_amax, void* stream) {
+  FP4Q_RANGE("fp4q_gemm_quantize_if");
+  if (!run_if_set) return FP4Q_ERR_ARG;
+  if (M > 0 && N > 0 && !out_payload) return FP4Q_ERR_ARG;
+  return gemm_common(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K, fmt, out_bf16, 0, c_tscale,
+                     out_payload, out_scales, out_amax, stream, run_if_set, /*zero_qamax=*/false);
+}
+
 }  // extern "C"
 
 namespace {
@@ -260,15 +274,29 @@ namespace {
 fp4q_status gemm_native_common(const uint8_t* A, const uint8_t* A_scales, const float* A_factor,
                                const float* A_tscale, const uint8_t* B, const uint8_t* B_scales,
                                const float* B_factor, const float* B_tscale, int64_t M, int64_t N,
-                               int64_t K, const int* skip_if, void* out, int out_is_f32, void* stream) {
+                               int64_t K, const int* skip_if, void* out, int out_is_f32, void* stream,
+                               const float* c_tscale = nullptr, uint8_t* qpay = nullptr, uint8_t* qsc = nullptr,
+                               float* qamax = nullptr, int qfmt = 0) {
   if (M < 0 || N < 0 || K < 0 || K % 256 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
     return FP4Q_ERR_SHAPE;
   if ((M + 127) / 128 > 65535) return FP4Q_ERR_SHAPE;   // 128-row tiles on the grid's y dimension
+  if (qpay && N % 32) return FP4Q_ERR_SHAPE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (qamax && !aligned4(qamax)) return FP4Q_ERR_ALIGN;
   if (M == 0 || N == 0) return FP4Q_OK;
-  if (!out) return FP4Q_ERR_ARG;
-  if (!aligned16(out)) return FP4Q_ERR_ALIGN;
-  if (K == 0) return from_cuda(cudaMemsetAsync(out, 0, (size_t)M * N * (out_is_f32 ? 4 : 2), st));
+  if (!out && !qpay) return FP4Q_ERR_ARG;
+  if (out && !aligned16(out)) return FP4Q_ERR_ALIGN;
+  if (qpay) {
+    if (!qsc || !c_tscale) return FP4Q_ERR_ARG;
+    if (!aligned16(qpay) || !aligned16(qsc) || !aligned4(c_tscale)) return FP4Q_ERR_ALIGN;
+  }
+  if (K == 0) {   // C = 0: zero output, payload and scale codes; qamax (max-ed into) unchanged
+    cudaError_t e = cudaSuccess;
+    if (out) e = cudaMemsetAsync(out, 0, (size_t)M * N * (out_is_f32 ? 4 : 2), st);
+    if (e == cudaSuccess && qpay) e = cudaMemsetAsync(qpay, 0, (size_t)M * N / 2, st);
+    if (e == cudaSuccess && qpay) e = cudaMemsetAsync(qsc, 0, (size_t)M * N / 16, st);
+    return from_cuda(e);
+  }
   if (!A || !A_scales || !A_tscale || !B || !B_scales || !B_tscale) return FP4Q_ERR_ARG;
   if (!aligned16(A) || !aligned16(B) || !aligned16(A_scales) || !aligned16(B_scales) ||
       !aligned4(A_tscale) || !aligned4(B_tscale) || !aligned4(A_factor) || !aligned4(B_factor) ||
@@ -293,6 +321,11 @@ fp4q_status gemm_native_common(const uint8_t* A, const uint8_t* A_scales, const 
   a.out = out;
   a.out_f32 = out_is_f32 != 0;
   a.status = status;
+  a.TC = c_tscale;
+  a.qpay = qpay;
+  a.qsc = qsc;
+  a.qamax = qamax;
+  a.fmt_out = qfmt;
   a.wait_cycles = 4000000000LL;   // about 2 s per wait, as fp4q_gemm
   a.skip_loads = false;
   if (const char* e = getenv("FP4Q_TEST_GEMM_WAIT_CYCLES")) {
@@ -324,6 +357,21 @@ fp4q_status fp4q_gemm_nvfp4_rebiased(const uint8_t* A, const uint8_t* A_scales4,
   if (M > 0 && N > 0 && K > 0 && (!A_factor || !B_factor)) return FP4Q_ERR_ARG;
   return gemm_native_common(A, A_scales4, A_factor, A_tscale, B, B_scales4, B_factor, B_tscale, M, N, K,
                             skip_if_set, out, out_is_f32, stream);
+}
+
+fp4q_status fp4q_gemm_nvfp4_rebiased_quantize(const uint8_t* A, const uint8_t* A_scales4, const float* A_factor,
+                                              const float* A_tscale, const uint8_t* B, const uint8_t* B_scales4,
+                                              const float* B_factor, const float* B_tscale, int64_t M, int64_t N,
+                                              int64_t K, const int* skip_if_set, fp4q_scale_fmt fmt,
+                                              const float* c_tscale, void* out_bf16, uint8_t* out_payload,
+                                              uint8_t* out_scales, float* out_amax, void* stream) {
+  FP4Q_RANGE("fp4q_gemm_nvfp4_rebiased_quantize");
+  if (!valid_fmt(fmt)) return FP4Q_ERR_ARG;
+  if (M > 0 && N > 0 && !out_payload) return FP4Q_ERR_ARG;
+  if (M > 0 && N > 0 && K > 0 && (!A_factor || !B_factor)) return FP4Q_ERR_ARG;
+  return gemm_native_common(A, A_scales4, A_factor, A_tscale, B, B_scales4, B_factor, B_tscale, M, N, K,
+                            skip_if_set, out_bf16, 0, stream, c_tscale, out_payload, out_scales, out_amax,
+                            (int)fmt);
 }
 
 fp4q_status fp4q_rebias_scales(const uint8_t* scales, int64_t rows, int64_t nblocks, int per_row,

@@ -53,6 +53,11 @@ struct GemmArgs {
   const int* skip_if = nullptr;
   // emulated GEMM: a device flag without which the launch is a no-op (nullable)
   const int* run_if = nullptr;
+  // epilogue quantisation: the scale format of the quantised result (the
+  // emulated GEMM uses fmt), and whether the launch zeroes qamax first
+  // (false: qamax is max-ed into as the caller left it)
+  int fmt_out = 0;
+  bool zero_qamax = true;
 };
 
 // The driver's cuTensorMapEncodeTiled (looked up once through the runtime);

@@ -671,7 +671,7 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   const bool tma_store = !a.out_f32 && a.out != nullptr && make_out_map(&mapC, a.out, a.M, a.N);
   if (!tma_store) memset(&mapC, 0, sizeof(mapC));
   if (a.qpay) {   // epilogue quantisation (BF16 result)
-    if (a.qamax) {
+    if (a.qamax && a.zero_qamax) {
       cudaError_t e = cudaMemsetAsync(a.qamax, 0, sizeof(float), st);
       if (e != cudaSuccess) return e;
     }

@@ -46,7 +46,11 @@
 // as UE4M3 codes times a power of two, per A row (fa) and for all of B (fb);
 // the epilogue multiplies each row by T_A T_B fb fa[row], exact products of
 // powers of two.  A device flag (skip_if) read once per pair makes the whole
-// launch a no-op, so that the caller need not read it on the host.
+// launch a no-op, so that the caller need not read it on the host.  With
+// QOUT the epilogue also quantises the BF16 result row-wise for the next
+// layer (RNE, blocks of 16 along N, tensor scale TC, the quantisers' own
+// block-scale and conversion code): two blocks per 32-column chunk, payload
+// and codes stored from registers, and max |bf16(C)| into qamax.
 // Every wait is bounded; a wait that runs out latches FP4Q_ERR_TIMEOUT and
 // the CTA winds down once the loads and MMAs it issued have completed; both
 // CTAs meet at a cluster barrier before the pair's TMEM is freed.
@@ -88,7 +92,8 @@ constexpr int NBARS = 2 * S + SF + 3;   // full, empty per stage; sf (rank 0) pe
 constexpr int OFF_BAR = S * STAGE;
 constexpr int OFF_TMEM = OFF_BAR + 8 * NBARS;
 constexpr int OFF_ABORT = OFF_TMEM + 8;
-constexpr int SMEM_BYTES = OFF_ABORT + 8 + 1024;   // + 1 KB alignment slack
+constexpr int OFF_TAB = OFF_ABORT + 8;           // the epilogue quantisation's scale table
+constexpr int SMEM_BYTES = OFF_TAB + (int)sizeof(ScaleTab) + 1024;   // + 1 KB alignment slack
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 
 // Instruction descriptor of kind::mxf4nvf4: A and B E2M1 (format 1), both
@@ -166,16 +171,50 @@ __device__ __forceinline__ void store_f32x32(void* out, int row, int col0, int N
   }
 }
 
+// The epilogue quantisation of one 32-column chunk of a BF16 result row
+// (hh: 16 words, element 2j in the low half of word j): two blocks of 16,
+// each scaled and converted as the quantisers do (RNE), stored as 16 payload
+// bytes and two scale codes; qmax collects max |bf16| as a 16-bit pattern.
+// N % 32 == 0, so the chunk is wholly inside a row.
+__device__ __forceinline__ void quantize_chunk(const uint32_t (&hh)[16], const ScaleTab& tab, const ScaleRegs& kr,
+                                               int row, int col0, int N, uint8_t* qpay, uint8_t* qsc,
+                                               uint32_t& qmax) {
+  uint32_t pw[4], codes = 0, cl = 0, fl = 0;
+#pragma unroll
+  for (int b = 0; b < 2; ++b) {
+    const uint32_t a = max(absmax16(hh + 8 * b), absmax16(hh + 8 * b + 4));
+    qmax = max(qmax, a);
+    const BlockScale bs = block_scale<false>(a, tab, kr);
+    pw[2 * b] = quantize8<false, false>(hh + 8 * b, bs.r, nullptr, &cl, &fl);
+    pw[2 * b + 1] = quantize8<false, false>(hh + 8 * b + 4, bs.r, nullptr, &cl, &fl);
+    codes |= bs.code << (8 * b);
+  }
+  *reinterpret_cast<uint4*>(qpay + (int64_t)row * (N / 2) + col0 / 2) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+  *reinterpret_cast<uint16_t*>(qsc + (int64_t)row * (N / 16) + col0 / 16) = (uint16_t)codes;
+}
+
+// BF16 store (out nullable) and quantisation of one chunk, if it starts
+// inside the row.
+__device__ __forceinline__ void store_quantize_chunk(const uint32_t (&hh)[16], void* out, const ScaleTab& tab,
+                                                     const ScaleRegs& kr, int row, int col0, int N, uint8_t* qpay,
+                                                     uint8_t* qsc, uint32_t& qmax) {
+  if (col0 >= N) return;
+  if (out) store_bf16x32(out, row, col0, N, hh);
+  quantize_chunk(hh, tab, kr, row, col0, N, qpay, qsc, qmax);
+}
+
 // Persistent, launched in clusters of two along x: cluster c (= blockIdx.x / 2)
 // takes tiles c, c + clusters, ... of the tiles_m x tiles_n grid of 256 x 256
 // tiles (row-major: consecutive clusters share A rows).
-template <bool F32OUT>
+template <bool F32OUT, bool QOUT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                       const __grid_constant__ CUtensorMap mapSA, const __grid_constant__ CUtensorMap mapSB,
                       const float* __restrict__ TA, const float* __restrict__ TB, int M, int N, int K,
                       void* __restrict__ out, int* status, long long budget, int skip_loads,
-                      const float* __restrict__ fa, const float* __restrict__ fb, const int* skip_if) {
+                      const float* __restrict__ fa, const float* __restrict__ fb, const int* skip_if,
+                      const float* __restrict__ TC, uint8_t* __restrict__ qpay, uint8_t* __restrict__ qsc,
+                      float* qamax, int qfmt) {
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
@@ -187,6 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_acc_empty = bar_acc_full + 8;   // both CTAs' epilogues read TMEM (rank 0)
   const uint32_t bar_done = bar_acc_empty + 8;       // every MMA issued completed
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
+  ScaleTab* tab = reinterpret_cast<ScaleTab*>(smem + OFF_TAB);
+  if (QOUT) build_scale_tab(tab, __ldg(TC), qfmt);   // block-wide, before the roles split
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
@@ -351,6 +392,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3, h = (warp - kEpiWarp0) >> 2;
     float alpha0 = __fmul_rn(__ldg(TA), __ldg(TB));
     if (fb) alpha0 = __fmul_rn(alpha0, __ldg(fb));   // a power of two: exact
+    uint32_t qmax = 0;                                // max |bf16(C)| of this lane's chunks (a pattern)
+    ScaleRegs kr{};
+    if (QOUT) kr = scale_regs(*tab);
     int j = 0;
     for (int tile = cid; tile < ntiles; tile += ncl, ++j) {
       if (!mbar_wait(bar_acc_full, (uint32_t)(j & 1), abort_flag, budget)) {
@@ -383,8 +427,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (live) store_f32x32(out, row, cbase + 64 * half + 32, N, r, 32, alpha);
         }
       } else {
-        // 64 columns at a time: loaded, packed to BF16, stored; TMEM released
-        // once the second load is complete
+        // 64 columns at a time: loaded, packed to BF16, stored (and, with
+        // QOUT, quantised); TMEM released once the second load is complete.
+        // (With QOUT, holding all 128 packed columns until the release, so
+        // that the first 64's work follows it, needs more than the 128
+        // registers a thread has here.)
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t r[64];
@@ -396,12 +443,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive_rank0(bar_acc_empty);
           }
-          uint32_t hh[16];
-          pack_bf16x32(r, 0, alpha, hh);
-          if (live) store_bf16x32(out, row, cbase + 64 * half, N, hh);
-          pack_bf16x32(r, 32, alpha, hh);
-          if (live) store_bf16x32(out, row, cbase + 64 * half + 32, N, hh);
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t hh[16];
+            pack_bf16x32(r, 32 * c, alpha, hh);
+            if (QOUT) {
+              if (live) store_quantize_chunk(hh, out, *tab, kr, row, cbase + 64 * half + 32 * c, N, qpay, qsc, qmax);
+            } else if (live) {
+              store_bf16x32(out, row, cbase + 64 * half + 32 * c, N, hh);
+            }
+          }
         }
+      }
+    }
+    if (QOUT) {
+      // max |bf16(C)| (a 16-bit pattern; inf/NaN compare above every finite)
+      qmax = __reduce_max_sync(0xFFFFFFFFu, qmax);
+      if (lane == 0) {
+        if (qmax >= 0x7F80u) atomicOr(status, kStatusNonFinite);
+        if (qamax && qmax) atomicMax(reinterpret_cast<unsigned int*>(qamax), qmax << 16);
       }
     }
   }
@@ -449,10 +509,10 @@ static bool make_scale_map(CUtensorMap* map, const uint8_t* base, int64_t rows, 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool F32OUT>
+template <bool F32OUT, bool QOUT = false>
 static cudaError_t launch_native_t(const GemmArgs& a, const CUtensorMap& mA, const CUtensorMap& mB,
                                    const CUtensorMap& mSA, const CUtensorMap& mSB, cudaStream_t st) {
-  auto kern = native::gemm_nvfp4_kernel<F32OUT>;
+  auto kern = native::gemm_nvfp4_kernel<F32OUT, QOUT>;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -485,7 +545,8 @@ static cudaError_t launch_native_t(const GemmArgs& a, const CUtensorMap& mA, con
   const int ncl = (int)(ntiles < clusters[dev] ? ntiles : clusters[dev]);
   cfg.gridDim = dim3(2u * (unsigned)ncl);
   e = cudaLaunchKernelEx(&cfg, kern, mA, mB, mSA, mSB, a.TA, a.TB, (int)a.M, (int)a.N, (int)a.K, a.out, a.status,
-                         a.wait_cycles, a.skip_loads ? 1 : 0, a.fa, a.fb, a.skip_if);
+                         a.wait_cycles, a.skip_loads ? 1 : 0, a.fa, a.fb, a.skip_if, a.TC, a.qpay, a.qsc, a.qamax,
+                         a.fmt_out);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -497,6 +558,7 @@ cudaError_t launch_gemm_nvfp4(const GemmArgs& a, cudaStream_t st) {
       !make_swizzled_payload_map(&mB, a.B, a.N, a.K, native::BH) ||
       !make_scale_map(&mSA, a.As, a.M, a.K, native::BM) || !make_scale_map(&mSB, a.Bs, a.N, a.K, native::BH))
     return cudaErrorNotSupported;
+  if (a.qpay) return launch_native_t<false, true>(a, mA, mB, mSA, mSB, st);   // BF16 result (nullable) + its quantisation
   return a.out_f32 ? launch_native_t<true>(a, mA, mB, mSA, mSB, st) : launch_native_t<false>(a, mA, mB, mSA, mSB, st);
 }
 

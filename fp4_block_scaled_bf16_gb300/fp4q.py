@@ -27,7 +27,8 @@ UE5M3, UE4M3 = 0, 1
 # every symbol include/fp4q.h declares
 EXPORTS = ("fp4q_amax", "fp4q_tensor_scale", "fp4q_quantize", "fp4q_dequantize", "fp4q_gemm",
            "fp4q_gemm_quantize", "fp4q_gemm_nvfp4", "fp4q_rebias_scales", "fp4q_gemm_nvfp4_rebiased",
-           "fp4q_gemm_if", "fp4q_get_device_status", "fp4q_status_string")
+           "fp4q_gemm_if", "fp4q_gemm_nvfp4_rebiased_quantize", "fp4q_gemm_quantize_if",
+           "fp4q_get_device_status", "fp4q_status_string")
 
 
 class Fp4qError(RuntimeError):
@@ -54,6 +55,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fp4q_rebias_scales.argtypes = [P, i64, i64, i32, P, P, P, P]
     lib.fp4q_gemm_nvfp4_rebiased.argtypes = [P, P, P, P, P, P, P, P, i64, i64, i64, P, P, i32, P]
     lib.fp4q_gemm_if.argtypes = [P, P, P, P, P, P, i64, i64, i64, i32, P, P, i32, P]
+    lib.fp4q_gemm_nvfp4_rebiased_quantize.argtypes = [P, P, P, P, P, P, P, P, i64, i64, i64, P, i32, P, P, P, P,
+                                                      P, P]
+    lib.fp4q_gemm_quantize_if.argtypes = [P, P, P, P, P, P, i64, i64, i64, i32, P, P, P, P, P, P, P]
     lib.fp4q_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), P]
     lib.fp4q_status_string.argtypes = [i32]
     lib.fp4q_status_string.restype = ctypes.c_char_p
@@ -286,6 +290,52 @@ def fp4q_gemm_if(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K, fmt, run
         M, N, K, fmt, _ptr(run_if_set), _ptr(out), int(f32), _stream()))
 
 
+def _quantize_outputs(M, N, c_tscale, out_bf16, out_payload, out_scales, out_amax):
+    if N % 32:
+        raise ValueError(f"N must be a multiple of 32 for the epilogue quantisation, got {N}")
+    _mat(out_payload, "out_payload", (M, N // 2), torch.uint8)
+    _mat(out_scales, "out_scales", (M, N // 16), torch.uint8)
+    if out_bf16 is not None:
+        _mat(out_bf16, "out_bf16", (M, N), torch.bfloat16)
+    _scalar(c_tscale, "c_tscale")
+    if out_amax is not None:
+        _scalar(out_amax, "out_amax")
+    return [("c_tscale", c_tscale), ("out_bf16", out_bf16), ("out_payload", out_payload),
+            ("out_scales", out_scales), ("out_amax", out_amax)]
+
+
+def fp4q_gemm_nvfp4_rebiased_quantize(A, A_scales4, A_factor, A_tscale, B, B_scales4, B_factor, B_tscale,
+                                      M, N, K, skip_if_set, fmt, c_tscale, out_bf16, out_payload, out_scales,
+                                      out_amax=None) -> None:
+    """fp4q_gemm_nvfp4_rebiased with the BF16 result quantised row-wise in its
+    epilogue; out_amax is max-ed into (the caller zeroes it)."""
+    ops = _gemm_operands(A, A_scales4, A_tscale, B, B_scales4, B_tscale, M, N, K)
+    _scalar(A_factor, "A_factor", M)
+    _scalar(B_factor, "B_factor")
+    if skip_if_set is not None:
+        _scalar(skip_if_set, "skip_if_set", 1, torch.int32)
+    qo = _quantize_outputs(M, N, c_tscale, out_bf16, out_payload, out_scales, out_amax)
+    _on_device(*ops, ("A_factor", A_factor), ("B_factor", B_factor), ("skip_if_set", skip_if_set), *qo)
+    _check("fp4q_gemm_nvfp4_rebiased_quantize", _lib.fp4q_gemm_nvfp4_rebiased_quantize(
+        _ptr(A), _ptr(A_scales4), _ptr(A_factor), _ptr(A_tscale), _ptr(B), _ptr(B_scales4), _ptr(B_factor),
+        _ptr(B_tscale), M, N, K, _ptr(skip_if_set), fmt, _ptr(c_tscale), _ptr(out_bf16), _ptr(out_payload),
+        _ptr(out_scales), _ptr(out_amax), _stream()))
+
+
+def fp4q_gemm_quantize_if(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K, fmt, run_if_set, c_tscale,
+                          out_bf16, out_payload, out_scales, out_amax=None) -> None:
+    """fp4q_gemm_quantize run only when the device int run_if_set is
+    non-zero; out_amax max-ed into, not zeroed."""
+    ops = _gemm_operands(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K)
+    _scalar(run_if_set, "run_if_set", 1, torch.int32)
+    qo = _quantize_outputs(M, N, c_tscale, out_bf16, out_payload, out_scales, out_amax)
+    _on_device(*ops, ("run_if_set", run_if_set), *qo)
+    _check("fp4q_gemm_quantize_if", _lib.fp4q_gemm_quantize_if(
+        _ptr(A), _ptr(A_scales), _ptr(A_tscale), _ptr(B), _ptr(B_scales), _ptr(B_tscale), M, N, K, fmt,
+        _ptr(run_if_set), _ptr(c_tscale), _ptr(out_bf16), _ptr(out_payload), _ptr(out_scales),
+        _ptr(out_amax), _stream()))
+
+
 def fp4q_gemm_quantize(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K, fmt, c_tscale,
                        out_bf16, out_payload, out_scales, out_amax=None) -> None:
     ops = _gemm_operands(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K)
@@ -435,3 +485,31 @@ def gemm_ue5m3_rebiased(A, A_scales, A_tscale, B, B_scales, B_tscale, dtype=torc
     fp4q_gemm_nvfp4_rebiased(A, a4, fa, A_tscale, B, b4, fb, B_tscale, M, N, K, nofit, out)
     fp4q_gemm_if(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K, UE5M3, nofit, out)
     return out
+
+
+def gemm_quantize_ue5m3_rebiased(A, A_scales, A_tscale, B, B_scales, B_tscale, c_tscale,
+                                 want_bf16: bool = True, want_amax: bool = True,
+                                 nofit: torch.Tensor | None = None) -> Quantized:
+    """gemm_quantize's outputs (UE5M3 operands and result scales) from
+    gemm_ue5m3_rebiased's path: the native MMA through rebiased codes with
+    the quantisation in its epilogue, the emulated fused GEMM in its place
+    (decided on the device) when a group does not fit."""
+    fmt = UE5M3
+    M, K = A.shape[0], A.shape[1] * 2
+    N = B.shape[0]
+    dev = A.device
+    pr = torch.empty((M, N // 2), dtype=torch.uint8, device=dev)
+    sr = torch.empty((M, N // 16), dtype=torch.uint8, device=dev)
+    C = torch.empty((M, N), dtype=torch.bfloat16, device=dev) if want_bf16 else None
+    am = torch.zeros(1, dtype=torch.float32, device=dev) if want_amax else None
+    if nofit is None:
+        nofit = torch.empty(1, dtype=torch.int32, device=dev)
+    nofit.zero_()
+    a4, fa, _ = rebias_scales(A_scales, True, nofit)
+    b4, fb, _ = rebias_scales(B_scales, False, nofit)
+    fp4q_gemm_nvfp4_rebiased_quantize(A, a4, fa, A_tscale, B, b4, fb, B_tscale, M, N, K, nofit, fmt, c_tscale, C,
+                                      pr, sr, am)
+    fp4q_gemm_quantize_if(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K, UE5M3, nofit, c_tscale, C, pr,
+                          sr, am)
+    return Quantized(payload_row=pr, scales_row=sr, C=C, amax=am, T=c_tscale, fmt=fmt)
+

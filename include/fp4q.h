@@ -240,6 +240,37 @@ fp4q_status fp4q_gemm_if(const uint8_t* A, const uint8_t* A_scales, const float*
                          int64_t N, int64_t K, fp4q_scale_fmt fmt, const int* run_if_set, void* out,
                          int out_is_f32, void* stream);
 
+/* fp4q_gemm_nvfp4_rebiased whose epilogue also quantises the BF16 result for
+ * the next layer, as fp4q_gemm_quantize does for the emulated GEMM (the
+ * "format-aware fusion" direction the UE5M3 page lists among related work):
+ * bf16(C) row-wise, blocks of 16 along N, round to nearest even, scale
+ * format fmt, device tensor scale c_tscale:
+ *   out_payload [M, N/2], out_scales [M, N/16] = fp4q_quantize(bf16(C), ROW,
+ *   fmt, c_tscale, RNE) byte for byte; out_bf16 (nullable) = bf16(C);
+ *   out_amax (nullable): max-ed with max |bf16(C)| -- NOT zeroed first, so
+ *   that this call and fp4q_gemm_quantize_if (its fallback) can share it;
+ *   the caller zeroes it before the pair (a non-finite element latches
+ *   FP4Q_ERR_NONFINITE).
+ * skip_if_set as fp4q_gemm_nvfp4_rebiased (a skipped launch writes none of
+ * the outputs); N must be a multiple of 32; otherwise as that call. */
+fp4q_status fp4q_gemm_nvfp4_rebiased_quantize(const uint8_t* A, const uint8_t* A_scales4, const float* A_factor,
+                                              const float* A_tscale, const uint8_t* B, const uint8_t* B_scales4,
+                                              const float* B_factor, const float* B_tscale, int64_t M, int64_t N,
+                                              int64_t K, const int* skip_if_set, fp4q_scale_fmt fmt,
+                                              const float* c_tscale, void* out_bf16, uint8_t* out_payload,
+                                              uint8_t* out_scales, float* out_amax, void* stream);
+
+/* fp4q_gemm_quantize run only when the device int *run_if_set is non-zero
+ * (read once on the device), its out_amax max-ed into rather than zeroed
+ * first: the exact fallback of fp4q_gemm_nvfp4_rebiased_quantize into the
+ * same outputs.  K = 0 still writes zero outputs (out_amax unchanged).
+ * Arguments otherwise as fp4q_gemm_quantize; run_if_set 4-byte aligned. */
+fp4q_status fp4q_gemm_quantize_if(const uint8_t* A, const uint8_t* A_scales, const float* A_tscale,
+                                  const uint8_t* B, const uint8_t* B_scales, const float* B_tscale, int64_t M,
+                                  int64_t N, int64_t K, fp4q_scale_fmt fmt, const int* run_if_set,
+                                  const float* c_tscale, void* out_bf16, uint8_t* out_payload,
+                                  uint8_t* out_scales, float* out_amax, void* stream);
+
 /* Reads the device status word of the current device in the order of
  * `stream` (after every call already issued on it), waits for `stream` alone
  * (no other stream of the device is synchronised), returns the latched

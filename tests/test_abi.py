@@ -140,6 +140,21 @@ def test_host_validation_rejects_before_launch(lib):
     assert n(ok, ok, ok, ok, ok, ok, ok, ok, 128, 128, 256, P(18), ok, 0, None) == ERR_ALIGN
     assert n(ok, ok, ok, ok, ok, ok, ok, ok, 0, 128, 256, None, ok, 0, None) == 0   # empty: no-op
 
+    nq = lib.fp4q_gemm_nvfp4_rebiased_quantize
+    nq.argtypes = [P, P, P, P, P, P, P, P, i64, i64, i64, P, ctypes.c_int, P, P, P, P, P, P]
+    assert nq(ok, ok, ok, ok, ok, ok, ok, ok, 128, 48, 256, None, 0, ok, ok, ok, ok, None, None) == ERR_SHAPE  # N % 32
+    assert nq(ok, ok, ok, ok, ok, ok, ok, ok, 128, 64, 256, None, 0, ok, ok, None, ok, None, None) == ERR_ARG
+    assert nq(ok, ok, ok, ok, ok, ok, ok, ok, 128, 64, 256, None, 0, None, ok, ok, ok, None, None) == ERR_ARG
+    assert nq(ok, ok, ok, ok, ok, ok, ok, ok, 128, 64, 256, None, 3, ok, ok, ok, ok, None, None) == ERR_ARG
+    assert nq(ok, ok, ok, ok, ok, ok, ok, ok, 128, 64, 256, None, 0, ok, ok, ok, ok, P(18), None) == ERR_ALIGN
+    assert nq(ok, ok, ok, ok, ok, ok, ok, ok, 0, 64, 256, None, 0, ok, ok, ok, ok, None, None) == 0
+    qi = lib.fp4q_gemm_quantize_if
+    qi.argtypes = [P, P, P, P, P, P, i64, i64, i64, ctypes.c_int, P, P, P, P, P, P, P]
+    assert qi(ok, ok, ok, ok, ok, ok, 128, 64, 128, 0, None, ok, ok, ok, ok, None, None) == ERR_ARG   # flag
+    assert qi(ok, ok, ok, ok, ok, ok, 128, 64, 128, 0, ok, ok, ok, None, ok, None, None) == ERR_ARG   # payload
+    assert qi(ok, ok, ok, ok, ok, ok, 128, 48, 128, 0, ok, ok, ok, ok, ok, None, None) == ERR_SHAPE
+    assert qi(ok, ok, ok, ok, ok, ok, 0, 64, 128, 0, ok, ok, ok, ok, ok, None, None) == 0
+
     c = lib.fp4q_gemm_if
     c.argtypes = [P, P, P, P, P, P, i64, i64, i64, ctypes.c_int, P, P, ctypes.c_int, P]
     assert c(ok, ok, ok, ok, ok, ok, 128, 128, 128, 0, None, ok, 0, None) == ERR_ARG     # flag required

@@ -140,6 +140,29 @@ def test_rebiased_gemm_shapes(fp4q):
     raises(c, A, As, TA, B, Bs, TB, M, N, K, 0, flag, bf(M, N + 16), match="out")
 
 
+def test_rebiased_fused_gemm_shapes(fp4q):
+    M, N, K = 32, 64, 256
+    A, As, TA, B, Bs, TB = _gemm_ops(M, N, K)
+    flag = torch.zeros(1, dtype=torch.int32)
+    fa, fb = torch.ones(M), torch.ones(1)
+    g = fp4q.fp4q_gemm_nvfp4_rebiased_quantize
+    raises(g, A, As, fa, TA, B, Bs, fb, TB, M, N, K, flag, 0, T, bf(M, N), u8(M, N // 2), u8(M, N // 16), T,
+           match="CUDA")
+    raises(g, A, As, fa, TA, B, Bs, fb, TB, M, N, K, flag, 0, T, None, u8(M, N // 4), u8(M, N // 16), None,
+           match="out_payload")
+    raises(g, A, As, torch.ones(1), TA, B, Bs, fb, TB, M, N, K, flag, 0, T, None, u8(M, N // 2),
+           u8(M, N // 16), None, match="A_factor")
+    ops48 = _gemm_ops(M, 48, K)
+    raises(g, ops48[0], ops48[1], fa, TA, ops48[3], ops48[4], fb, TB, M, 48, K, flag, 0, T, None, u8(M, 24),
+           u8(M, 3), None, match="multiple of 32")
+    c = fp4q.fp4q_gemm_quantize_if
+    raises(c, A, As, TA, B, Bs, TB, M, N, K, 0, flag, T, None, u8(M, N // 2), u8(M, N // 16), None, match="CUDA")
+    raises(c, A, As, TA, B, Bs, TB, M, N, K, 0, None, T, None, u8(M, N // 2), u8(M, N // 16), None,
+           match="run_if_set")
+    raises(c, A, As, TA, B, Bs, TB, M, N, K, 0, flag, T, None, u8(M, N // 2), u8(M, N // 8), None,
+           match="out_scales")
+
+
 def test_scalar_entry_points(fp4q):
     raises(fp4q.fp4q_amax, bf(16), torch.ones(0), match="out_amax")
     raises(fp4q.fp4q_amax, torch.zeros(16), torch.ones(1), match="bfloat16")
