@@ -28,9 +28,11 @@ B's per tensor to UE4M3 codes times powers of two (fp4q_rebias_scales), the
 native kernel applies the factors (fp4q_gemm_nvfp4_rebiased), and the
 emulated kernel (fp4q_gemm_if) is launched after it and runs only if some
 group spanned more than the 14 binades UE4M3 holds -- decided on the device,
-no host read.  wgrad stays emulated: its A operand is dY column-wise, each row
-running over the batch's tokens, whose gradient magnitudes differ by many
-more binades than that.
+no host read.  wgrad stays emulated by default: its A operand is dY
+column-wise, each row running over the batch's tokens, whose gradient
+magnitudes can differ by many more binades than that (in the bench's inputs
+they span ten decades); `rebias_wgrad=True` sends it the same way, with the
+same exact fallback.
 
 Every launch goes through libfp4q.so; buffers are allocated once here with
 torch and reused by every step.
@@ -46,12 +48,14 @@ from .periodic import PeriodicScaler
 class LinearStep:
     def __init__(self, X: torch.Tensor, W: torch.Tensor, dY: torch.Tensor, seed: int = 7,
                  period: int = 16, fmt: int = _fp4q.UE5M3, native: bool = False, rebias: bool = False,
-                 lib=None):
+                 rebias_wgrad: bool = False, lib=None):
         q = self.q = lib if lib is not None else _fp4q
         if native and fmt != q.UE4M3:
             raise ValueError("the native block-scaled MMA takes UE4M3 scales (fmt=UE4M3)")
         if rebias and (native or fmt != q.UE5M3):
             raise ValueError("rebias re-expresses UE5M3 scales (fmt=UE5M3, native=False)")
+        if rebias_wgrad and not rebias:
+            raise ValueError("rebias_wgrad needs rebias=True")
         self.native = native
         tokens, hid = X.shape
         out = W.shape[0]
@@ -76,13 +80,16 @@ class LinearStep:
         self.Y = torch.empty((tokens, out), **bf)
         self.dX = torch.empty((tokens, hid), **bf)
         self.dW = torch.empty((out, hid), **bf)
-        # fprop (A = X rows, B = W rows) and dgrad (A = dY rows, B = W columns)
-        # on the native MMA: rebiased codes, factors and a fallback flag each;
-        # a GEMM whose K is not a multiple of 256 stays emulated
-        self.rb = [None, None]
-        self.nofit = torch.zeros(2, dtype=torch.int32, device=dev)
+        # fprop (A = X rows, B = W rows), dgrad (A = dY rows, B = W columns)
+        # and, optionally, wgrad (A = dY columns, B = X columns) on the
+        # native MMA: rebiased codes, factors and a fallback flag each; a GEMM
+        # whose K is not a multiple of 256 stays emulated
+        ngemms = 3 if rebias_wgrad else 2
+        self.rb = [None] * 3
+        self.nofit = torch.zeros(ngemms, dtype=torch.int32, device=dev)
         if rebias:
-            for g, (m, n, k) in enumerate(((tokens, out, hid), (tokens, hid, out))):
+            shapes = ((tokens, out, hid), (tokens, hid, out), (out, hid, tokens))[:ngemms]
+            for g, (m, n, k) in enumerate(shapes):
                 if k % 256 == 0:
                     self.rb[g] = (torch.empty((m, k // 16), **u8), torch.empty(m, **f32),
                                   torch.empty((n, k // 16), **u8), torch.empty(1, **f32), self.nofit[g:g + 1])
@@ -159,8 +166,9 @@ class LinearStep:
         self.launches += 1
 
     def fallbacks(self):
-        """Whether fprop and dgrad each fell back to the emulated GEMM on the
-        last step (reads the device flags; synchronises)."""
+        """Whether fprop, dgrad (and wgrad, with rebias_wgrad) each fell back
+        to the emulated GEMM on the last step (reads the device flags;
+        synchronises)."""
         return [bool(v) for v in self.nofit.tolist()]
 
     def tensor_scales(self, periodic: bool):
@@ -191,7 +199,7 @@ class LinearStep:
         rec(5)
         self._gemm((self.Dr, self.Drs, TD), (self.Wc, self.Wcs, TW), tokens, hid, out, self.dX, self.rb[1])
         rec(6)
-        self._gemm((self.Dc, self.Dcs, TD), (self.Xc, self.Xcs, TX), out, hid, tokens, self.dW)
+        self._gemm((self.Dc, self.Dcs, TD), (self.Xc, self.Xcs, TX), out, hid, tokens, self.dW, self.rb[2])
         rec(7)
         return self
 
@@ -229,7 +237,7 @@ class LinearStep:
         with torch_.cuda.stream(self.side2):
             self.side2.wait_event(self.ev_dq)
             self.side2.wait_event(self.ev_xw)
-            self._gemm((self.Dc, self.Dcs, TD), (self.Xc, self.Xcs, TX), out, hid, tokens, self.dW)
+            self._gemm((self.Dc, self.Dcs, TD), (self.Xc, self.Xcs, TX), out, hid, tokens, self.dW, self.rb[2])
             self.ev_side2.record(self.side2)
         with torch_.cuda.stream(main):
             self._gemm((self.Xr, self.Xrs, TX), (self.Wr, self.Wrs, TW), tokens, out, hid, self.Y, self.rb[0], 0)

@@ -155,7 +155,7 @@ def test_rebiased_step_matches_oracle():
     W = torch.empty((OUT, HID), dtype=torch.bfloat16, device=dev)
     dY = torch.empty((TOK, OUT), dtype=torch.bfloat16, device=dev)
     step = LinearStep(X, W, dY, seed=7, period=period, rebias=True)
-    assert all(rb is not None for rb in step.rb)
+    assert step.rb[0] is not None and step.rb[1] is not None and step.rb[2] is None   # wgrad emulated
     for t in range(steps):
         xb, wb, db = _inputs(t, amaxes)
         X.copy_(workloads.to_torch_bf16(xb))
@@ -280,5 +280,44 @@ def test_two_steps_on_two_caller_streams():
     for st, ref in zip(steps, alone):
         for a, b in zip((st.Y, st.dX, st.dW), ref):
             assert torch.equal(a, b)
+    assert fp4q.fp4q_get_device_status() == fp4q.OK
+
+
+def test_wgrad_through_the_native_path_when_it_fits():
+    """rebias_wgrad: with gradients whose per-token magnitudes stay within a
+    decade, dY's column-wise codes fit their rows' windows and wgrad runs on
+    the native MMA (flag clear, dW within the BF16 bound of the oracle's
+    UE5M3 contraction); with one block of 16 tokens 2^-30 smaller, every row
+    of wgrad's A operand spans more than 14 binades, wgrad falls back and dW
+    equals the all-emulated step's bit for bit (the bench's ten-decade
+    gradients do the same at 8192 tokens: spans up to 20 binades)."""
+    from fp4_block_scaled_bf16_gb300 import build
+    build.build()
+    from fp4_block_scaled_bf16_gb300 import fp4q
+    from fp4_block_scaled_bf16_gb300.linear_step import LinearStep
+
+    dev = torch.device("cuda")
+    X = workloads.to_torch_bf16(workloads.activations(TOK, HID, 81)).to(dev)
+    W = workloads.to_torch_bf16(workloads.weights(OUT, HID, 82)).to(dev)
+    for tiny, want in ((False, False), (True, True)):
+        g = workloads.bf16_bits_to_f32(workloads.gradients(TOK, OUT, 83, -1.0, 0.0))
+        if tiny:
+            g[32:48] *= np.float32(2.0 ** -30)
+        dY = workloads.to_torch_bf16(workloads.f32_to_bf16_bits(g)).to(dev)
+        fast = LinearStep(X, W, dY, seed=7, rebias=True, rebias_wgrad=True)
+        ref = LinearStep(X, W, dY, seed=7)
+        fast.run_overlapped()
+        ref.run_overlapped()
+        torch.cuda.synchronize()
+        fell = fast.fallbacks()
+        fits = (oracle.rebias_scales(_u8(fast.Dcs), True)[2] and oracle.rebias_scales(_u8(fast.Xcs), False)[2])
+        assert fell[2] == (not fits) == want, (tiny, fell)
+        assert fell[:2] == [False, False]
+        if want:
+            assert torch.equal(fast.dW, ref.dW)
+        else:
+            TD, TX = float(fast.T[2].item()), float(fast.T[0].item())
+            R = oracle.gemm(_u8(fast.Dc), _u8(fast.Dcs), TD, _u8(fast.Xc), _u8(fast.Xcs), TX)
+            check_gemm_bf16(fast.dW.float().cpu().numpy().astype(np.float64), R)
     assert fp4q.fp4q_get_device_status() == fp4q.OK
 
