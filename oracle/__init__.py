@@ -89,6 +89,7 @@ def _load():
             "orc_scale_encode_array": (None, [P, i64, i32, P, P]),
             "orc_sr_uniform_array": (None, [u64, P, i64, u32, P]),
             "orc_rebias_scales": (None, [P, i64, i64, i32, P, P, P]),
+            "orc_rebias_scales2": (None, [P, i64, i64, P, P, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -272,6 +273,21 @@ def rebias_scales(scales, per_row: bool = True):
     nofit = np.zeros(1, np.int32)
     _load().orc_rebias_scales(_ptr(scales), rows, nb, int(bool(per_row)), _ptr(out), _ptr(f), _ptr(nofit))
     return out, f, not bool(nofit[0])
+
+
+def rebias_scales2(scales):
+    """UE5M3 scale codes [rows, nb] -> (hi codes, lo codes, hi factors, lo
+    factors, fits): each row's top 14 binades as UE4M3 codes times
+    2^(e_top - 7), the 14 below them times 2^(e_top - 21); every value is
+    hi * f_hi + lo * f_lo with one of the two codes zero; fits unless a
+    value lies below both windows."""
+    scales = _c(scales, np.uint8)
+    rows, nb = scales.shape
+    hi, lo = np.empty_like(scales), np.empty_like(scales)
+    fh, fl = np.empty(rows, np.float32), np.empty(rows, np.float32)
+    nofit = np.zeros(1, np.int32)
+    _load().orc_rebias_scales2(_ptr(scales), rows, nb, _ptr(hi), _ptr(lo), _ptr(fh), _ptr(fl), _ptr(nofit))
+    return hi, lo, fh, fl, not bool(nofit[0])
 
 
 def gemm(A, As, TA, B, Bs, TB, fmt: int = UE5M3, ms=None, ns=None) -> np.ndarray:

@@ -510,6 +510,52 @@ void orc_rebias_scales(const uint8_t *codes, int64_t rows, int64_t nb, int per_r
     }
 }
 
+/* Two windows per row: the row's top 14 binades [e_top - 13, e_top] as in
+ * orc_rebias_scales (factor 2^(e_top - 7)), and the 14 below them
+ * [e_top - 27, e_top - 14] (factor 2^(e_top - 21), its top binade again in
+ * UE4M3's exponent field 14).  Every non-zero UE5M3 value equals
+ * hi[i] * f_hi + lo[i] * f_lo with exactly one of the two UE4M3 codes
+ * non-zero, so a GEMM on the row splits into two block-scaled contractions
+ * of the same payload, one with the hi codes and one with the lo codes,
+ * scaled by their factors.  A value below both windows sets *nofit (its
+ * codes are then unspecified); a zero row gets factors 1 and 2^-14 and zero
+ * codes. */
+void orc_rebias_scales2(const uint8_t *codes, int64_t rows, int64_t nb, uint8_t *out_hi, uint8_t *out_lo,
+                        float *f_hi, float *f_lo, int *nofit) {
+    for (int64_t r = 0; r < rows; ++r) {
+        const uint8_t *c = codes + r * nb;
+        uint8_t *h = out_hi + r * nb, *l = out_lo + r * nb;
+        int emax = -1000;
+        for (int64_t i = 0; i < nb; ++i) {
+            const double v = orc_scale_decode(c[i], ORC_UE5M3);
+            if (v != 0.0 && ilogb(v) > emax) emax = ilogb(v);
+        }
+        if (emax == -1000) {
+            f_hi[r] = 1.0f;
+            f_lo[r] = (float)ldexp(1.0, -14);
+            for (int64_t i = 0; i < nb; ++i) h[i] = l[i] = 0;
+            continue;
+        }
+        const double fh = ldexp(1.0, emax - 7), fl = ldexp(1.0, emax - 21);
+        f_hi[r] = (float)fh;
+        f_lo[r] = (float)fl;
+        for (int64_t i = 0; i < nb; ++i) {
+            const double v = orc_scale_decode(c[i], ORC_UE5M3);
+            int sat = 0;
+            h[i] = l[i] = 0;
+            if (v == 0.0) continue;
+            const int e = ilogb(v);
+            if (e >= emax - 13) {
+                h[i] = orc_scale_encode((float)(v / fh), ORC_UE4M3, &sat);
+            } else if (e >= emax - 27) {
+                l[i] = orc_scale_encode((float)(v / fl), ORC_UE4M3, &sat);
+            } else {
+                *nofit = 1;
+            }
+        }
+    }
+}
+
 /* ------------------------------------------------------------------------ */
 /* Array forms of the scalar steps, so that the tests can sweep many values  */
 /* through exactly the functions above.                                      */

@@ -130,3 +130,74 @@ def test_quantised_operand_and_gemm_are_unchanged():
     R4 = oracle.gemm(pa, sa4, ta, pb, sb4, tb, oracle.UE4M3) * fa.astype(np.float64)[:, None] * float(fb[0])
     assert np.array_equal(R4, R5)
     del rng
+
+
+@pytest.mark.parametrize("span", [0, 9, 13, 14, 20, 27, 28, 31])
+def test_two_windows_are_exact(span):
+    """Two windows per row: every value is hi * f_hi + lo * f_lo exactly,
+    with one of the two codes zero; a value sits in the hi window iff its
+    binade is within 13 of the row's top (else the lo one, down to 27);
+    the fit flag is "span <= 27"; factors 2^(e_top - 7) and 2^(e_top - 21)."""
+    rng = np.random.default_rng(100 + span)
+    codes = _codes_with_span(rng, 24, 64, span)
+    hi, lo, fh, fl, fits = oracle.rebias_scales2(codes)
+    spans = []
+    for r in range(codes.shape[0]):
+        vals = [V5[c] for c in codes[r] if c != 0]
+        b = [_binade(v) for v in vals]
+        spans.append(max(b) - min(b))
+        top = max(b)
+        assert Fraction(float(fh[r])) == Fraction(2) ** (top - 7)
+        assert Fraction(float(fl[r])) == Fraction(2) ** (top - 21)
+        for i, c in enumerate(codes[r]):
+            if c == 0:
+                assert hi[r, i] == 0 and lo[r, i] == 0
+                continue
+            e = _binade(V5[c])
+            if e < top - 27:
+                continue   # outside both windows: codes unspecified
+            assert (hi[r, i] != 0) == (e >= top - 13) and (lo[r, i] != 0) == (e < top - 13)
+            assert V4[hi[r, i]] * Fraction(float(fh[r])) + V4[lo[r, i]] * Fraction(float(fl[r])) == V5[c]
+            for x in (hi[r, i], lo[r, i]):
+                assert x == 0 or 1 <= (x >> 3) <= 14
+    assert fits == (max(spans) <= 27)
+
+
+def test_two_windows_reduce_to_one_within_fourteen_binades():
+    """Rows spanning at most 13 binades: the hi codes and factor are the
+    one-window rebias's, the lo codes all zero."""
+    rng = np.random.default_rng(5)
+    codes = _codes_with_span(rng, 40, 48, 11)
+    codes[3] = 0
+    hi, lo, fh, fl, fits = oracle.rebias_scales2(codes)
+    c4, f, fits1 = oracle.rebias_scales(codes, per_row=True)
+    assert fits and fits1
+    assert np.array_equal(hi, c4) and np.array_equal(fh, f) and not lo.any()
+    assert float(fh[3]) == 1.0 and float(fl[3]) == 2.0 ** -14
+
+
+def test_two_window_gemm_is_the_ue5m3_gemm():
+    """The UE5M3 GEMM of a wide-span operand equals f_hi * GEMM(hi codes) +
+    f_lo * GEMM(lo codes) of the same payload (binary64; the two sides sum
+    the same exact products in different orders)."""
+    rng = np.random.default_rng(21)
+    g = workloads.bf16_bits_to_f32(workloads.gradients(4096, 64, 9))   # per-token magnitudes over ten decades
+    gt = workloads.f32_to_bf16_bits(np.ascontiguousarray(g.T))          # rows: features, K: tokens
+    x = workloads.activations(96, 4096, 10)
+    ta, tb = oracle.tensor_scale(oracle.amax(gt)[0]), oracle.tensor_scale(oracle.amax(x)[0])
+    pa, sa, _ = oracle.quantize(gt, oracle.ROW, ta)
+    pb, sb, _ = oracle.quantize(x, oracle.ROW, tb)
+    hi, lo, fh, fl, fits = oracle.rebias_scales2(sa)
+    assert fits and lo.any()                       # the span needs the second window
+    R5 = oracle.gemm(pa, sa, ta, pb, sb, tb, oracle.UE5M3)
+    del rng
+    # B keeps its UE5M3 codes; A's dequantised values split exactly by window
+    ea5 = oracle.deq_es(pa, sa, oracle.UE5M3)
+    ea2 = (oracle.deq_es(pa, hi, oracle.UE4M3) * fh.astype(np.float64)[:, None]
+           + oracle.deq_es(pa, lo, oracle.UE4M3) * fl.astype(np.float64)[:, None])
+    assert np.array_equal(ea2, ea5)
+    eb = oracle.deq_es(pb, sb, oracle.UE5M3)
+    R2 = ta * tb * (fh.astype(np.float64)[:, None] * (oracle.deq_es(pa, hi, oracle.UE4M3) @ eb.T)
+                    + fl.astype(np.float64)[:, None] * (oracle.deq_es(pa, lo, oracle.UE4M3) @ eb.T))
+    assert np.abs(R2 - R5).max() <= 1e-12 * np.abs(R5).max()
+
