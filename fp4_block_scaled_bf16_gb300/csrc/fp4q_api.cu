@@ -276,7 +276,7 @@ fp4q_status gemm_native_common(const uint8_t* A, const uint8_t* A_scales, const 
                                const float* B_factor, const float* B_tscale, int64_t M, int64_t N,
                                int64_t K, const int* skip_if, void* out, int out_is_f32, void* stream,
                                const float* c_tscale = nullptr, uint8_t* qpay = nullptr, uint8_t* qsc = nullptr,
-                               float* qamax = nullptr, int qfmt = 0) {
+                               float* qamax = nullptr, int qfmt = 0, const uint8_t* A_scales_lo = nullptr) {
   if (M < 0 || N < 0 || K < 0 || K % 256 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
     return FP4Q_ERR_SHAPE;
   if ((M + 127) / 128 > 65535) return FP4Q_ERR_SHAPE;   // 128-row tiles on the grid's y dimension
@@ -299,8 +299,8 @@ fp4q_status gemm_native_common(const uint8_t* A, const uint8_t* A_scales, const 
   }
   if (!A || !A_scales || !A_tscale || !B || !B_scales || !B_tscale) return FP4Q_ERR_ARG;
   if (!aligned16(A) || !aligned16(B) || !aligned16(A_scales) || !aligned16(B_scales) ||
-      !aligned4(A_tscale) || !aligned4(B_tscale) || !aligned4(A_factor) || !aligned4(B_factor) ||
-      !aligned4(skip_if))
+      !aligned16(A_scales_lo) || !aligned4(A_tscale) || !aligned4(B_tscale) || !aligned4(A_factor) ||
+      !aligned4(B_factor) || !aligned4(skip_if))
     return FP4Q_ERR_ALIGN;
   int* status = status_ptr();
   if (!status) return FP4Q_ERR_CUDA;
@@ -326,6 +326,7 @@ fp4q_status gemm_native_common(const uint8_t* A, const uint8_t* A_scales, const 
   a.qsc = qsc;
   a.qamax = qamax;
   a.fmt_out = qfmt;
+  a.As_lo = A_scales_lo;
   a.wait_cycles = 4000000000LL;   // about 2 s per wait, as fp4q_gemm
   a.skip_loads = false;
   if (const char* e = getenv("FP4Q_TEST_GEMM_WAIT_CYCLES")) {
@@ -372,6 +373,41 @@ fp4q_status fp4q_gemm_nvfp4_rebiased_quantize(const uint8_t* A, const uint8_t* A
   return gemm_native_common(A, A_scales4, A_factor, A_tscale, B, B_scales4, B_factor, B_tscale, M, N, K,
                             skip_if_set, out_bf16, 0, stream, c_tscale, out_payload, out_scales, out_amax,
                             (int)fmt);
+}
+
+fp4q_status fp4q_gemm_nvfp4_two_windows(const uint8_t* A, const uint8_t* A_scales_hi, const uint8_t* A_scales_lo,
+                                        const float* A_factor_hi, const float* A_tscale, const uint8_t* B,
+                                        const uint8_t* B_scales4, const float* B_factor, const float* B_tscale,
+                                        int64_t M, int64_t N, int64_t K, const int* skip_if_set, void* out,
+                                        int out_is_f32, void* stream) {
+  FP4Q_RANGE("fp4q_gemm_nvfp4_two_windows");
+  if (M > 0 && N > 0 && K > 0 && (!A_factor_hi || !B_factor || !A_scales_lo)) return FP4Q_ERR_ARG;
+  return gemm_native_common(A, A_scales_hi, A_factor_hi, A_tscale, B, B_scales4, B_factor, B_tscale, M, N, K,
+                            skip_if_set, out, out_is_f32, stream, nullptr, nullptr, nullptr, nullptr, 0,
+                            A_scales_lo);
+}
+
+fp4q_status fp4q_rebias_scales_two_windows(const uint8_t* scales, int64_t rows, int64_t nblocks, uint8_t* out_hi,
+                                           uint8_t* out_lo, float* out_factor_hi, float* out_factor_lo,
+                                           int* inout_nofit, void* stream) {
+  FP4Q_RANGE("fp4q_rebias_scales_two_windows");
+  if (rows < 0 || nblocks < 0 || nblocks % 16 || nblocks > INT32_MAX) return FP4Q_ERR_SHAPE;
+  if (!inout_nofit || (rows > 0 && (!out_factor_hi || !out_factor_lo))) return FP4Q_ERR_ARG;
+  if (rows > 0 && nblocks > 0 && (!scales || !out_hi || !out_lo)) return FP4Q_ERR_ARG;
+  if (!aligned16(scales) || !aligned16(out_hi) || !aligned16(out_lo) || !aligned4(out_factor_hi) ||
+      !aligned4(out_factor_lo) || !aligned4(inout_nofit))
+    return FP4Q_ERR_ALIGN;
+  if (rows > 0 && nblocks > 0) {
+    const int64_t n = rows * nblocks;
+    auto overlap = [n](const void* x, const void* y) {
+      const uint8_t *a = static_cast<const uint8_t*>(x), *b = static_cast<const uint8_t*>(y);
+      return a < b + n && b < a + n;
+    };
+    // the input is read after outputs are written; the two outputs are written together
+    if (overlap(scales, out_hi) || overlap(scales, out_lo) || overlap(out_hi, out_lo)) return FP4Q_ERR_ARG;
+  }
+  return from_cuda(fp4q::launch_rebias2(scales, rows, nblocks, out_hi, out_lo, out_factor_hi, out_factor_lo,
+                                        inout_nofit, static_cast<cudaStream_t>(stream)));
 }
 
 fp4q_status fp4q_rebias_scales(const uint8_t* scales, int64_t rows, int64_t nblocks, int per_row,

@@ -58,6 +58,10 @@ struct GemmArgs {
   // (false: qamax is max-ed into as the caller left it)
   int fmt_out = 0;
   bool zero_qamax = true;
+  // native GEMM, two-window rebiased A (nullable): A's low-window codes, the
+  // high-window codes in As and their per-row factor in fa, the low window's
+  // factor fa * 2^-14
+  const uint8_t* As_lo = nullptr;
 };
 
 // The driver's cuTensorMapEncodeTiled (looked up once through the runtime);
@@ -69,8 +73,7 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn();
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st);
 
 // The native NVFP4 GEMM (gemm_native.cu): UE4M3-scaled E2M1 operands on the
-// tensor cores' block-scaled MMA.  K % 256 == 0; the epilogue-quantisation
-// fields are unused.
+// tensor cores' block-scaled MMA.  K % 256 == 0.
 cudaError_t launch_gemm_nvfp4(const GemmArgs& a, cudaStream_t st);
 
 // UE5M3 scale codes [rows, nb] -> UE4M3 codes and power-of-two factors
@@ -78,5 +81,10 @@ cudaError_t launch_gemm_nvfp4(const GemmArgs& a, cudaStream_t st);
 // ORs 1 into *nofit when a group does not fit.  nb % 16 == 0.
 cudaError_t launch_rebias(const uint8_t* scales, int64_t rows, int64_t nb, bool per_row, uint8_t* out,
                           float* factor, int* nofit, cudaStream_t st);
+
+// The same per row with two windows (rebias.cu): high-window codes and
+// factor (out_hi, f_hi), low-window codes and factor (out_lo, f_lo).
+cudaError_t launch_rebias2(const uint8_t* scales, int64_t rows, int64_t nb, uint8_t* out_hi, uint8_t* out_lo,
+                           float* f_hi, float* f_lo, int* nofit, cudaStream_t st);
 
 }  // namespace fp4q

@@ -66,48 +66,82 @@
 namespace fp4q {
 namespace native {
 
-constexpr int PM = 256, PN = 256;                // output tile of a CTA pair
-constexpr int BM = 128, BH = 128, BN = 256;      // A rows and B rows per CTA; N of the MMA
+constexpr int PM = 256;                          // output rows of a pair's tile
+constexpr int BM = 128;                          // A rows per CTA
 constexpr int BK = 256;                          // K elements per stage
 constexpr int ROWB = BK / 2;                     // payload bytes per row per stage (128)
-constexpr int S = 5;                             // shared-memory ring stages
-constexpr int SF = 4;                            // TMEM scale slots (64 columns each)
 constexpr int A_BYTES = BM * ROWB;               // 16384
-constexpr int B_BYTES = BH * ROWB;               // 16384: this CTA's half of B
 constexpr int SA_BYTES = BM * (BK / 16);         // 2048: 16 scale codes per row
-constexpr int SB_BYTES = BN * (BK / 16);         // 4096: every B row of the tile
-constexpr int OFF_A = 0, OFF_B = A_BYTES, OFF_SA = OFF_B + B_BYTES, OFF_SB = OFF_SA + SA_BYTES;
-constexpr int STAGE = OFF_SB + SB_BYTES;         // 38912 = 38 KB
-static_assert(STAGE % 1024 == 0 && OFF_B % 1024 == 0 && OFF_SA % 128 == 0 && OFF_SB % 128 == 0, "alignment");
 constexpr int MMAS = BK / 64;                    // four K64 MMAs per stage
 constexpr int kSfWarps = 4, kEpiWarp0 = 4, kEpiWarps = 8;
 constexpr int kProducerWarp = 12, kMmaWarp = 13;
 constexpr int kThreads = 32 * 14;
 static_assert(kEpiWarp0 % 4 == 0, "epilogue warp w drains TMEM lane quadrant w % 4");
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSfCol0 = 256;                // scale ring: stage s at 256 + 64 s
-constexpr uint32_t kSfStageCols = 64;            // per MMA 16 columns: B (8) then A (4)
-static_assert(kSfCol0 + SF * kSfStageCols <= kTmemCols && BN <= (int)kSfCol0 && SF < S, "TMEM map");
-constexpr int NBARS = 2 * S + SF + 3;   // full, empty per stage; sf (rank 0) per slot; acc full / empty, done
-constexpr int OFF_BAR = S * STAGE;
-constexpr int OFF_TMEM = OFF_BAR + 8 * NBARS;
-constexpr int OFF_ABORT = OFF_TMEM + 8;
-constexpr int OFF_TAB = OFF_ABORT + 8;           // the epilogue quantisation's scale table
-constexpr int SMEM_BYTES = OFF_TAB + (int)sizeof(ScaleTab) + 1024;   // + 1 KB alignment slack
-static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+constexpr uint32_t kSfCol0 = 256;                // scale ring from column 256; accumulators below
 
-// Instruction descriptor of kind::mxf4nvf4: A and B E2M1 (format 1), both
-// K-major, UE4M3 scales (bit 23 clear), scale-factor data IDs 0,
-// N = 256 (bits 17..22: N / 8), M = 256 for the pair (bits 24..28: M / 16); dense.
-constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(PM >> 4) << 24);
+// The two shapes of the kernel.  One window (TWO = false): 256 x 256 tiles,
+// one 256-column accumulator, five 38 KB stages; the scale ring holds four
+// entries of one stage each (per K64 step a group of 16 columns: B's words in
+// 8, A's in 4 from column 8).  Two windows (TWO = true, A's codes split in a
+// high and a low window): 256 x 128 tiles, two 128-column accumulators (high
+// in columns 0..127, low in 128..255), both fed by each K64 step from the same
+// operand tiles, seven 30 KB stages (the low-window A codes added); a K64 step
+// takes 32 scale columns (the high MMA's group -- B's words in 4, A's
+// high-window words from column 8 -- and the low MMA's the same way), so the
+// ring holds two entries of one stage each.  (Entries of half a stage, each
+// released as soon as its own MMAs completed, so that three entries' MMAs
+// rather than one stage's cover the next copy into TMEM, ran 23 % slower:
+// the extra barrier wait and commits sit on the one thread that issues the
+// MMAs.)
+template <bool TWO>
+struct Geo {
+  static constexpr int PN = TWO ? 128 : 256;     // output columns of a pair's tile = N of the MMA
+  static constexpr int BH = PN / 2;              // B rows per CTA
+  static constexpr int S = TWO ? 7 : 5;          // shared-memory ring stages
+  static constexpr int ESTEPS = 4;               // K64 steps per scale-ring entry (a stage)
+  static constexpr int EPS = MMAS / ESTEPS;      // entries per stage
+  static constexpr uint32_t kStepCols = TWO ? 32 : 16;            // scale columns per K64 step
+  static constexpr uint32_t kEntryCols = ESTEPS * kStepCols;      // 64
+  static constexpr int NENT = (int)((kTmemCols - kSfCol0) / kEntryCols);   // ring entries (4, TWO: 2)
+  static constexpr bool kEntryIsStage = EPS == 1;  // released with the stage (bar_empty)
+  static constexpr int B_BYTES = BH * ROWB;      // this CTA's half of B
+  static constexpr int SB_BYTES = PN * (BK / 16);   // every B row of the tile
+  static constexpr int OFF_A = 0, OFF_B = A_BYTES, OFF_SA = OFF_B + B_BYTES;
+  static constexpr int OFF_SA2 = OFF_SA + SA_BYTES;   // A's low-window codes (TWO)
+  static constexpr int OFF_SB = OFF_SA2 + (TWO ? SA_BYTES : 0);
+  static constexpr int STAGE = OFF_SB + SB_BYTES;     // 38912 or 30720
+  static constexpr uint32_t kLoCol = 128;             // the low accumulator (TWO)
+  static constexpr uint32_t kLoSf = 16;               // the low MMA's scale group, from its step's (TWO)
+  // full, empty per stage; sf (rank 0) and sfree per entry; acc full / empty, done
+  static constexpr int NBARS = 2 * S + 2 * NENT + 3;
+  static constexpr int OFF_BAR = S * STAGE;
+  static constexpr int OFF_TMEM = OFF_BAR + 8 * NBARS;
+  static constexpr int OFF_ABORT = OFF_TMEM + 8;
+  static constexpr int OFF_TAB = OFF_ABORT + 8;  // the epilogue quantisation's scale table
+  static constexpr int SMEM_BYTES = OFF_TAB + (int)sizeof(ScaleTab) + 1024;   // + 1 KB alignment slack
+  // Instruction descriptor of kind::mxf4nvf4: A and B E2M1 (format 1), both
+  // K-major, UE4M3 scales (bit 23 clear), scale-factor data IDs 0,
+  // N (bits 17..22: N / 8), M = 256 for the pair (bits 24..28: M / 16); dense.
+  static constexpr uint32_t kIdesc =
+      (1u << 7) | (1u << 10) | ((uint32_t)(PN >> 3) << 17) | ((uint32_t)(PM >> 4) << 24);
+  static_assert(STAGE % 1024 == 0 && OFF_B % 1024 == 0 && OFF_SA % 128 == 0 && OFF_SA2 % 128 == 0 &&
+                    OFF_SB % 128 == 0,
+                "alignment");
+  static_assert(MMAS % ESTEPS == 0 && kSfCol0 + NENT * kEntryCols <= kTmemCols &&
+                    (TWO ? 2 * PN : PN) <= (int)kSfCol0 && NENT >= 2 && (!kEntryIsStage || NENT < S),
+                "TMEM map");
+  static_assert(PN % 32 == 0 && PN / 32 <= 8, "B's scale words fill at most 8 columns per MMA");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+};
 
-__device__ __forceinline__ void mma_nvfp4_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t sfa,
-                                               uint32_t sfb, uint32_t accum) {
+__device__ __forceinline__ void mma_nvfp4_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t sfa, uint32_t sfb, uint32_t accum) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %6, 0;\n\t"
       "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
-      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(sfa), "r"(sfb), "r"(accum)
+      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accum)
       : "memory");
 }
 
@@ -204,25 +238,34 @@ __device__ __forceinline__ void store_quantize_chunk(const uint32_t (&hh)[16], v
 }
 
 // Persistent, launched in clusters of two along x: cluster c (= blockIdx.x / 2)
-// takes tiles c, c + clusters, ... of the tiles_m x tiles_n grid of 256 x 256
-// tiles (row-major: consecutive clusters share A rows).
-template <bool F32OUT, bool QOUT>
+// takes tiles c, c + clusters, ... of the tiles_m x tiles_n grid of 256 x PN
+// tiles (row-major: consecutive clusters share A rows).  With TWO, mapSA holds
+// A's high-window codes and mapSA2 its low-window codes (unused otherwise).
+template <bool F32OUT, bool QOUT, bool TWO>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                       const __grid_constant__ CUtensorMap mapSA, const __grid_constant__ CUtensorMap mapSB,
+                      const __grid_constant__ CUtensorMap mapSA2,
                       const float* __restrict__ TA, const float* __restrict__ TB, int M, int N, int K,
                       void* __restrict__ out, int* status, long long budget, int skip_loads,
                       const float* __restrict__ fa, const float* __restrict__ fb, const int* skip_if,
                       const float* __restrict__ TC, uint8_t* __restrict__ qpay, uint8_t* __restrict__ qsc,
                       float* qamax, int qfmt) {
+  using G = Geo<TWO>;
+  constexpr int PN = G::PN, BH = G::BH, S = G::S, STAGE = G::STAGE;
+  constexpr int ESTEPS = G::ESTEPS, EPS = G::EPS, NENT = G::NENT;
+  constexpr int OFF_A = G::OFF_A, OFF_B = G::OFF_B, OFF_SA = G::OFF_SA, OFF_SA2 = G::OFF_SA2, OFF_SB = G::OFF_SB;
+  constexpr int OFF_BAR = G::OFF_BAR, OFF_TMEM = G::OFF_TMEM, OFF_ABORT = G::OFF_ABORT, OFF_TAB = G::OFF_TAB;
+  constexpr uint32_t kStepCols = G::kStepCols, kEntryCols = G::kEntryCols, kLoCol = G::kLoCol, kLoSf = G::kLoSf;
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
   if (skip_if && pair_read_flag(skip_if, sb + OFF_ABORT + 4)) return;   // both CTAs, before any setup
   const uint32_t bar_full = sb + OFF_BAR;            // TMA bytes of stage s landed (this CTA)
   const uint32_t bar_empty = bar_full + 8 * S;       // stage s MMAs completed
-  const uint32_t bar_sf = bar_empty + 8 * S;         // slot t scales in both CTAs' TMEM (rank 0)
-  const uint32_t bar_acc_full = bar_sf + 8 * SF;     // a tile's MMAs completed
+  const uint32_t bar_sf = bar_empty + 8 * S;         // entry t's scales in both CTAs' TMEM (rank 0)
+  const uint32_t bar_sfree = bar_sf + 8 * NENT;      // entry t's MMAs completed (unused when an entry is a stage)
+  const uint32_t bar_acc_full = bar_sfree + 8 * NENT;   // a tile's MMAs completed
   const uint32_t bar_acc_empty = bar_acc_full + 8;   // both CTAs' epilogues read TMEM (rank 0)
   const uint32_t bar_done = bar_acc_empty + 8;       // every MMA issued completed
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
@@ -248,7 +291,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_full + 8 * i, 1);
       mbar_init(bar_empty + 8 * i, 1);
     }
-    for (int i = 0; i < SF; ++i) mbar_init(bar_sf + 8 * i, 2 * kSfWarps);   // the scale warps of both CTAs
+    for (int i = 0; i < NENT; ++i) {
+      mbar_init(bar_sf + 8 * i, 2 * kSfWarps);   // the scale warps of both CTAs
+      mbar_init(bar_sfree + 8 * i, 1);
+    }
     mbar_init(bar_acc_full, 1);
     mbar_init(bar_acc_empty, 2 * kEpiWarps);          // the epilogue warps of both CTAs
     mbar_init(bar_done, 1);
@@ -282,7 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(st + OFF_A, &mapA, kb * ROWB, am0, bar_full + 8 * s);
           tma_load_2d(st + OFF_B, &mapB, kb * ROWB, bn0, bar_full + 8 * s);
           tma_load_2d(st + OFF_SA, &mapSA, kb * (BK / 16), am0, bar_full + 8 * s);
-          // the tile's 256 B rows of scale codes: this CTA loads its 128 and
+          if (TWO) tma_load_2d(st + OFF_SA2, &mapSA2, kb * (BK / 16), am0, bar_full + 8 * s);
+          // the tile's PN B rows of scale codes: this CTA loads its PN / 2 and
           // delivers them to both CTAs of the pair
           tma_load_2d_multicast(st + OFF_SB + (uint32_t)(BH * (BK / 16)) * rank, &mapSB, kb * (BK / 16), bn0,
                                 bar_full + 8 * s, (uint16_t)0x3);
@@ -313,24 +360,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          for (int kb = 0; kb < nk; ++kb, ++g) {
-            const int s = (int)(g % S), t = (int)(g % SF);
-            // both CTAs' scale warps have seen the stage's bytes land and put
-            // its scales in TMEM slot t
-            if (!mbar_wait_cluster(bar_sf + 8 * t, (uint32_t)((g / SF) & 1), abort_flag, budget)) {
-              fail(abort_flag, status);
-              ok = false;
-              break;
-            }
-            tc_fence_after();
+          for (int kb = 0; kb < nk && ok; ++kb, ++g) {
+            const int s = (int)(g % S);
             const uint32_t st = sb + s * STAGE;
             const uint64_t ad = sw128_desc(st + OFF_A), bd = sw128_desc(st + OFF_B);
 #pragma unroll
-            for (int i = 0; i < MMAS; ++i) {
-              const uint32_t sf = tmem + kSfCol0 + kSfStageCols * t + 16 * i;
-              mma_nvfp4_pair(tmem, ad + 2 * i, bd + 2 * i, sf + 8, sf, (kb | i) != 0 ? 1u : 0u);
+            for (int el = 0; el < EPS; ++el) {
+              const int64_t e = g * EPS + el;   // ring entry, over all tiles
+              const int t = (int)(e % NENT);
+              // both CTAs' scale warps have seen the stage's bytes land and put
+              // the entry's scales in TMEM
+              if (!mbar_wait_cluster(bar_sf + 8 * t, (uint32_t)((e / NENT) & 1), abort_flag, budget)) {
+                fail(abort_flag, status);
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+#pragma unroll
+              for (int jj = 0; jj < ESTEPS; ++jj) {
+                const int i = el * ESTEPS + jj;   // K64 step within the stage
+                const uint32_t sf = tmem + kSfCol0 + kEntryCols * t + kStepCols * jj;
+                const uint32_t acc = (kb | i) != 0 ? 1u : 0u;
+                mma_nvfp4_pair(tmem, ad + 2 * i, bd + 2 * i, G::kIdesc, sf + 8, sf, acc);
+                if (TWO)   // the low window: same operand tiles, its own scales and accumulator
+                  mma_nvfp4_pair(tmem + kLoCol, ad + 2 * i, bd + 2 * i, G::kIdesc, sf + kLoSf + 8, sf + kLoSf, acc);
+              }
+              if (!G::kEntryIsStage) mma_commit_pair(bar_sfree + 8 * t);
             }
-            mma_commit_pair(bar_empty + 8 * s);
+            if (ok) mma_commit_pair(bar_empty + 8 * s);
           }
           if (ok) mma_commit_pair(bar_acc_full);
         }
@@ -343,52 +400,87 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < kSfWarps) {
     // ------------------------------------------------ scale codes -> TMEM
-    // lane r0 of warp q writes TMEM lane 32 q + r0 of slot t: for MMA i,
-    // column 16 i + j holds the word of B row r0 + 32 j (j < 8, the tile's
-    // 256 B rows), column 16 i + 8 + j the word of A row r0 + 32 j (j < 4,
-    // this CTA's 128 A rows).  Slot t is rewritten once the MMAs of the
-    // stage that last used it (SF stages back) have completed.
+    // lane r0 of warp q writes TMEM lane 32 q + r0 of ring entry t: for the
+    // entry's K64 step j, column kStepCols j + c holds the word of B row
+    // r0 + 32 c (c < PN / 32, the tile's PN B rows), column kStepCols j + 8 + c
+    // the word of A row r0 + 32 c (c < 4, this CTA's 128 A rows); with TWO
+    // these are the high-window words, and the same group kLoSf columns on
+    // holds B's words and A's low-window words.  Entry t is rewritten once the
+    // MMAs that last read it (NENT entries back) have completed.
+    constexpr int NBW = PN / 32;   // B's words per lane and K64 step
     int64_t g = 0;
     bool ok = true;
     for (int tile = cid; tile < ntiles && ok; tile += ncl) {
-      for (int kb = 0; kb < nk; ++kb, ++g) {
-        const int s = (int)(g % S), t = (int)(g % SF);
-        const int64_t gp = g - SF;   // the stage that last used slot t
-        if (!mbar_wait(bar_full + 8 * s, (uint32_t)((g / S) & 1), abort_flag, budget) ||
-            (gp >= 0 && !mbar_wait(bar_empty + 8 * (int)(gp % S), (uint32_t)((gp / S) & 1), abort_flag, budget))) {
+      for (int kb = 0; kb < nk && ok; ++kb, ++g) {
+        const int s = (int)(g % S);
+        if (!mbar_wait(bar_full + 8 * s, (uint32_t)((g / S) & 1), abort_flag, budget)) {
           fail(abort_flag, status);
           ok = false;
           break;
         }
         const uint32_t st = sb + s * STAGE;
-        uint4 a[4], b[8];
+        uint4 a[4], b[NBW];
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) a[jj] = lds128(st + OFF_SA + (uint32_t)(lane + 32 * jj) * 16);
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) b[jj] = lds128(st + OFF_SB + (uint32_t)(lane + 32 * jj) * 16);
-        const uint32_t col = tmem + ((uint32_t)(32 * warp) << 16) + kSfCol0 + kSfStageCols * t;
+        for (int jj = 0; jj < NBW; ++jj) b[jj] = lds128(st + OFF_SB + (uint32_t)(lane + 32 * jj) * 16);
 #pragma unroll
-        for (int i = 0; i < MMAS; ++i) {
-          uint32_t v[16];
+        for (int el = 0; el < EPS; ++el) {
+          const int64_t e = g * EPS + el, ep = e - NENT;   // ep: the entry that last used t
+          const int t = (int)(e % NENT);
+          if (ep >= 0) {
+            const bool done = G::kEntryIsStage
+                                  ? mbar_wait(bar_empty + 8 * (int)(ep % S), (uint32_t)((ep / S) & 1), abort_flag, budget)
+                                  : mbar_wait(bar_sfree + 8 * t, (uint32_t)((ep / NENT) & 1), abort_flag, budget);
+            if (!done) {
+              fail(abort_flag, status);
+              ok = false;
+              break;
+            }
+          }
+          const uint32_t col = tmem + ((uint32_t)(32 * warp) << 16) + kSfCol0 + kEntryCols * t;
 #pragma unroll
-          for (int jj = 0; jj < 8; ++jj) v[jj] = word_of(b[jj], i);
+          for (int jj = 0; jj < ESTEPS; ++jj) {
+            const int i = el * ESTEPS + jj;
+            uint32_t v[16];
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) v[8 + jj] = word_of(a[jj], i);
+            for (int c = 0; c < 8; ++c) v[c] = c < NBW ? word_of(b[c], i) : 0u;
 #pragma unroll
-          for (int jj = 12; jj < 16; ++jj) v[jj] = 0u;
-          tmem_st16(col + 16 * i, v);
+            for (int c = 0; c < 4; ++c) v[8 + c] = word_of(a[c], i);
+#pragma unroll
+            for (int c = 12; c < 16; ++c) v[c] = 0u;
+            tmem_st16(col + kStepCols * jj, v);
+          }
+          if (TWO) {   // the low-window groups, loaded once the high ones are written
+            uint4 a2[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) a2[c] = lds128(st + OFF_SA2 + (uint32_t)(lane + 32 * c) * 16);
+#pragma unroll
+            for (int jj = 0; jj < ESTEPS; ++jj) {
+              const int i = el * ESTEPS + jj;
+              uint32_t v[16];
+#pragma unroll
+              for (int c = 0; c < 8; ++c) v[c] = c < NBW ? word_of(b[c], i) : 0u;
+#pragma unroll
+              for (int c = 0; c < 4; ++c) v[8 + c] = word_of(a2[c], i);
+#pragma unroll
+              for (int c = 12; c < 16; ++c) v[c] = 0u;
+              tmem_st16(col + kStepCols * jj + kLoSf, v);
+            }
+          }
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_rank0(bar_sf + 8 * t);
         }
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_rank0(bar_sf + 8 * t);
       }
     }
   } else {
     // ------------------------------------------------ epilogue (warps 4..11)
     // warp w takes TMEM lanes 32 (w % 4) .. +31 (the CTA's rows), columns
-    // 128 h .. 128 h + 127 (h = (w - 4) / 4), 64 at a time; TMEM is released
-    // to the next tile's MMAs as soon as the last 64 are in registers.
+    // (PN / 2) h .. (PN / 2) (h + 1) - 1 (h = (w - 4) / 4), 64 at a time; TMEM
+    // is released to the next tile's MMAs as soon as the last 64 are in
+    // registers.
     const int q = warp & 3, h = (warp - kEpiWarp0) >> 2;
     float alpha0 = __fmul_rn(__ldg(TA), __ldg(TB));
     if (fb) alpha0 = __fmul_rn(alpha0, __ldg(fb));   // a power of two: exact
@@ -405,11 +497,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       int am0, bn0, n0;
       tile_rows(tile, am0, bn0, n0);
       const int row = am0 + 32 * q + lane;
-      const int cbase = n0 + 128 * h;
+      const int cbase = n0 + (PN / 2) * h;
       const bool live = row < M && cbase < N;
       const float alpha = (fa && row < M) ? __fmul_rn(alpha0, __ldg(fa + row)) : alpha0;
-      const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(128 * h);
-      if (F32OUT) {
+      const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)((PN / 2) * h);
+      if (TWO) {
+        // 32 columns of each accumulator at a time: C = alpha (high + 2^-14
+        // low) -- the low window's factor is the high one's times 2^-14, an
+        // exact scaling, so the sum is rounded once, then alpha as below;
+        // TMEM released once the second chunk is in registers
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t r[64];
+          tmem_ld32_nowait(taddr + 32 * c, r);
+          tmem_ld32_nowait(taddr + kLoCol + 32 * c, r + 32);
+          tmem_ld_wait(r, 64);
+          if (c == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_rank0(bar_acc_empty);
+          }
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj)
+            r[jj] = __float_as_uint(__fmaf_rn(__uint_as_float(r[32 + jj]), 0x1p-14f, __uint_as_float(r[jj])));
+          if (F32OUT) {
+            if (live) store_f32x32(out, row, cbase + 32 * c, N, r, 0, alpha);
+          } else {
+            uint32_t hh[16];
+            pack_bf16x32(r, 0, alpha, hh);
+            if (live) store_bf16x32(out, row, cbase + 32 * c, N, hh);
+          }
+        }
+      } else if (F32OUT) {
         // 64 columns at a time; TMEM released (the next tile's MMAs may
         // overwrite the accumulator) once the second load is complete
 #pragma unroll
@@ -509,10 +628,12 @@ static bool make_scale_map(CUtensorMap* map, const uint8_t* base, int64_t rows, 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool F32OUT, bool QOUT = false>
+template <bool F32OUT, bool QOUT, bool TWO>
 static cudaError_t launch_native_t(const GemmArgs& a, const CUtensorMap& mA, const CUtensorMap& mB,
-                                   const CUtensorMap& mSA, const CUtensorMap& mSB, cudaStream_t st) {
-  auto kern = native::gemm_nvfp4_kernel<F32OUT, QOUT>;
+                                   const CUtensorMap& mSA, const CUtensorMap& mSB, const CUtensorMap& mSA2,
+                                   cudaStream_t st) {
+  using G = native::Geo<TWO>;
+  auto kern = native::gemm_nvfp4_kernel<F32OUT, QOUT, TWO>;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -522,7 +643,7 @@ static cudaError_t launch_native_t(const GemmArgs& a, const CUtensorMap& mA, con
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cfg.blockDim = dim3(native::kThreads);
-  cfg.dynamicSmemBytes = native::SMEM_BYTES;
+  cfg.dynamicSmemBytes = G::SMEM_BYTES;
   cfg.stream = st;
   // one cluster per SM pair that can hold one (asked once per device and
   // output type; the tiles are then walked by the resident clusters)
@@ -531,7 +652,7 @@ static cudaError_t launch_native_t(const GemmArgs& a, const CUtensorMap& mA, con
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, native::SMEM_BYTES);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   if (clusters[dev] == 0) {
     cfg.gridDim = dim3(2);
@@ -541,10 +662,10 @@ static cudaError_t launch_native_t(const GemmArgs& a, const CUtensorMap& mA, con
     if (n <= 0) return cudaErrorNotSupported;
     clusters[dev] = n;
   }
-  const int64_t ntiles = ((a.N + native::PN - 1) / native::PN) * ((a.M + native::PM - 1) / native::PM);
+  const int64_t ntiles = ((a.N + G::PN - 1) / G::PN) * ((a.M + native::PM - 1) / native::PM);
   const int ncl = (int)(ntiles < clusters[dev] ? ntiles : clusters[dev]);
   cfg.gridDim = dim3(2u * (unsigned)ncl);
-  e = cudaLaunchKernelEx(&cfg, kern, mA, mB, mSA, mSB, a.TA, a.TB, (int)a.M, (int)a.N, (int)a.K, a.out, a.status,
+  e = cudaLaunchKernelEx(&cfg, kern, mA, mB, mSA, mSB, mSA2, a.TA, a.TB, (int)a.M, (int)a.N, (int)a.K, a.out, a.status,
                          a.wait_cycles, a.skip_loads ? 1 : 0, a.fa, a.fb, a.skip_if, a.TC, a.qpay, a.qsc, a.qamax,
                          a.fmt_out);
   if (e != cudaSuccess) return e;
@@ -553,13 +674,21 @@ static cudaError_t launch_native_t(const GemmArgs& a, const CUtensorMap& mA, con
 
 cudaError_t launch_gemm_nvfp4(const GemmArgs& a, cudaStream_t st) {
   if (a.M == 0 || a.N == 0) return cudaSuccess;
-  CUtensorMap mA, mB, mSA, mSB;
+  const bool two = a.As_lo != nullptr;
+  const uint32_t bh = two ? native::Geo<true>::BH : native::Geo<false>::BH;
+  CUtensorMap mA, mB, mSA, mSB, mSA2;
   if (!make_swizzled_payload_map(&mA, a.A, a.M, a.K, native::BM) ||
-      !make_swizzled_payload_map(&mB, a.B, a.N, a.K, native::BH) ||
-      !make_scale_map(&mSA, a.As, a.M, a.K, native::BM) || !make_scale_map(&mSB, a.Bs, a.N, a.K, native::BH))
+      !make_swizzled_payload_map(&mB, a.B, a.N, a.K, bh) || !make_scale_map(&mSA, a.As, a.M, a.K, native::BM) ||
+      !make_scale_map(&mSB, a.Bs, a.N, a.K, bh) ||
+      !make_scale_map(&mSA2, two ? a.As_lo : a.As, a.M, a.K, native::BM))
     return cudaErrorNotSupported;
-  if (a.qpay) return launch_native_t<false, true>(a, mA, mB, mSA, mSB, st);   // BF16 result (nullable) + its quantisation
-  return a.out_f32 ? launch_native_t<true>(a, mA, mB, mSA, mSB, st) : launch_native_t<false>(a, mA, mB, mSA, mSB, st);
+  if (two)   // A's codes in two windows: BF16 or binary32 result, no epilogue quantisation
+    return a.out_f32 ? launch_native_t<true, false, true>(a, mA, mB, mSA, mSB, mSA2, st)
+                     : launch_native_t<false, false, true>(a, mA, mB, mSA, mSB, mSA2, st);
+  if (a.qpay)   // BF16 result (nullable) + its quantisation
+    return launch_native_t<false, true, false>(a, mA, mB, mSA, mSB, mSA2, st);
+  return a.out_f32 ? launch_native_t<true, false, false>(a, mA, mB, mSA, mSB, mSA2, st)
+                   : launch_native_t<false, false, false>(a, mA, mB, mSA, mSB, mSA2, st);
 }
 
 }  // namespace fp4q

@@ -16,6 +16,11 @@
 //                every code is checked on its own.
 // A group that does not fit sets *nofit (never cleared here); its codes and
 // factor are then unspecified.
+// Two windows per row (rebias_rows2_kernel): the 14 binades under the row's
+// top as above (factor f_hi = 2^(e_top - 7)) and the 14 below them
+// [e_top - 27, e_top - 14] (factor f_lo = 2^(e_top - 21) = f_hi 2^-14), each
+// code in exactly one of the two outputs and zero in the other; a code below
+// both windows sets *nofit and is zero in both.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -146,7 +151,112 @@ __global__ void __launch_bounds__(256) rebias_tensor_kernel(const uint4* __restr
   if (__any_sync(0xFFFFFFFFu, bad != 0u) && (threadIdx.x & 31) == 0) atomicOr(nofit, 1);
 }
 
+// The UE4M3 codes of a non-zero UE5M3 code in the two windows of a row with
+// top binade etop (exactly one of hi, lo non-zero, or neither below both).
+__device__ __forceinline__ void recode2(uint32_t c, int etop, uint32_t& hi, uint32_t& lo) {
+  hi = lo = 0;
+  if (c == 0) return;
+  uint32_t mn;
+  const int e = binade(c, mn);
+  if (e >= etop - 13)
+    hi = ((uint32_t)(e - etop + 14) << 3) | mn;
+  else if (e >= etop - 27)
+    lo = ((uint32_t)(e - etop + 28) << 3) | mn;
+}
+
+// Two windows per row, one warp per row (grid-stride); layout as
+// rebias_rows_kernel.  When every non-zero code is normal, a code's window is
+// decided by a bytewise compare of the code against the first code of the
+// window (E_top - 13 and E_top - 27 exponent fields, clamped at 0), and each
+// window's re-encode is one bytewise add: fields drop by E_top - 14 (high)
+// and E_top - 28 (low).
+__global__ void __launch_bounds__(256) rebias_rows2_kernel(const uint8_t* __restrict__ in, int64_t rows, int nb,
+                                                           uint8_t* __restrict__ out_hi,
+                                                           uint8_t* __restrict__ out_lo, float* __restrict__ f_hi,
+                                                           float* __restrict__ f_lo, int* nofit) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int chunks = nb >> 4;
+  for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += nwarps) {
+    const uint4* src = reinterpret_cast<const uint4*>(in + r * nb);
+    uint32_t vmax = 0u, vmin = 0xFFFFFFFFu;
+    for (int j = lane; j < chunks; j += 32) {
+      const uint4 v = __ldg(src + j);
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const uint32_t word = word_at(v, w);
+        vmax = __vmaxu4(vmax, word);
+        vmin = __vminu4(vmin, word | ~__vcmpne4(word, 0u));
+      }
+    }
+    const uint32_t cmax = __reduce_max_sync(0xFFFFFFFFu, max_byte(vmax));
+    const uint32_t cmin = __reduce_min_sync(0xFFFFFFFFu, min_byte(vmin));
+    uint32_t mn;
+    const bool any = cmax != 0u;
+    const int emax = any ? binade(cmax, mn) : kNone;
+    if (lane == 0) {
+      f_hi[r] = any ? pow2(emax - 7) : 1.0f;
+      f_lo[r] = any ? pow2(emax - 21) : pow2(-14);
+      if (any && binade(cmin, mn) < emax - 27) atomicOr(nofit, 1);
+    }
+    uint4* dh = reinterpret_cast<uint4*>(out_hi + r * nb);
+    uint4* dl = reinterpret_cast<uint4*>(out_lo + r * nb);
+    if (cmin >= 8u) {   // every non-zero code normal (an all-zero row: cmin = 0xFF)
+      const int et = (int)(cmax >> 3);
+      const uint32_t thi = (uint32_t)(max(et - 13, 0) << 3) * 0x01010101u;
+      const uint32_t tlo = (uint32_t)(max(et - 27, 0) << 3) * 0x01010101u;
+      const uint32_t khi = ((uint32_t)(14 - et) << 3 & 0xFFu) * 0x01010101u;
+      const uint32_t klo = ((uint32_t)(28 - et) << 3 & 0xFFu) * 0x01010101u;
+      for (int j = lane; j < chunks; j += 32) {
+        const uint4 v = __ldg(src + j);
+        uint32_t h[4], l[4];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const uint32_t word = word_at(v, w);
+          const uint32_t nz = __vcmpne4(word, 0u);
+          const uint32_t inhi = __vcmpgeu4(word, thi) & nz;
+          const uint32_t inlo = __vcmpgeu4(word, tlo) & nz & ~inhi;
+          h[w] = __vadd4(word, khi) & inhi;
+          l[w] = __vadd4(word, klo) & inlo;
+        }
+        dh[j] = make_uint4(h[0], h[1], h[2], h[3]);
+        dl[j] = make_uint4(l[0], l[1], l[2], l[3]);
+      }
+    } else {            // subnormal codes: normalised code by code
+      for (int j = lane; j < chunks; j += 32) {
+        const uint4 v = __ldg(src + j);
+        uint32_t h[4], l[4];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const uint32_t word = word_at(v, w);
+          h[w] = l[w] = 0;
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            uint32_t ch, cl;
+            recode2((word >> (8 * b)) & 0xFFu, emax, ch, cl);
+            h[w] |= ch << (8 * b);
+            l[w] |= cl << (8 * b);
+          }
+        }
+        dh[j] = make_uint4(h[0], h[1], h[2], h[3]);
+        dl[j] = make_uint4(l[0], l[1], l[2], l[3]);
+      }
+    }
+  }
+}
+
 }  // namespace rebias
+
+cudaError_t launch_rebias2(const uint8_t* scales, int64_t rows, int64_t nb, uint8_t* out_hi, uint8_t* out_lo,
+                           float* f_hi, float* f_lo, int* nofit, cudaStream_t st) {
+  if (rows == 0) return cudaSuccess;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t want = (rows + 7) / 8;   // eight rows (warps) per 256-thread block
+  const int grid = (int)(want < (int64_t)sms * 8 ? want : (int64_t)sms * 8);
+  rebias::rebias_rows2_kernel<<<grid, 256, 0, st>>>(scales, rows, (int)nb, out_hi, out_lo, f_hi, f_lo, nofit);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_rebias(const uint8_t* scales, int64_t rows, int64_t nb, bool per_row, uint8_t* out,
                           float* factor, int* nofit, cudaStream_t st) {

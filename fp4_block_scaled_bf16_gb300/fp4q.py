@@ -28,6 +28,7 @@ UE5M3, UE4M3 = 0, 1
 EXPORTS = ("fp4q_amax", "fp4q_tensor_scale", "fp4q_quantize", "fp4q_dequantize", "fp4q_gemm",
            "fp4q_gemm_quantize", "fp4q_gemm_nvfp4", "fp4q_rebias_scales", "fp4q_gemm_nvfp4_rebiased",
            "fp4q_gemm_if", "fp4q_gemm_nvfp4_rebiased_quantize", "fp4q_gemm_quantize_if",
+           "fp4q_rebias_scales_two_windows", "fp4q_gemm_nvfp4_two_windows",
            "fp4q_get_device_status", "fp4q_status_string")
 
 
@@ -53,6 +54,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fp4q_gemm_quantize.argtypes = [P, P, P, P, P, P, i64, i64, i64, i32, P, P, P, P, P, P]
     lib.fp4q_gemm_nvfp4.argtypes = [P, P, P, P, P, P, i64, i64, i64, P, i32, P]
     lib.fp4q_rebias_scales.argtypes = [P, i64, i64, i32, P, P, P, P]
+    lib.fp4q_rebias_scales_two_windows.argtypes = [P, i64, i64, P, P, P, P, P, P]
+    lib.fp4q_gemm_nvfp4_two_windows.argtypes = [P, P, P, P, P, P, P, P, P, i64, i64, i64, P, P, i32, P]
     lib.fp4q_gemm_nvfp4_rebiased.argtypes = [P, P, P, P, P, P, P, P, i64, i64, i64, P, P, i32, P]
     lib.fp4q_gemm_if.argtypes = [P, P, P, P, P, P, i64, i64, i64, i32, P, P, i32, P]
     lib.fp4q_gemm_nvfp4_rebiased_quantize.argtypes = [P, P, P, P, P, P, P, P, i64, i64, i64, P, i32, P, P, P, P,
@@ -277,6 +280,47 @@ def fp4q_gemm_nvfp4_rebiased(A, A_scales4, A_factor, A_tscale, B, B_scales4, B_f
         _ptr(B_factor), _ptr(B_tscale), M, N, K, _ptr(skip_if_set), _ptr(out), int(f32), _stream()))
 
 
+def fp4q_rebias_scales_two_windows(scales, rows, nblocks, out_hi, out_lo, out_factor_hi, out_factor_lo,
+                                   inout_nofit) -> None:
+    """UE5M3 codes -> UE4M3 codes in two 14-binade windows per row (high and
+    low) with their power-of-two factors; ORs 1 into inout_nofit when a code
+    lies below both."""
+    if rows < 0 or nblocks < 0 or nblocks % 16:
+        raise ValueError(f"rows >= 0 and nblocks a multiple of 16 required, got {rows}, {nblocks}")
+    for t, name in ((scales, "scales"), (out_hi, "out_hi"), (out_lo, "out_lo")):
+        _mat(t, name, (rows, nblocks), torch.uint8)
+    _scalar(out_factor_hi, "out_factor_hi", rows)
+    _scalar(out_factor_lo, "out_factor_lo", rows)
+    _scalar(inout_nofit, "inout_nofit", 1, torch.int32)
+    _on_device(("scales", scales), ("out_hi", out_hi), ("out_lo", out_lo), ("out_factor_hi", out_factor_hi),
+               ("out_factor_lo", out_factor_lo), ("inout_nofit", inout_nofit))
+    _check("fp4q_rebias_scales_two_windows", _lib.fp4q_rebias_scales_two_windows(
+        _ptr(scales), rows, nblocks, _ptr(out_hi), _ptr(out_lo), _ptr(out_factor_hi), _ptr(out_factor_lo),
+        _ptr(inout_nofit), _stream()))
+
+
+def fp4q_gemm_nvfp4_two_windows(A, A_scales_hi, A_scales_lo, A_factor_hi, A_tscale, B, B_scales4, B_factor,
+                                B_tscale, M, N, K, skip_if_set, out) -> None:
+    """Native block-scaled GEMM with A's codes in two windows (two
+    accumulators, the low one scaled by 2^-14) and B's per-tensor rebiased;
+    a no-op when the device int skip_if_set is set."""
+    ops = _gemm_operands(A, A_scales_hi, A_tscale, B, B_scales4, B_tscale, M, N, K)
+    _mat(A_scales_lo, "A_scales_lo", (M, K // 16), torch.uint8)
+    _scalar(A_factor_hi, "A_factor_hi", M)
+    _scalar(B_factor, "B_factor")
+    if skip_if_set is not None:
+        _scalar(skip_if_set, "skip_if_set", 1, torch.int32)
+    _out_dtype(out)
+    _mat(out, "out", (M, N), out.dtype)
+    _on_device(*ops, ("A_scales_lo", A_scales_lo), ("A_factor_hi", A_factor_hi), ("B_factor", B_factor),
+               ("skip_if_set", skip_if_set), ("out", out))
+    f32 = out.dtype == torch.float32
+    _check("fp4q_gemm_nvfp4_two_windows", _lib.fp4q_gemm_nvfp4_two_windows(
+        _ptr(A), _ptr(A_scales_hi), _ptr(A_scales_lo), _ptr(A_factor_hi), _ptr(A_tscale), _ptr(B),
+        _ptr(B_scales4), _ptr(B_factor), _ptr(B_tscale), M, N, K, _ptr(skip_if_set), _ptr(out), int(f32),
+        _stream()))
+
+
 def fp4q_gemm_if(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K, fmt, run_if_set, out) -> None:
     """fp4q_gemm, run only when the device int run_if_set is non-zero."""
     ops = _gemm_operands(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K)
@@ -483,6 +527,40 @@ def gemm_ue5m3_rebiased(A, A_scales, A_tscale, B, B_scales, B_tscale, dtype=torc
     a4, fa, _ = rebias_scales(A_scales, True, nofit)
     b4, fb, _ = rebias_scales(B_scales, False, nofit)
     fp4q_gemm_nvfp4_rebiased(A, a4, fa, A_tscale, B, b4, fb, B_tscale, M, N, K, nofit, out)
+    fp4q_gemm_if(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K, UE5M3, nofit, out)
+    return out
+
+
+def rebias_scales_two_windows(scales, nofit: torch.Tensor | None = None):
+    """fp4q_rebias_scales_two_windows with allocated outputs: (high codes, low
+    codes, high factors, low factors, nofit).  A given `nofit` (int32 [1]) is
+    OR-ed into, not cleared."""
+    R, nb = scales.shape
+    hi, lo = torch.empty_like(scales), torch.empty_like(scales)
+    fh = torch.empty(R, dtype=torch.float32, device=scales.device)
+    fl = torch.empty(R, dtype=torch.float32, device=scales.device)
+    if nofit is None:
+        nofit = torch.zeros(1, dtype=torch.int32, device=scales.device)
+    fp4q_rebias_scales_two_windows(scales, R, nb, hi, lo, fh, fl, nofit)
+    return hi, lo, fh, fl, nofit
+
+
+def gemm_ue5m3_two_windows(A, A_scales, A_tscale, B, B_scales, B_tscale, dtype=torch.bfloat16, out=None,
+                           nofit: torch.Tensor | None = None) -> torch.Tensor:
+    """gemm_ue5m3_rebiased with A's scales in two windows per row: the native
+    GEMM with two accumulators, and the emulated GEMM in its place (decided on
+    the device) when a code of A lies below both windows or one of B outside
+    B's window.  `nofit` (int32 [1], zeroed here) receives the decision."""
+    M, K = A.shape[0], A.shape[1] * 2
+    N = B.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=dtype, device=A.device)
+    if nofit is None:
+        nofit = torch.empty(1, dtype=torch.int32, device=A.device)
+    nofit.zero_()
+    ah, al, fh, _, _ = rebias_scales_two_windows(A_scales, nofit)
+    b4, fb, _ = rebias_scales(B_scales, False, nofit)
+    fp4q_gemm_nvfp4_two_windows(A, ah, al, fh, A_tscale, B, b4, fb, B_tscale, M, N, K, nofit, out)
     fp4q_gemm_if(A, A_scales, A_tscale, B, B_scales, B_tscale, M, N, K, UE5M3, nofit, out)
     return out
 

@@ -271,6 +271,47 @@ fp4q_status fp4q_gemm_quantize_if(const uint8_t* A, const uint8_t* A_scales, con
                                   const float* c_tscale, void* out_bf16, uint8_t* out_payload,
                                   uint8_t* out_scales, float* out_amax, void* stream);
 
+/* Two-window exponent rebias of UE5M3 block-scale codes, per row, for an
+ * operand whose rows span more binades than one UE4M3 window holds (the
+ * column-wise codes of a gradient whose per-token magnitudes differ by many
+ * decades, the A operand of wgrad).  Same reading of the page as
+ * fp4q_rebias_scales (its Abstract: UE5M3 is emulated because the hardware
+ * takes E4M3/E8M0 block scales), with two 14-binade windows under each row's
+ * largest binade e_top:
+ *   high window [e_top - 13, e_top]:      out_hi code, factor 2^(e_top - 7)
+ *   low window  [e_top - 27, e_top - 14]: out_lo code, factor 2^(e_top - 21)
+ * each non-zero code going to exactly one of out_hi, out_lo (zero in the
+ * other), so that
+ *   s = factor_hi * UE4M3(out_hi) + factor_lo * UE4M3(out_lo)   exactly.
+ * factor_lo = factor_hi * 2^-14 always (a row with no non-zero scale: 1 and
+ * 2^-14, zero codes).  A non-zero code below both windows sets *inout_nofit to
+ * 1 (OR-ed, never cleared here) and is zero in both outputs.
+ * scales: UE5M3 codes [rows, nblocks]; out_hi, out_lo: UE4M3 codes of the
+ * same shape; out_factor_hi, out_factor_lo: binary32 [rows]; all device.  The
+ * three code arrays must not overlap (FP4Q_ERR_ARG).  nblocks a multiple of
+ * 16; code arrays 16-byte aligned, factors and inout_nofit 4-byte aligned.
+ * Asynchronous on `stream`; nothing is read back to the host. */
+fp4q_status fp4q_rebias_scales_two_windows(const uint8_t* scales, int64_t rows, int64_t nblocks, uint8_t* out_hi,
+                                           uint8_t* out_lo, float* out_factor_hi, float* out_factor_lo,
+                                           int* inout_nofit, void* stream);
+
+/* The UE5M3 GEMM on the native block-scaled MMA with A's codes in two windows
+ * (fp4q_rebias_scales_two_windows) and B's in one (fp4q_rebias_scales,
+ * per_row == 0): each K step multiplies the same E2M1 operand tiles twice,
+ * once with A's high-window codes and once with its low-window codes, into
+ * two binary32 accumulators, and the epilogue forms
+ *   C[m, n] = (T_A * T_B * fb * fa_hi[m]) * (acc_hi[m, n] + 2^-14 acc_lo[m, n])
+ * (the 2^-14 scaling exact, the sum rounded once in binary32), which is the
+ * UE5M3 contraction of fp4q_gemm on the original scales up to the
+ * accumulation order.  A_factor_hi: the per-row high-window factors [M];
+ * skip_if_set, shapes (K a multiple of 256), alignment, waits, test hooks and
+ * out as fp4q_gemm_nvfp4_rebiased; A_scales_lo 16-byte aligned. */
+fp4q_status fp4q_gemm_nvfp4_two_windows(const uint8_t* A, const uint8_t* A_scales_hi, const uint8_t* A_scales_lo,
+                                        const float* A_factor_hi, const float* A_tscale, const uint8_t* B,
+                                        const uint8_t* B_scales4, const float* B_factor, const float* B_tscale,
+                                        int64_t M, int64_t N, int64_t K, const int* skip_if_set, void* out,
+                                        int out_is_f32, void* stream);
+
 /* Reads the device status word of the current device in the order of
  * `stream` (after every call already issued on it), waits for `stream` alone
  * (no other stream of the device is synchronised), returns the latched

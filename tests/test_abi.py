@@ -131,6 +131,31 @@ def test_host_validation_rejects_before_launch(lib):
     assert r(src, 16, 16, 1, P(base + 16 * 8), ok, ok, None) == ERR_ARG   # overlapping in/out
     assert r(src, 0, 16, 1, dst, ok, ok, None) == 0                     # no rows: no-op
 
+    r2 = lib.fp4q_rebias_scales_two_windows
+    r2.argtypes = [P, i64, i64, P, P, P, P, P, P]
+    buf2 = ctypes.create_string_buffer(16 * 16 + 16)   # a third 16 x 16 array, apart from src and dst
+    lo = P((ctypes.addressof(buf2) + 15) & ~15)
+    assert r2(src, 16, 24, dst, lo, ok, ok, ok, None) == ERR_SHAPE     # nblocks % 16
+    assert r2(src, 16, 16, dst, lo, None, ok, ok, None) == ERR_ARG     # high factors
+    assert r2(src, 16, 16, dst, lo, ok, None, ok, None) == ERR_ARG     # low factors
+    assert r2(src, 16, 16, dst, lo, ok, ok, None, None) == ERR_ARG     # flag
+    assert r2(src, 16, 16, dst, None, ok, ok, ok, None) == ERR_ARG
+    assert r2(src, 16, 16, dst, P(base + 8), ok, ok, ok, None) == ERR_ALIGN
+    assert r2(src, 16, 16, dst, lo, ok, P(18), ok, None) == ERR_ALIGN
+    assert r2(src, 16, 16, dst, P(base + 16 * 8), ok, ok, ok, None) == ERR_ARG   # low codes over the input
+    assert r2(src, 16, 16, dst, P(base + 16 * 40), ok, ok, ok, None) == ERR_ARG  # the two outputs overlap
+    assert r2(src, 0, 16, dst, lo, ok, ok, ok, None) == 0                       # no rows: no-op
+
+    w = lib.fp4q_gemm_nvfp4_two_windows
+    w.argtypes = [P, P, P, P, P, P, P, P, P, i64, i64, i64, P, P, ctypes.c_int, P]
+    assert w(ok, ok, ok, ok, ok, ok, ok, ok, ok, 128, 128, 128, None, ok, 0, None) == ERR_SHAPE   # K % 256
+    assert w(ok, ok, None, ok, ok, ok, ok, ok, ok, 128, 128, 256, None, ok, 0, None) == ERR_ARG   # low codes
+    assert w(ok, ok, ok, None, ok, ok, ok, ok, ok, 128, 128, 256, None, ok, 0, None) == ERR_ARG   # A factors
+    assert w(ok, ok, ok, ok, ok, ok, ok, None, ok, 128, 128, 256, None, ok, 0, None) == ERR_ARG   # B factor
+    assert w(ok, ok, P(8), ok, ok, ok, ok, ok, ok, 128, 128, 256, None, ok, 0, None) == ERR_ALIGN
+    assert w(ok, ok, ok, P(18), ok, ok, ok, ok, ok, 128, 128, 256, None, ok, 0, None) == ERR_ALIGN
+    assert w(ok, ok, ok, ok, ok, ok, ok, ok, ok, 0, 128, 256, None, ok, 0, None) == 0   # empty: no-op
+
     n = lib.fp4q_gemm_nvfp4_rebiased
     n.argtypes = [P, P, P, P, P, P, P, P, i64, i64, i64, P, P, ctypes.c_int, P]
     assert n(ok, ok, ok, ok, ok, ok, ok, ok, 128, 128, 128, None, ok, 0, None) == ERR_SHAPE   # K % 256

@@ -140,6 +140,26 @@ def test_rebiased_gemm_shapes(fp4q):
     raises(c, A, As, TA, B, Bs, TB, M, N, K, 0, flag, bf(M, N + 16), match="out")
 
 
+def test_two_window_shapes(fp4q):
+    r = fp4q.fp4q_rebias_scales_two_windows
+    f8 = torch.ones(8)
+    flag = torch.zeros(1, dtype=torch.int32)
+    raises(r, u8(8, 32), 8, 32, u8(8, 32), u8(8, 32), f8, f8, flag, match="CUDA")
+    raises(r, u8(8, 24), 8, 24, u8(8, 24), u8(8, 24), f8, f8, flag, match="multiple of 16")
+    raises(r, u8(8, 32), 8, 32, u8(8, 32), u8(8, 16), f8, f8, flag, match="out_lo")
+    raises(r, u8(8, 32), 8, 32, u8(8, 32), u8(8, 32), torch.ones(1), f8, flag, match="out_factor_hi")
+    raises(r, u8(8, 32), 8, 32, u8(8, 32), u8(8, 32), f8, f8, torch.zeros(1), match="inout_nofit")
+    M, N, K = 32, 64, 256
+    A, As, TA, B, Bs, TB = _gemm_ops(M, N, K)
+    g = fp4q.fp4q_gemm_nvfp4_two_windows
+    fa, fb = torch.ones(M), torch.ones(1)
+    raises(g, A, As, u8(M, K // 16), fa, TA, B, Bs, fb, TB, M, N, K, flag, bf(M, N), match="CUDA")
+    raises(g, A, As, u8(M, K // 32), fa, TA, B, Bs, fb, TB, M, N, K, flag, bf(M, N), match="A_scales_lo")
+    raises(g, A, As, u8(M, K // 16), torch.ones(1), TA, B, Bs, fb, TB, M, N, K, flag, bf(M, N),
+           match="A_factor_hi")
+    raises(g, A, As, u8(M, K // 16), fa, TA, B, Bs, None, TB, M, N, K, flag, bf(M, N), match="B_factor")
+
+
 def test_rebiased_fused_gemm_shapes(fp4q):
     M, N, K = 32, 64, 256
     A, As, TA, B, Bs, TB = _gemm_ops(M, N, K)
