@@ -8,12 +8,14 @@ an amax pass only on the very first step); dual-axis block-16 E2M1/UE5M3
 quantisation of X and W (RNE) and of dY (Philox SR, seed 7); the three
 training GEMMs on the block-scaled operands (fprop Y = X W^T, dgrad
 dX = dY W, wgrad dW = dY^T X), each 8192 x 16384 x 4096 multiply-adds.
-fprop and dgrad run on the tensor cores' block-scaled MMA with their UE5M3
-scale codes rebiased to UE4M3 codes times powers of two (exact; the emulated
-GEMM takes over on the device when a group does not fit), wgrad on the
-emulated GEMM.  The same step with all three GEMMs emulated, and under
-current scaling (amax pass + scale before every quantisation), are timed
-beside it.
+All three run on the tensor cores' block-scaled MMA with their UE5M3 scale
+codes rebiased to UE4M3 codes times powers of two (exact; the emulated GEMM
+takes over on the device when a group does not fit): fprop and dgrad with
+one window per A row, wgrad -- whose A rows run over tokens of very
+different gradient magnitude -- with two windows per row and two
+accumulators.  The same step with wgrad emulated, with all three GEMMs
+emulated, and under current scaling (amax pass + scale before every
+quantisation), are timed beside it.
 
 value = the three GEMMs' 2MNK flops / step time (quantisation included),
 TFLOP/s.  Per-kernel CUDA-event times give the quantiser GB/s and the GEMM
@@ -61,6 +63,7 @@ def kernel_sources_sha(files):
 
 
 GEMM_SOURCES = ["gemm.cu", "fp4q_device.cuh", "fp4q_pipeline.cuh", "fp4q_tcgen05.cuh"]
+NATIVE_SOURCES = ["gemm_native.cu", "fp4q_device.cuh", "fp4q_pipeline.cuh", "fp4q_tcgen05.cuh"]
 
 
 def committed_traffic(name, sources, launch=None):
@@ -268,6 +271,32 @@ def rebias_parts(torch, fp4q, st, steps):
             "skipped_emulated_launch_ms": seg(3, 4), "flag": int(flag.item())}
 
 
+def wgrad_parts(torch, fp4q, st, steps):
+    """The same for the step's wgrad through two-window codes: the per-row
+    two-window rebias of dY's column-wise codes, the per-tensor rebias of X's,
+    the two-accumulator native GEMM, and the emulated GEMM's skipped launch."""
+    tokens, hid, out = st.dims
+    ah, al, fh, fl, b4, fb, flag = st.rb[2]
+    TX, TD = st.tensor_scales(periodic=False)[0], st.tensor_scales(periodic=False)[2]
+    flag.zero_()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    for k in range(steps):
+        ev[k][0].record()
+        fp4q.fp4q_rebias_scales_two_windows(st.Dcs, out, tokens // 16, ah, al, fh, fl, flag)
+        ev[k][1].record()
+        fp4q.fp4q_rebias_scales(st.Xcs, hid, tokens // 16, False, b4, fb, flag)
+        ev[k][2].record()
+        fp4q.fp4q_gemm_nvfp4_two_windows(st.Dc, ah, al, fh, TD, st.Xc, b4, fb, TX, out, hid, tokens, flag, st.dW)
+        ev[k][3].record()
+        fp4q.fp4q_gemm_if(st.Dc, st.Dcs, TD, st.Xc, st.Xcs, TX, out, hid, tokens, fp4q.UE5M3, flag, st.dW)
+        ev[k][4].record()
+    torch.cuda.synchronize()
+    seg = lambda a, b: sum(e[a].elapsed_time(e[b]) for e in ev) / steps
+    return {"rebias_two_windows_dY_ms": seg(0, 1), "rebias_tensor_X_ms": seg(1, 2), "native_gemm_ms": seg(2, 3),
+            "skipped_emulated_launch_ms": seg(3, 4), "flag": int(flag.item())}
+
+
 def run_gpu(args, rank, world):
     import torch
     from fp4_block_scaled_bf16_gb300 import build, fp4q, workloads
@@ -287,14 +316,15 @@ def run_gpu(args, rank, world):
     hW = workloads.to_torch_bf16(Wb).pin_memory()
     hD = workloads.to_torch_bf16(dYb).pin_memory()
     X, W, dY = hX.to(dev), hW.to(dev), hD.to(dev)
-    # the step as the library runs it: fprop and dgrad on the block-scaled
-    # MMA through rebiased UE5M3 scale codes (emulated fallback decided on
-    # the device), wgrad emulated; and the same step with all three GEMMs
-    # emulated
-    rstep = LinearStep(X, W, dY, seed=7, rebias=True)
+    # the step as the library runs it: the three GEMMs on the block-scaled
+    # MMA through rebiased UE5M3 scale codes (wgrad's A in two windows;
+    # emulated fallback decided on the device); the same step with wgrad
+    # emulated; and with all three GEMMs emulated
+    rstep = LinearStep(X, W, dY, seed=7, rebias=True, rebias_wgrad=True)
+    wstep = LinearStep(X, W, dY, seed=7, rebias=True)
     step = LinearStep(X, W, dY, seed=7)
     for _ in range(args.warmup):
-        for st_w in (rstep, step):
+        for st_w in (rstep, wstep, step):
             st_w.run_overlapped(periodic=True)
             st_w.run_overlapped()
             st_w.run()
@@ -331,14 +361,18 @@ def run_gpu(args, rank, world):
         fallbacks = rstep.fallbacks()
         refreshes = [sc.step for sc in rstep.scalers]
         ms_emulated = timed(lambda k: step.run_overlapped(periodic=True))
+        ms_wgrad_emulated = timed(lambda k: wstep.run_overlapped(periodic=True))
         ms_current = timed(lambda k: rstep.run_overlapped())
         ms_serial = timed(lambda k: step.run(evs[k]))
         ms_serial_r = timed(lambda k: rstep.run(evr[k]))
         parts = rebias_parts(torch, fp4q, rstep, args.steps)
+        wparts = wgrad_parts(torch, fp4q, rstep, args.steps)
+    del wstep
     if world > 1:
         ms = max_over_ranks(ms, dev)
         ms_emulated = max_over_ranks(ms_emulated, dev)
         ms_current = max_over_ranks(ms_current, dev)
+        ms_wgrad_emulated = max_over_ranks(ms_wgrad_emulated, dev)
     seg = lambda a, b: sum(e[a].elapsed_time(e[b]) for e in evs) / args.steps
     segr = lambda a, b: sum(e[a].elapsed_time(e[b]) for e in evr) / args.steps
     t_scale, t_qx, t_qw, t_qd = seg(0, 1), seg(1, 2), seg(2, 3), seg(3, 4)
@@ -355,7 +389,7 @@ def run_gpu(args, rank, world):
     hdX = [torch.empty(step.dX.shape, dtype=torch.bfloat16).pin_memory() for _ in range(NSETS)]
     hdW = [torch.empty(step.dW.shape, dtype=torch.bfloat16).pin_memory() for _ in range(NSETS)]
     steps2 = [rstep] + [LinearStep(torch.empty_like(X), torch.empty_like(W), torch.empty_like(dY), seed=7,
-                                   rebias=True) for _ in range(NSETS - 1)]
+                                   rebias=True, rebias_wgrad=True) for _ in range(NSETS - 1)]
     s_h2d, s_cmp, s_d2h = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     e2e_warm = NSETS + 1
     e2e_steps = max(2, args.steps)
@@ -568,7 +602,7 @@ def run_gpu(args, rank, world):
         for name in workloads.LINEARS:
             xb, wb, db = workloads.linear_block(name)
             lin.append(LinearStep(workloads.to_torch_bf16(xb).to(dev), workloads.to_torch_bf16(wb).to(dev),
-                                  workloads.to_torch_bf16(db).to(dev), seed=7, rebias=True))
+                                  workloads.to_torch_bf16(db).to(dev), seed=7, rebias=True, rebias_wgrad=True))
         for _ in range(2):
             for st_l in lin:
                 st_l.run_overlapped(periodic=True)
@@ -585,7 +619,7 @@ def run_gpu(args, rank, world):
         bms = c0.elapsed_time(c1) / nb
         bflops = sum(3 * 2.0 * workloads.TOKENS * fi * fo for fi, fo in workloads.LINEARS.values())
         block = {"ms_per_block_step": bms, "TFLOP/s": bflops / (bms * 1e-3) / 1e12, "steps": nb,
-                 "fallbacks_fprop_dgrad": [st_l.fallbacks() for st_l in lin],
+                 "fallbacks_fprop_dgrad_wgrad": [st_l.fallbacks() for st_l in lin],
                  "linears": ", ".join(f"{k} {fi}->{fo}" for k, (fi, fo) in workloads.LINEARS.items()),
                  "tokens": workloads.TOKENS}
         del lin
@@ -629,7 +663,8 @@ def run_gpu(args, rank, world):
         del lin
 
     return dict(ms=ms, ms_emulated=ms_emulated, ms_current=ms_current, refreshes=refreshes, ms_serial=ms_serial,
-                ms_serial_r=ms_serial_r, t_gr=t_gr, parts=parts, fallbacks=fallbacks, dual=dual,
+                ms_serial_r=ms_serial_r, t_gr=t_gr, parts=parts, wparts=wparts, fallbacks=fallbacks, dual=dual,
+                ms_wgrad_emulated=ms_wgrad_emulated,
                 native=native, fused=fused, block=block, t_scale=t_scale, t_q=(t_qx, t_qw, t_qd), t_g=t_g, launches=launches, rates=rates,
                 clocks=clk.summary(), status=status, e2e_ms=e2e_ms, e2e_steps=e2e_steps, e2e_sets=NSETS,
                 h2d=h2d, d2h=d2h, link=link, affinity=affinity,
@@ -833,13 +868,16 @@ def main():
     value = job_tflops(world, STEP_FLOPS, ms)
     t_gemm = sum(r["t_g"]) / 3
     gemm_tflops = GEMM_FLOPS / (t_gemm * 1e-3) / 1e12
-    # the dominant kernel of the headline step: the emulated GEMM, which runs
-    # its wgrad (the one-stream pass of the headline step's GEMM paths)
-    wgrad_tflops = GEMM_FLOPS / (r["t_gr"][2] * 1e-3) / 1e12
-    pr = r["parts"]
-    native_tflops = GEMM_FLOPS / (pr["native_gemm_ms"] * 1e-3) / 1e12
-    wgrad_with_skips = GEMM_FLOPS / ((r["t_gr"][2] + 2 * pr["skipped_emulated_launch_ms"]) * 1e-3) / 1e12
+    # the dominant kernel of the headline step: the two-window native GEMM of
+    # its wgrad (CUDA events around its launch, one stream); algorithmic
+    # flops are the UE5M3 GEMM's 2MNK (its two MMAs per K step are the cost
+    # of the second window, not work of the method)
+    pr, pw = r["parts"], r["wparts"]
     fp4_peak = bf16 * FP4_OVER_BF16 if bf16 else None
+    two_tflops = GEMM_FLOPS / (pw["native_gemm_ms"] * 1e-3) / 1e12
+    native_tflops = GEMM_FLOPS / (pr["native_gemm_ms"] * 1e-3) / 1e12
+    # the emulated GEMM on the same wgrad (the all-emulated one-stream step)
+    wgrad_tflops = GEMM_FLOPS / (r["t_g"][2] * 1e-3) / 1e12
     nX, nW, nD = r["elems"]
     q_bytes = [n * DUAL_BYTES_PER_ELEM for n in (nX, nW, nD)]
     # the dual-axis quantisers: their own rate (graph replays), and the rate
@@ -863,10 +901,11 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms, "ms_per_step_periodic": ms,
         "ms_per_step_current_scaling": r["ms_current"] / args.steps,
         "ms_per_step_all_gemms_emulated": r["ms_emulated"] / args.steps,
+        "ms_per_step_wgrad_emulated": r["ms_wgrad_emulated"] / args.steps,
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "E2M1/UE5M3 operands; fprop, dgrad: e2m1 x e2m1 block-scaled MMA -> f32 (UE5M3 scales as UE4M3 "
-                 "codes x 2^k, exact); wgrad: f16xf16->f32 (exact FP16 expansion)",
+        "dtype": "E2M1/UE5M3 operands; e2m1 x e2m1 block-scaled MMA -> f32 (UE5M3 scales as UE4M3 codes x 2^k, "
+                 "exact; wgrad's A in two windows, two f32 accumulators)",
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "M": M_TOK, "hidden": HID, "ffn": FFN,
                    "l2": "inputs larger than L2 (dY 256 MiB, step working set ~1 GiB)",
@@ -875,29 +914,37 @@ def main():
                    "tensor_scaling": "periodic: T refreshed every 16 steps from the amax fused into the "
                                      "previous quantisation; amax pass on the first step only "
                                      f"(scaler steps after the timed region: {r['refreshes']})",
-                   "gemm_paths": "fprop, dgrad: scale codes rebiased (A per row, B per tensor) + native "
-                                 "block-scaled MMA, emulated GEMM launched after it and run on the device only "
-                                 "if a group spans > 14 binades; wgrad: emulated (FP16 expansion)",
-                   "fallbacks_fprop_dgrad": r["fallbacks"],
+                   "gemm_paths": "scale codes rebiased (A per row, B per tensor) + native block-scaled MMA, "
+                                 "emulated GEMM launched after it and run on the device only if a group does not "
+                                 "fit: fprop, dgrad one window (14 binades) per A row; wgrad two windows (28 "
+                                 "binades) per A row, two accumulators",
+                   "fallbacks_fprop_dgrad_wgrad": r["fallbacks"],
+                   "wgrad_emulated_TFLOP/s": job_tflops(world, STEP_FLOPS, r["ms_wgrad_emulated"] / args.steps),
                    "current_scaling_TFLOP/s": job_tflops(world, STEP_FLOPS, r["ms_current"] / args.steps),
                    "all_gemms_emulated_TFLOP/s": job_tflops(world, STEP_FLOPS, r["ms_emulated"] / args.steps),
                    "ms_per_step_one_stream_current_scaling": r["ms_serial_r"] / args.steps,
                    "ms_per_step_one_stream_current_scaling_all_emulated": r["ms_serial"] / args.steps,
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": {"bound": "tensor", "achieved": wgrad_tflops, "peak": bf16,
-                     "unit": "TFLOP/s", "frac": wgrad_tflops / bf16 if bf16 else None,
-                     "traffic": committed_traffic("gemm_kernel_traffic_8B_linear.json", GEMM_SOURCES, "wgrad"),
-                     "kernel": "fp4q gemm_kernel (emulated UE5M3 GEMM; its wgrad launch, 16384 x 4096 x 8192)",
-                     "peak_source": f"{src} bf16 ({'burst' if burst else 'sustained'}: the per-kernel "
-                                    f"region ran {r['ms_serial_r']:.0f} ms)",
-                     "with_skipped_launches": {
-                         "achieved": wgrad_with_skips, "frac": wgrad_with_skips / bf16 if bf16 else None,
-                         "note": "the step's wgrad flops over its three launches of this kernel: wgrad and the "
-                                 "two conditional fallbacks of fprop and dgrad, which skipped (no algorithmic work)"},
-                     "all_three_emulated": {"achieved": gemm_tflops, "frac": gemm_tflops / bf16 if bf16 else None,
-                                            "traffic": committed_traffic("gemm_kernel_traffic_8B_linear.json",
-                                                                         GEMM_SOURCES),
-                                            "note": "mean over fprop/dgrad/wgrad of the all-emulated one-stream step"}},
+        "roofline": {"bound": "tensor", "achieved": two_tflops, "peak": fp4_peak,
+                     "unit": "TFLOP/s", "frac": two_tflops / fp4_peak if fp4_peak else None,
+                     "traffic": committed_traffic("gemm_nvfp4_two_windows_traffic_wgrad.json", NATIVE_SOURCES),
+                     "kernel": "fp4q gemm_nvfp4_kernel, two windows (the step's wgrad, 16384 x 4096 x 8192)",
+                     "peak_source": f"{src} bf16 x {FP4_OVER_BF16:g} (nominal dense fp4 / bf16; "
+                                    f"{'burst' if burst else 'sustained'}: the per-kernel region ran "
+                                    f"{r['ms_serial_r']:.0f} ms)",
+                     "mma_work": {"achieved": 2 * two_tflops, "frac": 2 * two_tflops / fp4_peak if fp4_peak else None,
+                                  "note": "the same launch counting both MMAs of each K step (high and low "
+                                          "window): the tensor cores' own throughput"},
+                     "parts_ms": pw},
+        "roofline_emulated_wgrad": {
+            "bound": "tensor", "achieved": wgrad_tflops, "peak": bf16, "unit": "TFLOP/s",
+            "frac": wgrad_tflops / bf16 if bf16 else None,
+            "traffic": committed_traffic("gemm_kernel_traffic_8B_linear.json", GEMM_SOURCES, "wgrad"),
+            "kernel": "fp4q gemm_kernel (emulated UE5M3 GEMM; the same wgrad, all-emulated step)",
+            "peak_source": f"{src} bf16 ({'burst' if burst else 'sustained'})",
+            "all_three_emulated": {"achieved": gemm_tflops, "frac": gemm_tflops / bf16 if bf16 else None,
+                                   "traffic": committed_traffic("gemm_kernel_traffic_8B_linear.json", GEMM_SOURCES),
+                                   "note": "mean over fprop/dgrad/wgrad of the all-emulated one-stream step"}},
         "roofline_native_rebiased": {"bound": "tensor", "achieved": native_tflops, "peak": fp4_peak,
                                      "unit": "TFLOP/s", "frac": native_tflops / fp4_peak if fp4_peak else None,
                                      "kernel": "fp4q gemm_nvfp4_kernel on rebiased UE5M3 operands (fprop)",

@@ -11,13 +11,19 @@ Small cases of this command are what the committed ncu summaries capture.
   cases: amax, row_rne, row_sr, dual_rne, dual_sr, 2d_rne, 2d_sr, dequant, gemm and gemm_nvfp4
   (--m --n --k; gemm_nvfp4 on UE4M3-scaled operands), gemm_rebias (the UE5M3
   GEMM through rebiased codes: two rebias launches, the native GEMM, the
-  conditional emulated one), and step: the whole linear fwd+bwd step of the
+  conditional emulated one), gemm_two_windows (the same for wgrad's shape of
+  operands -- A a gradient column-wise with SR, B activations column-wise, K
+  the tokens -- with A's codes in two windows: two rebias launches, the
+  two-accumulator native GEMM, the conditional emulated one), and step: the
+  whole linear fwd+bwd step of the
   bench (X [m, k], W [n, k], dY [m, n]) under periodic tensor scaling on
   three streams, one "launch" per step (its first step launches 12 kernels --
   amax and tensor scale of X, W, dY, three quantisations, three GEMMs -- every
   later one 6, plus a tensor scale per tensor every 16 steps); step_rebias:
   the same step with fprop and dgrad through rebiased codes (6 more launches
-  per step: two rebias kernels and a conditional emulated GEMM each).
+  per step: two rebias kernels and a conditional emulated GEMM each);
+  step_rebias_wgrad: that step with wgrad through two-window codes as well
+  (3 more launches per step).
 """
 from __future__ import annotations
 
@@ -29,7 +35,7 @@ import torch
 from . import build, fp4q, workloads
 
 CASES = ("amax", "row_rne", "row_sr", "dual_rne", "dual_sr", "2d_rne", "2d_sr", "dequant", "gemm", "gemm_nvfp4",
-         "gemm_rebias", "step", "step_rebias")
+         "gemm_rebias", "gemm_two_windows", "step", "step_rebias", "step_rebias_wgrad")
 
 
 def _inputs(case, rows, cols, dev):
@@ -41,15 +47,33 @@ def run(case, rows=16384, cols=4096, m=8192, n=16384, k=4096, reps=10, warmup=3)
     build.build()
     dev = torch.device("cuda")
     u8 = dict(dtype=torch.uint8, device=dev)
-    if case in ("step", "step_rebias"):
+    if case.startswith("step"):
         from .linear_step import LinearStep
 
         X = workloads.to_torch_bf16(workloads.activations(m, k, 1)).to(dev)
         W = workloads.to_torch_bf16(workloads.weights(n, k, 2)).to(dev)
         dY = workloads.to_torch_bf16(workloads.gradients(m, n, 3)).to(dev)
-        st = LinearStep(X, W, dY, seed=7, rebias=case == "step_rebias")
+        st = LinearStep(X, W, dY, seed=7, rebias=case != "step", rebias_wgrad=case == "step_rebias_wgrad")
         launch = lambda j: st.run_overlapped(periodic=True)
         work, unit = 3 * 2.0 * m * n * k, "TFLOP/s"
+    elif case == "gemm_two_windows":
+        qa = fp4q.quantize(workloads.to_torch_bf16(workloads.gradients(k, m, 62)).to(dev), fp4q.AXIS_COL, None,
+                           fp4q.UE5M3, fp4q.SR, 7)
+        qb = fp4q.quantize(workloads.to_torch_bf16(workloads.activations(k, n, 63)).to(dev), fp4q.AXIS_COL)
+        A = (qa.payload_col, qa.scales_col, qa.T)
+        B = (qb.payload_col, qb.scales_col, qb.T)
+        out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        ah, al, b4 = torch.empty_like(A[1]), torch.empty_like(A[1]), torch.empty_like(B[1])
+        fh, fl = (torch.empty(m, dtype=torch.float32, device=dev) for _ in range(2))
+        fb = torch.empty(1, dtype=torch.float32, device=dev)
+        flag = torch.zeros(1, dtype=torch.int32, device=dev)
+
+        def launch(j):
+            fp4q.fp4q_rebias_scales_two_windows(A[1], m, k // 16, ah, al, fh, fl, flag)
+            fp4q.fp4q_rebias_scales(B[1], n, k // 16, False, b4, fb, flag)
+            fp4q.fp4q_gemm_nvfp4_two_windows(A[0], ah, al, fh, A[2], B[0], b4, fb, B[2], m, n, k, flag, out)
+            fp4q.fp4q_gemm_if(*A, *B, m, n, k, fp4q.UE5M3, flag, out)
+        work, unit = 2.0 * m * n * k, "TFLOP/s"
     elif case in ("gemm", "gemm_nvfp4", "gemm_rebias"):
         fmt = fp4q.UE4M3 if case == "gemm_nvfp4" else fp4q.UE5M3
         xs = [fp4q.quantize(workloads.to_torch_bf16(workloads.activations(m, k, 60)).to(dev), fmt=fmt),
@@ -112,9 +136,10 @@ def run(case, rows=16384, cols=4096, m=8192, n=16384, k=4096, reps=10, warmup=3)
     ms = e0.elapsed_time(e1) / reps
     rate = work / (ms * 1e-3) / (1e12 if unit == "TFLOP/s" else 1e9)
     status = fp4q.fp4q_get_device_status()
+    extra = {"fallback": int(flag.item())} if case == "gemm_two_windows" else {}
     shape = {"m": m, "n": n, "k": k} if case.startswith(("gemm", "step")) else {"rows": rows, "cols": cols}
     return {"case": case, **shape, "reps": reps, "ms_per_launch": ms, "rate": rate, "unit": unit,
-            "device_status": status}
+            "device_status": status, **extra}
 
 
 def main():

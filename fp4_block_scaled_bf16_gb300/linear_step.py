@@ -31,8 +31,11 @@ group spanned more than the 14 binades UE4M3 holds -- decided on the device,
 no host read.  wgrad stays emulated by default: its A operand is dY
 column-wise, each row running over the batch's tokens, whose gradient
 magnitudes can differ by many more binades than that (in the bench's inputs
-they span ten decades); `rebias_wgrad=True` sends it the same way, with the
-same exact fallback.
+they span ten decades).  `rebias_wgrad=True` sends it to the block-scaled MMA
+as well, with A's codes in two 14-binade windows per row
+(fp4q_rebias_scales_two_windows: 28 binades under each row's largest scale)
+multiplied into two accumulators (fp4q_gemm_nvfp4_two_windows), and the same
+exact fallback when a code lies below both windows.
 
 Every launch goes through libfp4q.so; buffers are allocated once here with
 torch and reused by every step.
@@ -82,17 +85,21 @@ class LinearStep:
         self.dW = torch.empty((out, hid), **bf)
         # fprop (A = X rows, B = W rows), dgrad (A = dY rows, B = W columns)
         # and, optionally, wgrad (A = dY columns, B = X columns) on the
-        # native MMA: rebiased codes, factors and a fallback flag each; a GEMM
-        # whose K is not a multiple of 256 stays emulated
+        # native MMA: rebiased codes, factors and a fallback flag each (wgrad:
+        # A's codes and factors in two windows); a GEMM whose K is not a
+        # multiple of 256 stays emulated
         ngemms = 3 if rebias_wgrad else 2
         self.rb = [None] * 3
         self.nofit = torch.zeros(ngemms, dtype=torch.int32, device=dev)
         if rebias:
             shapes = ((tokens, out, hid), (tokens, hid, out), (out, hid, tokens))[:ngemms]
             for g, (m, n, k) in enumerate(shapes):
-                if k % 256 == 0:
-                    self.rb[g] = (torch.empty((m, k // 16), **u8), torch.empty(m, **f32),
-                                  torch.empty((n, k // 16), **u8), torch.empty(1, **f32), self.nofit[g:g + 1])
+                if k % 256:
+                    continue
+                a = (torch.empty((m, k // 16), **u8), torch.empty(m, **f32))
+                if g == 2:
+                    a = (a[0], torch.empty((m, k // 16), **u8), a[1], torch.empty(m, **f32))
+                self.rb[g] = a + (torch.empty((n, k // 16), **u8), torch.empty(1, **f32), self.nofit[g:g + 1])
         self.scalers = [PeriodicScaler(period, fmt, device=dev, lib=q) for _ in range(3)]
         self.launches = 0
         # run_overlapped's streams, by priority: X, W and fprop highest, dY
@@ -136,25 +143,35 @@ class LinearStep:
             self.scalers[i].advance()
 
     def _gemm(self, A, B, M, N, K, out, rb=None, g=None):
-        """One GEMM on the current stream.  Through rebiased codes (rb), the
-        emulated fallback goes on the low-priority stream when g (0 fprop,
-        1 dgrad) is given -- after the rebias launches, joined back before
-        anything later on the current stream -- else in line."""
+        """One GEMM on the current stream.  Through rebiased codes (rb: one
+        window per A row, or two), the emulated fallback goes on the
+        low-priority stream when g (0 fprop, 1 dgrad) is given -- after the
+        rebias launches, joined back before anything later on the current
+        stream -- else in line."""
         q = self.q
         if self.native:
             q.fp4q_gemm_nvfp4(*A, *B, M, N, K, out)
         elif rb is not None:
-            a4, fa, b4, fb, flag = rb
+            b4, fb, flag = rb[-3:]
             flag.zero_()
-            q.fp4q_rebias_scales(A[1], M, K // 16, True, a4, fa, flag)
+            if len(rb) == 7:   # A's codes in two windows
+                ah, al, fh, fl = rb[:4]
+                q.fp4q_rebias_scales_two_windows(A[1], M, K // 16, ah, al, fh, fl, flag)
+                native = lambda: q.fp4q_gemm_nvfp4_two_windows(A[0], ah, al, fh, A[2], B[0], b4, fb, B[2], M, N,
+                                                               K, flag, out)
+            else:
+                a4, fa = rb[:2]
+                q.fp4q_rebias_scales(A[1], M, K // 16, True, a4, fa, flag)
+                native = lambda: q.fp4q_gemm_nvfp4_rebiased(A[0], a4, fa, A[2], B[0], b4, fb, B[2], M, N, K, flag,
+                                                            out)
             q.fp4q_rebias_scales(B[1], N, K // 16, False, b4, fb, flag)
             if g is None:
-                q.fp4q_gemm_nvfp4_rebiased(A[0], a4, fa, A[2], B[0], b4, fb, B[2], M, N, K, flag, out)
+                native()
                 q.fp4q_gemm_if(*A, *B, M, N, K, self.fmt, flag, out)
             else:
                 cur = torch.cuda.current_stream()
                 self.ev_rb[g].record(cur)
-                q.fp4q_gemm_nvfp4_rebiased(A[0], a4, fa, A[2], B[0], b4, fb, B[2], M, N, K, flag, out)
+                native()
                 self.fallback.wait_event(self.ev_rb[g])
                 with torch.cuda.stream(self.fallback):
                     q.fp4q_gemm_if(*A, *B, M, N, K, self.fmt, flag, out)

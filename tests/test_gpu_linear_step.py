@@ -284,13 +284,13 @@ def test_two_steps_on_two_caller_streams():
 
 
 def test_wgrad_through_the_native_path_when_it_fits():
-    """rebias_wgrad: with gradients whose per-token magnitudes stay within a
-    decade, dY's column-wise codes fit their rows' windows and wgrad runs on
-    the native MMA (flag clear, dW within the BF16 bound of the oracle's
-    UE5M3 contraction); with one block of 16 tokens 2^-30 smaller, every row
-    of wgrad's A operand spans more than 14 binades, wgrad falls back and dW
-    equals the all-emulated step's bit for bit (the bench's ten-decade
-    gradients do the same at 8192 tokens: spans up to 20 binades)."""
+    """rebias_wgrad: wgrad's A operand (dY column-wise) in two windows per
+    row.  Gradients whose per-token magnitudes stay within a decade fit; with
+    one block of 16 tokens 2^-20 smaller every row needs the low window and
+    still fits (the bench's ten-decade gradients span up to 20 binades per row
+    at 8192 tokens) -- dW within the BF16 bound of the oracle's UE5M3
+    contraction, flag clear; 2^-30 smaller lies below both windows, wgrad falls
+    back and dW equals the all-emulated step's bit for bit."""
     from fp4_block_scaled_bf16_gb300 import build
     build.build()
     from fp4_block_scaled_bf16_gb300 import fp4q
@@ -299,10 +299,10 @@ def test_wgrad_through_the_native_path_when_it_fits():
     dev = torch.device("cuda")
     X = workloads.to_torch_bf16(workloads.activations(TOK, HID, 81)).to(dev)
     W = workloads.to_torch_bf16(workloads.weights(OUT, HID, 82)).to(dev)
-    for tiny, want in ((False, False), (True, True)):
+    for tiny, want_one, want_fall in ((None, True, False), (-20, False, False), (-30, False, True)):
         g = workloads.bf16_bits_to_f32(workloads.gradients(TOK, OUT, 83, -1.0, 0.0))
-        if tiny:
-            g[32:48] *= np.float32(2.0 ** -30)
+        if tiny is not None:
+            g[32:48] *= np.float32(2.0 ** tiny)
         dY = workloads.to_torch_bf16(workloads.f32_to_bf16_bits(g)).to(dev)
         fast = LinearStep(X, W, dY, seed=7, rebias=True, rebias_wgrad=True)
         ref = LinearStep(X, W, dY, seed=7)
@@ -310,10 +310,13 @@ def test_wgrad_through_the_native_path_when_it_fits():
         ref.run_overlapped()
         torch.cuda.synchronize()
         fell = fast.fallbacks()
-        fits = (oracle.rebias_scales(_u8(fast.Dcs), True)[2] and oracle.rebias_scales(_u8(fast.Xcs), False)[2])
-        assert fell[2] == (not fits) == want, (tiny, fell)
+        dcs = _u8(fast.Dcs)
+        assert oracle.rebias_scales(dcs, True)[2] == want_one
+        assert dcs[:, 2].all()                                   # the small block's codes are not zero
+        fits = oracle.rebias_scales2(dcs)[4] and oracle.rebias_scales(_u8(fast.Xcs), False)[2]
+        assert fell[2] == (not fits) == want_fall, (tiny, fell)
         assert fell[:2] == [False, False]
-        if want:
+        if want_fall:
             assert torch.equal(fast.dW, ref.dW)
         else:
             TD, TX = float(fast.T[2].item()), float(fast.T[0].item())
