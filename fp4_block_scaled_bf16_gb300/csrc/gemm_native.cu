@@ -87,9 +87,10 @@ constexpr uint32_t kSfCol0 = 256;                // scale ring from column 256; 
 // high and a low window): 256 x 128 tiles, two 128-column accumulators (high
 // in columns 0..127, low in 128..255), both fed by each K64 step from the same
 // operand tiles, seven 30 KB stages (the low-window A codes added); a K64 step
-// takes 32 scale columns (the high MMA's group -- B's words in 4, A's
-// high-window words from column 8 -- and the low MMA's the same way), so the
-// ring holds two entries of one stage each.  (Entries of half a stage, each
+// takes two 16-column scale groups (the high MMA's -- B's words in 4, A's
+// high-window words from column 8 -- among the entry's first 64 columns, the
+// low MMA's the same way 64 columns on), so the ring holds two entries of one
+// stage each.  (Entries of half a stage, each
 // released as soon as its own MMAs completed, so that three entries' MMAs
 // rather than one stage's cover the next copy into TMEM, ran 23 % slower:
 // the extra barrier wait and commits sit on the one thread that issues the
@@ -101,8 +102,8 @@ struct Geo {
   static constexpr int S = TWO ? 7 : 5;          // shared-memory ring stages
   static constexpr int ESTEPS = 4;               // K64 steps per scale-ring entry (a stage)
   static constexpr int EPS = MMAS / ESTEPS;      // entries per stage
-  static constexpr uint32_t kStepCols = TWO ? 32 : 16;            // scale columns per K64 step
-  static constexpr uint32_t kEntryCols = ESTEPS * kStepCols;      // 64
+  static constexpr uint32_t kStepCols = 16;                       // a K64 step's scale group
+  static constexpr uint32_t kEntryCols = (TWO ? 2 : 1) * ESTEPS * kStepCols;   // 64, TWO: 128
   static constexpr int NENT = (int)((kTmemCols - kSfCol0) / kEntryCols);   // ring entries (4, TWO: 2)
   static constexpr bool kEntryIsStage = EPS == 1;  // released with the stage (bar_empty)
   static constexpr int B_BYTES = BH * ROWB;      // this CTA's half of B
@@ -112,7 +113,7 @@ struct Geo {
   static constexpr int OFF_SB = OFF_SA2 + (TWO ? SA_BYTES : 0);
   static constexpr int STAGE = OFF_SB + SB_BYTES;     // 38912 or 30720
   static constexpr uint32_t kLoCol = 128;             // the low accumulator (TWO)
-  static constexpr uint32_t kLoSf = 16;               // the low MMA's scale group, from its step's (TWO)
+  static constexpr uint32_t kLoSf = ESTEPS * kStepCols;   // the low MMAs' scale groups, after the high ones (TWO)
   // full, empty per stage; sf (rank 0) and sfree per entry; acc full / empty, done
   static constexpr int NBARS = 2 * S + 2 * NENT + 3;
   static constexpr int OFF_BAR = S * STAGE;
@@ -501,11 +502,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool live = row < M && cbase < N;
       const float alpha = (fa && row < M) ? __fmul_rn(alpha0, __ldg(fa + row)) : alpha0;
       const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)((PN / 2) * h);
-      if (TWO) {
+      if (TWO && !F32OUT) {
         // 32 columns of each accumulator at a time: C = alpha (high + 2^-14
         // low) -- the low window's factor is the high one's times 2^-14, an
-        // exact scaling, so the sum is rounded once, then alpha as below;
-        // TMEM released once the second chunk is in registers
+        // exact scaling, so the sum is rounded once, then alpha as below.
+        // The first chunk is packed to BF16 before the second is loaded, TMEM
+        // released, and only then are both stored: the next tile's MMAs wait
+        // for the loads alone.
+        uint32_t h0[16], h1[16];
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t r[64];
@@ -520,13 +524,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj)
             r[jj] = __float_as_uint(__fmaf_rn(__uint_as_float(r[32 + jj]), 0x1p-14f, __uint_as_float(r[jj])));
-          if (F32OUT) {
-            if (live) store_f32x32(out, row, cbase + 32 * c, N, r, 0, alpha);
-          } else {
-            uint32_t hh[16];
-            pack_bf16x32(r, 0, alpha, hh);
-            if (live) store_bf16x32(out, row, cbase + 32 * c, N, hh);
+          if (c == 0)
+            pack_bf16x32(r, 0, alpha, h0);
+          else
+            pack_bf16x32(r, 0, alpha, h1);
+        }
+        if (live) {
+          store_bf16x32(out, row, cbase, N, h0);
+          store_bf16x32(out, row, cbase + 32, N, h1);
+        }
+      } else if (TWO) {
+        // the same with a binary32 result, stored chunk by chunk
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t r[64];
+          tmem_ld32_nowait(taddr + 32 * c, r);
+          tmem_ld32_nowait(taddr + kLoCol + 32 * c, r + 32);
+          tmem_ld_wait(r, 64);
+          if (c == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_rank0(bar_acc_empty);
           }
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj)
+            r[jj] = __float_as_uint(__fmaf_rn(__uint_as_float(r[32 + jj]), 0x1p-14f, __uint_as_float(r[jj])));
+          if (live) store_f32x32(out, row, cbase + 32 * c, N, r, 0, alpha);
         }
       } else if (F32OUT) {
         // 64 columns at a time; TMEM released (the next tile's MMAs may
@@ -545,12 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (live) store_f32x32(out, row, cbase + 64 * half, N, r, 0, alpha);
           if (live) store_f32x32(out, row, cbase + 64 * half + 32, N, r, 32, alpha);
         }
-      } else {
-        // 64 columns at a time: loaded, packed to BF16, stored (and, with
-        // QOUT, quantised); TMEM released once the second load is complete.
-        // (With QOUT, holding all 128 packed columns until the release, so
-        // that the first 64's work follows it, needs more than the 128
-        // registers a thread has here.)
+      } else if (!QOUT) {
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t r[64];
@@ -566,11 +584,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 2; ++c) {
             uint32_t hh[16];
             pack_bf16x32(r, 32 * c, alpha, hh);
-            if (QOUT) {
-              if (live) store_quantize_chunk(hh, out, *tab, kr, row, cbase + 64 * half + 32 * c, N, qpay, qsc, qmax);
-            } else if (live) {
-              store_bf16x32(out, row, cbase + 64 * half + 32 * c, N, hh);
-            }
+            if (live) store_bf16x32(out, row, cbase + 64 * half + 32 * c, N, hh);
+          }
+        }
+      } else {
+        // 64 columns at a time: loaded, packed to BF16, stored and
+        // quantised; TMEM released once the second load is complete.
+        // (Holding all 128 packed columns until the release, so that the
+        // first 64's work follows it, needs more than the 128 registers a
+        // thread has here.)
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t r[64];
+          tmem_ld32_nowait(taddr + 64 * half, r);
+          tmem_ld32_nowait(taddr + 64 * half + 32, r + 32);
+          tmem_ld_wait(r, 64);
+          if (half == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_rank0(bar_acc_empty);
+          }
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t hh[16];
+            pack_bf16x32(r, 32 * c, alpha, hh);
+            if (live) store_quantize_chunk(hh, out, *tab, kr, row, cbase + 64 * half + 32 * c, N, qpay, qsc, qmax);
           }
         }
       }
