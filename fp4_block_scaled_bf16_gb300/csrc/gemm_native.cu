@@ -120,7 +120,12 @@ struct Geo {
   static constexpr int OFF_TMEM = OFF_BAR + 8 * NBARS;
   static constexpr int OFF_ABORT = OFF_TMEM + 8;
   static constexpr int OFF_TAB = OFF_ABORT + 8;  // the epilogue quantisation's scale table
-  static constexpr int SMEM_BYTES = OFF_TAB + (int)sizeof(ScaleTab) + 1024;   // + 1 KB alignment slack
+  // one-window BF16 result through TMA stores: a 32-row x 64-column box per
+  // epilogue warp (4 KB, 128-byte swizzle, 1 KB aligned)
+  static constexpr int OUT_BOX = 32 * 128;
+  static constexpr int OFF_OUT = (OFF_TAB + (int)sizeof(ScaleTab) + 1023) / 1024 * 1024;
+  static constexpr int OUT_BYTES = TWO ? 0 : kEpiWarps * OUT_BOX;
+  static constexpr int SMEM_BYTES = OFF_OUT + OUT_BYTES + 1024;   // + 1 KB alignment slack
   // Instruction descriptor of kind::mxf4nvf4: A and B E2M1 (format 1), both
   // K-major, UE4M3 scales (bit 23 clear), scale-factor data IDs 0,
   // N (bits 17..22: N / 8), M = 256 for the pair (bits 24..28: M / 16); dense.
@@ -156,6 +161,14 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
       : "memory");
 }
 
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+// bulk-group bookkeeping of this thread's TMA stores
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
@@ -171,7 +184,9 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
 // col0; columns at or past N are not written).  A lane's row segment is
 // written with 256-bit stores when its address is 32-byte aligned (whole L2
 // sectors: 7 % on fprop's 268 MB result against 128-bit stores, which write
-// each sector in two halves), else with 128-bit or scalar stores.
+// each sector in two halves), else with 128-bit or scalar stores.  (The
+// one-window BF16 result goes through TMA stores instead when a tensor map
+// describes it: another 9 % on fprop.)
 __device__ __forceinline__ bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 __device__ __forceinline__ void st_global_v8(void* p, const uint32_t* w) {
   asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
@@ -266,7 +281,8 @@ template <bool F32OUT, bool QOUT, bool TWO>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                       const __grid_constant__ CUtensorMap mapSA, const __grid_constant__ CUtensorMap mapSB,
-                      const __grid_constant__ CUtensorMap mapSA2,
+                      const __grid_constant__ CUtensorMap mapSA2, const __grid_constant__ CUtensorMap mapC,
+                      int tma_out,
                       const float* __restrict__ TA, const float* __restrict__ TB, int M, int N, int K,
                       void* __restrict__ out, int* status, long long budget, int skip_loads,
                       const float* __restrict__ fa, const float* __restrict__ fb, const int* skip_if,
@@ -588,6 +604,45 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (live) store_f32x32(out, row, cbase + 64 * half, N, r, 0, alpha);
           if (live) store_f32x32(out, row, cbase + 64 * half + 32, N, r, 32, alpha);
         }
+      } else if (!QOUT && tma_out) {
+        // BF16 through TMA stores: each 64-column half is packed into the
+        // warp's staging box (row = lane, 16-byte chunk c at c ^ (lane % 8):
+        // the 128-byte swizzle of the output map, no bank conflicts) once the
+        // box's previous store has read it, and lane 0 stores the 32 x 64 box;
+        // TMEM is released once the second half is loaded.  Boxes starting
+        // outside the result are skipped; the store clips a ragged edge.
+        const uint32_t stg = sb + G::OFF_OUT + (uint32_t)(warp - kEpiWarp0) * G::OUT_BOX;
+        const int y0 = am0 + 32 * q;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t r[64];
+          tmem_ld32_nowait(taddr + 64 * half, r);
+          tmem_ld32_nowait(taddr + 64 * half + 32, r + 32);
+          tmem_ld_wait(r, 64);
+          if (half == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_rank0(bar_acc_empty);
+          }
+          if (lane == 0) bulk_wait_read0();
+          __syncwarp();
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t hh[16];
+            pack_bf16x32(r, 32 * c, alpha, hh);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              sts128(stg + (uint32_t)lane * 128 + ((uint32_t)((4 * c + i) ^ (lane & 7)) << 4), hh[4 * i],
+                     hh[4 * i + 1], hh[4 * i + 2], hh[4 * i + 3]);
+          }
+          fence_proxy_async();
+          __syncwarp();
+          const int x0 = cbase + 64 * half;
+          if (lane == 0 && x0 < N && y0 < M) {
+            tma_store_2d(&mapC, stg, x0, y0);
+            bulk_commit();
+          }
+        }
       } else if (!QOUT) {
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -633,6 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    if (!QOUT && !TWO && tma_out && lane == 0) bulk_wait0();   // this warp's TMA stores complete
     if (QOUT) {
       // max |bf16(C)| (a 16-bit pattern; inf/NaN compare above every finite)
       qmax = __reduce_max_sync(0xFFFFFFFFu, qmax);
@@ -686,6 +742,20 @@ static bool make_scale_map(CUtensorMap* map, const uint8_t* base, int64_t rows, 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D BF16 tensor map over the [M, N] result, box (64 columns, 32 rows),
+// 128-byte swizzle; needs a row stride that is a multiple of 16 bytes.
+static bool make_out_map(CUtensorMap* map, void* base, int64_t M, int64_t N) {
+  auto fn = get_encode_fn();
+  if (!fn || N % 8 != 0 || (reinterpret_cast<uintptr_t>(base) & 15u) != 0) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+  const cuuint64_t strides[1] = {(cuuint64_t)(N * 2)};
+  const cuuint32_t box[2] = {64u, 32u};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <bool F32OUT, bool QOUT, bool TWO>
 static cudaError_t launch_native_t(const GemmArgs& a, const CUtensorMap& mA, const CUtensorMap& mB,
                                    const CUtensorMap& mSA, const CUtensorMap& mSB, const CUtensorMap& mSA2,
@@ -723,7 +793,11 @@ static cudaError_t launch_native_t(const GemmArgs& a, const CUtensorMap& mA, con
   const int64_t ntiles = ((a.N + G::PN - 1) / G::PN) * ((a.M + native::PM - 1) / native::PM);
   const int ncl = (int)(ntiles < clusters[dev] ? ntiles : clusters[dev]);
   cfg.gridDim = dim3(2u * (unsigned)ncl);
-  e = cudaLaunchKernelEx(&cfg, kern, mA, mB, mSA, mSB, mSA2, a.TA, a.TB, (int)a.M, (int)a.N, (int)a.K, a.out, a.status,
+  // the one-window BF16 result through TMA stores when a map describes it
+  CUtensorMap mC;
+  const bool tma_out = !F32OUT && !QOUT && !TWO && a.out != nullptr && make_out_map(&mC, a.out, a.M, a.N);
+  if (!tma_out) memset(&mC, 0, sizeof(mC));
+  e = cudaLaunchKernelEx(&cfg, kern, mA, mB, mSA, mSB, mSA2, mC, tma_out ? 1 : 0, a.TA, a.TB, (int)a.M, (int)a.N, (int)a.K, a.out, a.status,
                          a.wait_cycles, a.skip_loads ? 1 : 0, a.fa, a.fb, a.skip_if, a.TC, a.qpay, a.qsc, a.qamax,
                          a.fmt_out);
   if (e != cudaSuccess) return e;
