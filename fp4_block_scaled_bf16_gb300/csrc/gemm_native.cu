@@ -41,7 +41,10 @@
 //               commits them to both CTAs' "empty" barriers; a tile's first
 //               MMA waits until both CTAs' epilogues have read the last one.
 //   warps 4..11 epilogue: TMEM -> registers (64 columns per lane at a time)
-//               -> alpha -> BF16 or FP32 -> global.
+//               -> alpha -> BF16 or FP32 -> global: a BF16 result through a
+//               4 KB staging box per warp and TMA stores when a tensor map
+//               describes it, else 256-bit stores of each lane's row
+//               segment where 32-byte aligned (both write whole L2 sectors).
 // Rebiased mode (fp4q_gemm_nvfp4_rebiased): UE5M3 block scales re-expressed
 // as UE4M3 codes times a power of two, per A row (fa) and for all of B (fb);
 // the epilogue multiplies each row by T_A T_B fb fa[row], exact products of
@@ -51,6 +54,11 @@
 // layer (RNE, blocks of 16 along N, tensor scale TC, the quantisers' own
 // block-scale and conversion code): two blocks per 32-column chunk, payload
 // and codes stored from registers, and max |bf16(C)| into qamax.
+// Two-window mode (fp4q_gemm_nvfp4_two_windows, the TWO shape): A's UE5M3
+// codes split per row into a high and a low 14-binade window of UE4M3 codes;
+// 256 x 128 tiles whose two 128-column accumulators take the high- and the
+// low-window MMA of each K64 step on the same operand tiles, and the
+// epilogue forms alpha (high + 2^-14 low).  Geometry of both shapes: Geo.
 // Every wait is bounded; a wait that runs out latches FP4Q_ERR_TIMEOUT and
 // the CTA winds down once the loads and MMAs it issued have completed; both
 // CTAs meet at a cluster barrier before the pair's TMEM is freed.
@@ -663,11 +671,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        // 64 columns at a time: loaded, packed to BF16, stored and
-        // quantised; TMEM released once the second load is complete.
-        // (Holding all 128 packed columns until the release, so that the
-        // first 64's work follows it, needs more than the 128 registers a
-        // thread has here.)
+        // 64 columns at a time: loaded, packed to BF16 and quantised (the
+        // payload and codes stored from registers); the BF16 result through
+        // the warp's staging box and a TMA store as above when tma_out, else
+        // stored with its chunk; TMEM released once the second load is
+        // complete.  (Holding all 128 packed columns until the release, so
+        // that the first 64's work follows it, needs more than the 128
+        // registers a thread has here.)
+        const uint32_t stg = sb + G::OFF_OUT + (uint32_t)(warp - kEpiWarp0) * G::OUT_BOX;
+        const int y0 = am0 + 32 * q;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t r[64];
@@ -679,16 +691,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive_rank0(bar_acc_empty);
           }
+          if (tma_out) {
+            if (lane == 0) bulk_wait_read0();
+            __syncwarp();
+          }
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             uint32_t hh[16];
             pack_bf16x32(r, 32 * c, alpha, hh);
-            if (live) store_quantize_chunk(hh, out, *tab, kr, row, cbase + 64 * half + 32 * c, N, qpay, qsc, qmax);
+            if (tma_out) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                sts128(stg + (uint32_t)lane * 128 + ((uint32_t)((4 * c + i) ^ (lane & 7)) << 4), hh[4 * i],
+                       hh[4 * i + 1], hh[4 * i + 2], hh[4 * i + 3]);
+            }
+            if (live)
+              store_quantize_chunk(hh, tma_out ? nullptr : out, *tab, kr, row, cbase + 64 * half + 32 * c, N, qpay,
+                                   qsc, qmax);
+          }
+          if (tma_out) {
+            fence_proxy_async();
+            __syncwarp();
+            const int x0 = cbase + 64 * half;
+            if (lane == 0 && x0 < N && y0 < M) {
+              tma_store_2d(&mapC, stg, x0, y0);
+              bulk_commit();
+            }
           }
         }
       }
     }
-    if (!QOUT && !TWO && tma_out && lane == 0) bulk_wait0();   // this warp's TMA stores complete
+    if (!TWO && tma_out && lane == 0) bulk_wait0();   // this warp's TMA stores complete
     if (QOUT) {
       // max |bf16(C)| (a 16-bit pattern; inf/NaN compare above every finite)
       qmax = __reduce_max_sync(0xFFFFFFFFu, qmax);
@@ -795,7 +828,7 @@ static cudaError_t launch_native_t(const GemmArgs& a, const CUtensorMap& mA, con
   cfg.gridDim = dim3(2u * (unsigned)ncl);
   // the one-window BF16 result through TMA stores when a map describes it
   CUtensorMap mC;
-  const bool tma_out = !F32OUT && !QOUT && !TWO && a.out != nullptr && make_out_map(&mC, a.out, a.M, a.N);
+  const bool tma_out = !F32OUT && !TWO && a.out != nullptr && make_out_map(&mC, a.out, a.M, a.N);
   if (!tma_out) memset(&mC, 0, sizeof(mC));
   e = cudaLaunchKernelEx(&cfg, kern, mA, mB, mSA, mSB, mSA2, mC, tma_out ? 1 : 0, a.TA, a.TB, (int)a.M, (int)a.N, (int)a.K, a.out, a.status,
                          a.wait_cycles, a.skip_loads ? 1 : 0, a.fa, a.fb, a.skip_if, a.TC, a.qpay, a.qsc, a.qamax,
