@@ -94,7 +94,8 @@ constexpr uint32_t kSfCol0 = 256;                // scale ring from column 256; 
 // 8, A's in 4 from column 8).  Two windows (TWO = true, A's codes split in a
 // high and a low window): 256 x 128 tiles, two 128-column accumulators (high
 // in columns 0..127, low in 128..255), both fed by each K64 step from the same
-// operand tiles, seven 30 KB stages (the low-window A codes added); a K64 step
+// operand tiles, six 30 KB stages (the low-window A codes added; six rather
+// than seven leave room for the result's staging boxes: 1 % faster); a K64 step
 // takes two 16-column scale groups (the high MMA's -- B's words in 4, A's
 // high-window words from column 8 -- among the entry's first 64 columns, the
 // low MMA's the same way 64 columns on), so the ring holds two entries of one
@@ -107,7 +108,7 @@ template <bool TWO>
 struct Geo {
   static constexpr int PN = TWO ? 128 : 256;     // output columns of a pair's tile = N of the MMA
   static constexpr int BH = PN / 2;              // B rows per CTA
-  static constexpr int S = TWO ? 7 : 5;          // shared-memory ring stages
+  static constexpr int S = TWO ? 6 : 5;          // shared-memory ring stages
   static constexpr int ESTEPS = 4;               // K64 steps per scale-ring entry (a stage)
   static constexpr int EPS = MMAS / ESTEPS;      // entries per stage
   static constexpr uint32_t kStepCols = 16;                       // a K64 step's scale group
@@ -128,11 +129,11 @@ struct Geo {
   static constexpr int OFF_TMEM = OFF_BAR + 8 * NBARS;
   static constexpr int OFF_ABORT = OFF_TMEM + 8;
   static constexpr int OFF_TAB = OFF_ABORT + 8;  // the epilogue quantisation's scale table
-  // one-window BF16 result through TMA stores: a 32-row x 64-column box per
-  // epilogue warp (4 KB, 128-byte swizzle, 1 KB aligned)
+  // BF16 result through TMA stores: a 32-row x 64-column box per epilogue
+  // warp (4 KB, 128-byte swizzle, 1 KB aligned)
   static constexpr int OUT_BOX = 32 * 128;
   static constexpr int OFF_OUT = (OFF_TAB + (int)sizeof(ScaleTab) + 1023) / 1024 * 1024;
-  static constexpr int OUT_BYTES = TWO ? 0 : kEpiWarps * OUT_BOX;
+  static constexpr int OUT_BYTES = kEpiWarps * OUT_BOX;
   static constexpr int SMEM_BYTES = OFF_OUT + OUT_BYTES + 1024;   // + 1 KB alignment slack
   // Instruction descriptor of kind::mxf4nvf4: A and B E2M1 (format 1), both
   // K-major, UE4M3 scales (bit 23 clear), scale-factor data IDs 0,
@@ -194,7 +195,7 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
 // sectors: 7 % on fprop's 268 MB result against 128-bit stores, which write
 // each sector in two halves), else with 128-bit or scalar stores.  (The
 // one-window BF16 result goes through TMA stores instead when a tensor map
-// describes it: another 9 % on fprop.)
+// describes it: another 9 % on fprop, 1 % on the two-window wgrad.)
 __device__ __forceinline__ bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 __device__ __forceinline__ void st_global_v8(void* p, const uint32_t* w) {
   asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
@@ -573,7 +574,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           else
             pack_bf16x32(r, 0, alpha, h1);
         }
-        if (live) {
+        if (tma_out) {
+          const uint32_t stg = sb + G::OFF_OUT + (uint32_t)(warp - kEpiWarp0) * G::OUT_BOX;
+          const int y0 = am0 + 32 * q;
+          if (lane == 0) bulk_wait_read0();
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            sts128(stg + (uint32_t)lane * 128 + ((uint32_t)(i ^ (lane & 7)) << 4), h0[4 * i], h0[4 * i + 1],
+                   h0[4 * i + 2], h0[4 * i + 3]);
+            sts128(stg + (uint32_t)lane * 128 + ((uint32_t)((4 + i) ^ (lane & 7)) << 4), h1[4 * i], h1[4 * i + 1],
+                   h1[4 * i + 2], h1[4 * i + 3]);
+          }
+          fence_proxy_async();
+          __syncwarp();
+          if (lane == 0 && cbase < N && y0 < M) {
+            tma_store_2d(&mapC, stg, cbase, y0);
+            bulk_commit();
+          }
+        } else if (live) {
           store_bf16x32(out, row, cbase, N, h0);
           store_bf16x32(out, row, cbase + 32, N, h1);
         }
@@ -721,7 +740,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (!TWO && tma_out && lane == 0) bulk_wait0();   // this warp's TMA stores complete
+    if (tma_out && lane == 0) bulk_wait0();   // this warp's TMA stores complete
     if (QOUT) {
       // max |bf16(C)| (a 16-bit pattern; inf/NaN compare above every finite)
       qmax = __reduce_max_sync(0xFFFFFFFFu, qmax);
@@ -826,9 +845,9 @@ static cudaError_t launch_native_t(const GemmArgs& a, const CUtensorMap& mA, con
   const int64_t ntiles = ((a.N + G::PN - 1) / G::PN) * ((a.M + native::PM - 1) / native::PM);
   const int ncl = (int)(ntiles < clusters[dev] ? ntiles : clusters[dev]);
   cfg.gridDim = dim3(2u * (unsigned)ncl);
-  // the one-window BF16 result through TMA stores when a map describes it
+  // the BF16 result through TMA stores when a map describes it
   CUtensorMap mC;
-  const bool tma_out = !F32OUT && !TWO && a.out != nullptr && make_out_map(&mC, a.out, a.M, a.N);
+  const bool tma_out = !F32OUT && a.out != nullptr && make_out_map(&mC, a.out, a.M, a.N);
   if (!tma_out) memset(&mC, 0, sizeof(mC));
   e = cudaLaunchKernelEx(&cfg, kern, mA, mB, mSA, mSB, mSA2, mC, tma_out ? 1 : 0, a.TA, a.TB, (int)a.M, (int)a.N, (int)a.K, a.out, a.status,
                          a.wait_cycles, a.skip_loads ? 1 : 0, a.fa, a.fb, a.skip_if, a.TC, a.qpay, a.qsc, a.qamax,
