@@ -187,3 +187,41 @@ def test_persistent_tiles_with_ragged_edges(lib):
     assert gemm_error(C32, R) <= GEMM_TOL
     check_gemm_elementwise(C32, R, S, K)
     check_gemm_bf16(C16, R)
+
+
+@pytest.mark.parametrize("M,N", [(200, 300), (200, 304), (96, 776)])
+def test_result_written_at_every_alignment(lib, M, N):
+    """The result's store paths (TMA stores of staged boxes when a tensor map
+    describes the BF16 result, 256-bit stores where a row segment is 32-byte
+    aligned, else 128-bit or scalar ones) write the same bits wherever the
+    output starts: a result 16 bytes into a larger buffer (so that the
+    32-byte alignment of its rows varies) equals the one in a fresh tensor,
+    for the one-window and the two-window shapes, BF16 and binary32, ragged N
+    included."""
+    rng = np.random.default_rng(M * N)
+    K = 512
+    pa, pb = _payload(rng, M, K), _payload(rng, N, K)
+    sa = rng.integers(0x30, 0x48, (M, K // 16), dtype=np.uint8)
+    sb = rng.integers(0x30, 0x48, (N, K // 16), dtype=np.uint8)
+    A = (_dev(pa), _dev(sa), torch.ones(1, device="cuda"))
+    B = (_dev(pb), _dev(sb), torch.ones(1, device="cuda"))
+    lo = torch.zeros((M, K // 16), dtype=torch.uint8, device="cuda")
+    lo[:, ::7] = 0x70                                   # low-window codes ~2^-7 of the high ones: visible in BF16
+    fa, fb = torch.ones(M, device="cuda"), torch.ones(1, device="cuda")
+    for dtype, esz in ((torch.bfloat16, 2), (torch.float32, 4)):
+        ref_n = torch.empty((M, N), dtype=dtype, device="cuda")
+        ref_t = torch.empty((M, N), dtype=dtype, device="cuda")
+        buf = torch.full((M * N + 64 // esz,), 7, dtype=dtype, device="cuda")
+        off = 16 // esz
+        out = buf[off:off + M * N].view(M, N)
+        assert out.data_ptr() % 32 == 16
+        lib.fp4q_gemm_nvfp4(*A, *B, M, N, K, ref_n)
+        lib.fp4q_gemm_nvfp4(*A, *B, M, N, K, out)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref_n), dtype
+        lib.fp4q_gemm_nvfp4_two_windows(A[0], A[1], lo, fa, A[2], B[0], B[1], fb, B[2], M, N, K, None, ref_t)
+        lib.fp4q_gemm_nvfp4_two_windows(A[0], A[1], lo, fa, A[2], B[0], B[1], fb, B[2], M, N, K, None, out)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref_t), dtype
+        assert (buf[:off] == 7).all() and (buf[off + M * N:] == 7).all()   # nothing outside the result
+        assert not torch.equal(ref_t, ref_n)                                # the low window contributes
